@@ -1,0 +1,575 @@
+#!/usr/bin/env python3
+"""Benchmark of one layer step of the paged-KV hot path on GB300.
+
+A step is one pass of the whole path over one synthetic ragged batch:
+paged_kv_write of the step's new K/V rows, then ragged paged attention
+(decode kernel, prefill kernel, split combine: whatever the planner
+launches).  Inputs are resident in HBM when the timed region starts.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload 1..5] [--no-breakdown]
+
+Prints ONE JSON line on rank 0.  The headline workload is the 48-request
+engine step with a shared system prompt; the other four workloads are
+measured too and reported under "workloads".  `--impl reference` times the
+CPU oracle (the only reference there is) on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import CONFIG_NAMES, build_meta, config_spec, make_batch  # noqa: E402
+
+METRIC = "ragged paged-attn step µs + KV-read HBM GB/s vs 8 TB/s; query tokens/s"
+UNIT = "query tokens/s"
+HEADLINE = 2
+L2_BYTES = 129 * 1024 * 1024
+NOMINAL_HBM_GBS = 8000.0
+SM_COUNT = 152
+SM_MAX_MHZ = 2070.0
+FP32_LANES_PER_SM = 128
+
+
+# ---------------------------------------------------------------------------- environment
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": float(pk["hbm_gbs"]), "bf16_tflops": float(pk["bf16_tflops"]),
+                "bf16_tflops_sustained": float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])),
+                "sm_max_mhz": float(pk.get("sm_max_mhz", SM_MAX_MHZ)), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "sm_max_mhz": SM_MAX_MHZ, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        if not self.samples:
+            return None
+        inside = [s for t, s in self.samples if t0 - 0.15 <= t <= t1 + 0.15]
+        window = "timed region"
+        if not inside:
+            inside = [s for _, s in self.samples]
+            window = "whole GPU phase (timed region shorter than the sampling interval)"
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(s[1]) for s in inside if num(s[1]) is not None]
+        mx = [num(s[2]) for s in inside if num(s[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in inside for i in range(4) if s[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside), "window": window,
+                "power_w_max": max((num(s[3]) or 0.0) for s in inside)}
+
+
+# ---------------------------------------------------------------------------- accounting
+
+def accounting(spec, meta, classes):
+    """Algorithmic bytes and FLOPs of one step, whole and per kernel class.
+
+    KV bytes count every pool slot a request must read (positions < L) once,
+    however many requests share its block; FLOPs are 4*d*Hq per unmasked
+    (query, key) pair.  The kernel class of each request is the library's
+    own planner decision (pkv.plan_request_kernels)."""
+    hq, hkv, d, bs = spec.num_q_heads, spec.num_kv_heads, spec.head_dim, spec.block_size
+    slot_bytes = hkv * d * 2 * 2                       # K and V of one slot
+    n = meta.num_tokens
+    per_class = {}
+    rows_used = {}                                     # class -> {block: rows}
+    for r, cls in enumerate(classes):
+        t = meta.query_start_loc[r + 1] - meta.query_start_loc[r]
+        L = meta.seq_lens[r]
+        c = per_class.setdefault(cls, {"kv_bytes": 0, "q_out_bytes": 0, "flops": 0.0, "tokens": 0})
+        c["q_out_bytes"] += 2 * t * hq * d * 2
+        c["tokens"] += t
+        if L == 0 or t == 0:
+            continue
+        c["flops"] += 4.0 * d * hq * (t * (L - t) + t * (t + 1) / 2)
+        table = spec.reqs[r].table
+        used = rows_used.setdefault(cls, {})
+        for blk_i in range(-(-L // bs)):
+            rows = min(bs, L - blk_i * bs)
+            blk = table[blk_i]
+            if used.get(blk, 0) < rows:
+                used[blk] = rows
+    all_used = {}
+    for cls, used in rows_used.items():
+        per_class[cls]["kv_bytes"] = sum(used.values()) * slot_bytes
+        for blk, rows in used.items():
+            if all_used.get(blk, 0) < rows:
+                all_used[blk] = rows
+    unique_kv = sum(all_used.values()) * slot_bytes
+    logical_kv = sum(meta.seq_lens) * slot_bytes
+    write_bytes = n * hkv * d * 2 * 2 * 2 + n * 8     # new K/V read + written, slots
+    q_out = 2 * n * hq * d * 2
+    flops = sum(c["flops"] for c in per_class.values())
+    return {"unique_kv_bytes": unique_kv, "logical_kv_bytes": logical_kv, "write_bytes": write_bytes,
+            "q_out_bytes": q_out, "step_bytes": unique_kv + q_out + write_bytes, "flops": flops,
+            "per_class": per_class, "tokens": n}
+
+
+KERNEL_CLASS = {"attn_fma_decode": ("decode", "padding"), "attn_fma_prefill": ("prefill_cuda_core",),
+                "attn_tc_prefill": ("prefill_tensor",)}
+KERNEL_BOUND = {"paged_kv_write": "hbm", "attn_fma_decode": "hbm", "attn_fma_prefill": "alu",
+                "attn_tc_prefill": "tensor", "attn_split_combine": "hbm"}
+
+
+def kernel_work(name, acc):
+    """(algorithmic bytes, FLOPs) of one step attributable to kernel `name`."""
+    if name == "paged_kv_write":
+        return acc["write_bytes"], 0.0
+    b = f = 0.0
+    for cls in KERNEL_CLASS.get(name, ()):
+        c = acc["per_class"].get(cls)
+        if c:
+            b += c["kv_bytes"] + c["q_out_bytes"]
+            f += c["flops"]
+    return b, f
+
+
+def alu_peak_tflops(peaks):
+    return SM_COUNT * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+
+
+def source_hash(name):
+    """Hash of the source file of a kernel, to tell whether stored ncu counters are current."""
+    fname = {"paged_kv_write": "kv_write.cu", "attn_fma_decode": "attn_fma.cu", "attn_fma_prefill": "attn_fma.cu",
+             "attn_split_combine": "attn_fma.cu", "attn_tc_prefill": "attn_tc.cu"}.get(name)
+    path = os.path.join(ROOT, "paged_kv_cache_84_gb300", "csrc", fname or "")
+    if not fname or not os.path.exists(path):
+        return None
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:12]
+
+
+def stored_traffic(name, workload):
+    """DRAM bytes per launch from a committed ncu summary (profiles/ncu_traffic.txt:
+    `kernel workload bytes_per_launch source_hash`), or None when absent or stale."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    h = source_hash(name)
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 4 and not line.startswith("#") and parts[0] == name and parts[1] == workload:
+            return float(parts[2]) if parts[3] == h else None
+    return None
+
+
+def roofline(name, avg_s, launches_per_step, acc, peaks, workload):
+    b, f = kernel_work(name, acc)
+    b /= launches_per_step
+    f /= launches_per_step
+    bound = KERNEL_BOUND.get(name, "hbm")
+    if bound == "hbm":
+        achieved, peak, unit = b / avg_s / 1e9, peaks["hbm_gbs"], "GB/s"
+        note = f"of {peaks['source']} HBM copy bandwidth"
+    elif bound == "tensor":
+        achieved, peak, unit = f / avg_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+        note = f"of {peaks['source']} bf16 dense (burst)"
+    else:
+        achieved, peak, unit = f / avg_s / 1e12, alu_peak_tflops(peaks), "TFLOP/s"
+        note = "of fp32 FMA peak derived as 152 SMs x 128 lanes x 2 flop x max SM clock"
+    return {"kernel": name, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "traffic": stored_traffic(name, workload), "peak_note": note,
+            "algorithmic_bytes_per_launch": b, "algorithmic_flops_per_launch": f,
+            "avg_launch_us": avg_s * 1e6}
+
+
+# ---------------------------------------------------------------------------- GPU arm
+
+class Step:
+    """One copy of a workload resident on the device."""
+
+    def __init__(self, pkv, batch, device):
+        m, s = batch.meta, batch.spec
+        self.pkv, self.spec, self.meta = pkv, s, m
+        self.kc = batch.k_cache.to(device)
+        self.vc = batch.v_cache.to(device)
+        self.q, self.k, self.v = batch.q.to(device), batch.k.to(device), batch.v.to(device)
+        self.qsl = torch.tensor(m.query_start_loc, dtype=torch.int32, device=device)
+        self.sl = torch.tensor(m.seq_lens, dtype=torch.int32, device=device)
+        self.bt = m.block_table.to(device)
+        self.slots = m.slot_mapping.to(device)
+        self.out = torch.empty_like(self.q)
+        self.ws = pkv.make_workspace(pkv.attention_workspace_bytes(
+            max(1, m.num_reqs), max(1, m.num_tokens), s.num_q_heads, s.head_dim, max(1, m.max_seq_len)), device)
+        self.qsl_h = torch.tensor(m.query_start_loc, dtype=torch.int32)
+        self.sl_h = torch.tensor(m.seq_lens, dtype=torch.int32)
+
+    def nbytes(self):
+        ts = (self.kc, self.vc, self.q, self.k, self.v, self.out, self.bt, self.slots)
+        return sum(t.numel() * t.element_size() for t in ts)
+
+    def run(self, q=None, k=None, v=None, qsl=None, sl=None, bt=None, slots=None, out=None):
+        pkv = self.pkv
+        pkv.paged_kv_write(k if k is not None else self.k, v if v is not None else self.v, self.kc, self.vc,
+                           slots if slots is not None else self.slots)
+        pkv.ragged_paged_attention(out if out is not None else self.out, q if q is not None else self.q,
+                                   self.kc, self.vc, qsl if qsl is not None else self.qsl,
+                                   sl if sl is not None else self.sl, bt if bt is not None else self.bt,
+                                   self.qsl_h, self.sl_h, self.meta.max_query_len, self.meta.max_seq_len,
+                                   self.spec.scale, self.ws)
+
+
+def build_copies(pkv, cfg, device, max_copies=512):
+    spec = config_spec(cfg)
+    gen_dev = "cpu" if cfg in (1, 2) else device
+    batch = make_batch(spec, device=gen_dev)
+    first = Step(pkv, batch, device)
+    copies = [first]
+    per = first.nbytes()
+    n = 1 if per > 2 * L2_BYTES else min(max_copies, math.ceil(2 * L2_BYTES / per) + 1)
+    for _ in range(n - 1):
+        copies.append(Step(pkv, batch, device))
+    del batch
+    return spec, copies
+
+
+def time_workload(pkv, cfg, steps, warmup, device, peaks, dist=None, clocks=None, use_graph=True):
+    spec, copies = build_copies(pkv, cfg, device)
+    meta = copies[0].meta
+    classes = pkv.plan_request_kernels(meta.query_start_loc, meta.seq_lens, spec.num_q_heads,
+                                       spec.num_kv_heads, spec.head_dim)
+    acc = accounting(spec, meta, classes)
+    stream = torch.cuda.current_stream()
+    for i in range(max(3, warmup)):
+        copies[i % len(copies)].run()
+    torch.cuda.synchronize()
+    before = pkv.launch_count()
+    copies[0].run()
+    torch.cuda.synchronize()
+    launches_per_step = pkv.launch_count() - before
+
+    graphs = []
+    if use_graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            for c in copies:
+                c.run()
+        torch.cuda.synchronize()
+        for c in copies:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                c.run()
+            graphs.append(g)
+        torch.cuda.synchronize()
+        for i in range(max(3, warmup)):
+            graphs[i % len(graphs)].replay()
+        torch.cuda.synchronize()
+
+    # ---- timed region: exactly `steps` steps
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(steps):
+        if graphs:
+            graphs[i % len(graphs)].replay()
+        else:
+            copies[i % len(copies)].run()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_per_step = elapsed_ms / steps
+
+    # ---- per-kernel durations: eager steps with events around every launch
+    prof_steps = max(3, min(steps, 50))
+    pkv.profile_start(prof_steps * launches_per_step + 16)
+    for i in range(prof_steps):
+        copies[i % len(copies)].run()
+    recs = pkv.profile_stop()
+    kern = {}
+    for name, ms in recs:
+        k = kern.setdefault(name, {"launches": 0, "total_ms": 0.0})
+        k["launches"] += 1
+        k["total_ms"] += ms
+    total = sum(k["total_ms"] for k in kern.values()) or 1.0
+    kernels = {}
+    for name, k in kern.items():
+        kernels[name] = {"launches_per_step": k["launches"] / prof_steps,
+                         "avg_launch_us": 1e3 * k["total_ms"] / k["launches"],
+                         "share": k["total_ms"] / total}
+    dominant = max(kern, key=lambda n: kern[n]["total_ms"]) if kern else None
+    roof = None
+    if dominant:
+        avg_s = kern[dominant]["total_ms"] / kern[dominant]["launches"] / 1e3
+        roof = roofline(dominant, avg_s, kernels[dominant]["launches_per_step"], acc, peaks, f"cfg{cfg}")
+
+    step_s = ms_per_step / 1e3
+    res = {
+        "workload": CONFIG_NAMES[cfg], "config_index": cfg,
+        "ms_per_step": ms_per_step, "step_us": ms_per_step * 1e3,
+        "query_tokens_per_s": acc["tokens"] / step_s,
+        "kv_read_gbs": acc["unique_kv_bytes"] / step_s / 1e9,
+        "kv_read_frac_of_8tbs": acc["unique_kv_bytes"] / step_s / 1e9 / NOMINAL_HBM_GBS,
+        "step_hbm_frac": acc["step_bytes"] / step_s / 1e9 / peaks["hbm_gbs"],
+        "step_tensor_frac": acc["flops"] / step_s / 1e12 / peaks["bf16_tflops"],
+        "algorithmic": {k: acc[k] for k in ("unique_kv_bytes", "logical_kv_bytes", "q_out_bytes",
+                                            "write_bytes", "step_bytes", "flops", "tokens")},
+        "launches_per_step": launches_per_step, "copies": len(copies),
+        "inputs_bytes_per_copy": copies[0].nbytes(),
+        "l2": ("rotating %d copies of the inputs (%.0f MB > 2x L2)" % (len(copies), len(copies) * copies[0].nbytes() / 1e6)
+               if len(copies) > 1 else "inputs larger than 2x L2"),
+        "launch": "CUDA graph per step" if graphs else "eager",
+        "kernels": kernels, "roofline": roof, "timed_wall": (t_wall0, t_wall1),
+    }
+    return spec, copies, res
+
+
+def e2e_workload(pkv, copies, steps, device):
+    """Same step through the C ABI from pinned host buffers: h2d of the step's
+    inputs, write + attention, d2h of the output, every step, all timed."""
+    c0 = copies[0]
+    host = {name: getattr(c0, name).cpu().pin_memory() for name in ("q", "k", "v", "qsl", "sl", "bt", "slots")}
+    dev = [{name: torch.empty_like(getattr(c, name)) for name in host} for c in copies]
+    outs_h = torch.empty_like(c0.out, device="cpu").pin_memory()
+    stream = torch.cuda.current_stream()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = outs_h.numel() * outs_h.element_size()
+
+    def one(i):
+        c, d = copies[i % len(copies)], dev[i % len(dev)]
+        for name, t in host.items():
+            d[name].copy_(t, non_blocking=True)
+        c.run(q=d["q"], k=d["k"], v=d["v"], qsl=d["qsl"], sl=d["sl"], bt=d["bt"], slots=d["slots"])
+        outs_h.copy_(c.out, non_blocking=True)
+
+    for i in range(3):
+        one(i)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(steps):
+        one(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / steps
+    return {"value": c0.meta.num_tokens / (ms / 1e3), "unit": UNIT, "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "path": "pinned host -> device copies, pkv_paged_kv_write + pkv_ragged_paged_attention, device -> pinned host"}
+
+
+# ---------------------------------------------------------------------------- CPU oracle
+
+def oracle_step_timer(cfg, threads):
+    """Time the CPU oracle (write + attention) on the workload's full step."""
+    import oracle
+    spec = config_spec(cfg)
+    b = make_batch(spec, device="cpu")
+    m = b.meta
+
+    def step():
+        oracle.paged_kv_write(b.k_cache, b.v_cache, b.k, b.v, m.slot_mapping)
+        oracle.ragged_paged_attention(b.q, b.k_cache, b.v_cache, m.query_start_loc, m.seq_lens,
+                                      m.block_table, spec.scale, threads)
+    return spec, m, step
+
+
+def cpu_baseline(cfg, budget_s=10.0):
+    threads = os.cpu_count() or 1
+    spec, m, step = oracle_step_timer(cfg, threads)
+    step()                                               # build and warm
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        step()
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = (time.perf_counter() - t0) / n
+    t1 = time.perf_counter()
+    _, _, step1 = oracle_step_timer(cfg, 1)
+    step1()
+    one_thread = time.perf_counter() - t1
+    return {"value": m.num_tokens / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{n} full steps of the {CONFIG_NAMES[cfg]} workload (write + attention), "
+                      f"{dt * 1e3:.1f} ms each on {threads} threads; one step on 1 thread took {one_thread * 1e3:.0f} ms",
+            "ms_per_step": dt * 1e3, "one_thread_ms_per_step": one_thread * 1e3}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    threads = os.cpu_count() or 1
+    spec, m, step = oracle_step_timer(args.workload, threads)
+    for _ in range(max(3, args.warmup)):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = m.num_tokens / dt
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) values, shapes of the pages' workloads)",
+            "config": {"workload": CONFIG_NAMES[args.workload], "query_tokens": m.num_tokens,
+                       "requests": m.num_reqs, "parallelism": "host cores"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": f"full steps of {CONFIG_NAMES[args.workload]} (write + attention)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    rank, world, local = dist_env()
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl")
+        dist = tdist
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    import paged_kv_cache_84_gb300 as pkv
+    from paged_kv_cache_84_gb300 import build as pkv_build
+    pkv_build.build()
+    pkv.load()
+    peaks = load_peaks()
+    warmup = max(3, args.warmup)
+
+    clocks = ClockSampler(local).start()
+    spec, copies, head = time_workload(pkv, args.workload, args.steps, warmup, device, peaks, dist)
+    t0, t1 = head.pop("timed_wall")
+    e2e = e2e_workload(pkv, copies, max(3, min(args.steps, 200)), device)
+    del copies
+    torch.cuda.empty_cache()
+
+    breakdown = {}
+    if not args.no_breakdown:
+        for cfg in (1, 2, 3, 4, 5):
+            if cfg == args.workload:
+                r = dict(head)
+            else:
+                _, cps, r = time_workload(pkv, cfg, max(10, min(args.steps, 50)), warmup, device, peaks, None)
+                r.pop("timed_wall")
+                del cps
+                torch.cuda.empty_cache()
+            breakdown[str(cfg)] = r
+    clocks.stop()
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+    cpu = cpu_baseline(args.workload) if world == 1 and not args.no_cpu_baseline else None
+    tokens = head["algorithmic"]["tokens"]
+    line = {
+        "metric": METRIC, "value": tokens * world / (head["ms_per_step"] / 1e3), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": warmup, "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 values, shapes of the pages' workloads)",
+        "config": {"workload": head["workload"], "query_tokens": tokens, "requests": len(spec.reqs),
+                   "q_heads": spec.num_q_heads, "kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim,
+                   "block_size": spec.block_size, "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                   "l2": head["l2"], "launch": head["launch"]},
+        "step_us": head["step_us"], "kv_read_gbs": head["kv_read_gbs"],
+        "kv_read_frac_of_8tbs": head["kv_read_frac_of_8tbs"],
+        "roofline": head["roofline"], "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": head["launches_per_step"] * args.steps,
+        "clocks": clocks.summary(t0, t1), "peaks": peaks, "kernels": head["kernels"],
+        "workloads": breakdown,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=HEADLINE, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--no-breakdown", action="store_true", help="time only the headline workload")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,206 @@
+/*
+ * pkv — paged KV write and ragged paged attention for GB300 (sm_103a).
+ *
+ * A C ABI over hand-written CUDA kernels.  Its calls mirror the flattened
+ * batch metadata of "31. Engine v2: one core for every request" (section
+ * "Flattened ragged batches", the BatchMeta fields query_start_loc, seq_lens,
+ * block_table, slot_mapping, block_size and their host copies) and the two
+ * backend calls of its section "Attention over the pool": write_kv (scatter
+ * this step's K/V rows into the pool) and forward (causal attention of each
+ * request's new tokens over its paged context).
+ *
+ * Conventions shared by every call:
+ *  - Device pointers are caller-owned device memory; *_host pointers are
+ *    caller-owned host memory read during the call only.  The library
+ *    allocates no memory, never synchronises the stream (except
+ *    pkv_read_device_error, which exists to do so) and enqueues all work on
+ *    `stream` in call order.
+ *  - Values (q, k, v, pools, out) are bf16, row-major and densely packed.
+ *  - The KV pool of one layer is [num_blocks_total][block_size][num_kv_heads]
+ *    [head_dim] ("Attention over the pool": slot-major rows).  Its last
+ *    block is the scratch block that padding rows write into; the block
+ *    manager never hands it out.  num_blocks_total counts it.
+ *  - A device error word (uint32_t) collects bounds violations found on the
+ *    device: PKV_DEVERR_SLOT (a slot past the pool) and PKV_DEVERR_BLOCK
+ *    (a block id outside [0, num_blocks_total)).  The access is skipped, the
+ *    bit is OR-ed in, and nothing traps.  The word is sticky until cleared.
+ *  - Every call validates its host-visible arguments first and returns an
+ *    error status without enqueuing anything when they are invalid.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,    /* inconsistent or out-of-range host arguments */
+    PKV_ERR_UNSUPPORTED = 2,    /* valid, but a shape or alignment this build has no kernel for */
+    PKV_ERR_WORKSPACE = 3,      /* workspace missing or smaller than the minimum */
+    PKV_ERR_CUDA = 4,           /* a CUDA runtime call failed (see pkv_last_cuda_error) */
+    PKV_ERR_DEVICE_BOUNDS = 5   /* pkv_read_device_error found bounds violations */
+} pkv_status;
+
+#define PKV_DEVERR_SLOT  1u     /* paged_kv_write: slot >= num_blocks_total * block_size */
+#define PKV_DEVERR_BLOCK 2u     /* attention: a block id outside [0, num_blocks_total) */
+
+/* Static description of a status code. */
+const char *pkv_status_string(pkv_status status);
+
+/* Text of the last CUDA error seen by this library on the calling thread. */
+const char *pkv_last_cuda_error(void);
+
+/*
+ * Number of kernels this library has launched since it was loaded (all
+ * threads).  A diagnostic: the difference over a region counts its launches.
+ */
+int64_t pkv_launch_count(void);
+
+/*
+ * Per-launch timing, for diagnostics and the benchmark.  After
+ * pkv_profile_start(capacity), each kernel launch of the library (up to
+ * `capacity` of them) is bracketed by two CUDA events recorded on its
+ * launching stream.  pkv_profile_stop() ends recording and returns the
+ * number of records; pkv_profile_read() waits for record `index` and gives
+ * its kernel id and duration in ms; pkv_kernel_name() names a kernel id.
+ * Events are created once by pkv_profile_start (host-side CUDA objects, no
+ * device memory).  Do not profile while capturing a CUDA graph.
+ */
+pkv_status pkv_profile_start(int32_t capacity);
+int32_t pkv_profile_stop(void);
+pkv_status pkv_profile_read(int32_t index, int32_t *kernel_id, float *ms);
+const char *pkv_kernel_name(int32_t kernel_id);
+
+/*
+ * paged_kv_write — scatter this step's new K/V rows into the pool
+ * ("31. Engine v2", "Attention over the pool", write_kv).
+ *
+ *   k, v          device bf16 [num_tokens][num_kv_heads][head_dim]
+ *   k_cache,      device bf16 [num_blocks_total][block_size][num_kv_heads][head_dim]
+ *   v_cache       (written in place)
+ *   slot_mapping  device int64 [num_tokens]: flat slot of row i
+ *                 (table[p / block_size] * block_size + p % block_size,
+ *                 "Flattened ragged batches"); a negative slot marks a
+ *                 padding row, which is written to the last slot of the pool
+ *                 (the scratch block).  A slot >= num_blocks_total*block_size
+ *                 is skipped and sets PKV_DEVERR_SLOT in *device_error.
+ *   device_error  device uint32_t, may be NULL (then violations are only skipped)
+ *
+ * Row i is copied bit for bit.  Two real rows with the same slot are a
+ * caller error (which one lands is unspecified); padding rows may share the
+ * scratch slot, whose contents are unspecified.
+ * Requirements: head_dim % 8 == 0; k, v, k_cache, v_cache 16-byte aligned.
+ * num_tokens == 0 is a no-op.
+ */
+pkv_status pkv_paged_kv_write(const void *k, const void *v, void *k_cache, void *v_cache,
+                              const int64_t *slot_mapping, int32_t num_tokens,
+                              int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                              int32_t num_blocks_total, uint32_t *device_error,
+                              cudaStream_t stream);
+
+/*
+ * Workspace size that lets pkv_ragged_paged_attention split long decodes
+ * over KV freely for any batch within the given maxima.  A smaller
+ * workspace (at least PKV_WORKSPACE_MIN_BYTES) is accepted: the planner
+ * then splits less.  The workspace holds the device error word (first 256
+ * bytes) and fp32 split-KV partials.
+ */
+#define PKV_WORKSPACE_MIN_BYTES 256
+size_t pkv_attention_workspace_bytes(int32_t max_num_reqs, int32_t max_num_tokens,
+                                     int32_t num_q_heads, int32_t head_dim,
+                                     int32_t max_seq_len);
+
+/*
+ * ragged_paged_attention — causal grouped-query attention of one flattened
+ * ragged batch over the paged pool ("31. Engine v2", "Attention over the
+ * pool", the reference backend's forward; grouped heads as in the vllm-lite
+ * README; tiled exact attention as in "vLLM: LLM Inference as a memory and
+ * scheduling problem", "FlashAttention is not PagedAttention").
+ *
+ *   out               device bf16 [num_tokens][num_q_heads][head_dim]
+ *   q                 device bf16 [num_tokens][num_q_heads][head_dim]
+ *   k_cache, v_cache  device bf16 pool, as in pkv_paged_kv_write (read only)
+ *   query_start_loc   device int32 [num_reqs + 1]: request r owns rows
+ *                     query_start_loc[r] .. query_start_loc[r+1]-1
+ *   seq_lens          device int32 [num_reqs]: context length L after this step
+ *   block_table       device int32 [num_reqs][block_table_stride]: physical
+ *                     blocks of each request in logical order
+ *   query_start_loc_host, seq_lens_host
+ *                     host copies of the two arrays above, used to plan the
+ *                     launches without reading device memory
+ *   max_query_len, max_seq_len
+ *                     maxima of the host arrays (validated)
+ *   scale             softmax scale; <= 0 selects 1/sqrt(head_dim)
+ *   workspace         device memory, >= PKV_WORKSPACE_MIN_BYTES, 256-byte
+ *                     aligned; its first 4 bytes are the device error word
+ *                     (PKV_DEVERR_BLOCK), the rest holds split partials
+ *
+ * Row i of request r (t rows, L = seq_lens[r]) is the query at position
+ * L - t + i.  Query head h reads KV head h / (num_q_heads / num_kv_heads)
+ * and attends to the keys at positions 0 .. L - t + i.  A request with
+ * L == 0 or t == 0 is padding: its rows of `out` are set to zero.
+ * All keys a request reads must already be in the pool: call
+ * pkv_paged_kv_write for the step first, on the same stream.
+ *
+ * Host validation (PKV_ERR_INVALID_ARG, nothing enqueued):
+ *   query_start_loc_host not non-decreasing from 0 to num_tokens; a request
+ *   with L > 0 and t > L; ceil(L / block_size) > block_table_stride;
+ *   num_q_heads % num_kv_heads != 0; the max_* arguments below the data.
+ * PKV_ERR_UNSUPPORTED: head_dim not in {48, 64, 128}, block_size not 16,
+ *   or misaligned pointers.
+ */
+pkv_status pkv_ragged_paged_attention(void *out, const void *q,
+                                      const void *k_cache, const void *v_cache,
+                                      const int32_t *query_start_loc, const int32_t *seq_lens,
+                                      const int32_t *block_table, int32_t block_table_stride,
+                                      const int32_t *query_start_loc_host,
+                                      const int32_t *seq_lens_host,
+                                      int32_t num_reqs, int32_t num_tokens,
+                                      int32_t max_query_len, int32_t max_seq_len,
+                                      int32_t num_q_heads, int32_t num_kv_heads,
+                                      int32_t head_dim, int32_t block_size,
+                                      int32_t num_blocks_total, float scale,
+                                      void *workspace, size_t workspace_bytes,
+                                      cudaStream_t stream);
+
+/*
+ * Which kernel path pkv_ragged_paged_attention takes for each request
+ * (host only, no CUDA call): class_out[r] receives one of PKV_CLASS_*.
+ * Decode-class requests (t * g <= 16) run on the CUDA-core decode kernel,
+ * with KV split across CTAs for long contexts; prefill-class requests run
+ * in tiles of new tokens.  For accounting and tests.
+ */
+#define PKV_CLASS_NONE 0                 /* no rows */
+#define PKV_CLASS_PADDING 1              /* seq_len 0: rows zeroed */
+#define PKV_CLASS_DECODE 2               /* CUDA-core decode kernel (+ split combine) */
+#define PKV_CLASS_PREFILL_CUDA_CORE 3    /* CUDA-core prefill tiles */
+#define PKV_CLASS_PREFILL_TENSOR 4       /* tcgen05 prefill tiles */
+pkv_status pkv_plan_request_kernels(const int32_t *query_start_loc_host, const int32_t *seq_lens_host,
+                                    int32_t num_reqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                    int32_t head_dim, int32_t *class_out);
+
+/*
+ * Set a device error word to zero (enqueued on stream).
+ */
+pkv_status pkv_clear_device_error(uint32_t *device_error, cudaStream_t stream);
+
+/*
+ * Synchronise `stream`, read the device error word at `device_error` (for
+ * attention: the workspace pointer) into *flags_out, and return
+ * PKV_ERR_DEVICE_BOUNDS if any bit is set, PKV_OK otherwise.  A diagnostic
+ * for tests and debugging; not for the hot path.
+ */
+pkv_status pkv_read_device_error(const uint32_t *device_error, uint32_t *flags_out,
+                                 cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

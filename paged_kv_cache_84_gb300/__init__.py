@@ -1,0 +1,210 @@
+"""Paged KV write and ragged paged attention on GB300 (sm_103a).
+
+A thin ctypes binding over ``libpkv.so`` (C ABI in ``include/pkv.h``).  The
+functions here only marshal torch tensors into pointers, sizes and the
+current CUDA stream; every step of the computation runs in the library's
+CUDA kernels.  There is no CPU or PyTorch fallback: if the library is
+missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "PkvError", "load", "paged_kv_write", "ragged_paged_attention", "attention_workspace_bytes",
+    "make_workspace", "read_device_error", "clear_device_error", "launch_count", "LIB_PATH",
+    "DEVERR_SLOT", "DEVERR_BLOCK", "WORKSPACE_MIN_BYTES", "profile_start", "profile_stop",
+    "plan_request_kernels", "CLASS_NAMES",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpkv.so")
+DEVERR_SLOT = 1
+DEVERR_BLOCK = 2
+WORKSPACE_MIN_BYTES = 256
+
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape or alignment",
+          3: "workspace missing or too small", 4: "CUDA error", 5: "device bounds violation recorded"}
+
+_c_i32, _c_i64, _c_p, _c_f, _c_sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_size_t
+_lib = None
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, what: str, detail: str = ""):
+        self.status = status
+        msg = f"{what}: {STATUS.get(status, status)}"
+        if detail:
+            msg += f" ({detail})"
+        super().__init__(msg)
+
+
+def load():
+    """Load libpkv.so (built by ``build.py``); raise if it is not there."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with paged_kv_cache_84_gb300/build.py "
+                          "(nvcc, sm_103a); there is no fallback path")
+    L = ctypes.CDLL(LIB_PATH)
+    L.pkv_status_string.restype = ctypes.c_char_p
+    L.pkv_status_string.argtypes = [ctypes.c_int]
+    L.pkv_last_cuda_error.restype = ctypes.c_char_p
+    L.pkv_last_cuda_error.argtypes = []
+    L.pkv_launch_count.restype = _c_i64
+    L.pkv_launch_count.argtypes = []
+    L.pkv_paged_kv_write.restype = ctypes.c_int
+    L.pkv_paged_kv_write.argtypes = [_c_p, _c_p, _c_p, _c_p, _c_p, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
+                                     _c_p, _c_p]
+    L.pkv_attention_workspace_bytes.restype = _c_sz
+    L.pkv_attention_workspace_bytes.argtypes = [_c_i32] * 5
+    L.pkv_ragged_paged_attention.restype = ctypes.c_int
+    L.pkv_ragged_paged_attention.argtypes = [_c_p] * 7 + [_c_i32, _c_p, _c_p] + [_c_i32] * 9 + \
+        [_c_f, _c_p, _c_sz, _c_p]
+    L.pkv_clear_device_error.restype = ctypes.c_int
+    L.pkv_clear_device_error.argtypes = [_c_p, _c_p]
+    L.pkv_read_device_error.restype = ctypes.c_int
+    L.pkv_read_device_error.argtypes = [_c_p, ctypes.POINTER(ctypes.c_uint32), _c_p]
+    L.pkv_profile_start.restype = ctypes.c_int
+    L.pkv_profile_start.argtypes = [_c_i32]
+    L.pkv_profile_stop.restype = _c_i32
+    L.pkv_profile_stop.argtypes = []
+    L.pkv_profile_read.restype = ctypes.c_int
+    L.pkv_profile_read.argtypes = [_c_i32, ctypes.POINTER(_c_i32), ctypes.POINTER(ctypes.c_float)]
+    L.pkv_kernel_name.restype = ctypes.c_char_p
+    L.pkv_kernel_name.argtypes = [_c_i32]
+    L.pkv_plan_request_kernels.restype = ctypes.c_int
+    L.pkv_plan_request_kernels.argtypes = [_c_p, _c_p, _c_i32, _c_i32, _c_i32, _c_i32, _c_p]
+    _lib = L
+    return L
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        detail = load().pkv_last_cuda_error().decode() if status == 4 else ""
+        raise PkvError(status, what, detail)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return _c_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return _c_p(s.cuda_stream)
+
+
+def _host_i32(x, name):
+    t = torch.as_tensor(x, dtype=torch.int32)
+    if t.device.type != "cpu":
+        raise TypeError(f"{name} must be host data")
+    return t.contiguous()
+
+
+def profile_start(capacity: int = 4096):
+    """Time each library kernel launch with CUDA events on its stream (diagnostics)."""
+    _check(load().pkv_profile_start(capacity), "profile_start")
+
+
+def profile_stop():
+    """Stop recording; return [(kernel name, ms), ...] in launch order (waits for them)."""
+    L = load()
+    n = L.pkv_profile_stop()
+    out = []
+    kid, ms = _c_i32(0), ctypes.c_float(0)
+    for i in range(n):
+        _check(L.pkv_profile_read(i, ctypes.byref(kid), ctypes.byref(ms)), "profile_read")
+        out.append((L.pkv_kernel_name(kid.value).decode(), float(ms.value)))
+    return out
+
+
+CLASS_NAMES = {0: "none", 1: "padding", 2: "decode", 3: "prefill_cuda_core", 4: "prefill_tensor"}
+
+
+def plan_request_kernels(query_start_loc_host, seq_lens_host, num_q_heads, num_kv_heads, head_dim):
+    """Kernel class of every request, as the attention planner assigns it (host only)."""
+    qsl = _host_i32(query_start_loc_host, "query_start_loc_host")
+    sl = _host_i32(seq_lens_host, "seq_lens_host")
+    out = torch.zeros(sl.numel(), dtype=torch.int32)
+    _check(load().pkv_plan_request_kernels(_c_p(qsl.data_ptr()), _c_p(sl.data_ptr()), sl.numel(), num_q_heads,
+                                           num_kv_heads, head_dim, _c_p(out.data_ptr())), "plan_request_kernels")
+    return [CLASS_NAMES[int(c)] for c in out]
+
+
+def launch_count() -> int:
+    """Kernels launched by the library since it was loaded."""
+    return int(load().pkv_launch_count())
+
+
+def paged_kv_write(k, v, k_cache, v_cache, slot_mapping, device_error=None, stream=None):
+    """Scatter k, v [N, Hkv, d] into the pools [nbt, bs, Hkv, d] at ``slot_mapping`` (int64 [N])."""
+    L = load()
+    n, hkv, d = k.shape
+    nbt, bs, hkv2, d2 = k_cache.shape
+    if (hkv2, d2) != (hkv, d) or v.shape != k.shape or v_cache.shape != k_cache.shape:
+        raise ValueError("shape mismatch between k/v and the pools")
+    err = _dev(device_error, "device_error", torch.int32) if device_error is not None else None
+    st = L.pkv_paged_kv_write(_dev(k, "k", torch.bfloat16), _dev(v, "v", torch.bfloat16),
+                              _dev(k_cache, "k_cache", torch.bfloat16), _dev(v_cache, "v_cache", torch.bfloat16),
+                              _dev(slot_mapping, "slot_mapping", torch.int64), n, hkv, d, bs, nbt, err,
+                              _stream(stream))
+    _check(st, "paged_kv_write")
+
+
+def attention_workspace_bytes(max_num_reqs, max_num_tokens, num_q_heads, head_dim, max_seq_len) -> int:
+    return int(load().pkv_attention_workspace_bytes(max_num_reqs, max_num_tokens, num_q_heads, head_dim,
+                                                    max_seq_len))
+
+
+def make_workspace(nbytes: int, device=None) -> torch.Tensor:
+    """A zeroed uint8 CUDA buffer of ``nbytes`` (torch allocations are 256-byte aligned)."""
+    return torch.zeros(max(int(nbytes), WORKSPACE_MIN_BYTES), dtype=torch.uint8, device=device or "cuda")
+
+
+def ragged_paged_attention(out, q, k_cache, v_cache, query_start_loc, seq_lens, block_table,
+                           query_start_loc_host, seq_lens_host, max_query_len, max_seq_len, scale,
+                           workspace, stream=None):
+    """Causal GQA attention of a flattened ragged batch over the paged pool; writes ``out``."""
+    L = load()
+    n, hq, d = q.shape
+    nbt, bs, hkv, d2 = k_cache.shape
+    if out.shape != q.shape or d2 != d or v_cache.shape != k_cache.shape:
+        raise ValueError("shape mismatch")
+    qsl_h = _host_i32(query_start_loc_host, "query_start_loc_host")
+    sl_h = _host_i32(seq_lens_host, "seq_lens_host")
+    if qsl_h.numel() != sl_h.numel() + 1:
+        raise ValueError("query_start_loc needs num_reqs + 1 entries")
+    if block_table.dim() != 2:
+        raise ValueError("block_table must be [num_reqs, width]")
+    st = L.pkv_ragged_paged_attention(
+        _dev(out, "out", torch.bfloat16), _dev(q, "q", torch.bfloat16),
+        _dev(k_cache, "k_cache", torch.bfloat16), _dev(v_cache, "v_cache", torch.bfloat16),
+        _dev(query_start_loc, "query_start_loc", torch.int32), _dev(seq_lens, "seq_lens", torch.int32),
+        _dev(block_table, "block_table", torch.int32), block_table.shape[1],
+        _c_p(qsl_h.data_ptr()), _c_p(sl_h.data_ptr()), sl_h.numel(), n, int(max_query_len), int(max_seq_len),
+        hq, hkv, d, bs, nbt, float(scale), _dev(workspace, "workspace", torch.uint8), workspace.numel(),
+        _stream(stream))
+    _check(st, "ragged_paged_attention")
+
+
+def clear_device_error(word: torch.Tensor, stream=None):
+    """Zero a device error word (a CUDA int32 tensor, or the attention workspace)."""
+    _check(load().pkv_clear_device_error(_c_p(word.data_ptr()), _stream(stream)), "clear_device_error")
+
+
+def read_device_error(word: torch.Tensor, stream=None) -> int:
+    """Synchronise the stream and return the device error bits (0 when clean)."""
+    flags = ctypes.c_uint32(0)
+    st = load().pkv_read_device_error(_c_p(word.data_ptr()), ctypes.byref(flags), _stream(stream))
+    if st not in (0, 5):
+        _check(st, "read_device_error")
+    return int(flags.value)

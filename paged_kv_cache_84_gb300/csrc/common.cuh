@@ -1,0 +1,119 @@
+// Shared device helpers and the internal launch interface of libpkv.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pkv {
+
+// ---------------------------------------------------------------- launch plan
+//
+// A launch's work list travels in the kernel parameters (no host->device
+// copy, no sync): `req[li]` is a request index and request li owns the
+// items item_off[li] .. item_off[li+1]-1 of the grid's x dimension.
+// Decode-class lists split a request's keys into chunks of `split_tokens`;
+// prefill-class lists cut its new tokens into tiles of `tile_tokens`.
+constexpr int kPlanMax = 256;
+
+struct WorkList {
+    int32_t n;              // listed requests
+    int32_t mode;           // kModeDecode or kModePrefill
+    int32_t split_tokens;   // decode: keys per split (multiple of the block size)
+    int32_t tile_tokens;    // prefill: tokens per tile
+    int32_t req[kPlanMax];
+    int32_t item_off[kPlanMax + 1];
+    int32_t part_off[kPlanMax];   // decode: first partial row of a split request, -1 if unsplit
+};
+
+constexpr int kModeDecode = 0;
+constexpr int kModePrefill = 1;
+
+struct AttnParams {
+    __nv_bfloat16 *out;
+    const __nv_bfloat16 *q;
+    const __nv_bfloat16 *k_cache;
+    const __nv_bfloat16 *v_cache;
+    const int32_t *qsl;
+    const int32_t *seq_lens;
+    const int32_t *block_table;
+    int32_t bt_stride;
+    int32_t hq, hkv, group, block_size, nb_total;
+    float scale_log2;           // softmax scale * log2(e): scores live in the exp2 domain
+    uint32_t *err;              // device error word
+    float *part_o;              // [rows][head_dim] unnormalised split outputs
+    float2 *part_ml;            // [rows] (running max in exp2 domain, sum of weights)
+};
+
+// ---------------------------------------------------------------- device helpers
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void *p)
+{
+    uint4 r;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Index of the listed request that owns grid item `item` (binary search over item_off).
+__device__ __forceinline__ int find_listed(const WorkList &wl, int item)
+{
+    int lo = 0, hi = wl.n - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (wl.item_off[mid] <= item) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+}  // namespace pkv
+
+// ---------------------------------------------------------------- launchers (internal C++ linkage)
+
+namespace pkv {
+
+cudaError_t launch_kv_write(const void *k, const void *v, void *k_cache, void *v_cache,
+                            const int64_t *slot_mapping, int32_t num_tokens, int32_t row_bytes,
+                            int64_t num_slots, uint32_t *err, cudaStream_t stream);
+
+// CUDA-core attention over one work list; rows = largest tokens*group of an item.
+cudaError_t launch_attn_fma(const AttnParams &p, const WorkList &wl, int head_dim, int rows,
+                            int num_items, cudaStream_t stream);
+
+// Merge split-KV partials of the split requests in `wl` into bf16 output.
+cudaError_t launch_attn_combine(const AttnParams &p, const WorkList &wl, int head_dim,
+                                int max_rows_per_req, cudaStream_t stream);
+
+// Kernel ids for launch accounting and the optional per-launch event timing.
+enum KernelId : int {
+    kKvWrite = 0,
+    kAttnFmaDecode = 1,
+    kAttnFmaPrefill = 2,
+    kAttnCombine = 3,
+    kAttnTcPrefill = 4,
+    kNumKernelIds = 5
+};
+
+// Call around every kernel launch: counts it and, while profiling is on,
+// records a CUDA event before and after it on the launching stream.
+void launch_begin(cudaStream_t stream, int kernel_id);
+void launch_end(cudaStream_t stream);
+
+}  // namespace pkv

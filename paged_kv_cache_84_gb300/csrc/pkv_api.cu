@@ -1,0 +1,424 @@
+// C ABI of libpkv: argument validation, launch planning, launches.
+//
+// Planning reads only the host copies of query_start_loc and seq_lens
+// ("31. Engine v2", "Flattened ragged batches": the batch metadata keeps
+// host copies so that kernels launch without a device sync).  It sorts the
+// requests into
+//   - decode-class: t * g <= 16 rows per KV head (decodes, short chunks,
+//     padding requests); their keys may be split across CTAs, with a
+//     combine pass when a request has more than one split;
+//   - prefill-class: everything else, cut into tiles of new tokens.
+// Each class goes to its kernel with the work list in the kernel
+// parameters, so nothing is copied to the device and nothing waits.
+#include <atomic>
+#include <cmath>
+#include <mutex>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <vector>
+
+#include "pkv.h"
+#include "common.cuh"
+
+namespace pkv {
+
+static std::atomic<int64_t> g_launches{0};
+
+// Optional per-launch timing: events recorded on the launching stream.
+struct Profile {
+    std::mutex mu;
+    bool on = false;
+    std::vector<cudaEvent_t> events;     // 2 per record
+    std::vector<int> kernel;
+    int n = 0;
+    int open = -1;                       // record opened by launch_begin, closed by launch_end
+};
+static Profile g_prof;
+
+void launch_begin(cudaStream_t stream, int kernel_id)
+{
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (!g_prof.on) return;
+    std::lock_guard<std::mutex> lock(g_prof.mu);
+    if (!g_prof.on || g_prof.n >= (int)g_prof.kernel.size()) return;
+    g_prof.open = g_prof.n;
+    g_prof.kernel[g_prof.n] = kernel_id;
+    cudaEventRecord(g_prof.events[2 * g_prof.n], stream);
+}
+
+void launch_end(cudaStream_t stream)
+{
+    if (!g_prof.on) return;
+    std::lock_guard<std::mutex> lock(g_prof.mu);
+    if (g_prof.open < 0) return;
+    cudaEventRecord(g_prof.events[2 * g_prof.open + 1], stream);
+    g_prof.n = g_prof.open + 1;
+    g_prof.open = -1;
+}
+
+static thread_local char g_cuda_err[256] = "";
+
+static pkv_status cuda_fail(cudaError_t e, const char *where)
+{
+    snprintf(g_cuda_err, sizeof g_cuda_err, "%s: %s", where, cudaGetErrorString(e));
+    return PKV_ERR_CUDA;
+}
+
+static int num_sms()
+{
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+    if (!cached[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+static bool aligned(const void *p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
+
+constexpr int kDecodeRows = 16;       // decode-class: t * g <= this
+constexpr int kMinSplit = 256;        // smallest KV split, tokens
+constexpr int kMaxSplits = 64;        // most splits of one request
+constexpr size_t kErrBytes = 256;     // device error word area at the workspace start
+
+// Kernel class of request r (host rule shared by the planner and pkv_plan_request_kernels).
+static int request_class(int32_t t, int32_t L, int32_t g)
+{
+    if (t == 0) return PKV_CLASS_NONE;
+    if (L == 0) return PKV_CLASS_PADDING;
+    if (t * g <= kDecodeRows) return PKV_CLASS_DECODE;
+    return PKV_CLASS_PREFILL_CUDA_CORE;
+}
+
+static int env_int(const char *name, int dflt)
+{
+    const char *s = getenv(name);
+    return (s && *s) ? atoi(s) : dflt;
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+const char *pkv_status_string(pkv_status s)
+{
+    switch (s) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID_ARG: return "invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "unsupported shape or alignment";
+    case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+    case PKV_ERR_CUDA: return "CUDA error";
+    case PKV_ERR_DEVICE_BOUNDS: return "device bounds violation recorded";
+    }
+    return "unknown status";
+}
+
+const char *pkv_last_cuda_error(void) { return g_cuda_err; }
+
+int64_t pkv_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char *pkv_kernel_name(int32_t kernel_id)
+{
+    switch (kernel_id) {
+    case kKvWrite: return "paged_kv_write";
+    case kAttnFmaDecode: return "attn_fma_decode";
+    case kAttnFmaPrefill: return "attn_fma_prefill";
+    case kAttnCombine: return "attn_split_combine";
+    case kAttnTcPrefill: return "attn_tc_prefill";
+    }
+    return "unknown";
+}
+
+pkv_status pkv_profile_start(int32_t capacity)
+{
+    if (capacity <= 0) return PKV_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_prof.mu);
+    while ((int)g_prof.kernel.size() < capacity) {
+        cudaEvent_t a, b;
+        cudaError_t e = cudaEventCreate(&a);
+        if (e == cudaSuccess) e = cudaEventCreate(&b);
+        if (e != cudaSuccess) return cuda_fail(e, "profile events");
+        g_prof.events.push_back(a);
+        g_prof.events.push_back(b);
+        g_prof.kernel.push_back(-1);
+    }
+    g_prof.n = 0;
+    g_prof.open = -1;
+    g_prof.on = true;
+    return PKV_OK;
+}
+
+int32_t pkv_profile_stop(void)
+{
+    std::lock_guard<std::mutex> lock(g_prof.mu);
+    g_prof.on = false;
+    return g_prof.n;
+}
+
+pkv_status pkv_profile_read(int32_t index, int32_t *kernel_id, float *ms)
+{
+    std::lock_guard<std::mutex> lock(g_prof.mu);
+    if (index < 0 || index >= g_prof.n || !kernel_id || !ms) return PKV_ERR_INVALID_ARG;
+    cudaError_t e = cudaEventSynchronize(g_prof.events[2 * index + 1]);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(ms, g_prof.events[2 * index], g_prof.events[2 * index + 1]);
+    if (e != cudaSuccess) return cuda_fail(e, "profile read");
+    *kernel_id = g_prof.kernel[index];
+    return PKV_OK;
+}
+
+pkv_status pkv_paged_kv_write(const void *k, const void *v, void *k_cache, void *v_cache,
+                              const int64_t *slot_mapping, int32_t num_tokens,
+                              int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                              int32_t num_blocks_total, uint32_t *device_error,
+                              cudaStream_t stream)
+{
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks_total <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k || !v || !k_cache || !v_cache || !slot_mapping) return PKV_ERR_INVALID_ARG;
+    if (head_dim % 8 != 0) return PKV_ERR_UNSUPPORTED;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(slot_mapping, 8))
+        return PKV_ERR_UNSUPPORTED;
+    int64_t row_bytes = (int64_t)num_kv_heads * head_dim * 2;
+    if (row_bytes > (1 << 30)) return PKV_ERR_UNSUPPORTED;
+    int64_t num_slots = (int64_t)num_blocks_total * block_size;
+    cudaError_t e = launch_kv_write(k, v, k_cache, v_cache, slot_mapping, num_tokens, (int32_t)row_bytes,
+                                    num_slots, device_error, stream);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "paged_kv_write launch");
+}
+
+size_t pkv_attention_workspace_bytes(int32_t max_num_reqs, int32_t max_num_tokens, int32_t num_q_heads,
+                                     int32_t head_dim, int32_t max_seq_len)
+{
+    if (max_num_reqs <= 0 || max_num_tokens <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_seq_len <= 0)
+        return kErrBytes;
+    int64_t splits = (max_seq_len + kMinSplit - 1) / kMinSplit;
+    if (splits > kMaxSplits) splits = kMaxSplits;
+    int64_t dec_tokens = (int64_t)max_num_reqs * kDecodeRows;
+    if (dec_tokens > max_num_tokens) dec_tokens = max_num_tokens;
+    int64_t rows = splits * dec_tokens * num_q_heads;
+    return kErrBytes + (size_t)rows * ((size_t)head_dim * 4 + 8) + 64;
+}
+
+pkv_status pkv_plan_request_kernels(const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs,
+                                    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                    int32_t *class_out)
+{
+    if (num_reqs < 0 || !qsl_h || (num_reqs > 0 && (!sl_h || !class_out))) return PKV_ERR_INVALID_ARG;
+    if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads || head_dim <= 0)
+        return PKV_ERR_INVALID_ARG;
+    const int32_t g = num_q_heads / num_kv_heads;
+    for (int r = 0; r < num_reqs; r++) class_out[r] = request_class(qsl_h[r + 1] - qsl_h[r], sl_h[r], g);
+    return PKV_OK;
+}
+
+pkv_status pkv_clear_device_error(uint32_t *device_error, cudaStream_t stream)
+{
+    if (!device_error) return PKV_ERR_INVALID_ARG;
+    cudaError_t e = cudaMemsetAsync(device_error, 0, sizeof(uint32_t), stream);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "clear device error");
+}
+
+pkv_status pkv_read_device_error(const uint32_t *device_error, uint32_t *flags_out, cudaStream_t stream)
+{
+    if (!device_error) return PKV_ERR_INVALID_ARG;
+    uint32_t flags = 0;
+    cudaError_t e = cudaMemcpyAsync(&flags, device_error, sizeof flags, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "read device error");
+    if (flags_out) *flags_out = flags;
+    return flags ? PKV_ERR_DEVICE_BOUNDS : PKV_OK;
+}
+
+pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                      const int32_t *query_start_loc, const int32_t *seq_lens,
+                                      const int32_t *block_table, int32_t block_table_stride,
+                                      const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs,
+                                      int32_t num_tokens, int32_t max_query_len, int32_t max_seq_len,
+                                      int32_t hq, int32_t hkv, int32_t d, int32_t bs,
+                                      int32_t num_blocks_total, float scale, void *workspace,
+                                      size_t workspace_bytes, cudaStream_t stream)
+{
+    // ---- host validation
+    if (num_reqs < 0 || num_tokens < 0 || hq <= 0 || hkv <= 0 || d <= 0 || bs <= 0 || num_blocks_total <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (hq % hkv != 0) return PKV_ERR_INVALID_ARG;
+    if (!qsl_h || (num_reqs > 0 && !sl_h)) return PKV_ERR_INVALID_ARG;
+    if (qsl_h[0] != 0 || qsl_h[num_reqs] != num_tokens) return PKV_ERR_INVALID_ARG;
+    int32_t seen_q = 0, seen_l = 0;
+    for (int r = 0; r < num_reqs; r++) {
+        int32_t t = qsl_h[r + 1] - qsl_h[r], L = sl_h[r];
+        if (t < 0 || L < 0) return PKV_ERR_INVALID_ARG;
+        if (L > 0 && t > L) return PKV_ERR_INVALID_ARG;
+        if (L > 0 && (int64_t)(L + bs - 1) / bs > block_table_stride) return PKV_ERR_INVALID_ARG;
+        seen_q = t > seen_q ? t : seen_q;
+        seen_l = L > seen_l ? L : seen_l;
+    }
+    if (max_query_len < seen_q || max_seq_len < seen_l) return PKV_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < PKV_WORKSPACE_MIN_BYTES) return PKV_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return PKV_ERR_WORKSPACE;
+    if (num_tokens == 0) return PKV_OK;
+    if (!out || !q || !k_cache || !v_cache || !query_start_loc || !seq_lens || !block_table)
+        return PKV_ERR_INVALID_ARG;
+    const int32_t g = hq / hkv;
+    if (d != 48 && d != 64 && d != 128) return PKV_ERR_UNSUPPORTED;
+    if (bs != 16) return PKV_ERR_UNSUPPORTED;
+    if (g > kDecodeRows) return PKV_ERR_UNSUPPORTED;
+    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+        return PKV_ERR_UNSUPPORTED;
+
+    // ---- classify
+    std::vector<int32_t> dec, pre;
+    int64_t dec_keys = 0;
+    for (int r = 0; r < num_reqs; r++) {
+        int32_t t = qsl_h[r + 1] - qsl_h[r], L = sl_h[r];
+        switch (request_class(t, L, g)) {
+        case PKV_CLASS_PADDING:
+        case PKV_CLASS_DECODE: dec.push_back(r); dec_keys += L; break;
+        case PKV_CLASS_PREFILL_CUDA_CORE: pre.push_back(r); break;
+        default: break;                                         // no rows at all
+        }
+    }
+
+    // ---- split size for decode-class requests
+    const int sms = num_sms();
+    int split = env_int("PKV_SPLIT_TOKENS", 0);
+    if (split <= 0) {
+        int64_t target_ctas = (int64_t)sms * 8;
+        int64_t s = (dec_keys * hkv + target_ctas - 1) / (target_ctas > 0 ? target_ctas : 1);
+        if (s < kMinSplit) s = kMinSplit;
+        split = (int)((s + 127) / 128 * 128);
+    }
+    if (split % bs) split += bs - split % bs;
+    auto splits_of = [&](int32_t L, int sp) { return L <= 0 ? 1 : (L + sp - 1) / sp; };
+    // every split request keeps S * t * hq partial rows; grow the split until they fit
+    const size_t row_bytes = (size_t)d * 4 + 8;
+    const size_t avail = workspace_bytes - kErrBytes;
+    for (;;) {
+        size_t rows = 0;
+        bool too_many = false;
+        for (int32_t r : dec) {
+            int32_t S = splits_of(sl_h[r], split);
+            if (S > kMaxSplits) too_many = true;
+            if (S > 1) rows += (size_t)S * (qsl_h[r + 1] - qsl_h[r]) * hq;
+        }
+        if (!too_many && rows * row_bytes + 64 <= avail) break;
+        if (split >= seen_l) break;                              // nothing is split any more
+        split *= 2;
+    }
+
+    char *ws = static_cast<char *>(workspace);
+    AttnParams p;
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.k_cache = static_cast<const __nv_bfloat16 *>(k_cache);
+    p.v_cache = static_cast<const __nv_bfloat16 *>(v_cache);
+    p.qsl = query_start_loc;
+    p.seq_lens = seq_lens;
+    p.block_table = block_table;
+    p.bt_stride = block_table_stride;
+    p.hq = hq;
+    p.hkv = hkv;
+    p.group = g;
+    p.block_size = bs;
+    p.nb_total = num_blocks_total;
+    const float sc = scale > 0.f ? scale : 1.0f / sqrtf((float)d);
+    p.scale_log2 = sc * 1.4426950408889634f;
+    p.err = reinterpret_cast<uint32_t *>(ws);
+    // partial rows: first all o rows, then the (m, l) pairs
+    size_t total_rows = 0;
+    for (int32_t r : dec) {
+        int32_t S = splits_of(sl_h[r], split);
+        if (S > 1) total_rows += (size_t)S * (qsl_h[r + 1] - qsl_h[r]) * hq;
+    }
+    p.part_o = reinterpret_cast<float *>(ws + kErrBytes);
+    p.part_ml = reinterpret_cast<float2 *>(ws + kErrBytes + ((total_rows * d * 4 + 15) / 16) * 16);
+
+    // ---- decode-class launches (chunks of kPlanMax requests)
+    std::vector<int32_t> combine_reqs, combine_off;
+    int combine_max_rows = 0;
+    size_t part_cursor = 0;
+    for (size_t c0 = 0; c0 < dec.size(); c0 += kPlanMax) {
+        WorkList wl;
+        memset(&wl, 0, sizeof wl);
+        wl.mode = kModeDecode;
+        wl.split_tokens = split;
+        wl.tile_tokens = 0;
+        int items = 0, rows = 1;
+        size_t c1 = c0 + kPlanMax < dec.size() ? c0 + kPlanMax : dec.size();
+        for (size_t x = c0; x < c1; x++) {
+            int32_t r = dec[x];
+            int32_t t = qsl_h[r + 1] - qsl_h[r];
+            int32_t S = splits_of(sl_h[r], split);
+            int li = wl.n++;
+            wl.req[li] = r;
+            wl.item_off[li] = items;
+            wl.part_off[li] = -1;
+            if (S > 1) {
+                wl.part_off[li] = (int32_t)part_cursor;
+                combine_reqs.push_back(r);
+                combine_off.push_back((int32_t)part_cursor);
+                part_cursor += (size_t)S * t * hq;
+                if (t * hq > combine_max_rows) combine_max_rows = t * hq;
+            }
+            items += S;
+            if (sl_h[r] > 0 && t * g > rows) rows = t * g;
+        }
+        wl.item_off[wl.n] = items;
+        cudaError_t e = launch_attn_fma(p, wl, d, rows, items, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
+    }
+    if (part_cursor > (size_t)INT32_MAX) return PKV_ERR_WORKSPACE;
+
+    // ---- prefill-class launches
+    const int tile = kDecodeRows / g;
+    for (size_t c0 = 0; c0 < pre.size(); c0 += kPlanMax) {
+        WorkList wl;
+        memset(&wl, 0, sizeof wl);
+        wl.mode = kModePrefill;
+        wl.split_tokens = 0;
+        wl.tile_tokens = tile;
+        int items = 0;
+        size_t c1 = c0 + kPlanMax < pre.size() ? c0 + kPlanMax : pre.size();
+        for (size_t x = c0; x < c1; x++) {
+            int32_t r = pre[x];
+            int32_t t = qsl_h[r + 1] - qsl_h[r];
+            int li = wl.n++;
+            wl.req[li] = r;
+            wl.item_off[li] = items;
+            wl.part_off[li] = -1;
+            items += (t + tile - 1) / tile;
+        }
+        wl.item_off[wl.n] = items;
+        cudaError_t e = launch_attn_fma(p, wl, d, kDecodeRows, items, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "prefill attention launch");
+    }
+
+    // ---- combine split partials
+    for (size_t c0 = 0; c0 < combine_reqs.size(); c0 += kPlanMax) {
+        WorkList wl;
+        memset(&wl, 0, sizeof wl);
+        wl.mode = kModeDecode;
+        wl.split_tokens = split;
+        size_t c1 = c0 + kPlanMax < combine_reqs.size() ? c0 + kPlanMax : combine_reqs.size();
+        for (size_t x = c0; x < c1; x++) {
+            int li = wl.n++;
+            wl.req[li] = combine_reqs[x];
+            wl.part_off[li] = combine_off[x];
+            wl.item_off[li] = li;
+        }
+        wl.item_off[wl.n] = wl.n;
+        cudaError_t e = launch_attn_combine(p, wl, d, combine_max_rows, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "split combine launch");
+    }
+    return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,102 @@
+"""The C ABI on a host without a GPU: the library loads, exports every
+function include/pkv.h declares, and its host-only logic (status strings,
+workspace sizing, request classification, argument validation) answers
+without touching CUDA."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pkv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_84_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_two_calls():
+    names = declared()
+    assert "pkv_paged_kv_write" in names and "pkv_ragged_paged_attention" in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (pkv_\w+)", out))
+    assert set(declared()) <= exported
+
+
+def test_header_compiles_as_c():
+    src = '#include "pkv.h"\nint main(void){return (int)PKV_OK;}\n'
+    r = subprocess.run(["gcc", "-x", "c", "-std=c99", "-fsyntax-only", "-I", os.path.join(ROOT, "include"),
+                        "-I", "/usr/local/cuda/include", "-"], input=src, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
+def test_host_only_functions(lib):
+    import paged_kv_cache_84_gb300 as pkv
+    lib.pkv_status_string.restype = ctypes.c_char_p
+    assert lib.pkv_status_string(0) == b"ok"
+    assert lib.pkv_status_string(3).startswith(b"workspace")
+    assert pkv.attention_workspace_bytes(0, 0, 8, 64, 0) == pkv.WORKSPACE_MIN_BYTES
+    small = pkv.attention_workspace_bytes(4, 9, 8, 48, 42)
+    big = pkv.attention_workspace_bytes(32, 32, 64, 128, 32768)
+    assert pkv.WORKSPACE_MIN_BYTES < small < big
+    # layout example: every request is decode-class (t * g <= 16)
+    assert pkv.plan_request_kernels([0, 3, 4, 5, 9], [9, 42, 10, 4], 8, 4, 48) == ["decode"] * 4
+    # a 64-token chunk with g = 2 is a prefill tile job; seq_len 0 is padding; t = 0 is nothing
+    assert pkv.plan_request_kernels([0, 64, 65, 65], [300, 0, 7], 8, 4, 48) == \
+        ["prefill_cuda_core", "padding", "none"]
+
+
+def _attn_args(qsl, sl, R, N, maxq, maxl, hq=8, hkv=4, d=64, bs=16, stride=4, ws=1 << 20):
+    fake = ctypes.c_void_p(1 << 20)                 # never dereferenced: validation fails first
+    qsl_h = (ctypes.c_int32 * len(qsl))(*qsl)
+    sl_h = (ctypes.c_int32 * max(1, len(sl)))(*sl)
+    return [fake] * 7 + [stride, qsl_h, sl_h, R, N, maxq, maxl, hq, hkv, d, bs, 100, ctypes.c_float(0.1),
+                         fake, ctypes.c_size_t(ws), None]
+
+
+@pytest.mark.parametrize("qsl,sl,maxq,maxl,kw", [
+    ([0, 3, 2, 5], [9, 9, 9], 3, 9, {}),             # not non-decreasing
+    ([0, 3, 4, 6], [9, 9, 9], 3, 9, {}),             # does not end at N
+    ([0, 3, 4, 5], [2, 9, 9], 3, 9, {}),             # t > L
+    ([0, 3, 4, 5], [9, 99, 9], 3, 99, {}),           # table narrower than ceil(L / 16)
+    ([0, 3, 4, 5], [9, 9, 9], 2, 9, {}),             # max_query_len below the data
+    ([0, 3, 4, 5], [9, 9, 9], 3, 8, {}),             # max_seq_len below the data
+    ([0, 3, 4, 5], [9, 9, 9], 3, 9, {"hkv": 3}),     # hq % hkv != 0
+])
+def test_attention_host_validation(lib, qsl, sl, maxq, maxl, kw):
+    lib.pkv_ragged_paged_attention.restype = ctypes.c_int
+    args = _attn_args(qsl, sl, len(sl), 5, maxq, maxl, **kw)
+    assert lib.pkv_ragged_paged_attention(*args) == 1
+
+
+def test_attention_unsupported_and_workspace(lib):
+    lib.pkv_ragged_paged_attention.restype = ctypes.c_int
+    assert lib.pkv_ragged_paged_attention(*_attn_args([0, 1], [5], 1, 1, 1, 5, d=96)) == 2
+    assert lib.pkv_ragged_paged_attention(*_attn_args([0, 1], [5], 1, 1, 1, 5, bs=32)) == 2
+    assert lib.pkv_ragged_paged_attention(*_attn_args([0, 1], [5], 1, 1, 1, 5, ws=64)) == 3
+
+
+def test_write_host_validation(lib):
+    lib.pkv_paged_kv_write.restype = ctypes.c_int
+    fake = ctypes.c_void_p(1 << 20)
+    assert lib.pkv_paged_kv_write(fake, fake, fake, fake, fake, -1, 4, 64, 16, 10, None, None) == 1
+    assert lib.pkv_paged_kv_write(fake, fake, fake, fake, fake, 0, 4, 64, 16, 10, None, None) == 0
+    assert lib.pkv_paged_kv_write(fake, fake, fake, fake, fake, 3, 4, 60, 16, 10, None, None) == 2
+    odd = ctypes.c_void_p((1 << 20) + 8)
+    assert lib.pkv_paged_kv_write(odd, fake, fake, fake, fake, 3, 4, 64, 16, 10, None, None) == 2

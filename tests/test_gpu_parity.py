@@ -1,0 +1,301 @@
+"""CUDA library vs the CPU oracle, element by element, on the same seeded inputs.
+
+paged_kv_write and all indexing: bit-exact (whole pool except the scratch
+slot).  Attention (bf16 in, fp32 accumulate) against the fp64 oracle:
+max |err| <= 2e-2 and mean |err| <= 2e-3.
+"""
+import math
+
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_84_gb300 as pkv
+from workloads import Batch, Req, Spec, build_meta, config_spec, make_batch, random_spec
+from _helpers import (DeviceStep, assert_close, cpu_copy, device_batch, oracle_full, oracle_rows,
+                      oracle_write)
+
+pytestmark = pytest.mark.gpu
+
+
+def _pool_bits(t):
+    nbt, bs, hkv, d = t.shape
+    return t.contiguous().view(torch.int16).view(nbt * bs, hkv * d)
+
+
+def _check_write(dev: DeviceStep, ref_cpu):
+    """Whole pool except the scratch slot, bit for bit."""
+    for got, want in ((dev.k_cache, ref_cpu.k_cache), (dev.v_cache, ref_cpu.v_cache)):
+        g = _pool_bits(got.cpu())[:-1]
+        w = _pool_bits(want)[:-1]
+        assert torch.equal(g, w)
+    assert pkv.read_device_error(dev.write_err) == 0
+
+
+# ------------------------------------------------------------------ small configs: full compare
+
+@pytest.mark.parametrize("cfg", [1, 2])
+def test_config_full_parity(cfg):
+    spec = config_spec(cfg)
+    b = make_batch(spec, device="cpu")
+    dev = DeviceStep(b)
+    dev.step()
+    torch.cuda.synchronize()
+    ref = cpu_copy(b)
+    oracle_write(ref)
+    _check_write(dev, ref)
+    want = oracle_full(ref)
+    assert_close(dev.out, want, f"config {cfg}")
+    assert pkv.read_device_error(dev.ws) == 0
+
+
+RANDOM_CASES = [
+    # seed, reqs, max_ctx, max_new, hq, hkv, d, pad rows
+    (0, 6, 300, 40, 8, 8, 48, 0),
+    (1, 9, 700, 70, 8, 4, 64, 2),
+    (2, 5, 1200, 130, 32, 8, 128, 1),
+    (3, 12, 2500, 33, 16, 2, 128, 0),
+    (4, 7, 90, 90, 8, 1, 64, 3),
+    (5, 4, 4100, 300, 64, 8, 128, 0),
+    (6, 16, 600, 1, 32, 8, 128, 0),
+    (7, 3, 33, 33, 4, 4, 48, 1),
+]
+
+
+@pytest.mark.parametrize("case", RANDOM_CASES, ids=[f"seed{c[0]}" for c in RANDOM_CASES])
+def test_random_mixes_full_parity(case):
+    seed, reqs, ctx, new, hq, hkv, d, pad = case
+    spec = random_spec(seed, reqs, ctx, new, hq, hkv, d, pad_rows=pad)
+    b = make_batch(spec, device="cpu")
+    dev = DeviceStep(b)
+    dev.step()
+    torch.cuda.synchronize()
+    ref = cpu_copy(b)
+    oracle_write(ref)
+    _check_write(dev, ref)
+    assert_close(dev.out, oracle_full(ref), f"random {seed}")
+
+
+@pytest.mark.parametrize("split", [256, 512, 4096])
+def test_forced_split_sizes(split, monkeypatch):
+    monkeypatch.setenv("PKV_SPLIT_TOKENS", str(split))
+    spec = random_spec(11, 10, 3000, 3, 32, 8, 128, decode_frac=0.8)
+    b = make_batch(spec, device="cpu")
+    dev = DeviceStep(b)
+    dev.step()
+    ref = cpu_copy(b)
+    oracle_write(ref)
+    assert_close(dev.out, oracle_full(ref), f"split {split}")
+
+
+def test_minimum_workspace_disables_splitting():
+    spec = random_spec(12, 6, 5000, 1, 64, 8, 128, decode_frac=1.0)
+    b = make_batch(spec, device="cpu")
+    dev = DeviceStep(b, workspace_bytes=pkv.WORKSPACE_MIN_BYTES)
+    dev.step()
+    ref = cpu_copy(b)
+    oracle_write(ref)
+    assert_close(dev.out, oracle_full(ref), "min workspace")
+
+
+# ------------------------------------------------------------------ full-size configs: sampled rows
+
+def _sample_rows(spec, meta, gen, per_req_heads=1, extra=()):
+    toks, heads = [], []
+    for r, req in enumerate(spec.reqs):
+        b = meta.query_start_loc[r]
+        t = req.new
+        picks = sorted({0, t - 1, t // 2, min(t - 1, 127), min(t - 1, 128)})
+        for i in picks:
+            for h in torch.randint(0, spec.num_q_heads, (per_req_heads,), generator=gen).tolist():
+                toks.append(b + i)
+                heads.append(h)
+    for tok, h in extra:
+        toks.append(tok)
+        heads.append(h)
+    return toks, heads
+
+
+@pytest.mark.parametrize("cfg", [3, 4, 5])
+def test_config_full_size_sampled_parity(cfg):
+    spec = config_spec(cfg)
+    b = device_batch(spec)
+    ref = cpu_copy(b)                     # inputs, copied before any library kernel runs
+    dev = DeviceStep(b)
+    dev.step()
+    torch.cuda.synchronize()
+    assert torch.isfinite(dev.out.float()).all()
+    oracle_write(ref)
+    _check_write(dev, ref)
+    gen = torch.Generator().manual_seed(cfg)
+    extra = []
+    if cfg == 4:                          # tile edges of the long chunk, every head of one row
+        extra = [(i, h) for i in (31, 32, 63, 64, 1000, 2047) for h in range(0, 32, 7)]
+        extra += [(2048 + 64 + 1023, h) for h in range(32)]
+    toks, heads = _sample_rows(spec, b.meta, gen, per_req_heads=2 if cfg != 3 else 1, extra=extra)
+    want = oracle_rows(ref, toks, heads)
+    got = dev.out[torch.tensor(toks), torch.tensor(heads)]
+    assert_close(got, want, f"config {cfg} sampled")
+    assert pkv.read_device_error(dev.ws) == 0
+
+
+# ------------------------------------------------------------------ invariances through the GPU path
+
+def test_chunked_prefill_steps_match_oracle():
+    """One prompt in chunks of 8/33/64/4096 over successive write+attend steps."""
+    L, hq, hkv, d, bs = 300, 32, 8, 128, 16
+    gen = torch.Generator().manual_seed(71)
+    K = torch.randn((L, hkv, d), generator=gen).to(torch.bfloat16)
+    V = torch.randn((L, hkv, d), generator=gen).to(torch.bfloat16)
+    Q = torch.randn((L, hq, d), generator=gen).to(torch.bfloat16)
+    nb = -(-L // bs) + 3
+    table = torch.randperm(nb, generator=gen)[: -(-L // bs)].tolist()
+    outs = {}
+    for chunk in (8, 33, 64, 4096):
+        kc = torch.zeros((nb + 1, bs, hkv, d), dtype=torch.bfloat16, device="cuda")
+        vc = torch.zeros_like(kc)
+        kc_ref = kc.cpu()
+        vc_ref = vc.cpu()
+        got = []
+        c = 0
+        while c < L:
+            t = min(chunk, L - c)
+            spec = Spec("chunk", [Req(c, t, table)], hq, hkv, d, bs, nb, 1 / math.sqrt(d), 0)
+            meta = build_meta(spec)
+            step = DeviceStep(Batch(spec, meta, Q[c:c + t], K[c:c + t], V[c:c + t], kc_ref, vc_ref),
+                              pools=(kc, vc))
+            step.step()
+            oracle.paged_kv_write(kc_ref, vc_ref, K[c:c + t], V[c:c + t], meta.slot_mapping)
+            want = oracle.ragged_paged_attention(Q[c:c + t], kc_ref, vc_ref, meta.query_start_loc,
+                                                 meta.seq_lens, meta.block_table, spec.scale, 8)
+            assert_close(step.out, want, f"chunk {chunk} at {c}")
+            got.append(step.out.float().cpu())
+            c += t
+        outs[chunk] = torch.cat(got)
+    base = outs[8]
+    for chunk, o in outs.items():
+        assert (o - base).abs().max().item() <= 2 * 2e-2
+
+
+def test_block_permutation_and_shared_prefix():
+    """Shared prefix blocks vs private copies, and a physical permutation of the pool."""
+    spec = config_spec(2)
+    b = make_batch(spec, device="cpu")
+    dev = DeviceStep(b)
+    dev.step()
+    base = dev.out.float().cpu()
+    # permute physical blocks (scratch block stays last)
+    nbt = b.k_cache.shape[0]
+    perm = torch.randperm(nbt - 1, generator=torch.Generator().manual_seed(5))
+    kc2, vc2 = b.k_cache.clone(), b.v_cache.clone()
+    kc2[perm] = b.k_cache[:nbt - 1]
+    vc2[perm] = b.v_cache[:nbt - 1]
+    reqs2 = [Req(r.computed, r.new, [int(perm[x]) for x in r.table]) for r in spec.reqs]
+    spec2 = Spec(spec.name, reqs2, spec.num_q_heads, spec.num_kv_heads, spec.head_dim, spec.block_size,
+                 spec.num_blocks, spec.scale, spec.seed)
+    b2 = Batch(spec2, build_meta(spec2), b.q, b.k, b.v, kc2, vc2)
+    dev2 = DeviceStep(b2)
+    dev2.step()
+    ref2 = cpu_copy(b2)
+    oracle_write(ref2)
+    assert_close(dev2.out, oracle_full(ref2), "permuted")
+    assert (dev2.out.float().cpu() - base).abs().max().item() <= 2 * 2e-2
+
+
+# ------------------------------------------------------------------ edge cases
+
+def test_empty_batch_is_a_noop():
+    spec = Spec("empty", [], 8, 4, 64, 16, 4, 0.125, 0)
+    b = make_batch(spec, device="cpu")
+    dev = DeviceStep(b)
+    before = pkv.launch_count()
+    dev.step()
+    torch.cuda.synchronize()
+    assert pkv.launch_count() == before
+
+
+def test_padding_requests_give_zero_rows():
+    reqs = [Req(10, 2, [0]), Req(0, 1, [], pad=True), Req(20, 1, [1, 2]), Req(0, 1, [], pad=True)]
+    spec = Spec("pad", reqs, 8, 2, 64, 16, 4, 0.125, 3)
+    b = make_batch(spec, device="cpu")
+    dev = DeviceStep(b)
+    dev.step()
+    ref = cpu_copy(b)
+    oracle_write(ref)
+    want = oracle_full(ref)
+    assert_close(dev.out, want, "padding")
+    assert dev.out[2].abs().sum().item() == 0 and dev.out[4].abs().sum().item() == 0
+    # padding rows wrote to the scratch slot only
+    _check_write(dev, ref)
+
+
+def test_invalid_metadata_is_rejected_on_host():
+    spec = Spec("bad", [Req(5, 3, [0]), Req(20, 1, [1, 2]), Req(0, 4, [3])], 8, 4, 64, 16, 5, 0.125, 0)
+    b = make_batch(spec, device="cpu")
+    dev = DeviceStep(b)
+    m = b.meta
+
+    def call(qsl=m.query_start_loc, sl=m.seq_lens, bt=dev.bt, maxq=m.max_query_len, maxl=m.max_seq_len):
+        pkv.ragged_paged_attention(dev.out, dev.q, dev.k_cache, dev.v_cache, dev.qsl, dev.sl, bt,
+                                   qsl, sl, maxq, maxl, 0.1, dev.ws)
+
+    before = pkv.launch_count()
+    cases = [
+        dict(sl=[2, 21, 4]),                                  # t = 3 > seq_len = 2
+        dict(bt=dev.bt[:, :1].contiguous()),                  # table narrower than ceil(L / 16)
+        dict(qsl=[0, 4, 3, 8]),                               # query_start_loc not non-decreasing
+        dict(qsl=[0, 3, 4, 7]),                               # does not end at num_tokens
+        dict(maxl=10),                                        # max_seq_len below the data
+    ]
+    for kw in cases:
+        with pytest.raises(pkv.PkvError) as e:
+            call(**kw)
+        assert e.value.status == 1, kw
+    assert pkv.launch_count() == before
+    call()                                                    # the valid call still works
+    assert pkv.launch_count() > before
+
+
+def test_unsupported_head_dim():
+    spec = Spec("d96", [Req(3, 1, [0])], 4, 2, 96, 16, 2, 0.1, 0)
+    b = make_batch(spec, device="cpu")
+    dev = DeviceStep(b)
+    with pytest.raises(pkv.PkvError) as e:
+        dev.attend()
+    assert e.value.status == 2
+
+
+def test_out_of_pool_block_id_sets_flag_without_fault():
+    spec = random_spec(21, 4, 200, 4, 8, 4, 64)
+    b = make_batch(spec, device="cpu")
+    dev = DeviceStep(b)
+    dev.write()
+    bt = dev.bt.clone()
+    bt[0, 0] = spec.num_blocks_total + 5          # the device table points outside the pool
+    dev.bt = bt
+    pkv.clear_device_error(dev.ws)
+    dev.attend()
+    assert pkv.read_device_error(dev.ws) & pkv.DEVERR_BLOCK
+    torch.cuda.synchronize()                      # the context is still usable
+    dev.bt = b.meta.block_table.cuda()
+    pkv.clear_device_error(dev.ws)
+    dev.attend()
+    assert pkv.read_device_error(dev.ws) == 0
+
+
+def test_out_of_pool_slot_sets_flag_and_skips():
+    spec = random_spec(22, 3, 100, 4, 8, 4, 64)
+    b = make_batch(spec, device="cpu")
+    dev = DeviceStep(b)
+    before = dev.k_cache.clone()
+    dev.slots = dev.slots.clone()
+    dev.slots[0] = spec.num_blocks_total * spec.block_size + 3
+    dev.write()
+    assert pkv.read_device_error(dev.write_err) & pkv.DEVERR_SLOT
+    ref = cpu_copy(b)
+    sm = b.meta.slot_mapping.clone()
+    keep = torch.ones(sm.numel(), dtype=torch.bool)
+    keep[0] = False
+    oracle.paged_kv_write(ref.k_cache, ref.v_cache, b.k[keep], b.v[keep], sm[keep])
+    assert torch.equal(_pool_bits(dev.k_cache.cpu())[:-1], _pool_bits(ref.k_cache)[:-1])
+    del before
