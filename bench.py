@@ -32,7 +32,7 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from workloads import CONFIG_NAMES, build_meta, config_spec, make_batch  # noqa: E402
+from workloads import CONFIG_NAMES, config_spec, make_batch, subset_spec  # noqa: E402
 
 METRIC = "ragged paged-attn step µs + KV-read HBM GB/s vs 8 TB/s; query tokens/s"
 UNIT = "query tokens/s"
@@ -280,8 +280,10 @@ class Step:
                                    self.spec.scale, self.ws)
 
 
-def build_copies(pkv, cfg, device, max_copies=512):
+def build_copies(pkv, cfg, device, max_copies=512, subset=0):
     spec = config_spec(cfg)
+    if subset:
+        spec = subset_spec(spec, subset)
     gen_dev = "cpu" if cfg in (1, 2) else device
     batch = make_batch(spec, device=gen_dev)
     first = Step(pkv, batch, device)
@@ -294,8 +296,8 @@ def build_copies(pkv, cfg, device, max_copies=512):
     return spec, copies
 
 
-def time_workload(pkv, cfg, steps, warmup, device, peaks, dist=None, clocks=None, use_graph=True):
-    spec, copies = build_copies(pkv, cfg, device)
+def time_workload(pkv, cfg, steps, warmup, device, peaks, dist=None, use_graph=True, subset=0):
+    spec, copies = build_copies(pkv, cfg, device, subset=subset)
     meta = copies[0].meta
     classes = pkv.plan_request_kernels(meta.query_start_loc, meta.seq_lens, spec.num_q_heads,
                                        spec.num_kv_heads, spec.head_dim)
@@ -376,7 +378,7 @@ def time_workload(pkv, cfg, steps, warmup, device, peaks, dist=None, clocks=None
 
     step_s = ms_per_step / 1e3
     res = {
-        "workload": CONFIG_NAMES[cfg], "config_index": cfg,
+        "workload": spec.name, "config_index": cfg,
         "ms_per_step": ms_per_step, "step_us": ms_per_step * 1e3,
         "query_tokens_per_s": acc["tokens"] / step_s,
         "kv_read_gbs": acc["unique_kv_bytes"] / step_s / 1e9,
@@ -509,7 +511,8 @@ def run_ours(args):
     warmup = max(3, args.warmup)
 
     clocks = ClockSampler(local).start()
-    spec, copies, head = time_workload(pkv, args.workload, args.steps, warmup, device, peaks, dist)
+    spec, copies, head = time_workload(pkv, args.workload, args.steps, warmup, device, peaks, dist,
+                                       subset=args.subset)
     t0, t1 = head.pop("timed_wall")
     e2e = e2e_workload(pkv, copies, max(3, min(args.steps, 200)), device)
     del copies
@@ -565,6 +568,8 @@ def main():
     ap.add_argument("--workload", type=int, default=HEADLINE, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--no-breakdown", action="store_true", help="time only the headline workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--subset", type=int, default=0,
+                    help="keep only the first N requests of the workload (smaller profiling runs)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

@@ -24,7 +24,7 @@ import torch
 
 __all__ = [
     "Req", "Spec", "Meta", "Batch", "build_meta", "make_batch", "config_spec",
-    "CONFIG_NAMES", "fill_normal_bf16",
+    "CONFIG_NAMES", "fill_normal_bf16", "subset_spec", "random_spec",
 ]
 
 
@@ -289,6 +289,23 @@ def config_spec(cfg: int, seed: int | None = None) -> Spec:
             reqs.append(Req(32767, 1, tab))
         return Spec(CONFIG_NAMES[5], reqs, 64, 8, 128, bs, nb, 1.0 / math.sqrt(128), seed)
     raise ValueError(f"unknown workload {cfg}")
+
+
+def subset_spec(spec: Spec, n: int) -> Spec:
+    """The first ``n`` requests of ``spec`` on a pool of their own: their blocks
+    renumbered in order of first use, the pool sized to the blocks used plus
+    10%.  A smaller instance of the same workload shape (for profiling)."""
+    reqs = spec.reqs[:n]
+    remap = {}
+    for r in reqs:
+        for blk in r.table:
+            remap.setdefault(blk, len(remap))
+    gen = torch.Generator().manual_seed(spec.seed)
+    nb = math.ceil(1.1 * max(1, len(remap)))
+    perm = torch.randperm(nb, generator=gen).tolist()
+    new = [Req(r.computed, r.new, [perm[remap[b]] for b in r.table], r.pad) for r in reqs]
+    return Spec(f"{spec.name}[:{n}]", new, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
+                spec.block_size, nb, spec.scale, spec.seed)
 
 
 def random_spec(seed: int, num_reqs: int, max_ctx: int, max_new: int, num_q_heads: int,
