@@ -170,6 +170,47 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q,
                                       cudaStream_t stream);
 
 /*
+ * ragged_paged_attention without a caller workspace.  The pages have no
+ * counterpart of this call: it exists for callers that cannot allocate
+ * device memory, such as code running under a stream capture that forbids
+ * allocation, plain C hosts without a device allocator, and serving loops
+ * that must not call cudaMalloc because it may synchronise the device.
+ *
+ * Same arguments and results as pkv_ragged_paged_attention, except:
+ *  - No workspace: the split-KV partials and the device error word live in
+ *    one static device array of PKV_NOALLOC_SCRATCH_BYTES inside the
+ *    library.  Every GPU that loads the library holds that array until the
+ *    process exits.  The call allocates nothing and calls no allocating
+ *    routine.
+ *  - A batch whose workspace need, pkv_attention_workspace_bytes(num_reqs,
+ *    num_tokens, num_q_heads, head_dim, max_seq_len), exceeds
+ *    PKV_NOALLOC_SCRATCH_BYTES is rejected with PKV_ERR_WORKSPACE before
+ *    anything is enqueued.
+ *  - device_error (device uint32_t, may be NULL) receives this call's
+ *    bounds flags (overwritten, not OR-ed).
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and keeps it; make
+ *    that first call before any stream capture.
+ *  - All calls share the one array and it keeps the last call's contents:
+ *    the call itself resets the error word, and calls whose work overlaps
+ *    on the GPU (other streams, other threads) race on the array.
+ *    Serialise them, for example on one stream.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (8u << 20)
+pkv_status pkv_ragged_paged_attention_noalloc(void *out, const void *q,
+                                              const void *k_cache, const void *v_cache,
+                                              const int32_t *query_start_loc, const int32_t *seq_lens,
+                                              const int32_t *block_table, int32_t block_table_stride,
+                                              const int32_t *query_start_loc_host,
+                                              const int32_t *seq_lens_host,
+                                              int32_t num_reqs, int32_t num_tokens,
+                                              int32_t max_query_len, int32_t max_seq_len,
+                                              int32_t num_q_heads, int32_t num_kv_heads,
+                                              int32_t head_dim, int32_t block_size,
+                                              int32_t num_blocks_total, float scale,
+                                              uint32_t *device_error, cudaStream_t stream);
+
+/*
  * Which kernel path pkv_ragged_paged_attention takes for each request
  * (host only, no CUDA call): class_out[r] receives one of PKV_CLASS_*.
  * Decode-class requests (t * g <= 16) run on the CUDA-core decode kernel,
