@@ -177,8 +177,10 @@ def accounting(spec, meta, classes):
 
 
 KERNEL_CLASS = {"attn_fma_decode": ("decode", "padding"), "attn_fma_prefill": ("prefill_cuda_core",),
+                "attn_mma_decode": ("decode", "padding"), "attn_mma_prefill": ("prefill_cuda_core",),
                 "attn_tc_prefill": ("prefill_tensor",)}
 KERNEL_BOUND = {"paged_kv_write": "hbm", "attn_fma_decode": "hbm", "attn_fma_prefill": "alu",
+                "attn_mma_decode": "hbm", "attn_mma_prefill": "tensor",
                 "attn_tc_prefill": "tensor", "attn_split_combine": "hbm"}
 
 
@@ -202,7 +204,8 @@ def alu_peak_tflops(peaks):
 def source_hash(name):
     """Hash of the source file of a kernel, to tell whether stored ncu counters are current."""
     fname = {"paged_kv_write": "kv_write.cu", "attn_fma_decode": "attn_fma.cu", "attn_fma_prefill": "attn_fma.cu",
-             "attn_split_combine": "attn_fma.cu", "attn_tc_prefill": "attn_tc.cu"}.get(name)
+             "attn_split_combine": "attn_fma.cu", "attn_tc_prefill": "attn_tc.cu",
+             "attn_mma_decode": "attn_mma.cu", "attn_mma_prefill": "attn_mma.cu"}.get(name)
     path = os.path.join(ROOT, "paged_kv_cache_84_gb300", "csrc", fname or "")
     if not fname or not os.path.exists(path):
         return None

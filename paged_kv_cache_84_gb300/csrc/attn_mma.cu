@@ -1,0 +1,441 @@
+// Ragged paged attention with TMA-staged KV blocks and warp-level MMA.
+//
+// One CTA = (listed request, KV head, item), 5 warps:
+//   - warp 4 (producer) walks the CTA's key range block by block: it reads
+//     the physical block ids from the request's block table ("31. Engine
+//     v2", "Attention over the pool": key j lives in block table[j / 16],
+//     row j % 16) and issues one 3-D TMA copy per 16-row slice of a K or V
+//     block (one KV head, [16][head_dim]) into a ring of shared-memory
+//     stages, each completing on its stage's "full" mbarrier;
+//   - warps 0..3 (consumers) take the rows of the CTA (pairs (token, query
+//     head) that share KV head kh: the grouped-query fold of the vllm-lite
+//     README) in tiles of 16.  With KG key groups, warp w works on row tile
+//     w / KG and on every KG-th block of the stage ring.
+// Each consumer computes S = Q K^T for 16 rows x 16 keys with
+// mma.m16n8k16 (bf16 in, fp32 accumulate), applies the causal rule (query i
+// of a request with t new tokens and context L sits at position L - t + i
+// and sees keys 0 .. that position), runs the online softmax in the exp2
+// domain, and accumulates O += P V with P taken straight from the S
+// registers.  Key groups merge through shared memory at the end.  Unsplit
+// items write bf16 output; split items write fp32 partials (unnormalised o,
+// running max, weight sum) for the combine kernel.
+//
+// Shared-memory tiles: for head_dim 64/128 each TMA box is 16 rows x 64
+// columns (128 bytes) with the 128-byte swizzle, so that ldmatrix reads
+// eight rows without bank conflicts; for head_dim 48 rows are 96 bytes, not
+// swizzled.
+#include <mutex>
+
+#include "common.cuh"
+#include "sm100.cuh"
+
+namespace pkv {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kMmaThreads = (kConsumerWarps + 1) * 32;
+constexpr int kStageBudget = 96 * 1024;      // bytes of KV stages per CTA (two CTAs per SM)
+
+template <int D>
+struct MmaTile {
+    static constexpr bool kSwizzle = D != 48;
+    static constexpr int kBoxCols = kSwizzle ? 64 : D;       // columns per TMA box
+    static constexpr int kBoxes = D / kBoxCols;              // boxes per 16-row slice
+    static constexpr int kBoxBytes = 16 * kBoxCols * 2;
+    static constexpr int kTile = 16 * D * 2;                 // one K (or V) slice
+    static constexpr int kSlot = 2 * kTile;                  // K then V
+};
+
+// Byte offset of 16-byte chunk `chunk` of row `row` inside a K or V slice.
+template <int D>
+__device__ __forceinline__ uint32_t tile_off(int row, int chunk)
+{
+    if constexpr (D == 48) {
+        return row * 96 + chunk * 16;
+    } else {
+        const int box = chunk >> 3, c = chunk & 7;
+        return box * 2048 + row * 128 + ((c ^ (row & 7)) << 4);
+    }
+}
+
+template <int D, int KG>
+struct MmaCfg {
+    static constexpr int kRT = kConsumerWarps / KG;                          // row tiles
+    static constexpr int kStages0 = kStageBudget / (KG * MmaTile<D>::kSlot);
+    static constexpr int kStages = kStages0 > 8 ? 8 : (kStages0 < 2 ? 2 : kStages0);
+    static constexpr int kStageBytes = KG * MmaTile<D>::kSlot;
+    static constexpr int kRingBytes = kStages * kStageBytes;
+    static constexpr int kMergeBytes = kConsumerWarps * 16 * (D + 2) * 4;
+    static constexpr int kBodyBytes = kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes;
+    static constexpr int kSmemBytes = 1024 + kBodyBytes + 2 * kStages * 8;   // + alignment slack, barriers
+};
+
+template <int D, int KG>
+__global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, const __grid_constant__ WorkList wl,
+                                                               const __grid_constant__ CUtensorMap kmap,
+                                                               const __grid_constant__ CUtensorMap vmap)
+{
+    using T = MmaTile<D>;
+    using C = MmaCfg<D, KG>;
+    constexpr int S = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t ring = (raw + 1023u) & ~1023u;                 // 1024-aligned for the swizzle
+    uint8_t *ring_ptr = smem_raw + (ring - raw);
+    const uint32_t bars = ring + C::kBodyBytes;                   // full[S], then empty[S]
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kh = blockIdx.y;
+    const int li = find_listed(wl, blockIdx.x);
+    const int local = blockIdx.x - wl.item_off[li];
+    const int r = wl.req[li];
+    const int b = p.qsl[r], t = p.qsl[r + 1] - b, L = p.seq_lens[r];
+    const int g = p.group;
+
+    if (L == 0 || t == 0) {                                       // padding request: zero rows
+        for (int idx = threadIdx.x; idx < t * g * D; idx += kMmaThreads) {
+            const int rr = idx / D, e = idx - rr * D;
+            p.out[((size_t)(b + rr / g) * p.hq + kh * g + rr % g) * D + e] = __float2bfloat16(0.f);
+        }
+        return;
+    }
+
+    int i0, ntok, k_begin, k_end, split = 0;
+    bool partial = false;
+    if (wl.mode == kModeDecode) {
+        i0 = 0;
+        ntok = t;
+        split = local;
+        k_begin = split * wl.split_tokens;
+        k_end = min(L, k_begin + wl.split_tokens);
+        partial = wl.part_off[li] >= 0;
+    } else {
+        i0 = local * wl.tile_tokens;
+        ntok = min(wl.tile_tokens, t - i0);
+        k_begin = 0;
+        k_end = L - t + i0 + ntok;                                // one past the tile's last position
+    }
+    const int nr = ntok * g;                                      // rows of this CTA
+    const int blk0 = k_begin >> 4;
+    const int nblk = ((k_end + 15) >> 4) - blk0;
+    const int iters = (nblk + KG - 1) / KG;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; s++) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), kConsumerWarps);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            prefetch_tmap(&kmap);
+            prefetch_tmap(&vmap);
+        }
+        const int32_t *bt = p.block_table + (size_t)r * p.bt_stride + blk0;
+        int ids = 0, issued = 0;
+        for (int it = 0; it < iters; it++) {
+            const int base = it * KG;
+            if ((base & 31) == 0) ids = (base + lane < nblk) ? __ldg(bt + base + lane) : 0;
+            const int s = it % S;
+            bool ok = true;
+            if (it >= S) ok = mbar_wait(empty_bar(s), ((it / S) & 1) ^ 1, p.err);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            issued = it + 1;
+            const int nv = min(KG, nblk - base);
+            if (lane == 0) mbar_arrive_expect_tx(full_bar(s), nv * T::kSlot);
+            for (int j = 0; j < nv; j++) {
+                int blk = __shfl_sync(0xffffffffu, ids, (base + j) & 31);
+                if (lane == 0) {
+                    if (blk < 0 || blk >= p.nb_total) {           // outside the pool: report, read block 0
+                        atomicOr(p.err, 2u);
+                        blk = 0;
+                    }
+                    const uint32_t dst = ring + s * C::kStageBytes + j * T::kSlot;
+                    for (int x = 0; x < T::kBoxes; x++) {
+                        tma_load_3d(dst + x * T::kBoxBytes, &kmap, full_bar(s), x * T::kBoxCols, kh, blk * 16);
+                        tma_load_3d(dst + T::kTile + x * T::kBoxBytes, &vmap, full_bar(s), x * T::kBoxCols, kh,
+                                    blk * 16);
+                    }
+                }
+            }
+            __syncwarp();
+        }
+        // Normally every issued stage has been consumed by now.  If a wait
+        // gave up, keep the CTA (and its shared memory) alive until the
+        // copies still in flight have landed, within the same time limit.
+        if (issued < iters && lane == 0) {
+            for (int it = issued > S ? issued - S : 0; it < issued; it++)
+                mbar_wait(full_bar(it % S), (it / S) & 1, p.err);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int rt = warp / KG, kg = warp % KG;
+    const int row0 = rt * 16;
+    const int rA = row0 + (lane >> 2), rB = rA + 8;               // the two rows this lane holds
+    const int qbase = L - t + i0;
+    const int qposA = rA < nr ? qbase + rA / g : -1;
+    const int qposB = rB < nr ? qbase + rB / g : -1;
+
+    // Q as mma A fragments, straight from global memory (bf16 pairs).
+    uint32_t qa[D / 16][4];
+    {
+        const uint32_t *qw = reinterpret_cast<const uint32_t *>(p.q);
+        const size_t rowA = rA < nr ? ((size_t)(b + i0 + rA / g) * p.hq + kh * g + rA % g) * (D / 2) : 0;
+        const size_t rowB = rB < nr ? ((size_t)(b + i0 + rB / g) * p.hq + kh * g + rB % g) * (D / 2) : 0;
+        const int c = (lane & 3);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; kk++) {
+            qa[kk][0] = rA < nr ? __ldg(qw + rowA + kk * 8 + c) : 0u;
+            qa[kk][1] = rB < nr ? __ldg(qw + rowB + kk * 8 + c) : 0u;
+            qa[kk][2] = rA < nr ? __ldg(qw + rowA + kk * 8 + 4 + c) : 0u;
+            qa[kk][3] = rB < nr ? __ldg(qw + rowB + kk * 8 + 4 + c) : 0u;
+        }
+    }
+
+    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+    float o[D / 8][4];
+#pragma unroll
+    for (int n = 0; n < D / 8; n++) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+
+    const float sl2 = p.scale_log2;
+    const int mi = lane >> 3, mr = lane & 7;                      // ldmatrix: matrix, row within it
+    bool alive = true;
+    for (int it = 0; it < iters; it++) {
+        const int s = it % S;
+        if (!mbar_wait(full_bar(s), (it / S) & 1, p.err)) {
+            alive = false;
+            break;
+        }
+        const int bl = it * KG + kg;
+        if (bl < nblk) {
+            const uint32_t kt = ring + s * C::kStageBytes + kg * T::kSlot;
+            const uint32_t vt = kt + T::kTile;
+            const int key0 = (blk0 + bl) << 4;
+            float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+            for (int kk = 0; kk < D / 16; kk++) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(kt + tile_off<D>((mi >> 1) * 8 + mr, 2 * kk + (mi & 1)), b0, b1, b2, b3);
+                mma_16816(sc[0], qa[kk], b0, b1);
+                mma_16816(sc[1], qa[kk], b2, b3);
+            }
+            // scale into the exp2 domain, causal and range mask
+            const int kc = key0 + 2 * (lane & 3);
+#pragma unroll
+            for (int n = 0; n < 2; n++) {
+#pragma unroll
+                for (int v = 0; v < 4; v++) {
+                    const int key = kc + n * 8 + (v & 1);
+                    const int qp = v < 2 ? qposA : qposB;
+                    sc[n][v] = (key < k_end && key <= qp) ? sc[n][v] * sl2 : -INFINITY;
+                }
+            }
+            float pr[2][4];
+#pragma unroll
+            for (int hr = 0; hr < 2; hr++) {
+                float mx = fmaxf(fmaxf(sc[0][2 * hr], sc[0][2 * hr + 1]), fmaxf(sc[1][2 * hr], sc[1][2 * hr + 1]));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                const float mnew = fmaxf(m[hr], mx);
+                const float ms = mnew == -INFINITY ? 0.f : mnew;
+                const float alpha = exp2f(m[hr] - ms);
+                m[hr] = mnew;
+                pr[0][2 * hr] = exp2f(sc[0][2 * hr] - ms);
+                pr[0][2 * hr + 1] = exp2f(sc[0][2 * hr + 1] - ms);
+                pr[1][2 * hr] = exp2f(sc[1][2 * hr] - ms);
+                pr[1][2 * hr + 1] = exp2f(sc[1][2 * hr + 1] - ms);
+                l[hr] = l[hr] * alpha + (pr[0][2 * hr] + pr[0][2 * hr + 1]) + (pr[1][2 * hr] + pr[1][2 * hr + 1]);
+#pragma unroll
+                for (int n = 0; n < D / 8; n++) {
+                    o[n][2 * hr] *= alpha;
+                    o[n][2 * hr + 1] *= alpha;
+                }
+            }
+            uint32_t pa[4];
+            pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
+            pa[1] = pack_bf16x2(pr[0][2], pr[0][3]);
+            pa[2] = pack_bf16x2(pr[1][0], pr[1][1]);
+            pa[3] = pack_bf16x2(pr[1][2], pr[1][3]);
+#pragma unroll
+            for (int np = 0; np < D / 16; np++) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(vt + tile_off<D>((mi & 1) * 8 + mr, 2 * np + (mi >> 1)), b0, b1, b2, b3);
+                mma_16816(o[2 * np], pa, b0, b1);
+                mma_16816(o[2 * np + 1], pa, b2, b3);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(s));
+    }
+
+#pragma unroll
+    for (int hr = 0; hr < 2; hr++) {
+        l[hr] += __shfl_xor_sync(0xffffffffu, l[hr], 1);
+        l[hr] += __shfl_xor_sync(0xffffffffu, l[hr], 2);
+    }
+
+    // rows rA / rB -> (token, head) and the output or partial row
+    auto out_row = [&](int rr) -> size_t {
+        const int i = i0 + rr / g, h = kh * g + rr % g;
+        if (!partial) return (size_t)(b + i) * p.hq + h;
+        return (size_t)wl.part_off[li] + ((size_t)split * t + i) * p.hq + h;
+    };
+
+    if constexpr (KG == 1) {
+        if (!alive) return;
+#pragma unroll
+        for (int hr = 0; hr < 2; hr++) {
+            const int rr = hr ? rB : rA;
+            if (rr >= nr) continue;
+            const size_t orow = out_row(rr);
+            const int c = 2 * (lane & 3);
+            if (!partial) {
+                const float inv = l[hr] > 0.f ? 1.f / l[hr] : 0.f;
+                uint32_t *dst = reinterpret_cast<uint32_t *>(p.out + orow * D);
+#pragma unroll
+                for (int n = 0; n < D / 8; n++) dst[(n * 8 + c) / 2] = pack_bf16x2(o[n][2 * hr] * inv, o[n][2 * hr + 1] * inv);
+            } else {
+                float2 *dst = reinterpret_cast<float2 *>(p.part_o + orow * D);
+#pragma unroll
+                for (int n = 0; n < D / 8; n++) dst[(n * 8 + c) / 2] = make_float2(o[n][2 * hr], o[n][2 * hr + 1]);
+                if ((lane & 3) == 0) p.part_ml[orow] = make_float2(m[hr], l[hr]);
+            }
+        }
+    } else {
+        // merge the KG key groups of each row tile through shared memory
+        named_bar_sync(1, kConsumerWarps * 32);                   // every consumer is done with the ring
+        float *mo = reinterpret_cast<float *>(ring_ptr);          // [warp][16][D]
+        float *mml = mo + kConsumerWarps * 16 * D;                // [warp][16][2]
+        const int c = 2 * (lane & 3);
+#pragma unroll
+        for (int hr = 0; hr < 2; hr++) {
+            const int lr = (lane >> 2) + 8 * hr;
+#pragma unroll
+            for (int n = 0; n < D / 8; n++) {
+                mo[(warp * 16 + lr) * D + n * 8 + c] = o[n][2 * hr];
+                mo[(warp * 16 + lr) * D + n * 8 + c + 1] = o[n][2 * hr + 1];
+            }
+            if ((lane & 3) == 0) {
+                mml[(warp * 16 + lr) * 2] = m[hr];
+                mml[(warp * 16 + lr) * 2 + 1] = l[hr];
+            }
+        }
+        named_bar_sync(1, kConsumerWarps * 32);
+        if (!alive) return;
+        const int tid = threadIdx.x;
+        for (int idx = tid; idx < C::kRT * 16 * D; idx += kConsumerWarps * 32) {
+            const int rowc = idx / D, e = idx - rowc * D;        // row within the CTA
+            if (rowc >= nr) continue;
+            const int rtile = rowc >> 4, lr = rowc & 15;
+            float M = -INFINITY;
+#pragma unroll
+            for (int q = 0; q < KG; q++) M = fmaxf(M, mml[((rtile * KG + q) * 16 + lr) * 2]);
+            const float Ms = M == -INFINITY ? 0.f : M;
+            float acc = 0.f, ls = 0.f;
+#pragma unroll
+            for (int q = 0; q < KG; q++) {
+                const int wq = rtile * KG + q;
+                const float sc = exp2f(mml[(wq * 16 + lr) * 2] - Ms);
+                acc = fmaf(sc, mo[(wq * 16 + lr) * D + e], acc);
+                ls = fmaf(sc, mml[(wq * 16 + lr) * 2 + 1], ls);
+            }
+            const size_t orow = out_row(rowc);
+            if (!partial) {
+                p.out[orow * D + e] = __float2bfloat16(ls > 0.f ? acc / ls : 0.f);
+            } else {
+                p.part_o[orow * D + e] = acc;
+                if (e == 0) p.part_ml[orow] = make_float2(M, ls);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// Tensor map of one pool viewed as [slots][Hkv][D] with a box of one KV
+// head's 16 rows x box_cols columns.
+cudaError_t make_pool_tmap(CUtensorMap *map, const void *pool, int64_t num_slots, int hkv, int d, int box_cols,
+                           bool swizzle128)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)hkv, (cuuint64_t)num_slots};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)hkv * d * 2};
+    cuuint32_t box[3] = {(cuuint32_t)box_cols, 1, 16};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(pool), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return res == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int D, int KG>
+static cudaError_t launch_mma_dk(const AttnParams &p, const WorkList &wl, int num_items, const CUtensorMap &km,
+                                 const CUtensorMap &vm, cudaStream_t stream)
+{
+    constexpr int smem = MmaCfg<D, KG>::kSmemBytes;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(attn_mma_kernel<D, KG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    dim3 grid(num_items, p.hkv);
+    launch_begin(stream, wl.mode == kModeDecode ? kAttnMmaDecode : kAttnMmaPrefill);
+    attn_mma_kernel<D, KG><<<grid, kMmaThreads, smem, stream>>>(p, wl, km, vm);
+    launch_end(stream);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_attn_mma(const AttnParams &p, const WorkList &wl, int head_dim, int num_items,
+                            const void *k_cache, const void *v_cache, int64_t num_slots, cudaStream_t stream)
+{
+    if (num_items <= 0) return cudaSuccess;
+    CUtensorMap km, vm;
+    const bool sw = head_dim != 48;
+    const int box = sw ? 64 : head_dim;
+    cudaError_t e = make_pool_tmap(&km, k_cache, num_slots, p.hkv, head_dim, box, sw);
+    if (e == cudaSuccess) e = make_pool_tmap(&vm, v_cache, num_slots, p.hkv, head_dim, box, sw);
+    if (e != cudaSuccess) return e;
+    const bool dec = wl.mode == kModeDecode;
+    switch (head_dim) {
+    case 48: return dec ? launch_mma_dk<48, 4>(p, wl, num_items, km, vm, stream)
+                        : launch_mma_dk<48, 1>(p, wl, num_items, km, vm, stream);
+    case 64: return dec ? launch_mma_dk<64, 4>(p, wl, num_items, km, vm, stream)
+                        : launch_mma_dk<64, 1>(p, wl, num_items, km, vm, stream);
+    case 128: return dec ? launch_mma_dk<128, 4>(p, wl, num_items, km, vm, stream)
+                         : launch_mma_dk<128, 1>(p, wl, num_items, km, vm, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+int mma_prefill_rows() { return 16 * kConsumerWarps; }
+
+}  // namespace pkv

@@ -97,6 +97,12 @@ cudaError_t launch_kv_write(const void *k, const void *v, void *k_cache, void *v
 cudaError_t launch_attn_fma(const AttnParams &p, const WorkList &wl, int head_dim, int rows,
                             int num_items, cudaStream_t stream);
 
+// TMA-staged attention with warp-level MMA (decode-class: 4 key groups per
+// CTA; prefill-class: 4 row tiles of 16 per CTA).
+cudaError_t launch_attn_mma(const AttnParams &p, const WorkList &wl, int head_dim, int num_items,
+                            const void *k_cache, const void *v_cache, int64_t num_slots, cudaStream_t stream);
+int mma_prefill_rows();
+
 // Merge split-KV partials of the split requests in `wl` into bf16 output.
 cudaError_t launch_attn_combine(const AttnParams &p, const WorkList &wl, int head_dim,
                                 int max_rows_per_req, cudaStream_t stream);
@@ -108,7 +114,9 @@ enum KernelId : int {
     kAttnFmaPrefill = 2,
     kAttnCombine = 3,
     kAttnTcPrefill = 4,
-    kNumKernelIds = 5
+    kAttnMmaDecode = 5,
+    kAttnMmaPrefill = 6,
+    kNumKernelIds = 7
 };
 
 // Call around every kernel launch: counts it and, while profiling is on,

@@ -131,6 +131,8 @@ const char *pkv_kernel_name(int32_t kernel_id)
     case kAttnFmaPrefill: return "attn_fma_prefill";
     case kAttnCombine: return "attn_split_combine";
     case kAttnTcPrefill: return "attn_tc_prefill";
+    case kAttnMmaDecode: return "attn_mma_decode";
+    case kAttnMmaPrefill: return "attn_mma_prefill";
     }
     return "unknown";
 }
@@ -290,8 +292,9 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
     // ---- split size for decode-class requests
     const int sms = num_sms();
     int split = env_int("PKV_SPLIT_TOKENS", 0);
+    const bool use_fma = env_int("PKV_ATTN_CUDA_CORE", 0) != 0;    // CUDA-core kernels instead of the staged MMA ones
     if (split <= 0) {
-        int64_t target_ctas = (int64_t)sms * 8;
+        int64_t target_ctas = (int64_t)sms * (use_fma ? 8 : 16);
         int64_t s = (dec_keys * hkv + target_ctas - 1) / (target_ctas > 0 ? target_ctas : 1);
         if (s < kMinSplit) s = kMinSplit;
         split = (int)((s + 127) / 128 * 128);
@@ -314,6 +317,7 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
         split *= 2;
     }
 
+    const int64_t num_slots = (int64_t)num_blocks_total * bs;
     char *ws = static_cast<char *>(workspace);
     AttnParams p;
     p.out = static_cast<__nv_bfloat16 *>(out);
@@ -372,13 +376,14 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
             if (sl_h[r] > 0 && t * g > rows) rows = t * g;
         }
         wl.item_off[wl.n] = items;
-        cudaError_t e = launch_attn_fma(p, wl, d, rows, items, stream);
+        cudaError_t e = use_fma ? launch_attn_fma(p, wl, d, rows, items, stream)
+                                : launch_attn_mma(p, wl, d, items, k_cache, v_cache, num_slots, stream);
         if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
     }
     if (part_cursor > (size_t)INT32_MAX) return PKV_ERR_WORKSPACE;
 
     // ---- prefill-class launches
-    const int tile = kDecodeRows / g;
+    const int tile = use_fma ? kDecodeRows / g : (mma_prefill_rows() / g > 0 ? mma_prefill_rows() / g : 1);
     for (size_t c0 = 0; c0 < pre.size(); c0 += kPlanMax) {
         WorkList wl;
         memset(&wl, 0, sizeof wl);
@@ -397,7 +402,8 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
             items += (t + tile - 1) / tile;
         }
         wl.item_off[wl.n] = items;
-        cudaError_t e = launch_attn_fma(p, wl, d, kDecodeRows, items, stream);
+        cudaError_t e = use_fma ? launch_attn_fma(p, wl, d, kDecodeRows, items, stream)
+                                : launch_attn_mma(p, wl, d, items, k_cache, v_cache, num_slots, stream);
         if (e != cudaSuccess) return cuda_fail(e, "prefill attention launch");
     }
 

@@ -76,6 +76,23 @@ def test_random_mixes_full_parity(case):
     assert_close(dev.out, oracle_full(ref), f"random {seed}")
 
 
+@pytest.mark.parametrize("case", [RANDOM_CASES[1], RANDOM_CASES[2], RANDOM_CASES[5]], ids=["d64", "d128", "g8"])
+def test_cuda_core_kernels_full_parity(case, monkeypatch):
+    """The CUDA-core (FMA) kernels, selected with PKV_ATTN_CUDA_CORE=1."""
+    monkeypatch.setenv("PKV_ATTN_CUDA_CORE", "1")
+    seed, reqs, ctx, new, hq, hkv, d, pad = case
+    spec = random_spec(seed, reqs, ctx, new, hq, hkv, d, pad_rows=pad)
+    b = make_batch(spec, device="cpu")
+    dev = DeviceStep(b)
+    pkv.profile_start(16)
+    dev.step()
+    names = {n for n, _ in pkv.profile_stop()}
+    assert "attn_fma_decode" in names or "attn_fma_prefill" in names
+    ref = cpu_copy(b)
+    oracle_write(ref)
+    assert_close(dev.out, oracle_full(ref), f"cuda-core {seed}")
+
+
 @pytest.mark.parametrize("split", [256, 512, 4096])
 def test_forced_split_sizes(split, monkeypatch):
     monkeypatch.setenv("PKV_SPLIT_TOKENS", str(split))
