@@ -396,6 +396,22 @@ cudaError_t make_pool_tmap(CUtensorMap *map, const void *pool, int64_t num_slots
     return res == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Tensor map of q [tokens][Hq][D] with a box of one KV head's g query heads
+// x 128/g tokens x 64 columns (128 rows of the MMA tile), 128-byte swizzle.
+cudaError_t make_q_tmap(CUtensorMap *map, const void *q, int num_tokens, int hq, int d, int g)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)hq, (cuuint64_t)num_tokens};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)hq * d * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)g, (cuuint32_t)(128 / g)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return res == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int D, int KG>
 static cudaError_t launch_mma_dk(const AttnParams &p, const WorkList &wl, int num_items, const CUtensorMap &km,
                                  const CUtensorMap &vm, cudaStream_t stream)

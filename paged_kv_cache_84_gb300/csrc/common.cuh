@@ -103,6 +103,12 @@ cudaError_t launch_attn_mma(const AttnParams &p, const WorkList &wl, int head_di
                             const void *k_cache, const void *v_cache, int64_t num_slots, cudaStream_t stream);
 int mma_prefill_rows();
 
+// tcgen05 prefill tiles of 128 query rows (head_dim 128, g dividing 128).
+bool tc_prefill_supported(int head_dim, int group);
+int tc_prefill_rows();
+cudaError_t launch_attn_tc(const AttnParams &p, const WorkList &wl, int num_items, const void *q, int num_tokens,
+                           const void *k_cache, const void *v_cache, int64_t num_slots, cudaStream_t stream);
+
 // Merge split-KV partials of the split requests in `wl` into bf16 output.
 cudaError_t launch_attn_combine(const AttnParams &p, const WorkList &wl, int head_dim,
                                 int max_rows_per_req, cudaStream_t stream);

@@ -11,6 +11,7 @@
 // Each class goes to its kernel with the work list in the kernel
 // parameters, so nothing is copied to the device and nothing waits.
 #include <atomic>
+#include <climits>
 #include <cmath>
 #include <mutex>
 #include <cstdio>
@@ -86,11 +87,16 @@ constexpr int kMaxSplits = 64;        // most splits of one request
 constexpr size_t kErrBytes = 256;     // device error word area at the workspace start
 
 // Kernel class of request r (host rule shared by the planner and pkv_plan_request_kernels).
-static int request_class(int32_t t, int32_t L, int32_t g)
+static int env_int(const char *name, int dflt);
+
+static int request_class(int32_t t, int32_t L, int32_t g, int32_t d)
 {
     if (t == 0) return PKV_CLASS_NONE;
     if (L == 0) return PKV_CLASS_PADDING;
     if (t * g <= kDecodeRows) return PKV_CLASS_DECODE;
+    if (tc_prefill_supported(d, g) && t * g >= tc_prefill_rows() && !env_int("PKV_ATTN_CUDA_CORE", 0) &&
+        !env_int("PKV_DISABLE_TCGEN05", 0))
+        return PKV_CLASS_PREFILL_TENSOR;
     return PKV_CLASS_PREFILL_CUDA_CORE;
 }
 
@@ -217,7 +223,7 @@ pkv_status pkv_plan_request_kernels(const int32_t *qsl_h, const int32_t *sl_h, i
     if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads || head_dim <= 0)
         return PKV_ERR_INVALID_ARG;
     const int32_t g = num_q_heads / num_kv_heads;
-    for (int r = 0; r < num_reqs; r++) class_out[r] = request_class(qsl_h[r + 1] - qsl_h[r], sl_h[r], g);
+    for (int r = 0; r < num_reqs; r++) class_out[r] = request_class(qsl_h[r + 1] - qsl_h[r], sl_h[r], g, head_dim);
     return PKV_OK;
 }
 
@@ -277,17 +283,20 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
         return PKV_ERR_UNSUPPORTED;
 
     // ---- classify
-    std::vector<int32_t> dec, pre;
+    std::vector<int32_t> dec, pre, tcp;
     int64_t dec_keys = 0;
     for (int r = 0; r < num_reqs; r++) {
         int32_t t = qsl_h[r + 1] - qsl_h[r], L = sl_h[r];
-        switch (request_class(t, L, g)) {
+        switch (request_class(t, L, g, d)) {
         case PKV_CLASS_PADDING:
         case PKV_CLASS_DECODE: dec.push_back(r); dec_keys += L; break;
         case PKV_CLASS_PREFILL_CUDA_CORE: pre.push_back(r); break;
+        case PKV_CLASS_PREFILL_TENSOR: tcp.push_back(r); break;
         default: break;                                         // no rows at all
         }
     }
+    if (!tcp.empty() && ((int64_t)num_blocks_total * bs >= INT32_MAX || num_tokens >= INT32_MAX / 2))
+        return PKV_ERR_UNSUPPORTED;
 
     // ---- split size for decode-class requests
     const int sms = num_sms();
@@ -381,6 +390,28 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
         if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
     }
     if (part_cursor > (size_t)INT32_MAX) return PKV_ERR_WORKSPACE;
+
+    // ---- tensor-core prefill launches (first: the longest work)
+    for (size_t c0 = 0; c0 < tcp.size(); c0 += kPlanMax) {
+        WorkList wl;
+        memset(&wl, 0, sizeof wl);
+        wl.mode = kModePrefill;
+        wl.tile_tokens = tc_prefill_rows() / g;
+        int items = 0;
+        size_t c1 = c0 + kPlanMax < tcp.size() ? c0 + kPlanMax : tcp.size();
+        for (size_t x = c0; x < c1; x++) {
+            int32_t r = tcp[x];
+            int32_t t = qsl_h[r + 1] - qsl_h[r];
+            int li = wl.n++;
+            wl.req[li] = r;
+            wl.item_off[li] = items;
+            wl.part_off[li] = -1;
+            items += (t + wl.tile_tokens - 1) / wl.tile_tokens;
+        }
+        wl.item_off[wl.n] = items;
+        cudaError_t e = launch_attn_tc(p, wl, items, q, num_tokens, k_cache, v_cache, num_slots, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "tensor-core prefill launch");
+    }
 
     // ---- prefill-class launches
     const int tile = use_fma ? kDecodeRows / g : (mma_prefill_rows() / g > 0 ? mma_prefill_rows() / g : 1);

@@ -59,6 +59,9 @@ RANDOM_CASES = [
     (5, 4, 4100, 300, 64, 8, 128, 0),
     (6, 16, 600, 1, 32, 8, 128, 0),
     (7, 3, 33, 33, 4, 4, 48, 1),
+    (8, 4, 700, 260, 8, 8, 128, 0),       # g = 1 tensor-core tiles
+    (9, 3, 500, 200, 16, 1, 128, 1),      # g = 16
+    (10, 5, 900, 300, 16, 8, 128, 0),     # g = 2
 ]
 
 
@@ -91,6 +94,27 @@ def test_cuda_core_kernels_full_parity(case, monkeypatch):
     ref = cpu_copy(b)
     oracle_write(ref)
     assert_close(dev.out, oracle_full(ref), f"cuda-core {seed}")
+
+
+@pytest.mark.parametrize("disable_tc", [False, True])
+def test_long_chunks_tensor_core_path(disable_tc, monkeypatch):
+    """Prefill chunks of 128+ rows go to the tcgen05 kernel; the same batch with
+    it disabled runs on the warp-level MMA kernel.  Both match the oracle."""
+    if disable_tc:
+        monkeypatch.setenv("PKV_DISABLE_TCGEN05", "1")
+    reqs = [Req(1000, 300, list(range(0, 82))), Req(0, 257, list(range(82, 99))), Req(77, 1, list(range(99, 104))),
+            Req(5000, 64, list(range(104, 421)))]
+    spec = Spec("chunks", reqs, 32, 8, 128, 16, 430, 1 / math.sqrt(128), 17)
+    b = make_batch(spec, device="cpu")
+    dev = DeviceStep(b)
+    pkv.profile_start(16)
+    dev.step()
+    names = {n for n, _ in pkv.profile_stop()}
+    assert ("attn_tc_prefill" in names) != disable_tc
+    ref = cpu_copy(b)
+    oracle_write(ref)
+    assert_close(dev.out, oracle_full(ref), "chunks")
+    assert pkv.read_device_error(dev.ws) == 0
 
 
 @pytest.mark.parametrize("split", [256, 512, 4096])
