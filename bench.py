@@ -356,12 +356,20 @@ def time_workload(pkv, cfg, steps, warmup, device, peaks, dist=None, use_graph=T
         elapsed_ms = float(t.item())
     ms_per_step = elapsed_ms / steps
 
-    # ---- per-kernel durations: eager steps with events around every launch
+    # ---- per-kernel durations: eager steps with events around every launch.
+    # Kernels that overlap on a side stream in the timed region run one after
+    # another here, so that each event pair times one kernel alone.
     prof_steps = max(3, min(steps, 50))
+    saved = os.environ.get("PKV_NO_OVERLAP")
+    os.environ["PKV_NO_OVERLAP"] = "1"
     pkv.profile_start(prof_steps * launches_per_step + 16)
     for i in range(prof_steps):
         copies[i % len(copies)].run()
     recs = pkv.profile_stop()
+    if saved is None:
+        os.environ.pop("PKV_NO_OVERLAP", None)
+    else:
+        os.environ["PKV_NO_OVERLAP"] = saved
     kern = {}
     for name, ms in recs:
         k = kern.setdefault(name, {"launches": 0, "total_ms": 0.0})

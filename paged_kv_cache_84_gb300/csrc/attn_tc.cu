@@ -1,29 +1,32 @@
 // Ragged paged attention for prefill chunks on the 5th-generation tensor
 // cores (tcgen05, accumulators in tensor memory), head_dim 128.
 //
-// One CTA = (listed request, KV head, tile of 128 query rows).  A row is a
-// (token, query head) pair of the KV head's group: 128/g consecutive new
-// tokens x g heads (the vllm-lite README's grouped-query fold, so a K/V tile
-// feeds all g heads in one MMA).  Query i of a request with t new tokens and
-// context L sits at position L - t + i and sees keys 0 .. that position
-// ("31. Engine v2", "Attention over the pool").  Keys are taken in tiles of
-// 128 = 8 paged blocks, each block's 16-row K and V slices of this KV head
-// copied by TMA straight from the pool through the block table (key j lives
-// in block table[j / 16], row j % 16): the paged layout is read in place.
+// One CTA = (listed request, KV head, pair of 128-row query tiles).  A row
+// is a (token, query head) pair of the KV head's group: 128/g consecutive
+// new tokens x g heads per tile (the vllm-lite README's grouped-query fold,
+// so one K/V tile feeds all g heads).  Query i of a request with t new
+// tokens and context L sits at position L - t + i and sees keys 0 .. that
+// position ("31. Engine v2", "Attention over the pool").  Keys come in
+// tiles of 128 = 8 paged blocks; each block's 16-row K and V slices of this
+// KV head are copied by TMA straight from the pool through the block table
+// (key j lives in block table[j / 16], row j % 16).
 //
-// Warp roles (256 threads):
-//   warp 0      TMA producer: Q once, then K and V tiles into a 2-stage ring;
-//   warp 1      MMA issuer (one thread): S = Q K^T into a double-buffered
-//               TMEM tile, then O += P V into a TMEM accumulator;
-//   warps 4..7  softmax, one thread per row (TMEM lane): S row from TMEM,
-//               causal mask, online softmax in the exp2 domain with the
-//               running max only moved (and O rescaled in TMEM) when it
-//               grows by more than 2^8, P written to shared memory in the
-//               MMA's operand layout; at the end O / l to bf16 output.
-// The MMA for S(j+1) runs while the softmax works on S(j).
-//
-// All shared-memory operands use the 128-byte swizzle: Q, K and P are
-// K-major ([rows][64 columns] sub-tiles), V is MN-major ([keys][64 dims]).
+// Warp roles (384 threads):
+//   warp 0      TMA producer: both Q tiles once, then K and V tiles into two
+//               2-stage rings (a K stage is refilled once both S MMAs that
+//               read it are done, a V stage once both PV MMAs are done);
+//   warp 1      MMA issuer (one thread) and TMEM owner; per key tile it
+//               issues PV_a(j-1), S_a(j), PV_b(j-1), S_b(j), so the tensor
+//               core always has the other tile's work while a softmax runs;
+//   warps 4..7  softmax of tile a, warps 8..11 softmax of tile b, one row per
+//               thread (= TMEM lane): two passes over the S row in TMEM (row
+//               max, then exp2 in the log2 domain), P written back as bf16
+//               pairs over the first half of the S columns, where the PV MMA
+//               reads it as its A operand.  The running max only moves (and O
+//               is rescaled in TMEM) when it grows by more than 2^8.
+// TMEM: S_a [0,128), S_b [128,256), O_a [256,384), O_b [384,512).
+// Shared memory (128-byte swizzle): Q_a, Q_b, K and V tiles as [128][64]
+// sub-tiles, K-major for Q and K, MN-major for V.
 #include <climits>
 #include <mutex>
 
@@ -32,39 +35,123 @@
 
 namespace pkv {
 
-constexpr int kTcThreads = 256;
-constexpr int kTcRows = 128;          // query rows per CTA (MMA M)
+constexpr int kTcThreads = 384;
+constexpr int kTcRows = 128;          // query rows per tile (MMA M)
 constexpr int kTcKeys = 128;          // keys per tile (MMA N of S, K of PV)
 constexpr int kTcD = 128;
 constexpr int kSub = 16384;           // one [128][64] bf16 sub-tile
 constexpr int kTile = 2 * kSub;       // [128][128]
-constexpr int kQOff = 0;
-constexpr int kKOff = kQOff + kTile;                  // 2 stages
+constexpr int kQOff = 0;                              // Q_a, Q_b
+constexpr int kKOff = kQOff + 2 * kTile;              // 2 stages
 constexpr int kVOff = kKOff + 2 * kTile;              // 2 stages
-constexpr int kPOff = kVOff + 2 * kTile;
-constexpr int kBarOff = kPOff + kTile;
+constexpr int kBarOff = kVOff + 2 * kTile;
 constexpr int kTcSmem = 1024 + kBarOff + 256;
-constexpr uint32_t kTmemCols = 512;   // S0 [0,128), S1 [128,256), O [256,384)
+constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;  // move the running max only when it grows by more than this
 
 enum TcBar {
     kBarQ = 0,
     kBarK0 = 1, kBarK1 = 2,
     kBarV0 = 3, kBarV1 = 4,
-    kBarKVEmpty0 = 5, kBarKVEmpty1 = 6,
-    kBarS0 = 7, kBarS1 = 8,
-    kBarSFree0 = 9, kBarSFree1 = 10,
-    kBarP = 11,
-    kBarO = 12,
-    kBarMmaDone = 13,
-    kNumTcBars = 14
+    kBarKEmpty0 = 5, kBarKEmpty1 = 6,
+    kBarVEmpty0 = 7, kBarVEmpty1 = 8,
+    kBarSA = 9, kBarSB = 10,          // S of tile a / b ready
+    kBarPA = 11, kBarPB = 12,         // P of tile a / b written (4 warps each)
+    kBarOA = 13, kBarOB = 14,         // PV of tile a / b done
+    kBarMmaDone = 15,
+    kNumTcBars = 16
 };
 
-// byte offset of 16-byte chunk c (8 columns) of row `row` in a [128][128]
-// K-major tile made of two swizzled [128][64] sub-tiles
-__device__ __forceinline__ uint32_t kmaj_off(int row, int c)
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
 {
-    return (c >> 3) * kSub + (row >> 3) * 1024 + (row & 7) * 128 + (((c & 7) ^ (row & 7)) << 4);
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]: the A operand (P) read from tensor memory.
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Pass 1 of the softmax: max of the raw scores of this thread's S row (128
+// TMEM columns at ts); keys past qpos are masked when MASK.
+template <bool MASK>
+__device__ __forceinline__ float tc_row_max(uint32_t ts, int key0, int qpos)
+{
+    float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int c = 0; c < 4; c++) {
+        uint32_t v[32];
+        tmem_ld32(ts + c * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+            float s0 = __uint_as_float(v[k]), s1 = __uint_as_float(v[k + 1]);
+            if (MASK) {
+                if (key0 + c * 32 + k > qpos) s0 = -INFINITY;
+                if (key0 + c * 32 + k + 1 > qpos) s1 = -INFINITY;
+            }
+            m[(k >> 1) & 3] = max3f(m[(k >> 1) & 3], s0, s1);
+        }
+    }
+    return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+}
+
+// Pass 2: P = 2^(s * sl2 - ms) as bf16 pairs written over the first 64 S
+// columns (each 16-column chunk goes over columns already read); returns
+// this row's sum of P.
+template <bool MASK>
+__device__ __forceinline__ float tc_row_exp(uint32_t ts, int key0, int qpos, float sl2, float ms)
+{
+    const uint64_t scale2 = f2_pack(sl2, sl2), neg2 = f2_pack(-ms, -ms);
+    uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+    for (int c = 0; c < 8; c++) {
+        uint32_t v[16];
+        tmem_ld16(ts + c * 16, v);
+        tmem_ld_wait();
+        uint32_t pw[8];
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            float s0 = __uint_as_float(v[2 * k]), s1 = __uint_as_float(v[2 * k + 1]);
+            if (MASK) {
+                if (key0 + c * 16 + 2 * k > qpos) s0 = -INFINITY;
+                if (key0 + c * 16 + 2 * k + 1 > qpos) s1 = -INFINITY;
+            }
+            float t0, t1;
+            f2_unpack(f2_fma(f2_pack(s0, s1), scale2, neg2), t0, t1);
+            const float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
+            acc[k & 3] = f2_add(acc[k & 3], f2_pack(p0, p1));
+            pw[k] = pack_bf16x2(p0, p1);
+        }
+        tmem_st8(ts + c * 8, pw);
+    }
+    tmem_st_wait();
+    float sum = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+        float a, b;
+        f2_unpack(acc[q], a, b);
+        sum += a + b;
+    }
+    return sum;
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, const __grid_constant__ WorkList wl,
@@ -81,27 +168,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, co
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sp + kBarOff + 8 * kNumTcBars);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int kh = blockIdx.y;
-    const int li = find_listed(wl, blockIdx.x);
+    const int kh = blockIdx.x;                                     // all KV heads of an item are adjacent
+    const int li = find_listed(wl, blockIdx.y);
     const int r = wl.req[li];
     const int b = p.qsl[r], t = p.qsl[r + 1] - b, L = p.seq_lens[r];
     const int g = p.group;
-    const int tile_tokens = wl.tile_tokens;                       // 128 / g
-    const int ntiles = (t + tile_tokens - 1) / tile_tokens;
-    const int tile = ntiles - 1 - (blockIdx.x - wl.item_off[li]);   // longest tiles first
-    const int i0 = tile * tile_tokens;
-    const int ntok = min(tile_tokens, t - i0);
-    const int nr = ntok * g;
-    const int k_end = L - t + i0 + ntok;                           // one past the last position
+    const int tt = wl.tile_tokens;                                 // tokens per tile: 128 / g
+    const int npairs = (t + 2 * tt - 1) / (2 * tt);
+    const int pair = npairs - 1 - (blockIdx.y - wl.item_off[li]);  // longest pairs first
+    const int i0 = pair * 2 * tt;                                  // first token of tile a
+    const int ntok_a = min(tt, t - i0);
+    const int ntok_b = max(0, min(tt, t - i0 - tt));
+    const bool has_b = ntok_b > 0;
+    const int k_end = L - t + i0 + ntok_a + ntok_b;                // one past the last position
     const int nkt = (k_end + kTcKeys - 1) / kTcKeys;               // key tiles
     const int nblk = (k_end + 15) >> 4;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kNumTcBars; i++) {
-            uint32_t cnt = 1;
-            if (i == kBarSFree0 || i == kBarSFree1 || i == kBarP) cnt = 4;
-            mbar_init(bar(i), cnt);
-        }
+        for (int i = 0; i < kNumTcBars; i++) mbar_init(bar(i), (i == kBarPA || i == kBarPB) ? 4u : 1u);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -119,188 +203,184 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, co
             prefetch_tmap(&qmap);
             prefetch_tmap(&kmap);
             prefetch_tmap(&vmap);
-            mbar_arrive_expect_tx(bar(kBarQ), kTile);
+            mbar_arrive_expect_tx(bar(kBarQ), has_b ? 2 * kTile : kTile);
             tma_load_3d(sb + kQOff, &qmap, bar(kBarQ), 0, kh * g, b + i0);
             tma_load_3d(sb + kQOff + kSub, &qmap, bar(kBarQ), 64, kh * g, b + i0);
+            if (has_b) {
+                tma_load_3d(sb + kQOff + kTile, &qmap, bar(kBarQ), 0, kh * g, b + i0 + tt);
+                tma_load_3d(sb + kQOff + kTile + kSub, &qmap, bar(kBarQ), 64, kh * g, b + i0 + tt);
+            }
         }
         const int32_t *bt = p.block_table + (size_t)r * p.bt_stride;
-        int ids = 0, issued = 0;
+        int ids = 0, issued_k = 0, issued_v = 0;
         for (int j = 0; j < nkt; j++) {
             const int st = j & 1;
             if ((j & 3) == 0) {                                    // 32 block ids = 4 key tiles
                 const int jb = j * 8 + lane;
                 ids = jb < nblk ? __ldg(bt + jb) : INT_MIN;
             }
+            // slot rows of this tile's 8 blocks (beyond the range: past the pool, TMA fills zeros)
+            int rows8[8];
+#pragma unroll
+            for (int bi = 0; bi < 8; bi++) {
+                const int blk = __shfl_sync(0xffffffffu, ids, ((j & 3) << 3) + bi);
+                rows8[bi] = (int)num_slots;
+                if (blk != INT_MIN) {
+                    if (blk < 0 || blk >= p.nb_total) {
+                        if (lane == 0) atomicOr(p.err, 2u);
+                    } else {
+                        rows8[bi] = blk * 16;
+                    }
+                }
+            }
             bool ok = true;
-            if (j >= 2) ok = mbar_wait(bar(kBarKVEmpty0 + st), ((j >> 1) - 1) & 1, p.err);
+            if (j >= 2) ok = mbar_wait(bar(kBarKEmpty0 + st), ((j >> 1) - 1) & 1, p.err);
             if (!__all_sync(0xffffffffu, ok)) break;
-            issued = j + 1;
+            issued_k = j + 1;
             if (lane == 0) {
                 mbar_arrive_expect_tx(bar(kBarK0 + st), kTile);
-                mbar_arrive_expect_tx(bar(kBarV0 + st), kTile);
+                const uint32_t kd = sb + kKOff + st * kTile;
+#pragma unroll
+                for (int bi = 0; bi < 8; bi++) {
+                    tma_load_3d(kd + bi * 2048, &kmap, bar(kBarK0 + st), 0, kh, rows8[bi]);
+                    tma_load_3d(kd + kSub + bi * 2048, &kmap, bar(kBarK0 + st), 64, kh, rows8[bi]);
+                }
             }
-            for (int bi = 0; bi < 8; bi++) {
-                int blk = __shfl_sync(0xffffffffu, ids, ((j & 3) << 3) + bi);
-                if (lane == 0) {
-                    int row = (int)num_slots;                      // beyond the pool: TMA fills zeros
-                    if (blk != INT_MIN) {                          // a block of the key range
-                        if (blk < 0 || blk >= p.nb_total) atomicOr(p.err, 2u);
-                        else row = blk * 16;
-                    }
-                    const uint32_t kd = sb + kKOff + st * kTile + bi * 2048;
-                    const uint32_t vd = sb + kVOff + st * kTile + bi * 2048;
-                    tma_load_3d(kd, &kmap, bar(kBarK0 + st), 0, kh, row);
-                    tma_load_3d(kd + kSub, &kmap, bar(kBarK0 + st), 64, kh, row);
-                    tma_load_3d(vd, &vmap, bar(kBarV0 + st), 0, kh, row);
-                    tma_load_3d(vd + kSub, &vmap, bar(kBarV0 + st), 64, kh, row);
+            if (j >= 2) ok = mbar_wait(bar(kBarVEmpty0 + st), ((j >> 1) - 1) & 1, p.err);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            issued_v = j + 1;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar(kBarV0 + st), kTile);
+                const uint32_t vd = sb + kVOff + st * kTile;
+#pragma unroll
+                for (int bi = 0; bi < 8; bi++) {
+                    tma_load_3d(vd + bi * 2048, &vmap, bar(kBarV0 + st), 0, kh, rows8[bi]);
+                    tma_load_3d(vd + kSub + bi * 2048, &vmap, bar(kBarV0 + st), 64, kh, rows8[bi]);
                 }
             }
             __syncwarp();
         }
-        if (issued < nkt && lane == 0) {                           // a wait gave up: drain own copies
-            for (int j = issued > 2 ? issued - 2 : 0; j < issued; j++) {
+        if ((issued_k < nkt || issued_v < nkt) && lane == 0) {     // a wait gave up: drain own copies
+            mbar_wait(bar(kBarQ), 0, p.err);
+            for (int j = issued_k > 2 ? issued_k - 2 : 0; j < issued_k; j++)
                 mbar_wait(bar(kBarK0 + (j & 1)), (j >> 1) & 1, p.err);
+            for (int j = issued_v > 2 ? issued_v - 2 : 0; j < issued_v; j++)
                 mbar_wait(bar(kBarV0 + (j & 1)), (j >> 1) & 1, p.err);
-            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16(kTcRows, kTcKeys, false);
             constexpr uint32_t idO = idesc_bf16(kTcRows, kTcD, true);
-            bool ok = mbar_wait(bar(kBarQ), 0, p.err);
-            auto issue_pv = [&](int i) -> bool {
-                if (!mbar_wait(bar(kBarP), i & 1, p.err)) return false;
-                if (!mbar_wait(bar(kBarV0 + (i & 1)), (i >> 1) & 1, p.err)) return false;
+            const int ntile = has_b ? 2 : 1;
+            auto issue_s = [&](int x, int j) {                     // S_x(j) = Q_x K_j^T
+                const uint32_t kbase = sb + kKOff + (j & 1) * kTile;
+                const uint32_t qbase = sb + kQOff + x * kTile;
+#pragma unroll
+                for (int kk = 0; kk < 8; kk++) {
+                    const uint64_t ad = sdesc_sw128(qbase + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(kbase + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024);
+                    tc_mma(tmem + x * 128, ad, bd, idS, kk > 0 ? 1u : 0u);
+                }
+                tc_commit(bar(kBarSA + x));
+                if (x == ntile - 1) tc_commit(bar(kBarKEmpty0 + (j & 1)));
+            };
+            auto issue_pv = [&](int x, int i) -> bool {            // O_x += P_x(i) V_i
+                if (!mbar_wait(bar(kBarPA + x), i & 1, p.err)) return false;
+                if (x == 0 && !mbar_wait(bar(kBarV0 + (i & 1)), (i >> 1) & 1, p.err)) return false;
                 tc_fence_after();
                 const uint32_t vbase = sb + kVOff + (i & 1) * kTile;
 #pragma unroll
                 for (int kk = 0; kk < 8; kk++) {
-                    const uint64_t ad = sdesc_sw128(sb + kPOff + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024);
                     const uint64_t bd = sdesc_sw128(vbase + kk * 2048, kSub, 1024);
-                    tc_mma(tmem + 256, ad, bd, idO, (i > 0 || kk > 0) ? 1u : 0u);
+                    tc_mma_ts(tmem + 256 + x * 128, tmem + x * 128 + kk * 8, bd, idO, (i > 0 || kk > 0) ? 1u : 0u);
                 }
-                tc_commit(bar(kBarO));
-                tc_commit(bar(kBarKVEmpty0 + (i & 1)));
+                tc_commit(bar(kBarOA + x));
+                if (x == ntile - 1) tc_commit(bar(kBarVEmpty0 + (i & 1)));
                 return true;
             };
+            bool ok = mbar_wait(bar(kBarQ), 0, p.err);
             for (int j = 0; j < nkt && ok; j++) {
-                const int s = j & 1;
-                ok = mbar_wait(bar(kBarK0 + s), (j >> 1) & 1, p.err);
-                if (ok && j >= 2) ok = mbar_wait(bar(kBarSFree0 + s), ((j >> 1) - 1) & 1, p.err);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t kbase = sb + kKOff + s * kTile;
-#pragma unroll
-                for (int kk = 0; kk < 8; kk++) {
-                    const uint64_t ad = sdesc_sw128(sb + kQOff + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024);
-                    const uint64_t bd = sdesc_sw128(kbase + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024);
-                    tc_mma(tmem + s * 128, ad, bd, idS, kk > 0 ? 1u : 0u);
+                for (int x = 0; x < ntile && ok; x++) {
+                    if (j >= 1) ok = issue_pv(x, j - 1);         // reads P_x(j-1) before S_x(j) overwrites it
+                    if (ok && x == 0) {
+                        ok = mbar_wait(bar(kBarK0 + (j & 1)), (j >> 1) & 1, p.err);
+                        tc_fence_after();
+                    }
+                    if (ok) issue_s(x, j);
                 }
-                tc_commit(bar(kBarS0 + s));
-                if (j >= 1) ok = issue_pv(j - 1);
             }
-            if (ok) issue_pv(nkt - 1);
+            for (int x = 0; x < ntile && ok; x++) ok = issue_pv(x, nkt - 1);
             // every MMA this thread issued has finished before TMEM is released
             tc_commit(bar(kBarMmaDone));
             mbar_wait(bar(kBarMmaDone), 0, p.err);
         }
         __syncwarp();
-    } else if (warp >= 4) {
+    } else if (warp >= 4 && (warp < 8 || has_b)) {
         // ------------------------------------------------------------ softmax, one row per thread
-        const int row = threadIdx.x - 128;
+        const int x = warp >= 8 ? 1 : 0;                           // tile a or b
+        const int row = threadIdx.x - (x ? 256 : 128);
+        const int ntok_x = x ? ntok_b : ntok_a;
+        const int nr = ntok_x * g;
+        const int tok0 = i0 + x * tt;                              // first token of this tile
         const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-        const int qpos = row < nr ? L - t + i0 + row / g : -1;
+        const uint32_t ts = tl + x * 128;                          // S_x (and P_x) columns
+        const uint32_t to = tl + 256 + x * 128;                    // O_x columns
+        const int qpos = row < nr ? L - t + tok0 + row / g : -1;
         const float sl2 = p.scale_log2;
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < nkt; j++) {
-            const int s = j & 1;
-            ok = mbar_wait(bar(kBarS0 + s), (j >> 1) & 1, p.err);
+            ok = mbar_wait(bar(kBarSA + x), j & 1, p.err);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
-            float x[kTcKeys];
-#pragma unroll
-            for (int c = 0; c < 4; c++) {
-                uint32_t v[32];
-                tmem_ld32(tl + s * 128 + c * 32, v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int k = 0; k < 32; k++) x[c * 32 + k] = __uint_as_float(v[k]);
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarSFree0 + s));
-
             const int key0 = j * kTcKeys;
-            float mt = -INFINITY;
-            if (key0 + kTcKeys - 1 <= qpos) {
-#pragma unroll
-                for (int k = 0; k < kTcKeys; k++) {
-                    x[k] *= sl2;
-                    mt = fmaxf(mt, x[k]);
-                }
+            // warp-uniform: does any row of this warp see masked keys in this tile?
+            const bool diag = __any_sync(0xffffffffu, key0 + kTcKeys - 1 > qpos);
+            const float mraw = diag ? tc_row_max<true>(ts, key0, qpos) : tc_row_max<false>(ts, key0, qpos);
+            const float mt = mraw * sl2;                            // in the exp2 domain (scale > 0)
+            if (j == 0) {
+                m_used = mt;
             } else {
-#pragma unroll
-                for (int k = 0; k < kTcKeys; k++) {
-                    x[k] = (key0 + k <= qpos) ? x[k] * sl2 : -INFINITY;
-                    mt = fmaxf(mt, x[k]);
-                }
-            }
-            if (j > 0) {
-                // PV(j-1) has finished: O is stable and the P buffer is free
-                ok = mbar_wait(bar(kBarO), (j - 1) & 1, p.err);
-                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                tc_fence_after();
                 const bool need = mt > m_used + kRescaleLog2;
                 if (__any_sync(0xffffffffu, need)) {
+                    // move the running max: O_x must be stable, so wait for PV_x(j-1)
+                    ok = mbar_wait(bar(kBarOA + x), (j - 1) & 1, p.err);
+                    if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                    tc_fence_after();
                     const float alpha = need ? exp2f(m_used - mt) : 1.f;
                     if (need) {
                         l *= alpha;
                         m_used = mt;
                     }
-#pragma unroll
+#pragma unroll 1
                     for (int c = 0; c < 4; c++) {
-                        uint32_t v[32];
-                        tmem_ld32(tl + 256 + c * 32, v);
+                        uint32_t ov[32];
+                        tmem_ld32(to + c * 32, ov);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int k = 0; k < 32; k++) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
-                        tmem_st32(tl + 256 + c * 32, v);
+                        for (int k = 0; k < 32; k++) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * alpha);
+                        tmem_st32(to + c * 32, ov);
                     }
                     tmem_st_wait();
                 }
-            } else {
-                m_used = mt;
             }
+            // pass 2: P = 2^(s * scale * log2e - m) over the first 64 S columns
             const float ms = m_used == -INFINITY ? 0.f : m_used;
-            uint8_t *prow = sp + kPOff;
-#pragma unroll
-            for (int c = 0; c < 16; c++) {
-                uint32_t w4[4];
-#pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    const float p0 = exp2f(x[c * 8 + 2 * q] - ms);
-                    const float p1 = exp2f(x[c * 8 + 2 * q + 1] - ms);
-                    l += p0 + p1;
-                    w4[q] = pack_bf16x2(p0, p1);
-                }
-                *reinterpret_cast<uint4 *>(prow + kmaj_off(row, c)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-            }
-            fence_proxy_async_smem();
+            l += diag ? tc_row_exp<true>(ts, key0, qpos, sl2, ms) : tc_row_exp<false>(ts, key0, qpos, sl2, ms);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarP));
+            if (lane == 0) mbar_arrive(bar(kBarPA + x));
         }
-        if (ok) ok = mbar_wait(bar(kBarO), (nkt - 1) & 1, p.err);
+        if (ok) ok = mbar_wait(bar(kBarOA + x), (nkt - 1) & 1, p.err);
         if (__all_sync(0xffffffffu, ok)) {
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            const size_t orow = row < nr ? ((size_t)(b + i0 + row / g) * p.hq + kh * g + row % g) * kTcD : 0;
+            const size_t orow = row < nr ? ((size_t)(b + tok0 + row / g) * p.hq + kh * g + row % g) * kTcD : 0;
 #pragma unroll
             for (int c = 0; c < 4; c++) {
                 uint32_t v[32];
-                tmem_ld32(tl + 256 + c * 32, v);
+                tmem_ld32(to + c * 32, v);
                 tmem_ld_wait();
                 if (row < nr) {
                     uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow + c * 32);
@@ -350,7 +430,8 @@ cudaError_t launch_attn_tc(const AttnParams &p, const WorkList &wl, int num_item
     if (e == cudaSuccess) e = make_pool_tmap(&km, k_cache, num_slots, p.hkv, kTcD, 64, true);
     if (e == cudaSuccess) e = make_pool_tmap(&vm, v_cache, num_slots, p.hkv, kTcD, 64, true);
     if (e != cudaSuccess) return e;
-    dim3 grid(num_items, p.hkv);
+    if (num_items > 65535) return cudaErrorInvalidConfiguration;
+    dim3 grid(p.hkv, num_items);                   // items in launch order: the planner puts the longest first
     launch_begin(stream, kAttnTcPrefill);
     attn_tc_kernel<<<grid, kTcThreads, kTcSmem, stream>>>(p, wl, qm, km, vm, num_slots);
     launch_end(stream);

@@ -17,6 +17,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <algorithm>
 #include <vector>
 
 #include "pkv.h"
@@ -77,6 +78,35 @@ static int num_sms()
         cached[dev] = n;
     }
     return cached[dev];
+}
+
+// One non-blocking side stream and a fork/join event pair per device,
+// created on first use (host-side CUDA objects, no device memory).
+struct SideStream {
+    std::mutex mu;
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+static SideStream *side_stream()
+{
+    static SideStream sides[64];
+    static std::mutex init_mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    SideStream &s = sides[dev];
+    std::lock_guard<std::mutex> lock(init_mu);
+    if (!s.stream) {
+        cudaStream_t st;
+        cudaEvent_t a, b;
+        if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+        if (cudaEventCreateWithFlags(&a, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+        if (cudaEventCreateWithFlags(&b, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+        s.fork = a;
+        s.join = b;
+        s.stream = st;
+    }
+    return &s;
 }
 
 static bool aligned(const void *p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
@@ -297,6 +327,13 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
     }
     if (!tcp.empty() && ((int64_t)num_blocks_total * bs >= INT32_MAX || num_tokens >= INT32_MAX / 2))
         return PKV_ERR_UNSUPPORTED;
+    // heaviest tensor-core requests first (work ~ new tokens x context), so
+    // that the long tiles start in the first wave and short ones fill the tail
+    std::stable_sort(tcp.begin(), tcp.end(), [&](int32_t a, int32_t c) {
+        const int64_t wa = (int64_t)(qsl_h[a + 1] - qsl_h[a]) * sl_h[a];
+        const int64_t wc = (int64_t)(qsl_h[c + 1] - qsl_h[c]) * sl_h[c];
+        return wa > wc;
+    });
 
     // ---- split size for decode-class requests
     const int sms = num_sms();
@@ -354,6 +391,58 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
     p.part_o = reinterpret_cast<float *>(ws + kErrBytes);
     p.part_ml = reinterpret_cast<float2 *>(ws + kErrBytes + ((total_rows * d * 4 + 15) / 16) * 16);
 
+    // ---- decode-class work runs on a side stream, concurrently with the
+    // tensor-core prefill, when both are present: its CTAs fill the SMs that
+    // the prefill's last wave leaves idle.  Fork and join with events, so the
+    // caller's stream order (and CUDA-graph capture) is preserved.
+    cudaStream_t dstream = stream;
+    SideStream *side = nullptr;
+    const bool fork = !tcp.empty() && !dec.empty() && !env_int("PKV_NO_OVERLAP", 0);
+    if (fork) {
+        side = side_stream();
+        if (!side) return cuda_fail(cudaErrorUnknown, "side stream");
+        side->mu.lock();
+        cudaError_t e = cudaEventRecord(side->fork, stream);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
+        if (e != cudaSuccess) {
+            side->mu.unlock();
+            return cuda_fail(e, "fork");
+        }
+        dstream = side->stream;
+    }
+    auto join = [&]() -> cudaError_t {
+        if (!fork) return cudaSuccess;
+        cudaError_t e = cudaEventRecord(side->join, side->stream);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, side->join, 0);
+        side->mu.unlock();
+        return e;
+    };
+
+    // ---- tensor-core prefill launches, submitted first: the longest work
+    for (size_t c0 = 0; c0 < tcp.size(); c0 += kPlanMax) {
+        WorkList wl;
+        memset(&wl, 0, sizeof wl);
+        wl.mode = kModePrefill;
+        wl.tile_tokens = tc_prefill_rows() / g;
+        int items = 0;
+        size_t c1 = c0 + kPlanMax < tcp.size() ? c0 + kPlanMax : tcp.size();
+        for (size_t x = c0; x < c1; x++) {
+            int32_t r = tcp[x];
+            int32_t t = qsl_h[r + 1] - qsl_h[r];
+            int li = wl.n++;
+            wl.req[li] = r;
+            wl.item_off[li] = items;
+            wl.part_off[li] = -1;
+            items += (t + 2 * wl.tile_tokens - 1) / (2 * wl.tile_tokens);   // pairs of 128-row tiles
+        }
+        wl.item_off[wl.n] = items;
+        cudaError_t e = launch_attn_tc(p, wl, items, q, num_tokens, k_cache, v_cache, num_slots, stream);
+        if (e != cudaSuccess) {
+            join();
+            return cuda_fail(e, "tensor-core prefill launch");
+        }
+    }
+
     // ---- decode-class launches (chunks of kPlanMax requests)
     std::vector<int32_t> combine_reqs, combine_off;
     int combine_max_rows = 0;
@@ -385,32 +474,32 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
             if (sl_h[r] > 0 && t * g > rows) rows = t * g;
         }
         wl.item_off[wl.n] = items;
-        cudaError_t e = use_fma ? launch_attn_fma(p, wl, d, rows, items, stream)
-                                : launch_attn_mma(p, wl, d, items, k_cache, v_cache, num_slots, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
+        cudaError_t e = use_fma ? launch_attn_fma(p, wl, d, rows, items, dstream)
+                                : launch_attn_mma(p, wl, d, items, k_cache, v_cache, num_slots, dstream);
+        if (e != cudaSuccess) {
+            join();
+            return cuda_fail(e, "decode attention launch");
+        }
     }
-    if (part_cursor > (size_t)INT32_MAX) return PKV_ERR_WORKSPACE;
-
-    // ---- tensor-core prefill launches (first: the longest work)
-    for (size_t c0 = 0; c0 < tcp.size(); c0 += kPlanMax) {
+    // ---- combine split partials (same stream as the decode kernels)
+    for (size_t c0 = 0; c0 < combine_reqs.size(); c0 += kPlanMax) {
         WorkList wl;
         memset(&wl, 0, sizeof wl);
-        wl.mode = kModePrefill;
-        wl.tile_tokens = tc_prefill_rows() / g;
-        int items = 0;
-        size_t c1 = c0 + kPlanMax < tcp.size() ? c0 + kPlanMax : tcp.size();
+        wl.mode = kModeDecode;
+        wl.split_tokens = split;
+        size_t c1 = c0 + kPlanMax < combine_reqs.size() ? c0 + kPlanMax : combine_reqs.size();
         for (size_t x = c0; x < c1; x++) {
-            int32_t r = tcp[x];
-            int32_t t = qsl_h[r + 1] - qsl_h[r];
             int li = wl.n++;
-            wl.req[li] = r;
-            wl.item_off[li] = items;
-            wl.part_off[li] = -1;
-            items += (t + wl.tile_tokens - 1) / wl.tile_tokens;
+            wl.req[li] = combine_reqs[x];
+            wl.part_off[li] = combine_off[x];
+            wl.item_off[li] = li;
         }
-        wl.item_off[wl.n] = items;
-        cudaError_t e = launch_attn_tc(p, wl, items, q, num_tokens, k_cache, v_cache, num_slots, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "tensor-core prefill launch");
+        wl.item_off[wl.n] = wl.n;
+        cudaError_t e = launch_attn_combine(p, wl, d, combine_max_rows, dstream);
+        if (e != cudaSuccess) {
+            join();
+            return cuda_fail(e, "split combine launch");
+        }
     }
 
     // ---- prefill-class launches
@@ -435,26 +524,14 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
         wl.item_off[wl.n] = items;
         cudaError_t e = use_fma ? launch_attn_fma(p, wl, d, kDecodeRows, items, stream)
                                 : launch_attn_mma(p, wl, d, items, k_cache, v_cache, num_slots, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "prefill attention launch");
+        if (e != cudaSuccess) {
+            join();
+            return cuda_fail(e, "prefill attention launch");
+        }
     }
 
-    // ---- combine split partials
-    for (size_t c0 = 0; c0 < combine_reqs.size(); c0 += kPlanMax) {
-        WorkList wl;
-        memset(&wl, 0, sizeof wl);
-        wl.mode = kModeDecode;
-        wl.split_tokens = split;
-        size_t c1 = c0 + kPlanMax < combine_reqs.size() ? c0 + kPlanMax : combine_reqs.size();
-        for (size_t x = c0; x < c1; x++) {
-            int li = wl.n++;
-            wl.req[li] = combine_reqs[x];
-            wl.part_off[li] = combine_off[x];
-            wl.item_off[li] = li;
-        }
-        wl.item_off[wl.n] = wl.n;
-        cudaError_t e = launch_attn_combine(p, wl, d, combine_max_rows, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "split combine launch");
-    }
+    cudaError_t ej = join();
+    if (ej != cudaSuccess) return cuda_fail(ej, "join");
     return PKV_OK;
 }
 

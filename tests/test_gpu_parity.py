@@ -117,6 +117,40 @@ def test_long_chunks_tensor_core_path(disable_tc, monkeypatch):
     assert pkv.read_device_error(dev.ws) == 0
 
 
+@pytest.mark.parametrize("overlap", [True, False])
+def test_mixed_step_side_stream_and_cuda_graph(overlap, monkeypatch):
+    """Decodes next to long prefill chunks: the decode kernels run on a forked
+    side stream (or, with PKV_NO_OVERLAP=1, on the caller's stream).  The step
+    is also captured in a CUDA graph and replayed; every result matches the
+    oracle."""
+    if not overlap:
+        monkeypatch.setenv("PKV_NO_OVERLAP", "1")
+    reqs = [Req(3000, 512, list(range(0, 220))), Req(0, 300, list(range(220, 239)))]
+    reqs += [Req(700 + 97 * i, 1, list(range(239 + 111 * i, 239 + 111 * (i + 1)))) for i in range(12)]
+    spec = Spec("mixed", reqs, 32, 8, 128, 16, 1600, 1 / math.sqrt(128), 23)
+    b = make_batch(spec, device="cpu")
+    dev = DeviceStep(b)
+    dev.step()
+    ref = cpu_copy(b)
+    oracle_write(ref)
+    want = oracle_full(ref)
+    assert_close(dev.out, want, "eager")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        dev.step()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph, stream=side):
+            dev.step()
+    torch.cuda.synchronize()
+    dev.out.fill_(float("nan"))
+    graph.replay()
+    torch.cuda.synchronize()
+    assert_close(dev.out, want, "graph replay")
+    assert pkv.read_device_error(dev.ws) == 0
+
+
 @pytest.mark.parametrize("split", [256, 512, 4096])
 def test_forced_split_sizes(split, monkeypatch):
     monkeypatch.setenv("PKV_SPLIT_TOKENS", str(split))
