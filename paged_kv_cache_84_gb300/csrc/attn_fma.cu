@@ -18,6 +18,7 @@
 // end.  Unsplit items write bf16 output; split items write fp32 partials
 // (unnormalised o, running max, weight sum) for the combine kernel.
 #include "common.cuh"
+#include "sm100.cuh"
 
 namespace pkv {
 
@@ -312,6 +313,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnParams p,
     const int rows = t * p.hq;
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.y * (blockDim.x / 32) + (threadIdx.x >> 5);
+    pdl_wait();                                                   // the split partials are written
     if (row >= rows) return;
     const size_t base = (size_t)wl.part_off[li];
 
@@ -348,14 +350,15 @@ cudaError_t launch_attn_combine(const AttnParams &p, const WorkList &wl, int hea
     if (wl.n <= 0) return cudaSuccess;
     dim3 grid(wl.n, (max_rows_per_req + 7) / 8);
     launch_begin(stream, kAttnCombine);
+    cudaError_t e;
     switch (head_dim) {
-    case 48: attn_combine_kernel<48><<<grid, 256, 0, stream>>>(p, wl); break;
-    case 64: attn_combine_kernel<64><<<grid, 256, 0, stream>>>(p, wl); break;
-    case 128: attn_combine_kernel<128><<<grid, 256, 0, stream>>>(p, wl); break;
+    case 48: e = launch_maybe_pdl(attn_combine_kernel<48>, grid, dim3(256), 0, stream, p, wl); break;
+    case 64: e = launch_maybe_pdl(attn_combine_kernel<64>, grid, dim3(256), 0, stream, p, wl); break;
+    case 128: e = launch_maybe_pdl(attn_combine_kernel<128>, grid, dim3(256), 0, stream, p, wl); break;
     default: launch_end(stream); return cudaErrorInvalidValue;
     }
     launch_end(stream);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace pkv

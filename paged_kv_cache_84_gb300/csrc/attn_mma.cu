@@ -10,7 +10,9 @@
 //   - warps 0..3 (consumers) take the rows of the CTA (pairs (token, query
 //     head) that share KV head kh: the grouped-query fold of the vllm-lite
 //     README) in tiles of 16.  With KG key groups, warp w works on row tile
-//     w / KG and on every KG-th block of the stage ring.
+//     w / KG and on every KG-th block, two blocks per iteration (two
+//     independent MMA chains, one softmax update per 32 keys).  Decode-class
+//     CTAs use 4 key groups, prefill-class CTAs 2 row tiles x 2 key groups.
 // Each consumer computes S = Q K^T for 16 rows x 16 keys with
 // mma.m16n8k16 (bf16 in, fp32 accumulate), applies the causal rule (query i
 // of a request with t new tokens and context L sits at position L - t + i
@@ -34,6 +36,7 @@ namespace pkv {
 constexpr int kConsumerWarps = 4;
 constexpr int kMmaThreads = (kConsumerWarps + 1) * 32;
 constexpr int kStageBudget = 96 * 1024;      // bytes of KV stages per CTA (two CTAs per SM)
+constexpr int kLongSplit = 512;              // decode splits of at least this many keys use the streaming kernel
 
 template <int D>
 struct MmaTile {
@@ -57,8 +60,329 @@ __device__ __forceinline__ uint32_t tile_off(int row, int chunk)
     }
 }
 
-template <int D, int KG>
+template <int D, int KG, int NB>
 struct MmaCfg {
+    static constexpr int kRT = kConsumerWarps / KG;                          // row tiles
+    static constexpr int kSlots0 = kStageBudget / MmaTile<D>::kSlot;
+    static constexpr int kSlots = kSlots0 > 32 ? 32 : kSlots0;               // ring of one-block slots
+    static_assert(kSlots >= 2 * KG, "the ring must hold two blocks of every key group");
+    static constexpr int kRingBytes = kSlots * MmaTile<D>::kSlot;
+    static constexpr int kMergeBytes = kConsumerWarps * 16 * (D + 2) * 4;
+    static constexpr int kBodyBytes = kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes;
+    static constexpr int kSmemBytes = 1024 + kBodyBytes + 2 * kSlots * 8;   // + alignment slack, barriers
+};
+
+// S for one 16-key block: sc[0], sc[1] = the two 8-key n-tiles.
+template <int D>
+__device__ __forceinline__ void block_scores(float (&sc0)[4], float (&sc1)[4], const uint32_t (&qa)[D / 16][4],
+                                             uint32_t kt, int mi, int mr)
+{
+#pragma unroll
+    for (int kk = 0; kk < D / 16; kk++) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kt + tile_off<D>((mi >> 1) * 8 + mr, 2 * kk + (mi & 1)), b0, b1, b2, b3);
+        mma_16816(sc0, qa[kk], b0, b1);
+        mma_16816(sc1, qa[kk], b2, b3);
+    }
+}
+
+// O += P V for one 16-key block.
+template <int D>
+__device__ __forceinline__ void block_pv(float (&o)[D / 8][4], const uint32_t (&pa)[4], uint32_t vt, int mi, int mr)
+{
+#pragma unroll
+    for (int np = 0; np < D / 16; np++) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vt + tile_off<D>((mi & 1) * 8 + mr, 2 * np + (mi >> 1)), b0, b1, b2, b3);
+        mma_16816(o[2 * np], pa, b0, b1);
+        mma_16816(o[2 * np + 1], pa, b2, b3);
+    }
+}
+
+template <int D, int KG, int NB>
+__global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, const __grid_constant__ WorkList wl,
+                                                               const __grid_constant__ CUtensorMap kmap,
+                                                               const __grid_constant__ CUtensorMap vmap)
+{
+    using T = MmaTile<D>;
+    using C = MmaCfg<D, KG, NB>;
+    constexpr int R = C::kSlots;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t ring = (raw + 1023u) & ~1023u;                 // 1024-aligned for the swizzle
+    uint8_t *ring_ptr = smem_raw + (ring - raw);
+    const uint32_t bars = ring + C::kBodyBytes;                   // full[R], then empty[R]
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (R + s); };
+    auto slot_addr = [&](int s) { return ring + (uint32_t)s * T::kSlot; };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kh = blockIdx.y;
+    const int li = find_listed(wl, blockIdx.x);
+    const int local = blockIdx.x - wl.item_off[li];
+    const int r = wl.req[li];
+    const int b = p.qsl[r], t = p.qsl[r + 1] - b, L = p.seq_lens[r];
+    const int g = p.group;
+
+    if (L == 0 || t == 0) {                                       // padding request: zero rows
+        // Wait like every other CTA: this grid then never completes before the
+        // grids it follows, which keeps later programmatic waits transitive.
+        pdl_wait();
+        for (int idx = threadIdx.x; idx < t * g * D; idx += kMmaThreads) {
+            const int rr = idx / D, e = idx - rr * D;
+            p.out[((size_t)(b + rr / g) * p.hq + kh * g + rr % g) * D + e] = __float2bfloat16(0.f);
+        }
+        return;
+    }
+
+    int i0, ntok, k_begin, k_end, split = 0;
+    bool partial = false;
+    if (wl.mode == kModeDecode) {
+        i0 = 0;
+        ntok = t;
+        split = local;
+        k_begin = split * wl.split_tokens;
+        k_end = min(L, k_begin + wl.split_tokens);
+        partial = wl.part_off[li] >= 0;
+    } else {
+        i0 = local * wl.tile_tokens;
+        ntok = min(wl.tile_tokens, t - i0);
+        k_begin = 0;
+        k_end = L - t + i0 + ntok;                                // one past the tile's last position
+    }
+    const int nr = ntok * g;                                      // rows of this CTA
+    const int blk0 = k_begin >> 4;
+    const int nblk = ((k_end + 15) >> 4) - blk0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < R; s++) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), C::kRT);                      // the row tiles that read a block
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            prefetch_tmap(&kmap);
+            prefetch_tmap(&vmap);
+        }
+        const int32_t *bt = p.block_table + (size_t)r * p.bt_stride + blk0;
+        pdl_wait();                                               // the step's K/V rows are in the pool
+        int ids = 0, issued = 0;
+        for (int i = 0; i < nblk; i++) {
+            if ((i & 31) == 0) ids = (i + lane < nblk) ? __ldg(bt + i + lane) : 0;
+            const int s = i % R;
+            bool ok = true;
+            if (i >= R) ok = mbar_wait(empty_bar(s), ((i / R) - 1) & 1, p.err);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            issued = i + 1;
+            int blk = __shfl_sync(0xffffffffu, ids, i & 31);
+            if (lane == 0) {
+                if (blk < 0 || blk >= p.nb_total) {               // outside the pool: report, read block 0
+                    atomicOr(p.err, 2u);
+                    blk = 0;
+                }
+                mbar_arrive_expect_tx(full_bar(s), T::kSlot);
+                const uint32_t dst = slot_addr(s);
+#pragma unroll
+                for (int x = 0; x < T::kBoxes; x++) {
+                    tma_load_3d(dst + x * T::kBoxBytes, &kmap, full_bar(s), x * T::kBoxCols, kh, blk * 16);
+                    tma_load_3d(dst + T::kTile + x * T::kBoxBytes, &vmap, full_bar(s), x * T::kBoxCols, kh,
+                                blk * 16);
+                }
+            }
+            __syncwarp();
+        }
+        // Normally every issued block has been consumed by now.  If a wait
+        // gave up, keep the CTA (and its shared memory) alive until the copies
+        // still in flight have landed, within the same time limit.
+        if (issued < nblk && lane == 0) {
+            for (int i = issued > R ? issued - R : 0; i < issued; i++) mbar_wait(full_bar(i % R), (i / R) & 1, p.err);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int rt = warp / KG, kg = warp % KG;
+    const int row0 = rt * 16;
+    const int rA = row0 + (lane >> 2), rB = rA + 8;               // the two rows this lane holds
+    const int qbase = L - t + i0;
+    const int qposA = rA < nr ? qbase + rA / g : -1;
+    const int qposB = rB < nr ? qbase + rB / g : -1;
+
+    // Q as mma A fragments, straight from global memory (bf16 pairs).
+    uint32_t qa[D / 16][4];
+    {
+        const uint32_t *qw = reinterpret_cast<const uint32_t *>(p.q);
+        const size_t rowA = rA < nr ? ((size_t)(b + i0 + rA / g) * p.hq + kh * g + rA % g) * (D / 2) : 0;
+        const size_t rowB = rB < nr ? ((size_t)(b + i0 + rB / g) * p.hq + kh * g + rB % g) * (D / 2) : 0;
+        const int c = (lane & 3);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; kk++) {
+            qa[kk][0] = rA < nr ? __ldg(qw + rowA + kk * 8 + c) : 0u;
+            qa[kk][1] = rB < nr ? __ldg(qw + rowB + kk * 8 + c) : 0u;
+            qa[kk][2] = rA < nr ? __ldg(qw + rowA + kk * 8 + 4 + c) : 0u;
+            qa[kk][3] = rB < nr ? __ldg(qw + rowB + kk * 8 + 4 + c) : 0u;
+        }
+    }
+
+    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+    float o[D / 8][4];
+#pragma unroll
+    for (int n = 0; n < D / 8; n++) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+
+    const float sl2 = p.scale_log2;
+    const int mi = lane >> 3, mr = lane & 7;                      // ldmatrix: matrix, row within it
+    bool alive = true;
+    // Each iteration takes NB blocks of this key group (kg, kg + KG): with NB
+    // = 2, two independent MMA chains and one softmax update per 32 keys
+    // (shorter latency chains); with NB = 1 each warp holds one ring slot at
+    // a time, leaving more of the ring for copies in flight.
+    for (int bl0 = kg; bl0 < nblk; bl0 += NB * KG) {
+        const int bl1 = bl0 + KG;
+        const bool two = NB == 2 && bl1 < nblk;
+        const int s0 = bl0 % R, s1 = bl1 % R;
+        if (!mbar_wait(full_bar(s0), (bl0 / R) & 1, p.err) || (two && !mbar_wait(full_bar(s1), (bl1 / R) & 1, p.err))) {
+            alive = false;
+            break;
+        }
+        float sc[4][4];
+#pragma unroll
+        for (int n = 0; n < 4; n++) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+        block_scores<D>(sc[0], sc[1], qa, slot_addr(s0), mi, mr);
+        if (two) block_scores<D>(sc[2], sc[3], qa, slot_addr(s1), mi, mr);
+        // scale into the exp2 domain, causal and range mask
+        const int kc0 = ((blk0 + bl0) << 4) + 2 * (lane & 3);
+        const int kc1 = ((blk0 + bl1) << 4) + 2 * (lane & 3);
+#pragma unroll
+        for (int n = 0; n < 4; n++) {
+#pragma unroll
+            for (int v = 0; v < 4; v++) {
+                const int key = (n < 2 ? kc0 : kc1) + (n & 1) * 8 + (v & 1);
+                const int qp = v < 2 ? qposA : qposB;
+                const bool ok = (n < 2 || two) && key < k_end && key <= qp;
+                sc[n][v] = ok ? sc[n][v] * sl2 : -INFINITY;
+            }
+        }
+        float pr[4][4];
+#pragma unroll
+        for (int hr = 0; hr < 2; hr++) {
+            float mx = fmaxf(max3f(sc[0][2 * hr], sc[0][2 * hr + 1], sc[1][2 * hr]),
+                             max3f(sc[1][2 * hr + 1], sc[2][2 * hr], sc[2][2 * hr + 1]));
+            mx = max3f(mx, sc[3][2 * hr], sc[3][2 * hr + 1]);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const float mnew = fmaxf(m[hr], mx);
+            const float ms = mnew == -INFINITY ? 0.f : mnew;
+            const float alpha = exp2f(m[hr] - ms);
+            m[hr] = mnew;
+            float sum = 0.f;
+#pragma unroll
+            for (int n = 0; n < 4; n++) {
+                pr[n][2 * hr] = exp2f(sc[n][2 * hr] - ms);
+                pr[n][2 * hr + 1] = exp2f(sc[n][2 * hr + 1] - ms);
+                sum += pr[n][2 * hr] + pr[n][2 * hr + 1];
+            }
+            l[hr] = l[hr] * alpha + sum;
+#pragma unroll
+            for (int n = 0; n < D / 8; n++) {
+                o[n][2 * hr] *= alpha;
+                o[n][2 * hr + 1] *= alpha;
+            }
+        }
+        uint32_t pa0[4], pa1[4];
+        pa0[0] = pack_bf16x2(pr[0][0], pr[0][1]);
+        pa0[1] = pack_bf16x2(pr[0][2], pr[0][3]);
+        pa0[2] = pack_bf16x2(pr[1][0], pr[1][1]);
+        pa0[3] = pack_bf16x2(pr[1][2], pr[1][3]);
+        block_pv<D>(o, pa0, slot_addr(s0) + T::kTile, mi, mr);
+        if (two) {
+            pa1[0] = pack_bf16x2(pr[2][0], pr[2][1]);
+            pa1[1] = pack_bf16x2(pr[2][2], pr[2][3]);
+            pa1[2] = pack_bf16x2(pr[3][0], pr[3][1]);
+            pa1[3] = pack_bf16x2(pr[3][2], pr[3][3]);
+            block_pv<D>(o, pa1, slot_addr(s1) + T::kTile, mi, mr);
+        }
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(empty_bar(s0));
+            if (two) mbar_arrive(empty_bar(s1));
+        }
+    }
+    pdl_launch_dependents();                                      // a combine kernel may start launching
+
+#pragma unroll
+    for (int hr = 0; hr < 2; hr++) {
+        l[hr] += __shfl_xor_sync(0xffffffffu, l[hr], 1);
+        l[hr] += __shfl_xor_sync(0xffffffffu, l[hr], 2);
+    }
+
+    // rows rA / rB -> (token, head) and the output or partial row
+    auto out_row = [&](int rr) -> size_t {
+        const int i = i0 + rr / g, h = kh * g + rr % g;
+        if (!partial) return (size_t)(b + i) * p.hq + h;
+        return (size_t)wl.part_off[li] + ((size_t)split * t + i) * p.hq + h;
+    };
+
+    // merge the KG key groups of each row tile through shared memory
+    named_bar_sync(1, kConsumerWarps * 32);                       // every consumer is done with the ring
+    float *mo = reinterpret_cast<float *>(ring_ptr);              // [warp][16][D]
+    float *mml = mo + kConsumerWarps * 16 * D;                    // [warp][16][2]
+    {
+        const int c = 2 * (lane & 3);
+#pragma unroll
+        for (int hr = 0; hr < 2; hr++) {
+            const int lr = (lane >> 2) + 8 * hr;
+#pragma unroll
+            for (int n = 0; n < D / 8; n++)
+                *reinterpret_cast<float2 *>(mo + (warp * 16 + lr) * D + n * 8 + c) = make_float2(o[n][2 * hr], o[n][2 * hr + 1]);
+            if ((lane & 3) == 0) {
+                mml[(warp * 16 + lr) * 2] = m[hr];
+                mml[(warp * 16 + lr) * 2 + 1] = l[hr];
+            }
+        }
+    }
+    named_bar_sync(1, kConsumerWarps * 32);
+    if (!alive) return;
+    for (int idx = threadIdx.x; idx < C::kRT * 16 * D; idx += kConsumerWarps * 32) {
+        const int rowc = idx / D, e = idx - rowc * D;            // row within the CTA
+        if (rowc >= nr) continue;
+        const int rtile = rowc >> 4, lr = rowc & 15;
+        float M = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < KG; q++) M = fmaxf(M, mml[((rtile * KG + q) * 16 + lr) * 2]);
+        const float Ms = M == -INFINITY ? 0.f : M;
+        float acc = 0.f, ls = 0.f;
+#pragma unroll
+        for (int q = 0; q < KG; q++) {
+            const int wq = rtile * KG + q;
+            const float sc = exp2f(mml[(wq * 16 + lr) * 2] - Ms);
+            acc = fmaf(sc, mo[(wq * 16 + lr) * D + e], acc);
+            ls = fmaf(sc, mml[(wq * 16 + lr) * 2 + 1], ls);
+        }
+        const size_t orow = out_row(rowc);
+        if (!partial) {
+            p.out[orow * D + e] = __float2bfloat16(ls > 0.f ? acc / ls : 0.f);
+        } else {
+            p.part_o[orow * D + e] = acc;
+            if (e == 0) p.part_ml[orow] = make_float2(M, ls);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- streaming decode
+//
+// Long decode splits (at least kLongSplit keys per CTA) stream their blocks
+// through a ring of stages of KG blocks each, one full/empty barrier pair per
+// stage: every consumer warp takes one block of each stage.  Measured on the
+// 256-request and the 32 x 32768 decode workloads this keeps more copies in
+// flight per SM than the one-block slot ring above, which wins on short,
+// latency-bound ranges instead.
+template <int D, int KG>
+struct StreamCfg {
     static constexpr int kRT = kConsumerWarps / KG;                          // row tiles
     static constexpr int kStages0 = kStageBudget / (KG * MmaTile<D>::kSlot);
     static constexpr int kStages = kStages0 > 8 ? 8 : (kStages0 < 2 ? 2 : kStages0);
@@ -70,12 +394,12 @@ struct MmaCfg {
 };
 
 template <int D, int KG>
-__global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, const __grid_constant__ WorkList wl,
+__global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, const __grid_constant__ WorkList wl,
                                                                const __grid_constant__ CUtensorMap kmap,
                                                                const __grid_constant__ CUtensorMap vmap)
 {
     using T = MmaTile<D>;
-    using C = MmaCfg<D, KG>;
+    using C = StreamCfg<D, KG>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -94,6 +418,7 @@ __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, con
     const int g = p.group;
 
     if (L == 0 || t == 0) {                                       // padding request: zero rows
+        pdl_wait();                                               // keeps later programmatic waits transitive
         for (int idx = threadIdx.x; idx < t * g * D; idx += kMmaThreads) {
             const int rr = idx / D, e = idx - rr * D;
             p.out[((size_t)(b + rr / g) * p.hq + kh * g + rr % g) * D + e] = __float2bfloat16(0.f);
@@ -137,6 +462,7 @@ __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, con
             prefetch_tmap(&vmap);
         }
         const int32_t *bt = p.block_table + (size_t)r * p.bt_stride + blk0;
+        pdl_wait();                                               // the step's K/V rows are in the pool
         int ids = 0, issued = 0;
         for (int it = 0; it < iters; it++) {
             const int base = it * KG;
@@ -275,6 +601,7 @@ __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, con
         if (lane == 0) mbar_arrive(empty_bar(s));
     }
 
+    pdl_launch_dependents();                                      // a combine kernel may start launching
 #pragma unroll
     for (int hr = 0; hr < 2; hr++) {
         l[hr] += __shfl_xor_sync(0xffffffffu, l[hr], 1);
@@ -412,22 +739,53 @@ cudaError_t make_q_tmap(CUtensorMap *map, const void *q, int num_tokens, int hq,
     return res == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D, int KG>
+template <int D, int KG, int NB>
 static cudaError_t launch_mma_dk(const AttnParams &p, const WorkList &wl, int num_items, const CUtensorMap &km,
                                  const CUtensorMap &vm, cudaStream_t stream)
 {
-    constexpr int smem = MmaCfg<D, KG>::kSmemBytes;
+    constexpr int smem = MmaCfg<D, KG, NB>::kSmemBytes;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(attn_mma_kernel<D, KG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        attr_err = cudaFuncSetAttribute(attn_mma_kernel<D, KG, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     });
     if (attr_err != cudaSuccess) return attr_err;
     dim3 grid(num_items, p.hkv);
     launch_begin(stream, wl.mode == kModeDecode ? kAttnMmaDecode : kAttnMmaPrefill);
-    attn_mma_kernel<D, KG><<<grid, kMmaThreads, smem, stream>>>(p, wl, km, vm);
+    cudaError_t e = launch_maybe_pdl(attn_mma_kernel<D, KG, NB>, grid, dim3(kMmaThreads), smem, stream, p, wl, km, vm);
     launch_end(stream);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t launch_stream_d(const AttnParams &p, const WorkList &wl, int num_items, const CUtensorMap &km,
+                                   const CUtensorMap &vm, cudaStream_t stream)
+{
+    constexpr int smem = StreamCfg<D, 4>::kSmemBytes;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(attn_stream_kernel<D, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    dim3 grid(num_items, p.hkv);
+    launch_begin(stream, kAttnMmaDecode);
+    cudaError_t e = launch_maybe_pdl(attn_stream_kernel<D, 4>, grid, dim3(kMmaThreads), smem, stream, p, wl, km, vm);
+    launch_end(stream);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// Decode-class CTAs: 4 key groups; the streaming kernel when each CTA
+// walks a long key range, the slot-ring kernel with two blocks per
+// iteration when ranges are short and latency dominates.  Prefill-class
+// CTAs: 2 row tiles x 2 key groups, two blocks per iteration.
+template <int D>
+static cudaError_t launch_mma_d(const AttnParams &p, const WorkList &wl, int num_items, const CUtensorMap &km,
+                                const CUtensorMap &vm, cudaStream_t stream)
+{
+    if (wl.mode != kModeDecode) return launch_mma_dk<D, 2, 2>(p, wl, num_items, km, vm, stream);
+    if (wl.split_tokens >= kLongSplit) return launch_stream_d<D>(p, wl, num_items, km, vm, stream);
+    return launch_mma_dk<D, 4, 2>(p, wl, num_items, km, vm, stream);
 }
 
 cudaError_t launch_attn_mma(const AttnParams &p, const WorkList &wl, int head_dim, int num_items,
@@ -440,18 +798,14 @@ cudaError_t launch_attn_mma(const AttnParams &p, const WorkList &wl, int head_di
     cudaError_t e = make_pool_tmap(&km, k_cache, num_slots, p.hkv, head_dim, box, sw);
     if (e == cudaSuccess) e = make_pool_tmap(&vm, v_cache, num_slots, p.hkv, head_dim, box, sw);
     if (e != cudaSuccess) return e;
-    const bool dec = wl.mode == kModeDecode;
     switch (head_dim) {
-    case 48: return dec ? launch_mma_dk<48, 4>(p, wl, num_items, km, vm, stream)
-                        : launch_mma_dk<48, 1>(p, wl, num_items, km, vm, stream);
-    case 64: return dec ? launch_mma_dk<64, 4>(p, wl, num_items, km, vm, stream)
-                        : launch_mma_dk<64, 1>(p, wl, num_items, km, vm, stream);
-    case 128: return dec ? launch_mma_dk<128, 4>(p, wl, num_items, km, vm, stream)
-                         : launch_mma_dk<128, 1>(p, wl, num_items, km, vm, stream);
+    case 48: return launch_mma_d<48>(p, wl, num_items, km, vm, stream);
+    case 64: return launch_mma_d<64>(p, wl, num_items, km, vm, stream);
+    case 128: return launch_mma_d<128>(p, wl, num_items, km, vm, stream);
     default: return cudaErrorInvalidValue;
     }
 }
 
-int mma_prefill_rows() { return 16 * kConsumerWarps; }
+int mma_prefill_rows() { return 16 * (kConsumerWarps / 2); }   // prefill CTAs: 2 row tiles x 2 key groups
 
 }  // namespace pkv

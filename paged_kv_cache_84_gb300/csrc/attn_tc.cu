@@ -212,6 +212,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, co
             }
         }
         const int32_t *bt = p.block_table + (size_t)r * p.bt_stride;
+        pdl_wait();                                                // the step's K/V rows are in the pool
         int ids = 0, issued_k = 0, issued_v = 0;
         for (int j = 0; j < nkt; j++) {
             const int st = j & 1;
@@ -372,6 +373,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, co
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kBarPA + x));
         }
+        pdl_launch_dependents();
         if (ok) ok = mbar_wait(bar(kBarOA + x), (nkt - 1) & 1, p.err);
         if (__all_sync(0xffffffffu, ok)) {
             tc_fence_after();
@@ -433,9 +435,9 @@ cudaError_t launch_attn_tc(const AttnParams &p, const WorkList &wl, int num_item
     if (num_items > 65535) return cudaErrorInvalidConfiguration;
     dim3 grid(p.hkv, num_items);                   // items in launch order: the planner puts the longest first
     launch_begin(stream, kAttnTcPrefill);
-    attn_tc_kernel<<<grid, kTcThreads, kTcSmem, stream>>>(p, wl, qm, km, vm, num_slots);
+    e = launch_maybe_pdl(attn_tc_kernel, grid, dim3(kTcThreads), kTcSmem, stream, p, wl, qm, km, vm, num_slots);
     launch_end(stream);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace pkv

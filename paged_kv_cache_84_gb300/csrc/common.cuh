@@ -130,4 +130,26 @@ enum KernelId : int {
 void launch_begin(cudaStream_t stream, int kernel_id);
 void launch_end(cudaStream_t stream);
 
+// Whether kernels that read what an earlier kernel of the same stream wrote
+// are launched with programmatic stream serialization (they start early and
+// wait in-kernel with griddepcontrol.wait).  Off with PKV_NO_PDL=1.
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_maybe_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 }  // namespace pkv

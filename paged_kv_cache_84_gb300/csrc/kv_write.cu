@@ -6,6 +6,7 @@
 // scratch block.  A bit copy: 16-byte vectors, one per thread, the K and the
 // V chunk of the same offset handled together.
 #include "common.cuh"
+#include "sm100.cuh"
 
 namespace pkv {
 
@@ -14,6 +15,7 @@ __global__ void __launch_bounds__(256) kv_write_kernel(
     uint4 *__restrict__ v_cache, const int64_t *__restrict__ slot_mapping, int64_t total_chunks,
     int32_t chunks_per_row, int64_t num_slots, uint32_t *err)
 {
+    pdl_launch_dependents();                              // the attention kernel may start its set-up
     int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < total_chunks; c += stride) {
         int64_t row = c / chunks_per_row;

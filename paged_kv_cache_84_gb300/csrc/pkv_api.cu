@@ -59,6 +59,12 @@ void launch_end(cudaStream_t stream)
     g_prof.open = -1;
 }
 
+bool pdl_enabled()
+{
+    const char *s = getenv("PKV_NO_PDL");
+    return !(s && *s && atoi(s) != 0);
+}
+
 static thread_local char g_cuda_err[256] = "";
 
 static pkv_status cuda_fail(cudaError_t e, const char *where)
@@ -392,12 +398,12 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
     p.part_ml = reinterpret_cast<float2 *>(ws + kErrBytes + ((total_rows * d * 4 + 15) / 16) * 16);
 
     // ---- decode-class work runs on a side stream, concurrently with the
-    // tensor-core prefill, when both are present: its CTAs fill the SMs that
-    // the prefill's last wave leaves idle.  Fork and join with events, so the
+    // prefill kernels, when both are present: its CTAs fill the SMs that the
+    // prefill leaves idle (its last wave, or a small batch's spare SMs).  Fork and join with events, so the
     // caller's stream order (and CUDA-graph capture) is preserved.
     cudaStream_t dstream = stream;
     SideStream *side = nullptr;
-    const bool fork = !tcp.empty() && !dec.empty() && !env_int("PKV_NO_OVERLAP", 0);
+    const bool fork = !dec.empty() && (!tcp.empty() || !pre.empty()) && !env_int("PKV_NO_OVERLAP", 0);
     if (fork) {
         side = side_stream();
         if (!side) return cuda_fail(cudaErrorUnknown, "side stream");

@@ -165,6 +165,16 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
     return r;
 }
 
+// Programmatic dependent launch: let the next kernel of the stream start
+// launching, and wait until the grids this one depends on have completed
+// and their memory is visible.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Named barrier over `count` threads (a subset of the CTA).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count)
 {

@@ -151,6 +151,26 @@ def test_mixed_step_side_stream_and_cuda_graph(overlap, monkeypatch):
     assert pkv.read_device_error(dev.ws) == 0
 
 
+@pytest.mark.parametrize("pdl", [True, False])
+def test_programmatic_launch_and_padding_only_decodes(pdl, monkeypatch):
+    """Kernels launched with programmatic stream serialization wait in-kernel
+    for the pool write.  A batch whose decode-class requests are all padding,
+    next to a prefill chunk, must still see the step's K/V (PKV_NO_PDL=1 gives
+    plain stream order)."""
+    if not pdl:
+        monkeypatch.setenv("PKV_NO_PDL", "1")
+    reqs = [Req(0, 1, [], pad=True), Req(200, 90, list(range(0, 19))), Req(0, 1, [], pad=True)]
+    spec = Spec("pad-mix", reqs, 8, 4, 64, 16, 24, 0.125, 31)
+    b = make_batch(spec, device="cpu")
+    for _ in range(3):
+        dev = DeviceStep(b)
+        dev.step()
+        ref = cpu_copy(b)
+        oracle_write(ref)
+        assert_close(dev.out, oracle_full(ref), "padding-only decodes")
+        assert dev.out[0].abs().sum().item() == 0 and dev.out[-1].abs().sum().item() == 0
+
+
 @pytest.mark.parametrize("split", [256, 512, 4096])
 def test_forced_split_sizes(split, monkeypatch):
     monkeypatch.setenv("PKV_SPLIT_TOKENS", str(split))
