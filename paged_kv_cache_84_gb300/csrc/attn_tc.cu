@@ -12,9 +12,10 @@
 // (key j lives in block table[j / 16], row j % 16).
 //
 // Warp roles (384 threads):
-//   warp 0      TMA producer: both Q tiles once, then K and V tiles into two
-//               2-stage rings (a K stage is refilled once both S MMAs that
-//               read it are done, a V stage once both PV MMAs are done);
+//   warps 0, 2  TMA producers: warp 0 both Q tiles once, then K tiles, warp 2
+//               V tiles, each into a 2-stage ring (a K stage is refilled once
+//               both S MMAs that read it are done, a V stage once both PV
+//               MMAs are done); a tile's 16 boxes go out from 16 lanes at once;
 //   warp 1      MMA issuer (one thread) and TMEM owner; per key tile it
 //               issues PV_a(j-1), S_a(j), PV_b(j-1), S_b(j), so the tensor
 //               core always has the other tile's work while a softmax runs;
@@ -53,13 +54,11 @@ enum TcBar {
     kBarQ = 0,
     kBarK0 = 1, kBarK1 = 2,
     kBarV0 = 3, kBarV1 = 4,
-    kBarKEmpty0 = 5, kBarKEmpty1 = 6,
-    kBarVEmpty0 = 7, kBarVEmpty1 = 8,
-    kBarSA = 9, kBarSB = 10,          // S of tile a / b ready
-    kBarPA = 11, kBarPB = 12,         // P of tile a / b written (4 warps each)
-    kBarOA = 13, kBarOB = 14,         // PV of tile a / b done
-    kBarMmaDone = 15,
-    kNumTcBars = 16
+    kBarSA = 5, kBarSB = 6,           // S of tile a / b done (also frees a K stage)
+    kBarPA = 7, kBarPB = 8,           // P of tile a / b written (4 warps each)
+    kBarOA = 9, kBarOB = 10,          // PV of tile a / b done (also frees a V stage)
+    kBarMmaDone = 11,
+    kNumTcBars = 12
 };
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
@@ -197,76 +196,67 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, co
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
+    if (warp == 0 || warp == 2) {
+        // ------------------------------------------------------------ TMA producers
+        // warp 0 loads Q and the K tiles, warp 2 the V tiles.  A tile's 16
+        // boxes (8 blocks x 2 column halves) are issued by 16 lanes at once.
+        const bool is_k = warp == 0;
         if (lane == 0) {
-            prefetch_tmap(&qmap);
-            prefetch_tmap(&kmap);
-            prefetch_tmap(&vmap);
-            mbar_arrive_expect_tx(bar(kBarQ), has_b ? 2 * kTile : kTile);
-            tma_load_3d(sb + kQOff, &qmap, bar(kBarQ), 0, kh * g, b + i0);
-            tma_load_3d(sb + kQOff + kSub, &qmap, bar(kBarQ), 64, kh * g, b + i0);
-            if (has_b) {
-                tma_load_3d(sb + kQOff + kTile, &qmap, bar(kBarQ), 0, kh * g, b + i0 + tt);
-                tma_load_3d(sb + kQOff + kTile + kSub, &qmap, bar(kBarQ), 64, kh * g, b + i0 + tt);
+            if (is_k) {
+                prefetch_tmap(&qmap);
+                prefetch_tmap(&kmap);
+                mbar_arrive_expect_tx(bar(kBarQ), has_b ? 2 * kTile : kTile);
+                tma_load_3d(sb + kQOff, &qmap, bar(kBarQ), 0, kh * g, b + i0);
+                tma_load_3d(sb + kQOff + kSub, &qmap, bar(kBarQ), 64, kh * g, b + i0);
+                if (has_b) {
+                    tma_load_3d(sb + kQOff + kTile, &qmap, bar(kBarQ), 0, kh * g, b + i0 + tt);
+                    tma_load_3d(sb + kQOff + kTile + kSub, &qmap, bar(kBarQ), 64, kh * g, b + i0 + tt);
+                }
+            } else {
+                prefetch_tmap(&vmap);
             }
         }
+        const CUtensorMap *map = is_k ? &kmap : &vmap;
+        const uint32_t ring = sb + (is_k ? kKOff : kVOff);
+        const int full0 = is_k ? kBarK0 : kBarV0;
+        // A K stage is free once the last S MMA that reads it is done, a V
+        // stage once the last PV MMA is: wait on those MMAs' own completion
+        // barriers (their next completion needs a tile not loaded yet).
+        const int done_bar = is_k ? (has_b ? kBarSB : kBarSA) : (has_b ? kBarOB : kBarOA);
         const int32_t *bt = p.block_table + (size_t)r * p.bt_stride;
+        const int bi = (lane >> 1) & 7, half = lane & 1;           // this lane's box (lanes 0..15)
         pdl_wait();                                                // the step's K/V rows are in the pool
-        int ids = 0, issued_k = 0, issued_v = 0;
+        int ids = 0, issued = 0;
         for (int j = 0; j < nkt; j++) {
             const int st = j & 1;
             if ((j & 3) == 0) {                                    // 32 block ids = 4 key tiles
                 const int jb = j * 8 + lane;
                 ids = jb < nblk ? __ldg(bt + jb) : INT_MIN;
             }
-            // slot rows of this tile's 8 blocks (beyond the range: past the pool, TMA fills zeros)
-            int rows8[8];
-#pragma unroll
-            for (int bi = 0; bi < 8; bi++) {
-                const int blk = __shfl_sync(0xffffffffu, ids, ((j & 3) << 3) + bi);
-                rows8[bi] = (int)num_slots;
-                if (blk != INT_MIN) {
-                    if (blk < 0 || blk >= p.nb_total) {
-                        if (lane == 0) atomicOr(p.err, 2u);
-                    } else {
-                        rows8[bi] = blk * 16;
-                    }
+            // slot row of this lane's block (beyond the range: past the pool, TMA fills zeros)
+            const int blk = __shfl_sync(0xffffffffu, ids, ((j & 3) << 3) + bi);
+            int row = (int)num_slots;
+            if (blk != INT_MIN) {
+                if (blk < 0 || blk >= p.nb_total) {
+                    if (is_k && lane < 16 && half == 0) atomicOr(p.err, 2u);
+                } else {
+                    row = blk * 16;
                 }
             }
             bool ok = true;
-            if (j >= 2) ok = mbar_wait(bar(kBarKEmpty0 + st), ((j >> 1) - 1) & 1, p.err);
+            if (j >= 2) ok = mbar_wait(bar(done_bar), (j - 2) & 1, p.err);
             if (!__all_sync(0xffffffffu, ok)) break;
-            issued_k = j + 1;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(bar(kBarK0 + st), kTile);
-                const uint32_t kd = sb + kKOff + st * kTile;
-#pragma unroll
-                for (int bi = 0; bi < 8; bi++) {
-                    tma_load_3d(kd + bi * 2048, &kmap, bar(kBarK0 + st), 0, kh, rows8[bi]);
-                    tma_load_3d(kd + kSub + bi * 2048, &kmap, bar(kBarK0 + st), 64, kh, rows8[bi]);
-                }
-            }
-            if (j >= 2) ok = mbar_wait(bar(kBarVEmpty0 + st), ((j >> 1) - 1) & 1, p.err);
-            if (!__all_sync(0xffffffffu, ok)) break;
-            issued_v = j + 1;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(bar(kBarV0 + st), kTile);
-                const uint32_t vd = sb + kVOff + st * kTile;
-#pragma unroll
-                for (int bi = 0; bi < 8; bi++) {
-                    tma_load_3d(vd + bi * 2048, &vmap, bar(kBarV0 + st), 0, kh, rows8[bi]);
-                    tma_load_3d(vd + kSub + bi * 2048, &vmap, bar(kBarV0 + st), 64, kh, rows8[bi]);
-                }
-            }
+            issued = j + 1;
+            if (lane == 0) mbar_arrive_expect_tx(bar(full0 + st), kTile);
+            __syncwarp();
+            if (lane < 16)
+                tma_load_3d(ring + st * kTile + half * kSub + bi * 2048, map, bar(full0 + st), half * 64, kh, row);
             __syncwarp();
         }
-        if ((issued_k < nkt || issued_v < nkt) && lane == 0) {     // a wait gave up: drain own copies
-            mbar_wait(bar(kBarQ), 0, p.err);
-            for (int j = issued_k > 2 ? issued_k - 2 : 0; j < issued_k; j++)
-                mbar_wait(bar(kBarK0 + (j & 1)), (j >> 1) & 1, p.err);
-            for (int j = issued_v > 2 ? issued_v - 2 : 0; j < issued_v; j++)
-                mbar_wait(bar(kBarV0 + (j & 1)), (j >> 1) & 1, p.err);
+        if (issued < nkt && lane == 0) {                           // a wait gave up: drain own copies
+            if (is_k) mbar_wait(bar(kBarQ), 0, p.err);
+            for (int j = issued > 2 ? issued - 2 : 0; j < issued; j++)
+                mbar_wait(bar(full0 + (j & 1)), (j >> 1) & 1, p.err);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -284,7 +274,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, co
                     tc_mma(tmem + x * 128, ad, bd, idS, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(bar(kBarSA + x));
-                if (x == ntile - 1) tc_commit(bar(kBarKEmpty0 + (j & 1)));
             };
             auto issue_pv = [&](int x, int i) -> bool {            // O_x += P_x(i) V_i
                 if (!mbar_wait(bar(kBarPA + x), i & 1, p.err)) return false;
@@ -297,7 +286,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, co
                     tc_mma_ts(tmem + 256 + x * 128, tmem + x * 128 + kk * 8, bd, idO, (i > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(bar(kBarOA + x));
-                if (x == ntile - 1) tc_commit(bar(kBarVEmpty0 + (i & 1)));
                 return true;
             };
             bool ok = mbar_wait(bar(kBarQ), 0, p.err);
