@@ -63,9 +63,11 @@ __device__ __forceinline__ uint32_t tile_off(int row, int chunk)
 template <int D, int KG, int NB>
 struct MmaCfg {
     static constexpr int kRT = kConsumerWarps / KG;                          // row tiles
-    static constexpr int kSlots0 = kStageBudget / MmaTile<D>::kSlot;
-    static constexpr int kSlots = kSlots0 > 32 ? 32 : kSlots0;               // ring of one-block slots
-    static_assert(kSlots >= 2 * KG, "the ring must hold two blocks of every key group");
+    // Ring of one-block slots: this kernel serves short, latency-bound key
+    // ranges, so the ring holds one iteration of every key group plus a few
+    // blocks in flight, small enough for several CTAs per SM.
+    static constexpr int kSlots = KG * NB + KG + 4;
+    static_assert(kSlots >= KG * NB + KG, "the ring must hold an iteration of every key group plus one block each");
     static constexpr int kRingBytes = kSlots * MmaTile<D>::kSlot;
     static constexpr int kMergeBytes = kConsumerWarps * 16 * (D + 2) * 4;
     static constexpr int kBodyBytes = kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes;
@@ -145,14 +147,22 @@ __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, con
         k_end = min(L, k_begin + wl.split_tokens);
         partial = wl.part_off[li] >= 0;
     } else {
-        i0 = local * wl.tile_tokens;
+        // tile of new tokens; when split, every tile has the request's
+        // ceil(L / split) splits and those past the tile's last position
+        // leave empty partials (m = -inf, l = 0)
+        const int S = wl.split_tokens > 0 ? (L + wl.split_tokens - 1) / wl.split_tokens : 1;
+        const int tile = local / S;
+        split = local - tile * S;
+        i0 = tile * wl.tile_tokens;
         ntok = min(wl.tile_tokens, t - i0);
-        k_begin = 0;
-        k_end = L - t + i0 + ntok;                                // one past the tile's last position
+        const int tend = L - t + i0 + ntok;                       // one past the tile's last position
+        k_begin = wl.split_tokens > 0 ? split * wl.split_tokens : 0;
+        k_end = wl.split_tokens > 0 ? min(tend, k_begin + wl.split_tokens) : tend;
+        partial = wl.part_off[li] >= 0;
     }
     const int nr = ntok * g;                                      // rows of this CTA
     const int blk0 = k_begin >> 4;
-    const int nblk = ((k_end + 15) >> 4) - blk0;
+    const int nblk = max(0, ((k_end + 15) >> 4) - blk0);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < R; s++) {
@@ -237,42 +247,49 @@ __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, con
     const float sl2 = p.scale_log2;
     const int mi = lane >> 3, mr = lane & 7;                      // ldmatrix: matrix, row within it
     bool alive = true;
-    // Each iteration takes NB blocks of this key group (kg, kg + KG): with NB
-    // = 2, two independent MMA chains and one softmax update per 32 keys
+    // Each iteration takes NB blocks of this key group (kg, kg + KG, ...):
+    // NB independent MMA chains and one softmax update per 16*NB keys
     // (shorter latency chains); with NB = 1 each warp holds one ring slot at
     // a time, leaving more of the ring for copies in flight.
     for (int bl0 = kg; bl0 < nblk; bl0 += NB * KG) {
-        const int bl1 = bl0 + KG;
-        const bool two = NB == 2 && bl1 < nblk;
-        const int s0 = bl0 % R, s1 = bl1 % R;
-        if (!mbar_wait(full_bar(s0), (bl0 / R) & 1, p.err) || (two && !mbar_wait(full_bar(s1), (bl1 / R) & 1, p.err))) {
+        int slot[NB];
+        bool has[NB];
+        bool waited = true;
+#pragma unroll
+        for (int q = 0; q < NB; q++) {
+            const int bl = bl0 + q * KG;
+            has[q] = bl < nblk;
+            slot[q] = bl % R;
+            if (has[q] && waited) waited = mbar_wait(full_bar(slot[q]), (bl / R) & 1, p.err);
+        }
+        if (!waited) {
             alive = false;
             break;
         }
-        float sc[4][4];
+        float sc[2 * NB][4];
 #pragma unroll
-        for (int n = 0; n < 4; n++) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
-        block_scores<D>(sc[0], sc[1], qa, slot_addr(s0), mi, mr);
-        if (two) block_scores<D>(sc[2], sc[3], qa, slot_addr(s1), mi, mr);
+        for (int n = 0; n < 2 * NB; n++) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+#pragma unroll
+        for (int q = 0; q < NB; q++)
+            if (has[q]) block_scores<D>(sc[2 * q], sc[2 * q + 1], qa, slot_addr(slot[q]), mi, mr);
         // scale into the exp2 domain, causal and range mask
-        const int kc0 = ((blk0 + bl0) << 4) + 2 * (lane & 3);
-        const int kc1 = ((blk0 + bl1) << 4) + 2 * (lane & 3);
 #pragma unroll
-        for (int n = 0; n < 4; n++) {
+        for (int n = 0; n < 2 * NB; n++) {
+            const int kc = ((blk0 + bl0 + (n >> 1) * KG) << 4) + (n & 1) * 8 + 2 * (lane & 3);
 #pragma unroll
             for (int v = 0; v < 4; v++) {
-                const int key = (n < 2 ? kc0 : kc1) + (n & 1) * 8 + (v & 1);
+                const int key = kc + (v & 1);
                 const int qp = v < 2 ? qposA : qposB;
-                const bool ok = (n < 2 || two) && key < k_end && key <= qp;
+                const bool ok = has[n >> 1] && key < k_end && key <= qp;
                 sc[n][v] = ok ? sc[n][v] * sl2 : -INFINITY;
             }
         }
-        float pr[4][4];
+        float pr[2 * NB][4];
 #pragma unroll
         for (int hr = 0; hr < 2; hr++) {
-            float mx = fmaxf(max3f(sc[0][2 * hr], sc[0][2 * hr + 1], sc[1][2 * hr]),
-                             max3f(sc[1][2 * hr + 1], sc[2][2 * hr], sc[2][2 * hr + 1]));
-            mx = max3f(mx, sc[3][2 * hr], sc[3][2 * hr + 1]);
+            float mx = -INFINITY;
+#pragma unroll
+            for (int n = 0; n < 2 * NB; n++) mx = max3f(mx, sc[n][2 * hr], sc[n][2 * hr + 1]);
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
             const float mnew = fmaxf(m[hr], mx);
@@ -281,7 +298,7 @@ __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, con
             m[hr] = mnew;
             float sum = 0.f;
 #pragma unroll
-            for (int n = 0; n < 4; n++) {
+            for (int n = 0; n < 2 * NB; n++) {
                 pr[n][2 * hr] = exp2f(sc[n][2 * hr] - ms);
                 pr[n][2 * hr + 1] = exp2f(sc[n][2 * hr + 1] - ms);
                 sum += pr[n][2 * hr] + pr[n][2 * hr + 1];
@@ -293,23 +310,21 @@ __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, con
                 o[n][2 * hr + 1] *= alpha;
             }
         }
-        uint32_t pa0[4], pa1[4];
-        pa0[0] = pack_bf16x2(pr[0][0], pr[0][1]);
-        pa0[1] = pack_bf16x2(pr[0][2], pr[0][3]);
-        pa0[2] = pack_bf16x2(pr[1][0], pr[1][1]);
-        pa0[3] = pack_bf16x2(pr[1][2], pr[1][3]);
-        block_pv<D>(o, pa0, slot_addr(s0) + T::kTile, mi, mr);
-        if (two) {
-            pa1[0] = pack_bf16x2(pr[2][0], pr[2][1]);
-            pa1[1] = pack_bf16x2(pr[2][2], pr[2][3]);
-            pa1[2] = pack_bf16x2(pr[3][0], pr[3][1]);
-            pa1[3] = pack_bf16x2(pr[3][2], pr[3][3]);
-            block_pv<D>(o, pa1, slot_addr(s1) + T::kTile, mi, mr);
+#pragma unroll
+        for (int q = 0; q < NB; q++) {
+            if (!has[q]) continue;
+            uint32_t pa[4];
+            pa[0] = pack_bf16x2(pr[2 * q][0], pr[2 * q][1]);
+            pa[1] = pack_bf16x2(pr[2 * q][2], pr[2 * q][3]);
+            pa[2] = pack_bf16x2(pr[2 * q + 1][0], pr[2 * q + 1][1]);
+            pa[3] = pack_bf16x2(pr[2 * q + 1][2], pr[2 * q + 1][3]);
+            block_pv<D>(o, pa, slot_addr(slot[q]) + T::kTile, mi, mr);
         }
         __syncwarp();
         if (lane == 0) {
-            mbar_arrive(empty_bar(s0));
-            if (two) mbar_arrive(empty_bar(s1));
+#pragma unroll
+            for (int q = 0; q < NB; q++)
+                if (has[q]) mbar_arrive(empty_bar(slot[q]));
         }
     }
     pdl_launch_dependents();                                      // a combine kernel may start launching
@@ -783,9 +798,10 @@ template <int D>
 static cudaError_t launch_mma_d(const AttnParams &p, const WorkList &wl, int num_items, const CUtensorMap &km,
                                 const CUtensorMap &vm, cudaStream_t stream)
 {
-    if (wl.mode != kModeDecode) return launch_mma_dk<D, 2, 2>(p, wl, num_items, km, vm, stream);
+    constexpr int NB = 2;                                       // blocks per warp iteration
+    if (wl.mode != kModeDecode) return launch_mma_dk<D, 2, NB>(p, wl, num_items, km, vm, stream);
     if (wl.split_tokens >= kLongSplit) return launch_stream_d<D>(p, wl, num_items, km, vm, stream);
-    return launch_mma_dk<D, 4, 2>(p, wl, num_items, km, vm, stream);
+    return launch_mma_dk<D, 4, NB>(p, wl, num_items, km, vm, stream);
 }
 
 cudaError_t launch_attn_mma(const AttnParams &p, const WorkList &wl, int head_dim, int num_items,

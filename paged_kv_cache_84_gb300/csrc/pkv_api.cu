@@ -121,6 +121,7 @@ constexpr int kDecodeRows = 16;       // decode-class: t * g <= this
 constexpr int kMinSplit = 256;        // smallest KV split, tokens
 constexpr int kMaxSplits = 64;        // most splits of one request
 constexpr size_t kErrBytes = 256;     // device error word area at the workspace start
+constexpr int kMaxPrefillRowSplits = 4;   // workspace sizing of split prefill tiles
 
 // Kernel class of request r (host rule shared by the planner and pkv_plan_request_kernels).
 static int env_int(const char *name, int dflt);
@@ -248,6 +249,12 @@ size_t pkv_attention_workspace_bytes(int32_t max_num_reqs, int32_t max_num_token
     int64_t dec_tokens = (int64_t)max_num_reqs * kDecodeRows;
     if (dec_tokens > max_num_tokens) dec_tokens = max_num_tokens;
     int64_t rows = splits * dec_tokens * num_q_heads;
+    // short prefill tiles of small batches (fewer than 2 CTAs per SM) may be
+    // split too: at most ~2*SMs tiles of 32 rows, kMaxPrefillRowSplits splits each
+    int64_t pre_rows = (int64_t)max_num_tokens * num_q_heads;
+    if (pre_rows > 2 * 152 * 32) pre_rows = 2 * 152 * 32;
+    int64_t pre_splits = splits < kMaxPrefillRowSplits ? splits : kMaxPrefillRowSplits;
+    rows += pre_rows * pre_splits;
     return kErrBytes + (size_t)rows * ((size_t)head_dim * 4 + 8) + 64;
 }
 
@@ -341,7 +348,7 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
         return wa > wc;
     });
 
-    // ---- split size for decode-class requests
+    // ---- KV split size, common to every split request
     const int sms = num_sms();
     int split = env_int("PKV_SPLIT_TOKENS", 0);
     const bool use_fma = env_int("PKV_ATTN_CUDA_CORE", 0) != 0;    // CUDA-core kernels instead of the staged MMA ones
@@ -353,17 +360,33 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
     }
     if (split % bs) split += bs - split % bs;
     auto splits_of = [&](int32_t L, int sp) { return L <= 0 ? 1 : (L + sp - 1) / sp; };
+    // Prefill-class tiles are split over keys as well when the batch has too
+    // few of them to fill the GPU (small, latency-bound steps): every tile of
+    // such a request gets the request's number of splits.
+    const int tile = use_fma ? kDecodeRows / g : (mma_prefill_rows() / g > 0 ? mma_prefill_rows() / g : 1);
+    int64_t pre_ctas = 0;
+    for (int32_t r : pre) pre_ctas += (int64_t)((qsl_h[r + 1] - qsl_h[r] + tile - 1) / tile) * hkv;
+    // Measured on the 48-request engine step it costs more (extra CTAs and a
+    // combine on the critical path) than it saves, so it is opt-in.
+    const bool pre_split = !use_fma && !pre.empty() && pre_ctas < 2 * (int64_t)sms && env_int("PKV_PREFILL_SPLIT", 0);
     // every split request keeps S * t * hq partial rows; grow the split until they fit
+    auto partial_rows = [&](int sp, bool *too_many) {
+        size_t rows = 0;
+        auto add = [&](int32_t r) {
+            int32_t S = splits_of(sl_h[r], sp);
+            if (S > kMaxSplits) *too_many = true;
+            if (S > 1) rows += (size_t)S * (qsl_h[r + 1] - qsl_h[r]) * hq;
+        };
+        for (int32_t r : dec) add(r);
+        if (pre_split)
+            for (int32_t r : pre) add(r);
+        return rows;
+    };
     const size_t row_bytes = (size_t)d * 4 + 8;
     const size_t avail = workspace_bytes - kErrBytes;
     for (;;) {
-        size_t rows = 0;
         bool too_many = false;
-        for (int32_t r : dec) {
-            int32_t S = splits_of(sl_h[r], split);
-            if (S > kMaxSplits) too_many = true;
-            if (S > 1) rows += (size_t)S * (qsl_h[r + 1] - qsl_h[r]) * hq;
-        }
+        const size_t rows = partial_rows(split, &too_many);
         if (!too_many && rows * row_bytes + 64 <= avail) break;
         if (split >= seen_l) break;                              // nothing is split any more
         split *= 2;
@@ -389,18 +412,16 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
     p.scale_log2 = sc * 1.4426950408889634f;
     p.err = reinterpret_cast<uint32_t *>(ws);
     // partial rows: first all o rows, then the (m, l) pairs
-    size_t total_rows = 0;
-    for (int32_t r : dec) {
-        int32_t S = splits_of(sl_h[r], split);
-        if (S > 1) total_rows += (size_t)S * (qsl_h[r + 1] - qsl_h[r]) * hq;
-    }
+    bool unused = false;
+    const size_t total_rows = partial_rows(split, &unused);
     p.part_o = reinterpret_cast<float *>(ws + kErrBytes);
     p.part_ml = reinterpret_cast<float2 *>(ws + kErrBytes + ((total_rows * d * 4 + 15) / 16) * 16);
 
     // ---- decode-class work runs on a side stream, concurrently with the
     // prefill kernels, when both are present: its CTAs fill the SMs that the
-    // prefill leaves idle (its last wave, or a small batch's spare SMs).  Fork and join with events, so the
-    // caller's stream order (and CUDA-graph capture) is preserved.
+    // prefill leaves idle (its last wave, or a small batch's spare SMs).
+    // Fork and join with events, so the caller's stream order (and CUDA-graph
+    // capture) is preserved.
     cudaStream_t dstream = stream;
     SideStream *side = nullptr;
     const bool fork = !dec.empty() && (!tcp.empty() || !pre.empty()) && !env_int("PKV_NO_OVERLAP", 0);
@@ -416,8 +437,10 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
         }
         dstream = side->stream;
     }
+    bool joined = !fork;
     auto join = [&]() -> cudaError_t {
-        if (!fork) return cudaSuccess;
+        if (joined) return cudaSuccess;
+        joined = true;
         cudaError_t e = cudaEventRecord(side->join, side->stream);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, side->join, 0);
         side->mu.unlock();
@@ -450,9 +473,42 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
     }
 
     // ---- decode-class launches (chunks of kPlanMax requests)
-    std::vector<int32_t> combine_reqs, combine_off;
-    int combine_max_rows = 0;
+    struct CombineSet {
+        std::vector<int32_t> reqs, offs;
+        int max_rows = 0;
+    };
+    CombineSet dec_combine, pre_combine;
     size_t part_cursor = 0;
+    auto take_partials = [&](CombineSet &set, int32_t r, int32_t S) -> int32_t {
+        if (S <= 1) return -1;
+        const int32_t t = qsl_h[r + 1] - qsl_h[r];
+        const int32_t off = (int32_t)part_cursor;
+        set.reqs.push_back(r);
+        set.offs.push_back(off);
+        part_cursor += (size_t)S * t * hq;
+        if (t * hq > set.max_rows) set.max_rows = t * hq;
+        return off;
+    };
+    // merge the split partials of one set of requests on `st`
+    auto launch_combines = [&](const CombineSet &set, cudaStream_t st) -> cudaError_t {
+        for (size_t c0 = 0; c0 < set.reqs.size(); c0 += kPlanMax) {
+            WorkList wl;
+            memset(&wl, 0, sizeof wl);
+            wl.mode = kModeDecode;
+            wl.split_tokens = split;
+            size_t c1 = c0 + kPlanMax < set.reqs.size() ? c0 + kPlanMax : set.reqs.size();
+            for (size_t x = c0; x < c1; x++) {
+                int li = wl.n++;
+                wl.req[li] = set.reqs[x];
+                wl.part_off[li] = set.offs[x];
+                wl.item_off[li] = li;
+            }
+            wl.item_off[wl.n] = wl.n;
+            cudaError_t e = launch_attn_combine(p, wl, d, set.max_rows, st);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    };
     for (size_t c0 = 0; c0 < dec.size(); c0 += kPlanMax) {
         WorkList wl;
         memset(&wl, 0, sizeof wl);
@@ -468,14 +524,7 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
             int li = wl.n++;
             wl.req[li] = r;
             wl.item_off[li] = items;
-            wl.part_off[li] = -1;
-            if (S > 1) {
-                wl.part_off[li] = (int32_t)part_cursor;
-                combine_reqs.push_back(r);
-                combine_off.push_back((int32_t)part_cursor);
-                part_cursor += (size_t)S * t * hq;
-                if (t * hq > combine_max_rows) combine_max_rows = t * hq;
-            }
+            wl.part_off[li] = take_partials(dec_combine, r, S);
             items += S;
             if (sl_h[r] > 0 && t * g > rows) rows = t * g;
         }
@@ -487,45 +536,31 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
             return cuda_fail(e, "decode attention launch");
         }
     }
-    // ---- combine split partials (same stream as the decode kernels)
-    for (size_t c0 = 0; c0 < combine_reqs.size(); c0 += kPlanMax) {
-        WorkList wl;
-        memset(&wl, 0, sizeof wl);
-        wl.mode = kModeDecode;
-        wl.split_tokens = split;
-        size_t c1 = c0 + kPlanMax < combine_reqs.size() ? c0 + kPlanMax : combine_reqs.size();
-        for (size_t x = c0; x < c1; x++) {
-            int li = wl.n++;
-            wl.req[li] = combine_reqs[x];
-            wl.part_off[li] = combine_off[x];
-            wl.item_off[li] = li;
-        }
-        wl.item_off[wl.n] = wl.n;
-        cudaError_t e = launch_attn_combine(p, wl, d, combine_max_rows, dstream);
-        if (e != cudaSuccess) {
-            join();
-            return cuda_fail(e, "split combine launch");
-        }
+
+    if (cudaError_t e = launch_combines(dec_combine, dstream); e != cudaSuccess) {
+        join();
+        return cuda_fail(e, "split combine launch");
     }
 
-    // ---- prefill-class launches
-    const int tile = use_fma ? kDecodeRows / g : (mma_prefill_rows() / g > 0 ? mma_prefill_rows() / g : 1);
+    // ---- prefill-class launches (tiles of `tile` tokens, split over keys
+    // when pre_split)
     for (size_t c0 = 0; c0 < pre.size(); c0 += kPlanMax) {
         WorkList wl;
         memset(&wl, 0, sizeof wl);
         wl.mode = kModePrefill;
-        wl.split_tokens = 0;
+        wl.split_tokens = pre_split ? split : 0;
         wl.tile_tokens = tile;
         int items = 0;
         size_t c1 = c0 + kPlanMax < pre.size() ? c0 + kPlanMax : pre.size();
         for (size_t x = c0; x < c1; x++) {
             int32_t r = pre[x];
             int32_t t = qsl_h[r + 1] - qsl_h[r];
+            const int32_t S = pre_split ? splits_of(sl_h[r], split) : 1;
             int li = wl.n++;
             wl.req[li] = r;
             wl.item_off[li] = items;
-            wl.part_off[li] = -1;
-            items += (t + tile - 1) / tile;
+            wl.part_off[li] = take_partials(pre_combine, r, S);
+            items += ((t + tile - 1) / tile) * S;
         }
         wl.item_off[wl.n] = items;
         cudaError_t e = use_fma ? launch_attn_fma(p, wl, d, kDecodeRows, items, stream)
@@ -535,7 +570,15 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
             return cuda_fail(e, "prefill attention launch");
         }
     }
+    if (part_cursor > (size_t)INT32_MAX) {
+        join();
+        return PKV_ERR_WORKSPACE;
+    }
 
+    if (cudaError_t e = launch_combines(pre_combine, stream); e != cudaSuccess) {
+        join();
+        return cuda_fail(e, "split combine launch");
+    }
     cudaError_t ej = join();
     if (ej != cudaSuccess) return cuda_fail(ej, "join");
     return PKV_OK;

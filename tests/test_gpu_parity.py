@@ -117,17 +117,23 @@ def test_long_chunks_tensor_core_path(disable_tc, monkeypatch):
     assert pkv.read_device_error(dev.ws) == 0
 
 
-@pytest.mark.parametrize("overlap", [True, False])
-def test_mixed_step_side_stream_and_cuda_graph(overlap, monkeypatch):
-    """Decodes next to long prefill chunks: the decode kernels run on a forked
-    side stream (or, with PKV_NO_OVERLAP=1, on the caller's stream).  The step
-    is also captured in a CUDA graph and replayed; every result matches the
-    oracle."""
-    if not overlap:
-        monkeypatch.setenv("PKV_NO_OVERLAP", "1")
+def _mixed_spec():
     reqs = [Req(3000, 512, list(range(0, 220))), Req(0, 300, list(range(220, 239)))]
     reqs += [Req(700 + 97 * i, 1, list(range(239 + 111 * i, 239 + 111 * (i + 1)))) for i in range(12)]
-    spec = Spec("mixed", reqs, 32, 8, 128, 16, 1600, 1 / math.sqrt(128), 23)
+    return Spec("mixed", reqs, 32, 8, 128, 16, 1600, 1 / math.sqrt(128), 23)
+
+
+@pytest.mark.parametrize("shape", ["long-chunks", "engine-step"])
+@pytest.mark.parametrize("overlap", [True, False])
+def test_mixed_step_side_stream_and_cuda_graph(overlap, shape, monkeypatch):
+    """Decodes next to prefill chunks: the decode kernels run on a forked side
+    stream (or, with PKV_NO_OVERLAP=1, on the caller's stream); in the small
+    engine step the short prefill tiles are split over keys and all split
+    partials are merged by one combine launch.  The step is also captured in
+    a CUDA graph and replayed; every result matches the oracle."""
+    if not overlap:
+        monkeypatch.setenv("PKV_NO_OVERLAP", "1")
+    spec = _mixed_spec() if shape == "long-chunks" else config_spec(2)
     b = make_batch(spec, device="cpu")
     dev = DeviceStep(b)
     dev.step()
@@ -169,6 +175,20 @@ def test_programmatic_launch_and_padding_only_decodes(pdl, monkeypatch):
         oracle_write(ref)
         assert_close(dev.out, oracle_full(ref), "padding-only decodes")
         assert dev.out[0].abs().sum().item() == 0 and dev.out[-1].abs().sum().item() == 0
+
+
+@pytest.mark.parametrize("prefill_split", [False, True])
+def test_engine_step_prefill_split_toggle(prefill_split, monkeypatch):
+    """The small engine step with and without key splits of its short prefill
+    tiles (PKV_PREFILL_SPLIT=1)."""
+    if prefill_split:
+        monkeypatch.setenv("PKV_PREFILL_SPLIT", "1")
+    b = make_batch(config_spec(2), device="cpu")
+    dev = DeviceStep(b)
+    dev.step()
+    ref = cpu_copy(b)
+    oracle_write(ref)
+    assert_close(dev.out, oracle_full(ref), "engine step")
 
 
 @pytest.mark.parametrize("split", [256, 512, 4096])
