@@ -20,10 +20,20 @@
  *    [head_dim] ("Attention over the pool": slot-major rows).  Its last
  *    block is the scratch block that padding rows write into; the block
  *    manager never hands it out.  num_blocks_total counts it.
- *  - A device error word (uint32_t) collects bounds violations found on the
- *    device: PKV_DEVERR_SLOT (a slot past the pool) and PKV_DEVERR_BLOCK
- *    (a block id outside [0, num_blocks_total)).  The access is skipped, the
- *    bit is OR-ed in, and nothing traps.  The word is sticky until cleared.
+ *  - A device error word (uint32_t) collects violations found on the
+ *    device: PKV_DEVERR_SLOT (a slot past the pool), PKV_DEVERR_BLOCK (a
+ *    block id outside [0, num_blocks_total)), PKV_DEVERR_TIMEOUT (a bounded
+ *    pipeline wait gave up) and PKV_DEVERR_META (device metadata that
+ *    disagrees with its host copy).  The access is skipped, the bit is OR-ed
+ *    in, and nothing traps.  The word is sticky until cleared.
+ *  - Kernels are launched as programmatic dependents (PDL) of the kernel
+ *    before them on `stream` (set PKV_NO_PDL=1 in the environment to turn
+ *    this off).  pkv_paged_kv_write reads nothing before its grid-dependency
+ *    wait and releases its dependents only after it.  The attention kernels
+ *    read q, query_start_loc, seq_lens and block_table before that wait (only
+ *    the pool rows wait for it), so the kernel before them on the stream must
+ *    either be pkv_paged_kv_write or not release its dependents early while
+ *    it still writes those inputs (kernels that do not use PDL never do).
  *  - Every call validates its host-visible arguments first and returns an
  *    error status without enqueuing anything when they are invalid.
  */
@@ -47,8 +57,11 @@ typedef enum pkv_status {
     PKV_ERR_DEVICE_BOUNDS = 5   /* pkv_read_device_error found bounds violations */
 } pkv_status;
 
-#define PKV_DEVERR_SLOT  1u     /* paged_kv_write: slot >= num_blocks_total * block_size */
-#define PKV_DEVERR_BLOCK 2u     /* attention: a block id outside [0, num_blocks_total) */
+#define PKV_DEVERR_SLOT    1u   /* paged_kv_write: slot >= num_blocks_total * block_size */
+#define PKV_DEVERR_BLOCK   2u   /* attention: a block id outside [0, num_blocks_total) */
+#define PKV_DEVERR_TIMEOUT 4u   /* attention: a pipeline wait gave up (about 2 s); its rows are not written */
+#define PKV_DEVERR_META    8u   /* attention: query_start_loc / seq_lens on the device differ from the host copies */
+#define PKV_DEVERR_COUNTER 16u  /* attention: a split counter in the workspace was not zero (workspace not zero-filled) */
 
 /* Static description of a status code. */
 const char *pkv_status_string(pkv_status status);
@@ -109,7 +122,11 @@ pkv_status pkv_paged_kv_write(const void *k, const void *v, void *k_cache, void 
  * over KV freely for any batch within the given maxima.  A smaller
  * workspace (at least PKV_WORKSPACE_MIN_BYTES) is accepted: the planner
  * then splits less.  The workspace holds the device error word (first 256
- * bytes) and fp32 split-KV partials.
+ * bytes), then — when it has room for them (64 KiB) — the split counters of
+ * the combines that run inside the attention kernels, then fp32 split-KV
+ * partials.  Zero-fill a workspace once before its first use: every call
+ * leaves the counters zero again.  Use one workspace at one size, on one
+ * stream at a time.
  */
 #define PKV_WORKSPACE_MIN_BYTES 256
 size_t pkv_attention_workspace_bytes(int32_t max_num_reqs, int32_t max_num_tokens,
@@ -133,7 +150,9 @@ size_t pkv_attention_workspace_bytes(int32_t max_num_reqs, int32_t max_num_token
  *                     blocks of each request in logical order
  *   query_start_loc_host, seq_lens_host
  *                     host copies of the two arrays above, used to plan the
- *                     launches without reading device memory
+ *                     launches without reading device memory; the kernels
+ *                     take each request's rows and context length from them
+ *                     and flag PKV_DEVERR_META where the device arrays differ
  *   max_query_len, max_seq_len
  *                     maxima of the host arrays (validated)
  *   scale             softmax scale; <= 0 selects 1/sqrt(head_dim)

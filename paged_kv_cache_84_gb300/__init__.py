@@ -16,13 +16,16 @@ import torch
 __all__ = [
     "PkvError", "load", "paged_kv_write", "ragged_paged_attention", "attention_workspace_bytes",
     "make_workspace", "read_device_error", "clear_device_error", "launch_count", "LIB_PATH",
-    "DEVERR_SLOT", "DEVERR_BLOCK", "WORKSPACE_MIN_BYTES", "profile_start", "profile_stop",
+    "DEVERR_SLOT", "DEVERR_BLOCK", "DEVERR_TIMEOUT", "DEVERR_META", "DEVERR_COUNTER", "WORKSPACE_MIN_BYTES", "profile_start", "profile_stop",
     "plan_request_kernels", "CLASS_NAMES",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpkv.so")
 DEVERR_SLOT = 1
 DEVERR_BLOCK = 2
+DEVERR_TIMEOUT = 4
+DEVERR_META = 8
+DEVERR_COUNTER = 16
 WORKSPACE_MIN_BYTES = 256
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape or alignment",

@@ -58,8 +58,9 @@ __global__ void __launch_bounds__(kFmaThreads) attn_fma_kernel(AttnParams p,
     const int li = find_listed(wl, blockIdx.x);
     const int local = blockIdx.x - wl.item_off[li];
     const int r = wl.req[li];
-    const int b = p.qsl[r], t = p.qsl[r + 1] - b, L = p.seq_lens[r];
+    const int b = wl.qb[li], t = wl.qt[li], L = wl.len[li];
     const int g = p.group;
+    if (tid == 0 && local == 0 && kh == 0) check_meta(p, wl, li);
 
     if (L == 0 || t == 0) {                       // padding request: its rows are zero
         for (int idx = tid; idx < t * g * D; idx += kFmaThreads) {
@@ -307,8 +308,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnParams p,
 {
     constexpr int EPL = FmaShape<D>::EPL;
     const int li = blockIdx.x;
-    const int r = wl.req[li];
-    const int b = p.qsl[r], t = p.qsl[r + 1] - b, L = p.seq_lens[r];
+    const int b = wl.qb[li], t = wl.qt[li], L = wl.len[li];
     const int S = (L + wl.split_tokens - 1) / wl.split_tokens;
     const int rows = t * p.hq;
     const int lane = threadIdx.x & 31;

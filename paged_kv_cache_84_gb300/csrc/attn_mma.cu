@@ -101,6 +101,161 @@ __device__ __forceinline__ void block_pv(float (&o)[D / 8][4], const uint32_t (&
     }
 }
 
+// Split-KV combine of one (request, KV head) inside the CTA that completed
+// its last split.  Row (token i, head h) has S partials o_s (unnormalised),
+// m_s (running max, exp2 domain) and l_s (weight sum) at rows
+// base + s * t * hq + i * hq + h; the exact result is
+//   o = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s,   M = max_s m_s.
+// The partials of the other splits were written by other CTAs: they are read
+// through L2 (ld.global.cg), after the counter handshake's fences.
+template <int D>
+__device__ __forceinline__ void combine_in_cta(const AttnParams &p, size_t base, int b, int t, int kh, int g, int S,
+                                               int tid, int nthreads)
+{
+    constexpr int kChunks = D / 8;
+    const size_t rows = (size_t)t * p.hq;
+    for (int idx = tid; idx < t * g * kChunks; idx += nthreads) {
+        const int rr = idx / kChunks, e0 = (idx - rr * kChunks) * 8;
+        const int i = rr / g, h = kh * g + (rr - (rr / g) * g);
+        const size_t row = (size_t)i * p.hq + h;
+        // one pass, four splits at a time: their loads go out together, then
+        // each is merged into the running (M, ls, acc) with the usual rescale
+        float M = -INFINITY, ls = 0.f;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int s0 = 0; s0 < S; s0 += 4) {
+            float2 ml[4];
+            float4 x0[4], x1[4];
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                if (s0 + u < S) {
+                    const size_t prow = base + (size_t)(s0 + u) * rows + row;
+                    ml[u] = __ldcg(&p.part_ml[prow]);
+                    const float4 *src = reinterpret_cast<const float4 *>(p.part_o + prow * D + e0);
+                    x0[u] = __ldcg(src);
+                    x1[u] = __ldcg(src + 1);
+                } else {
+                    ml[u] = make_float2(-INFINITY, 0.f);
+                    x0[u] = x1[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                const float Mn = fmaxf(M, ml[u].x);
+                const float Ms = Mn == -INFINITY ? 0.f : Mn;
+                const float a = exp2f(M - Ms), w = exp2f(ml[u].x - Ms);   // 2^-inf = 0
+                ls = fmaf(ls, a, w * ml[u].y);
+                acc[0] = fmaf(acc[0], a, w * x0[u].x); acc[1] = fmaf(acc[1], a, w * x0[u].y);
+                acc[2] = fmaf(acc[2], a, w * x0[u].z); acc[3] = fmaf(acc[3], a, w * x0[u].w);
+                acc[4] = fmaf(acc[4], a, w * x1[u].x); acc[5] = fmaf(acc[5], a, w * x1[u].y);
+                acc[6] = fmaf(acc[6], a, w * x1[u].z); acc[7] = fmaf(acc[7], a, w * x1[u].w);
+                M = Mn;
+            }
+        }
+        const float inv = ls > 0.f ? 1.f / ls : 0.f;
+        uint4 v;
+        v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+        v.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+        v.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+        *reinterpret_cast<uint4 *>(p.out + ((size_t)(b + i) * p.hq + h) * D + e0) = v;
+    }
+}
+
+// Epilogue of both MMA kernels, run by the kConsumerWarps consumer warps
+// (named barrier 1).  Merges the KG key groups of each row tile through
+// shared memory (the ring is free by then), writes the CTA's rows as bf16
+// output or as fp32 split partials, and, for split decode rows whose combine
+// runs in the kernel (wl.cnt_off[li] >= 0), counts the finished splits of
+// (request, KV head): the CTA that finishes the last one combines them and
+// returns the counter to zero for the next call.  A CTA whose pipeline wait
+// gave up writes nothing but still counts, so counters stay consistent.
+template <int D, int KG>
+__device__ __forceinline__ void mma_epilogue(const AttnParams &p, const WorkList &wl, int li, int kh,
+                                             const float (&o)[D / 8][4], const float (&m)[2], const float (&l)[2],
+                                             bool alive, float *mo, float *mml, uint32_t *s_flags, int nr,
+                                             int i0, int split, bool partial, int b, int t, int L, int g)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int kRT = kConsumerWarps / KG;
+    constexpr int kThreads = kConsumerWarps * 32;
+    named_bar_sync(1, kThreads);                                  // every consumer is done with the ring
+    {
+        const int c = 2 * (lane & 3);
+#pragma unroll
+        for (int hr = 0; hr < 2; hr++) {
+            const int lr = (lane >> 2) + 8 * hr;
+#pragma unroll
+            for (int n = 0; n < D / 8; n++)
+                *reinterpret_cast<float2 *>(mo + (warp * 16 + lr) * D + n * 8 + c) = make_float2(o[n][2 * hr], o[n][2 * hr + 1]);
+            if ((lane & 3) == 0) {
+                mml[(warp * 16 + lr) * 2] = m[hr];
+                mml[(warp * 16 + lr) * 2 + 1] = l[hr];
+            }
+        }
+        if (!alive && lane == 0) s_flags[0] = 1u;
+    }
+    named_bar_sync(1, kThreads);
+    const bool ok = s_flags[0] == 0u;                            // the same in every consumer thread
+    // one item = 8 consecutive columns of one row: a 16-byte bf16 store (or
+    // two 16-byte fp32 stores for a partial)
+    constexpr int kChunks = D / 8;
+    for (int idx = threadIdx.x; ok && idx < nr * kChunks; idx += kThreads) {
+        const int rowc = idx / kChunks, e0 = (idx - rowc * kChunks) * 8;   // row within the CTA
+        const int rtile = rowc >> 4, lr = rowc & 15;
+        float M = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < KG; q++) M = fmaxf(M, mml[((rtile * KG + q) * 16 + lr) * 2]);
+        const float Ms = M == -INFINITY ? 0.f : M;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, ls = 0.f;
+#pragma unroll
+        for (int q = 0; q < KG; q++) {
+            const int wq = rtile * KG + q;
+            const float w = exp2f(mml[(wq * 16 + lr) * 2] - Ms);
+            ls = fmaf(w, mml[(wq * 16 + lr) * 2 + 1], ls);
+            const float4 *src = reinterpret_cast<const float4 *>(mo + (wq * 16 + lr) * D + e0);
+            const float4 x0 = src[0], x1 = src[1];
+            acc[0] = fmaf(w, x0.x, acc[0]); acc[1] = fmaf(w, x0.y, acc[1]);
+            acc[2] = fmaf(w, x0.z, acc[2]); acc[3] = fmaf(w, x0.w, acc[3]);
+            acc[4] = fmaf(w, x1.x, acc[4]); acc[5] = fmaf(w, x1.y, acc[5]);
+            acc[6] = fmaf(w, x1.z, acc[6]); acc[7] = fmaf(w, x1.w, acc[7]);
+        }
+        const int i = i0 + rowc / g, h = kh * g + rowc % g;
+        if (!partial) {
+            const float inv = ls > 0.f ? 1.f / ls : 0.f;
+            uint4 v;
+            v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+            v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+            v.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+            v.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+            *reinterpret_cast<uint4 *>(p.out + ((size_t)(b + i) * p.hq + h) * D + e0) = v;
+        } else {
+            const size_t orow = (size_t)wl.part_off[li] + ((size_t)split * t + i) * p.hq + h;
+            float4 *dst = reinterpret_cast<float4 *>(p.part_o + orow * D + e0);
+            dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+            if (e0 == 0) p.part_ml[orow] = make_float2(M, ls);
+        }
+    }
+    (void)kRT;
+    if (!partial || wl.cnt_off[li] < 0) return;
+    // ---- in-kernel split combine: count this split, the last one combines
+    const int S = (L + wl.split_tokens - 1) / wl.split_tokens;
+    uint32_t *cnt = p.counters + (size_t)(wl.cnt_off[li] + kh) * kCounterStride;
+    named_bar_sync(1, kThreads);                                  // every partial store of the CTA is issued
+    if (threadIdx.x == 0) {
+        __threadfence();                                          // release them (cumulative over the barrier)
+        const uint32_t old = atomicAdd(cnt, 1u);
+        if (old >= (uint32_t)S) atomicOr(p.err, kDevErrCounter); // the workspace was not zero-filled
+        const bool last = old + 1u == (uint32_t)S;
+        if (last) __threadfence();                                // acquire the other splits' partials
+        s_flags[1] = last ? 1u : 0u;
+    }
+    named_bar_sync(1, kThreads);
+    if (s_flags[1] == 0u) return;
+    combine_in_cta<D>(p, (size_t)wl.part_off[li], b, t, kh, g, S, threadIdx.x, kThreads);
+    if (threadIdx.x == 0) atomicExch(cnt, 0u);                    // ready for the next call
+}
+
 template <int D, int KG, int NB>
 __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, const __grid_constant__ WorkList wl,
                                                                const __grid_constant__ CUtensorMap kmap,
@@ -123,13 +278,14 @@ __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, con
     const int li = find_listed(wl, blockIdx.x);
     const int local = blockIdx.x - wl.item_off[li];
     const int r = wl.req[li];
-    const int b = p.qsl[r], t = p.qsl[r + 1] - b, L = p.seq_lens[r];
+    const int b = wl.qb[li], t = wl.qt[li], L = wl.len[li];
     const int g = p.group;
 
     if (L == 0 || t == 0) {                                       // padding request: zero rows
         // Wait like every other CTA: this grid then never completes before the
         // grids it follows, which keeps later programmatic waits transitive.
         pdl_wait();
+        if (threadIdx.x == 0 && local == 0 && kh == 0) check_meta(p, wl, li);
         for (int idx = threadIdx.x; idx < t * g * D; idx += kMmaThreads) {
             const int rr = idx / D, e = idx - rr * D;
             p.out[((size_t)(b + rr / g) * p.hq + kh * g + rr % g) * D + e] = __float2bfloat16(0.f);
@@ -164,11 +320,13 @@ __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, con
     const int blk0 = k_begin >> 4;
     const int nblk = max(0, ((k_end + 15) >> 4) - blk0);
 
+    __shared__ uint32_t s_flags[2];                               // epilogue: a wait gave up; last split
     if (threadIdx.x == 0) {
         for (int s = 0; s < R; s++) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), C::kRT);                      // the row tiles that read a block
         }
+        s_flags[0] = s_flags[1] = 0u;
         fence_mbar_init();
     }
     __syncthreads();
@@ -180,10 +338,12 @@ __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, con
             prefetch_tmap(&vmap);
         }
         const int32_t *bt = p.block_table + (size_t)r * p.bt_stride + blk0;
+        // The block table is not written by the step's K/V scatter: read the
+        // first 32 block ids while that kernel may still be running.
+        int ids = lane < nblk ? __ldg(bt + lane) : 0, issued = 0;
         pdl_wait();                                               // the step's K/V rows are in the pool
-        int ids = 0, issued = 0;
         for (int i = 0; i < nblk; i++) {
-            if ((i & 31) == 0) ids = (i + lane < nblk) ? __ldg(bt + i + lane) : 0;
+            if ((i & 31) == 0 && i > 0) ids = (i + lane < nblk) ? __ldg(bt + i + lane) : 0;
             const int s = i % R;
             bool ok = true;
             if (i >= R) ok = mbar_wait(empty_bar(s), ((i / R) - 1) & 1, p.err);
@@ -212,6 +372,7 @@ __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, con
         if (issued < nblk && lane == 0) {
             for (int i = issued > R ? issued - R : 0; i < issued; i++) mbar_wait(full_bar(i % R), (i / R) & 1, p.err);
         }
+        if (lane == 0 && local == 0 && kh == 0) check_meta(p, wl, li);
         return;
     }
 
@@ -328,64 +489,14 @@ __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, con
         }
     }
     pdl_launch_dependents();                                      // a combine kernel may start launching
-
 #pragma unroll
     for (int hr = 0; hr < 2; hr++) {
         l[hr] += __shfl_xor_sync(0xffffffffu, l[hr], 1);
         l[hr] += __shfl_xor_sync(0xffffffffu, l[hr], 2);
     }
-
-    // rows rA / rB -> (token, head) and the output or partial row
-    auto out_row = [&](int rr) -> size_t {
-        const int i = i0 + rr / g, h = kh * g + rr % g;
-        if (!partial) return (size_t)(b + i) * p.hq + h;
-        return (size_t)wl.part_off[li] + ((size_t)split * t + i) * p.hq + h;
-    };
-
-    // merge the KG key groups of each row tile through shared memory
-    named_bar_sync(1, kConsumerWarps * 32);                       // every consumer is done with the ring
     float *mo = reinterpret_cast<float *>(ring_ptr);              // [warp][16][D]
     float *mml = mo + kConsumerWarps * 16 * D;                    // [warp][16][2]
-    {
-        const int c = 2 * (lane & 3);
-#pragma unroll
-        for (int hr = 0; hr < 2; hr++) {
-            const int lr = (lane >> 2) + 8 * hr;
-#pragma unroll
-            for (int n = 0; n < D / 8; n++)
-                *reinterpret_cast<float2 *>(mo + (warp * 16 + lr) * D + n * 8 + c) = make_float2(o[n][2 * hr], o[n][2 * hr + 1]);
-            if ((lane & 3) == 0) {
-                mml[(warp * 16 + lr) * 2] = m[hr];
-                mml[(warp * 16 + lr) * 2 + 1] = l[hr];
-            }
-        }
-    }
-    named_bar_sync(1, kConsumerWarps * 32);
-    if (!alive) return;
-    for (int idx = threadIdx.x; idx < C::kRT * 16 * D; idx += kConsumerWarps * 32) {
-        const int rowc = idx / D, e = idx - rowc * D;            // row within the CTA
-        if (rowc >= nr) continue;
-        const int rtile = rowc >> 4, lr = rowc & 15;
-        float M = -INFINITY;
-#pragma unroll
-        for (int q = 0; q < KG; q++) M = fmaxf(M, mml[((rtile * KG + q) * 16 + lr) * 2]);
-        const float Ms = M == -INFINITY ? 0.f : M;
-        float acc = 0.f, ls = 0.f;
-#pragma unroll
-        for (int q = 0; q < KG; q++) {
-            const int wq = rtile * KG + q;
-            const float sc = exp2f(mml[(wq * 16 + lr) * 2] - Ms);
-            acc = fmaf(sc, mo[(wq * 16 + lr) * D + e], acc);
-            ls = fmaf(sc, mml[(wq * 16 + lr) * 2 + 1], ls);
-        }
-        const size_t orow = out_row(rowc);
-        if (!partial) {
-            p.out[orow * D + e] = __float2bfloat16(ls > 0.f ? acc / ls : 0.f);
-        } else {
-            p.part_o[orow * D + e] = acc;
-            if (e == 0) p.part_ml[orow] = make_float2(M, ls);
-        }
-    }
+    mma_epilogue<D, KG>(p, wl, li, kh, o, m, l, alive, mo, mml, s_flags, nr, i0, split, partial, b, t, L, g);
 }
 
 // ---------------------------------------------------------------- streaming decode
@@ -429,11 +540,12 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
     const int li = find_listed(wl, blockIdx.x);
     const int local = blockIdx.x - wl.item_off[li];
     const int r = wl.req[li];
-    const int b = p.qsl[r], t = p.qsl[r + 1] - b, L = p.seq_lens[r];
+    const int b = wl.qb[li], t = wl.qt[li], L = wl.len[li];
     const int g = p.group;
 
     if (L == 0 || t == 0) {                                       // padding request: zero rows
         pdl_wait();                                               // keeps later programmatic waits transitive
+        if (threadIdx.x == 0 && local == 0 && kh == 0) check_meta(p, wl, li);
         for (int idx = threadIdx.x; idx < t * g * D; idx += kMmaThreads) {
             const int rr = idx / D, e = idx - rr * D;
             p.out[((size_t)(b + rr / g) * p.hq + kh * g + rr % g) * D + e] = __float2bfloat16(0.f);
@@ -461,11 +573,13 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
     const int nblk = ((k_end + 15) >> 4) - blk0;
     const int iters = (nblk + KG - 1) / KG;
 
+    __shared__ uint32_t s_flags[2];                               // epilogue: a wait gave up; last split
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; s++) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), kConsumerWarps);
         }
+        s_flags[0] = s_flags[1] = 0u;
         fence_mbar_init();
     }
     __syncthreads();
@@ -477,11 +591,11 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
             prefetch_tmap(&vmap);
         }
         const int32_t *bt = p.block_table + (size_t)r * p.bt_stride + blk0;
+        int ids = lane < nblk ? __ldg(bt + lane) : 0, issued = 0;   // not written by the scatter
         pdl_wait();                                               // the step's K/V rows are in the pool
-        int ids = 0, issued = 0;
         for (int it = 0; it < iters; it++) {
             const int base = it * KG;
-            if ((base & 31) == 0) ids = (base + lane < nblk) ? __ldg(bt + base + lane) : 0;
+            if ((base & 31) == 0 && base > 0) ids = (base + lane < nblk) ? __ldg(bt + base + lane) : 0;
             const int s = it % S;
             bool ok = true;
             if (it >= S) ok = mbar_wait(empty_bar(s), ((it / S) & 1) ^ 1, p.err);
@@ -513,6 +627,7 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
             for (int it = issued > S ? issued - S : 0; it < issued; it++)
                 mbar_wait(full_bar(it % S), (it / S) & 1, p.err);
         }
+        if (lane == 0 && local == 0 && kh == 0) check_meta(p, wl, li);
         return;
     }
 
@@ -622,81 +737,9 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
         l[hr] += __shfl_xor_sync(0xffffffffu, l[hr], 1);
         l[hr] += __shfl_xor_sync(0xffffffffu, l[hr], 2);
     }
-
-    // rows rA / rB -> (token, head) and the output or partial row
-    auto out_row = [&](int rr) -> size_t {
-        const int i = i0 + rr / g, h = kh * g + rr % g;
-        if (!partial) return (size_t)(b + i) * p.hq + h;
-        return (size_t)wl.part_off[li] + ((size_t)split * t + i) * p.hq + h;
-    };
-
-    if constexpr (KG == 1) {
-        if (!alive) return;
-#pragma unroll
-        for (int hr = 0; hr < 2; hr++) {
-            const int rr = hr ? rB : rA;
-            if (rr >= nr) continue;
-            const size_t orow = out_row(rr);
-            const int c = 2 * (lane & 3);
-            if (!partial) {
-                const float inv = l[hr] > 0.f ? 1.f / l[hr] : 0.f;
-                uint32_t *dst = reinterpret_cast<uint32_t *>(p.out + orow * D);
-#pragma unroll
-                for (int n = 0; n < D / 8; n++) dst[(n * 8 + c) / 2] = pack_bf16x2(o[n][2 * hr] * inv, o[n][2 * hr + 1] * inv);
-            } else {
-                float2 *dst = reinterpret_cast<float2 *>(p.part_o + orow * D);
-#pragma unroll
-                for (int n = 0; n < D / 8; n++) dst[(n * 8 + c) / 2] = make_float2(o[n][2 * hr], o[n][2 * hr + 1]);
-                if ((lane & 3) == 0) p.part_ml[orow] = make_float2(m[hr], l[hr]);
-            }
-        }
-    } else {
-        // merge the KG key groups of each row tile through shared memory
-        named_bar_sync(1, kConsumerWarps * 32);                   // every consumer is done with the ring
-        float *mo = reinterpret_cast<float *>(ring_ptr);          // [warp][16][D]
-        float *mml = mo + kConsumerWarps * 16 * D;                // [warp][16][2]
-        const int c = 2 * (lane & 3);
-#pragma unroll
-        for (int hr = 0; hr < 2; hr++) {
-            const int lr = (lane >> 2) + 8 * hr;
-#pragma unroll
-            for (int n = 0; n < D / 8; n++) {
-                mo[(warp * 16 + lr) * D + n * 8 + c] = o[n][2 * hr];
-                mo[(warp * 16 + lr) * D + n * 8 + c + 1] = o[n][2 * hr + 1];
-            }
-            if ((lane & 3) == 0) {
-                mml[(warp * 16 + lr) * 2] = m[hr];
-                mml[(warp * 16 + lr) * 2 + 1] = l[hr];
-            }
-        }
-        named_bar_sync(1, kConsumerWarps * 32);
-        if (!alive) return;
-        const int tid = threadIdx.x;
-        for (int idx = tid; idx < C::kRT * 16 * D; idx += kConsumerWarps * 32) {
-            const int rowc = idx / D, e = idx - rowc * D;        // row within the CTA
-            if (rowc >= nr) continue;
-            const int rtile = rowc >> 4, lr = rowc & 15;
-            float M = -INFINITY;
-#pragma unroll
-            for (int q = 0; q < KG; q++) M = fmaxf(M, mml[((rtile * KG + q) * 16 + lr) * 2]);
-            const float Ms = M == -INFINITY ? 0.f : M;
-            float acc = 0.f, ls = 0.f;
-#pragma unroll
-            for (int q = 0; q < KG; q++) {
-                const int wq = rtile * KG + q;
-                const float sc = exp2f(mml[(wq * 16 + lr) * 2] - Ms);
-                acc = fmaf(sc, mo[(wq * 16 + lr) * D + e], acc);
-                ls = fmaf(sc, mml[(wq * 16 + lr) * 2 + 1], ls);
-            }
-            const size_t orow = out_row(rowc);
-            if (!partial) {
-                p.out[orow * D + e] = __float2bfloat16(ls > 0.f ? acc / ls : 0.f);
-            } else {
-                p.part_o[orow * D + e] = acc;
-                if (e == 0) p.part_ml[orow] = make_float2(M, ls);
-            }
-        }
-    }
+    float *mo = reinterpret_cast<float *>(ring_ptr);              // [warp][16][D]
+    float *mml = mo + kConsumerWarps * 16 * D;                    // [warp][16][2]
+    mma_epilogue<D, KG>(p, wl, li, kh, o, m, l, alive, mo, mml, s_flags, nr, i0, split, partial, b, t, L, g);
 }
 
 // ---------------------------------------------------------------- host side

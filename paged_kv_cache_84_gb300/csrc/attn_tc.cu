@@ -1,5 +1,5 @@
 // Ragged paged attention for prefill chunks on the 5th-generation tensor
-// cores (tcgen05, accumulators in tensor memory), head_dim 128.
+// cores (tcgen05, accumulators in tensor memory), head_dim 48, 64 or 128.
 //
 // One CTA = (listed request, KV head, pair of 128-row query tiles).  A row
 // is a (token, query head) pair of the KV head's group: 128/g consecutive
@@ -24,10 +24,19 @@
 //               max, then exp2 in the log2 domain), P written back as bf16
 //               pairs over the first half of the S columns, where the PV MMA
 //               reads it as its A operand.  The running max only moves (and O
-//               is rescaled in TMEM) when it grows by more than 2^8.
+//               is rescaled in TMEM) when it grows by more than 2^8.  A CTA
+//               with a single tile splits each row between warps w and w + 4,
+//               one per 64-column half of S (and of O): they swap half-row
+//               maxima and sums through shared memory, and each writes its
+//               half of P over its own first 32 columns ([0,32) and [64,96)),
+//               and S alternates between two TMEM buffers (the unused S_b
+//               columns), so the MMA of key tile j+1 overlaps tile j's softmax.
 // TMEM: S_a [0,128), S_b [128,256), O_a [256,384), O_b [384,512).
 // Shared memory (128-byte swizzle): Q_a, Q_b, K and V tiles as [128][64]
-// sub-tiles, K-major for Q and K, MN-major for V.
+// sub-tiles, K-major for Q and K, MN-major for V.  Head dims below 64 are
+// padded to 64 columns: the TMA box is 64 columns wide and fills the
+// columns past head_dim with zeros, which add nothing to Q K^T and give
+// zero output columns in P V that are not stored.
 #include <climits>
 #include <mutex>
 
@@ -39,14 +48,20 @@ namespace pkv {
 constexpr int kTcThreads = 384;
 constexpr int kTcRows = 128;          // query rows per tile (MMA M)
 constexpr int kTcKeys = 128;          // keys per tile (MMA N of S, K of PV)
-constexpr int kTcD = 128;
 constexpr int kSub = 16384;           // one [128][64] bf16 sub-tile
-constexpr int kTile = 2 * kSub;       // [128][128]
-constexpr int kQOff = 0;                              // Q_a, Q_b
-constexpr int kKOff = kQOff + 2 * kTile;              // 2 stages
-constexpr int kVOff = kKOff + 2 * kTile;              // 2 stages
-constexpr int kBarOff = kVOff + 2 * kTile;
-constexpr int kTcSmem = 1024 + kBarOff + 256;
+
+// Shared-memory layout for a padded head dim DP (64 or 128).
+template <int DP>
+struct TcCfg {
+    static constexpr int kHalves = DP / 64;            // 64-column sub-tiles per row
+    static constexpr int kTile = kHalves * kSub;        // [128][DP]
+    static constexpr int kQOff = 0;                     // Q_a, Q_b
+    static constexpr int kKOff = kQOff + 2 * kTile;     // 2 stages
+    static constexpr int kVOff = kKOff + 2 * kTile;     // 2 stages
+    static constexpr int kBarOff = kVOff + 2 * kTile;
+    static constexpr int kXOff = kBarOff + 256;        // softmax pair exchange: max [2][2][128], sum [2][128]
+    static constexpr int kSmem = 1024 + kXOff + 3 * 1024;
+};
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;  // move the running max only when it grows by more than this
 
@@ -58,7 +73,8 @@ enum TcBar {
     kBarPA = 7, kBarPB = 8,           // P of tile a / b written (4 warps each)
     kBarOA = 9, kBarOB = 10,          // PV of tile a / b done (also frees a V stage)
     kBarMmaDone = 11,
-    kNumTcBars = 12
+    kBarOFin = 12,                    // single tile: every PV done (one phase)
+    kNumTcBars = 13
 };
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
@@ -89,14 +105,15 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
         : "memory");
 }
 
-// Pass 1 of the softmax: max of the raw scores of this thread's S row (128
-// TMEM columns at ts); keys past qpos are masked when MASK.
-template <bool MASK>
+// Pass 1 of the softmax: max of the raw scores of NC columns of this
+// thread's S row (TMEM columns at ts, keys key0 ..); keys past qpos are
+// masked when MASK.
+template <bool MASK, int NC>
 __device__ __forceinline__ float tc_row_max(uint32_t ts, int key0, int qpos)
 {
     float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-    for (int c = 0; c < 4; c++) {
+    for (int c = 0; c < NC / 32; c++) {
         uint32_t v[32];
         tmem_ld32(ts + c * 32, v);
         tmem_ld_wait();
@@ -113,16 +130,16 @@ __device__ __forceinline__ float tc_row_max(uint32_t ts, int key0, int qpos)
     return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
 }
 
-// Pass 2: P = 2^(s * sl2 - ms) as bf16 pairs written over the first 64 S
-// columns (each 16-column chunk goes over columns already read); returns
-// this row's sum of P.
-template <bool MASK>
+// Pass 2: P = 2^(s * sl2 - ms) for NC columns at ts, as bf16 pairs written
+// over the first NC/2 of them (each 16-column chunk goes over columns
+// already read); returns this row's sum of P over them.
+template <bool MASK, int NC>
 __device__ __forceinline__ float tc_row_exp(uint32_t ts, int key0, int qpos, float sl2, float ms)
 {
     const uint64_t scale2 = f2_pack(sl2, sl2), neg2 = f2_pack(-ms, -ms);
     uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-    for (int c = 0; c < 8; c++) {
+    for (int c = 0; c < NC / 16; c++) {
         uint32_t v[16];
         tmem_ld16(ts + c * 16, v);
         tmem_ld_wait();
@@ -153,12 +170,62 @@ __device__ __forceinline__ float tc_row_exp(uint32_t ts, int key0, int qpos, flo
     return sum;
 }
 
+// O columns [32 c0, 32 (c0 + nc)) of this thread's TMEM row *= alpha.
+__device__ __forceinline__ void tc_rescale_cols(uint32_t to, int c0, int nc, float alpha)
+{
+#pragma unroll 1
+    for (int c = c0; c < c0 + nc; c++) {
+        uint32_t ov[32];
+        tmem_ld32(to + c * 32, ov);
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 32; k++) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * alpha);
+        tmem_st32(to + c * 32, ov);
+    }
+    tmem_st_wait();
+}
+
+// Store O columns [32 c0, 32 (c0 + nc)) of this thread's row (clipped to D)
+// as bf16, scaled by inv: row `row` of the tile is token tok0 + row / g,
+// query head kh * g + row % g.
+template <int D>
+__device__ __forceinline__ void tc_store_rows(const AttnParams &p, uint32_t to, int row, int nr, int tok0, int kh,
+                                              int g, float inv, int c0, int nc)
+{
+    const size_t orow = row < nr ? ((size_t)(tok0 + row / g) * p.hq + kh * g + row % g) * D : 0;
+#pragma unroll 1
+    for (int c = c0; c < c0 + nc; c++) {
+        if (c * 32 >= D) break;                                     // warp-uniform
+        uint32_t v[32];
+        tmem_ld32(to + c * 32, v);
+        tmem_ld_wait();
+        if (row < nr) {
+            uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow + c * 32);
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                if (c * 32 + q * 8 >= D) break;                     // padding columns are not stored
+                uint32_t w4[4];
+#pragma unroll
+                for (int e = 0; e < 4; e++)
+                    w4[e] = pack_bf16x2(__uint_as_float(v[q * 8 + 2 * e]) * inv,
+                                        __uint_as_float(v[q * 8 + 2 * e + 1]) * inv);
+                dst[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+        }
+    }
+}
+
+// DP: head dim padded to the 64-column sub-tile; D: head dim of q and out.
+template <int DP, int D>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, const __grid_constant__ WorkList wl,
                                                                 const __grid_constant__ CUtensorMap qmap,
                                                                 const __grid_constant__ CUtensorMap kmap,
                                                                 const __grid_constant__ CUtensorMap vmap,
                                                                 int64_t num_slots)
 {
+    using C = TcCfg<DP>;
+    constexpr int kTile = C::kTile, kQOff = C::kQOff, kKOff = C::kKOff, kVOff = C::kVOff, kBarOff = C::kBarOff;
+    constexpr int kHalves = C::kHalves;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sb = (raw + 1023u) & ~1023u;
@@ -170,7 +237,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, co
     const int kh = blockIdx.x;                                     // all KV heads of an item are adjacent
     const int li = find_listed(wl, blockIdx.y);
     const int r = wl.req[li];
-    const int b = p.qsl[r], t = p.qsl[r + 1] - b, L = p.seq_lens[r];
+    const int b = wl.qb[li], t = wl.qt[li], L = wl.len[li];
     const int g = p.group;
     const int tt = wl.tile_tokens;                                 // tokens per tile: 128 / g
     const int npairs = (t + 2 * tt - 1) / (2 * tt);
@@ -184,7 +251,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, co
     const int nblk = (k_end + 15) >> 4;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kNumTcBars; i++) mbar_init(bar(i), (i == kBarPA || i == kBarPB) ? 4u : 1u);
+        // P of tile a comes from 8 warps when a single tile splits its rows
+        for (int i = 0; i < kNumTcBars; i++)
+            mbar_init(bar(i), i == kBarPA ? (has_b ? 4u : 8u) : i == kBarPB ? 4u : 1u);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -198,19 +267,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, co
 
     if (warp == 0 || warp == 2) {
         // ------------------------------------------------------------ TMA producers
-        // warp 0 loads Q and the K tiles, warp 2 the V tiles.  A tile's 16
-        // boxes (8 blocks x 2 column halves) are issued by 16 lanes at once.
+        // warp 0 loads Q and the K tiles, warp 2 the V tiles.  A tile's
+        // 8 x kHalves boxes (8 blocks x its 64-column halves) are issued by
+        // as many lanes at once.
         const bool is_k = warp == 0;
         if (lane == 0) {
             if (is_k) {
                 prefetch_tmap(&qmap);
                 prefetch_tmap(&kmap);
                 mbar_arrive_expect_tx(bar(kBarQ), has_b ? 2 * kTile : kTile);
-                tma_load_3d(sb + kQOff, &qmap, bar(kBarQ), 0, kh * g, b + i0);
-                tma_load_3d(sb + kQOff + kSub, &qmap, bar(kBarQ), 64, kh * g, b + i0);
-                if (has_b) {
-                    tma_load_3d(sb + kQOff + kTile, &qmap, bar(kBarQ), 0, kh * g, b + i0 + tt);
-                    tma_load_3d(sb + kQOff + kTile + kSub, &qmap, bar(kBarQ), 64, kh * g, b + i0 + tt);
+#pragma unroll
+                for (int hf = 0; hf < kHalves; hf++) {
+                    tma_load_3d(sb + kQOff + hf * kSub, &qmap, bar(kBarQ), hf * 64, kh * g, b + i0);
+                    if (has_b) tma_load_3d(sb + kQOff + kTile + hf * kSub, &qmap, bar(kBarQ), hf * 64, kh * g, b + i0 + tt);
                 }
             } else {
                 prefetch_tmap(&vmap);
@@ -224,12 +293,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, co
         // barriers (their next completion needs a tile not loaded yet).
         const int done_bar = is_k ? (has_b ? kBarSB : kBarSA) : (has_b ? kBarOB : kBarOA);
         const int32_t *bt = p.block_table + (size_t)r * p.bt_stride;
-        const int bi = (lane >> 1) & 7, half = lane & 1;           // this lane's box (lanes 0..15)
+        // this lane's box (lanes 0 .. 8 * kHalves - 1): block bi, column half
+        const int bi = kHalves == 2 ? (lane >> 1) & 7 : lane & 7, half = kHalves == 2 ? lane & 1 : 0;
+        // the block table is not written by the step's K/V scatter: the first
+        // 32 block ids are read while that kernel may still be running
+        int ids = lane < nblk ? __ldg(bt + lane) : INT_MIN, issued = 0;
         pdl_wait();                                                // the step's K/V rows are in the pool
-        int ids = 0, issued = 0;
         for (int j = 0; j < nkt; j++) {
             const int st = j & 1;
-            if ((j & 3) == 0) {                                    // 32 block ids = 4 key tiles
+            if ((j & 3) == 0 && j > 0) {                           // 32 block ids = 4 key tiles
                 const int jb = j * 8 + lane;
                 ids = jb < nblk ? __ldg(bt + jb) : INT_MIN;
             }
@@ -238,18 +310,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, co
             int row = (int)num_slots;
             if (blk != INT_MIN) {
                 if (blk < 0 || blk >= p.nb_total) {
-                    if (is_k && lane < 16 && half == 0) atomicOr(p.err, 2u);
+                    if (is_k && lane < 8 * kHalves && half == 0) atomicOr(p.err, 2u);
                 } else {
                     row = blk * 16;
                 }
             }
             bool ok = true;
-            if (j >= 2) ok = mbar_wait(bar(done_bar), (j - 2) & 1, p.err);
+            // a single tile alternates S(j) between two TMEM buffers, each
+            // with its own barrier (kBarSA for even j, kBarSB for odd j)
+            if (j >= 2)
+                ok = (is_k && !has_b) ? mbar_wait(bar(kBarSA + (j & 1)), ((j - 2) >> 1) & 1, p.err)
+                                      : mbar_wait(bar(done_bar), (j - 2) & 1, p.err);
             if (!__all_sync(0xffffffffu, ok)) break;
             issued = j + 1;
             if (lane == 0) mbar_arrive_expect_tx(bar(full0 + st), kTile);
             __syncwarp();
-            if (lane < 16)
+            if (lane < 8 * kHalves)
                 tma_load_3d(ring + st * kTile + half * kSub + bi * 2048, map, bar(full0 + st), half * 64, kh, row);
             __syncwarp();
         }
@@ -258,17 +334,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, co
             for (int j = issued > 2 ? issued - 2 : 0; j < issued; j++)
                 mbar_wait(bar(full0 + (j & 1)), (j >> 1) & 1, p.err);
         }
+        if (!is_k && lane == 0 && kh == 0 && blockIdx.y == wl.item_off[li]) check_meta(p, wl, li);
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16(kTcRows, kTcKeys, false);
-            constexpr uint32_t idO = idesc_bf16(kTcRows, kTcD, true);
+            constexpr uint32_t idO = idesc_bf16(kTcRows, DP, true);
             const int ntile = has_b ? 2 : 1;
             auto issue_s = [&](int x, int j) {                     // S_x(j) = Q_x K_j^T
                 const uint32_t kbase = sb + kKOff + (j & 1) * kTile;
                 const uint32_t qbase = sb + kQOff + x * kTile;
 #pragma unroll
-                for (int kk = 0; kk < 8; kk++) {
+                for (int kk = 0; kk < DP / 16; kk++) {
                     const uint64_t ad = sdesc_sw128(qbase + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024);
                     const uint64_t bd = sdesc_sw128(kbase + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024);
                     tc_mma(tmem + x * 128, ad, bd, idS, kk > 0 ? 1u : 0u);
@@ -288,24 +365,73 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, co
                 tc_commit(bar(kBarOA + x));
                 return true;
             };
-            bool ok = mbar_wait(bar(kBarQ), 0, p.err);
-            for (int j = 0; j < nkt && ok; j++) {
-                for (int x = 0; x < ntile && ok; x++) {
-                    if (j >= 1) ok = issue_pv(x, j - 1);         // reads P_x(j-1) before S_x(j) overwrites it
-                    if (ok && x == 0) {
-                        ok = mbar_wait(bar(kBarK0 + (j & 1)), (j >> 1) & 1, p.err);
-                        tc_fence_after();
-                    }
-                    if (ok) issue_s(x, j);
+            auto issue_s1 = [&](int j) {                          // single tile: S(j) into buffer j & 1
+                const uint32_t kbase = sb + kKOff + (j & 1) * kTile;
+#pragma unroll
+                for (int kk = 0; kk < DP / 16; kk++) {
+                    const uint64_t ad = sdesc_sw128(sb + kQOff + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(kbase + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024);
+                    tc_mma(tmem + (j & 1) * 128, ad, bd, idS, kk > 0 ? 1u : 0u);
                 }
+                tc_commit(bar(kBarSA + (j & 1)));
+            };
+            auto issue_pv1 = [&](int j) -> bool {                  // single tile: O += P(j) V_j
+                if (!mbar_wait(bar(kBarPA), j & 1, p.err)) return false;
+                if (!mbar_wait(bar(kBarV0 + (j & 1)), (j >> 1) & 1, p.err)) return false;
+                tc_fence_after();
+                const uint32_t vbase = sb + kVOff + (j & 1) * kTile;
+#pragma unroll
+                for (int kk = 0; kk < 8; kk++) {
+                    const uint64_t bd = sdesc_sw128(vbase + kk * 2048, kSub, 1024);
+                    // P of keys 0..63 at columns [0,32), of keys 64..127 at [64,96)
+                    const uint32_t pcol = (j & 1) * 128 + kk * 8 + (kk >= 4 ? 32 : 0);
+                    tc_mma_ts(tmem + 256, tmem + pcol, bd, idO, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc_commit(bar(kBarOA));
+                return true;
+            };
+            bool ok = mbar_wait(bar(kBarQ), 0, p.err);
+            if (has_b) {
+                for (int j = 0; j < nkt && ok; j++) {
+                    for (int x = 0; x < ntile && ok; x++) {
+                        if (j >= 1) ok = issue_pv(x, j - 1);     // reads P_x(j-1) before S_x(j) overwrites it
+                        if (ok && x == 0) {
+                            ok = mbar_wait(bar(kBarK0 + (j & 1)), (j >> 1) & 1, p.err);
+                            tc_fence_after();
+                        }
+                        if (ok) issue_s(x, j);
+                    }
+                }
+                for (int x = 0; x < ntile && ok; x++) ok = issue_pv(x, nkt - 1);
+            } else {
+                // single tile: S(j) goes to TMEM columns [128 (j & 1), +128)
+                // and completes on barrier kBarSA + (j & 1), so S(j+1) runs
+                // while the softmax of tile j does; PV(j) reads P(j) there
+                // before S(j+2) overwrites it (MMAs complete in issue order)
+                for (int j = 0; j < nkt && ok; j++) {
+                    if (j == 0) {
+                        ok = mbar_wait(bar(kBarK0), 0, p.err);
+                        tc_fence_after();
+                        if (ok) issue_s1(0);
+                    }
+                    if (ok && j + 1 < nkt) {
+                        ok = mbar_wait(bar(kBarK0 + ((j + 1) & 1)), ((j + 1) >> 1) & 1, p.err);
+                        tc_fence_after();
+                        if (ok) issue_s1(j + 1);
+                    }
+                    if (ok) ok = issue_pv1(j);
+                }
+                // With S double-buffered, S(j) does not imply PV(j-1) done,
+                // so kBarOA may lag its waiters by two phases at the end: the
+                // final O gets its own single-phase barrier.
+                tc_commit(bar(kBarOFin));
             }
-            for (int x = 0; x < ntile && ok; x++) ok = issue_pv(x, nkt - 1);
             // every MMA this thread issued has finished before TMEM is released
             tc_commit(bar(kBarMmaDone));
             mbar_wait(bar(kBarMmaDone), 0, p.err);
         }
         __syncwarp();
-    } else if (warp >= 4 && (warp < 8 || has_b)) {
+    } else if (warp >= 4 && has_b) {
         // ------------------------------------------------------------ softmax, one row per thread
         const int x = warp >= 8 ? 1 : 0;                           // tile a or b
         const int row = threadIdx.x - (x ? 256 : 128);
@@ -326,7 +452,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, co
             const int key0 = j * kTcKeys;
             // warp-uniform: does any row of this warp see masked keys in this tile?
             const bool diag = __any_sync(0xffffffffu, key0 + kTcKeys - 1 > qpos);
-            const float mraw = diag ? tc_row_max<true>(ts, key0, qpos) : tc_row_max<false>(ts, key0, qpos);
+            const float mraw = diag ? tc_row_max<true, 128>(ts, key0, qpos) : tc_row_max<false, 128>(ts, key0, qpos);
             const float mt = mraw * sl2;                            // in the exp2 domain (scale > 0)
             if (j == 0) {
                 m_used = mt;
@@ -342,21 +468,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, co
                         l *= alpha;
                         m_used = mt;
                     }
-#pragma unroll 1
-                    for (int c = 0; c < 4; c++) {
-                        uint32_t ov[32];
-                        tmem_ld32(to + c * 32, ov);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int k = 0; k < 32; k++) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * alpha);
-                        tmem_st32(to + c * 32, ov);
-                    }
-                    tmem_st_wait();
+                    tc_rescale_cols(to, 0, DP / 32, alpha);
                 }
             }
             // pass 2: P = 2^(s * scale * log2e - m) over the first 64 S columns
             const float ms = m_used == -INFINITY ? 0.f : m_used;
-            l += diag ? tc_row_exp<true>(ts, key0, qpos, sl2, ms) : tc_row_exp<false>(ts, key0, qpos, sl2, ms);
+            l += diag ? tc_row_exp<true, 128>(ts, key0, qpos, sl2, ms) : tc_row_exp<false, 128>(ts, key0, qpos, sl2, ms);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kBarPA + x));
@@ -365,26 +482,71 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, co
         if (ok) ok = mbar_wait(bar(kBarOA + x), (nkt - 1) & 1, p.err);
         if (__all_sync(0xffffffffu, ok)) {
             tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            const size_t orow = row < nr ? ((size_t)(b + tok0 + row / g) * p.hq + kh * g + row % g) * kTcD : 0;
-#pragma unroll
-            for (int c = 0; c < 4; c++) {
-                uint32_t v[32];
-                tmem_ld32(to + c * 32, v);
-                tmem_ld_wait();
-                if (row < nr) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow + c * 32);
-#pragma unroll
-                    for (int q = 0; q < 4; q++) {
-                        uint32_t w4[4];
-#pragma unroll
-                        for (int e = 0; e < 4; e++)
-                            w4[e] = pack_bf16x2(__uint_as_float(v[q * 8 + 2 * e]) * inv,
-                                                __uint_as_float(v[q * 8 + 2 * e + 1]) * inv);
-                        dst[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            tc_store_rows<D>(p, to, row, nr, b + tok0, kh, g, l > 0.f ? 1.f / l : 0.f, 0, DP / 32);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ single tile: two warps per row
+        // Warps w and w + 4 share TMEM lanes 32 (w % 4) ..: warp hc = 0 takes
+        // S columns [0,64) and O columns [0,DP/2), hc = 1 the other halves.
+        // Each pair meets at a named barrier per key tile (ids 2..5) to swap
+        // half-row maxima; it ANDs the pair's progress so both leave together.
+        const int hc = warp >= 8 ? 1 : 0;
+        const int rg = warp & 3;
+        const int row = threadIdx.x - (hc ? 256 : 128);
+        const int nr = ntok_a * g;
+        const uint32_t tl = tmem + ((uint32_t)(rg * 32) << 16);
+        const uint32_t to = tl + 256;                              // O_a
+        const int qpos = row < nr ? L - t + i0 + row / g : -1;
+        const float sl2 = p.scale_log2;
+        float *xm = reinterpret_cast<float *>(sp + C::kXOff);      // [parity][half][128]
+        float *xl = xm + 512;                                      // [half][128]
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nkt; j++) {
+            const uint32_t ts = tl + (j & 1) * 128 + hc * 64;     // this half of S(j); P at its first 32 columns
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarSA + (j & 1)), (j >> 1) & 1, p.err));
+            const int key0 = j * kTcKeys + hc * 64;
+            const bool diag = __any_sync(0xffffffffu, key0 + 63 > qpos);
+            float mh = -INFINITY;
+            if (ok) {
+                tc_fence_after();
+                mh = diag ? tc_row_max<true, 64>(ts, key0, qpos) : tc_row_max<false, 64>(ts, key0, qpos);
+                xm[((j & 1) * 2 + hc) * 128 + row] = mh;
+            }
+            if (!named_bar_and(2 + rg, 64, ok)) { ok = false; break; }
+            const float mt = fmaxf(mh, xm[((j & 1) * 2 + (hc ^ 1)) * 128 + row]) * sl2;
+            if (j == 0) {
+                m_used = mt;
+            } else {
+                const bool need = mt > m_used + kRescaleLog2;       // the same in both halves
+                if (__any_sync(0xffffffffu, need)) {
+                    // move the running max: O must be stable, so wait for PV(j-1);
+                    // both warps of the pair take this branch and agree on the outcome
+                    ok = mbar_wait(bar(kBarOA), (j - 1) & 1, p.err);
+                    if (!named_bar_and(2 + rg, 64, __all_sync(0xffffffffu, ok))) { ok = false; break; }
+                    tc_fence_after();
+                    const float alpha = need ? exp2f(m_used - mt) : 1.f;
+                    if (need) {
+                        l *= alpha;
+                        m_used = mt;
                     }
+                    tc_rescale_cols(to, hc * (DP / 64), DP / 64, alpha);
                 }
             }
+            const float ms = m_used == -INFINITY ? 0.f : m_used;
+            l += diag ? tc_row_exp<true, 64>(ts, key0, qpos, sl2, ms) : tc_row_exp<false, 64>(ts, key0, qpos, sl2, ms);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarPA));
+        }
+        pdl_launch_dependents();
+        if (ok) ok = mbar_wait(bar(kBarOFin), 0, p.err);
+        xl[hc * 128 + row] = l;
+        ok = named_bar_and(2 + rg, 64, __all_sync(0xffffffffu, ok));
+        if (ok) {
+            tc_fence_after();
+            const float lt = l + xl[(hc ^ 1) * 128 + row];
+            tc_store_rows<D>(p, to, row, nr, b + i0, kh, g, lt > 0.f ? 1.f / lt : 0.f, hc * (DP / 64), DP / 64);
         }
     }
 
@@ -402,30 +564,48 @@ cudaError_t make_pool_tmap(CUtensorMap *map, const void *pool, int64_t num_slots
                            bool swizzle128);
 cudaError_t make_q_tmap(CUtensorMap *map, const void *q, int num_tokens, int hq, int d, int g);
 
-bool tc_prefill_supported(int head_dim, int group) { return head_dim == kTcD && group >= 1 && kTcRows % group == 0; }
+bool tc_prefill_supported(int head_dim, int group)
+{
+    return (head_dim == 48 || head_dim == 64 || head_dim == 128) && group >= 1 && kTcRows % group == 0;
+}
 int tc_prefill_rows() { return kTcRows; }
 
-cudaError_t launch_attn_tc(const AttnParams &p, const WorkList &wl, int num_items, const void *q, int num_tokens,
-                           const void *k_cache, const void *v_cache, int64_t num_slots, cudaStream_t stream)
+template <int DP, int D>
+static cudaError_t launch_tc_d(const AttnParams &p, const WorkList &wl, int num_items, const void *q, int num_tokens,
+                               const void *k_cache, const void *v_cache, int64_t num_slots, cudaStream_t stream)
 {
-    if (num_items <= 0) return cudaSuccess;
+    constexpr int smem = TcCfg<DP>::kSmem;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+        attr_err = cudaFuncSetAttribute(attn_tc_kernel<DP, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     });
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap qm, km, vm;
-    cudaError_t e = make_q_tmap(&qm, q, num_tokens, p.hq, kTcD, p.group);
-    if (e == cudaSuccess) e = make_pool_tmap(&km, k_cache, num_slots, p.hkv, kTcD, 64, true);
-    if (e == cudaSuccess) e = make_pool_tmap(&vm, v_cache, num_slots, p.hkv, kTcD, 64, true);
+    // 64-column boxes; for D < 64 they reach past the row and TMA fills zeros
+    cudaError_t e = make_q_tmap(&qm, q, num_tokens, p.hq, D, p.group);
+    if (e == cudaSuccess) e = make_pool_tmap(&km, k_cache, num_slots, p.hkv, D, 64, true);
+    if (e == cudaSuccess) e = make_pool_tmap(&vm, v_cache, num_slots, p.hkv, D, 64, true);
     if (e != cudaSuccess) return e;
     if (num_items > 65535) return cudaErrorInvalidConfiguration;
     dim3 grid(p.hkv, num_items);                   // items in launch order: the planner puts the longest first
     launch_begin(stream, kAttnTcPrefill);
-    e = launch_maybe_pdl(attn_tc_kernel, grid, dim3(kTcThreads), kTcSmem, stream, p, wl, qm, km, vm, num_slots);
+    e = launch_maybe_pdl(attn_tc_kernel<DP, D>, grid, dim3(kTcThreads), smem, stream, p, wl, qm, km, vm, num_slots);
     launch_end(stream);
     return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_attn_tc(const AttnParams &p, const WorkList &wl, int num_items, const void *q, int num_tokens,
+                           const void *k_cache, const void *v_cache, int64_t num_slots, int head_dim,
+                           cudaStream_t stream)
+{
+    if (num_items <= 0) return cudaSuccess;
+    switch (head_dim) {
+    case 48: return launch_tc_d<64, 48>(p, wl, num_items, q, num_tokens, k_cache, v_cache, num_slots, stream);
+    case 64: return launch_tc_d<64, 64>(p, wl, num_items, q, num_tokens, k_cache, v_cache, num_slots, stream);
+    case 128: return launch_tc_d<128, 128>(p, wl, num_items, q, num_tokens, k_cache, v_cache, num_slots, stream);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace pkv

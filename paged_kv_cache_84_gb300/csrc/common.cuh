@@ -14,6 +14,10 @@ namespace pkv {
 // items item_off[li] .. item_off[li+1]-1 of the grid's x dimension.
 // Decode-class lists split a request's keys into chunks of `split_tokens`;
 // prefill-class lists cut its new tokens into tiles of `tile_tokens`.
+// Each listed request also carries its first row, row count and context
+// length from the host copies of the metadata, so that a CTA starts without
+// a dependent read of device memory; one lane per request compares them
+// with the device arrays later (check_meta).
 constexpr int kPlanMax = 256;
 
 struct WorkList {
@@ -24,6 +28,10 @@ struct WorkList {
     int32_t req[kPlanMax];
     int32_t item_off[kPlanMax + 1];
     int32_t part_off[kPlanMax];   // decode: first partial row of a split request, -1 if unsplit
+    int32_t qb[kPlanMax];         // query_start_loc[req]
+    int32_t qt[kPlanMax];         // query_start_loc[req + 1] - query_start_loc[req]
+    int32_t len[kPlanMax];        // seq_lens[req]
+    int32_t cnt_off[kPlanMax];    // decode: first split counter of a request combined in-kernel, else -1
 };
 
 constexpr int kModeDecode = 0;
@@ -43,9 +51,23 @@ struct AttnParams {
     uint32_t *err;              // device error word
     float *part_o;              // [rows][head_dim] unnormalised split outputs
     float2 *part_ml;            // [rows] (running max in exp2 domain, sum of weights)
+    uint32_t *counters;         // split counters of in-kernel combines (zero between calls), or null
 };
 
 // ---------------------------------------------------------------- device helpers
+
+constexpr uint32_t kDevErrMeta = 8u;    // device metadata differs from the host copies
+constexpr uint32_t kDevErrCounter = 16u; // a split counter was not zero at the start of a call
+constexpr int kCounterStride = 8;        // uint32 words between two split counters (32 bytes)
+
+// Flags a listed request whose device metadata disagrees with the host copies
+// the launch was planned from (the kernels use the planned values).
+__device__ __forceinline__ void check_meta(const AttnParams &p, const WorkList &wl, int li)
+{
+    const int r = wl.req[li];
+    const int b = p.qsl[r], e = p.qsl[r + 1], L = p.seq_lens[r];
+    if (b != wl.qb[li] || e - b != wl.qt[li] || L != wl.len[li]) atomicOr(p.err, kDevErrMeta);
+}
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -103,11 +125,12 @@ cudaError_t launch_attn_mma(const AttnParams &p, const WorkList &wl, int head_di
                             const void *k_cache, const void *v_cache, int64_t num_slots, cudaStream_t stream);
 int mma_prefill_rows();
 
-// tcgen05 prefill tiles of 128 query rows (head_dim 128, g dividing 128).
+// tcgen05 prefill tiles of 128 query rows (head_dim 48, 64 or 128, g dividing 128).
 bool tc_prefill_supported(int head_dim, int group);
 int tc_prefill_rows();
 cudaError_t launch_attn_tc(const AttnParams &p, const WorkList &wl, int num_items, const void *q, int num_tokens,
-                           const void *k_cache, const void *v_cache, int64_t num_slots, cudaStream_t stream);
+                           const void *k_cache, const void *v_cache, int64_t num_slots, int head_dim,
+                           cudaStream_t stream);
 
 // Merge split-KV partials of the split requests in `wl` into bf16 output.
 cudaError_t launch_attn_combine(const AttnParams &p, const WorkList &wl, int head_dim,

@@ -121,7 +121,19 @@ constexpr int kDecodeRows = 16;       // decode-class: t * g <= this
 constexpr int kMinSplit = 256;        // smallest KV split, tokens
 constexpr int kMaxSplits = 64;        // most splits of one request
 constexpr size_t kErrBytes = 256;     // device error word area at the workspace start
+// Split counters of in-kernel combines: a fixed region after the error word
+// in every workspace large enough to hold it (zero-filled by the caller once;
+// each call leaves it zero again).  One counter per (split request, KV head).
+// Counters sit 32 bytes apart so that concurrent atomics of different
+// requests do not queue on one L2 sector.
+constexpr int kCounterGroups = 2048;
+constexpr size_t kCounterBytes = 4 * (size_t)kCounterStride * kCounterGroups;
 constexpr int kMaxPrefillRowSplits = 4;   // workspace sizing of split prefill tiles
+// Every prefill-class request (more than kDecodeRows query rows) whose head
+// dim and group fit a 128-row tile runs on the tcgen05 kernel: measured on
+// the 48-request engine step, one 128-row tile per (request, KV head) beats
+// several 32-row warp-MMA CTAs that each re-read the request's keys.
+constexpr int kTcMinRows = kDecodeRows + 1;
 
 // Kernel class of request r (host rule shared by the planner and pkv_plan_request_kernels).
 static int env_int(const char *name, int dflt);
@@ -131,7 +143,9 @@ static int request_class(int32_t t, int32_t L, int32_t g, int32_t d)
     if (t == 0) return PKV_CLASS_NONE;
     if (L == 0) return PKV_CLASS_PADDING;
     if (t * g <= kDecodeRows) return PKV_CLASS_DECODE;
-    if (tc_prefill_supported(d, g) && t * g >= tc_prefill_rows() && !env_int("PKV_ATTN_CUDA_CORE", 0) &&
+    // a request fills at least kTcMinRows of a 128-row tensor-core tile
+    const int min_rows = env_int("PKV_TC_MIN_ROWS", kTcMinRows);
+    if (tc_prefill_supported(d, g) && t * g >= min_rows && !env_int("PKV_ATTN_CUDA_CORE", 0) &&
         !env_int("PKV_DISABLE_TCGEN05", 0))
         return PKV_CLASS_PREFILL_TENSOR;
     return PKV_CLASS_PREFILL_CUDA_CORE;
@@ -255,7 +269,7 @@ size_t pkv_attention_workspace_bytes(int32_t max_num_reqs, int32_t max_num_token
     if (pre_rows > 2 * 152 * 32) pre_rows = 2 * 152 * 32;
     int64_t pre_splits = splits < kMaxPrefillRowSplits ? splits : kMaxPrefillRowSplits;
     rows += pre_rows * pre_splits;
-    return kErrBytes + (size_t)rows * ((size_t)head_dim * 4 + 8) + 64;
+    return kErrBytes + kCounterBytes + (size_t)rows * ((size_t)head_dim * 4 + 8) + 64;
 }
 
 pkv_status pkv_plan_request_kernels(const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs,
@@ -383,7 +397,11 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
         return rows;
     };
     const size_t row_bytes = (size_t)d * 4 + 8;
-    const size_t avail = workspace_bytes - kErrBytes;
+    // The layout depends on the workspace size only: [error word][counters,
+    // if the workspace holds them][partials].
+    const bool has_counters = workspace_bytes >= kErrBytes + kCounterBytes + 64;
+    const size_t part_base = kErrBytes + (has_counters ? kCounterBytes : 0);
+    const size_t avail = workspace_bytes - part_base;
     for (;;) {
         bool too_many = false;
         const size_t rows = partial_rows(split, &too_many);
@@ -414,15 +432,16 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
     // partial rows: first all o rows, then the (m, l) pairs
     bool unused = false;
     const size_t total_rows = partial_rows(split, &unused);
-    p.part_o = reinterpret_cast<float *>(ws + kErrBytes);
-    p.part_ml = reinterpret_cast<float2 *>(ws + kErrBytes + ((total_rows * d * 4 + 15) / 16) * 16);
+    p.part_o = reinterpret_cast<float *>(ws + part_base);
+    p.part_ml = reinterpret_cast<float2 *>(ws + part_base + ((total_rows * d * 4 + 15) / 16) * 16);
+    p.counters = has_counters ? reinterpret_cast<uint32_t *>(ws + kErrBytes) : nullptr;
 
     // ---- decode-class work runs on a side stream, concurrently with the
     // prefill kernels, when both are present: its CTAs fill the SMs that the
     // prefill leaves idle (its last wave, or a small batch's spare SMs).
     // Fork and join with events, so the caller's stream order (and CUDA-graph
     // capture) is preserved.
-    cudaStream_t dstream = stream;
+    cudaStream_t dstream = stream, pstream = stream;         // decode-class / prefill-class work
     SideStream *side = nullptr;
     const bool fork = !dec.empty() && (!tcp.empty() || !pre.empty()) && !env_int("PKV_NO_OVERLAP", 0);
     if (fork) {
@@ -435,7 +454,27 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
             side->mu.unlock();
             return cuda_fail(e, "fork");
         }
-        dstream = side->stream;
+        // The class on the caller's stream follows the K/V scatter as a
+        // programmatic dependent (it starts while the scatter drains); the
+        // other one waits for the fork event.
+        // The class expected to take longer goes on the caller's stream:
+        // decode time ~ its K/V bytes at HBM speed, prefill time ~ its
+        // causal pairs at tensor-core speed (rough rates; only the ratio
+        // matters).  PKV_DECODE_MAIN=0/1 forces the choice.
+        double dec_us = 0.0, pre_us = 0.0;
+        for (int32_t r : dec) dec_us += (double)sl_h[r] * hkv * d * 4.0 / 6.5e6;
+        for (int32_t r : pre) {
+            const double t = qsl_h[r + 1] - qsl_h[r], L = sl_h[r];
+            pre_us += (t * L - 0.5 * t * t) * hq * d * 4.0 / 1.2e9;
+        }
+        for (int32_t r : tcp) {
+            const double t = qsl_h[r + 1] - qsl_h[r], L = sl_h[r];
+            pre_us += (t * L - 0.5 * t * t) * hq * d * 4.0 / 1.2e9;
+        }
+        const int forced = env_int("PKV_DECODE_MAIN", -1);
+        const bool decode_main = forced >= 0 ? forced != 0 : dec_us > pre_us;
+        if (decode_main) pstream = side->stream;
+        else dstream = side->stream;
     }
     bool joined = !fork;
     auto join = [&]() -> cudaError_t {
@@ -445,6 +484,17 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
         if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, side->join, 0);
         side->mu.unlock();
         return e;
+    };
+
+    // list request r in wl with its planned metadata; returns its index
+    auto list_request = [&](WorkList &wl, int32_t r) -> int {
+        const int li = wl.n++;
+        wl.req[li] = r;
+        wl.qb[li] = qsl_h[r];
+        wl.qt[li] = qsl_h[r + 1] - qsl_h[r];
+        wl.len[li] = sl_h[r];
+        wl.cnt_off[li] = -1;
+        return li;
     };
 
     // ---- tensor-core prefill launches, submitted first: the longest work
@@ -458,14 +508,13 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
         for (size_t x = c0; x < c1; x++) {
             int32_t r = tcp[x];
             int32_t t = qsl_h[r + 1] - qsl_h[r];
-            int li = wl.n++;
-            wl.req[li] = r;
+            int li = list_request(wl, r);
             wl.item_off[li] = items;
             wl.part_off[li] = -1;
             items += (t + 2 * wl.tile_tokens - 1) / (2 * wl.tile_tokens);   // pairs of 128-row tiles
         }
         wl.item_off[wl.n] = items;
-        cudaError_t e = launch_attn_tc(p, wl, items, q, num_tokens, k_cache, v_cache, num_slots, stream);
+        cudaError_t e = launch_attn_tc(p, wl, items, q, num_tokens, k_cache, v_cache, num_slots, d, pstream);
         if (e != cudaSuccess) {
             join();
             return cuda_fail(e, "tensor-core prefill launch");
@@ -479,12 +528,17 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
     };
     CombineSet dec_combine, pre_combine;
     size_t part_cursor = 0;
-    auto take_partials = [&](CombineSet &set, int32_t r, int32_t S) -> int32_t {
+    int counter_cursor = 0;
+    // partial rows of a split request; combined by `set`'s combine launch,
+    // or inside the attention kernel when in_kernel
+    auto take_partials = [&](CombineSet &set, int32_t r, int32_t S, bool in_kernel = false) -> int32_t {
         if (S <= 1) return -1;
         const int32_t t = qsl_h[r + 1] - qsl_h[r];
         const int32_t off = (int32_t)part_cursor;
-        set.reqs.push_back(r);
-        set.offs.push_back(off);
+        if (!in_kernel) {
+            set.reqs.push_back(r);
+            set.offs.push_back(off);
+        }
         part_cursor += (size_t)S * t * hq;
         if (t * hq > set.max_rows) set.max_rows = t * hq;
         return off;
@@ -498,8 +552,7 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
             wl.split_tokens = split;
             size_t c1 = c0 + kPlanMax < set.reqs.size() ? c0 + kPlanMax : set.reqs.size();
             for (size_t x = c0; x < c1; x++) {
-                int li = wl.n++;
-                wl.req[li] = set.reqs[x];
+                int li = list_request(wl, set.reqs[x]);
                 wl.part_off[li] = set.offs[x];
                 wl.item_off[li] = li;
             }
@@ -521,10 +574,16 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
             int32_t r = dec[x];
             int32_t t = qsl_h[r + 1] - qsl_h[r];
             int32_t S = splits_of(sl_h[r], split);
-            int li = wl.n++;
-            wl.req[li] = r;
+            int li = list_request(wl, r);
             wl.item_off[li] = items;
-            wl.part_off[li] = take_partials(dec_combine, r, S);
+            // split decodes of the MMA kernels combine in the kernel (the CTA
+            // finishing a request's last split) when counters are available
+            const bool in_kernel = S > 1 && !use_fma && has_counters && counter_cursor + hkv <= kCounterGroups;
+            wl.part_off[li] = take_partials(dec_combine, r, S, in_kernel);
+            if (in_kernel) {
+                wl.cnt_off[li] = counter_cursor;
+                counter_cursor += hkv;
+            }
             items += S;
             if (sl_h[r] > 0 && t * g > rows) rows = t * g;
         }
@@ -556,15 +615,14 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
             int32_t r = pre[x];
             int32_t t = qsl_h[r + 1] - qsl_h[r];
             const int32_t S = pre_split ? splits_of(sl_h[r], split) : 1;
-            int li = wl.n++;
-            wl.req[li] = r;
+            int li = list_request(wl, r);
             wl.item_off[li] = items;
             wl.part_off[li] = take_partials(pre_combine, r, S);
             items += ((t + tile - 1) / tile) * S;
         }
         wl.item_off[wl.n] = items;
-        cudaError_t e = use_fma ? launch_attn_fma(p, wl, d, kDecodeRows, items, stream)
-                                : launch_attn_mma(p, wl, d, items, k_cache, v_cache, num_slots, stream);
+        cudaError_t e = use_fma ? launch_attn_fma(p, wl, d, kDecodeRows, items, pstream)
+                                : launch_attn_mma(p, wl, d, items, k_cache, v_cache, num_slots, pstream);
         if (e != cudaSuccess) {
             join();
             return cuda_fail(e, "prefill attention launch");
@@ -575,7 +633,7 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
         return PKV_ERR_WORKSPACE;
     }
 
-    if (cudaError_t e = launch_combines(pre_combine, stream); e != cudaSuccess) {
+    if (cudaError_t e = launch_combines(pre_combine, pstream); e != cudaSuccess) {
         join();
         return cuda_fail(e, "split combine launch");
     }

@@ -181,6 +181,21 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Named barrier over `count` threads that also ANDs `pred` across them.
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t count, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
 // ---------------------------------------------------------------- tcgen05 / TMEM
 
 // Allocate `ncols` TMEM columns (power of two >= 32) for this CTA; the base

@@ -57,9 +57,12 @@ def test_host_only_functions(lib):
     assert pkv.WORKSPACE_MIN_BYTES < small < big
     # layout example: every request is decode-class (t * g <= 16)
     assert pkv.plan_request_kernels([0, 3, 4, 5, 9], [9, 42, 10, 4], 8, 4, 48) == ["decode"] * 4
-    # a 64-token chunk with g = 2 is a prefill tile job; seq_len 0 is padding; t = 0 is nothing
+    # a 64-token chunk with g = 2 is a tensor-core tile job; seq_len 0 is padding; t = 0 is nothing
     assert pkv.plan_request_kernels([0, 64, 65, 65], [300, 0, 7], 8, 4, 48) == \
-        ["prefill_cuda_core", "padding", "none"]
+        ["prefill_tensor", "padding", "none"]
+    # 18 rows (t = 6, g = 3) exceed a decode tile; g = 3 does not divide the
+    # 128-row tensor-core tile, so the chunk runs on the warp-level MMA kernel
+    assert pkv.plan_request_kernels([0, 6], [40], 9, 3, 64) == ["prefill_cuda_core"]
 
 
 def _attn_args(qsl, sl, R, N, maxq, maxl, hq=8, hkv=4, d=64, bs=16, stride=4, ws=1 << 20):

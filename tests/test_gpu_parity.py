@@ -97,14 +97,17 @@ def test_cuda_core_kernels_full_parity(case, monkeypatch):
 
 
 @pytest.mark.parametrize("disable_tc", [False, True])
-def test_long_chunks_tensor_core_path(disable_tc, monkeypatch):
-    """Prefill chunks of 128+ rows go to the tcgen05 kernel; the same batch with
-    it disabled runs on the warp-level MMA kernel.  Both match the oracle."""
+@pytest.mark.parametrize("heads", [(32, 8, 128), (16, 4, 64), (8, 4, 48), (16, 2, 48)], ids=["d128g4", "d64g4", "d48g2", "d48g8"])
+def test_long_chunks_tensor_core_path(disable_tc, heads, monkeypatch):
+    """Prefill chunks of 128+ rows go to the tcgen05 kernel (head dims below 64
+    padded to 64 columns); the same batch with it disabled runs on the
+    warp-level MMA kernel.  Both match the oracle."""
     if disable_tc:
         monkeypatch.setenv("PKV_DISABLE_TCGEN05", "1")
+    hq, hkv, d = heads
     reqs = [Req(1000, 300, list(range(0, 82))), Req(0, 257, list(range(82, 99))), Req(77, 1, list(range(99, 104))),
             Req(5000, 64, list(range(104, 421)))]
-    spec = Spec("chunks", reqs, 32, 8, 128, 16, 430, 1 / math.sqrt(128), 17)
+    spec = Spec("chunks", reqs, hq, hkv, d, 16, 430, 1 / math.sqrt(d), 17)
     b = make_batch(spec, device="cpu")
     dev = DeviceStep(b)
     pkv.profile_start(16)
@@ -179,8 +182,10 @@ def test_programmatic_launch_and_padding_only_decodes(pdl, monkeypatch):
 
 @pytest.mark.parametrize("prefill_split", [False, True])
 def test_engine_step_prefill_split_toggle(prefill_split, monkeypatch):
-    """The small engine step with and without key splits of its short prefill
-    tiles (PKV_PREFILL_SPLIT=1)."""
+    """The small engine step on the warp-level MMA kernels only (tensor cores
+    off), with and without key splits of its short prefill tiles
+    (PKV_PREFILL_SPLIT=1)."""
+    monkeypatch.setenv("PKV_DISABLE_TCGEN05", "1")
     if prefill_split:
         monkeypatch.setenv("PKV_PREFILL_SPLIT", "1")
     b = make_batch(config_spec(2), device="cpu")
@@ -414,3 +419,121 @@ def test_out_of_pool_slot_sets_flag_and_skips():
     oracle.paged_kv_write(ref.k_cache, ref.v_cache, b.k[keep], b.v[keep], sm[keep])
     assert torch.equal(_pool_bits(dev.k_cache.cpu())[:-1], _pool_bits(ref.k_cache)[:-1])
     del before
+
+
+@pytest.mark.parametrize("path", ["default", "cuda-core"])
+def test_device_metadata_differing_from_host_copies_is_flagged(path, monkeypatch):
+    """The kernels take each request's rows and context length from the host
+    copies they were planned with; device arrays that disagree set
+    DEVERR_META and change nothing else."""
+    if path == "cuda-core":
+        monkeypatch.setenv("PKV_ATTN_CUDA_CORE", "1")
+    # decodes, short chunks and one tensor-core-sized chunk (t*g >= 128, d 128)
+    reqs = [Req(300, 1, list(range(0, 19))), Req(40, 24, list(range(19, 23))),
+            Req(100, 64, list(range(23, 34)))]
+    spec = Spec("meta", reqs, 8, 2, 128, 16, 40, 1.0 / math.sqrt(128), 5)
+    b = make_batch(spec, device="cpu")
+    dev = DeviceStep(b)
+    dev.write()
+    pkv.clear_device_error(dev.ws)
+    dev.attend()
+    assert pkv.read_device_error(dev.ws) == 0
+    ref = cpu_copy(b)
+    oracle_write(ref)
+    want = oracle_full(ref)
+    for r in range(len(reqs)):                    # each request is checked by the kernel serving it
+        dev.sl = torch.tensor(b.meta.seq_lens, dtype=torch.int32, device="cuda")
+        dev.sl[r] -= 1                            # the device copy disagrees with the host copy
+        dev.out.fill_(float("nan"))
+        pkv.clear_device_error(dev.ws)
+        dev.attend()
+        assert pkv.read_device_error(dev.ws) & pkv.DEVERR_META, f"request {r}"
+        assert_close(dev.out.cpu(), want, f"planned metadata, request {r} altered")
+
+
+COUNTER_BYTES = 65536          # split-counter region after the 256-byte error word
+
+
+@pytest.mark.parametrize("split", [128, 1024])
+@pytest.mark.parametrize("d", [48, 128])
+def test_in_kernel_split_combine_repeats_and_leaves_counters_zero(split, d, monkeypatch):
+    """Split decodes combine inside the kernel (the CTA finishing the last
+    split of a request and KV head); repeated calls, eager and replayed from a
+    CUDA graph, stay exact, and every call leaves the counters at zero."""
+    monkeypatch.setenv("PKV_SPLIT_TOKENS", str(split))
+    spec = random_spec(31, 12, 4000, 3, 16 if d == 128 else 8, 4 if d == 128 else 2, d, decode_frac=0.85)
+    b = make_batch(spec, device="cpu")
+    dev = DeviceStep(b)
+    dev.write()
+    ref = cpu_copy(b)
+    oracle_write(ref)
+    want = oracle_full(ref)
+    for i in range(3):
+        dev.out.fill_(float("nan"))
+        dev.attend()
+        assert_close(dev.out, want, f"eager call {i}")
+    assert int(dev.ws[256:256 + COUNTER_BYTES].count_nonzero()) == 0
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        dev.attend()
+    torch.cuda.synchronize()
+    for i in range(3):
+        dev.out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert_close(dev.out, want, f"graph replay {i}")
+    assert int(dev.ws[256:256 + COUNTER_BYTES].count_nonzero()) == 0
+    assert pkv.read_device_error(dev.ws) == 0
+
+
+def test_workspace_without_counter_room_uses_the_combine_kernel(monkeypatch):
+    """A workspace too small for the counter region still splits (partials
+    after the error word) and combines with the separate kernel."""
+    monkeypatch.setenv("PKV_SPLIT_TOKENS", "256")
+    # one decode at L = 1500: 8 partial rows of 264 bytes per split, so the
+    # 12 KiB workspace holds 5 splits (of 512 keys: 3 splits)
+    spec = Spec("ws", [Req(1499, 1, list(range(94)))], 8, 2, 64, 16, 100, 0.125, 32)
+    b = make_batch(spec, device="cpu")
+    dev = DeviceStep(b, workspace_bytes=12 * 1024)
+    before = pkv.launch_count()
+    dev.step()
+    ref = cpu_copy(b)
+    oracle_write(ref)
+    assert_close(dev.out, oracle_full(ref), "small workspace")
+    assert pkv.launch_count() - before >= 3              # write, attention, combine
+
+
+def test_nonzero_split_counter_is_flagged(monkeypatch):
+    """A workspace whose counter region was not zero-filled is reported."""
+    monkeypatch.setenv("PKV_SPLIT_TOKENS", "256")
+    spec = random_spec(33, 4, 2000, 1, 8, 2, 64, decode_frac=1.0)
+    b = make_batch(spec, device="cpu")
+    dev = DeviceStep(b)
+    dev.write()
+    dev.ws[256:256 + COUNTER_BYTES] = 0x7f
+    dev.attend()
+    assert pkv.read_device_error(dev.ws) & pkv.DEVERR_COUNTER
+    torch.cuda.synchronize()                              # no fault, the context is usable
+
+
+
+@pytest.mark.parametrize("d", [48, 64, 128])
+def test_short_chunks_on_tensor_cores(d, monkeypatch):
+    """With the row threshold lowered, chunks that fill only part of a 128-row
+    tile (ragged token counts, unaligned contexts) run on the tcgen05 kernel."""
+    monkeypatch.setenv("PKV_TC_MIN_ROWS", "16")
+    reqs = [Req(256 + 64 * k, t, list(range(40 * k, 40 * k + 40))) for k, t in enumerate((64, 17, 33, 5, 1, 40))]
+    reqs[4] = Req(300, 1, list(range(160, 200)))                  # a decode stays on the decode kernel
+    spec = Spec("short", reqs, 8, 2 if d == 128 else 4, d, 16, 250, 1 / math.sqrt(d), 41)
+    b = make_batch(spec, device="cpu")
+    dev = DeviceStep(b)
+    pkv.profile_start(16)
+    dev.step()
+    names = {n for n, _ in pkv.profile_stop()}
+    assert "attn_tc_prefill" in names
+    ref = cpu_copy(b)
+    oracle_write(ref)
+    assert_close(dev.out, oracle_full(ref), f"short chunks d{d}")
+    assert pkv.read_device_error(dev.ws) == 0

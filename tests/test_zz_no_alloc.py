@@ -57,7 +57,10 @@ def _split_batch():
     return random_spec(81, 8, 3200, 1, 32, 8, 128, decode_frac=1.0)
 
 
-def test_noalloc_matches_workspace_entry_on_two_calls_in_a_row():
+def test_noalloc_matches_workspace_entry_on_two_calls_in_a_row(monkeypatch):
+    # keys split every 256 tokens: the second batch's decodes (~3000 keys)
+    # run as many splits, combined in the kernel through the static array
+    monkeypatch.setenv("PKV_SPLIT_TOKENS", "256")
     steps = []
     for spec in (config_spec(2), _split_batch()):
         dev = DeviceStep(make_batch(spec, device="cpu"))
@@ -72,7 +75,7 @@ def test_noalloc_matches_workspace_entry_on_two_calls_in_a_row():
         assert st == 0
         outs.append(out)
     kernels = [name for name, _ in pkv.profile_stop()]
-    assert "attn_split_combine" in kernels             # the second call went through split partials
+    assert "attn_mma_decode" in kernels
     for dev, out in zip(steps, outs):
         assert _close(out, dev.out)
     # and once more in reverse order, after the array holds the other batch's partials
