@@ -202,15 +202,19 @@ def alu_peak_tflops(peaks):
 
 
 def source_hash(name):
-    """Hash of the source file of a kernel, to tell whether stored ncu counters are current."""
+    """Hash of a kernel's source file and the shared device headers, to tell
+    whether stored ncu counters are current."""
     fname = {"paged_kv_write": "kv_write.cu", "attn_fma_decode": "attn_fma.cu", "attn_fma_prefill": "attn_fma.cu",
              "attn_split_combine": "attn_fma.cu", "attn_tc_prefill": "attn_tc.cu",
              "attn_mma_decode": "attn_mma.cu", "attn_mma_prefill": "attn_mma.cu"}.get(name)
-    path = os.path.join(ROOT, "paged_kv_cache_84_gb300", "csrc", fname or "")
-    if not fname or not os.path.exists(path):
+    csrc = os.path.join(ROOT, "paged_kv_cache_84_gb300", "csrc")
+    if not fname or not os.path.exists(os.path.join(csrc, fname)):
         return None
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:12]
+    h = hashlib.sha256()
+    for f in (fname, "common.cuh", "sm100.cuh"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
 
 
 def stored_traffic(name, workload):
@@ -232,6 +236,13 @@ def roofline(name, avg_s, launches_per_step, acc, peaks, workload):
     b /= launches_per_step
     f /= launches_per_step
     bound = KERNEL_BOUND.get(name, "hbm")
+    # A kernel whose class is tensor-bound at scale may be closer to the HBM
+    # roofline on a small, latency-bound workload: report the binding one,
+    # the roofline this launch comes closest to.
+    hbm_frac = b / avg_s / 1e9 / peaks["hbm_gbs"]
+    tensor_frac = f / avg_s / 1e12 / peaks["bf16_tflops"]
+    if bound == "tensor" and hbm_frac > tensor_frac:
+        bound = "hbm"
     if bound == "hbm":
         achieved, peak, unit = b / avg_s / 1e9, peaks["hbm_gbs"], "GB/s"
         note = f"of {peaks['source']} HBM copy bandwidth"
@@ -243,6 +254,7 @@ def roofline(name, avg_s, launches_per_step, acc, peaks, workload):
         note = "of fp32 FMA peak derived as 152 SMs x 128 lanes x 2 flop x max SM clock"
     return {"kernel": name, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
             "frac": achieved / peak, "traffic": stored_traffic(name, workload), "peak_note": note,
+            "hbm_frac": hbm_frac, "tensor_frac": tensor_frac,
             "algorithmic_bytes_per_launch": b, "algorithmic_flops_per_launch": f,
             "avg_launch_us": avg_s * 1e6}
 
