@@ -32,7 +32,7 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from workloads import CONFIG_NAMES, config_spec, make_batch, subset_spec  # noqa: E402
+from workloads import CONFIG_NAMES, config_spec, fill_normal_bf16, make_batch, subset_spec  # noqa: E402
 
 METRIC = "ragged paged-attn step µs + KV-read HBM GB/s vs 8 TB/s; query tokens/s"
 UNIT = "query tokens/s"
@@ -479,6 +479,54 @@ def e2e_workload(pkv, copies, steps, device):
             "path": "pinned host -> device copies, pkv_paged_kv_write + pkv_ragged_paged_attention, device -> pinned host"}
 
 
+def block_copy_workload(pkv, device, peaks, reps=20):
+    """Copy-on-write and swap-out/in of whole blocks over 8 pools (4 layers' K and V, 16 x 8 heads x
+    128 dims per block = 32 KB), 1 GB of pools: the block copies of the block manager, timed with CUDA
+    events over `reps` calls each.  Copy-on-write moves 1024 blocks per pool per call; swap-out
+    gathers 256 blocks per pool into pinned host memory, swap-in scatters them back."""
+    nbt, bs, hkv, d = 4096, 16, 8, 128
+    gen = torch.Generator(device=device).manual_seed(77)
+    pools = [torch.empty((nbt, bs, hkv, d), dtype=torch.bfloat16, device=device) for _ in range(8)]
+    for t in pools:
+        fill_normal_bf16(t, gen)
+    bb = bs * hkv * d * 2
+    perm = torch.randperm(nbt, generator=torch.Generator().manual_seed(78)).to(torch.int32)
+    srcs = [perm[i * 2048:i * 2048 + 1024].to(device) for i in range(2)]
+    dsts = [perm[i * 2048 + 1024:(i + 1) * 2048].to(device) for i in range(2)]
+    ids = perm[:256].to(device)
+    host = torch.empty((len(pools), 256, bb), dtype=torch.uint8).pin_memory()
+    stream = torch.cuda.current_stream()
+
+    def timed(fn):
+        for i in range(3):
+            fn(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(reps):
+            fn(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps / 1e3
+
+    cow_s = timed(lambda i: pkv.copy_blocks(pools, srcs[i % 2], dsts[i % 2]))
+    out_s = timed(lambda i: pkv.gather_blocks(pools, ids, host))
+    in_s = timed(lambda i: pkv.scatter_blocks(pools, ids, host))
+    cow_bytes = 2 * len(pools) * 1024 * bb                     # read + write
+    swap_bytes = len(pools) * 256 * bb
+    res = {
+        "pools": len(pools), "block_bytes": bb, "pool_bytes_total": len(pools) * nbt * bb,
+        "copy_on_write": {"blocks_per_pool": 1024, "us": cow_s * 1e6, "gbs": cow_bytes / cow_s / 1e9,
+                          "frac_of_hbm": cow_bytes / cow_s / 1e9 / peaks["hbm_gbs"],
+                          "bytes": "HBM read + write of the copied blocks"},
+        "swap_out_to_pinned_host": {"blocks_per_pool": 256, "us": out_s * 1e6, "gbs": swap_bytes / out_s / 1e9},
+        "swap_in_from_pinned_host": {"blocks_per_pool": 256, "us": in_s * 1e6, "gbs": swap_bytes / in_s / 1e9},
+    }
+    del pools, host
+    torch.cuda.empty_cache()
+    return res
+
+
 # ---------------------------------------------------------------------------- CPU oracle
 
 def oracle_step_timer(cfg, threads):
@@ -568,7 +616,9 @@ def run_ours(args):
     torch.cuda.empty_cache()
 
     breakdown = {}
+    block_copies = None
     if not args.no_breakdown:
+        block_copies = block_copy_workload(pkv, device, peaks)
         for cfg in (1, 2, 3, 4, 5):
             if cfg == args.workload:
                 r = dict(head)
@@ -603,7 +653,7 @@ def run_ours(args):
         "roofline": head["roofline"], "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": head["launches_per_step"] * args.steps,
         "clocks": clocks.summary(t0, t1), "peaks": peaks, "kernels": head["kernels"],
-        "workloads": breakdown,
+        "workloads": breakdown, "block_copies": block_copies,
     }
     print(json.dumps(line), flush=True)
     if dist is not None:

@@ -259,6 +259,54 @@ pkv_status pkv_clear_device_error(uint32_t *device_error, cudaStream_t stream);
 pkv_status pkv_read_device_error(const uint32_t *device_error, uint32_t *flags_out,
                                  cudaStream_t stream);
 
+/*
+ * Block copies of the block manager, over many pools in one launch.
+ * "vllm-lite README": blocks are reference counted, and a write into a
+ * block two sequences share is preceded by a copy of it (copy-on-write),
+ * done by the runner before the forward pass.  "31. Engine v2",
+ * "Preemption: recompute or swap": swap-out copies a preempted request's
+ * blocks of every layer's K and V (and, for quantized pools, their scales)
+ * to host memory; swap-in copies them into newly allocated blocks.
+ *
+ *   pools             host array of num_pools (1 .. PKV_MAX_POOLS) device
+ *                     pointers, read during the call; each is a pool of
+ *                     num_blocks_total blocks of block_bytes bytes (for a
+ *                     bf16 K or V pool: block_size * num_kv_heads * head_dim
+ *                     * 2).  Pools may have different base addresses but
+ *                     share num_blocks_total and block_bytes.
+ *   device_error      device uint32_t, may be NULL; a block id outside
+ *                     [0, num_blocks_total) is skipped and sets
+ *                     PKV_DEVERR_BLOCK.
+ * Requirements: block_bytes % 16 == 0; pools and buffers 16-byte aligned
+ * (else PKV_ERR_UNSUPPORTED).  Zero pairs/blocks is a no-op.  The copy is a
+ * bit copy; the launch waits for the kernel before it on `stream` before
+ * reading anything.
+ */
+#define PKV_MAX_POOLS 256
+
+/* Copy-on-write: in every pool, block dst_blocks[i] := block src_blocks[i].
+ * src_blocks, dst_blocks: device int32 [num_pairs].  A block that is both a
+ * source and a destination, or a destination twice, is a caller error
+ * (which bytes land is unspecified). */
+pkv_status pkv_copy_blocks(void *const *pools, int32_t num_pools, const int32_t *src_blocks,
+                           const int32_t *dst_blocks, int32_t num_pairs, int32_t num_blocks_total,
+                           size_t block_bytes, uint32_t *device_error, cudaStream_t stream);
+
+/* Swap-out: out[q][i] := block blocks[i] of pool q, out laid out
+ * [num_pools][num_blocks][block_bytes].  blocks: device int32 [num_blocks].
+ * out may be device memory or pinned host memory the device can address
+ * (then the kernel writes host memory directly). */
+pkv_status pkv_gather_blocks(void *const *pools, int32_t num_pools, const int32_t *blocks, int32_t num_blocks,
+                             int32_t num_blocks_total, size_t block_bytes, void *out, uint32_t *device_error,
+                             cudaStream_t stream);
+
+/* Swap-in: block blocks[i] of pool q := in[q][i], in laid out as for
+ * pkv_gather_blocks (device memory or device-addressable pinned host
+ * memory). */
+pkv_status pkv_scatter_blocks(void *const *pools, int32_t num_pools, const int32_t *blocks, int32_t num_blocks,
+                              int32_t num_blocks_total, size_t block_bytes, const void *in, uint32_t *device_error,
+                              cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

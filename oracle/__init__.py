@@ -48,6 +48,10 @@ def lib():
             [c_i32] * 7 + [c_dbl, c_i32]
         L.oracle_max_threads.restype = ctypes.c_int
         L.oracle_max_threads.argtypes = []
+        for name in ("oracle_copy_blocks", "oracle_gather_blocks", "oracle_scatter_blocks"):
+            f = getattr(L, name)
+            f.restype = ctypes.c_int
+            f.argtypes = [c_p, c_p, c_p, c_i32, c_i32, c_i64]
         _lib = L
     return _lib
 
@@ -121,3 +125,46 @@ def attention_rows(tokens, heads, q, k_cache, v_cache, query_start_loc, seq_lens
     if rc:
         raise ValueError(f"oracle_attention_rows: {rc}")
     return out
+
+
+def _pool_bytes(pool: torch.Tensor):
+    """A CPU pool [nbt, ...] as raw bytes, with its block count and bytes per block."""
+    assert pool.device.type == "cpu" and pool.is_contiguous()
+    nbt = pool.shape[0]
+    return pool.view(torch.uint8).view(nbt, -1), nbt, pool[0].numel() * pool.element_size()
+
+
+def copy_blocks(pools, src_blocks, dst_blocks):
+    """In every CPU pool, in list order: block dst[i] := block src[i]."""
+    src = torch.as_tensor(src_blocks, dtype=torch.int32).contiguous()
+    dst = torch.as_tensor(dst_blocks, dtype=torch.int32).contiguous()
+    for pool in pools:
+        raw, nbt, bb = _pool_bytes(pool)
+        rc = lib().oracle_copy_blocks(_ptr(raw), _ptr(src), _ptr(dst), src.numel(), nbt, bb)
+        if rc:
+            raise ValueError(f"oracle_copy_blocks: {rc}")
+
+
+def gather_blocks(pools, blocks) -> torch.Tensor:
+    """uint8 [len(pools), len(blocks), bytes per block]: block blocks[i] of pool q."""
+    ids = torch.as_tensor(blocks, dtype=torch.int32).contiguous()
+    outs = []
+    for pool in pools:
+        raw, nbt, bb = _pool_bytes(pool)
+        out = torch.empty((ids.numel(), bb), dtype=torch.uint8)
+        rc = lib().oracle_gather_blocks(_ptr(out), _ptr(raw), _ptr(ids), ids.numel(), nbt, bb)
+        if rc:
+            raise ValueError(f"oracle_gather_blocks: {rc}")
+        outs.append(out)
+    return torch.stack(outs)
+
+
+def scatter_blocks(pools, blocks, inp: torch.Tensor):
+    """Block blocks[i] of pool q := inp[q][i] (uint8 [len(pools), len(blocks), bytes per block])."""
+    ids = torch.as_tensor(blocks, dtype=torch.int32).contiguous()
+    for q, pool in enumerate(pools):
+        raw, nbt, bb = _pool_bytes(pool)
+        src = inp[q].contiguous()
+        rc = lib().oracle_scatter_blocks(_ptr(raw), _ptr(src), _ptr(ids), ids.numel(), nbt, bb)
+        if rc:
+            raise ValueError(f"oracle_scatter_blocks: {rc}")

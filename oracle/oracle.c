@@ -300,3 +300,52 @@ int oracle_max_threads(void)
     return 1;
 #endif
 }
+
+/*
+ * Block copies of the block manager.  "vllm-lite README": blocks are
+ * reference counted; a write into a block two sequences share is preceded
+ * by a copy of that block, which the runner makes before the forward pass.
+ * "31. Engine v2", "Preemption: recompute or swap": swap-out copies a
+ * preempted request's blocks (every layer's K and V) to host memory, and
+ * swap-in copies them back into newly allocated blocks.  A pool is viewed
+ * as nb_total blocks of block_bytes bytes (the slot-major layout keeps a
+ * block contiguous).  Copies are byte copies applied in list order.
+ * Each returns 0, or -1 at the first block id outside the pool.
+ */
+int oracle_copy_blocks(uint8_t *pool, const int32_t *src, const int32_t *dst, int32_t n, int32_t nb_total,
+                       int64_t block_bytes)
+{
+    for (int32_t i = 0; i < n; i++) {
+        if (src[i] < 0 || src[i] >= nb_total || dst[i] < 0 || dst[i] >= nb_total)
+            return -1;
+        for (int64_t b = 0; b < block_bytes; b++)
+            pool[(int64_t)dst[i] * block_bytes + b] = pool[(int64_t)src[i] * block_bytes + b];
+    }
+    return 0;
+}
+
+/* out[i] := block blocks[i] (out is n * block_bytes bytes). */
+int oracle_gather_blocks(uint8_t *out, const uint8_t *pool, const int32_t *blocks, int32_t n, int32_t nb_total,
+                         int64_t block_bytes)
+{
+    for (int32_t i = 0; i < n; i++) {
+        if (blocks[i] < 0 || blocks[i] >= nb_total)
+            return -1;
+        for (int64_t b = 0; b < block_bytes; b++)
+            out[(int64_t)i * block_bytes + b] = pool[(int64_t)blocks[i] * block_bytes + b];
+    }
+    return 0;
+}
+
+/* block blocks[i] := in[i]. */
+int oracle_scatter_blocks(uint8_t *pool, const uint8_t *in, const int32_t *blocks, int32_t n, int32_t nb_total,
+                          int64_t block_bytes)
+{
+    for (int32_t i = 0; i < n; i++) {
+        if (blocks[i] < 0 || blocks[i] >= nb_total)
+            return -1;
+        for (int64_t b = 0; b < block_bytes; b++)
+            pool[(int64_t)blocks[i] * block_bytes + b] = in[(int64_t)i * block_bytes + b];
+    }
+    return 0;
+}

@@ -17,7 +17,7 @@ __all__ = [
     "PkvError", "load", "paged_kv_write", "ragged_paged_attention", "attention_workspace_bytes",
     "make_workspace", "read_device_error", "clear_device_error", "launch_count", "LIB_PATH",
     "DEVERR_SLOT", "DEVERR_BLOCK", "DEVERR_TIMEOUT", "DEVERR_META", "DEVERR_COUNTER", "WORKSPACE_MIN_BYTES", "profile_start", "profile_stop",
-    "plan_request_kernels", "CLASS_NAMES",
+    "plan_request_kernels", "CLASS_NAMES", "copy_blocks", "gather_blocks", "scatter_blocks", "MAX_POOLS",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpkv.so")
@@ -81,6 +81,12 @@ def load():
     L.pkv_kernel_name.argtypes = [_c_i32]
     L.pkv_plan_request_kernels.restype = ctypes.c_int
     L.pkv_plan_request_kernels.argtypes = [_c_p, _c_p, _c_i32, _c_i32, _c_i32, _c_i32, _c_p]
+    L.pkv_copy_blocks.restype = ctypes.c_int
+    L.pkv_copy_blocks.argtypes = [_c_p, _c_i32, _c_p, _c_p, _c_i32, _c_i32, _c_sz, _c_p, _c_p]
+    L.pkv_gather_blocks.restype = ctypes.c_int
+    L.pkv_gather_blocks.argtypes = [_c_p, _c_i32, _c_p, _c_i32, _c_i32, _c_sz, _c_p, _c_p, _c_p]
+    L.pkv_scatter_blocks.restype = ctypes.c_int
+    L.pkv_scatter_blocks.argtypes = [_c_p, _c_i32, _c_p, _c_i32, _c_i32, _c_sz, _c_p, _c_p, _c_p]
     _lib = L
     return L
 
@@ -211,3 +217,65 @@ def read_device_error(word: torch.Tensor, stream=None) -> int:
     if st not in (0, 5):
         _check(st, "read_device_error")
     return int(flags.value)
+
+
+MAX_POOLS = 256
+
+
+def _pool_array(pools):
+    """Host array of the pools' device pointers; all pools share their block count and block bytes."""
+    pools = list(pools)
+    if not pools:
+        raise ValueError("no pools")
+    nbt = pools[0].shape[0]
+    block_bytes = pools[0][0].numel() * pools[0].element_size()
+    for i, t in enumerate(pools):
+        _dev(t, f"pools[{i}]")
+        if t.shape[0] != nbt or t[0].numel() * t.element_size() != block_bytes:
+            raise ValueError("pools must share the number of blocks and the bytes per block")
+    arr = (ctypes.c_void_p * len(pools))(*[t.data_ptr() for t in pools])
+    return arr, len(pools), nbt, block_bytes
+
+
+def _err(device_error):
+    return _dev(device_error, "device_error", torch.int32) if device_error is not None else None
+
+
+def _buf(t: torch.Tensor, name: str):
+    """A device tensor, or pinned host memory the device can address."""
+    if not isinstance(t, torch.Tensor) or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous tensor")
+    if not t.is_cuda and not t.is_pinned():
+        raise TypeError(f"{name} must be a CUDA tensor or pinned host memory")
+    return _c_p(t.data_ptr())
+
+
+def copy_blocks(pools, src_blocks, dst_blocks, device_error=None, stream=None):
+    """Copy-on-write: block dst[i] := block src[i] in every pool ([nbt, ...] tensors)."""
+    arr, n_pools, nbt, bb = _pool_array(pools)
+    n = src_blocks.numel()
+    if dst_blocks.numel() != n:
+        raise ValueError("src_blocks and dst_blocks differ in length")
+    _check(load().pkv_copy_blocks(arr, n_pools, _dev(src_blocks, "src_blocks", torch.int32),
+                                  _dev(dst_blocks, "dst_blocks", torch.int32), n, nbt, bb, _err(device_error),
+                                  _stream(stream)), "copy_blocks")
+
+
+def gather_blocks(pools, blocks, out, device_error=None, stream=None):
+    """Swap-out: out[q][i] = block blocks[i] of pool q; out holds len(pools) * len(blocks) blocks."""
+    arr, n_pools, nbt, bb = _pool_array(pools)
+    n = blocks.numel()
+    if out.numel() * out.element_size() != n_pools * n * bb:
+        raise ValueError("out must hold num_pools * num_blocks blocks")
+    _check(load().pkv_gather_blocks(arr, n_pools, _dev(blocks, "blocks", torch.int32), n, nbt, bb,
+                                    _buf(out, "out"), _err(device_error), _stream(stream)), "gather_blocks")
+
+
+def scatter_blocks(pools, blocks, inp, device_error=None, stream=None):
+    """Swap-in: block blocks[i] of pool q = inp[q][i] (the layout gather_blocks writes)."""
+    arr, n_pools, nbt, bb = _pool_array(pools)
+    n = blocks.numel()
+    if inp.numel() * inp.element_size() != n_pools * n * bb:
+        raise ValueError("inp must hold num_pools * num_blocks blocks")
+    _check(load().pkv_scatter_blocks(arr, n_pools, _dev(blocks, "blocks", torch.int32), n, nbt, bb,
+                                     _buf(inp, "inp"), _err(device_error), _stream(stream)), "scatter_blocks")

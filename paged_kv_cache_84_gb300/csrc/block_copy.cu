@@ -1,0 +1,99 @@
+// Block copies of the block manager, on every pool of a model at once.
+//
+// "vllm-lite README": blocks are reference counted and a write into a block
+// that two sequences share is preceded by a copy of it (copy-on-write),
+// which the runner performs before the forward pass.  "31. Engine v2",
+// "Preemption: recompute or swap": swap-out copies a preempted request's
+// blocks of every layer's K and V (and scales, when quantized) to host
+// memory; swap-in copies them into newly allocated blocks before the step.
+//
+// A pool is num_blocks_total blocks of block_bytes bytes (slot-major block
+// layout, so a block is one contiguous byte range).  One launch covers all
+// pools and all listed blocks: each thread moves four independent 16-byte
+// vectors per iteration (four loads in flight before the stores).
+#include "common.cuh"
+#include "sm100.cuh"
+
+namespace pkv {
+
+struct PoolList {
+    char *p[kMaxPools];
+};
+
+// mode 0: copy block src[i] -> dst[i] inside every pool; 1: gather block
+// ids[i] of pool q -> buf[q][i]; 2: scatter buf[q][i] -> block ids[i] of pool q
+template <int MODE>
+__global__ void __launch_bounds__(256) block_copy_kernel(const __grid_constant__ PoolList pools, int32_t num_pools,
+                                                         const int32_t *__restrict__ src, const int32_t *__restrict__ dst,
+                                                         int32_t n, int32_t nb_total, int64_t chunks_per_block,
+                                                         char *buf, uint32_t *err)
+{
+    pdl_wait();                                                   // block ids / data may come from the kernel before
+    pdl_launch_dependents();
+    const int64_t per_pool = (int64_t)n * chunks_per_block;
+    const int64_t total = per_pool * num_pools;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t c0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c0 < total; c0 += 4 * stride) {
+        uint4 v[4];
+        uint4 *to[4];
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+            to[u] = nullptr;
+            const int64_t c = c0 + u * stride;
+            if (c >= total) continue;
+            const int32_t q = (int32_t)(c / per_pool);
+            const int64_t r = c - (int64_t)q * per_pool;
+            const int32_t i = (int32_t)(r / chunks_per_block);
+            const int64_t off = r - (int64_t)i * chunks_per_block;
+            const uint4 *from;
+            if (MODE == 0) {
+                const int32_t s = __ldg(src + i), d = __ldg(dst + i);
+                if (s < 0 || s >= nb_total || d < 0 || d >= nb_total) {
+                    if (off == 0 && q == 0 && err) atomicOr(err, 2u);
+                    continue;
+                }
+                from = reinterpret_cast<const uint4 *>(pools.p[q]) + (int64_t)s * chunks_per_block + off;
+                to[u] = reinterpret_cast<uint4 *>(pools.p[q]) + (int64_t)d * chunks_per_block + off;
+            } else {
+                const int32_t b = __ldg(src + i);
+                if (b < 0 || b >= nb_total) {
+                    if (off == 0 && q == 0 && err) atomicOr(err, 2u);
+                    continue;
+                }
+                uint4 *blk = reinterpret_cast<uint4 *>(pools.p[q]) + (int64_t)b * chunks_per_block + off;
+                uint4 *flat = reinterpret_cast<uint4 *>(buf) + c;    // [pool][i][chunk]
+                from = MODE == 1 ? blk : flat;
+                to[u] = MODE == 1 ? flat : blk;
+            }
+            v[u] = *from;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; u++)
+            if (to[u]) *to[u] = v[u];
+    }
+}
+
+cudaError_t launch_block_copy(int mode, void *const *pools, int32_t num_pools, const int32_t *src,
+                              const int32_t *dst, int32_t n, int32_t nb_total, int64_t block_bytes, void *buf,
+                              uint32_t *err, cudaStream_t stream)
+{
+    if (n <= 0 || num_pools <= 0) return cudaSuccess;
+    PoolList pl;
+    for (int q = 0; q < kMaxPools; q++) pl.p[q] = q < num_pools ? static_cast<char *>(pools[q]) : nullptr;
+    const int64_t cpb = block_bytes / 16;
+    const int64_t total = cpb * n * num_pools;
+    int64_t blocks = (total + 4 * 256 - 1) / (4 * 256);
+    if (blocks > 152 * 16) blocks = 152 * 16;                     // grid-stride beyond 16 CTAs per SM
+    launch_begin(stream, kBlockCopy);
+    cudaError_t e;
+    char *b = static_cast<char *>(buf);
+    switch (mode) {
+    case 0: e = launch_maybe_pdl(block_copy_kernel<0>, dim3((unsigned)blocks), dim3(256), 0, stream, pl, num_pools, src, dst, n, nb_total, cpb, b, err); break;
+    case 1: e = launch_maybe_pdl(block_copy_kernel<1>, dim3((unsigned)blocks), dim3(256), 0, stream, pl, num_pools, src, dst, n, nb_total, cpb, b, err); break;
+    default: e = launch_maybe_pdl(block_copy_kernel<2>, dim3((unsigned)blocks), dim3(256), 0, stream, pl, num_pools, src, dst, n, nb_total, cpb, b, err); break;
+    }
+    launch_end(stream);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -132,6 +132,14 @@ cudaError_t launch_attn_tc(const AttnParams &p, const WorkList &wl, int num_item
                            const void *k_cache, const void *v_cache, int64_t num_slots, int head_dim,
                            cudaStream_t stream);
 
+// Block copies over up to kMaxPools pools: mode 0 copies block src[i] to
+// dst[i] in every pool, 1 gathers block src[i] of pool q to buf[q][i], 2
+// scatters buf[q][i] to block src[i] of pool q.
+constexpr int kMaxPools = 256;
+cudaError_t launch_block_copy(int mode, void *const *pools, int32_t num_pools, const int32_t *src,
+                              const int32_t *dst, int32_t n, int32_t nb_total, int64_t block_bytes, void *buf,
+                              uint32_t *err, cudaStream_t stream);
+
 // Merge split-KV partials of the split requests in `wl` into bf16 output.
 cudaError_t launch_attn_combine(const AttnParams &p, const WorkList &wl, int head_dim,
                                 int max_rows_per_req, cudaStream_t stream);
@@ -145,7 +153,8 @@ enum KernelId : int {
     kAttnTcPrefill = 4,
     kAttnMmaDecode = 5,
     kAttnMmaPrefill = 6,
-    kNumKernelIds = 7
+    kBlockCopy = 7,
+    kNumKernelIds = 8
 };
 
 // Call around every kernel launch: counts it and, while profiling is on,

@@ -190,6 +190,7 @@ const char *pkv_kernel_name(int32_t kernel_id)
     case kAttnTcPrefill: return "attn_tc_prefill";
     case kAttnMmaDecode: return "attn_mma_decode";
     case kAttnMmaPrefill: return "attn_mma_prefill";
+    case kBlockCopy: return "block_copy";
     }
     return "unknown";
 }
@@ -640,6 +641,55 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
     cudaError_t ej = join();
     if (ej != cudaSuccess) return cuda_fail(ej, "join");
     return PKV_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- block copies
+
+extern "C" {
+
+static pkv_status block_copy_common(int mode, void *const *pools, int32_t num_pools, const int32_t *src,
+                                    const int32_t *dst, int32_t n, int32_t num_blocks_total, size_t block_bytes,
+                                    void *buf, uint32_t *device_error, cudaStream_t stream)
+{
+    if (num_pools <= 0 || num_pools > PKV_MAX_POOLS || n < 0 || num_blocks_total <= 0 || block_bytes == 0 || !pools)
+        return PKV_ERR_INVALID_ARG;
+    if (n == 0) return PKV_OK;
+    if (!src || (mode == 0 && !dst) || (mode != 0 && !buf)) return PKV_ERR_INVALID_ARG;
+    if (block_bytes % 16 != 0 || (mode != 0 && !aligned(buf, 16))) return PKV_ERR_UNSUPPORTED;
+    for (int q = 0; q < num_pools; q++) {
+        if (!pools[q]) return PKV_ERR_INVALID_ARG;
+        if (!aligned(pools[q], 16)) return PKV_ERR_UNSUPPORTED;
+    }
+    if ((int64_t)block_bytes * num_blocks_total / 16 > ((int64_t)1 << 60)) return PKV_ERR_INVALID_ARG;
+    cudaError_t e = launch_block_copy(mode, pools, num_pools, src, dst, n, num_blocks_total, (int64_t)block_bytes,
+                                      buf, device_error, stream);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "block copy launch");
+}
+
+pkv_status pkv_copy_blocks(void *const *pools, int32_t num_pools, const int32_t *src_blocks,
+                           const int32_t *dst_blocks, int32_t num_pairs, int32_t num_blocks_total,
+                           size_t block_bytes, uint32_t *device_error, cudaStream_t stream)
+{
+    return block_copy_common(0, pools, num_pools, src_blocks, dst_blocks, num_pairs, num_blocks_total, block_bytes,
+                             nullptr, device_error, stream);
+}
+
+pkv_status pkv_gather_blocks(void *const *pools, int32_t num_pools, const int32_t *blocks, int32_t num_blocks,
+                             int32_t num_blocks_total, size_t block_bytes, void *out, uint32_t *device_error,
+                             cudaStream_t stream)
+{
+    return block_copy_common(1, pools, num_pools, blocks, nullptr, num_blocks, num_blocks_total, block_bytes, out,
+                             device_error, stream);
+}
+
+pkv_status pkv_scatter_blocks(void *const *pools, int32_t num_pools, const int32_t *blocks, int32_t num_blocks,
+                              int32_t num_blocks_total, size_t block_bytes, const void *in, uint32_t *device_error,
+                              cudaStream_t stream)
+{
+    return block_copy_common(2, pools, num_pools, blocks, nullptr, num_blocks, num_blocks_total, block_bytes,
+                             const_cast<void *>(in), device_error, stream);
 }
 
 }  // extern "C"

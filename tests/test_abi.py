@@ -103,3 +103,26 @@ def test_write_host_validation(lib):
     assert lib.pkv_paged_kv_write(fake, fake, fake, fake, fake, 3, 4, 60, 16, 10, None, None) == 2
     odd = ctypes.c_void_p((1 << 20) + 8)
     assert lib.pkv_paged_kv_write(odd, fake, fake, fake, fake, 3, 4, 64, 16, 10, None, None) == 2
+
+
+def test_block_copy_validation_on_host(lib):
+    """Block-copy calls reject bad arguments before touching the device."""
+    P = ctypes.c_void_p
+    fake = (P * 2)(1 << 20, 1 << 21)                 # never dereferenced: validation fails first
+    ids = P(1 << 22)
+    for fn in (lib.pkv_copy_blocks, lib.pkv_gather_blocks, lib.pkv_scatter_blocks):
+        fn.restype = ctypes.c_int
+    # zero pools, too many pools, zero block bytes: invalid
+    assert lib.pkv_copy_blocks(fake, 0, ids, ids, 4, 10, ctypes.c_size_t(512), None, None) == 1
+    assert lib.pkv_copy_blocks(fake, 257, ids, ids, 4, 10, ctypes.c_size_t(512), None, None) == 1
+    assert lib.pkv_copy_blocks(fake, 2, ids, ids, 4, 10, ctypes.c_size_t(0), None, None) == 1
+    # zero pairs: a no-op
+    assert lib.pkv_copy_blocks(fake, 2, ids, ids, 0, 10, ctypes.c_size_t(512), None, None) == 0
+    # missing destination list / buffer: invalid
+    assert lib.pkv_copy_blocks(fake, 2, ids, None, 4, 10, ctypes.c_size_t(512), None, None) == 1
+    assert lib.pkv_gather_blocks(fake, 2, ids, 4, 10, ctypes.c_size_t(512), None, None, None) == 1
+    # block bytes not a multiple of 16, or a misaligned buffer: unsupported
+    assert lib.pkv_copy_blocks(fake, 2, ids, ids, 4, 10, ctypes.c_size_t(520), None, None) == 2
+    assert lib.pkv_scatter_blocks(fake, 2, ids, 4, 10, ctypes.c_size_t(512), P((1 << 22) + 8), None, None) == 2
+    odd = (P * 2)(1 << 20, (1 << 21) + 4)
+    assert lib.pkv_copy_blocks(odd, 2, ids, ids, 4, 10, ctypes.c_size_t(512), None, None) == 2

@@ -376,3 +376,60 @@ def test_inconsistent_metadata_is_rejected():
     bad[0, 0] = P.kc.shape[0]                        # block id outside the pool
     with pytest.raises(ValueError):
         oracle.ragged_paged_attention(P.Q, P.kc, P.vc, P.meta.query_start_loc, P.meta.seq_lens, bad, 0.1)
+
+
+# ---------------------------------------------------------------- block copies
+# Copy-on-write and swap-out / swap-in of whole blocks ("vllm-lite README";
+# "31. Engine v2", "Preemption: recompute or swap").
+
+def _example_pool(nb, bb):
+    return torch.tensor([[10 * b + i for i in range(bb)] for b in range(nb)], dtype=torch.uint8)
+
+
+def test_block_copies_match_the_worked_example():
+    g = _golden("block_copy_example.txt")
+    nb, bb = g["blocks"][0][0], g["bytes"][0][0]
+    pool = _example_pool(nb, bb)
+    pairs = g["pair"]
+    oracle.copy_blocks([pool], [p[0] for p in pairs], [p[1] for p in pairs])
+    for row in g["after"]:
+        assert pool[row[0]].tolist() == row[1:]
+    pool = _example_pool(nb, bb)
+    out = oracle.gather_blocks([pool], g["gather"][0])
+    assert out[0].tolist() == g["gathered"]
+    pool = _example_pool(nb, bb)
+    oracle.scatter_blocks([pool], g["scatter"][0], torch.tensor([g["saved"]], dtype=torch.uint8))
+    for row in g["scattered"]:
+        assert pool[row[0]].tolist() == row[1:]
+
+
+def test_block_copies_against_torch_indexing_on_several_pools():
+    gen = torch.Generator().manual_seed(7)
+    # a layer's K and V pools (bf16, [nbt, bs, Hkv, d]); scale pools (fp32 [nbt, bs, Hkv])
+    # have other block bytes and go through their own call
+    groups = [[_bf16((12, 16, 2, 8), gen) for _ in range(2)],
+              [torch.rand((12, 16, 2), generator=gen) for _ in range(2)]]
+    for pools in groups:
+        ref = [p.clone() for p in pools]
+        src, dst = [3, 7, 11], [0, 5, 9]
+        oracle.copy_blocks(pools, src, dst)
+        for p, r in zip(pools, ref):
+            r.index_copy_(0, torch.tensor(dst), r.index_select(0, torch.tensor(src)))
+            assert torch.equal(p.view(torch.uint8), r.view(torch.uint8))
+        ids = [8, 2, 2, 10]
+        out = oracle.gather_blocks(pools, ids)
+        for q, p in enumerate(pools):
+            want = p.index_select(0, torch.tensor(ids)).contiguous().view(torch.uint8).view(len(ids), -1)
+            assert torch.equal(out[q], want)
+        # swap-out then swap-in into other blocks copies those blocks and nothing else
+        fresh = [p.clone() for p in pools]
+        oracle.scatter_blocks(fresh, [1, 4, 6, 0], out)
+        for p, f in zip(pools, fresh):
+            for a, b in zip(ids, [1, 4, 6, 0]):
+                assert torch.equal(f[b].view(torch.uint8), p[a].view(torch.uint8))
+            for b in set(range(12)) - {1, 4, 6, 0}:
+                assert torch.equal(f[b].view(torch.uint8), p[b].view(torch.uint8))
+    with pytest.raises(ValueError):
+        oracle.copy_blocks(groups[0], [12], [0])
+    with pytest.raises(ValueError):
+        oracle.gather_blocks(groups[0], [-1])
