@@ -42,10 +42,10 @@ def lib():
         L.oracle_paged_kv_write.argtypes = [c_p, c_p, c_p, c_p, c_p, c_i32, c_i32, c_i32, c_i32, c_i32]
         L.oracle_ragged_paged_attention.restype = ctypes.c_int
         L.oracle_ragged_paged_attention.argtypes = [c_p] + [c_p] * 3 + [c_p, c_p, c_p, c_i32] + \
-            [c_i32] * 7 + [c_dbl, c_i32]
+            [c_i32] * 7 + [c_dbl, c_i32, c_i32]
         L.oracle_attention_rows.restype = ctypes.c_int
         L.oracle_attention_rows.argtypes = [c_p, c_p, c_p, c_i32] + [c_p] * 3 + [c_p, c_p, c_p, c_i32] + \
-            [c_i32] * 7 + [c_dbl, c_i32]
+            [c_i32] * 7 + [c_dbl, c_i32, c_i32]
         L.oracle_max_threads.restype = ctypes.c_int
         L.oracle_max_threads.argtypes = []
         for name in ("oracle_copy_blocks", "oracle_gather_blocks", "oracle_scatter_blocks"):
@@ -94,8 +94,8 @@ def _meta_tensors(query_start_loc, seq_lens, block_table):
 
 
 def ragged_paged_attention(q, k_cache, v_cache, query_start_loc, seq_lens, block_table, scale,
-                           threads: int = 1) -> torch.Tensor:
-    """Returns float64 [N, Hq, d]."""
+                           threads: int = 1, window: int = 0) -> torch.Tensor:
+    """Returns float64 [N, Hq, d]; ``window`` > 0 keeps only keys above position - window."""
     n, hq, d = q.shape
     nbt, bs, hkv, _ = k_cache.shape
     qsl, sl, bt = _meta_tensors(query_start_loc, seq_lens, block_table)
@@ -103,14 +103,14 @@ def ragged_paged_attention(q, k_cache, v_cache, query_start_loc, seq_lens, block
     rc = lib().oracle_ragged_paged_attention(
         _ptr(out), _ptr(_bits(q)), _ptr(_bits(k_cache)), _ptr(_bits(v_cache)),
         _ptr(qsl), _ptr(sl), _ptr(bt), bt.shape[1], sl.numel(), n, hq, hkv, d, bs, nbt,
-        float(scale), threads)
+        float(scale), int(window), threads)
     if rc:
         raise ValueError(f"oracle_ragged_paged_attention: {rc}")
     return out
 
 
 def attention_rows(tokens, heads, q, k_cache, v_cache, query_start_loc, seq_lens, block_table, scale,
-                   threads: int = 1) -> torch.Tensor:
+                   threads: int = 1, window: int = 0) -> torch.Tensor:
     """Outputs of the listed (token, head) pairs only: float64 [len(tokens), d]."""
     n, hq, d = q.shape
     nbt, bs, hkv, _ = k_cache.shape
@@ -121,7 +121,7 @@ def attention_rows(tokens, heads, q, k_cache, v_cache, query_start_loc, seq_lens
     rc = lib().oracle_attention_rows(
         _ptr(out), _ptr(tk), _ptr(hd), tk.numel(), _ptr(_bits(q)), _ptr(_bits(k_cache)),
         _ptr(_bits(v_cache)), _ptr(qsl), _ptr(sl), _ptr(bt), bt.shape[1], sl.numel(), n, hq, hkv,
-        d, bs, nbt, float(scale), threads)
+        d, bs, nbt, float(scale), int(window), threads)
     if rc:
         raise ValueError(f"oracle_attention_rows: {rc}")
     return out

@@ -15,7 +15,9 @@
  *    step's rows to their slots, a slot of -1 (padding row) goes to the
  *    pool's last slot (scratch block); the reference backend gives
  *    request r's t queries positions seq_len - t + i, each sees keys
- *    0 .. its position, padding requests (seq_len 0 or no rows) leave zeros.
+ *    0 .. its position, padding requests (seq_len 0 or no rows) leave zeros;
+ *    with a sliding window w > 0 a query at position p sees only the keys
+ *    at positions above p - w (the backend's `window` argument).
  *  - vllm-lite README, grouped-query attention: query heads fold onto KV
  *    heads in contiguous groups, query head h reads KV head h / (Hq / Hkv).
  *  - attention itself: softmax(scale * q . k) weighted sum of v over the
@@ -88,12 +90,14 @@ struct problem {
     const int32_t *qsl, *seq_lens, *block_table;
     int32_t stride, num_reqs, num_tokens, hq, hkv, d, bs, nb_total;
     double scale;
+    int32_t window;                                 /* 0: none; else keys above p - window */
 };
 
 /*
  * Output row (token n, query head h) of request r: the query sits at
- * position p = L - t + i and attends to keys 0..p of its context, read
- * through the block table.  scores[] holds p + 1 doubles.
+ * position p = L - t + i and attends to keys j0..p of its context, read
+ * through the block table: j0 = 0, or with a sliding window w the first
+ * key above p - w.  scores[] holds p + 1 doubles.
  */
 static int attend_row(const struct problem *P, int32_t r, int32_t n, int32_t h,
                       double *scores, double *out_row)
@@ -112,8 +116,11 @@ static int attend_row(const struct problem *P, int32_t r, int32_t n, int32_t h,
     if (L == 0 || t == 0)
         return 0;                                   /* padding request: zeros */
 
+    int64_t j0 = 0;
+    if (P->window > 0 && p - P->window + 1 > 0)
+        j0 = p - P->window + 1;
     double m = -INFINITY;
-    for (int64_t j = 0; j <= p; j++) {
+    for (int64_t j = j0; j <= p; j++) {
         int32_t blk = table[j / P->bs];
         if (blk < 0 || blk >= P->nb_total)
             return -1;
@@ -128,12 +135,12 @@ static int attend_row(const struct problem *P, int32_t r, int32_t n, int32_t h,
             m = s;
     }
     double l = 0.0;
-    for (int64_t j = 0; j <= p; j++) {
+    for (int64_t j = j0; j <= p; j++) {
         double w = exp(scores[j] - m);
         scores[j] = w;
         l += w;
     }
-    for (int64_t j = 0; j <= p; j++) {
+    for (int64_t j = j0; j <= p; j++) {
         int32_t blk = table[j / P->bs];
         int64_t slot = (int64_t)blk * P->bs + j % P->bs;
         const uint16_t *vrow = P->v_cache + slot * slot_elems + (int64_t)kh * P->d;
@@ -147,7 +154,7 @@ static int attend_row(const struct problem *P, int32_t r, int32_t n, int32_t h,
 
 static int check_problem(const struct problem *P)
 {
-    if (P->hkv <= 0 || P->hq <= 0 || P->hq % P->hkv != 0 || P->d <= 0 || P->bs <= 0)
+    if (P->hkv <= 0 || P->hq <= 0 || P->hq % P->hkv != 0 || P->d <= 0 || P->bs <= 0 || P->window < 0)
         return -2;
     if (P->qsl[0] != 0 || P->qsl[P->num_reqs] != P->num_tokens)
         return -2;
@@ -199,11 +206,11 @@ int oracle_ragged_paged_attention(double *out, const uint16_t *q,
                                   int32_t num_reqs, int32_t num_tokens,
                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                   int32_t block_size, int32_t num_blocks_total,
-                                  double scale, int32_t nthreads)
+                                  double scale, int32_t window, int32_t nthreads)
 {
     struct problem P = {q, k_cache, v_cache, query_start_loc, seq_lens, block_table,
                         block_table_stride, num_reqs, num_tokens, num_q_heads, num_kv_heads,
-                        head_dim, block_size, num_blocks_total, scale};
+                        head_dim, block_size, num_blocks_total, scale, window};
     int rc = check_problem(&P);
     if (rc)
         return rc;
@@ -250,11 +257,11 @@ int oracle_attention_rows(double *out, const int32_t *tokens, const int32_t *hea
                           int32_t num_reqs, int32_t num_tokens,
                           int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                           int32_t block_size, int32_t num_blocks_total,
-                          double scale, int32_t nthreads)
+                          double scale, int32_t window, int32_t nthreads)
 {
     struct problem P = {q, k_cache, v_cache, query_start_loc, seq_lens, block_table,
                         block_table_stride, num_reqs, num_tokens, num_q_heads, num_kv_heads,
-                        head_dim, block_size, num_blocks_total, scale};
+                        head_dim, block_size, num_blocks_total, scale, window};
     int rc = check_problem(&P);
     if (rc)
         return rc;

@@ -170,14 +170,15 @@ class Problem:
         self.v_new = torch.cat([v[c:] for v, (c, t) in zip(self.V, plan)])
         oracle.paged_kv_write(self.kc, self.vc, self.k_new, self.v_new, self.meta.slot_mapping)
 
-    def oracle_out(self, threads=1):
+    def oracle_out(self, threads=1, window=0):
         return oracle.ragged_paged_attention(self.Q, self.kc, self.vc, self.meta.query_start_loc,
                                              self.meta.seq_lens, self.meta.block_table,
-                                             self.spec.scale, threads)
+                                             self.spec.scale, threads, window=window)
 
-    def brute_force(self):
-        """torch SDPA in float64 on contiguous K/V, explicit offset-causal mask,
-        GQA by repeating each KV head over its contiguous group of query heads."""
+    def brute_force(self, window=0):
+        """torch SDPA in float64 on contiguous K/V, explicit offset-causal mask
+        (restricted to keys above position - window when window > 0), GQA by
+        repeating each KV head over its contiguous group of query heads."""
         g = self.hq // self.hkv
         out = torch.zeros((self.meta.num_tokens, self.hq, self.d), dtype=torch.float64)
         for r, (c, t) in enumerate(self.plan):
@@ -191,6 +192,8 @@ class Problem:
             qpos = torch.arange(L - t, L)[:, None]
             kpos = torch.arange(L)[None, :]
             allowed = kpos <= qpos
+            if window > 0:
+                allowed = allowed & (kpos > qpos - window)
             y = F.scaled_dot_product_attention(q[None], k[None], v[None], attn_mask=allowed,
                                                scale=self.spec.scale)
             out[b:b + t] = y[0].transpose(0, 1)
@@ -433,3 +436,56 @@ def test_block_copies_against_torch_indexing_on_several_pools():
         oracle.copy_blocks(groups[0], [12], [0])
     with pytest.raises(ValueError):
         oracle.gather_blocks(groups[0], [-1])
+
+
+
+# ---------------------------------------------------------------- sliding window
+# "31. Engine v2", "Attention over the pool": with a sliding window w > 0 a
+# query at position p sees only the keys above p - w (and, causally, up to p).
+
+@pytest.mark.parametrize("window", [1, 3, 16, 40, 1000])
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 2)])
+def test_sliding_window_matches_dense_brute_force(window, hq, hkv):
+    plan = [(6, 3), (41, 1), (9, 1), (0, 4), (17, 15), (31, 2), (60, 20)]
+    P = Problem(plan, hq, hkv, 48, 16, seed=window + hq + hkv)
+    got = P.oracle_out(window=window)
+    want = P.brute_force(window=window)
+    assert (got - want).abs().max().item() < 1e-10
+
+
+def test_window_one_returns_own_value_and_wide_window_is_no_window():
+    P = Problem([(20, 5), (50, 1), (0, 9)], 4, 2, 64, 16, seed=44)
+    got = P.oracle_out(window=1)
+    g = 2
+    for r, (c, t) in enumerate(P.plan):
+        b = P.meta.query_start_loc[r]
+        for i in range(t):
+            for h in range(4):
+                # the only visible key is the query's own position c + i
+                assert torch.equal(got[b + i, h], P.V[r][c + i, h // g].double())
+    assert torch.equal(P.oracle_out(window=10 ** 6), P.oracle_out())
+    assert torch.equal(P.oracle_out(window=60), P.oracle_out())           # 60 > every position
+
+
+def test_sliding_window_chunk_invariance():
+    gen = torch.Generator().manual_seed(45)
+    L, hq, hkv, d, w = 150, 8, 2, 48, 37
+    K, V, Q = _bf16((L, hkv, d), gen), _bf16((L, hkv, d), gen), _bf16((L, hq, d), gen)
+    runs = []
+    for chunk in (8, 33, 4096):
+        nb = -(-L // 16) + 2
+        table = list(range(nb - 1, -1, -1))[: -(-L // 16)]
+        kc = torch.zeros((nb + 1, 16, hkv, d), dtype=torch.bfloat16)
+        vc = torch.zeros_like(kc)
+        outs, c = [], 0
+        while c < L:
+            t = min(chunk, L - c)
+            spec = Spec("chunk", [Req(c, t, table)], hq, hkv, d, 16, nb, 1 / math.sqrt(d), 0)
+            meta = build_meta(spec)
+            oracle.paged_kv_write(kc, vc, K[c:c + t], V[c:c + t], meta.slot_mapping)
+            outs.append(oracle.ragged_paged_attention(Q[c:c + t], kc, vc, meta.query_start_loc, meta.seq_lens,
+                                                      meta.block_table, spec.scale, window=w))
+            c += t
+        runs.append(torch.cat(outs))
+    for r in runs[1:]:
+        assert torch.equal(runs[0], r)
