@@ -156,13 +156,17 @@ size_t pkv_attention_workspace_bytes(int32_t max_num_reqs, int32_t max_num_token
  *   max_query_len, max_seq_len
  *                     maxima of the host arrays (validated)
  *   scale             softmax scale; <= 0 selects 1/sqrt(head_dim)
+ *   window            sliding window (the reference backend's `window`):
+ *                     0 for none; w > 0 limits the query at position p to
+ *                     the keys above p - w.  Negative: PKV_ERR_INVALID_ARG
  *   workspace         device memory, >= PKV_WORKSPACE_MIN_BYTES, 256-byte
  *                     aligned; its first 4 bytes are the device error word
  *                     (PKV_DEVERR_BLOCK), the rest holds split partials
  *
  * Row i of request r (t rows, L = seq_lens[r]) is the query at position
  * L - t + i.  Query head h reads KV head h / (num_q_heads / num_kv_heads)
- * and attends to the keys at positions 0 .. L - t + i.  A request with
+ * and attends to the keys at positions 0 .. L - t + i (with a window w,
+ * max(0, L - t + i - w + 1) .. L - t + i; keys below are not read).  A request with
  * L == 0 or t == 0 is padding: its rows of `out` are set to zero.
  * All keys a request reads must already be in the pool: call
  * pkv_paged_kv_write for the step first, on the same stream.
@@ -184,7 +188,7 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q,
                                       int32_t max_query_len, int32_t max_seq_len,
                                       int32_t num_q_heads, int32_t num_kv_heads,
                                       int32_t head_dim, int32_t block_size,
-                                      int32_t num_blocks_total, float scale,
+                                      int32_t num_blocks_total, float scale, int32_t window,
                                       void *workspace, size_t workspace_bytes,
                                       cudaStream_t stream);
 
@@ -226,7 +230,7 @@ pkv_status pkv_ragged_paged_attention_noalloc(void *out, const void *q,
                                               int32_t max_query_len, int32_t max_seq_len,
                                               int32_t num_q_heads, int32_t num_kv_heads,
                                               int32_t head_dim, int32_t block_size,
-                                              int32_t num_blocks_total, float scale,
+                                              int32_t num_blocks_total, float scale, int32_t window,
                                               uint32_t *device_error, cudaStream_t stream);
 
 /*

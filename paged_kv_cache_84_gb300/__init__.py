@@ -66,7 +66,7 @@ def load():
     L.pkv_attention_workspace_bytes.argtypes = [_c_i32] * 5
     L.pkv_ragged_paged_attention.restype = ctypes.c_int
     L.pkv_ragged_paged_attention.argtypes = [_c_p] * 7 + [_c_i32, _c_p, _c_p] + [_c_i32] * 9 + \
-        [_c_f, _c_p, _c_sz, _c_p]
+        [_c_f, _c_i32, _c_p, _c_sz, _c_p]
     L.pkv_clear_device_error.restype = ctypes.c_int
     L.pkv_clear_device_error.argtypes = [_c_p, _c_p]
     L.pkv_read_device_error.restype = ctypes.c_int
@@ -181,8 +181,9 @@ def make_workspace(nbytes: int, device=None) -> torch.Tensor:
 
 def ragged_paged_attention(out, q, k_cache, v_cache, query_start_loc, seq_lens, block_table,
                            query_start_loc_host, seq_lens_host, max_query_len, max_seq_len, scale,
-                           workspace, stream=None):
-    """Causal GQA attention of a flattened ragged batch over the paged pool; writes ``out``."""
+                           workspace, stream=None, window: int = 0):
+    """Causal GQA attention of a flattened ragged batch over the paged pool; writes ``out``.
+    ``window`` > 0 restricts the query at position p to the keys above p - window."""
     L = load()
     n, hq, d = q.shape
     nbt, bs, hkv, d2 = k_cache.shape
@@ -200,7 +201,7 @@ def ragged_paged_attention(out, q, k_cache, v_cache, query_start_loc, seq_lens, 
         _dev(query_start_loc, "query_start_loc", torch.int32), _dev(seq_lens, "seq_lens", torch.int32),
         _dev(block_table, "block_table", torch.int32), block_table.shape[1],
         _c_p(qsl_h.data_ptr()), _c_p(sl_h.data_ptr()), sl_h.numel(), n, int(max_query_len), int(max_seq_len),
-        hq, hkv, d, bs, nbt, float(scale), _dev(workspace, "workspace", torch.uint8), workspace.numel(),
+        hq, hkv, d, bs, nbt, float(scale), int(window), _dev(workspace, "workspace", torch.uint8), workspace.numel(),
         _stream(stream))
     _check(st, "ragged_paged_attention")
 

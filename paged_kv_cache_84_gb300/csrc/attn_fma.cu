@@ -77,15 +77,16 @@ __global__ void __launch_bounds__(kFmaThreads) attn_fma_kernel(AttnParams p,
         i0 = 0;
         nt = t;
         split = local;
-        k_begin = split * wl.split_tokens;
+        k_begin = decode_key_begin(t, L, p.window) + split * wl.split_tokens;
         k_end = min(L, k_begin + wl.split_tokens);
         partial = wl.part_off[li] >= 0;
     } else {
         i0 = local * wl.tile_tokens;
         nt = min(wl.tile_tokens, t - i0);
-        k_begin = 0;
+        k_begin = window_lo(L - t + i0, p.window) & ~15;  // the first row's window start
         k_end = L - t + i0 + nt;                  // one past the tile's last query position
     }
+    const int wspan = win_span(p.window);         // keys <= position - wspan are outside the window
     const int nr = nt * g;
 
     for (int idx = tid; idx < R * D; idx += kFmaThreads) {
@@ -162,7 +163,7 @@ __global__ void __launch_bounds__(kFmaThreads) attn_fma_kernel(AttnParams p,
         float alpha[R];
 #pragma unroll
         for (int rr = 0; rr < R; rr++) {
-            const float sv = (valid && j <= qpos[rr]) ? s[rr] : -INFINITY;
+            const float sv = (valid && j <= qpos[rr] && j > qpos[rr] - wspan) ? s[rr] : -INFINITY;
             const float mnew = fmaxf(m[rr], warp_max(sv));
             const float msafe = mnew == -INFINITY ? 0.f : mnew;
             alpha[rr] = exp2f(m[rr] - msafe);
@@ -309,7 +310,10 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnParams p,
     constexpr int EPL = FmaShape<D>::EPL;
     const int li = blockIdx.x;
     const int b = wl.qb[li], t = wl.qt[li], L = wl.len[li];
-    const int S = (L + wl.split_tokens - 1) / wl.split_tokens;
+    // decode-class requests split their (windowed) key range; every tile of a
+    // split prefill request has ceil(L / split) splits
+    const int S = wl.mode == kModeDecode ? decode_splits(t, L, p.window, wl.split_tokens)
+                                         : (L + wl.split_tokens - 1) / wl.split_tokens;
     const int rows = t * p.hq;
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.y * (blockDim.x / 32) + (threadIdx.x >> 5);

@@ -239,7 +239,7 @@ __device__ __forceinline__ void mma_epilogue(const AttnParams &p, const WorkList
     (void)kRT;
     if (!partial || wl.cnt_off[li] < 0) return;
     // ---- in-kernel split combine: count this split, the last one combines
-    const int S = (L + wl.split_tokens - 1) / wl.split_tokens;
+    const int S = decode_splits(t, L, p.window, wl.split_tokens);
     uint32_t *cnt = p.counters + (size_t)(wl.cnt_off[li] + kh) * kCounterStride;
     named_bar_sync(1, kThreads);                                  // every partial store of the CTA is issued
     if (threadIdx.x == 0) {
@@ -299,11 +299,12 @@ __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, con
         i0 = 0;
         ntok = t;
         split = local;
-        k_begin = split * wl.split_tokens;
+        k_begin = decode_key_begin(t, L, p.window) + split * wl.split_tokens;
         k_end = min(L, k_begin + wl.split_tokens);
         partial = wl.part_off[li] >= 0;
     } else {
-        // tile of new tokens; when split, every tile has the request's
+        // tile of new tokens, keys from the first row's window start (a
+        // block boundary); when split, every tile has the request's
         // ceil(L / split) splits and those past the tile's last position
         // leave empty partials (m = -inf, l = 0)
         const int S = wl.split_tokens > 0 ? (L + wl.split_tokens - 1) / wl.split_tokens : 1;
@@ -312,7 +313,8 @@ __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, con
         i0 = tile * wl.tile_tokens;
         ntok = min(wl.tile_tokens, t - i0);
         const int tend = L - t + i0 + ntok;                       // one past the tile's last position
-        k_begin = wl.split_tokens > 0 ? split * wl.split_tokens : 0;
+        const int kb = window_lo(L - t + i0, p.window) & ~15;
+        k_begin = kb + (wl.split_tokens > 0 ? split * wl.split_tokens : 0);
         k_end = wl.split_tokens > 0 ? min(tend, k_begin + wl.split_tokens) : tend;
         partial = wl.part_off[li] >= 0;
     }
@@ -383,6 +385,7 @@ __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, con
     const int qbase = L - t + i0;
     const int qposA = rA < nr ? qbase + rA / g : -1;
     const int qposB = rB < nr ? qbase + rB / g : -1;
+    const int wspan = win_span(p.window);                         // keys <= position - wspan are outside
 
     // Q as mma A fragments, straight from global memory (bf16 pairs).
     uint32_t qa[D / 16][4];
@@ -441,7 +444,7 @@ __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, con
             for (int v = 0; v < 4; v++) {
                 const int key = kc + (v & 1);
                 const int qp = v < 2 ? qposA : qposB;
-                const bool ok = has[n >> 1] && key < k_end && key <= qp;
+                const bool ok = has[n >> 1] && key < k_end && key <= qp && key > qp - wspan;
                 sc[n][v] = ok ? sc[n][v] * sl2 : -INFINITY;
             }
         }
@@ -559,13 +562,13 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
         i0 = 0;
         ntok = t;
         split = local;
-        k_begin = split * wl.split_tokens;
+        k_begin = decode_key_begin(t, L, p.window) + split * wl.split_tokens;
         k_end = min(L, k_begin + wl.split_tokens);
         partial = wl.part_off[li] >= 0;
     } else {
         i0 = local * wl.tile_tokens;
         ntok = min(wl.tile_tokens, t - i0);
-        k_begin = 0;
+        k_begin = window_lo(L - t + i0, p.window) & ~15;
         k_end = L - t + i0 + ntok;                                // one past the tile's last position
     }
     const int nr = ntok * g;                                      // rows of this CTA
@@ -638,6 +641,7 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
     const int qbase = L - t + i0;
     const int qposA = rA < nr ? qbase + rA / g : -1;
     const int qposB = rB < nr ? qbase + rB / g : -1;
+    const int wspan = win_span(p.window);                         // keys <= position - wspan are outside
 
     // Q as mma A fragments, straight from global memory (bf16 pairs).
     uint32_t qa[D / 16][4];
@@ -690,7 +694,7 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
                 for (int v = 0; v < 4; v++) {
                     const int key = kc + n * 8 + (v & 1);
                     const int qp = v < 2 ? qposA : qposB;
-                    sc[n][v] = (key < k_end && key <= qp) ? sc[n][v] * sl2 : -INFINITY;
+                    sc[n][v] = (key < k_end && key <= qp && key > qp - wspan) ? sc[n][v] * sl2 : -INFINITY;
                 }
             }
             float pr[2][4];

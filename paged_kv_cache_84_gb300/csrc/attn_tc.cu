@@ -106,10 +106,10 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
 }
 
 // Pass 1 of the softmax: max of the raw scores of NC columns of this
-// thread's S row (TMEM columns at ts, keys key0 ..); keys past qpos are
-// masked when MASK.
-template <bool MASK, int NC>
-__device__ __forceinline__ float tc_row_max(uint32_t ts, int key0, int qpos)
+// thread's S row (TMEM columns at ts, keys key0 ..); keys past qpos, and
+// keys at or below qlo (outside a sliding window, WIN), are masked when MASK.
+template <bool MASK, int NC, bool WIN>
+__device__ __forceinline__ float tc_row_max(uint32_t ts, int key0, int qpos, int qlo)
 {
     float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
@@ -121,8 +121,9 @@ __device__ __forceinline__ float tc_row_max(uint32_t ts, int key0, int qpos)
         for (int k = 0; k < 32; k += 2) {
             float s0 = __uint_as_float(v[k]), s1 = __uint_as_float(v[k + 1]);
             if (MASK) {
-                if (key0 + c * 32 + k > qpos) s0 = -INFINITY;
-                if (key0 + c * 32 + k + 1 > qpos) s1 = -INFINITY;
+                const int k0 = key0 + c * 32 + k;
+                if (k0 > qpos || (WIN && k0 <= qlo)) s0 = -INFINITY;
+                if (k0 + 1 > qpos || (WIN && k0 + 1 <= qlo)) s1 = -INFINITY;
             }
             m[(k >> 1) & 3] = max3f(m[(k >> 1) & 3], s0, s1);
         }
@@ -133,8 +134,8 @@ __device__ __forceinline__ float tc_row_max(uint32_t ts, int key0, int qpos)
 // Pass 2: P = 2^(s * sl2 - ms) for NC columns at ts, as bf16 pairs written
 // over the first NC/2 of them (each 16-column chunk goes over columns
 // already read); returns this row's sum of P over them.
-template <bool MASK, int NC>
-__device__ __forceinline__ float tc_row_exp(uint32_t ts, int key0, int qpos, float sl2, float ms)
+template <bool MASK, int NC, bool WIN>
+__device__ __forceinline__ float tc_row_exp(uint32_t ts, int key0, int qpos, int qlo, float sl2, float ms)
 {
     const uint64_t scale2 = f2_pack(sl2, sl2), neg2 = f2_pack(-ms, -ms);
     uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
@@ -148,8 +149,9 @@ __device__ __forceinline__ float tc_row_exp(uint32_t ts, int key0, int qpos, flo
         for (int k = 0; k < 8; k++) {
             float s0 = __uint_as_float(v[2 * k]), s1 = __uint_as_float(v[2 * k + 1]);
             if (MASK) {
-                if (key0 + c * 16 + 2 * k > qpos) s0 = -INFINITY;
-                if (key0 + c * 16 + 2 * k + 1 > qpos) s1 = -INFINITY;
+                const int k0 = key0 + c * 16 + 2 * k;
+                if (k0 > qpos || (WIN && k0 <= qlo)) s0 = -INFINITY;
+                if (k0 + 1 > qpos || (WIN && k0 + 1 <= qlo)) s1 = -INFINITY;
             }
             float t0, t1;
             f2_unpack(f2_fma(f2_pack(s0, s1), scale2, neg2), t0, t1);
@@ -215,8 +217,9 @@ __device__ __forceinline__ void tc_store_rows(const AttnParams &p, uint32_t to, 
     }
 }
 
-// DP: head dim padded to the 64-column sub-tile; D: head dim of q and out.
-template <int DP, int D>
+// DP: head dim padded to the 64-column sub-tile; D: head dim of q and out;
+// WIN: a sliding window is set (p.window > 0).
+template <int DP, int D, bool WIN>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, const __grid_constant__ WorkList wl,
                                                                 const __grid_constant__ CUtensorMap qmap,
                                                                 const __grid_constant__ CUtensorMap kmap,
@@ -247,13 +250,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, co
     const int ntok_b = max(0, min(tt, t - i0 - tt));
     const bool has_b = ntok_b > 0;
     const int k_end = L - t + i0 + ntok_a + ntok_b;                // one past the last position
-    const int nkt = (k_end + kTcKeys - 1) / kTcKeys;               // key tiles
-    const int nblk = (k_end + 15) >> 4;
+    // key tiles jt0 .. jt0 + nkt - 1: with a sliding window the first is the
+    // one holding the window start of the pair's first row
+    const int jt0 = window_lo(L - t + i0, p.window) / kTcKeys;
+    const int nkt = (k_end + kTcKeys - 1) / kTcKeys - jt0;
+    const int nblk = ((k_end + 15) >> 4) - jt0 * 8;                // blocks from key tile jt0 on
+    const int wspan = win_span(p.window);                          // keys <= position - wspan are outside
 
     if (threadIdx.x == 0) {
-        // P of tile a comes from 8 warps when a single tile splits its rows
+        // P of tile a comes from 8 warps when a single tile splits its rows;
+        // that tile then alternates P(j) between kBarPA (even j) and kBarPB
+        // (odd j): a warp may start tile j+1 (its S is double-buffered)
+        // before every warp has arrived for tile j
         for (int i = 0; i < kNumTcBars; i++)
-            mbar_init(bar(i), i == kBarPA ? (has_b ? 4u : 8u) : i == kBarPB ? 4u : 1u);
+            mbar_init(bar(i), (i == kBarPA || i == kBarPB) ? (has_b ? 4u : 8u) : 1u);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -292,7 +302,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, co
         // stage once the last PV MMA is: wait on those MMAs' own completion
         // barriers (their next completion needs a tile not loaded yet).
         const int done_bar = is_k ? (has_b ? kBarSB : kBarSA) : (has_b ? kBarOB : kBarOA);
-        const int32_t *bt = p.block_table + (size_t)r * p.bt_stride;
+        const int32_t *bt = p.block_table + (size_t)r * p.bt_stride + jt0 * 8;
         // this lane's box (lanes 0 .. 8 * kHalves - 1): block bi, column half
         const int bi = kHalves == 2 ? (lane >> 1) & 7 : lane & 7, half = kHalves == 2 ? lane & 1 : 0;
         // the block table is not written by the step's K/V scatter: the first
@@ -376,7 +386,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, co
                 tc_commit(bar(kBarSA + (j & 1)));
             };
             auto issue_pv1 = [&](int j) -> bool {                  // single tile: O += P(j) V_j
-                if (!mbar_wait(bar(kBarPA), j & 1, p.err)) return false;
+                if (!mbar_wait(bar(kBarPA + (j & 1)), (j >> 1) & 1, p.err)) return false;
                 if (!mbar_wait(bar(kBarV0 + (j & 1)), (j >> 1) & 1, p.err)) return false;
                 tc_fence_after();
                 const uint32_t vbase = sb + kVOff + (j & 1) * kTile;
@@ -442,6 +452,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, co
         const uint32_t ts = tl + x * 128;                          // S_x (and P_x) columns
         const uint32_t to = tl + 256 + x * 128;                    // O_x columns
         const int qpos = row < nr ? L - t + tok0 + row / g : -1;
+        const int qlo = qpos - wspan;                              // keys at or below are outside the window
         const float sl2 = p.scale_log2;
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
@@ -449,10 +460,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, co
             ok = mbar_wait(bar(kBarSA + x), j & 1, p.err);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
-            const int key0 = j * kTcKeys;
+            const int key0 = (jt0 + j) * kTcKeys;
             // warp-uniform: does any row of this warp see masked keys in this tile?
-            const bool diag = __any_sync(0xffffffffu, key0 + kTcKeys - 1 > qpos);
-            const float mraw = diag ? tc_row_max<true, 128>(ts, key0, qpos) : tc_row_max<false, 128>(ts, key0, qpos);
+            const bool diag = __any_sync(0xffffffffu, key0 + kTcKeys - 1 > qpos || (WIN && key0 <= qlo));
+            const float mraw = diag ? tc_row_max<true, 128, WIN>(ts, key0, qpos, qlo) : tc_row_max<false, 128, WIN>(ts, key0, qpos, qlo);
             const float mt = mraw * sl2;                            // in the exp2 domain (scale > 0)
             if (j == 0) {
                 m_used = mt;
@@ -473,7 +484,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, co
             }
             // pass 2: P = 2^(s * scale * log2e - m) over the first 64 S columns
             const float ms = m_used == -INFINITY ? 0.f : m_used;
-            l += diag ? tc_row_exp<true, 128>(ts, key0, qpos, sl2, ms) : tc_row_exp<false, 128>(ts, key0, qpos, sl2, ms);
+            l += diag ? tc_row_exp<true, 128, WIN>(ts, key0, qpos, qlo, sl2, ms) : tc_row_exp<false, 128, WIN>(ts, key0, qpos, qlo, sl2, ms);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kBarPA + x));
@@ -497,6 +508,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, co
         const uint32_t tl = tmem + ((uint32_t)(rg * 32) << 16);
         const uint32_t to = tl + 256;                              // O_a
         const int qpos = row < nr ? L - t + i0 + row / g : -1;
+        const int qlo = qpos - wspan;                              // keys at or below are outside the window
         const float sl2 = p.scale_log2;
         float *xm = reinterpret_cast<float *>(sp + C::kXOff);      // [parity][half][128]
         float *xl = xm + 512;                                      // [half][128]
@@ -505,12 +517,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, co
         for (int j = 0; j < nkt; j++) {
             const uint32_t ts = tl + (j & 1) * 128 + hc * 64;     // this half of S(j); P at its first 32 columns
             ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarSA + (j & 1)), (j >> 1) & 1, p.err));
-            const int key0 = j * kTcKeys + hc * 64;
-            const bool diag = __any_sync(0xffffffffu, key0 + 63 > qpos);
+            const int key0 = (jt0 + j) * kTcKeys + hc * 64;
+            const bool diag = __any_sync(0xffffffffu, key0 + 63 > qpos || (WIN && key0 <= qlo));
             float mh = -INFINITY;
             if (ok) {
                 tc_fence_after();
-                mh = diag ? tc_row_max<true, 64>(ts, key0, qpos) : tc_row_max<false, 64>(ts, key0, qpos);
+                mh = diag ? tc_row_max<true, 64, WIN>(ts, key0, qpos, qlo) : tc_row_max<false, 64, WIN>(ts, key0, qpos, qlo);
                 xm[((j & 1) * 2 + hc) * 128 + row] = mh;
             }
             if (!named_bar_and(2 + rg, 64, ok)) { ok = false; break; }
@@ -534,10 +546,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, co
                 }
             }
             const float ms = m_used == -INFINITY ? 0.f : m_used;
-            l += diag ? tc_row_exp<true, 64>(ts, key0, qpos, sl2, ms) : tc_row_exp<false, 64>(ts, key0, qpos, sl2, ms);
+            l += diag ? tc_row_exp<true, 64, WIN>(ts, key0, qpos, qlo, sl2, ms) : tc_row_exp<false, 64, WIN>(ts, key0, qpos, qlo, sl2, ms);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarPA));
+            if (lane == 0) mbar_arrive(bar(kBarPA + (j & 1)));
         }
         pdl_launch_dependents();
         if (ok) ok = mbar_wait(bar(kBarOFin), 0, p.err);
@@ -570,7 +582,7 @@ bool tc_prefill_supported(int head_dim, int group)
 }
 int tc_prefill_rows() { return kTcRows; }
 
-template <int DP, int D>
+template <int DP, int D, bool WIN>
 static cudaError_t launch_tc_d(const AttnParams &p, const WorkList &wl, int num_items, const void *q, int num_tokens,
                                const void *k_cache, const void *v_cache, int64_t num_slots, cudaStream_t stream)
 {
@@ -578,7 +590,7 @@ static cudaError_t launch_tc_d(const AttnParams &p, const WorkList &wl, int num_
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(attn_tc_kernel<DP, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        attr_err = cudaFuncSetAttribute(attn_tc_kernel<DP, D, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     });
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap qm, km, vm;
@@ -590,7 +602,7 @@ static cudaError_t launch_tc_d(const AttnParams &p, const WorkList &wl, int num_
     if (num_items > 65535) return cudaErrorInvalidConfiguration;
     dim3 grid(p.hkv, num_items);                   // items in launch order: the planner puts the longest first
     launch_begin(stream, kAttnTcPrefill);
-    e = launch_maybe_pdl(attn_tc_kernel<DP, D>, grid, dim3(kTcThreads), smem, stream, p, wl, qm, km, vm, num_slots);
+    e = launch_maybe_pdl(attn_tc_kernel<DP, D, WIN>, grid, dim3(kTcThreads), smem, stream, p, wl, qm, km, vm, num_slots);
     launch_end(stream);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -600,10 +612,17 @@ cudaError_t launch_attn_tc(const AttnParams &p, const WorkList &wl, int num_item
                            cudaStream_t stream)
 {
     if (num_items <= 0) return cudaSuccess;
+    const bool win = p.window > 0;
     switch (head_dim) {
-    case 48: return launch_tc_d<64, 48>(p, wl, num_items, q, num_tokens, k_cache, v_cache, num_slots, stream);
-    case 64: return launch_tc_d<64, 64>(p, wl, num_items, q, num_tokens, k_cache, v_cache, num_slots, stream);
-    case 128: return launch_tc_d<128, 128>(p, wl, num_items, q, num_tokens, k_cache, v_cache, num_slots, stream);
+    case 48:
+        return win ? launch_tc_d<64, 48, true>(p, wl, num_items, q, num_tokens, k_cache, v_cache, num_slots, stream)
+                   : launch_tc_d<64, 48, false>(p, wl, num_items, q, num_tokens, k_cache, v_cache, num_slots, stream);
+    case 64:
+        return win ? launch_tc_d<64, 64, true>(p, wl, num_items, q, num_tokens, k_cache, v_cache, num_slots, stream)
+                   : launch_tc_d<64, 64, false>(p, wl, num_items, q, num_tokens, k_cache, v_cache, num_slots, stream);
+    case 128:
+        return win ? launch_tc_d<128, 128, true>(p, wl, num_items, q, num_tokens, k_cache, v_cache, num_slots, stream)
+                   : launch_tc_d<128, 128, false>(p, wl, num_items, q, num_tokens, k_cache, v_cache, num_slots, stream);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -52,7 +52,36 @@ struct AttnParams {
     float *part_o;              // [rows][head_dim] unnormalised split outputs
     float2 *part_ml;            // [rows] (running max in exp2 domain, sum of weights)
     uint32_t *counters;         // split counters of in-kernel combines (zero between calls), or null
+    int32_t window;             // sliding window: keys above position - window (0: none)
 };
+
+// ---------------------------------------------------------------- sliding window
+//
+// "31. Engine v2", "Attention over the pool": with a window w > 0 the query
+// at position qp sees the keys qp - w + 1 .. qp.  Shared by the planner and
+// the kernels so that both count the same splits.
+
+// Lowest key the query at position qp sees.
+__host__ __device__ __forceinline__ int window_lo(int qp, int window)
+{
+    return (window > 0 && qp - window + 1 > 0) ? qp - window + 1 : 0;
+}
+
+// The mask bound: keys at or below qp - win_span(window) are outside the window.
+__host__ __device__ __forceinline__ int win_span(int window) { return window > 0 ? window : (1 << 30); }
+
+// First key of a decode-class request's key range (its t rows sit at
+// positions L - t .. L - 1), rounded down to a 16-key block.
+__host__ __device__ __forceinline__ int decode_key_begin(int t, int L, int window)
+{
+    return window_lo(L - t, window) & ~15;
+}
+
+// Splits of `split` keys that cover a decode-class request's key range.
+__host__ __device__ __forceinline__ int decode_splits(int t, int L, int window, int split)
+{
+    return L <= 0 ? 1 : (L - decode_key_begin(t, L, window) + split - 1) / split;
+}
 
 // ---------------------------------------------------------------- device helpers
 

@@ -50,7 +50,8 @@ extern "C" pkv_status pkv_ragged_paged_attention_noalloc(
     const int32_t *seq_lens, const int32_t *block_table, int32_t block_table_stride,
     const int32_t *query_start_loc_host, const int32_t *seq_lens_host, int32_t num_reqs, int32_t num_tokens,
     int32_t max_query_len, int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-    int32_t block_size, int32_t num_blocks_total, float scale, uint32_t *device_error, cudaStream_t stream)
+    int32_t block_size, int32_t num_blocks_total, float scale, int32_t window, uint32_t *device_error,
+    cudaStream_t stream)
 {
     // Size check on the host, before anything touches the device.
     size_t need = pkv_attention_workspace_bytes(num_reqs, num_tokens, num_q_heads, head_dim, max_seq_len);
@@ -65,8 +66,8 @@ extern "C" pkv_status pkv_ragged_paged_attention_noalloc(
     st = pkv_ragged_paged_attention(out, q, k_cache, v_cache, query_start_loc, seq_lens, block_table,
                                     block_table_stride, query_start_loc_host, seq_lens_host, num_reqs,
                                     num_tokens, max_query_len, max_seq_len, num_q_heads, num_kv_heads,
-                                    head_dim, block_size, num_blocks_total, scale, scratch, kScratchBytes,
-                                    stream);
+                                    head_dim, block_size, num_blocks_total, scale, window, scratch,
+                                    kScratchBytes, stream);
     if (st != PKV_OK) return st;
     cudaError_t e = cudaSuccess;
     if (device_error)

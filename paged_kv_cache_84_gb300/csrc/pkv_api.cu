@@ -309,12 +309,13 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
                                       const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs,
                                       int32_t num_tokens, int32_t max_query_len, int32_t max_seq_len,
                                       int32_t hq, int32_t hkv, int32_t d, int32_t bs,
-                                      int32_t num_blocks_total, float scale, void *workspace,
-                                      size_t workspace_bytes, cudaStream_t stream)
+                                      int32_t num_blocks_total, float scale, int32_t window,
+                                      void *workspace, size_t workspace_bytes, cudaStream_t stream)
 {
     // ---- host validation
     if (num_reqs < 0 || num_tokens < 0 || hq <= 0 || hkv <= 0 || d <= 0 || bs <= 0 || num_blocks_total <= 0)
         return PKV_ERR_INVALID_ARG;
+    if (window < 0) return PKV_ERR_INVALID_ARG;
     if (hq % hkv != 0) return PKV_ERR_INVALID_ARG;
     if (!qsl_h || (num_reqs > 0 && !sl_h)) return PKV_ERR_INVALID_ARG;
     if (qsl_h[0] != 0 || qsl_h[num_reqs] != num_tokens) return PKV_ERR_INVALID_ARG;
@@ -347,7 +348,7 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
         int32_t t = qsl_h[r + 1] - qsl_h[r], L = sl_h[r];
         switch (request_class(t, L, g, d)) {
         case PKV_CLASS_PADDING:
-        case PKV_CLASS_DECODE: dec.push_back(r); dec_keys += L; break;
+        case PKV_CLASS_DECODE: dec.push_back(r); dec_keys += L - decode_key_begin(t, L, window); break;
         case PKV_CLASS_PREFILL_CUDA_CORE: pre.push_back(r); break;
         case PKV_CLASS_PREFILL_TENSOR: tcp.push_back(r); break;
         default: break;                                         // no rows at all
@@ -374,7 +375,10 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
         split = (int)((s + 127) / 128 * 128);
     }
     if (split % bs) split += bs - split % bs;
+    // prefill tiles: every tile of a split request gets ceil(L / split) splits;
+    // decode-class requests: splits over their (windowed) key range
     auto splits_of = [&](int32_t L, int sp) { return L <= 0 ? 1 : (L + sp - 1) / sp; };
+    auto dec_splits_of = [&](int32_t r, int sp) { return decode_splits(qsl_h[r + 1] - qsl_h[r], sl_h[r], window, sp); };
     // Prefill-class tiles are split over keys as well when the batch has too
     // few of them to fill the GPU (small, latency-bound steps): every tile of
     // such a request gets the request's number of splits.
@@ -387,14 +391,13 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
     // every split request keeps S * t * hq partial rows; grow the split until they fit
     auto partial_rows = [&](int sp, bool *too_many) {
         size_t rows = 0;
-        auto add = [&](int32_t r) {
-            int32_t S = splits_of(sl_h[r], sp);
+        auto add = [&](int32_t r, int32_t S) {
             if (S > kMaxSplits) *too_many = true;
             if (S > 1) rows += (size_t)S * (qsl_h[r + 1] - qsl_h[r]) * hq;
         };
-        for (int32_t r : dec) add(r);
+        for (int32_t r : dec) add(r, dec_splits_of(r, sp));
         if (pre_split)
-            for (int32_t r : pre) add(r);
+            for (int32_t r : pre) add(r, splits_of(sl_h[r], sp));
         return rows;
     };
     const size_t row_bytes = (size_t)d * 4 + 8;
@@ -436,6 +439,7 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
     p.part_o = reinterpret_cast<float *>(ws + part_base);
     p.part_ml = reinterpret_cast<float2 *>(ws + part_base + ((total_rows * d * 4 + 15) / 16) * 16);
     p.counters = has_counters ? reinterpret_cast<uint32_t *>(ws + kErrBytes) : nullptr;
+    p.window = window;
 
     // ---- decode-class work runs on a side stream, concurrently with the
     // prefill kernels, when both are present: its CTAs fill the SMs that the
@@ -544,12 +548,13 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
         if (t * hq > set.max_rows) set.max_rows = t * hq;
         return off;
     };
-    // merge the split partials of one set of requests on `st`
-    auto launch_combines = [&](const CombineSet &set, cudaStream_t st) -> cudaError_t {
+    // merge the split partials of one set of requests on `st` (mode: the
+    // class the partials come from, which fixes their split count)
+    auto launch_combines = [&](const CombineSet &set, int mode, cudaStream_t st) -> cudaError_t {
         for (size_t c0 = 0; c0 < set.reqs.size(); c0 += kPlanMax) {
             WorkList wl;
             memset(&wl, 0, sizeof wl);
-            wl.mode = kModeDecode;
+            wl.mode = mode;
             wl.split_tokens = split;
             size_t c1 = c0 + kPlanMax < set.reqs.size() ? c0 + kPlanMax : set.reqs.size();
             for (size_t x = c0; x < c1; x++) {
@@ -574,7 +579,7 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
         for (size_t x = c0; x < c1; x++) {
             int32_t r = dec[x];
             int32_t t = qsl_h[r + 1] - qsl_h[r];
-            int32_t S = splits_of(sl_h[r], split);
+            int32_t S = dec_splits_of(r, split);
             int li = list_request(wl, r);
             wl.item_off[li] = items;
             // split decodes of the MMA kernels combine in the kernel (the CTA
@@ -597,7 +602,7 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
         }
     }
 
-    if (cudaError_t e = launch_combines(dec_combine, dstream); e != cudaSuccess) {
+    if (cudaError_t e = launch_combines(dec_combine, kModeDecode, dstream); e != cudaSuccess) {
         join();
         return cuda_fail(e, "split combine launch");
     }
@@ -634,7 +639,7 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
         return PKV_ERR_WORKSPACE;
     }
 
-    if (cudaError_t e = launch_combines(pre_combine, pstream); e != cudaSuccess) {
+    if (cudaError_t e = launch_combines(pre_combine, kModePrefill, pstream); e != cudaSuccess) {
         join();
         return cuda_fail(e, "split combine launch");
     }

@@ -21,8 +21,9 @@ def threads() -> int:
 class DeviceStep:
     """One batch resident on the GPU: pools, new rows, metadata, output, workspace."""
 
-    def __init__(self, batch: Batch, device="cuda", workspace_bytes=None, pools=None):
+    def __init__(self, batch: Batch, device="cuda", workspace_bytes=None, pools=None, window=0):
         self.batch = batch
+        self.window = window
         spec, meta = batch.spec, batch.meta
         dev = torch.device(device)
         if pools is None:
@@ -52,7 +53,7 @@ class DeviceStep:
         b = self.batch
         pkv.ragged_paged_attention(self.out, self.q, self.k_cache, self.v_cache, self.qsl, self.sl, self.bt,
                                    b.meta.query_start_loc, b.meta.seq_lens, b.meta.max_query_len,
-                                   b.meta.max_seq_len, b.spec.scale, self.ws)
+                                   b.meta.max_seq_len, b.spec.scale, self.ws, window=self.window)
 
     def step(self):
         self.write()
@@ -76,16 +77,17 @@ def oracle_write(batch_cpu: Batch):
                           batch_cpu.meta.slot_mapping)
 
 
-def oracle_full(batch_cpu: Batch) -> torch.Tensor:
+def oracle_full(batch_cpu: Batch, window: int = 0) -> torch.Tensor:
     m = batch_cpu.meta
     return oracle.ragged_paged_attention(batch_cpu.q, batch_cpu.k_cache, batch_cpu.v_cache, m.query_start_loc,
-                                         m.seq_lens, m.block_table, batch_cpu.spec.scale, threads())
+                                         m.seq_lens, m.block_table, batch_cpu.spec.scale, threads(), window=window)
 
 
-def oracle_rows(batch_cpu: Batch, tokens, heads) -> torch.Tensor:
+def oracle_rows(batch_cpu: Batch, tokens, heads, window: int = 0) -> torch.Tensor:
     m = batch_cpu.meta
     return oracle.attention_rows(tokens, heads, batch_cpu.q, batch_cpu.k_cache, batch_cpu.v_cache,
-                                 m.query_start_loc, m.seq_lens, m.block_table, batch_cpu.spec.scale, threads())
+                                 m.query_start_loc, m.seq_lens, m.block_table, batch_cpu.spec.scale, threads(),
+                                 window=window)
 
 
 def errors(got_bf16: torch.Tensor, want: torch.Tensor):

@@ -65,12 +65,12 @@ def test_host_only_functions(lib):
     assert pkv.plan_request_kernels([0, 6], [40], 9, 3, 64) == ["prefill_cuda_core"]
 
 
-def _attn_args(qsl, sl, R, N, maxq, maxl, hq=8, hkv=4, d=64, bs=16, stride=4, ws=1 << 20):
+def _attn_args(qsl, sl, R, N, maxq, maxl, hq=8, hkv=4, d=64, bs=16, stride=4, ws=1 << 20, window=0):
     fake = ctypes.c_void_p(1 << 20)                 # never dereferenced: validation fails first
     qsl_h = (ctypes.c_int32 * len(qsl))(*qsl)
     sl_h = (ctypes.c_int32 * max(1, len(sl)))(*sl)
     return [fake] * 7 + [stride, qsl_h, sl_h, R, N, maxq, maxl, hq, hkv, d, bs, 100, ctypes.c_float(0.1),
-                         fake, ctypes.c_size_t(ws), None]
+                         ctypes.c_int32(window), fake, ctypes.c_size_t(ws), None]
 
 
 @pytest.mark.parametrize("qsl,sl,maxq,maxl,kw", [
@@ -81,6 +81,7 @@ def _attn_args(qsl, sl, R, N, maxq, maxl, hq=8, hkv=4, d=64, bs=16, stride=4, ws
     ([0, 3, 4, 5], [9, 9, 9], 2, 9, {}),             # max_query_len below the data
     ([0, 3, 4, 5], [9, 9, 9], 3, 8, {}),             # max_seq_len below the data
     ([0, 3, 4, 5], [9, 9, 9], 3, 9, {"hkv": 3}),     # hq % hkv != 0
+    ([0, 3, 4, 5], [9, 9, 9], 3, 9, {"window": -1}), # negative window
 ])
 def test_attention_host_validation(lib, qsl, sl, maxq, maxl, kw):
     lib.pkv_ragged_paged_attention.restype = ctypes.c_int

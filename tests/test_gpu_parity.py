@@ -537,3 +537,78 @@ def test_short_chunks_on_tensor_cores(d, monkeypatch):
     oracle_write(ref)
     assert_close(dev.out, oracle_full(ref), f"short chunks d{d}")
     assert pkv.read_device_error(dev.ws) == 0
+
+
+# ------------------------------------------------------------------ sliding window
+
+WINDOW_CASES = [
+    # (random case index, window)
+    (0, 1), (1, 7), (2, 64), (3, 300), (5, 1000), (6, 100), (8, 129), (9, 40), (10, 256),
+]
+
+
+@pytest.mark.parametrize("case,window", WINDOW_CASES, ids=[f"seed{RANDOM_CASES[c][0]}-w{w}" for c, w in WINDOW_CASES])
+def test_sliding_window_random_mixes(case, window):
+    """The reference backend's window: the query at position p sees keys above
+    p - window.  Decodes (split and unsplit), warp-MMA and tcgen05 prefill."""
+    seed, reqs, max_ctx, max_new, hq, hkv, d, pad = RANDOM_CASES[case]
+    spec = random_spec(100 + seed, reqs, max_ctx, max_new, hq, hkv, d, pad_rows=pad)
+    b = make_batch(spec, device="cpu")
+    dev = DeviceStep(b, window=window)
+    dev.step()
+    ref = cpu_copy(b)
+    oracle_write(ref)
+    assert_close(dev.out, oracle_full(ref, window=window), f"window {window}")
+    assert pkv.read_device_error(dev.ws) == 0
+
+
+@pytest.mark.parametrize("path", ["split64", "split1024", "cuda-core", "prefill-split", "no-tcgen05"])
+def test_sliding_window_on_every_kernel_path(path, monkeypatch):
+    if path == "split64":
+        monkeypatch.setenv("PKV_SPLIT_TOKENS", "64")          # many decode splits, in-kernel combine
+    elif path == "split1024":
+        monkeypatch.setenv("PKV_SPLIT_TOKENS", "1024")        # streaming decode kernel
+    elif path == "cuda-core":
+        monkeypatch.setenv("PKV_ATTN_CUDA_CORE", "1")
+    elif path == "prefill-split":
+        monkeypatch.setenv("PKV_DISABLE_TCGEN05", "1")
+        monkeypatch.setenv("PKV_PREFILL_SPLIT", "1")
+        monkeypatch.setenv("PKV_SPLIT_TOKENS", "128")
+    else:
+        monkeypatch.setenv("PKV_DISABLE_TCGEN05", "1")
+    reqs = [Req(3000, 1, list(range(0, 188))), Req(700, 40, list(range(188, 235))),
+            Req(2500, 3, list(range(235, 392))), Req(0, 300, list(range(392, 411))),
+            Req(5000, 1, list(range(411, 724)))]
+    spec = Spec("window-paths", reqs, 16, 4, 128, 16, 730, 1 / math.sqrt(128), 51)
+    b = make_batch(spec, device="cpu")
+    ref = cpu_copy(b)
+    oracle_write(ref)
+    for window in (33, 500):
+        dev = DeviceStep(b, window=window)
+        dev.step()
+        assert_close(dev.out, oracle_full(ref, window=window), f"{path} window {window}")
+
+
+def test_negative_window_is_rejected():
+    b = make_batch(config_spec(1), device="cpu")
+    dev = DeviceStep(b, window=-1)
+    with pytest.raises(pkv.PkvError) as e:
+        dev.attend()
+    assert e.value.status == 1
+
+
+def test_long_decodes_with_window_sampled():
+    """The 32 x 32768 decode shape (8 requests) with a 4096-key window: each
+    decode reads only its last 4096 keys."""
+    from workloads import subset_spec
+    spec = subset_spec(config_spec(5), 8)
+    b = device_batch(spec)
+    ref = cpu_copy(b)
+    dev = DeviceStep(b, window=4096)
+    dev.step()
+    oracle_write(ref)
+    gen = torch.Generator().manual_seed(5)
+    toks, heads = _sample_rows(spec, b.meta, gen, per_req_heads=3)
+    want = oracle_rows(ref, toks, heads, window=4096)
+    got = dev.out[torch.tensor(toks), torch.tensor(heads)]
+    assert_close(got, want, "long decodes, window 4096")

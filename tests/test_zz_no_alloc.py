@@ -26,7 +26,7 @@ _p, _i32 = ctypes.c_void_p, ctypes.c_int32
 def _fn():
     fn = pkv.load().pkv_ragged_paged_attention_noalloc
     fn.restype = ctypes.c_int
-    fn.argtypes = [_p] * 7 + [_i32, _p, _p] + [_i32] * 9 + [ctypes.c_float, _p, _p]
+    fn.argtypes = [_p] * 7 + [_i32, _p, _p] + [_i32] * 9 + [ctypes.c_float, _i32, _p, _p]
     return fn
 
 
@@ -40,7 +40,7 @@ def _call(dev: DeviceStep, bt=None, device_error=None, max_seq_len=None):
                dev.qsl.data_ptr(), dev.sl.data_ptr(), bt.data_ptr(), bt.shape[1], qsl_h.data_ptr(),
                sl_h.data_ptr(), m.num_reqs, m.num_tokens, m.max_query_len,
                m.max_seq_len if max_seq_len is None else max_seq_len, s.num_q_heads, s.num_kv_heads,
-               s.head_dim, s.block_size, s.num_blocks_total, s.scale,
+               s.head_dim, s.block_size, s.num_blocks_total, s.scale, 0,
                None if device_error is None else device_error.data_ptr(),
                torch.cuda.current_stream().cuda_stream)
     return st, out
