@@ -48,6 +48,18 @@ def lib():
             [c_i32] * 7 + [c_dbl, c_i32, c_i32]
         L.oracle_max_threads.restype = ctypes.c_int
         L.oracle_max_threads.argtypes = []
+        L.oracle_e4m3_decode.restype = c_dbl
+        L.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        L.oracle_e4m3_encode.restype = ctypes.c_uint8
+        L.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        L.oracle_paged_kv_write_fp8.restype = ctypes.c_int
+        L.oracle_paged_kv_write_fp8.argtypes = [c_p] * 7 + [c_i32] * 5
+        L.oracle_ragged_paged_attention_fp8.restype = ctypes.c_int
+        L.oracle_ragged_paged_attention_fp8.argtypes = [c_p] * 6 + [c_p, c_p, c_p, c_i32] + [c_i32] * 7 + \
+            [c_dbl, c_i32, c_i32]
+        L.oracle_attention_rows_fp8.restype = ctypes.c_int
+        L.oracle_attention_rows_fp8.argtypes = [c_p, c_p, c_p, c_i32] + [c_p] * 5 + [c_p, c_p, c_p, c_i32] + \
+            [c_i32] * 7 + [c_dbl, c_i32, c_i32]
         for name in ("oracle_copy_blocks", "oracle_gather_blocks", "oracle_scatter_blocks"):
             f = getattr(L, name)
             f.restype = ctypes.c_int
@@ -168,3 +180,59 @@ def scatter_blocks(pools, blocks, inp: torch.Tensor):
         rc = lib().oracle_scatter_blocks(_ptr(raw), _ptr(src), _ptr(ids), ids.numel(), nbt, bb)
         if rc:
             raise ValueError(f"oracle_scatter_blocks: {rc}")
+
+
+# ---------------------------------------------------------------- quantized pools
+
+def e4m3_encode(x: float) -> int:
+    """fp32 value -> E4M3 code (round to nearest even, saturating at +-448)."""
+    return int(lib().oracle_e4m3_encode(float(x)))
+
+
+def e4m3_decode(code: int) -> float:
+    return float(lib().oracle_e4m3_decode(int(code) & 0xFF))
+
+
+def paged_kv_write_fp8(k_codes, v_codes, k_scale, v_scale, k, v, slot_mapping):
+    """Quantizing write on CPU pools: codes uint8 [nbt, bs, Hkv, d], scales float32 [nbt, bs, Hkv]."""
+    nbt, bs, hkv, d = k_codes.shape
+    for t in (k_codes, v_codes, k_scale, v_scale):
+        assert t.is_contiguous() and t.device.type == "cpu"
+    sm = slot_mapping.to(torch.int64).contiguous()
+    rc = lib().oracle_paged_kv_write_fp8(_ptr(k_codes), _ptr(v_codes), _ptr(k_scale), _ptr(v_scale),
+                                         _ptr(_bits(k)), _ptr(_bits(v)), _ptr(sm), sm.numel(), hkv, d, bs, nbt)
+    if rc:
+        raise ValueError(f"oracle_paged_kv_write_fp8: {rc}")
+
+
+def ragged_paged_attention_fp8(q, k_codes, v_codes, k_scale, v_scale, query_start_loc, seq_lens, block_table,
+                               scale, threads: int = 1, window: int = 0) -> torch.Tensor:
+    """Attention over a quantized pool; returns float64 [N, Hq, d]."""
+    n, hq, d = q.shape
+    nbt, bs, hkv, _ = k_codes.shape
+    qsl, sl, bt = _meta_tensors(query_start_loc, seq_lens, block_table)
+    out = torch.empty((n, hq, d), dtype=torch.float64)
+    rc = lib().oracle_ragged_paged_attention_fp8(
+        _ptr(out), _ptr(_bits(q)), _ptr(k_codes), _ptr(v_codes), _ptr(k_scale), _ptr(v_scale),
+        _ptr(qsl), _ptr(sl), _ptr(bt), bt.shape[1], sl.numel(), n, hq, hkv, d, bs, nbt,
+        float(scale), int(window), threads)
+    if rc:
+        raise ValueError(f"oracle_ragged_paged_attention_fp8: {rc}")
+    return out
+
+
+def attention_rows_fp8(tokens, heads, q, k_codes, v_codes, k_scale, v_scale, query_start_loc, seq_lens,
+                       block_table, scale, threads: int = 1, window: int = 0) -> torch.Tensor:
+    n, hq, d = q.shape
+    nbt, bs, hkv, _ = k_codes.shape
+    qsl, sl, bt = _meta_tensors(query_start_loc, seq_lens, block_table)
+    tk = torch.as_tensor(tokens, dtype=torch.int32).contiguous()
+    hd = torch.as_tensor(heads, dtype=torch.int32).contiguous()
+    out = torch.empty((tk.numel(), d), dtype=torch.float64)
+    rc = lib().oracle_attention_rows_fp8(
+        _ptr(out), _ptr(tk), _ptr(hd), tk.numel(), _ptr(_bits(q)), _ptr(k_codes), _ptr(v_codes),
+        _ptr(k_scale), _ptr(v_scale), _ptr(qsl), _ptr(sl), _ptr(bt), bt.shape[1], sl.numel(), n, hq, hkv,
+        d, bs, nbt, float(scale), int(window), threads)
+    if rc:
+        raise ValueError(f"oracle_attention_rows_fp8: {rc}")
+    return out

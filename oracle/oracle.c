@@ -84,14 +84,31 @@ int oracle_paged_kv_write(uint16_t *k_cache, uint16_t *v_cache,
     return 0;
 }
 
-/* Everything one attention row needs. */
+/* Everything one attention row needs.  A quantized pool gives k8/v8 codes
+ * and ks/vs scales instead of k_cache/v_cache. */
 struct problem {
     const uint16_t *q, *k_cache, *v_cache;
     const int32_t *qsl, *seq_lens, *block_table;
     int32_t stride, num_reqs, num_tokens, hq, hkv, d, bs, nb_total;
     double scale;
     int32_t window;                                 /* 0: none; else keys above p - window */
+    const uint8_t *k8, *v8;                         /* E4M3 codes, or NULL */
+    const float *ks, *vs;                           /* their per (slot, head) scales */
 };
+
+double oracle_e4m3_decode(uint8_t c);
+
+/* element e of the K (which = 0) or V (1) row of `slot`, KV head kh */
+static double pool_value(const struct problem *P, int which, int64_t slot, int32_t kh, int32_t e)
+{
+    int64_t row = slot * P->hkv + kh;
+    if (P->k8) {
+        const uint8_t *codes = which ? P->v8 : P->k8;
+        const float *scales = which ? P->vs : P->ks;
+        return oracle_e4m3_decode(codes[row * P->d + e]) * (double)scales[row];
+    }
+    return widen((which ? P->v_cache : P->k_cache)[row * P->d + e]);
+}
 
 /*
  * Output row (token n, query head h) of request r: the query sits at
@@ -109,7 +126,6 @@ static int attend_row(const struct problem *P, int32_t r, int32_t n, int32_t h,
     int64_t p = (int64_t)L - t + i;
     const uint16_t *qrow = P->q + ((int64_t)n * P->hq + h) * P->d;
     const int32_t *table = P->block_table + (int64_t)r * P->stride;
-    int64_t slot_elems = (int64_t)P->hkv * P->d;
 
     for (int32_t e = 0; e < P->d; e++)
         out_row[e] = 0.0;
@@ -125,10 +141,9 @@ static int attend_row(const struct problem *P, int32_t r, int32_t n, int32_t h,
         if (blk < 0 || blk >= P->nb_total)
             return -1;
         int64_t slot = (int64_t)blk * P->bs + j % P->bs;
-        const uint16_t *krow = P->k_cache + slot * slot_elems + (int64_t)kh * P->d;
         double s = 0.0;
         for (int32_t e = 0; e < P->d; e++)
-            s += widen(qrow[e]) * widen(krow[e]);
+            s += widen(qrow[e]) * pool_value(P, 0, slot, kh, e);
         s *= P->scale;
         scores[j] = s;
         if (s > m)
@@ -143,9 +158,8 @@ static int attend_row(const struct problem *P, int32_t r, int32_t n, int32_t h,
     for (int64_t j = j0; j <= p; j++) {
         int32_t blk = table[j / P->bs];
         int64_t slot = (int64_t)blk * P->bs + j % P->bs;
-        const uint16_t *vrow = P->v_cache + slot * slot_elems + (int64_t)kh * P->d;
         for (int32_t e = 0; e < P->d; e++)
-            out_row[e] += scores[j] * widen(vrow[e]);
+            out_row[e] += scores[j] * pool_value(P, 1, slot, kh, e);
     }
     for (int32_t e = 0; e < P->d; e++)
         out_row[e] /= l;
@@ -199,6 +213,8 @@ static int32_t max_seq(const struct problem *P)
  * Returns 0, -1 on an out-of-pool block id, -2 on inconsistent metadata,
  * -3 when memory runs out.
  */
+static int run_all_rows(const struct problem *PP, double *out, int32_t nthreads);
+
 int oracle_ragged_paged_attention(double *out, const uint16_t *q,
                                   const uint16_t *k_cache, const uint16_t *v_cache,
                                   const int32_t *query_start_loc, const int32_t *seq_lens,
@@ -210,7 +226,33 @@ int oracle_ragged_paged_attention(double *out, const uint16_t *q,
 {
     struct problem P = {q, k_cache, v_cache, query_start_loc, seq_lens, block_table,
                         block_table_stride, num_reqs, num_tokens, num_q_heads, num_kv_heads,
-                        head_dim, block_size, num_blocks_total, scale, window};
+                        head_dim, block_size, num_blocks_total, scale, window, NULL, NULL, NULL, NULL};
+    return run_all_rows(&P, out, nthreads);
+}
+
+/* The same attention over a quantized pool: keys and values are E4M3 codes
+ * times their (slot, head) scale, dequantized exactly in double. */
+int oracle_ragged_paged_attention_fp8(double *out, const uint16_t *q,
+                                      const uint8_t *k_codes, const uint8_t *v_codes,
+                                      const float *k_scale, const float *v_scale,
+                                      const int32_t *query_start_loc, const int32_t *seq_lens,
+                                      const int32_t *block_table, int32_t block_table_stride,
+                                      int32_t num_reqs, int32_t num_tokens,
+                                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                      int32_t block_size, int32_t num_blocks_total,
+                                      double scale, int32_t window, int32_t nthreads)
+{
+    struct problem P = {q, NULL, NULL, query_start_loc, seq_lens, block_table,
+                        block_table_stride, num_reqs, num_tokens, num_q_heads, num_kv_heads,
+                        head_dim, block_size, num_blocks_total, scale, window,
+                        k_codes, v_codes, k_scale, v_scale};
+    return run_all_rows(&P, out, nthreads);
+}
+
+static int run_all_rows(const struct problem *PP, double *out, int32_t nthreads)
+{
+    struct problem P = *PP;
+    int32_t num_tokens = P.num_tokens, num_q_heads = P.hq, head_dim = P.d;
     int rc = check_problem(&P);
     if (rc)
         return rc;
@@ -245,6 +287,9 @@ int oracle_ragged_paged_attention(double *out, const uint16_t *q,
     return status;
 }
 
+static int run_rows(const struct problem *PP, double *out, const int32_t *tokens, const int32_t *heads,
+                    int32_t count, int32_t nthreads);
+
 /*
  * Selected outputs only: for k < count, out[k][0..d) = output of row
  * tokens[k], query head heads[k].  Same arithmetic as above; for checking
@@ -261,7 +306,33 @@ int oracle_attention_rows(double *out, const int32_t *tokens, const int32_t *hea
 {
     struct problem P = {q, k_cache, v_cache, query_start_loc, seq_lens, block_table,
                         block_table_stride, num_reqs, num_tokens, num_q_heads, num_kv_heads,
-                        head_dim, block_size, num_blocks_total, scale, window};
+                        head_dim, block_size, num_blocks_total, scale, window, NULL, NULL, NULL, NULL};
+    return run_rows(&P, out, tokens, heads, count, nthreads);
+}
+
+/* Selected outputs over a quantized pool. */
+int oracle_attention_rows_fp8(double *out, const int32_t *tokens, const int32_t *heads, int32_t count,
+                              const uint16_t *q, const uint8_t *k_codes, const uint8_t *v_codes,
+                              const float *k_scale, const float *v_scale,
+                              const int32_t *query_start_loc, const int32_t *seq_lens,
+                              const int32_t *block_table, int32_t block_table_stride,
+                              int32_t num_reqs, int32_t num_tokens,
+                              int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                              int32_t block_size, int32_t num_blocks_total,
+                              double scale, int32_t window, int32_t nthreads)
+{
+    struct problem P = {q, NULL, NULL, query_start_loc, seq_lens, block_table,
+                        block_table_stride, num_reqs, num_tokens, num_q_heads, num_kv_heads,
+                        head_dim, block_size, num_blocks_total, scale, window,
+                        k_codes, v_codes, k_scale, v_scale};
+    return run_rows(&P, out, tokens, heads, count, nthreads);
+}
+
+static int run_rows(const struct problem *PP, double *out, const int32_t *tokens, const int32_t *heads,
+                    int32_t count, int32_t nthreads)
+{
+    struct problem P = *PP;
+    int32_t num_tokens = P.num_tokens, num_q_heads = P.hq, head_dim = P.d;
     int rc = check_problem(&P);
     if (rc)
         return rc;
@@ -353,6 +424,94 @@ int oracle_scatter_blocks(uint8_t *pool, const uint8_t *in, const int32_t *block
             return -1;
         for (int64_t b = 0; b < block_bytes; b++)
             pool[(int64_t)blocks[i] * block_bytes + b] = in[(int64_t)i * block_bytes + b];
+    }
+    return 0;
+}
+
+/*
+ * Quantized pools.  "31. Engine v2", "Attention over the pool": a quantized
+ * pool carries its scales next to K and V (cache[2], cache[3]), one per slot
+ * and KV head, and the reference backend dequantizes a gathered row as
+ * x.float() * scale.  The pages leave the code format and the quantizing
+ * write open; this oracle takes the plain reading used with an fp8 KV cache:
+ * FP8 E4M3 codes (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no
+ * infinities, largest finite 448), per (slot, head) scale = max |x| / 448
+ * computed in fp32, code = E4M3(x / scale) with the fp32 quotient rounded to
+ * nearest-even and clamped to +-448; a row of zeros gets scale 0 and codes 0.
+ */
+
+/* E4M3 code -> value (exact). */
+double oracle_e4m3_decode(uint8_t c)
+{
+    int sign = c >> 7, field = (c >> 3) & 15, man = c & 7;
+    double v;
+    if (field == 15 && man == 7)
+        return NAN;
+    if (field == 0)
+        v = man * ldexp(1.0, -9);                   /* subnormal: man/8 * 2^-6 */
+    else
+        v = (1.0 + man / 8.0) * ldexp(1.0, field - 7);
+    return sign ? -v : v;
+}
+
+/* round half to even of a non-negative double */
+static double round_half_even(double y)
+{
+    double f = floor(y), r = y - f;
+    if (r > 0.5 || (r == 0.5 && fmod(f, 2.0) != 0.0))
+        return f + 1.0;
+    return f;
+}
+
+/* fp32 value -> E4M3 code, round to nearest even, saturating at +-448. */
+uint8_t oracle_e4m3_encode(float x)
+{
+    uint8_t sign = signbit(x) ? 0x80 : 0;
+    double a = fabs((double)x);
+    if (a >= 448.0)
+        return sign | 0x7E;                          /* 1111.110 = 448 */
+    if (a < ldexp(1.0, -6)) {                        /* subnormal range: k * 2^-9 */
+        double k = round_half_even(a / ldexp(1.0, -9));
+        return sign | (uint8_t)k;                    /* k == 8 is 0x08, the smallest normal */
+    }
+    int e;
+    frexp(a, &e);                                    /* a = f * 2^e, f in [0.5, 1) */
+    e -= 1;                                          /* a = m * 2^e, m in [1, 2) */
+    double m3 = round_half_even((a / ldexp(1.0, e) - 1.0) * 8.0);
+    if (m3 == 8.0) {
+        m3 = 0.0;
+        e += 1;
+    }
+    return sign | (uint8_t)(((e + 7) << 3) | (int)m3);
+}
+
+/* the quantizing write: like oracle_paged_kv_write, with codes and scales */
+int oracle_paged_kv_write_fp8(uint8_t *k_cache, uint8_t *v_cache, float *k_scale, float *v_scale,
+                              const uint16_t *k, const uint16_t *v, const int64_t *slot_mapping,
+                              int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                              int32_t block_size, int32_t num_blocks_total)
+{
+    int64_t scratch = (int64_t)num_blocks_total * block_size - 1;
+    for (int32_t i = 0; i < num_tokens; i++) {
+        int64_t s = slot_mapping[i] >= 0 ? slot_mapping[i] : scratch;
+        if (s > scratch)
+            return -1;
+        for (int32_t h = 0; h < num_kv_heads; h++) {
+            for (int which = 0; which < 2; which++) {
+                const uint16_t *src = (which ? v : k) + ((int64_t)i * num_kv_heads + h) * head_dim;
+                uint8_t *dst = (which ? v_cache : k_cache) + (s * num_kv_heads + h) * head_dim;
+                float amax = 0.0f;
+                for (int32_t e = 0; e < head_dim; e++) {
+                    float a = fabsf((float)widen(src[e]));
+                    if (a > amax)
+                        amax = a;
+                }
+                float scale = amax / 448.0f;             /* fp32 division */
+                for (int32_t e = 0; e < head_dim; e++)
+                    dst[e] = scale > 0.0f ? oracle_e4m3_encode((float)widen(src[e]) / scale) : 0;
+                (which ? v_scale : k_scale)[s * num_kv_heads + h] = scale;
+            }
+        }
     }
     return 0;
 }

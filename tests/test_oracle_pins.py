@@ -489,3 +489,124 @@ def test_sliding_window_chunk_invariance():
         runs.append(torch.cat(outs))
     for r in runs[1:]:
         assert torch.equal(runs[0], r)
+
+
+# ---------------------------------------------------------------- quantized pool
+# "31. Engine v2", "Attention over the pool": quantized pools carry per
+# (slot, head) scales beside K and V, dequantized as code * scale.  Codes are
+# FP8 E4M3 (reading of the pages' open kv_cache_dtype); the write uses
+# scale = max|x| / 448 and rounds x / scale to nearest even.
+
+def test_e4m3_worked_examples():
+    rows = []
+    for line in open(os.path.join(GOLDEN, "e4m3_examples.txt")):
+        if line.startswith("value"):
+            _, v, c, d = line.split()
+            rows.append((float(v), int(c, 16), float(d)))
+    for v, c, d in rows:
+        assert oracle.e4m3_encode(v) == c, v
+        assert oracle.e4m3_decode(c) == d, c
+
+
+def test_e4m3_decode_matches_torch_float8_on_every_finite_code():
+    codes = torch.tensor([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=torch.uint8)
+    want = codes.view(torch.float8_e4m3fn).to(torch.float64)
+    got = torch.tensor([oracle.e4m3_decode(int(c)) for c in codes], dtype=torch.float64)
+    assert torch.equal(got, want)
+
+
+def test_e4m3_encode_matches_torch_float8_below_saturation():
+    gen = torch.Generator().manual_seed(61)
+    mags = torch.cat([torch.rand(3000, generator=gen) * 447.0,
+                      torch.exp2(torch.rand(3000, generator=gen) * 18 - 12)])   # 2^-12 .. 2^6
+    xs = mags * torch.where(torch.rand(6000, generator=gen) < 0.5, -1.0, 1.0)
+    xs = xs.to(torch.float32)
+    want = xs.to(torch.float8_e4m3fn).view(torch.uint8)
+    got = torch.tensor([oracle.e4m3_encode(float(x)) for x in xs], dtype=torch.uint8)
+    assert torch.equal(got, want)
+
+
+def test_quantizing_write_against_torch():
+    gen = torch.Generator().manual_seed(62)
+    nbt, bs, hkv, d, n = 9, 16, 4, 64, 30
+    k, v = _bf16((n, hkv, d), gen) * 3, _bf16((n, hkv, d), gen)
+    k[3, 1] = 0                                               # an all-zero row: scale 0, codes 0
+    slots = torch.randperm(nbt * bs - 1, generator=gen)[:n]
+    pools = [torch.zeros((nbt, bs, hkv, d), dtype=torch.uint8) for _ in range(2)] + \
+            [torch.zeros((nbt, bs, hkv), dtype=torch.float32) for _ in range(2)]
+    oracle.paged_kv_write_fp8(pools[0], pools[1], pools[2], pools[3], k, v, slots)
+    for x, codes, scales in ((k, pools[0], pools[2]), (v, pools[1], pools[3])):
+        xf = x.float()
+        amax = xf.abs().amax(dim=-1)
+        sc = amax / 448.0                                      # fp32, as the pages' scales
+        q = torch.where(sc[..., None] > 0, xf / torch.where(sc > 0, sc, 1.0)[..., None], 0.0)
+        want = q.clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+        flat_c = codes.view(-1, hkv, d)[slots]
+        flat_s = scales.view(-1, hkv)[slots]
+        assert torch.equal(flat_c, want)
+        assert torch.equal(flat_s, sc)
+    # dequantized values are within half a code step of the inputs: 2^-4 of
+    # the value for normal codes, half the smallest subnormal (2^-10) times
+    # the scale below them
+    sc = pools[2].view(-1, hkv)[slots][..., None].double()
+    deq = pools[0].view(-1, hkv, d)[slots].view(torch.float8_e4m3fn).double() * sc
+    assert ((deq - k.double()).abs() <= k.double().abs() / 16 + sc * 2.0 ** -10).all()
+
+
+def _fp8_problem(plan, hq, hkv, d, seed):
+    """A quantized pool written by the oracle's quantizing write from random
+    bf16 K/V (history, then this step's rows); returns everything the
+    attention needs and the dequantized dense K/V per request."""
+    gen = torch.Generator().manual_seed(seed)
+    bs = 16
+    nblk = [-(-(c + t) // bs) for c, t in plan]
+    nb = sum(nblk) + 2
+    perm = torch.randperm(nb, generator=gen).tolist()
+    tables, cur = [], 0
+    for n in nblk:
+        tables.append(perm[cur:cur + n])
+        cur += n
+    reqs = [Req(c, t, tab) for (c, t), tab in zip(plan, tables)]
+    spec = Spec("fp8", reqs, hq, hkv, d, bs, nb, 1.0 / math.sqrt(d), seed)
+    meta = build_meta(spec)
+    kc = torch.randint(0, 255, (nb + 1, bs, hkv, d), generator=gen, dtype=torch.uint8)
+    kc[(kc & 0x7F) == 0x7F] = 0                               # junk codes, never NaN
+    vc = torch.randint(0, 255, (nb + 1, bs, hkv, d), generator=gen, dtype=torch.uint8)
+    vc[(vc & 0x7F) == 0x7F] = 0
+    ks = torch.rand((nb + 1, bs, hkv), generator=gen)
+    vs = torch.rand((nb + 1, bs, hkv), generator=gen)
+    K = [_bf16((c + t, hkv, d), gen) for c, t in plan]
+    V = [_bf16((c + t, hkv, d), gen) for c, t in plan]
+    hist = build_meta(Spec("hist", [Req(0, c, tab) for (c, t), tab in zip(plan, tables)], hq, hkv, d, bs, nb, 1.0, 0))
+    if hist.num_tokens:
+        oracle.paged_kv_write_fp8(kc, vc, ks, vs, torch.cat([k[:c] for k, (c, t) in zip(K, plan)]),
+                                  torch.cat([v[:c] for v, (c, t) in zip(V, plan)]), hist.slot_mapping)
+    oracle.paged_kv_write_fp8(kc, vc, ks, vs, torch.cat([k[c:] for k, (c, t) in zip(K, plan)]),
+                              torch.cat([v[c:] for v, (c, t) in zip(V, plan)]), meta.slot_mapping)
+    q = _bf16((meta.num_tokens, hq, d), gen)
+    return spec, meta, q, kc, vc, ks, vs
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 2)])
+def test_fp8_attention_matches_dense_dequantized_brute_force(hq, hkv):
+    plan = [(6, 3), (41, 1), (0, 4), (17, 15), (60, 1)]
+    spec, meta, q, kc, vc, ks, vs = _fp8_problem(plan, hq, hkv, 64, 63 + hq + hkv)
+    got = oracle.ragged_paged_attention_fp8(q, kc, vc, ks, vs, meta.query_start_loc, meta.seq_lens,
+                                            meta.block_table, spec.scale)
+    g = hq // hkv
+    for r, (c, t) in enumerate(plan):
+        L, b = c + t, meta.query_start_loc[r]
+        slots = [meta.block_table[r, j // 16].item() * 16 + j % 16 for j in range(L)]
+        # dequantize through torch's float8 type, independently of the oracle
+        k = kc.view(-1, hkv, 64)[slots].view(torch.float8_e4m3fn).double() * ks.view(-1, hkv)[slots][..., None].double()
+        v = vc.view(-1, hkv, 64)[slots].view(torch.float8_e4m3fn).double() * vs.view(-1, hkv)[slots][..., None].double()
+        qq = q[b:b + t].double().transpose(0, 1)[None]
+        kk = k.repeat_interleave(g, dim=1).transpose(0, 1)[None]
+        vv = v.repeat_interleave(g, dim=1).transpose(0, 1)[None]
+        mask = torch.arange(L)[None, :] <= torch.arange(L - t, L)[:, None]
+        want = F.scaled_dot_product_attention(qq, kk, vv, attn_mask=mask, scale=spec.scale)[0].transpose(0, 1)
+        assert (got[b:b + t] - want).abs().max().item() < 1e-10
+    # sampled rows equal the full computation
+    rows = oracle.attention_rows_fp8([0, 5, 12], [1, 0, hq - 1], q, kc, vc, ks, vs, meta.query_start_loc,
+                                     meta.seq_lens, meta.block_table, spec.scale)
+    assert torch.equal(rows, torch.stack([got[0, 1], got[5, 0], got[12, hq - 1]]))
