@@ -479,6 +479,75 @@ def e2e_workload(pkv, copies, steps, device):
             "path": "pinned host -> device copies, pkv_paged_kv_write + pkv_ragged_paged_attention, device -> pinned host"}
 
 
+def fp8_workload(pkv, cfg, device, peaks, steps=20):
+    """The decode workload `cfg` on a quantized pool: the whole bf16 pool is
+    quantized once by the library's quantizing write, then each timed step is
+    the quantizing write of the step's rows + attention over E4M3 codes and
+    per (slot, head) scales, one CUDA graph of `steps` steps."""
+    spec = config_spec(cfg)
+    b = make_batch(spec, device=device)
+    m = b.meta
+    nbt, bs, hkv, d = b.k_cache.shape
+    kc = torch.empty((nbt, bs, hkv, d), dtype=torch.uint8, device=device)
+    vc = torch.empty_like(kc)
+    ks = torch.empty((nbt, bs, hkv), dtype=torch.float32, device=device)
+    vs = torch.empty_like(ks)
+    all_slots = torch.arange(nbt * bs, dtype=torch.int64, device=device)
+    for s0 in range(0, nbt * bs, 1 << 20):                 # quantize the pool in slices
+        sl = all_slots[s0:s0 + (1 << 20)]
+        pkv.paged_kv_write_fp8(b.k_cache.view(-1, hkv, d)[sl], b.v_cache.view(-1, hkv, d)[sl], kc, vc, ks, vs, sl)
+    del b.k_cache, b.v_cache
+    torch.cuda.empty_cache()
+    q, k, v = b.q.to(device), b.k.to(device), b.v.to(device)
+    slots = m.slot_mapping.to(device)
+    qsl = torch.tensor(m.query_start_loc, dtype=torch.int32, device=device)
+    sln = torch.tensor(m.seq_lens, dtype=torch.int32, device=device)
+    bt = m.block_table.to(device)
+    out = torch.empty_like(q)
+    ws = pkv.make_workspace(pkv.attention_workspace_bytes(m.num_reqs, m.num_tokens, spec.num_q_heads, d,
+                                                          m.max_seq_len), device)
+
+    def step():
+        pkv.paged_kv_write_fp8(k, v, kc, vc, ks, vs, slots)
+        pkv.ragged_paged_attention_fp8(out, q, kc, vc, ks, vs, qsl, sln, bt, m.query_start_loc, m.seq_lens,
+                                       m.max_query_len, m.max_seq_len, spec.scale, ws)
+
+    stream = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        for _ in range(steps):
+            step()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    step_s = e0.elapsed_time(e1) / steps / 1e3
+    # algorithmic bytes: every unique slot read once (codes of K and V + their scales), q, out, the write
+    used = set()
+    for r in range(m.num_reqs):
+        L = m.seq_lens[r]
+        used.update(m.block_table[r, :(L + bs - 1) // bs].tolist())
+    kv_bytes = sum(min(bs, max(0, m.seq_lens[r] - j * bs)) for r in range(m.num_reqs)
+                   for j in range((m.seq_lens[r] + bs - 1) // bs)) * hkv * (2 * d + 8)
+    other = 2 * q.numel() * 2 + m.num_tokens * hkv * (2 * d * 2 + 2 * d + 8)
+    res = {"workload": spec.name, "step_us": step_s * 1e6, "query_tokens_per_s": m.num_tokens / step_s,
+           "kv_bytes": kv_bytes, "kv_read_gbs": kv_bytes / step_s / 1e9,
+           "step_hbm_frac": (kv_bytes + other) / step_s / 1e9 / peaks["hbm_gbs"],
+           "pool": "E4M3 codes + fp32 scale per (slot, head)"}
+    del kc, vc, ks, vs, q, k, v, out, ws, g
+    torch.cuda.empty_cache()
+    return res
+
+
 def block_copy_workload(pkv, device, peaks, reps=20):
     """Copy-on-write and swap-out/in of whole blocks over 8 pools (4 layers' K and V, 16 x 8 heads x
     128 dims per block = 32 KB), 1 GB of pools: the block copies of the block manager, timed with CUDA
@@ -617,8 +686,10 @@ def run_ours(args):
 
     breakdown = {}
     block_copies = None
+    fp8 = None
     if not args.no_breakdown:
         block_copies = block_copy_workload(pkv, device, peaks)
+        fp8 = {str(c): fp8_workload(pkv, c, device, peaks) for c in (3, 5)}
         for cfg in (1, 2, 3, 4, 5):
             if cfg == args.workload:
                 r = dict(head)
@@ -653,7 +724,7 @@ def run_ours(args):
         "roofline": head["roofline"], "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": head["launches_per_step"] * args.steps,
         "clocks": clocks.summary(t0, t1), "peaks": peaks, "kernels": head["kernels"],
-        "workloads": breakdown, "block_copies": block_copies,
+        "workloads": breakdown, "block_copies": block_copies, "fp8_pool": fp8,
     }
     print(json.dumps(line), flush=True)
     if dist is not None:

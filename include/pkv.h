@@ -118,6 +118,29 @@ pkv_status pkv_paged_kv_write(const void *k, const void *v, void *k_cache, void 
                               cudaStream_t stream);
 
 /*
+ * Quantized pools ("31. Engine v2", "Attention over the pool": a quantized
+ * pool carries one scale per slot and KV head beside K and V, and a row is
+ * read as code * scale).  Codes are FP8 E4M3 bytes, the pools uint8
+ * [num_blocks_total][block_size][num_kv_heads][head_dim]; scales are fp32
+ * [num_blocks_total][block_size][num_kv_heads].  The pages leave the code
+ * format and the quantizing write open; this library's reading: per row
+ * and KV head, scale = max |x| / 448 in fp32 and code = E4M3(x / scale)
+ * rounded to nearest even, saturating at +-448 (an all-zero row: scale 0,
+ * codes 0).
+ *
+ * pkv_paged_kv_write_fp8 — the quantizing write_kv: k, v bf16
+ *   [num_tokens][num_kv_heads][head_dim] -> codes at slot_mapping[i] (a
+ *   negative slot: the scratch slot), scales beside them.  Requirements:
+ *   head_dim 128; k, v, k_cache, v_cache 16-byte aligned.  Errors as
+ *   pkv_paged_kv_write.
+ */
+pkv_status pkv_paged_kv_write_fp8(const void *k, const void *v, void *k_cache, void *v_cache,
+                                  float *k_scale, float *v_scale, const int64_t *slot_mapping,
+                                  int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                                  int32_t block_size, int32_t num_blocks_total, uint32_t *device_error,
+                                  cudaStream_t stream);
+
+/*
  * Workspace size that lets pkv_ragged_paged_attention split long decodes
  * over KV freely for any batch within the given maxima.  A smaller
  * workspace (at least PKV_WORKSPACE_MIN_BYTES) is accepted: the planner
@@ -191,6 +214,33 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q,
                                       int32_t num_blocks_total, float scale, int32_t window,
                                       void *workspace, size_t workspace_bytes,
                                       cudaStream_t stream);
+
+/*
+ * ragged_paged_attention over a quantized pool (codes and scales as written
+ * by pkv_paged_kv_write_fp8).  Arguments as pkv_ragged_paged_attention plus
+ * the two scale pools (device fp32, 16-byte aligned).  Keys and values are
+ * code * scale; q, out stay bf16.  The products run on fp16 tensor-core MMAs
+ * (every E4M3 value is an fp16 value; q rounds to fp16 exactly within its
+ * range), so |q| and the per-key weight * V scale must stay inside fp16's
+ * range (65504).  Requirements (else PKV_ERR_UNSUPPORTED): head_dim 128,
+ * num_kv_heads a multiple of 4 and at most 16; the CUDA-core kernels
+ * (PKV_ATTN_CUDA_CORE) have no quantized path.  Prefill chunks run on the
+ * warp-level MMA kernels, not on tcgen05.
+ */
+pkv_status pkv_ragged_paged_attention_fp8(void *out, const void *q,
+                                          const void *k_cache, const void *v_cache,
+                                          const float *k_scale, const float *v_scale,
+                                          const int32_t *query_start_loc, const int32_t *seq_lens,
+                                          const int32_t *block_table, int32_t block_table_stride,
+                                          const int32_t *query_start_loc_host,
+                                          const int32_t *seq_lens_host,
+                                          int32_t num_reqs, int32_t num_tokens,
+                                          int32_t max_query_len, int32_t max_seq_len,
+                                          int32_t num_q_heads, int32_t num_kv_heads,
+                                          int32_t head_dim, int32_t block_size,
+                                          int32_t num_blocks_total, float scale, int32_t window,
+                                          void *workspace, size_t workspace_bytes,
+                                          cudaStream_t stream);
 
 /*
  * ragged_paged_attention without a caller workspace.  The pages have no

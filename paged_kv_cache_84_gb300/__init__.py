@@ -17,7 +17,7 @@ __all__ = [
     "PkvError", "load", "paged_kv_write", "ragged_paged_attention", "attention_workspace_bytes",
     "make_workspace", "read_device_error", "clear_device_error", "launch_count", "LIB_PATH",
     "DEVERR_SLOT", "DEVERR_BLOCK", "DEVERR_TIMEOUT", "DEVERR_META", "DEVERR_COUNTER", "WORKSPACE_MIN_BYTES", "profile_start", "profile_stop",
-    "plan_request_kernels", "CLASS_NAMES", "copy_blocks", "gather_blocks", "scatter_blocks", "MAX_POOLS",
+    "plan_request_kernels", "CLASS_NAMES", "paged_kv_write_fp8", "ragged_paged_attention_fp8", "copy_blocks", "gather_blocks", "scatter_blocks", "MAX_POOLS",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpkv.so")
@@ -81,6 +81,11 @@ def load():
     L.pkv_kernel_name.argtypes = [_c_i32]
     L.pkv_plan_request_kernels.restype = ctypes.c_int
     L.pkv_plan_request_kernels.argtypes = [_c_p, _c_p, _c_i32, _c_i32, _c_i32, _c_i32, _c_p]
+    L.pkv_paged_kv_write_fp8.restype = ctypes.c_int
+    L.pkv_paged_kv_write_fp8.argtypes = [_c_p] * 7 + [_c_i32] * 5 + [_c_p, _c_p]
+    L.pkv_ragged_paged_attention_fp8.restype = ctypes.c_int
+    L.pkv_ragged_paged_attention_fp8.argtypes = [_c_p] * 9 + [_c_i32, _c_p, _c_p] + [_c_i32] * 9 + \
+        [_c_f, _c_i32, _c_p, _c_sz, _c_p]
     L.pkv_copy_blocks.restype = ctypes.c_int
     L.pkv_copy_blocks.argtypes = [_c_p, _c_i32, _c_p, _c_p, _c_i32, _c_i32, _c_sz, _c_p, _c_p]
     L.pkv_gather_blocks.restype = ctypes.c_int
@@ -280,3 +285,47 @@ def scatter_blocks(pools, blocks, inp, device_error=None, stream=None):
         raise ValueError("inp must hold num_pools * num_blocks blocks")
     _check(load().pkv_scatter_blocks(arr, n_pools, _dev(blocks, "blocks", torch.int32), n, nbt, bb,
                                      _buf(inp, "inp"), _err(device_error), _stream(stream)), "scatter_blocks")
+
+
+
+def paged_kv_write_fp8(k, v, k_codes, v_codes, k_scale, v_scale, slot_mapping, device_error=None, stream=None):
+    """Quantizing write: k, v bf16 [N, Hkv, d] -> E4M3 codes uint8 [nbt, bs, Hkv, d] and fp32 scales
+    [nbt, bs, Hkv] at ``slot_mapping``."""
+    L = load()
+    n, hkv, d = k.shape
+    nbt, bs, hkv2, d2 = k_codes.shape
+    if (hkv2, d2) != (hkv, d) or v.shape != k.shape or v_codes.shape != k_codes.shape:
+        raise ValueError("shape mismatch between k/v and the pools")
+    if k_scale.shape != (nbt, bs, hkv) or v_scale.shape != (nbt, bs, hkv):
+        raise ValueError("scale pools must be [num_blocks, block_size, num_kv_heads]")
+    st = L.pkv_paged_kv_write_fp8(_dev(k, "k", torch.bfloat16), _dev(v, "v", torch.bfloat16),
+                                  _dev(k_codes, "k_codes", torch.uint8), _dev(v_codes, "v_codes", torch.uint8),
+                                  _dev(k_scale, "k_scale", torch.float32), _dev(v_scale, "v_scale", torch.float32),
+                                  _dev(slot_mapping, "slot_mapping", torch.int64), n, hkv, d, bs, nbt,
+                                  _err(device_error), _stream(stream))
+    _check(st, "paged_kv_write_fp8")
+
+
+def ragged_paged_attention_fp8(out, q, k_codes, v_codes, k_scale, v_scale, query_start_loc, seq_lens,
+                               block_table, query_start_loc_host, seq_lens_host, max_query_len, max_seq_len,
+                               scale, workspace, stream=None, window: int = 0):
+    """ragged_paged_attention over a quantized pool (E4M3 codes times per (slot, head) scales)."""
+    L = load()
+    n, hq, d = q.shape
+    nbt, bs, hkv, d2 = k_codes.shape
+    if out.shape != q.shape or d2 != d or v_codes.shape != k_codes.shape:
+        raise ValueError("shape mismatch")
+    qsl_h = _host_i32(query_start_loc_host, "query_start_loc_host")
+    sl_h = _host_i32(seq_lens_host, "seq_lens_host")
+    if qsl_h.numel() != sl_h.numel() + 1:
+        raise ValueError("query_start_loc needs num_reqs + 1 entries")
+    st = L.pkv_ragged_paged_attention_fp8(
+        _dev(out, "out", torch.bfloat16), _dev(q, "q", torch.bfloat16),
+        _dev(k_codes, "k_codes", torch.uint8), _dev(v_codes, "v_codes", torch.uint8),
+        _dev(k_scale, "k_scale", torch.float32), _dev(v_scale, "v_scale", torch.float32),
+        _dev(query_start_loc, "query_start_loc", torch.int32), _dev(seq_lens, "seq_lens", torch.int32),
+        _dev(block_table, "block_table", torch.int32), block_table.shape[1],
+        _c_p(qsl_h.data_ptr()), _c_p(sl_h.data_ptr()), sl_h.numel(), n, int(max_query_len), int(max_seq_len),
+        hq, hkv, d, bs, nbt, float(scale), int(window), _dev(workspace, "workspace", torch.uint8),
+        workspace.numel(), _stream(stream))
+    _check(st, "ragged_paged_attention_fp8")

@@ -38,29 +38,36 @@ constexpr int kMmaThreads = (kConsumerWarps + 1) * 32;
 constexpr int kStageBudget = 96 * 1024;      // bytes of KV stages per CTA (two CTAs per SM)
 constexpr int kLongSplit = 512;              // decode splits of at least this many keys use the streaming kernel
 
-template <int D>
+// Quantized pools: FP8 E4M3 K/V (one byte per element) with an fp32 scale
+// per (slot, KV head); a block's scales of every KV head are staged with it.
+constexpr int kFp8MaxHkv = 16;
+
+template <int D, bool FP8 = false>
 struct MmaTile {
-    static constexpr bool kSwizzle = D != 48;
-    static constexpr int kBoxCols = kSwizzle ? 64 : D;       // columns per TMA box
+    static constexpr int kElem = FP8 ? 1 : 2;
+    static constexpr int kRowBytes = D * kElem;
+    static constexpr bool kSwizzle = kRowBytes % 128 == 0;   // rows of 128-byte boxes, 128-byte swizzle
+    static constexpr int kBoxCols = kSwizzle ? 128 / kElem : D;   // columns per TMA box
     static constexpr int kBoxes = D / kBoxCols;              // boxes per 16-row slice
-    static constexpr int kBoxBytes = 16 * kBoxCols * 2;
-    static constexpr int kTile = 16 * D * 2;                 // one K (or V) slice
-    static constexpr int kSlot = 2 * kTile;                  // K then V
+    static constexpr int kBoxBytes = 16 * kBoxCols * kElem;
+    static constexpr int kTile = 16 * kRowBytes;             // one K (or V) slice
+    static constexpr int kScaleTile = FP8 ? 16 * kFp8MaxHkv * 4 : 0;   // [16 slots][Hkv] fp32
+    static constexpr int kSlot = 2 * kTile + 2 * kScaleTile; // K, V, K scales, V scales
 };
 
 // Byte offset of 16-byte chunk `chunk` of row `row` inside a K or V slice.
-template <int D>
+template <int D, bool FP8 = false>
 __device__ __forceinline__ uint32_t tile_off(int row, int chunk)
 {
-    if constexpr (D == 48) {
-        return row * 96 + chunk * 16;
+    if constexpr (!MmaTile<D, FP8>::kSwizzle) {
+        return row * MmaTile<D, FP8>::kRowBytes + chunk * 16;
     } else {
         const int box = chunk >> 3, c = chunk & 7;
         return box * 2048 + row * 128 + ((c ^ (row & 7)) << 4);
     }
 }
 
-template <int D, int KG, int NB>
+template <int D, int KG, int NB, bool FP8 = false>
 struct MmaCfg {
     static constexpr int kRT = kConsumerWarps / KG;                          // row tiles
     // Ring of one-block slots: this kernel serves short, latency-bound key
@@ -68,36 +75,130 @@ struct MmaCfg {
     // blocks in flight, small enough for several CTAs per SM.
     static constexpr int kSlots = KG * NB + KG + 4;
     static_assert(kSlots >= KG * NB + KG, "the ring must hold an iteration of every key group plus one block each");
-    static constexpr int kRingBytes = kSlots * MmaTile<D>::kSlot;
+    static constexpr int kRingBytes = kSlots * MmaTile<D, FP8>::kSlot;
     static constexpr int kMergeBytes = kConsumerWarps * 16 * (D + 2) * 4;
     static constexpr int kBodyBytes = kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes;
     static constexpr int kSmemBytes = 1024 + kBodyBytes + 2 * kSlots * 8;   // + alignment slack, barriers
 };
 
-// S for one 16-key block: sc[0], sc[1] = the two 8-key n-tiles.
-template <int D>
-__device__ __forceinline__ void block_scores(float (&sc0)[4], float (&sc1)[4], const uint32_t (&qa)[D / 16][4],
-                                             uint32_t kt, int mi, int mr)
+// Q rows rA / rB of this lane as m16n8k16 A fragments.  bf16 pools: bf16
+// pairs in the natural head-dim order.  FP8 pools (fp16 MMAs): the head
+// dims of every 16-wide chunk are taken in the order that an ldmatrix of the
+// FP8 K rows delivers (lane quad c holds dims 4c .. 4c+3: 4c, 4c+1 as MMA
+// k = 2c, 2c+1 and 4c+2, 4c+3 as k = 2c+8, 2c+9); the sum over the head
+// dim does not depend on the order.
+template <int D, bool FP8>
+__device__ __forceinline__ void load_q_frags(uint32_t (&qa)[D / 16][4], const __nv_bfloat16 *q, size_t rowA,
+                                             size_t rowB, bool okA, bool okB, int lane)
 {
+    const int c = lane & 3;
+    if constexpr (!FP8) {
+        const uint32_t *qw = reinterpret_cast<const uint32_t *>(q);
 #pragma unroll
-    for (int kk = 0; kk < D / 16; kk++) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(kt + tile_off<D>((mi >> 1) * 8 + mr, 2 * kk + (mi & 1)), b0, b1, b2, b3);
-        mma_16816(sc0, qa[kk], b0, b1);
-        mma_16816(sc1, qa[kk], b2, b3);
+        for (int kk = 0; kk < D / 16; kk++) {
+            qa[kk][0] = okA ? __ldg(qw + rowA * (D / 2) + kk * 8 + c) : 0u;
+            qa[kk][1] = okB ? __ldg(qw + rowB * (D / 2) + kk * 8 + c) : 0u;
+            qa[kk][2] = okA ? __ldg(qw + rowA * (D / 2) + kk * 8 + 4 + c) : 0u;
+            qa[kk][3] = okB ? __ldg(qw + rowB * (D / 2) + kk * 8 + 4 + c) : 0u;
+        }
+    } else {
+        const uint2 *q4 = reinterpret_cast<const uint2 *>(q);      // 4 bf16 per load
+#pragma unroll
+        for (int kk = 0; kk < D / 16; kk++) {
+            const uint2 a = okA ? __ldg(q4 + rowA * (D / 4) + kk * 4 + c) : make_uint2(0u, 0u);
+            const uint2 bb = okB ? __ldg(q4 + rowB * (D / 4) + kk * 4 + c) : make_uint2(0u, 0u);
+            qa[kk][0] = pack_f16x2(bf16_lo(a.x), bf16_hi(a.x));
+            qa[kk][1] = pack_f16x2(bf16_lo(bb.x), bf16_hi(bb.x));
+            qa[kk][2] = pack_f16x2(bf16_lo(a.y), bf16_hi(a.y));
+            qa[kk][3] = pack_f16x2(bf16_lo(bb.y), bf16_hi(bb.y));
+        }
     }
 }
 
-// O += P V for one 16-key block.
-template <int D>
+// S for one 16-key block: sc[0], sc[1] = the two 8-key n-tiles.  FP8: the
+// codes go through an fp16 MMA (exact conversion); the K scales are applied
+// by the caller.
+template <int D, bool FP8 = false>
+__device__ __forceinline__ void block_scores(float (&sc0)[4], float (&sc1)[4], const uint32_t (&qa)[D / 16][4],
+                                             uint32_t kt, int mi, int mr)
+{
+    if constexpr (!FP8) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; kk++) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(kt + tile_off<D>((mi >> 1) * 8 + mr, 2 * kk + (mi & 1)), b0, b1, b2, b3);
+            mma_16816(sc0, qa[kk], b0, b1);
+            mma_16816(sc1, qa[kk], b2, b3);
+        }
+    } else {
+        // matrix mi: n-tile mi & 1, 16-dim chunk kk + (mi >> 1); a lane gets
+        // 4 codes (dims 4c .. 4c+3) of key row lane / 4
+#pragma unroll
+        for (int kk = 0; kk < D / 16; kk += 2) {
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4(kt + tile_off<D, true>((mi & 1) * 8 + mr, kk + (mi >> 1)), r0, r1, r2, r3);
+            mma_16816_f16(sc0, qa[kk], e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r0 >> 16));
+            mma_16816_f16(sc1, qa[kk], e4m3x2_to_f16x2(r1), e4m3x2_to_f16x2(r1 >> 16));
+            mma_16816_f16(sc0, qa[kk + 1], e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r2 >> 16));
+            mma_16816_f16(sc1, qa[kk + 1], e4m3x2_to_f16x2(r3), e4m3x2_to_f16x2(r3 >> 16));
+        }
+    }
+}
+
+// O += P V for one 16-key block.  FP8: a transposed ldmatrix of the codes
+// gives a lane 2 keys x 2 adjacent dims; a byte permute splits them into the
+// even-dim and the odd-dim B fragments, so O's n-tile 2q holds the even and
+// 2q+1 the odd dims of 16-dim chunk q (see o_col).  P comes with the V
+// scales folded in (fp16).
+template <int D, bool FP8 = false>
 __device__ __forceinline__ void block_pv(float (&o)[D / 8][4], const uint32_t (&pa)[4], uint32_t vt, int mi, int mr)
 {
+    if constexpr (!FP8) {
 #pragma unroll
-    for (int np = 0; np < D / 16; np++) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vt + tile_off<D>((mi & 1) * 8 + mr, 2 * np + (mi >> 1)), b0, b1, b2, b3);
-        mma_16816(o[2 * np], pa, b0, b1);
-        mma_16816(o[2 * np + 1], pa, b2, b3);
+        for (int np = 0; np < D / 16; np++) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(vt + tile_off<D>((mi & 1) * 8 + mr, 2 * np + (mi >> 1)), b0, b1, b2, b3);
+            mma_16816(o[2 * np], pa, b0, b1);
+            mma_16816(o[2 * np + 1], pa, b2, b3);
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < D / 16; q += 2) {
+            uint32_t r0, r1, r2, r3;       // keys 0-7 / 8-15 of chunk q, then of chunk q + 1
+            ldsm_x4_t(vt + tile_off<D, true>((mi & 1) * 8 + mr, q + (mi >> 1)), r0, r1, r2, r3);
+            const uint32_t a0 = prmt(r0, 0u, 0x3120u), a1 = prmt(r1, 0u, 0x3120u);
+            const uint32_t c0 = prmt(r2, 0u, 0x3120u), c1 = prmt(r3, 0u, 0x3120u);
+            mma_16816_f16(o[2 * q], pa, e4m3x2_to_f16x2(a0), e4m3x2_to_f16x2(a1));
+            mma_16816_f16(o[2 * q + 1], pa, e4m3x2_to_f16x2(a0 >> 16), e4m3x2_to_f16x2(a1 >> 16));
+            mma_16816_f16(o[2 * q + 2], pa, e4m3x2_to_f16x2(c0), e4m3x2_to_f16x2(c1));
+            mma_16816_f16(o[2 * q + 3], pa, e4m3x2_to_f16x2(c0 >> 16), e4m3x2_to_f16x2(c1 >> 16));
+        }
+    }
+}
+
+// Head dim of accumulator o[n][2 hr + j] of lane quad c.
+template <bool FP8>
+__device__ __forceinline__ int o_col(int n, int c, int j)
+{
+    return FP8 ? 16 * (n >> 1) + 4 * c + 2 * j + (n & 1) : n * 8 + 2 * c + j;
+}
+
+// P fragments (A operand of PV) from the probabilities of two 8-key n-tiles;
+// FP8 pools fold each key's V scale in and use fp16.
+template <bool FP8>
+__device__ __forceinline__ void pack_p(uint32_t (&pa)[4], const float (&p0)[4], const float (&p1)[4],
+                                       const float (&vs0)[2], const float (&vs1)[2])
+{
+    if constexpr (!FP8) {
+        pa[0] = pack_bf16x2(p0[0], p0[1]);
+        pa[1] = pack_bf16x2(p0[2], p0[3]);
+        pa[2] = pack_bf16x2(p1[0], p1[1]);
+        pa[3] = pack_bf16x2(p1[2], p1[3]);
+    } else {
+        pa[0] = pack_f16x2(p0[0] * vs0[0], p0[1] * vs0[1]);
+        pa[1] = pack_f16x2(p0[2] * vs0[0], p0[3] * vs0[1]);
+        pa[2] = pack_f16x2(p1[0] * vs1[0], p1[1] * vs1[1]);
+        pa[3] = pack_f16x2(p1[2] * vs1[0], p1[3] * vs1[1]);
     }
 }
 
@@ -169,7 +270,7 @@ __device__ __forceinline__ void combine_in_cta(const AttnParams &p, size_t base,
 // (request, KV head): the CTA that finishes the last one combines them and
 // returns the counter to zero for the next call.  A CTA whose pipeline wait
 // gave up writes nothing but still counts, so counters stay consistent.
-template <int D, int KG>
+template <int D, int KG, bool FP8 = false>
 __device__ __forceinline__ void mma_epilogue(const AttnParams &p, const WorkList &wl, int li, int kh,
                                              const float (&o)[D / 8][4], const float (&m)[2], const float (&l)[2],
                                              bool alive, float *mo, float *mml, uint32_t *s_flags, int nr,
@@ -180,13 +281,19 @@ __device__ __forceinline__ void mma_epilogue(const AttnParams &p, const WorkList
     constexpr int kThreads = kConsumerWarps * 32;
     named_bar_sync(1, kThreads);                                  // every consumer is done with the ring
     {
-        const int c = 2 * (lane & 3);
 #pragma unroll
         for (int hr = 0; hr < 2; hr++) {
             const int lr = (lane >> 2) + 8 * hr;
 #pragma unroll
-            for (int n = 0; n < D / 8; n++)
-                *reinterpret_cast<float2 *>(mo + (warp * 16 + lr) * D + n * 8 + c) = make_float2(o[n][2 * hr], o[n][2 * hr + 1]);
+            for (int n = 0; n < D / 8; n++) {
+                if constexpr (!FP8) {
+                    *reinterpret_cast<float2 *>(mo + (warp * 16 + lr) * D + o_col<false>(n, lane & 3, 0)) =
+                        make_float2(o[n][2 * hr], o[n][2 * hr + 1]);
+                } else {
+                    mo[(warp * 16 + lr) * D + o_col<true>(n, lane & 3, 0)] = o[n][2 * hr];
+                    mo[(warp * 16 + lr) * D + o_col<true>(n, lane & 3, 1)] = o[n][2 * hr + 1];
+                }
+            }
             if ((lane & 3) == 0) {
                 mml[(warp * 16 + lr) * 2] = m[hr];
                 mml[(warp * 16 + lr) * 2 + 1] = l[hr];
@@ -256,13 +363,13 @@ __device__ __forceinline__ void mma_epilogue(const AttnParams &p, const WorkList
     if (threadIdx.x == 0) atomicExch(cnt, 0u);                    // ready for the next call
 }
 
-template <int D, int KG, int NB>
+template <int D, int KG, int NB, bool FP8>
 __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, const __grid_constant__ WorkList wl,
                                                                const __grid_constant__ CUtensorMap kmap,
                                                                const __grid_constant__ CUtensorMap vmap)
 {
-    using T = MmaTile<D>;
-    using C = MmaCfg<D, KG, NB>;
+    using T = MmaTile<D, FP8>;
+    using C = MmaCfg<D, KG, NB, FP8>;
     constexpr int R = C::kSlots;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -274,9 +381,9 @@ __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, con
     auto slot_addr = [&](int s) { return ring + (uint32_t)s * T::kSlot; };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int kh = blockIdx.y;
-    const int li = find_listed(wl, blockIdx.x);
-    const int local = blockIdx.x - wl.item_off[li];
+    const int kh = blockIdx.x;                                    // the KV heads of an item run side by side
+    const int li = find_listed(wl, blockIdx.y);
+    const int local = blockIdx.y - wl.item_off[li];
     const int r = wl.req[li];
     const int b = wl.qb[li], t = wl.qt[li], L = wl.len[li];
     const int g = p.group;
@@ -357,13 +464,21 @@ __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, con
                     atomicOr(p.err, 2u);
                     blk = 0;
                 }
-                mbar_arrive_expect_tx(full_bar(s), T::kSlot);
+                // a block's K and V slices of this head, and for FP8 pools the
+                // block's K and V scales of every head ([16 slots][Hkv] fp32)
+                const uint32_t scale_bytes = FP8 ? 16u * p.hkv * 4u : 0u;
+                mbar_arrive_expect_tx(full_bar(s), 2 * T::kTile + 2 * scale_bytes);
                 const uint32_t dst = slot_addr(s);
 #pragma unroll
                 for (int x = 0; x < T::kBoxes; x++) {
                     tma_load_3d(dst + x * T::kBoxBytes, &kmap, full_bar(s), x * T::kBoxCols, kh, blk * 16);
                     tma_load_3d(dst + T::kTile + x * T::kBoxBytes, &vmap, full_bar(s), x * T::kBoxCols, kh,
                                 blk * 16);
+                }
+                if constexpr (FP8) {                              // the block's scale rows are contiguous
+                    bulk_load(dst + 2 * T::kTile, p.k_scale + (size_t)blk * 16 * p.hkv, scale_bytes, full_bar(s));
+                    bulk_load(dst + 2 * T::kTile + T::kScaleTile, p.v_scale + (size_t)blk * 16 * p.hkv, scale_bytes,
+                              full_bar(s));
                 }
             }
             __syncwarp();
@@ -387,20 +502,12 @@ __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, con
     const int qposB = rB < nr ? qbase + rB / g : -1;
     const int wspan = win_span(p.window);                         // keys <= position - wspan are outside
 
-    // Q as mma A fragments, straight from global memory (bf16 pairs).
+    // Q as mma A fragments, straight from global memory.
     uint32_t qa[D / 16][4];
     {
-        const uint32_t *qw = reinterpret_cast<const uint32_t *>(p.q);
-        const size_t rowA = rA < nr ? ((size_t)(b + i0 + rA / g) * p.hq + kh * g + rA % g) * (D / 2) : 0;
-        const size_t rowB = rB < nr ? ((size_t)(b + i0 + rB / g) * p.hq + kh * g + rB % g) * (D / 2) : 0;
-        const int c = (lane & 3);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; kk++) {
-            qa[kk][0] = rA < nr ? __ldg(qw + rowA + kk * 8 + c) : 0u;
-            qa[kk][1] = rB < nr ? __ldg(qw + rowB + kk * 8 + c) : 0u;
-            qa[kk][2] = rA < nr ? __ldg(qw + rowA + kk * 8 + 4 + c) : 0u;
-            qa[kk][3] = rB < nr ? __ldg(qw + rowB + kk * 8 + 4 + c) : 0u;
-        }
+        const size_t rowA = rA < nr ? (size_t)(b + i0 + rA / g) * p.hq + kh * g + rA % g : 0;
+        const size_t rowB = rB < nr ? (size_t)(b + i0 + rB / g) * p.hq + kh * g + rB % g : 0;
+        load_q_frags<D, FP8>(qa, p.q, rowA, rowB, rA < nr, rB < nr, lane);
     }
 
     float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
@@ -435,7 +542,24 @@ __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, con
         for (int n = 0; n < 2 * NB; n++) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
 #pragma unroll
         for (int q = 0; q < NB; q++)
-            if (has[q]) block_scores<D>(sc[2 * q], sc[2 * q + 1], qa, slot_addr(slot[q]), mi, mr);
+            if (has[q]) block_scores<D, FP8>(sc[2 * q], sc[2 * q + 1], qa, slot_addr(slot[q]), mi, mr);
+        // FP8 pools: the K and V scales of this lane's four keys of each block
+        float ksc[2 * NB][2], vsc[2 * NB][2];
+#pragma unroll
+        for (int n = 0; n < 2 * NB; n++) {
+            ksc[n][0] = ksc[n][1] = vsc[n][0] = vsc[n][1] = 1.f;
+            if constexpr (FP8) {
+                const float *sk = reinterpret_cast<const float *>(ring_ptr + slot[n >> 1] * T::kSlot + 2 * T::kTile);
+                const float *sv = sk + T::kScaleTile / 4;
+                const int kr = (n & 1) * 8 + 2 * (lane & 3);    // key row within the block
+                if (has[n >> 1]) {
+                    ksc[n][0] = sk[kr * p.hkv + kh];
+                    ksc[n][1] = sk[(kr + 1) * p.hkv + kh];
+                    vsc[n][0] = sv[kr * p.hkv + kh];
+                    vsc[n][1] = sv[(kr + 1) * p.hkv + kh];
+                }
+            }
+        }
         // scale into the exp2 domain, causal and range mask
 #pragma unroll
         for (int n = 0; n < 2 * NB; n++) {
@@ -445,7 +569,7 @@ __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, con
                 const int key = kc + (v & 1);
                 const int qp = v < 2 ? qposA : qposB;
                 const bool ok = has[n >> 1] && key < k_end && key <= qp && key > qp - wspan;
-                sc[n][v] = ok ? sc[n][v] * sl2 : -INFINITY;
+                sc[n][v] = ok ? sc[n][v] * (FP8 ? ksc[n][v & 1] * sl2 : sl2) : -INFINITY;
             }
         }
         float pr[2 * NB][4];
@@ -478,11 +602,8 @@ __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, con
         for (int q = 0; q < NB; q++) {
             if (!has[q]) continue;
             uint32_t pa[4];
-            pa[0] = pack_bf16x2(pr[2 * q][0], pr[2 * q][1]);
-            pa[1] = pack_bf16x2(pr[2 * q][2], pr[2 * q][3]);
-            pa[2] = pack_bf16x2(pr[2 * q + 1][0], pr[2 * q + 1][1]);
-            pa[3] = pack_bf16x2(pr[2 * q + 1][2], pr[2 * q + 1][3]);
-            block_pv<D>(o, pa, slot_addr(slot[q]) + T::kTile, mi, mr);
+            pack_p<FP8>(pa, pr[2 * q], pr[2 * q + 1], vsc[2 * q], vsc[2 * q + 1]);
+            block_pv<D, FP8>(o, pa, slot_addr(slot[q]) + T::kTile, mi, mr);
         }
         __syncwarp();
         if (lane == 0) {
@@ -499,7 +620,7 @@ __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, con
     }
     float *mo = reinterpret_cast<float *>(ring_ptr);              // [warp][16][D]
     float *mml = mo + kConsumerWarps * 16 * D;                    // [warp][16][2]
-    mma_epilogue<D, KG>(p, wl, li, kh, o, m, l, alive, mo, mml, s_flags, nr, i0, split, partial, b, t, L, g);
+    mma_epilogue<D, KG, FP8>(p, wl, li, kh, o, m, l, alive, mo, mml, s_flags, nr, i0, split, partial, b, t, L, g);
 }
 
 // ---------------------------------------------------------------- streaming decode
@@ -510,25 +631,25 @@ __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, con
 // 256-request and the 32 x 32768 decode workloads this keeps more copies in
 // flight per SM than the one-block slot ring above, which wins on short,
 // latency-bound ranges instead.
-template <int D, int KG>
+template <int D, int KG, bool FP8 = false>
 struct StreamCfg {
     static constexpr int kRT = kConsumerWarps / KG;                          // row tiles
-    static constexpr int kStages0 = kStageBudget / (KG * MmaTile<D>::kSlot);
+    static constexpr int kStages0 = kStageBudget / (KG * MmaTile<D, FP8>::kSlot);
     static constexpr int kStages = kStages0 > 8 ? 8 : (kStages0 < 2 ? 2 : kStages0);
-    static constexpr int kStageBytes = KG * MmaTile<D>::kSlot;
+    static constexpr int kStageBytes = KG * MmaTile<D, FP8>::kSlot;
     static constexpr int kRingBytes = kStages * kStageBytes;
     static constexpr int kMergeBytes = kConsumerWarps * 16 * (D + 2) * 4;
     static constexpr int kBodyBytes = kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes;
     static constexpr int kSmemBytes = 1024 + kBodyBytes + 2 * kStages * 8;   // + alignment slack, barriers
 };
 
-template <int D, int KG>
+template <int D, int KG, bool FP8>
 __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, const __grid_constant__ WorkList wl,
                                                                const __grid_constant__ CUtensorMap kmap,
                                                                const __grid_constant__ CUtensorMap vmap)
 {
-    using T = MmaTile<D>;
-    using C = StreamCfg<D, KG>;
+    using T = MmaTile<D, FP8>;
+    using C = StreamCfg<D, KG, FP8>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -539,9 +660,9 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
     auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int kh = blockIdx.y;
-    const int li = find_listed(wl, blockIdx.x);
-    const int local = blockIdx.x - wl.item_off[li];
+    const int kh = blockIdx.x;                                    // the KV heads of an item run side by side
+    const int li = find_listed(wl, blockIdx.y);
+    const int local = blockIdx.y - wl.item_off[li];
     const int r = wl.req[li];
     const int b = wl.qb[li], t = wl.qt[li], L = wl.len[li];
     const int g = p.group;
@@ -593,6 +714,7 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
             prefetch_tmap(&kmap);
             prefetch_tmap(&vmap);
         }
+        const uint32_t scale_bytes = FP8 ? 16u * p.hkv * 4u : 0u;   // a block's scales of every head
         const int32_t *bt = p.block_table + (size_t)r * p.bt_stride + blk0;
         int ids = lane < nblk ? __ldg(bt + lane) : 0, issued = 0;   // not written by the scatter
         pdl_wait();                                               // the step's K/V rows are in the pool
@@ -605,7 +727,7 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
             if (!__all_sync(0xffffffffu, ok)) break;
             issued = it + 1;
             const int nv = min(KG, nblk - base);
-            if (lane == 0) mbar_arrive_expect_tx(full_bar(s), nv * T::kSlot);
+            if (lane == 0) mbar_arrive_expect_tx(full_bar(s), nv * (2 * T::kTile + 2 * scale_bytes));
             for (int j = 0; j < nv; j++) {
                 int blk = __shfl_sync(0xffffffffu, ids, (base + j) & 31);
                 if (lane == 0) {
@@ -618,6 +740,12 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
                         tma_load_3d(dst + x * T::kBoxBytes, &kmap, full_bar(s), x * T::kBoxCols, kh, blk * 16);
                         tma_load_3d(dst + T::kTile + x * T::kBoxBytes, &vmap, full_bar(s), x * T::kBoxCols, kh,
                                     blk * 16);
+                    }
+                    if constexpr (FP8) {                          // the block's scale rows are contiguous
+                        bulk_load(dst + 2 * T::kTile, p.k_scale + (size_t)blk * 16 * p.hkv, scale_bytes,
+                                  full_bar(s));
+                        bulk_load(dst + 2 * T::kTile + T::kScaleTile, p.v_scale + (size_t)blk * 16 * p.hkv,
+                                  scale_bytes, full_bar(s));
                     }
                 }
             }
@@ -643,20 +771,12 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
     const int qposB = rB < nr ? qbase + rB / g : -1;
     const int wspan = win_span(p.window);                         // keys <= position - wspan are outside
 
-    // Q as mma A fragments, straight from global memory (bf16 pairs).
+    // Q as mma A fragments, straight from global memory.
     uint32_t qa[D / 16][4];
     {
-        const uint32_t *qw = reinterpret_cast<const uint32_t *>(p.q);
-        const size_t rowA = rA < nr ? ((size_t)(b + i0 + rA / g) * p.hq + kh * g + rA % g) * (D / 2) : 0;
-        const size_t rowB = rB < nr ? ((size_t)(b + i0 + rB / g) * p.hq + kh * g + rB % g) * (D / 2) : 0;
-        const int c = (lane & 3);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; kk++) {
-            qa[kk][0] = rA < nr ? __ldg(qw + rowA + kk * 8 + c) : 0u;
-            qa[kk][1] = rB < nr ? __ldg(qw + rowB + kk * 8 + c) : 0u;
-            qa[kk][2] = rA < nr ? __ldg(qw + rowA + kk * 8 + 4 + c) : 0u;
-            qa[kk][3] = rB < nr ? __ldg(qw + rowB + kk * 8 + 4 + c) : 0u;
-        }
+        const size_t rowA = rA < nr ? (size_t)(b + i0 + rA / g) * p.hq + kh * g + rA % g : 0;
+        const size_t rowB = rB < nr ? (size_t)(b + i0 + rB / g) * p.hq + kh * g + rB % g : 0;
+        load_q_frags<D, FP8>(qa, p.q, rowA, rowB, rA < nr, rB < nr, lane);
     }
 
     float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
@@ -679,12 +799,21 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
             const uint32_t vt = kt + T::kTile;
             const int key0 = (blk0 + bl) << 4;
             float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            block_scores<D, FP8>(sc[0], sc[1], qa, kt, mi, mr);
+            // FP8 pools: the K and V scales of this lane's four keys
+            float ksc[2][2] = {{1.f, 1.f}, {1.f, 1.f}}, vsc[2][2] = {{1.f, 1.f}, {1.f, 1.f}};
+            if constexpr (FP8) {
+                const float *sk = reinterpret_cast<const float *>(ring_ptr + s * C::kStageBytes + kg * T::kSlot +
+                                                                  2 * T::kTile);
+                const float *sv = sk + T::kScaleTile / 4;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; kk++) {
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(kt + tile_off<D>((mi >> 1) * 8 + mr, 2 * kk + (mi & 1)), b0, b1, b2, b3);
-                mma_16816(sc[0], qa[kk], b0, b1);
-                mma_16816(sc[1], qa[kk], b2, b3);
+                for (int n = 0; n < 2; n++) {
+                    const int kr = n * 8 + 2 * (lane & 3);
+                    ksc[n][0] = sk[kr * p.hkv + kh];
+                    ksc[n][1] = sk[(kr + 1) * p.hkv + kh];
+                    vsc[n][0] = sv[kr * p.hkv + kh];
+                    vsc[n][1] = sv[(kr + 1) * p.hkv + kh];
+                }
             }
             // scale into the exp2 domain, causal and range mask
             const int kc = key0 + 2 * (lane & 3);
@@ -694,7 +823,8 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
                 for (int v = 0; v < 4; v++) {
                     const int key = kc + n * 8 + (v & 1);
                     const int qp = v < 2 ? qposA : qposB;
-                    sc[n][v] = (key < k_end && key <= qp && key > qp - wspan) ? sc[n][v] * sl2 : -INFINITY;
+                    sc[n][v] = (key < k_end && key <= qp && key > qp - wspan)
+                                   ? sc[n][v] * (FP8 ? ksc[n][v & 1] * sl2 : sl2) : -INFINITY;
                 }
             }
             float pr[2][4];
@@ -719,17 +849,8 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
                 }
             }
             uint32_t pa[4];
-            pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
-            pa[1] = pack_bf16x2(pr[0][2], pr[0][3]);
-            pa[2] = pack_bf16x2(pr[1][0], pr[1][1]);
-            pa[3] = pack_bf16x2(pr[1][2], pr[1][3]);
-#pragma unroll
-            for (int np = 0; np < D / 16; np++) {
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(vt + tile_off<D>((mi & 1) * 8 + mr, 2 * np + (mi >> 1)), b0, b1, b2, b3);
-                mma_16816(o[2 * np], pa, b0, b1);
-                mma_16816(o[2 * np + 1], pa, b2, b3);
-            }
+            pack_p<FP8>(pa, pr[0], pr[1], vsc[0], vsc[1]);
+            block_pv<D, FP8>(o, pa, vt, mi, mr);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_bar(s));
@@ -743,7 +864,7 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
     }
     float *mo = reinterpret_cast<float *>(ring_ptr);              // [warp][16][D]
     float *mml = mo + kConsumerWarps * 16 * D;                    // [warp][16][2]
-    mma_epilogue<D, KG>(p, wl, li, kh, o, m, l, alive, mo, mml, s_flags, nr, i0, split, partial, b, t, L, g);
+    mma_epilogue<D, KG, FP8>(p, wl, li, kh, o, m, l, alive, mo, mml, s_flags, nr, i0, split, partial, b, t, L, g);
 }
 
 // ---------------------------------------------------------------- host side
@@ -768,21 +889,32 @@ static EncodeTiledFn encode_fn()
 }
 
 // Tensor map of one pool viewed as [slots][Hkv][D] with a box of one KV
-// head's 16 rows x box_cols columns.
-cudaError_t make_pool_tmap(CUtensorMap *map, const void *pool, int64_t num_slots, int hkv, int d, int box_cols,
-                           bool swizzle128)
+// head's 16 rows x box_cols columns; elements of elem_bytes (2: bf16, 1:
+// FP8 codes).
+static cudaError_t make_pool_tmap_e(CUtensorMap *map, const void *pool, int64_t num_slots, int hkv, int d,
+                                   int box_cols, bool swizzle128, int elem_bytes)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return cudaErrorNotSupported;
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)hkv, (cuuint64_t)num_slots};
-    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)hkv * d * 2};
+    cuuint64_t strides[2] = {(cuuint64_t)d * elem_bytes, (cuuint64_t)hkv * d * elem_bytes};
     cuuint32_t box[3] = {(cuuint32_t)box_cols, 1, 16};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(pool), dims, strides, box, estr,
-                      CU_TENSOR_MAP_INTERLEAVE_NONE,
+    // a 128-byte code row (FP8, head_dim 128) is promoted to 128 bytes only:
+    // 256 would fetch the next head's row as well
+    CUresult res = fn(map, elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                      const_cast<void *>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                       swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                      (int64_t)d * elem_bytes >= 256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                                                     : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return res == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t make_pool_tmap(CUtensorMap *map, const void *pool, int64_t num_slots, int hkv, int d, int box_cols,
+                           bool swizzle128)
+{
+    return make_pool_tmap_e(map, pool, num_slots, hkv, d, box_cols, swizzle128, 2);
 }
 
 // Tensor map of q [tokens][Hq][D] with a box of one KV head's g query heads
@@ -801,38 +933,44 @@ cudaError_t make_q_tmap(CUtensorMap *map, const void *q, int num_tokens, int hq,
     return res == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D, int KG, int NB>
+template <int D, int KG, int NB, bool FP8>
 static cudaError_t launch_mma_dk(const AttnParams &p, const WorkList &wl, int num_items, const CUtensorMap &km,
                                  const CUtensorMap &vm, cudaStream_t stream)
 {
-    constexpr int smem = MmaCfg<D, KG, NB>::kSmemBytes;
+    constexpr int smem = MmaCfg<D, KG, NB, FP8>::kSmemBytes;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(attn_mma_kernel<D, KG, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        attr_err = cudaFuncSetAttribute(attn_mma_kernel<D, KG, NB, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        smem);
     });
     if (attr_err != cudaSuccess) return attr_err;
-    dim3 grid(num_items, p.hkv);
+    if (num_items > 65535) return cudaErrorInvalidConfiguration;
+    dim3 grid(p.hkv, num_items);                                // KV heads adjacent: they share pool pages
     launch_begin(stream, wl.mode == kModeDecode ? kAttnMmaDecode : kAttnMmaPrefill);
-    cudaError_t e = launch_maybe_pdl(attn_mma_kernel<D, KG, NB>, grid, dim3(kMmaThreads), smem, stream, p, wl, km, vm);
+    cudaError_t e = launch_maybe_pdl(attn_mma_kernel<D, KG, NB, FP8>, grid, dim3(kMmaThreads), smem, stream, p, wl,
+                                     km, vm);
     launch_end(stream);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool FP8>
 static cudaError_t launch_stream_d(const AttnParams &p, const WorkList &wl, int num_items, const CUtensorMap &km,
                                    const CUtensorMap &vm, cudaStream_t stream)
 {
-    constexpr int smem = StreamCfg<D, 4>::kSmemBytes;
+    constexpr int smem = StreamCfg<D, 4, FP8>::kSmemBytes;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(attn_stream_kernel<D, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        attr_err = cudaFuncSetAttribute(attn_stream_kernel<D, 4, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        smem);
     });
     if (attr_err != cudaSuccess) return attr_err;
-    dim3 grid(num_items, p.hkv);
+    if (num_items > 65535) return cudaErrorInvalidConfiguration;
+    dim3 grid(p.hkv, num_items);                                // KV heads adjacent: they share pool pages
     launch_begin(stream, kAttnMmaDecode);
-    cudaError_t e = launch_maybe_pdl(attn_stream_kernel<D, 4>, grid, dim3(kMmaThreads), smem, stream, p, wl, km, vm);
+    cudaError_t e = launch_maybe_pdl(attn_stream_kernel<D, 4, FP8>, grid, dim3(kMmaThreads), smem, stream, p, wl, km,
+                                     vm);
     launch_end(stream);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -841,30 +979,38 @@ static cudaError_t launch_stream_d(const AttnParams &p, const WorkList &wl, int 
 // walks a long key range, the slot-ring kernel with two blocks per
 // iteration when ranges are short and latency dominates.  Prefill-class
 // CTAs: 2 row tiles x 2 key groups, two blocks per iteration.
-template <int D>
+template <int D, bool FP8>
 static cudaError_t launch_mma_d(const AttnParams &p, const WorkList &wl, int num_items, const CUtensorMap &km,
                                 const CUtensorMap &vm, cudaStream_t stream)
 {
     constexpr int NB = 2;                                       // blocks per warp iteration
-    if (wl.mode != kModeDecode) return launch_mma_dk<D, 2, NB>(p, wl, num_items, km, vm, stream);
-    if (wl.split_tokens >= kLongSplit) return launch_stream_d<D>(p, wl, num_items, km, vm, stream);
-    return launch_mma_dk<D, 4, NB>(p, wl, num_items, km, vm, stream);
+    if (wl.mode != kModeDecode) return launch_mma_dk<D, 2, NB, FP8>(p, wl, num_items, km, vm, stream);
+    if (wl.split_tokens >= kLongSplit) return launch_stream_d<D, FP8>(p, wl, num_items, km, vm, stream);
+    return launch_mma_dk<D, 4, NB, FP8>(p, wl, num_items, km, vm, stream);
 }
 
 cudaError_t launch_attn_mma(const AttnParams &p, const WorkList &wl, int head_dim, int num_items,
-                            const void *k_cache, const void *v_cache, int64_t num_slots, cudaStream_t stream)
+                            const void *k_cache, const void *v_cache, int64_t num_slots, cudaStream_t stream,
+                            const float *k_scale, const float *v_scale)
 {
     if (num_items <= 0) return cudaSuccess;
     CUtensorMap km, vm;
+    if (k_scale) {                                              // FP8 pool: head_dim 128, 128-byte rows
+        if (head_dim != 128 || p.k_scale != k_scale || p.v_scale != v_scale) return cudaErrorInvalidValue;
+        cudaError_t e = make_pool_tmap_e(&km, k_cache, num_slots, p.hkv, 128, 128, true, 1);
+        if (e == cudaSuccess) e = make_pool_tmap_e(&vm, v_cache, num_slots, p.hkv, 128, 128, true, 1);
+        if (e != cudaSuccess) return e;
+        return launch_mma_d<128, true>(p, wl, num_items, km, vm, stream);
+    }
     const bool sw = head_dim != 48;
     const int box = sw ? 64 : head_dim;
     cudaError_t e = make_pool_tmap(&km, k_cache, num_slots, p.hkv, head_dim, box, sw);
     if (e == cudaSuccess) e = make_pool_tmap(&vm, v_cache, num_slots, p.hkv, head_dim, box, sw);
     if (e != cudaSuccess) return e;
     switch (head_dim) {
-    case 48: return launch_mma_d<48>(p, wl, num_items, km, vm, stream);
-    case 64: return launch_mma_d<64>(p, wl, num_items, km, vm, stream);
-    case 128: return launch_mma_d<128>(p, wl, num_items, km, vm, stream);
+    case 48: return launch_mma_d<48, false>(p, wl, num_items, km, vm, stream);
+    case 64: return launch_mma_d<64, false>(p, wl, num_items, km, vm, stream);
+    case 128: return launch_mma_d<128, false>(p, wl, num_items, km, vm, stream);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -53,6 +53,8 @@ struct AttnParams {
     float2 *part_ml;            // [rows] (running max in exp2 domain, sum of weights)
     uint32_t *counters;         // split counters of in-kernel combines (zero between calls), or null
     int32_t window;             // sliding window: keys above position - window (0: none)
+    const float *k_scale;       // FP8 pools: [slots][hkv] scales of the K and V codes (else null)
+    const float *v_scale;
 };
 
 // ---------------------------------------------------------------- sliding window
@@ -143,6 +145,9 @@ namespace pkv {
 cudaError_t launch_kv_write(const void *k, const void *v, void *k_cache, void *v_cache,
                             const int64_t *slot_mapping, int32_t num_tokens, int32_t row_bytes,
                             int64_t num_slots, uint32_t *err, cudaStream_t stream);
+cudaError_t launch_kv_write_fp8(const void *k, const void *v, void *k_codes, void *v_codes, float *k_scale,
+                                float *v_scale, const int64_t *slot_mapping, int32_t num_tokens, int32_t hkv,
+                                int64_t num_slots, uint32_t *err, cudaStream_t stream);
 
 // CUDA-core attention over one work list; rows = largest tokens*group of an item.
 cudaError_t launch_attn_fma(const AttnParams &p, const WorkList &wl, int head_dim, int rows,
@@ -151,7 +156,8 @@ cudaError_t launch_attn_fma(const AttnParams &p, const WorkList &wl, int head_di
 // TMA-staged attention with warp-level MMA (decode-class: 4 key groups per
 // CTA; prefill-class: 4 row tiles of 16 per CTA).
 cudaError_t launch_attn_mma(const AttnParams &p, const WorkList &wl, int head_dim, int num_items,
-                            const void *k_cache, const void *v_cache, int64_t num_slots, cudaStream_t stream);
+                            const void *k_cache, const void *v_cache, int64_t num_slots, cudaStream_t stream,
+                            const float *k_scale = nullptr, const float *v_scale = nullptr);
 int mma_prefill_rows();
 
 // tcgen05 prefill tiles of 128 query rows (head_dim 48, 64 or 128, g dividing 128).

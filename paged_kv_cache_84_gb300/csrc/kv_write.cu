@@ -5,6 +5,8 @@
 // negative slot marks a padding row and goes to the pool's last slot, the
 // scratch block.  A bit copy: 16-byte vectors, one per thread, the K and the
 // V chunk of the same offset handled together.
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 #include "sm100.cuh"
 
@@ -37,6 +39,68 @@ __global__ void __launch_bounds__(256) kv_write_kernel(
         k_cache[dst] = kv;
         v_cache[dst] = vv;
     }
+}
+
+// Quantizing write for FP8 pools (head_dim 128): one warp per (row, KV
+// head); lane l holds dims 4l .. 4l+3 of K and of V.  Per row and head:
+// scale = max |x| / 448 (fp32), codes = E4M3(x / scale) rounded to nearest
+// even with saturation ("31. Engine v2", "Attention over the pool": the
+// quantized pool's per (slot, head) scales; the code format is this
+// library's reading).  An all-zero row gets scale 0 and zero codes.
+__global__ void __launch_bounds__(256) kv_write_fp8_kernel(
+    const uint2 *__restrict__ k, const uint2 *__restrict__ v, uint32_t *__restrict__ k_codes,
+    uint32_t *__restrict__ v_codes, float *__restrict__ k_scale, float *__restrict__ v_scale,
+    const int64_t *__restrict__ slot_mapping, int64_t rows, int32_t hkv, int64_t num_slots, uint32_t *err)
+{
+    pdl_wait();                                           // as the bf16 write: nothing is read before this
+    pdl_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < rows; w += nwarps) {
+        const int64_t i = w / hkv;                        // token row; w = i * hkv + head
+        int64_t slot = __ldg(slot_mapping + i);
+        const uint2 kx = k[w * 32 + lane], vx = v[w * 32 + lane];   // 4 bf16 each
+        if (slot < 0) slot = num_slots - 1;               // padding row -> scratch slot
+        if (slot >= num_slots) {
+            if (lane == 0 && w % hkv == 0 && err) atomicOr(err, 1u);
+            continue;
+        }
+        const int64_t dst_row = slot * hkv + (w - i * hkv);
+#pragma unroll
+        for (int which = 0; which < 2; which++) {
+            const uint2 x = which ? vx : kx;
+            const float f[4] = {bf16_lo(x.x), bf16_hi(x.x), bf16_lo(x.y), bf16_hi(x.y)};
+            float amax = fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3])));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            const float scale = __fdiv_rn(amax, 448.0f);
+            uint32_t codes = 0u;
+            if (scale > 0.f) {
+                const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+                    make_float2(__fdiv_rn(f[0], scale), __fdiv_rn(f[1], scale)), __NV_SATFINITE, __NV_E4M3);
+                const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+                    make_float2(__fdiv_rn(f[2], scale), __fdiv_rn(f[3], scale)), __NV_SATFINITE, __NV_E4M3);
+                codes = (uint32_t)lo | ((uint32_t)hi << 16);
+            }
+            (which ? v_codes : k_codes)[dst_row * 32 + lane] = codes;
+            if (lane == 0) (which ? v_scale : k_scale)[dst_row] = scale;
+        }
+    }
+}
+
+cudaError_t launch_kv_write_fp8(const void *k, const void *v, void *k_codes, void *v_codes, float *k_scale,
+                                float *v_scale, const int64_t *slot_mapping, int32_t num_tokens, int32_t hkv,
+                                int64_t num_slots, uint32_t *err, cudaStream_t stream)
+{
+    const int64_t rows = (int64_t)num_tokens * hkv;
+    int64_t blocks = (rows + 7) / 8;                        // 8 warps per CTA
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    launch_begin(stream, kKvWrite);
+    cudaError_t e = launch_maybe_pdl(kv_write_fp8_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
+                                     (const uint2 *)k, (const uint2 *)v, (uint32_t *)k_codes, (uint32_t *)v_codes,
+                                     k_scale, v_scale, slot_mapping, rows, hkv, num_slots, err);
+    launch_end(stream);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_kv_write(const void *k, const void *v, void *k_cache, void *v_cache,

@@ -138,14 +138,14 @@ constexpr int kTcMinRows = kDecodeRows + 1;
 // Kernel class of request r (host rule shared by the planner and pkv_plan_request_kernels).
 static int env_int(const char *name, int dflt);
 
-static int request_class(int32_t t, int32_t L, int32_t g, int32_t d)
+static int request_class(int32_t t, int32_t L, int32_t g, int32_t d, bool fp8 = false)
 {
     if (t == 0) return PKV_CLASS_NONE;
     if (L == 0) return PKV_CLASS_PADDING;
     if (t * g <= kDecodeRows) return PKV_CLASS_DECODE;
     // a request fills at least kTcMinRows of a 128-row tensor-core tile
     const int min_rows = env_int("PKV_TC_MIN_ROWS", kTcMinRows);
-    if (tc_prefill_supported(d, g) && t * g >= min_rows && !env_int("PKV_ATTN_CUDA_CORE", 0) &&
+    if (!fp8 && tc_prefill_supported(d, g) && t * g >= min_rows && !env_int("PKV_ATTN_CUDA_CORE", 0) &&
         !env_int("PKV_DISABLE_TCGEN05", 0))
         return PKV_CLASS_PREFILL_TENSOR;
     return PKV_CLASS_PREFILL_CUDA_CORE;
@@ -254,6 +254,25 @@ pkv_status pkv_paged_kv_write(const void *k, const void *v, void *k_cache, void 
     return e == cudaSuccess ? PKV_OK : cuda_fail(e, "paged_kv_write launch");
 }
 
+pkv_status pkv_paged_kv_write_fp8(const void *k, const void *v, void *k_cache, void *v_cache, float *k_scale,
+                                  float *v_scale, const int64_t *slot_mapping, int32_t num_tokens,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                  int32_t num_blocks_total, uint32_t *device_error, cudaStream_t stream)
+{
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks_total <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k || !v || !k_cache || !v_cache || !k_scale || !v_scale || !slot_mapping) return PKV_ERR_INVALID_ARG;
+    if (head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(k_scale, 4) || !aligned(v_scale, 4) || !aligned(slot_mapping, 8))
+        return PKV_ERR_UNSUPPORTED;
+    int64_t num_slots = (int64_t)num_blocks_total * block_size;
+    cudaError_t e = launch_kv_write_fp8(k, v, k_cache, v_cache, k_scale, v_scale, slot_mapping, num_tokens,
+                                        num_kv_heads, num_slots, device_error, stream);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "paged_kv_write_fp8 launch");
+}
+
 size_t pkv_attention_workspace_bytes(int32_t max_num_reqs, int32_t max_num_tokens, int32_t num_q_heads,
                                      int32_t head_dim, int32_t max_seq_len)
 {
@@ -303,15 +322,19 @@ pkv_status pkv_read_device_error(const uint32_t *device_error, uint32_t *flags_o
     return flags ? PKV_ERR_DEVICE_BOUNDS : PKV_OK;
 }
 
-pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
-                                      const int32_t *query_start_loc, const int32_t *seq_lens,
-                                      const int32_t *block_table, int32_t block_table_stride,
-                                      const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs,
-                                      int32_t num_tokens, int32_t max_query_len, int32_t max_seq_len,
-                                      int32_t hq, int32_t hkv, int32_t d, int32_t bs,
-                                      int32_t num_blocks_total, float scale, int32_t window,
-                                      void *workspace, size_t workspace_bytes, cudaStream_t stream)
+}  // extern "C"
+
+// The attention call of both pool kinds: k_scale / v_scale non-null selects a
+// quantized (FP8 E4M3) pool.
+static pkv_status attention_impl(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                 const float *k_scale, const float *v_scale, const int32_t *query_start_loc,
+                                 const int32_t *seq_lens, const int32_t *block_table, int32_t block_table_stride,
+                                 const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs, int32_t num_tokens,
+                                 int32_t max_query_len, int32_t max_seq_len, int32_t hq, int32_t hkv, int32_t d,
+                                 int32_t bs, int32_t num_blocks_total, float scale, int32_t window, void *workspace,
+                                 size_t workspace_bytes, cudaStream_t stream)
 {
+    const bool fp8 = k_scale != nullptr;
     // ---- host validation
     if (num_reqs < 0 || num_tokens < 0 || hq <= 0 || hkv <= 0 || d <= 0 || bs <= 0 || num_blocks_total <= 0)
         return PKV_ERR_INVALID_ARG;
@@ -340,13 +363,18 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
     if (g > kDecodeRows) return PKV_ERR_UNSUPPORTED;
     if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
         return PKV_ERR_UNSUPPORTED;
+    // quantized pools: head_dim 128 (128-byte code rows), the scale rows of a
+    // block staged whole (KV heads a multiple of 4, at most 16), warp-MMA kernels
+    if (fp8 && (d != 128 || hkv % 4 != 0 || hkv > 16 || !aligned(k_scale, 16) || !aligned(v_scale, 16) ||
+                env_int("PKV_ATTN_CUDA_CORE", 0)))
+        return PKV_ERR_UNSUPPORTED;
 
     // ---- classify
     std::vector<int32_t> dec, pre, tcp;
     int64_t dec_keys = 0;
     for (int r = 0; r < num_reqs; r++) {
         int32_t t = qsl_h[r + 1] - qsl_h[r], L = sl_h[r];
-        switch (request_class(t, L, g, d)) {
+        switch (request_class(t, L, g, d, fp8)) {
         case PKV_CLASS_PADDING:
         case PKV_CLASS_DECODE: dec.push_back(r); dec_keys += L - decode_key_begin(t, L, window); break;
         case PKV_CLASS_PREFILL_CUDA_CORE: pre.push_back(r); break;
@@ -440,6 +468,8 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
     p.part_ml = reinterpret_cast<float2 *>(ws + part_base + ((total_rows * d * 4 + 15) / 16) * 16);
     p.counters = has_counters ? reinterpret_cast<uint32_t *>(ws + kErrBytes) : nullptr;
     p.window = window;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
 
     // ---- decode-class work runs on a side stream, concurrently with the
     // prefill kernels, when both are present: its CTAs fill the SMs that the
@@ -595,7 +625,8 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
         }
         wl.item_off[wl.n] = items;
         cudaError_t e = use_fma ? launch_attn_fma(p, wl, d, rows, items, dstream)
-                                : launch_attn_mma(p, wl, d, items, k_cache, v_cache, num_slots, dstream);
+                                : launch_attn_mma(p, wl, d, items, k_cache, v_cache, num_slots, dstream, k_scale,
+                                                  v_scale);
         if (e != cudaSuccess) {
             join();
             return cuda_fail(e, "decode attention launch");
@@ -628,7 +659,8 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
         }
         wl.item_off[wl.n] = items;
         cudaError_t e = use_fma ? launch_attn_fma(p, wl, d, kDecodeRows, items, pstream)
-                                : launch_attn_mma(p, wl, d, items, k_cache, v_cache, num_slots, pstream);
+                                : launch_attn_mma(p, wl, d, items, k_cache, v_cache, num_slots, pstream, k_scale,
+                                                  v_scale);
         if (e != cudaSuccess) {
             join();
             return cuda_fail(e, "prefill attention launch");
@@ -646,6 +678,38 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
     cudaError_t ej = join();
     if (ej != cudaSuccess) return cuda_fail(ej, "join");
     return PKV_OK;
+}
+
+extern "C" {
+
+pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                      const int32_t *query_start_loc, const int32_t *seq_lens,
+                                      const int32_t *block_table, int32_t block_table_stride,
+                                      const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs,
+                                      int32_t num_tokens, int32_t max_query_len, int32_t max_seq_len,
+                                      int32_t hq, int32_t hkv, int32_t d, int32_t bs,
+                                      int32_t num_blocks_total, float scale, int32_t window,
+                                      void *workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    return attention_impl(out, q, k_cache, v_cache, nullptr, nullptr, query_start_loc, seq_lens, block_table,
+                          block_table_stride, qsl_h, sl_h, num_reqs, num_tokens, max_query_len, max_seq_len, hq, hkv,
+                          d, bs, num_blocks_total, scale, window, workspace, workspace_bytes, stream);
+}
+
+pkv_status pkv_ragged_paged_attention_fp8(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                          const float *k_scale, const float *v_scale,
+                                          const int32_t *query_start_loc, const int32_t *seq_lens,
+                                          const int32_t *block_table, int32_t block_table_stride,
+                                          const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs,
+                                          int32_t num_tokens, int32_t max_query_len, int32_t max_seq_len,
+                                          int32_t hq, int32_t hkv, int32_t d, int32_t bs,
+                                          int32_t num_blocks_total, float scale, int32_t window,
+                                          void *workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    if (!k_scale || !v_scale) return PKV_ERR_INVALID_ARG;
+    return attention_impl(out, q, k_cache, v_cache, k_scale, v_scale, query_start_loc, seq_lens, block_table,
+                          block_table_stride, qsl_h, sl_h, num_reqs, num_tokens, max_query_len, max_seq_len, hq, hkv,
+                          d, bs, num_blocks_total, scale, window, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

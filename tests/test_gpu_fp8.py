@@ -1,0 +1,135 @@
+"""Quantized (FP8 E4M3) pools on the GPU against the oracle: the quantizing
+write bit for bit, attention within the usual tolerance ("31. Engine v2",
+"Attention over the pool": per (slot, head) scales beside K and V)."""
+import math
+
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_84_gb300 as pkv
+from workloads import Req, Spec, build_meta, config_spec, make_batch, random_spec, subset_spec
+from _helpers import MAX_ERR, MEAN_ERR, assert_close, threads
+
+pytestmark = pytest.mark.gpu
+
+
+def _quantized_pools(batch, seed):
+    """Junk codes and scales everywhere (never NaN codes), then the history of
+    every request written by the oracle's quantizing write from bf16 values."""
+    spec, m = batch.spec, batch.meta
+    nbt = spec.num_blocks_total + 1
+    g = torch.Generator().manual_seed(seed)
+    shape = (nbt, spec.block_size, spec.num_kv_heads, spec.head_dim)
+    kc = torch.randint(0, 255, shape, generator=g, dtype=torch.uint8)
+    vc = torch.randint(0, 255, shape, generator=g, dtype=torch.uint8)
+    kc[(kc & 0x7F) == 0x7F] = 0
+    vc[(vc & 0x7F) == 0x7F] = 0
+    ks = torch.rand(shape[:3], generator=g)
+    vs = torch.rand(shape[:3], generator=g)
+    # history rows (positions 0 .. c-1) from the batch's bf16 pools
+    hist = build_meta(Spec("hist", [Req(0, r.computed, r.table) for r in spec.reqs if not r.pad],
+                           spec.num_q_heads, spec.num_kv_heads, spec.head_dim, spec.block_size,
+                           spec.num_blocks_total, 1.0, 0))
+    if hist.num_tokens:
+        sm = hist.slot_mapping
+        kh = batch.k_cache.view(-1, spec.num_kv_heads, spec.head_dim)[sm]
+        vh = batch.v_cache.view(-1, spec.num_kv_heads, spec.head_dim)[sm]
+        oracle.paged_kv_write_fp8(kc, vc, ks, vs, kh, vh, sm)
+    return kc, vc, ks, vs
+
+
+def _run(batch, pools, window=0, workspace_bytes=None):
+    spec, m = batch.spec, batch.meta
+    kc, vc, ks, vs = [t.cuda() for t in pools]
+    k, v, q = batch.k.cuda(), batch.v.cuda(), batch.q.cuda()
+    slots = m.slot_mapping.cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.paged_kv_write_fp8(k, v, kc, vc, ks, vs, slots, err)
+    out = torch.full_like(q, float("nan"))
+    ws = pkv.make_workspace(workspace_bytes or pkv.attention_workspace_bytes(
+        max(1, m.num_reqs), max(1, m.num_tokens), spec.num_q_heads, spec.head_dim, max(1, m.max_seq_len)), "cuda")
+    pkv.ragged_paged_attention_fp8(out, q, kc, vc, ks, vs, torch.tensor(m.query_start_loc, dtype=torch.int32,
+                                   device="cuda"), torch.tensor(m.seq_lens, dtype=torch.int32, device="cuda"),
+                                   m.block_table.cuda(), m.query_start_loc, m.seq_lens, m.max_query_len,
+                                   m.max_seq_len, spec.scale, ws, window=window)
+    torch.cuda.synchronize()
+    return out, (kc, vc, ks, vs), err, ws
+
+
+def _oracle(batch, pools, window=0):
+    spec, m = batch.spec, batch.meta
+    kc, vc, ks, vs = [t.clone() for t in pools]
+    oracle.paged_kv_write_fp8(kc, vc, ks, vs, batch.k, batch.v, m.slot_mapping)
+    out = oracle.ragged_paged_attention_fp8(batch.q, kc, vc, ks, vs, m.query_start_loc, m.seq_lens, m.block_table,
+                                            spec.scale, threads(), window=window)
+    return out, (kc, vc, ks, vs)
+
+
+FP8_CASES = [
+    # seed, reqs, max_ctx, max_new, hq, hkv, pad rows
+    (0, 8, 700, 40, 32, 8, 1),
+    (1, 6, 3000, 3, 16, 4, 0),
+    (2, 5, 1500, 130, 8, 8, 0),
+    (3, 12, 400, 20, 64, 8, 2),
+    (4, 4, 5000, 1, 32, 4, 0),
+]
+
+
+@pytest.mark.parametrize("case", FP8_CASES, ids=[f"seed{c[0]}" for c in FP8_CASES])
+def test_fp8_write_bit_exact_and_attention_parity(case):
+    seed, reqs, max_ctx, max_new, hq, hkv, pad = case
+    spec = random_spec(200 + seed, reqs, max_ctx, max_new, hq, hkv, 128, pad_rows=pad)
+    b = make_batch(spec, device="cpu")
+    pools = _quantized_pools(b, seed)
+    got, dev_pools, err, ws = _run(b, pools)
+    want, ref_pools = _oracle(b, pools)
+    nbt = spec.num_blocks_total + 1
+    for d, r in zip(dev_pools, ref_pools):
+        d = d.cpu()
+        # the whole pool except the scratch block is bit-exact
+        assert torch.equal(d.view(nbt, -1)[:-1].view(torch.uint8), r.view(nbt, -1)[:-1].view(torch.uint8))
+    assert pkv.read_device_error(err) == 0
+    assert_close(got, want, f"fp8 seed {seed}")
+    assert pkv.read_device_error(ws) == 0
+
+
+@pytest.mark.parametrize("split", ["128", "1024"])
+@pytest.mark.parametrize("window", [0, 300])
+def test_fp8_split_paths_and_window(split, window, monkeypatch):
+    """Decode splits on the slot-ring (128) and the streaming kernel (1024),
+    with and without a sliding window."""
+    monkeypatch.setenv("PKV_SPLIT_TOKENS", split)
+    reqs = [Req(3000, 1, list(range(0, 188))), Req(700, 40, list(range(188, 235))),
+            Req(2500, 3, list(range(235, 392))), Req(5000, 1, list(range(392, 705)))]
+    spec = Spec("fp8-paths", reqs, 32, 8, 128, 16, 710, 1 / math.sqrt(128), 71)
+    b = make_batch(spec, device="cpu")
+    pools = _quantized_pools(b, 72)
+    got, _, _, _ = _run(b, pools, window=window)
+    want, _ = _oracle(b, pools, window=window)
+    assert_close(got, want, f"fp8 split {split} window {window}")
+
+
+def test_fp8_long_decodes_sampled():
+    """The 32 x 32768 decode shape (4 requests), the streaming kernel."""
+    spec = subset_spec(config_spec(5), 4)
+    b = make_batch(spec, device="cpu")
+    pools = _quantized_pools(b, 73)
+    got, _, _, _ = _run(b, pools)
+    m = b.meta
+    kc, vc, ks, vs = [t.clone() for t in pools]
+    oracle.paged_kv_write_fp8(kc, vc, ks, vs, b.k, b.v, m.slot_mapping)
+    toks = [0, 1, 2, 3, 0, 3]
+    heads = [0, 17, 40, 63, 63, 5]
+    want = oracle.attention_rows_fp8(toks, heads, b.q, kc, vc, ks, vs, m.query_start_loc, m.seq_lens,
+                                     m.block_table, spec.scale, threads())
+    assert_close(got[torch.tensor(toks), torch.tensor(heads)], want, "fp8 long decodes")
+
+
+def test_fp8_unsupported_shapes_are_rejected():
+    spec = random_spec(230, 3, 100, 1, 8, 2, 128)          # 2 KV heads: not a multiple of 4
+    b = make_batch(spec, device="cpu")
+    pools = _quantized_pools(b, 74)
+    with pytest.raises(pkv.PkvError) as e:
+        _run(b, pools)
+    assert e.value.status == 2
