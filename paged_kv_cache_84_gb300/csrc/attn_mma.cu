@@ -67,16 +67,18 @@ __device__ __forceinline__ uint32_t tile_off(int row, int chunk)
     }
 }
 
-template <int D, int KG, int NB, bool FP8 = false>
+template <int D, int KG, int NB, bool FP8 = false, int CW = kConsumerWarps>
 struct MmaCfg {
-    static constexpr int kRT = kConsumerWarps / KG;                          // row tiles
+    static constexpr int kRT = CW / KG;                                      // row tiles
     // Ring of one-block slots: this kernel serves short, latency-bound key
     // ranges, so the ring holds one iteration of every key group plus a few
     // blocks in flight, small enough for several CTAs per SM.
-    static constexpr int kSlots = KG * NB + KG + 4;
+    static constexpr int kSlotsWanted = KG * NB + KG + 4;
+    static constexpr int kSlotsMax = (200 * 1024) / MmaTile<D, FP8>::kSlot;   // stay within shared memory
+    static constexpr int kSlots = kSlotsWanted < kSlotsMax ? kSlotsWanted : kSlotsMax;
     static_assert(kSlots >= KG * NB + KG, "the ring must hold an iteration of every key group plus one block each");
     static constexpr int kRingBytes = kSlots * MmaTile<D, FP8>::kSlot;
-    static constexpr int kMergeBytes = kConsumerWarps * 16 * (D + 2) * 4;
+    static constexpr int kMergeBytes = CW * 16 * (D + 2) * 4;
     static constexpr int kBodyBytes = kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes;
     static constexpr int kSmemBytes = 1024 + kBodyBytes + 2 * kSlots * 8;   // + alignment slack, barriers
 };
@@ -270,15 +272,15 @@ __device__ __forceinline__ void combine_in_cta(const AttnParams &p, size_t base,
 // (request, KV head): the CTA that finishes the last one combines them and
 // returns the counter to zero for the next call.  A CTA whose pipeline wait
 // gave up writes nothing but still counts, so counters stay consistent.
-template <int D, int KG, bool FP8 = false>
+template <int D, int KG, bool FP8 = false, int CW = kConsumerWarps>
 __device__ __forceinline__ void mma_epilogue(const AttnParams &p, const WorkList &wl, int li, int kh,
                                              const float (&o)[D / 8][4], const float (&m)[2], const float (&l)[2],
                                              bool alive, float *mo, float *mml, uint32_t *s_flags, int nr,
                                              int i0, int split, bool partial, int b, int t, int L, int g)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    constexpr int kRT = kConsumerWarps / KG;
-    constexpr int kThreads = kConsumerWarps * 32;
+    constexpr int kRT = CW / KG;
+    constexpr int kThreads = CW * 32;
     named_bar_sync(1, kThreads);                                  // every consumer is done with the ring
     {
 #pragma unroll
@@ -363,13 +365,13 @@ __device__ __forceinline__ void mma_epilogue(const AttnParams &p, const WorkList
     if (threadIdx.x == 0) atomicExch(cnt, 0u);                    // ready for the next call
 }
 
-template <int D, int KG, int NB, bool FP8>
-__global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, const __grid_constant__ WorkList wl,
+template <int D, int KG, int NB, bool FP8, int CW>
+__global__ void __launch_bounds__((CW + 1) * 32) attn_mma_kernel(AttnParams p, const __grid_constant__ WorkList wl,
                                                                const __grid_constant__ CUtensorMap kmap,
                                                                const __grid_constant__ CUtensorMap vmap)
 {
     using T = MmaTile<D, FP8>;
-    using C = MmaCfg<D, KG, NB, FP8>;
+    using C = MmaCfg<D, KG, NB, FP8, CW>;
     constexpr int R = C::kSlots;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -393,7 +395,7 @@ __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, con
         // grids it follows, which keeps later programmatic waits transitive.
         pdl_wait();
         if (threadIdx.x == 0 && local == 0 && kh == 0) check_meta(p, wl, li);
-        for (int idx = threadIdx.x; idx < t * g * D; idx += kMmaThreads) {
+        for (int idx = threadIdx.x; idx < t * g * D; idx += (CW + 1) * 32) {
             const int rr = idx / D, e = idx - rr * D;
             p.out[((size_t)(b + rr / g) * p.hq + kh * g + rr % g) * D + e] = __float2bfloat16(0.f);
         }
@@ -440,7 +442,7 @@ __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, con
     }
     __syncthreads();
 
-    if (warp == kConsumerWarps) {
+    if (warp == CW) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             prefetch_tmap(&kmap);
@@ -619,8 +621,8 @@ __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnParams p, con
         l[hr] += __shfl_xor_sync(0xffffffffu, l[hr], 2);
     }
     float *mo = reinterpret_cast<float *>(ring_ptr);              // [warp][16][D]
-    float *mml = mo + kConsumerWarps * 16 * D;                    // [warp][16][2]
-    mma_epilogue<D, KG, FP8>(p, wl, li, kh, o, m, l, alive, mo, mml, s_flags, nr, i0, split, partial, b, t, L, g);
+    float *mml = mo + CW * 16 * D;                                // [warp][16][2]
+    mma_epilogue<D, KG, FP8, CW>(p, wl, li, kh, o, m, l, alive, mo, mml, s_flags, nr, i0, split, partial, b, t, L, g);
 }
 
 // ---------------------------------------------------------------- streaming decode
@@ -933,23 +935,23 @@ cudaError_t make_q_tmap(CUtensorMap *map, const void *q, int num_tokens, int hq,
     return res == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D, int KG, int NB, bool FP8>
+template <int D, int KG, int NB, bool FP8, int CW = kConsumerWarps>
 static cudaError_t launch_mma_dk(const AttnParams &p, const WorkList &wl, int num_items, const CUtensorMap &km,
                                  const CUtensorMap &vm, cudaStream_t stream)
 {
-    constexpr int smem = MmaCfg<D, KG, NB, FP8>::kSmemBytes;
+    constexpr int smem = MmaCfg<D, KG, NB, FP8, CW>::kSmemBytes;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(attn_mma_kernel<D, KG, NB, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        smem);
+        attr_err = cudaFuncSetAttribute(attn_mma_kernel<D, KG, NB, FP8, CW>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     });
     if (attr_err != cudaSuccess) return attr_err;
     if (num_items > 65535) return cudaErrorInvalidConfiguration;
     dim3 grid(p.hkv, num_items);                                // KV heads adjacent: they share pool pages
     launch_begin(stream, wl.mode == kModeDecode ? kAttnMmaDecode : kAttnMmaPrefill);
-    cudaError_t e = launch_maybe_pdl(attn_mma_kernel<D, KG, NB, FP8>, grid, dim3(kMmaThreads), smem, stream, p, wl,
-                                     km, vm);
+    cudaError_t e = launch_maybe_pdl(attn_mma_kernel<D, KG, NB, FP8, CW>, grid, dim3((CW + 1) * 32), smem, stream, p,
+                                     wl, km, vm);
     launch_end(stream);
     return e != cudaSuccess ? e : cudaGetLastError();
 }

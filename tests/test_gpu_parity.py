@@ -612,3 +612,16 @@ def test_long_decodes_with_window_sampled():
     want = oracle_rows(ref, toks, heads, window=4096)
     got = dev.out[torch.tensor(toks), torch.tensor(heads)]
     assert_close(got, want, "long decodes, window 4096")
+
+
+@pytest.mark.parametrize("d,hq,hkv", [(64, 16, 4), (128, 32, 8)])
+def test_short_decodes_head_dims_and_windows(d, hq, hkv):
+    reqs = [Req(L - 1, 1, list(range(64 * i, 64 * i + 64))) for i, L in enumerate((17, 300, 1000, 1024, 640, 1))]
+    spec = Spec("decodes", reqs, hq, hkv, d, 16, 64 * 6 + 2, 1 / math.sqrt(d), 81)
+    b = make_batch(spec, device="cpu")
+    ref = cpu_copy(b)
+    oracle_write(ref)
+    for window in (0, 100):
+        dev = DeviceStep(b, window=window)
+        dev.step()
+        assert_close(dev.out, oracle_full(ref, window=window), f"decodes d{d} window {window}")
