@@ -155,6 +155,16 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x)
     return r;
 }
 
+// Four FP8 E4M3 codes (bytes 0..3 of x) to two fp16 pairs: lo = codes 0, 1
+// and hi = codes 2, 3 (the lower code in the lower half); exact.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t x, uint32_t &lo, uint32_t &hi)
+{
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(x));
+}
+
 // Byte permute: bytes of a (0..3) and b (4..7) picked by the nibbles of sel.
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
 {
