@@ -26,6 +26,8 @@
 // columns (128 bytes) with the 128-byte swizzle, so that ldmatrix reads
 // eight rows without bank conflicts; for head_dim 48 rows are 96 bytes, not
 // swizzled.
+#include <stdlib.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -216,6 +218,195 @@ __device__ __forceinline__ void pack_p(uint32_t (&pa)[4], const float (&p0)[4], 
     }
 }
 
+// ---------------------------------------------------------------- key-major decode tiles
+//
+// A decode CTA holds few rows (t * g <= 8 pairs of (token, query head) per
+// KV head: 2, 4 and 8 on the decode workloads), so a 16-row MMA tile of
+// query rows is mostly padding.  The transposed products put the 16 keys of
+// a block (or 16 head dims) in the MMA's M dimension and up to 8 rows in N:
+//   S^T  = K Q^T        m16 keys      x n8 rows x k16 head dims
+//   O^T += V^T P^T      m16 head dims x n8 rows x k16 keys
+// which halves the MMAs per block.  Lane 4r + c holds S^T for keys r and
+// r + 8 of the block and rows 2c, 2c + 1; a movmatrix of each 8-key half of
+// P^T gives the B fragments of the second product.  O^T tile mt holds, for
+// rows 2c, 2c + 1, head dims ot_dim(mt, r, 0) and ot_dim(mt, r, 1).
+constexpr int kKeyMajorRows = 8;
+
+// Q^T as m16n8k16 B fragments: lane 4r + c holds row r (zero when r >= the
+// CTA's rows).  bf16: dims 2c, 2c+1 and 2c+8, 2c+9 of every 16-dim chunk;
+// FP8 pools: dims 4c .. 4c+3 (the order an ldmatrix of FP8 K rows gives, as
+// in load_q_frags), converted to fp16.
+template <int D, bool FP8>
+__device__ __forceinline__ void load_qt_frags(uint32_t (&qb)[D / 16][2], const __nv_bfloat16 *q, size_t row, bool ok,
+                                              int lane)
+{
+    const int c = lane & 3;
+    if constexpr (!FP8) {
+        const uint32_t *qw = reinterpret_cast<const uint32_t *>(q);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; kk++) {
+            qb[kk][0] = ok ? __ldg(qw + row * (D / 2) + kk * 8 + c) : 0u;
+            qb[kk][1] = ok ? __ldg(qw + row * (D / 2) + kk * 8 + 4 + c) : 0u;
+        }
+    } else {
+        const uint2 *q4 = reinterpret_cast<const uint2 *>(q);      // 4 bf16 per load
+#pragma unroll
+        for (int kk = 0; kk < D / 16; kk++) {
+            const uint2 a = ok ? __ldg(q4 + row * (D / 4) + kk * 4 + c) : make_uint2(0u, 0u);
+            qb[kk][0] = pack_f16x2(bf16_lo(a.x), bf16_hi(a.x));
+            qb[kk][1] = pack_f16x2(bf16_lo(a.y), bf16_hi(a.y));
+        }
+    }
+}
+
+// S^T for one 16-key block (accumulated into s; two chains over alternate
+// head-dim chunks).  FP8: K codes converted to fp16 (exact); the K scales
+// are applied by the caller.
+template <int D, bool FP8>
+__device__ __forceinline__ void block_scores_t(float (&s)[4], const uint32_t (&qb)[D / 16][2], uint32_t kt, int mi,
+                                               int mr)
+{
+    float s1[4] = {0.f, 0.f, 0.f, 0.f};
+    if constexpr (!FP8) {
+        // matrix mi: keys (mi & 1) * 8 .., dims of half mi >> 1 of the chunk
+#pragma unroll
+        for (int kk = 0; kk < D / 16; kk++) {
+            uint32_t a[4];
+            ldsm_x4(kt + tile_off<D>((mi & 1) * 8 + mr, 2 * kk + (mi >> 1)), a[0], a[1], a[2], a[3]);
+            if (kk & 1) mma_16816(s1, a, qb[kk][0], qb[kk][1]);
+            else mma_16816(s, a, qb[kk][0], qb[kk][1]);
+        }
+    } else {
+        // matrix mi: keys (mi & 1) * 8 .., 16-code chunk kk + (mi >> 1); a
+        // lane gets codes 4c .. 4c+3 of one key
+#pragma unroll
+        for (int kk = 0; kk < D / 16; kk += 2) {
+            uint32_t r0, r1, r2, r3, a[4], a2[4];
+            ldsm_x4(kt + tile_off<D, true>((mi & 1) * 8 + mr, kk + (mi >> 1)), r0, r1, r2, r3);
+            e4m3x4_to_f16x2x2(r0, a[0], a[2]);
+            e4m3x4_to_f16x2x2(r1, a[1], a[3]);
+            e4m3x4_to_f16x2x2(r2, a2[0], a2[2]);
+            e4m3x4_to_f16x2x2(r3, a2[1], a2[3]);
+            mma_16816_f16(s, a, qb[kk][0], qb[kk][1]);
+            mma_16816_f16(s1, a2, qb[kk + 1][0], qb[kk + 1][1]);
+        }
+    }
+#pragma unroll
+    for (int v = 0; v < 4; v++) s[v] += s1[v];
+}
+
+// Head dim of O^T tile mt, M-row r (hi = 0) or r + 8 (hi = 1).  FP8 pools:
+// tiles 2q and 2q + 1 hold the even and the odd dims of 16-dim chunks 2q
+// (rows 0-7) and 2q + 1 (rows 8-15), from the byte permute in block_pv_t.
+template <bool FP8>
+__device__ __forceinline__ int ot_dim(int mt, int r, int hi)
+{
+    return FP8 ? 16 * ((mt & ~1) + hi) + 2 * r + (mt & 1) : 16 * mt + 8 * hi + r;
+}
+
+// O^T += V^T P^T for one 16-key block; pb0 / pb1 = P^T for keys 2c, 2c+1 /
+// 2c+8, 2c+9 of row r.
+template <int D, bool FP8>
+__device__ __forceinline__ void block_pv_t(float (&o)[D / 16][4], uint32_t pb0, uint32_t pb1, uint32_t vt, int mi,
+                                           int mr)
+{
+    if constexpr (!FP8) {
+        // matrix mi: keys (mi >> 1) * 8 .., dims of half mi & 1 of tile mt;
+        // transposed, a lane gets keys 2c, 2c+1 of one dim
+#pragma unroll
+        for (int mt = 0; mt < D / 16; mt++) {
+            uint32_t a[4];
+            ldsm_x4_t(vt + tile_off<D>((mi >> 1) * 8 + mr, 2 * mt + (mi & 1)), a[0], a[1], a[2], a[3]);
+            mma_16816(o[mt], a, pb0, pb1);
+        }
+    } else {
+        // matrix mi: keys (mi >> 1) * 8 .., 16-code chunk q + (mi & 1);
+        // transposed, a lane gets dims 2r, 2r+1 of keys 2c, 2c+1, split by the
+        // permute into the even-dim and the odd-dim fp16 pair
+#pragma unroll
+        for (int q = 0; q < D / 16; q += 2) {
+            uint32_t r0, r1, r2, r3, ev[4], od[4];
+            ldsm_x4_t(vt + tile_off<D, true>((mi >> 1) * 8 + mr, q + (mi & 1)), r0, r1, r2, r3);
+            e4m3x4_to_f16x2x2(prmt(r0, 0u, 0x3120u), ev[0], od[0]);
+            e4m3x4_to_f16x2x2(prmt(r1, 0u, 0x3120u), ev[1], od[1]);
+            e4m3x4_to_f16x2x2(prmt(r2, 0u, 0x3120u), ev[2], od[2]);
+            e4m3x4_to_f16x2x2(prmt(r3, 0u, 0x3120u), ev[3], od[3]);
+            mma_16816_f16(o[q], ev, pb0, pb1);
+            mma_16816_f16(o[q + 1], od, pb0, pb1);
+        }
+    }
+}
+
+// Scale into the exp2 domain and mask one block of S^T: s[0], s[1] are key
+// `key` for rows 2c, 2c+1 (positions qp0, qp1; -1 = no row), s[2], s[3] key
+// `key` + 8.  f0 / f1: the factors of the two keys.
+__device__ __forceinline__ void mask_scale_t(float (&s)[4], int key, int k_end, int qp0, int qp1, int wspan, bool has,
+                                             float f0, float f1)
+{
+#pragma unroll
+    for (int v = 0; v < 4; v++) {
+        const int k = key + (v >> 1) * 8;
+        const int qp = (v & 1) ? qp1 : qp0;
+        const bool ok = has && k < k_end && k <= qp && k > qp - wspan;
+        s[v] = ok ? s[v] * ((v >> 1) ? f1 : f0) : -INFINITY;
+    }
+}
+
+// Online softmax over NB blocks of masked S^T (exp2 domain), then O^T +=
+// V^T P^T.  m, l: rows 2c, 2c+1 (l summed over this lane's keys only).  The
+// O^T rescale is skipped when no row of the warp raised its maximum.  FP8:
+// each key's V scale (vs: keys r, r+8) is folded into P, which is fp16.
+template <int D, bool FP8, int NB>
+__device__ __forceinline__ void softmax_pv_t(float (&o)[D / 16][4], float (&m)[2], float (&l)[2], float (&s)[NB][4],
+                                             const float (&vs)[NB][2], const uint32_t (&vt)[NB], const bool (&has)[NB],
+                                             int mi, int mr)
+{
+    float alpha[2];
+#pragma unroll
+    for (int j = 0; j < 2; j++) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < NB; q++) mx = max3f(mx, s[q][j], s[q][2 + j]);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float mnew = fmaxf(m[j], mx);
+        const float ms = mnew == -INFINITY ? 0.f : mnew;
+        alpha[j] = exp2f(m[j] - ms);
+        m[j] = mnew;
+        float sum = 0.f;
+#pragma unroll
+        for (int q = 0; q < NB; q++) {
+            s[q][j] = exp2f(s[q][j] - ms);
+            s[q][2 + j] = exp2f(s[q][2 + j] - ms);
+            sum += s[q][j] + s[q][2 + j];
+        }
+        l[j] = l[j] * alpha[j] + sum;
+    }
+    if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+        for (int mt = 0; mt < D / 16; mt++) {
+            o[mt][0] *= alpha[0];
+            o[mt][2] *= alpha[0];
+            o[mt][1] *= alpha[1];
+            o[mt][3] *= alpha[1];
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < NB; q++) {
+        if (!has[q]) continue;
+        uint32_t lo, hi;                                           // P^T [key][row] halves
+        if constexpr (FP8) {
+            lo = pack_f16x2(s[q][0] * vs[q][0], s[q][1] * vs[q][0]);
+            hi = pack_f16x2(s[q][2] * vs[q][1], s[q][3] * vs[q][1]);
+        } else {
+            lo = pack_bf16x2(s[q][0], s[q][1]);
+            hi = pack_bf16x2(s[q][2], s[q][3]);
+        }
+        block_pv_t<D, FP8>(o, movmatrix_t(lo), movmatrix_t(hi), vt[q], mi, mr);
+    }
+}
+
 // Split-KV combine of one (request, KV head) inside the CTA that completed
 // its last split.  Row (token i, head h) has S partials o_s (unnormalised),
 // m_s (running max, exp2 domain) and l_s (weight sum) at rows
@@ -276,45 +467,83 @@ __device__ __forceinline__ void combine_in_cta(const AttnParams &p, size_t base,
     }
 }
 
-// Epilogue of both MMA kernels, run by the kConsumerWarps consumer warps
-// (named barrier 1).  Merges the KG key groups of each row tile through
-// shared memory (the ring is free by then), writes the CTA's rows as bf16
-// output or as fp32 split partials, and, for split decode rows whose combine
-// runs in the kernel (wl.cnt_off[li] >= 0), counts the finished splits of
-// (request, KV head): the CTA that finishes the last one combines them and
-// returns the counter to zero for the next call.  A CTA whose pipeline wait
-// gave up writes nothing but still counts, so counters stay consistent.
-template <int D, int KG, bool FP8 = false, int CW = kConsumerWarps>
-__device__ __forceinline__ void mma_epilogue(const AttnParams &p, const WorkList &wl, int li, int kh,
-                                             const float (&o)[D / 8][4], const float (&m)[2], const float (&l)[2],
-                                             bool alive, float *mo, float *mml, uint32_t *s_flags, int nr,
-                                             int i0, int split, bool partial, int b, int t, int L, int g)
+// Per-warp results into shared memory for the epilogue (the ring is free
+// once every consumer has passed named barrier 1): o rows at mo[warp][row][D],
+// (m, l) at mml[warp][row][2].  Row-major tiles: lane quad c holds rows
+// lane / 4 and lane / 4 + 8.
+template <int D, bool FP8, int CW>
+__device__ __forceinline__ void stage_rows(const float (&o)[D / 8][4], const float (&m)[2], const float (&l)[2],
+                                           bool alive, float *mo, float *mml, uint32_t *s_flags)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    constexpr int kRT = CW / KG;
-    constexpr int kThreads = CW * 32;
-    named_bar_sync(1, kThreads);                                  // every consumer is done with the ring
-    {
+    named_bar_sync(1, CW * 32);                                   // every consumer is done with the ring
 #pragma unroll
-        for (int hr = 0; hr < 2; hr++) {
-            const int lr = (lane >> 2) + 8 * hr;
+    for (int hr = 0; hr < 2; hr++) {
+        const int lr = (lane >> 2) + 8 * hr;
 #pragma unroll
-            for (int n = 0; n < D / 8; n++) {
-                if constexpr (!FP8) {
-                    *reinterpret_cast<float2 *>(mo + (warp * 16 + lr) * D + o_col<false>(n, lane & 3, 0)) =
-                        make_float2(o[n][2 * hr], o[n][2 * hr + 1]);
-                } else {
-                    mo[(warp * 16 + lr) * D + o_col<true>(n, lane & 3, 0)] = o[n][2 * hr];
-                    mo[(warp * 16 + lr) * D + o_col<true>(n, lane & 3, 1)] = o[n][2 * hr + 1];
-                }
-            }
-            if ((lane & 3) == 0) {
-                mml[(warp * 16 + lr) * 2] = m[hr];
-                mml[(warp * 16 + lr) * 2 + 1] = l[hr];
+        for (int n = 0; n < D / 8; n++) {
+            if constexpr (!FP8) {
+                *reinterpret_cast<float2 *>(mo + (warp * 16 + lr) * D + o_col<false>(n, lane & 3, 0)) =
+                    make_float2(o[n][2 * hr], o[n][2 * hr + 1]);
+            } else {
+                mo[(warp * 16 + lr) * D + o_col<true>(n, lane & 3, 0)] = o[n][2 * hr];
+                mo[(warp * 16 + lr) * D + o_col<true>(n, lane & 3, 1)] = o[n][2 * hr + 1];
             }
         }
-        if (!alive && lane == 0) s_flags[0] = 1u;
+        if ((lane & 3) == 0) {
+            mml[(warp * 16 + lr) * 2] = m[hr];
+            mml[(warp * 16 + lr) * 2 + 1] = l[hr];
+        }
     }
+    if (!alive && lane == 0) s_flags[0] = 1u;
+}
+
+// The same for key-major tiles: lane 4r + c holds rows 2c, 2c+1 (of at
+// most kKeyMajorRows) and their weight sums over keys r, r+8 of each block,
+// which are summed across r here.
+template <int D, bool FP8, int CW>
+__device__ __forceinline__ void stage_rows_t(const float (&o)[D / 16][4], const float (&m)[2], float (&l)[2],
+                                             bool alive, float *mo, float *mml, uint32_t *s_flags)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = lane >> 2, c = lane & 3;
+#pragma unroll
+    for (int j = 0; j < 2; j++) {
+        l[j] += __shfl_xor_sync(0xffffffffu, l[j], 4);
+        l[j] += __shfl_xor_sync(0xffffffffu, l[j], 8);
+        l[j] += __shfl_xor_sync(0xffffffffu, l[j], 16);
+    }
+    named_bar_sync(1, CW * 32);                                   // every consumer is done with the ring
+#pragma unroll
+    for (int j = 0; j < 2; j++) {
+        float *row = mo + (warp * 16 + 2 * c + j) * D;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; mt++) {
+            row[ot_dim<FP8>(mt, r, 0)] = o[mt][j];
+            row[ot_dim<FP8>(mt, r, 1)] = o[mt][2 + j];
+        }
+        if (r == 0) {
+            mml[(warp * 16 + 2 * c + j) * 2] = m[j];
+            mml[(warp * 16 + 2 * c + j) * 2 + 1] = l[j];
+        }
+    }
+    if (!alive && lane == 0) s_flags[0] = 1u;
+}
+
+// Epilogue of both MMA kernels, run by the CW consumer warps (named barrier
+// 1) after stage_rows / stage_rows_t.  Merges the KG key groups of each row
+// tile, writes the CTA's rows as bf16 output or as fp32 split partials, and,
+// for split decode rows whose combine runs in the kernel (wl.cnt_off[li] >=
+// 0), counts the finished splits of (request, KV head): the CTA that finishes
+// the last one combines them and returns the counter to zero for the next
+// call.  A CTA whose pipeline wait gave up writes nothing but still counts,
+// so counters stay consistent.
+template <int D, int KG, int CW = kConsumerWarps>
+__device__ __forceinline__ void mma_epilogue(const AttnParams &p, const WorkList &wl, int li, int kh, float *mo,
+                                             float *mml, uint32_t *s_flags, int nr, int i0, int split, bool partial,
+                                             int b, int t, int L, int g)
+{
+    constexpr int kThreads = CW * 32;
     named_bar_sync(1, kThreads);
     const bool ok = s_flags[0] == 0u;                            // the same in every consumer thread
     // one item = 8 consecutive columns of one row: a 16-byte bf16 store (or
@@ -357,7 +586,6 @@ __device__ __forceinline__ void mma_epilogue(const AttnParams &p, const WorkList
             if (e0 == 0) p.part_ml[orow] = make_float2(M, ls);
         }
     }
-    (void)kRT;
     if (!partial || wl.cnt_off[li] < 0) return;
     // ---- in-kernel split combine: count this split, the last one combines
     const int S = decode_splits(t, L, p.window, wl.split_tokens);
@@ -377,7 +605,7 @@ __device__ __forceinline__ void mma_epilogue(const AttnParams &p, const WorkList
     if (threadIdx.x == 0) atomicExch(cnt, 0u);                    // ready for the next call
 }
 
-template <int D, int KG, int NB, bool FP8, int CW>
+template <int D, int KG, int NB, bool FP8, int CW, bool KM>
 __global__ void __launch_bounds__((CW + 1) * 32) attn_mma_kernel(AttnParams p, const __grid_constant__ WorkList wl,
                                                                const __grid_constant__ CUtensorMap kmap,
                                                                const __grid_constant__ CUtensorMap vmap)
@@ -509,132 +737,198 @@ __global__ void __launch_bounds__((CW + 1) * 32) attn_mma_kernel(AttnParams p, c
 
     // ---------------------------------------------------------------- consumers
     const int rt = warp / KG, kg = warp % KG;
-    const int row0 = rt * 16;
-    const int rA = row0 + (lane >> 2), rB = rA + 8;               // the two rows this lane holds
     const int qbase = L - t + i0;
-    const int qposA = rA < nr ? qbase + rA / g : -1;
-    const int qposB = rB < nr ? qbase + rB / g : -1;
     const int wspan = win_span(p.window);                         // keys <= position - wspan are outside
-
-    // Q as mma A fragments, straight from global memory.
-    uint32_t qa[D / 16][4];
-    {
-        const size_t rowA = rA < nr ? (size_t)(b + i0 + rA / g) * p.hq + kh * g + rA % g : 0;
-        const size_t rowB = rB < nr ? (size_t)(b + i0 + rB / g) * p.hq + kh * g + rB % g : 0;
-        load_q_frags<D, FP8>(qa, p.q, rowA, rowB, rA < nr, rB < nr, lane);
-    }
-
-    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-    float o[D / 8][4];
-#pragma unroll
-    for (int n = 0; n < D / 8; n++) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-
     const float sl2 = p.scale_log2;
     const int mi = lane >> 3, mr = lane & 7;                      // ldmatrix: matrix, row within it
     bool alive = true;
-    // Each iteration takes NB blocks of this key group (kg, kg + KG, ...):
-    // NB independent MMA chains and one softmax update per 16*NB keys
-    // (shorter latency chains); with NB = 1 each warp holds one ring slot at
-    // a time, leaving more of the ring for copies in flight.
-    for (int bl0 = kg; bl0 < nblk; bl0 += NB * KG) {
-        int slot[NB];
-        bool has[NB];
-        bool waited = true;
+    float *mo = reinterpret_cast<float *>(ring_ptr);              // epilogue: [warp][16][D]
+    float *mml = mo + CW * 16 * D;                                // [warp][16][2]
+
+    if constexpr (KM) {
+        // key-major decode tiles (nr <= kKeyMajorRows, one row tile)
+        const int rq = lane >> 2, c2 = 2 * (lane & 3);
+        uint32_t qb[D / 16][2];
+        load_qt_frags<D, FP8>(qb, p.q, rq < nr ? (size_t)(b + i0 + rq / g) * p.hq + kh * g + rq % g : 0, rq < nr,
+                              lane);
+        const int qp0 = c2 < nr ? qbase + c2 / g : -1;
+        const int qp1 = c2 + 1 < nr ? qbase + (c2 + 1) / g : -1;
+        float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+        float o[D / 16][4];
 #pragma unroll
-        for (int q = 0; q < NB; q++) {
-            const int bl = bl0 + q * KG;
-            has[q] = bl < nblk;
-            slot[q] = bl % R;
-            if (has[q] && waited) waited = mbar_wait(full_bar(slot[q]), (bl / R) & 1, p.err);
-        }
-        if (!waited) {
-            alive = false;
-            break;
-        }
-        float sc[2 * NB][4];
+        for (int n = 0; n < D / 16; n++) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+        for (int bl0 = kg; bl0 < nblk; bl0 += NB * KG) {
+            int slot[NB];
+            bool has[NB];
+            bool waited = true;
 #pragma unroll
-        for (int n = 0; n < 2 * NB; n++) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+            for (int q = 0; q < NB; q++) {
+                const int bl = bl0 + q * KG;
+                has[q] = bl < nblk;
+                slot[q] = bl % R;
+                if (has[q] && waited) waited = mbar_wait(full_bar(slot[q]), (bl / R) & 1, p.err);
+            }
+            if (!waited) {
+                alive = false;
+                break;
+            }
+            float sc[NB][4], vs[NB][2];
+            uint32_t vt[NB];
 #pragma unroll
-        for (int q = 0; q < NB; q++)
-            if (has[q]) block_scores<D, FP8>(sc[2 * q], sc[2 * q + 1], qa, slot_addr(slot[q]), mi, mr);
-        // FP8 pools: the K and V scales of this lane's four keys of each block
-        float ksc[2 * NB][2], vsc[2 * NB][2];
+            for (int q = 0; q < NB; q++) {
+                sc[q][0] = sc[q][1] = sc[q][2] = sc[q][3] = 0.f;
+                if (has[q]) block_scores_t<D, FP8>(sc[q], qb, slot_addr(slot[q]), mi, mr);
+            }
 #pragma unroll
-        for (int n = 0; n < 2 * NB; n++) {
-            ksc[n][0] = ksc[n][1] = vsc[n][0] = vsc[n][1] = 1.f;
-            if constexpr (FP8) {
-                const float *sk = reinterpret_cast<const float *>(ring_ptr + slot[n >> 1] * T::kSlot + 2 * T::kTile);
-                const float *sv = sk + T::kScaleTile / 4;
-                const int kr = (n & 1) * 8 + 2 * (lane & 3);    // key row within the block
-                if (has[n >> 1]) {
-                    ksc[n][0] = sk[kr * p.hkv + kh];
-                    ksc[n][1] = sk[(kr + 1) * p.hkv + kh];
-                    vsc[n][0] = sv[kr * p.hkv + kh];
-                    vsc[n][1] = sv[(kr + 1) * p.hkv + kh];
+            for (int q = 0; q < NB; q++) {
+                vt[q] = slot_addr(slot[q]) + T::kTile;
+                float f0 = sl2, f1 = sl2;
+                vs[q][0] = vs[q][1] = 1.f;
+                if constexpr (FP8) {                              // K and V scales of keys rq, rq + 8
+                    if (has[q]) {
+                        const float *sk = reinterpret_cast<const float *>(ring_ptr + slot[q] * T::kSlot + 2 * T::kTile);
+                        const float *sv = sk + T::kScaleTile / 4;
+                        f0 *= sk[rq * p.hkv + kh];
+                        f1 *= sk[(rq + 8) * p.hkv + kh];
+                        vs[q][0] = sv[rq * p.hkv + kh];
+                        vs[q][1] = sv[(rq + 8) * p.hkv + kh];
+                    }
                 }
+                mask_scale_t(sc[q], ((blk0 + bl0 + q * KG) << 4) + rq, k_end, qp0, qp1, wspan, has[q], f0, f1);
+            }
+            softmax_pv_t<D, FP8, NB>(o, m, l, sc, vs, vt, has, mi, mr);
+            __syncwarp();
+            if (lane == 0) {
+#pragma unroll
+                for (int q = 0; q < NB; q++)
+                    if (has[q]) mbar_arrive(empty_bar(slot[q]));
             }
         }
-        // scale into the exp2 domain, causal and range mask
-#pragma unroll
-        for (int n = 0; n < 2 * NB; n++) {
-            const int kc = ((blk0 + bl0 + (n >> 1) * KG) << 4) + (n & 1) * 8 + 2 * (lane & 3);
-#pragma unroll
-            for (int v = 0; v < 4; v++) {
-                const int key = kc + (v & 1);
-                const int qp = v < 2 ? qposA : qposB;
-                const bool ok = has[n >> 1] && key < k_end && key <= qp && key > qp - wspan;
-                sc[n][v] = ok ? sc[n][v] * (FP8 ? ksc[n][v & 1] * sl2 : sl2) : -INFINITY;
-            }
+        pdl_launch_dependents();                                  // a combine kernel may start launching
+        stage_rows_t<D, FP8, CW>(o, m, l, alive, mo, mml, s_flags);
+    } else {
+        const int row0 = rt * 16;
+        const int rA = row0 + (lane >> 2), rB = rA + 8;           // the two rows this lane holds
+        const int qposA = rA < nr ? qbase + rA / g : -1;
+        const int qposB = rB < nr ? qbase + rB / g : -1;
+
+        // Q as mma A fragments, straight from global memory.
+        uint32_t qa[D / 16][4];
+        {
+            const size_t rowA = rA < nr ? (size_t)(b + i0 + rA / g) * p.hq + kh * g + rA % g : 0;
+            const size_t rowB = rB < nr ? (size_t)(b + i0 + rB / g) * p.hq + kh * g + rB % g : 0;
+            load_q_frags<D, FP8>(qa, p.q, rowA, rowB, rA < nr, rB < nr, lane);
         }
-        float pr[2 * NB][4];
+
+        float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+        float o[D / 8][4];
 #pragma unroll
-        for (int hr = 0; hr < 2; hr++) {
-            float mx = -INFINITY;
+        for (int n = 0; n < D / 8; n++) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+
+        // Each iteration takes NB blocks of this key group (kg, kg + KG, ...):
+        // NB independent MMA chains and one softmax update per 16*NB keys
+        // (shorter latency chains); with NB = 1 each warp holds one ring slot
+        // at a time, leaving more of the ring for copies in flight.
+        for (int bl0 = kg; bl0 < nblk; bl0 += NB * KG) {
+            int slot[NB];
+            bool has[NB];
+            bool waited = true;
 #pragma unroll
-            for (int n = 0; n < 2 * NB; n++) mx = max3f(mx, sc[n][2 * hr], sc[n][2 * hr + 1]);
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            const float mnew = fmaxf(m[hr], mx);
-            const float ms = mnew == -INFINITY ? 0.f : mnew;
-            const float alpha = exp2f(m[hr] - ms);
-            m[hr] = mnew;
-            float sum = 0.f;
-#pragma unroll
-            for (int n = 0; n < 2 * NB; n++) {
-                pr[n][2 * hr] = exp2f(sc[n][2 * hr] - ms);
-                pr[n][2 * hr + 1] = exp2f(sc[n][2 * hr + 1] - ms);
-                sum += pr[n][2 * hr] + pr[n][2 * hr + 1];
+            for (int q = 0; q < NB; q++) {
+                const int bl = bl0 + q * KG;
+                has[q] = bl < nblk;
+                slot[q] = bl % R;
+                if (has[q] && waited) waited = mbar_wait(full_bar(slot[q]), (bl / R) & 1, p.err);
             }
-            l[hr] = l[hr] * alpha + sum;
-#pragma unroll
-            for (int n = 0; n < D / 8; n++) {
-                o[n][2 * hr] *= alpha;
-                o[n][2 * hr + 1] *= alpha;
+            if (!waited) {
+                alive = false;
+                break;
             }
-        }
+            float sc[2 * NB][4];
 #pragma unroll
-        for (int q = 0; q < NB; q++) {
-            if (!has[q]) continue;
-            uint32_t pa[4];
-            pack_p<FP8>(pa, pr[2 * q], pr[2 * q + 1], vsc[2 * q], vsc[2 * q + 1]);
-            block_pv<D, FP8>(o, pa, slot_addr(slot[q]) + T::kTile, mi, mr);
-        }
-        __syncwarp();
-        if (lane == 0) {
+            for (int n = 0; n < 2 * NB; n++) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
 #pragma unroll
             for (int q = 0; q < NB; q++)
-                if (has[q]) mbar_arrive(empty_bar(slot[q]));
-        }
-    }
-    pdl_launch_dependents();                                      // a combine kernel may start launching
+                if (has[q]) block_scores<D, FP8>(sc[2 * q], sc[2 * q + 1], qa, slot_addr(slot[q]), mi, mr);
+            // FP8 pools: the K and V scales of this lane's four keys of each block
+            float ksc[2 * NB][2], vsc[2 * NB][2];
 #pragma unroll
-    for (int hr = 0; hr < 2; hr++) {
-        l[hr] += __shfl_xor_sync(0xffffffffu, l[hr], 1);
-        l[hr] += __shfl_xor_sync(0xffffffffu, l[hr], 2);
+            for (int n = 0; n < 2 * NB; n++) {
+                ksc[n][0] = ksc[n][1] = vsc[n][0] = vsc[n][1] = 1.f;
+                if constexpr (FP8) {
+                    const float *sk =
+                        reinterpret_cast<const float *>(ring_ptr + slot[n >> 1] * T::kSlot + 2 * T::kTile);
+                    const float *sv = sk + T::kScaleTile / 4;
+                    const int kr = (n & 1) * 8 + 2 * (lane & 3);    // key row within the block
+                    if (has[n >> 1]) {
+                        ksc[n][0] = sk[kr * p.hkv + kh];
+                        ksc[n][1] = sk[(kr + 1) * p.hkv + kh];
+                        vsc[n][0] = sv[kr * p.hkv + kh];
+                        vsc[n][1] = sv[(kr + 1) * p.hkv + kh];
+                    }
+                }
+            }
+            // scale into the exp2 domain, causal and range mask
+#pragma unroll
+            for (int n = 0; n < 2 * NB; n++) {
+                const int kc = ((blk0 + bl0 + (n >> 1) * KG) << 4) + (n & 1) * 8 + 2 * (lane & 3);
+#pragma unroll
+                for (int v = 0; v < 4; v++) {
+                    const int key = kc + (v & 1);
+                    const int qp = v < 2 ? qposA : qposB;
+                    const bool ok = has[n >> 1] && key < k_end && key <= qp && key > qp - wspan;
+                    sc[n][v] = ok ? sc[n][v] * (FP8 ? ksc[n][v & 1] * sl2 : sl2) : -INFINITY;
+                }
+            }
+            float pr[2 * NB][4];
+#pragma unroll
+            for (int hr = 0; hr < 2; hr++) {
+                float mx = -INFINITY;
+#pragma unroll
+                for (int n = 0; n < 2 * NB; n++) mx = max3f(mx, sc[n][2 * hr], sc[n][2 * hr + 1]);
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                const float mnew = fmaxf(m[hr], mx);
+                const float ms = mnew == -INFINITY ? 0.f : mnew;
+                const float alpha = exp2f(m[hr] - ms);
+                m[hr] = mnew;
+                float sum = 0.f;
+#pragma unroll
+                for (int n = 0; n < 2 * NB; n++) {
+                    pr[n][2 * hr] = exp2f(sc[n][2 * hr] - ms);
+                    pr[n][2 * hr + 1] = exp2f(sc[n][2 * hr + 1] - ms);
+                    sum += pr[n][2 * hr] + pr[n][2 * hr + 1];
+                }
+                l[hr] = l[hr] * alpha + sum;
+#pragma unroll
+                for (int n = 0; n < D / 8; n++) {
+                    o[n][2 * hr] *= alpha;
+                    o[n][2 * hr + 1] *= alpha;
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < NB; q++) {
+                if (!has[q]) continue;
+                uint32_t pa[4];
+                pack_p<FP8>(pa, pr[2 * q], pr[2 * q + 1], vsc[2 * q], vsc[2 * q + 1]);
+                block_pv<D, FP8>(o, pa, slot_addr(slot[q]) + T::kTile, mi, mr);
+            }
+            __syncwarp();
+            if (lane == 0) {
+#pragma unroll
+                for (int q = 0; q < NB; q++)
+                    if (has[q]) mbar_arrive(empty_bar(slot[q]));
+            }
+        }
+        pdl_launch_dependents();                                  // a combine kernel may start launching
+#pragma unroll
+        for (int hr = 0; hr < 2; hr++) {
+            l[hr] += __shfl_xor_sync(0xffffffffu, l[hr], 1);
+            l[hr] += __shfl_xor_sync(0xffffffffu, l[hr], 2);
+        }
+        stage_rows<D, FP8, CW>(o, m, l, alive, mo, mml, s_flags);
     }
-    float *mo = reinterpret_cast<float *>(ring_ptr);              // [warp][16][D]
-    float *mml = mo + CW * 16 * D;                                // [warp][16][2]
-    mma_epilogue<D, KG, FP8, CW>(p, wl, li, kh, o, m, l, alive, mo, mml, s_flags, nr, i0, split, partial, b, t, L, g);
+    mma_epilogue<D, KG, CW>(p, wl, li, kh, mo, mml, s_flags, nr, i0, split, partial, b, t, L, g);
 }
 
 // ---------------------------------------------------------------- streaming decode
@@ -657,7 +951,7 @@ struct StreamCfg {
     static constexpr int kSmemBytes = 1024 + kBodyBytes + 2 * kStages * 8;   // + alignment slack, barriers
 };
 
-template <int D, int KG, bool FP8>
+template <int D, int KG, bool FP8, bool KM>
 __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, const __grid_constant__ WorkList wl,
                                                                const __grid_constant__ CUtensorMap kmap,
                                                                const __grid_constant__ CUtensorMap vmap)
@@ -778,107 +1072,156 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
 
     // ---------------------------------------------------------------- consumers
     const int rt = warp / KG, kg = warp % KG;
-    const int row0 = rt * 16;
-    const int rA = row0 + (lane >> 2), rB = rA + 8;               // the two rows this lane holds
     const int qbase = L - t + i0;
-    const int qposA = rA < nr ? qbase + rA / g : -1;
-    const int qposB = rB < nr ? qbase + rB / g : -1;
     const int wspan = win_span(p.window);                         // keys <= position - wspan are outside
-
-    // Q as mma A fragments, straight from global memory.
-    uint32_t qa[D / 16][4];
-    {
-        const size_t rowA = rA < nr ? (size_t)(b + i0 + rA / g) * p.hq + kh * g + rA % g : 0;
-        const size_t rowB = rB < nr ? (size_t)(b + i0 + rB / g) * p.hq + kh * g + rB % g : 0;
-        load_q_frags<D, FP8>(qa, p.q, rowA, rowB, rA < nr, rB < nr, lane);
-    }
-
-    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-    float o[D / 8][4];
-#pragma unroll
-    for (int n = 0; n < D / 8; n++) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-
     const float sl2 = p.scale_log2;
     const int mi = lane >> 3, mr = lane & 7;                      // ldmatrix: matrix, row within it
     bool alive = true;
-    for (int it = 0; it < iters; it++) {
-        const int s = it % S;
-        if (!mbar_wait(full_bar(s), (it / S) & 1, p.err)) {
-            alive = false;
-            break;
+    float *mo = reinterpret_cast<float *>(ring_ptr);              // epilogue: [warp][16][D]
+    float *mml = mo + kConsumerWarps * 16 * D;                    // [warp][16][2]
+
+    if constexpr (KM) {
+        // key-major decode tiles (nr <= kKeyMajorRows, one row tile)
+        const int rq = lane >> 2, c2 = 2 * (lane & 3);
+        uint32_t qb[D / 16][2];
+        load_qt_frags<D, FP8>(qb, p.q, rq < nr ? (size_t)(b + i0 + rq / g) * p.hq + kh * g + rq % g : 0, rq < nr,
+                              lane);
+        const int qp0 = c2 < nr ? qbase + c2 / g : -1;
+        const int qp1 = c2 + 1 < nr ? qbase + (c2 + 1) / g : -1;
+        float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+        float o[D / 16][4];
+#pragma unroll
+        for (int n = 0; n < D / 16; n++) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+        for (int it = 0; it < iters; it++) {
+            const int s = it % S;
+            if (!mbar_wait(full_bar(s), (it / S) & 1, p.err)) {
+                alive = false;
+                break;
+            }
+            const int bl = it * KG + kg;
+            if (bl < nblk) {
+                const uint32_t kt = ring + s * C::kStageBytes + kg * T::kSlot;
+                float sc[1][4] = {{0.f, 0.f, 0.f, 0.f}}, vs[1][2] = {{1.f, 1.f}};
+                const uint32_t vt[1] = {kt + T::kTile};
+                const bool has[1] = {true};
+                block_scores_t<D, FP8>(sc[0], qb, kt, mi, mr);
+                float f0 = sl2, f1 = sl2;
+                if constexpr (FP8) {                              // K and V scales of keys rq, rq + 8
+                    const float *sk = reinterpret_cast<const float *>(ring_ptr + s * C::kStageBytes + kg * T::kSlot +
+                                                                      2 * T::kTile);
+                    const float *sv = sk + T::kScaleTile / 4;
+                    f0 *= sk[rq * p.hkv + kh];
+                    f1 *= sk[(rq + 8) * p.hkv + kh];
+                    vs[0][0] = sv[rq * p.hkv + kh];
+                    vs[0][1] = sv[(rq + 8) * p.hkv + kh];
+                }
+                mask_scale_t(sc[0], ((blk0 + bl) << 4) + rq, k_end, qp0, qp1, wspan, true, f0, f1);
+                softmax_pv_t<D, FP8, 1>(o, m, l, sc, vs, vt, has, mi, mr);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_bar(s));
         }
-        const int bl = it * KG + kg;
-        if (bl < nblk) {
-            const uint32_t kt = ring + s * C::kStageBytes + kg * T::kSlot;
-            const uint32_t vt = kt + T::kTile;
-            const int key0 = (blk0 + bl) << 4;
-            float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            block_scores<D, FP8>(sc[0], sc[1], qa, kt, mi, mr);
-            // FP8 pools: the K and V scales of this lane's four keys
-            float ksc[2][2] = {{1.f, 1.f}, {1.f, 1.f}}, vsc[2][2] = {{1.f, 1.f}, {1.f, 1.f}};
-            if constexpr (FP8) {
-                const float *sk = reinterpret_cast<const float *>(ring_ptr + s * C::kStageBytes + kg * T::kSlot +
-                                                                  2 * T::kTile);
-                const float *sv = sk + T::kScaleTile / 4;
+        pdl_launch_dependents();                                  // a combine kernel may start launching
+        stage_rows_t<D, FP8, kConsumerWarps>(o, m, l, alive, mo, mml, s_flags);
+    } else {
+        const int row0 = rt * 16;
+        const int rA = row0 + (lane >> 2), rB = rA + 8;           // the two rows this lane holds
+        const int qposA = rA < nr ? qbase + rA / g : -1;
+        const int qposB = rB < nr ? qbase + rB / g : -1;
+
+        // Q as mma A fragments, straight from global memory.
+        uint32_t qa[D / 16][4];
+        {
+            const size_t rowA = rA < nr ? (size_t)(b + i0 + rA / g) * p.hq + kh * g + rA % g : 0;
+            const size_t rowB = rB < nr ? (size_t)(b + i0 + rB / g) * p.hq + kh * g + rB % g : 0;
+            load_q_frags<D, FP8>(qa, p.q, rowA, rowB, rA < nr, rB < nr, lane);
+        }
+
+        float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+        float o[D / 8][4];
+#pragma unroll
+        for (int n = 0; n < D / 8; n++) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+
+        for (int it = 0; it < iters; it++) {
+            const int s = it % S;
+            if (!mbar_wait(full_bar(s), (it / S) & 1, p.err)) {
+                alive = false;
+                break;
+            }
+            const int bl = it * KG + kg;
+            if (bl < nblk) {
+                const uint32_t kt = ring + s * C::kStageBytes + kg * T::kSlot;
+                const uint32_t vt = kt + T::kTile;
+                const int key0 = (blk0 + bl) << 4;
+                float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                block_scores<D, FP8>(sc[0], sc[1], qa, kt, mi, mr);
+                // FP8 pools: the K and V scales of this lane's four keys
+                float ksc[2][2] = {{1.f, 1.f}, {1.f, 1.f}}, vsc[2][2] = {{1.f, 1.f}, {1.f, 1.f}};
+                if constexpr (FP8) {
+                    const float *sk = reinterpret_cast<const float *>(ring_ptr + s * C::kStageBytes + kg * T::kSlot +
+                                                                      2 * T::kTile);
+                    const float *sv = sk + T::kScaleTile / 4;
+#pragma unroll
+                    for (int n = 0; n < 2; n++) {
+                        const int kr = n * 8 + 2 * (lane & 3);
+                        ksc[n][0] = sk[kr * p.hkv + kh];
+                        ksc[n][1] = sk[(kr + 1) * p.hkv + kh];
+                        vsc[n][0] = sv[kr * p.hkv + kh];
+                        vsc[n][1] = sv[(kr + 1) * p.hkv + kh];
+                    }
+                }
+                // scale into the exp2 domain, causal and range mask
+                const int kc = key0 + 2 * (lane & 3);
 #pragma unroll
                 for (int n = 0; n < 2; n++) {
-                    const int kr = n * 8 + 2 * (lane & 3);
-                    ksc[n][0] = sk[kr * p.hkv + kh];
-                    ksc[n][1] = sk[(kr + 1) * p.hkv + kh];
-                    vsc[n][0] = sv[kr * p.hkv + kh];
-                    vsc[n][1] = sv[(kr + 1) * p.hkv + kh];
+#pragma unroll
+                    for (int v = 0; v < 4; v++) {
+                        const int key = kc + n * 8 + (v & 1);
+                        const int qp = v < 2 ? qposA : qposB;
+                        sc[n][v] = (key < k_end && key <= qp && key > qp - wspan)
+                                       ? sc[n][v] * (FP8 ? ksc[n][v & 1] * sl2 : sl2) : -INFINITY;
+                    }
                 }
-            }
-            // scale into the exp2 domain, causal and range mask
-            const int kc = key0 + 2 * (lane & 3);
+                float pr[2][4];
 #pragma unroll
-            for (int n = 0; n < 2; n++) {
+                for (int hr = 0; hr < 2; hr++) {
+                    float mx =
+                        fmaxf(fmaxf(sc[0][2 * hr], sc[0][2 * hr + 1]), fmaxf(sc[1][2 * hr], sc[1][2 * hr + 1]));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                    const float mnew = fmaxf(m[hr], mx);
+                    const float ms = mnew == -INFINITY ? 0.f : mnew;
+                    const float alpha = exp2f(m[hr] - ms);
+                    m[hr] = mnew;
+                    pr[0][2 * hr] = exp2f(sc[0][2 * hr] - ms);
+                    pr[0][2 * hr + 1] = exp2f(sc[0][2 * hr + 1] - ms);
+                    pr[1][2 * hr] = exp2f(sc[1][2 * hr] - ms);
+                    pr[1][2 * hr + 1] = exp2f(sc[1][2 * hr + 1] - ms);
+                    l[hr] = l[hr] * alpha + (pr[0][2 * hr] + pr[0][2 * hr + 1]) +
+                            (pr[1][2 * hr] + pr[1][2 * hr + 1]);
 #pragma unroll
-                for (int v = 0; v < 4; v++) {
-                    const int key = kc + n * 8 + (v & 1);
-                    const int qp = v < 2 ? qposA : qposB;
-                    sc[n][v] = (key < k_end && key <= qp && key > qp - wspan)
-                                   ? sc[n][v] * (FP8 ? ksc[n][v & 1] * sl2 : sl2) : -INFINITY;
+                    for (int n = 0; n < D / 8; n++) {
+                        o[n][2 * hr] *= alpha;
+                        o[n][2 * hr + 1] *= alpha;
+                    }
                 }
+                uint32_t pa[4];
+                pack_p<FP8>(pa, pr[0], pr[1], vsc[0], vsc[1]);
+                block_pv<D, FP8>(o, pa, vt, mi, mr);
             }
-            float pr[2][4];
-#pragma unroll
-            for (int hr = 0; hr < 2; hr++) {
-                float mx = fmaxf(fmaxf(sc[0][2 * hr], sc[0][2 * hr + 1]), fmaxf(sc[1][2 * hr], sc[1][2 * hr + 1]));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                const float mnew = fmaxf(m[hr], mx);
-                const float ms = mnew == -INFINITY ? 0.f : mnew;
-                const float alpha = exp2f(m[hr] - ms);
-                m[hr] = mnew;
-                pr[0][2 * hr] = exp2f(sc[0][2 * hr] - ms);
-                pr[0][2 * hr + 1] = exp2f(sc[0][2 * hr + 1] - ms);
-                pr[1][2 * hr] = exp2f(sc[1][2 * hr] - ms);
-                pr[1][2 * hr + 1] = exp2f(sc[1][2 * hr + 1] - ms);
-                l[hr] = l[hr] * alpha + (pr[0][2 * hr] + pr[0][2 * hr + 1]) + (pr[1][2 * hr] + pr[1][2 * hr + 1]);
-#pragma unroll
-                for (int n = 0; n < D / 8; n++) {
-                    o[n][2 * hr] *= alpha;
-                    o[n][2 * hr + 1] *= alpha;
-                }
-            }
-            uint32_t pa[4];
-            pack_p<FP8>(pa, pr[0], pr[1], vsc[0], vsc[1]);
-            block_pv<D, FP8>(o, pa, vt, mi, mr);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_bar(s));
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty_bar(s));
-    }
 
-    pdl_launch_dependents();                                      // a combine kernel may start launching
+        pdl_launch_dependents();                                  // a combine kernel may start launching
 #pragma unroll
-    for (int hr = 0; hr < 2; hr++) {
-        l[hr] += __shfl_xor_sync(0xffffffffu, l[hr], 1);
-        l[hr] += __shfl_xor_sync(0xffffffffu, l[hr], 2);
+        for (int hr = 0; hr < 2; hr++) {
+            l[hr] += __shfl_xor_sync(0xffffffffu, l[hr], 1);
+            l[hr] += __shfl_xor_sync(0xffffffffu, l[hr], 2);
+        }
+        stage_rows<D, FP8, kConsumerWarps>(o, m, l, alive, mo, mml, s_flags);
     }
-    float *mo = reinterpret_cast<float *>(ring_ptr);              // [warp][16][D]
-    float *mml = mo + kConsumerWarps * 16 * D;                    // [warp][16][2]
-    mma_epilogue<D, KG, FP8>(p, wl, li, kh, o, m, l, alive, mo, mml, s_flags, nr, i0, split, partial, b, t, L, g);
+    mma_epilogue<D, KG>(p, wl, li, kh, mo, mml, s_flags, nr, i0, split, partial, b, t, L, g);
 }
 
 // ---------------------------------------------------------------- host side
@@ -947,7 +1290,7 @@ cudaError_t make_q_tmap(CUtensorMap *map, const void *q, int num_tokens, int hq,
     return res == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D, int KG, int NB, bool FP8, int CW = kConsumerWarps>
+template <int D, int KG, int NB, bool FP8, int CW = kConsumerWarps, bool KM = false>
 static cudaError_t launch_mma_dk(const AttnParams &p, const WorkList &wl, int num_items, const CUtensorMap &km,
                                  const CUtensorMap &vm, cudaStream_t stream)
 {
@@ -955,20 +1298,20 @@ static cudaError_t launch_mma_dk(const AttnParams &p, const WorkList &wl, int nu
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(attn_mma_kernel<D, KG, NB, FP8, CW>,
+        attr_err = cudaFuncSetAttribute(attn_mma_kernel<D, KG, NB, FP8, CW, KM>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     });
     if (attr_err != cudaSuccess) return attr_err;
     if (num_items > 65535) return cudaErrorInvalidConfiguration;
     dim3 grid(p.hkv, num_items);                                // KV heads adjacent: they share pool pages
     launch_begin(stream, wl.mode == kModeDecode ? kAttnMmaDecode : kAttnMmaPrefill);
-    cudaError_t e = launch_maybe_pdl(attn_mma_kernel<D, KG, NB, FP8, CW>, grid, dim3((CW + 1) * 32), smem, stream, p,
+    cudaError_t e = launch_maybe_pdl(attn_mma_kernel<D, KG, NB, FP8, CW, KM>, grid, dim3((CW + 1) * 32), smem, stream, p,
                                      wl, km, vm);
     launch_end(stream);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool KM>
 static cudaError_t launch_stream_d(const AttnParams &p, const WorkList &wl, int num_items, const CUtensorMap &km,
                                    const CUtensorMap &vm, cudaStream_t stream)
 {
@@ -976,14 +1319,14 @@ static cudaError_t launch_stream_d(const AttnParams &p, const WorkList &wl, int 
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(attn_stream_kernel<D, 4, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(attn_stream_kernel<D, 4, FP8, KM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         smem);
     });
     if (attr_err != cudaSuccess) return attr_err;
     if (num_items > 65535) return cudaErrorInvalidConfiguration;
     dim3 grid(p.hkv, num_items);                                // KV heads adjacent: they share pool pages
     launch_begin(stream, kAttnMmaDecode);
-    cudaError_t e = launch_maybe_pdl(attn_stream_kernel<D, 4, FP8>, grid, dim3(kMmaThreads), smem, stream, p, wl, km,
+    cudaError_t e = launch_maybe_pdl(attn_stream_kernel<D, 4, FP8, KM>, grid, dim3(kMmaThreads), smem, stream, p, wl, km,
                                      vm);
     launch_end(stream);
     return e != cudaSuccess ? e : cudaGetLastError();
@@ -991,16 +1334,26 @@ static cudaError_t launch_stream_d(const AttnParams &p, const WorkList &wl, int 
 
 // Decode-class CTAs: 4 key groups; the streaming kernel when each CTA
 // walks a long key range, the slot-ring kernel with two blocks per
-// iteration when ranges are short and latency dominates.  Prefill-class
-// CTAs: 2 row tiles x 2 key groups, two blocks per iteration.
+// iteration when ranges are short and latency dominates; key-major tiles
+// when every listed request has at most kKeyMajorRows rows per KV head
+// (PKV_DECODE_ROW_TILES=1 keeps the 16-row tiles, for comparison).
+// Prefill-class CTAs: 2 row tiles x 2 key groups, two blocks per iteration.
 template <int D, bool FP8>
 static cudaError_t launch_mma_d(const AttnParams &p, const WorkList &wl, int num_items, const CUtensorMap &km,
                                 const CUtensorMap &vm, cudaStream_t stream)
 {
     constexpr int NB = 2;                                       // blocks per warp iteration
     if (wl.mode != kModeDecode) return launch_mma_dk<D, 2, NB, FP8>(p, wl, num_items, km, vm, stream);
-    if (wl.split_tokens >= kLongSplit) return launch_stream_d<D, FP8>(p, wl, num_items, km, vm, stream);
-    return launch_mma_dk<D, 4, NB, FP8>(p, wl, num_items, km, vm, stream);
+    int max_t = 0;
+    for (int i = 0; i < wl.n; i++) max_t = wl.qt[i] > max_t ? wl.qt[i] : max_t;
+    const char *env = getenv("PKV_DECODE_ROW_TILES");
+    const bool km_tiles = max_t * p.group <= kKeyMajorRows && !(env && *env && atoi(env) != 0);
+    if (wl.split_tokens >= kLongSplit) {
+        return km_tiles ? launch_stream_d<D, FP8, true>(p, wl, num_items, km, vm, stream)
+                        : launch_stream_d<D, FP8, false>(p, wl, num_items, km, vm, stream);
+    }
+    return km_tiles ? launch_mma_dk<D, 4, NB, FP8, kConsumerWarps, true>(p, wl, num_items, km, vm, stream)
+                    : launch_mma_dk<D, 4, NB, FP8>(p, wl, num_items, km, vm, stream);
 }
 
 cudaError_t launch_attn_mma(const AttnParams &p, const WorkList &wl, int head_dim, int num_items,

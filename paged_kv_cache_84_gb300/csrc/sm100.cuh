@@ -126,6 +126,16 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t 
                  : "r"(addr));
 }
 
+// Transpose of an 8x8 matrix of 16-bit elements held one 32-bit pair per
+// lane (lane 4r + c: row r, columns 2c, 2c+1): afterwards lane 4r + c holds
+// row r, columns 2c, 2c+1 of the transpose.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x)
+{
+    uint32_t r;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+    return r;
+}
+
 // d += a * b, m16n8k16, bf16 inputs, fp32 accumulate (A row-major, B column-major).
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
 {

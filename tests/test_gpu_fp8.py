@@ -94,14 +94,16 @@ def test_fp8_write_bit_exact_and_attention_parity(case):
     assert pkv.read_device_error(ws) == 0
 
 
+@pytest.mark.parametrize("row_tiles", ["0", "1"], ids=["key-major", "row-tiles"])
 @pytest.mark.parametrize("split", ["128", "1024"])
 @pytest.mark.parametrize("window", [0, 300])
-def test_fp8_split_paths_and_window(split, window, monkeypatch):
+def test_fp8_split_paths_and_window(split, window, row_tiles, monkeypatch):
     """Decode splits on the slot-ring (128) and the streaming kernel (1024),
-    with and without a sliding window."""
+    in key-major and in 16-row tiles, with and without a sliding window."""
     monkeypatch.setenv("PKV_SPLIT_TOKENS", split)
+    monkeypatch.setenv("PKV_DECODE_ROW_TILES", row_tiles)
     reqs = [Req(3000, 1, list(range(0, 188))), Req(700, 40, list(range(188, 235))),
-            Req(2500, 3, list(range(235, 392))), Req(5000, 1, list(range(392, 705)))]
+            Req(2500, 2, list(range(235, 392))), Req(5000, 1, list(range(392, 705)))]
     spec = Spec("fp8-paths", reqs, 32, 8, 128, 16, 710, 1 / math.sqrt(128), 71)
     b = make_batch(spec, device="cpu")
     pools = _quantized_pools(b, 72)

@@ -625,3 +625,31 @@ def test_short_decodes_head_dims_and_windows(d, hq, hkv):
         dev = DeviceStep(b, window=window)
         dev.step()
         assert_close(dev.out, oracle_full(ref, window=window), f"decodes d{d} window {window}")
+
+
+@pytest.mark.parametrize("row_tiles", [0, 1], ids=["key-major", "row-tiles"])
+@pytest.mark.parametrize("split", [128, 1024], ids=["slot-ring", "streaming"])
+@pytest.mark.parametrize("d,hq,hkv", [(48, 8, 4), (64, 16, 4), (128, 64, 8)])
+def test_decode_tile_forms(d, hq, hkv, split, row_tiles, monkeypatch):
+    """Decode CTAs of at most 8 rows per KV head run key-major tiles (keys in
+    the MMA's M dimension); PKV_DECODE_ROW_TILES=1 keeps the 16-row tiles.
+    Both forms, both decode kernels, t = 1 and 2 where g allows, a window."""
+    monkeypatch.setenv("PKV_SPLIT_TOKENS", str(split))
+    monkeypatch.setenv("PKV_DECODE_ROW_TILES", str(row_tiles))
+    g = hq // hkv
+    lens = (17, 300, 1000, 2048, 2500, 1, 5000)
+    reqs, blk = [], 0
+    for i, L in enumerate(lens):
+        t = 2 if (g * 2 <= 8 and i % 2 == 1 and L > 1) else 1
+        nb = (L + 15) // 16
+        reqs.append(Req(L - t, t, list(range(blk, blk + nb))))
+        blk += nb
+    spec = Spec("decode-tiles", reqs, hq, hkv, d, 16, blk + 2, 1 / math.sqrt(d), 83)
+    b = make_batch(spec, device="cpu")
+    ref = cpu_copy(b)
+    oracle_write(ref)
+    for window in (0, 700):
+        dev = DeviceStep(b, window=window)
+        dev.step()
+        assert_close(dev.out, oracle_full(ref, window=window), f"decode tiles d{d} split {split} window {window}")
+        assert pkv.read_device_error(dev.ws) == 0
