@@ -223,7 +223,7 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q,
  * (every E4M3 value is an fp16 value; q rounds to fp16 exactly within its
  * range), so |q| and the per-key weight * V scale must stay inside fp16's
  * range (65504).  Requirements (else PKV_ERR_UNSUPPORTED): head_dim 128,
- * num_kv_heads a multiple of 4 and at most 16; the CUDA-core kernels
+ * num_kv_heads a multiple of 4; the CUDA-core kernels
  * (PKV_ATTN_CUDA_CORE) have no quantized path.  Prefill chunks run on the
  * warp-level MMA kernels, not on tcgen05.
  */

@@ -44,8 +44,9 @@ constexpr int kStageBudget = 64 * 1024;
 constexpr int kLongSplit = 512;              // decode splits of at least this many keys use the streaming kernel
 
 // Quantized pools: FP8 E4M3 K/V (one byte per element) with an fp32 scale
-// per (slot, KV head); a block's scales of every KV head are staged with it.
-constexpr int kFp8MaxHkv = 16;
+// per (slot, KV head).  A block's scales are staged with it as one 2-D TMA
+// box of 16 slots x the 4 KV heads of the CTA's group of four (256 bytes).
+constexpr int kScaleHeads = 4;
 
 template <int D, bool FP8 = false>
 struct MmaTile {
@@ -56,8 +57,10 @@ struct MmaTile {
     static constexpr int kBoxes = D / kBoxCols;              // boxes per 16-row slice
     static constexpr int kBoxBytes = 16 * kBoxCols * kElem;
     static constexpr int kTile = 16 * kRowBytes;             // one K (or V) slice
-    static constexpr int kScaleTile = FP8 ? 16 * kFp8MaxHkv * 4 : 0;   // [16 slots][Hkv] fp32
-    static constexpr int kSlot = 2 * kTile + 2 * kScaleTile; // K, V, K scales, V scales
+    static constexpr int kScaleTile = FP8 ? 16 * kScaleHeads * 4 : 0;  // [16 slots][4 heads] fp32
+    static constexpr int kData = 2 * kTile + 2 * kScaleTile; // K, V, K scales, V scales
+    // one-block ring slots keep swizzled tiles on 1024-byte boundaries
+    static constexpr int kSlot = kSwizzle ? (kData + 1023) / 1024 * 1024 : kData;
 };
 
 // Byte offset of 16-byte chunk `chunk` of row `row` inside a K or V slice.
@@ -608,7 +611,9 @@ __device__ __forceinline__ void mma_epilogue(const AttnParams &p, const WorkList
 template <int D, int KG, int NB, bool FP8, int CW, bool KM>
 __global__ void __launch_bounds__((CW + 1) * 32) attn_mma_kernel(AttnParams p, const __grid_constant__ WorkList wl,
                                                                const __grid_constant__ CUtensorMap kmap,
-                                                               const __grid_constant__ CUtensorMap vmap)
+                                                               const __grid_constant__ CUtensorMap vmap,
+                                                               const __grid_constant__ CUtensorMap ksmap,
+                                                               const __grid_constant__ CUtensorMap vsmap)
 {
     using T = MmaTile<D, FP8>;
     using C = MmaCfg<D, KG, NB, FP8, CW>;
@@ -687,6 +692,10 @@ __global__ void __launch_bounds__((CW + 1) * 32) attn_mma_kernel(AttnParams p, c
         if (lane == 0) {
             prefetch_tmap(&kmap);
             prefetch_tmap(&vmap);
+            if constexpr (FP8) {
+                prefetch_tmap(&ksmap);
+                prefetch_tmap(&vsmap);
+            }
         }
         const int32_t *bt = p.block_table + (size_t)r * p.bt_stride + blk0;
         // The block table is not written by the step's K/V scatter: read the
@@ -707,9 +716,8 @@ __global__ void __launch_bounds__((CW + 1) * 32) attn_mma_kernel(AttnParams p, c
                     blk = 0;
                 }
                 // a block's K and V slices of this head, and for FP8 pools the
-                // block's K and V scales of every head ([16 slots][Hkv] fp32)
-                const uint32_t scale_bytes = FP8 ? 16u * p.hkv * 4u : 0u;
-                mbar_arrive_expect_tx(full_bar(s), 2 * T::kTile + 2 * scale_bytes);
+                // block's K and V scales of this head's group of four
+                mbar_arrive_expect_tx(full_bar(s), T::kData);
                 const uint32_t dst = slot_addr(s);
 #pragma unroll
                 for (int x = 0; x < T::kBoxes; x++) {
@@ -717,10 +725,10 @@ __global__ void __launch_bounds__((CW + 1) * 32) attn_mma_kernel(AttnParams p, c
                     tma_load_3d(dst + T::kTile + x * T::kBoxBytes, &vmap, full_bar(s), x * T::kBoxCols, kh,
                                 blk * 16);
                 }
-                if constexpr (FP8) {                              // the block's scale rows are contiguous
-                    bulk_load(dst + 2 * T::kTile, p.k_scale + (size_t)blk * 16 * p.hkv, scale_bytes, full_bar(s));
-                    bulk_load(dst + 2 * T::kTile + T::kScaleTile, p.v_scale + (size_t)blk * 16 * p.hkv, scale_bytes,
-                              full_bar(s));
+                if constexpr (FP8) {
+                    tma_load_2d(dst + 2 * T::kTile, &ksmap, full_bar(s), kh & ~(kScaleHeads - 1), blk * 16);
+                    tma_load_2d(dst + 2 * T::kTile + T::kScaleTile, &vsmap, full_bar(s), kh & ~(kScaleHeads - 1),
+                                blk * 16);
                 }
             }
             __syncwarp();
@@ -788,10 +796,11 @@ __global__ void __launch_bounds__((CW + 1) * 32) attn_mma_kernel(AttnParams p, c
                     if (has[q]) {
                         const float *sk = reinterpret_cast<const float *>(ring_ptr + slot[q] * T::kSlot + 2 * T::kTile);
                         const float *sv = sk + T::kScaleTile / 4;
-                        f0 *= sk[rq * p.hkv + kh];
-                        f1 *= sk[(rq + 8) * p.hkv + kh];
-                        vs[q][0] = sv[rq * p.hkv + kh];
-                        vs[q][1] = sv[(rq + 8) * p.hkv + kh];
+                        const int hs = kh & (kScaleHeads - 1);
+                        f0 *= sk[rq * kScaleHeads + hs];
+                        f1 *= sk[(rq + 8) * kScaleHeads + hs];
+                        vs[q][0] = sv[rq * kScaleHeads + hs];
+                        vs[q][1] = sv[(rq + 8) * kScaleHeads + hs];
                     }
                 }
                 mask_scale_t(sc[q], ((blk0 + bl0 + q * KG) << 4) + rq, k_end, qp0, qp1, wspan, has[q], f0, f1);
@@ -860,11 +869,12 @@ __global__ void __launch_bounds__((CW + 1) * 32) attn_mma_kernel(AttnParams p, c
                         reinterpret_cast<const float *>(ring_ptr + slot[n >> 1] * T::kSlot + 2 * T::kTile);
                     const float *sv = sk + T::kScaleTile / 4;
                     const int kr = (n & 1) * 8 + 2 * (lane & 3);    // key row within the block
+                    const int hs = kh & (kScaleHeads - 1);
                     if (has[n >> 1]) {
-                        ksc[n][0] = sk[kr * p.hkv + kh];
-                        ksc[n][1] = sk[(kr + 1) * p.hkv + kh];
-                        vsc[n][0] = sv[kr * p.hkv + kh];
-                        vsc[n][1] = sv[(kr + 1) * p.hkv + kh];
+                        ksc[n][0] = sk[kr * kScaleHeads + hs];
+                        ksc[n][1] = sk[(kr + 1) * kScaleHeads + hs];
+                        vsc[n][0] = sv[kr * kScaleHeads + hs];
+                        vsc[n][1] = sv[(kr + 1) * kScaleHeads + hs];
                     }
                 }
             }
@@ -935,16 +945,23 @@ __global__ void __launch_bounds__((CW + 1) * 32) attn_mma_kernel(AttnParams p, c
 //
 // Long decode splits (at least kLongSplit keys per CTA) stream their blocks
 // through a ring of stages of KG blocks each, one full/empty barrier pair per
-// stage: every consumer warp takes one block of each stage.  Measured on the
+// stage: every consumer warp takes one block of each stage.  A stage holds
+// its KG K slices, then its KG V slices, then (FP8 pools) the KG K-scale and
+// KG V-scale boxes, so that swizzled slices stay on 1024-byte boundaries
+// without padding.  Measured on the
 // 256-request and the 32 x 32768 decode workloads this keeps more copies in
 // flight per SM than the one-block slot ring above, which wins on short,
 // latency-bound ranges instead.
 template <int D, int KG, bool FP8 = false>
 struct StreamCfg {
     static constexpr int kRT = kConsumerWarps / KG;                          // row tiles
-    static constexpr int kStages0 = kStageBudget / (KG * MmaTile<D, FP8>::kSlot);
+    using T = MmaTile<D, FP8>;
+    static constexpr int kStageBytes = KG * T::kData;
+    static constexpr int kStages0 = kStageBudget / kStageBytes;
     static constexpr int kStages = kStages0 > 8 ? 8 : (kStages0 < 2 ? 2 : kStages0);
-    static constexpr int kStageBytes = KG * MmaTile<D, FP8>::kSlot;
+    static constexpr int kVOff = KG * T::kTile;                              // offsets within a stage
+    static constexpr int kKsOff = 2 * KG * T::kTile;
+    static constexpr int kVsOff = kKsOff + KG * T::kScaleTile;
     static constexpr int kRingBytes = kStages * kStageBytes;
     static constexpr int kMergeBytes = kConsumerWarps * 16 * (D + 2) * 4;
     static constexpr int kBodyBytes = kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes;
@@ -954,7 +971,9 @@ struct StreamCfg {
 template <int D, int KG, bool FP8, bool KM>
 __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, const __grid_constant__ WorkList wl,
                                                                const __grid_constant__ CUtensorMap kmap,
-                                                               const __grid_constant__ CUtensorMap vmap)
+                                                               const __grid_constant__ CUtensorMap vmap,
+                                                               const __grid_constant__ CUtensorMap ksmap,
+                                                               const __grid_constant__ CUtensorMap vsmap)
 {
     using T = MmaTile<D, FP8>;
     using C = StreamCfg<D, KG, FP8>;
@@ -1021,8 +1040,11 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
         if (lane == 0) {
             prefetch_tmap(&kmap);
             prefetch_tmap(&vmap);
+            if constexpr (FP8) {
+                prefetch_tmap(&ksmap);
+                prefetch_tmap(&vsmap);
+            }
         }
-        const uint32_t scale_bytes = FP8 ? 16u * p.hkv * 4u : 0u;   // a block's scales of every head
         const int32_t *bt = p.block_table + (size_t)r * p.bt_stride + blk0;
         int ids = lane < nblk ? __ldg(bt + lane) : 0, issued = 0;   // not written by the scatter
         pdl_wait();                                               // the step's K/V rows are in the pool
@@ -1035,7 +1057,7 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
             if (!__all_sync(0xffffffffu, ok)) break;
             issued = it + 1;
             const int nv = min(KG, nblk - base);
-            if (lane == 0) mbar_arrive_expect_tx(full_bar(s), nv * (2 * T::kTile + 2 * scale_bytes));
+            if (lane == 0) mbar_arrive_expect_tx(full_bar(s), nv * T::kData);
             for (int j = 0; j < nv; j++) {
                 int blk = __shfl_sync(0xffffffffu, ids, (base + j) & 31);
                 if (lane == 0) {
@@ -1043,17 +1065,16 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
                         atomicOr(p.err, 2u);
                         blk = 0;
                     }
-                    const uint32_t dst = ring + s * C::kStageBytes + j * T::kSlot;
+                    const uint32_t st = ring + s * C::kStageBytes;
+                    const uint32_t kd = st + j * T::kTile, vd = st + C::kVOff + j * T::kTile;
                     for (int x = 0; x < T::kBoxes; x++) {
-                        tma_load_3d(dst + x * T::kBoxBytes, &kmap, full_bar(s), x * T::kBoxCols, kh, blk * 16);
-                        tma_load_3d(dst + T::kTile + x * T::kBoxBytes, &vmap, full_bar(s), x * T::kBoxCols, kh,
-                                    blk * 16);
+                        tma_load_3d(kd + x * T::kBoxBytes, &kmap, full_bar(s), x * T::kBoxCols, kh, blk * 16);
+                        tma_load_3d(vd + x * T::kBoxBytes, &vmap, full_bar(s), x * T::kBoxCols, kh, blk * 16);
                     }
-                    if constexpr (FP8) {                          // the block's scale rows are contiguous
-                        bulk_load(dst + 2 * T::kTile, p.k_scale + (size_t)blk * 16 * p.hkv, scale_bytes,
-                                  full_bar(s));
-                        bulk_load(dst + 2 * T::kTile + T::kScaleTile, p.v_scale + (size_t)blk * 16 * p.hkv,
-                                  scale_bytes, full_bar(s));
+                    if constexpr (FP8) {
+                        const int h4 = kh & ~(kScaleHeads - 1);
+                        tma_load_2d(st + C::kKsOff + j * T::kScaleTile, &ksmap, full_bar(s), h4, blk * 16);
+                        tma_load_2d(st + C::kVsOff + j * T::kScaleTile, &vsmap, full_bar(s), h4, blk * 16);
                     }
                 }
             }
@@ -1100,20 +1121,21 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
             }
             const int bl = it * KG + kg;
             if (bl < nblk) {
-                const uint32_t kt = ring + s * C::kStageBytes + kg * T::kSlot;
+                const uint32_t kt = ring + s * C::kStageBytes + kg * T::kTile;
                 float sc[1][4] = {{0.f, 0.f, 0.f, 0.f}}, vs[1][2] = {{1.f, 1.f}};
-                const uint32_t vt[1] = {kt + T::kTile};
+                const uint32_t vt[1] = {kt + C::kVOff};
                 const bool has[1] = {true};
                 block_scores_t<D, FP8>(sc[0], qb, kt, mi, mr);
                 float f0 = sl2, f1 = sl2;
                 if constexpr (FP8) {                              // K and V scales of keys rq, rq + 8
-                    const float *sk = reinterpret_cast<const float *>(ring_ptr + s * C::kStageBytes + kg * T::kSlot +
-                                                                      2 * T::kTile);
-                    const float *sv = sk + T::kScaleTile / 4;
-                    f0 *= sk[rq * p.hkv + kh];
-                    f1 *= sk[(rq + 8) * p.hkv + kh];
-                    vs[0][0] = sv[rq * p.hkv + kh];
-                    vs[0][1] = sv[(rq + 8) * p.hkv + kh];
+                    const uint8_t *st = ring_ptr + s * C::kStageBytes;
+                    const float *sk = reinterpret_cast<const float *>(st + C::kKsOff + kg * T::kScaleTile);
+                    const float *sv = reinterpret_cast<const float *>(st + C::kVsOff + kg * T::kScaleTile);
+                    const int hs = kh & (kScaleHeads - 1);
+                    f0 *= sk[rq * kScaleHeads + hs];
+                    f1 *= sk[(rq + 8) * kScaleHeads + hs];
+                    vs[0][0] = sv[rq * kScaleHeads + hs];
+                    vs[0][1] = sv[(rq + 8) * kScaleHeads + hs];
                 }
                 mask_scale_t(sc[0], ((blk0 + bl) << 4) + rq, k_end, qp0, qp1, wspan, true, f0, f1);
                 softmax_pv_t<D, FP8, 1>(o, m, l, sc, vs, vt, has, mi, mr);
@@ -1150,24 +1172,25 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
             }
             const int bl = it * KG + kg;
             if (bl < nblk) {
-                const uint32_t kt = ring + s * C::kStageBytes + kg * T::kSlot;
-                const uint32_t vt = kt + T::kTile;
+                const uint32_t kt = ring + s * C::kStageBytes + kg * T::kTile;
+                const uint32_t vt = kt + C::kVOff;
                 const int key0 = (blk0 + bl) << 4;
                 float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
                 block_scores<D, FP8>(sc[0], sc[1], qa, kt, mi, mr);
                 // FP8 pools: the K and V scales of this lane's four keys
                 float ksc[2][2] = {{1.f, 1.f}, {1.f, 1.f}}, vsc[2][2] = {{1.f, 1.f}, {1.f, 1.f}};
                 if constexpr (FP8) {
-                    const float *sk = reinterpret_cast<const float *>(ring_ptr + s * C::kStageBytes + kg * T::kSlot +
-                                                                      2 * T::kTile);
-                    const float *sv = sk + T::kScaleTile / 4;
+                    const uint8_t *st = ring_ptr + s * C::kStageBytes;
+                    const float *sk = reinterpret_cast<const float *>(st + C::kKsOff + kg * T::kScaleTile);
+                    const float *sv = reinterpret_cast<const float *>(st + C::kVsOff + kg * T::kScaleTile);
+                    const int hs = kh & (kScaleHeads - 1);
 #pragma unroll
                     for (int n = 0; n < 2; n++) {
                         const int kr = n * 8 + 2 * (lane & 3);
-                        ksc[n][0] = sk[kr * p.hkv + kh];
-                        ksc[n][1] = sk[(kr + 1) * p.hkv + kh];
-                        vsc[n][0] = sv[kr * p.hkv + kh];
-                        vsc[n][1] = sv[(kr + 1) * p.hkv + kh];
+                        ksc[n][0] = sk[kr * kScaleHeads + hs];
+                        ksc[n][1] = sk[(kr + 1) * kScaleHeads + hs];
+                        vsc[n][0] = sv[kr * kScaleHeads + hs];
+                        vsc[n][1] = sv[(kr + 1) * kScaleHeads + hs];
                     }
                 }
                 // scale into the exp2 domain, causal and range mask
@@ -1274,6 +1297,22 @@ cudaError_t make_pool_tmap(CUtensorMap *map, const void *pool, int64_t num_slots
     return make_pool_tmap_e(map, pool, num_slots, hkv, d, box_cols, swizzle128, 2);
 }
 
+// Tensor map of an FP8 pool's scales [slots][Hkv] fp32 with a box of 16
+// slots x kScaleHeads heads (16-byte rows; Hkv a multiple of kScaleHeads).
+static cudaError_t make_scale_tmap(CUtensorMap *map, const float *scales, int64_t num_slots, int hkv)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {(cuuint64_t)hkv, (cuuint64_t)num_slots};
+    cuuint64_t strides[1] = {(cuuint64_t)hkv * 4};
+    cuuint32_t box[2] = {(cuuint32_t)kScaleHeads, 16};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(scales), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return res == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // Tensor map of q [tokens][Hq][D] with a box of one KV head's g query heads
 // x 128/g tokens x 64 columns (128 rows of the MMA tile), 128-byte swizzle.
 cudaError_t make_q_tmap(CUtensorMap *map, const void *q, int num_tokens, int hq, int d, int g)
@@ -1292,7 +1331,8 @@ cudaError_t make_q_tmap(CUtensorMap *map, const void *q, int num_tokens, int hq,
 
 template <int D, int KG, int NB, bool FP8, int CW = kConsumerWarps, bool KM = false>
 static cudaError_t launch_mma_dk(const AttnParams &p, const WorkList &wl, int num_items, const CUtensorMap &km,
-                                 const CUtensorMap &vm, cudaStream_t stream)
+                                 const CUtensorMap &vm, const CUtensorMap &ksm, const CUtensorMap &vsm,
+                                 cudaStream_t stream)
 {
     constexpr int smem = MmaCfg<D, KG, NB, FP8, CW>::kSmemBytes;
     static std::once_flag once;
@@ -1306,14 +1346,15 @@ static cudaError_t launch_mma_dk(const AttnParams &p, const WorkList &wl, int nu
     dim3 grid(p.hkv, num_items);                                // KV heads adjacent: they share pool pages
     launch_begin(stream, wl.mode == kModeDecode ? kAttnMmaDecode : kAttnMmaPrefill);
     cudaError_t e = launch_maybe_pdl(attn_mma_kernel<D, KG, NB, FP8, CW, KM>, grid, dim3((CW + 1) * 32), smem, stream, p,
-                                     wl, km, vm);
+                                     wl, km, vm, ksm, vsm);
     launch_end(stream);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int D, bool FP8, bool KM>
 static cudaError_t launch_stream_d(const AttnParams &p, const WorkList &wl, int num_items, const CUtensorMap &km,
-                                   const CUtensorMap &vm, cudaStream_t stream)
+                                   const CUtensorMap &vm, const CUtensorMap &ksm, const CUtensorMap &vsm,
+                                   cudaStream_t stream)
 {
     constexpr int smem = StreamCfg<D, 4, FP8>::kSmemBytes;
     static std::once_flag once;
@@ -1327,7 +1368,7 @@ static cudaError_t launch_stream_d(const AttnParams &p, const WorkList &wl, int 
     dim3 grid(p.hkv, num_items);                                // KV heads adjacent: they share pool pages
     launch_begin(stream, kAttnMmaDecode);
     cudaError_t e = launch_maybe_pdl(attn_stream_kernel<D, 4, FP8, KM>, grid, dim3(kMmaThreads), smem, stream, p, wl, km,
-                                     vm);
+                                     vm, ksm, vsm);
     launch_end(stream);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -1340,20 +1381,21 @@ static cudaError_t launch_stream_d(const AttnParams &p, const WorkList &wl, int 
 // Prefill-class CTAs: 2 row tiles x 2 key groups, two blocks per iteration.
 template <int D, bool FP8>
 static cudaError_t launch_mma_d(const AttnParams &p, const WorkList &wl, int num_items, const CUtensorMap &km,
-                                const CUtensorMap &vm, cudaStream_t stream)
+                                const CUtensorMap &vm, const CUtensorMap &ksm, const CUtensorMap &vsm,
+                                cudaStream_t stream)
 {
     constexpr int NB = 2;                                       // blocks per warp iteration
-    if (wl.mode != kModeDecode) return launch_mma_dk<D, 2, NB, FP8>(p, wl, num_items, km, vm, stream);
+    if (wl.mode != kModeDecode) return launch_mma_dk<D, 2, NB, FP8>(p, wl, num_items, km, vm, ksm, vsm, stream);
     int max_t = 0;
     for (int i = 0; i < wl.n; i++) max_t = wl.qt[i] > max_t ? wl.qt[i] : max_t;
     const char *env = getenv("PKV_DECODE_ROW_TILES");
     const bool km_tiles = max_t * p.group <= kKeyMajorRows && !(env && *env && atoi(env) != 0);
     if (wl.split_tokens >= kLongSplit) {
-        return km_tiles ? launch_stream_d<D, FP8, true>(p, wl, num_items, km, vm, stream)
-                        : launch_stream_d<D, FP8, false>(p, wl, num_items, km, vm, stream);
+        return km_tiles ? launch_stream_d<D, FP8, true>(p, wl, num_items, km, vm, ksm, vsm, stream)
+                        : launch_stream_d<D, FP8, false>(p, wl, num_items, km, vm, ksm, vsm, stream);
     }
-    return km_tiles ? launch_mma_dk<D, 4, NB, FP8, kConsumerWarps, true>(p, wl, num_items, km, vm, stream)
-                    : launch_mma_dk<D, 4, NB, FP8>(p, wl, num_items, km, vm, stream);
+    return km_tiles ? launch_mma_dk<D, 4, NB, FP8, kConsumerWarps, true>(p, wl, num_items, km, vm, ksm, vsm, stream)
+                    : launch_mma_dk<D, 4, NB, FP8>(p, wl, num_items, km, vm, ksm, vsm, stream);
 }
 
 cudaError_t launch_attn_mma(const AttnParams &p, const WorkList &wl, int head_dim, int num_items,
@@ -1363,21 +1405,25 @@ cudaError_t launch_attn_mma(const AttnParams &p, const WorkList &wl, int head_di
     if (num_items <= 0) return cudaSuccess;
     CUtensorMap km, vm;
     if (k_scale) {                                              // FP8 pool: head_dim 128, 128-byte rows
-        if (head_dim != 128 || p.k_scale != k_scale || p.v_scale != v_scale) return cudaErrorInvalidValue;
+        if (head_dim != 128 || p.k_scale != k_scale || p.v_scale != v_scale || p.hkv % kScaleHeads != 0)
+            return cudaErrorInvalidValue;
+        CUtensorMap ksm, vsm;
         cudaError_t e = make_pool_tmap_e(&km, k_cache, num_slots, p.hkv, 128, 128, true, 1);
         if (e == cudaSuccess) e = make_pool_tmap_e(&vm, v_cache, num_slots, p.hkv, 128, 128, true, 1);
+        if (e == cudaSuccess) e = make_scale_tmap(&ksm, k_scale, num_slots, p.hkv);
+        if (e == cudaSuccess) e = make_scale_tmap(&vsm, v_scale, num_slots, p.hkv);
         if (e != cudaSuccess) return e;
-        return launch_mma_d<128, true>(p, wl, num_items, km, vm, stream);
+        return launch_mma_d<128, true>(p, wl, num_items, km, vm, ksm, vsm, stream);
     }
     const bool sw = head_dim != 48;
     const int box = sw ? 64 : head_dim;
     cudaError_t e = make_pool_tmap(&km, k_cache, num_slots, p.hkv, head_dim, box, sw);
     if (e == cudaSuccess) e = make_pool_tmap(&vm, v_cache, num_slots, p.hkv, head_dim, box, sw);
     if (e != cudaSuccess) return e;
-    switch (head_dim) {
-    case 48: return launch_mma_d<48, false>(p, wl, num_items, km, vm, stream);
-    case 64: return launch_mma_d<64, false>(p, wl, num_items, km, vm, stream);
-    case 128: return launch_mma_d<128, false>(p, wl, num_items, km, vm, stream);
+    switch (head_dim) {                                         // (no scale maps: the pool maps stand in)
+    case 48: return launch_mma_d<48, false>(p, wl, num_items, km, vm, km, vm, stream);
+    case 64: return launch_mma_d<64, false>(p, wl, num_items, km, vm, km, vm, stream);
+    case 128: return launch_mma_d<128, false>(p, wl, num_items, km, vm, km, vm, stream);
     default: return cudaErrorInvalidValue;
     }
 }

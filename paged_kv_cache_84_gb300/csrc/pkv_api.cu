@@ -363,9 +363,9 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
     if (g > kDecodeRows) return PKV_ERR_UNSUPPORTED;
     if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
         return PKV_ERR_UNSUPPORTED;
-    // quantized pools: head_dim 128 (128-byte code rows), the scale rows of a
-    // block staged whole (KV heads a multiple of 4, at most 16), warp-MMA kernels
-    if (fp8 && (d != 128 || hkv % 4 != 0 || hkv > 16 || !aligned(k_scale, 16) || !aligned(v_scale, 16) ||
+    // quantized pools: head_dim 128 (128-byte code rows), scales staged in
+    // boxes of 4 KV heads (KV heads a multiple of 4), warp-MMA kernels
+    if (fp8 && (d != 128 || hkv % 4 != 0 || !aligned(k_scale, 16) || !aligned(v_scale, 16) ||
                 env_int("PKV_ATTN_CUDA_CORE", 0)))
         return PKV_ERR_UNSUPPORTED;
 

@@ -73,6 +73,8 @@ FP8_CASES = [
     (2, 5, 1500, 130, 8, 8, 0),
     (3, 12, 400, 20, 64, 8, 2),
     (4, 4, 5000, 1, 32, 4, 0),
+    (5, 4, 900, 2, 32, 16, 0),
+    (6, 3, 2600, 1, 64, 32, 1),
 ]
 
 
