@@ -446,21 +446,44 @@ def time_workload(pkv, cfg, steps, warmup, device, peaks, dist=None, use_graph=T
     return spec, copies, res
 
 
-def e2e_workload(pkv, copies, steps, device):
-    """Same step through the C ABI from pinned host buffers: h2d of the step's
-    inputs, write + attention, d2h of the output, every step, all timed."""
+def e2e_workload(pkv, copies, steps, device, dist=None, world=1):
+    """Same step through the C ABI from pinned host memory: every step copies
+    that step's inputs (q, k, v and the batch metadata, packed in one pinned
+    buffer as a batch builder lays them out) to the device, runs the write and
+    the attention, and copies the output back to pinned host memory, all inside
+    the timed region.  Timed as one CUDA graph holding exactly `steps` such
+    steps over the rotated device copies (like the kernel-only timing), and
+    also as eager calls from Python (a diagnostic of the per-call host cost)."""
     c0 = copies[0]
-    host = {name: getattr(c0, name).cpu().pin_memory() for name in ("q", "k", "v", "qsl", "sl", "bt", "slots")}
-    dev = [{name: torch.empty_like(getattr(c, name)) for name in host} for c in copies]
+    names = ("q", "k", "v", "qsl", "sl", "bt", "slots")
+    offs, total = {}, 0
+    for name in names:
+        t = getattr(c0, name)
+        offs[name] = total
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    host = torch.empty(total, dtype=torch.uint8).pin_memory()
+
+    def views(buf):
+        out = {}
+        for name in names:
+            t = getattr(c0, name)
+            n = t.numel() * t.element_size()
+            out[name] = buf[offs[name]:offs[name] + n].view(t.dtype).view(t.shape)
+        return out
+
+    hv = views(host)
+    for name in names:
+        hv[name].copy_(getattr(c0, name).cpu())
+    devbufs = [torch.empty(total, dtype=torch.uint8, device=device) for _ in copies]
+    dev = [views(b) for b in devbufs]
     outs_h = torch.empty_like(c0.out, device="cpu").pin_memory()
     stream = torch.cuda.current_stream()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = sum(hv[name].numel() * hv[name].element_size() for name in names)
     d2h = outs_h.numel() * outs_h.element_size()
 
     def one(i):
-        c, d = copies[i % len(copies)], dev[i % len(dev)]
-        for name, t in host.items():
-            d[name].copy_(t, non_blocking=True)
+        c, b, d = copies[i % len(copies)], devbufs[i % len(devbufs)], dev[i % len(dev)]
+        b.copy_(host, non_blocking=True)
         c.run(q=d["q"], k=d["k"], v=d["v"], qsl=d["qsl"], sl=d["sl"], bt=d["bt"], slots=d["slots"])
         outs_h.copy_(c.out, non_blocking=True)
 
@@ -468,15 +491,50 @@ def e2e_workload(pkv, copies, steps, device):
         one(i)
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for i in range(steps):
-        one(i)
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    ms = ev0.elapsed_time(ev1) / steps
-    return {"value": c0.meta.num_tokens / (ms / 1e3), "unit": UNIT, "ms_per_step": ms,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "path": "pinned host -> device copies, pkv_paged_kv_write + pkv_ragged_paged_attention, device -> pinned host"}
+
+    def timed(fn, n):
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        fn()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        ms = ev0.elapsed_time(ev1) / n
+        if dist is not None:
+            t = torch.tensor([ms], dtype=torch.float64, device=device)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    eager_ms = timed(lambda: [one(i) for i in range(steps)], steps)
+    graph_ms, why = None, None
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            for i in range(steps):
+                one(i)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        graph_ms = timed(g.replay, steps)
+    except Exception as e:                                  # capture of host copies unsupported
+        why = str(e).splitlines()[0][:160] if str(e) else type(e).__name__
+        torch.cuda.synchronize()
+    ms = graph_ms if graph_ms is not None else eager_ms
+    res = {"value": c0.meta.num_tokens * world / (ms / 1e3), "unit": UNIT, "ms_per_step": ms,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "path": ("one CUDA graph of %d steps; each: one h2d copy of the packed pinned inputs, "
+                    "pkv_paged_kv_write + pkv_ragged_paged_attention, d2h copy of the output to pinned memory" % steps
+                    if graph_ms is not None else
+                    "eager Python calls per step: h2d copy of the packed pinned inputs, pkv_paged_kv_write + "
+                    "pkv_ragged_paged_attention, d2h copy of the output to pinned memory"),
+           "eager_ms_per_step": eager_ms}
+    if why is not None:
+        res["graph_unavailable"] = why
+    return res
 
 
 def fp8_workload(pkv, cfg, device, peaks, steps=20):
@@ -680,7 +738,7 @@ def run_ours(args):
     spec, copies, head = time_workload(pkv, args.workload, args.steps, warmup, device, peaks, dist,
                                        subset=args.subset)
     t0, t1 = head.pop("timed_wall")
-    e2e = e2e_workload(pkv, copies, max(3, min(args.steps, 200)), device)
+    e2e = e2e_workload(pkv, copies, max(3, min(args.steps, 200)), device, dist, world)
     del copies
     torch.cuda.empty_cache()
 
