@@ -265,10 +265,14 @@ __device__ __forceinline__ void load_qt_frags(uint32_t (&qb)[D / 16][2], const _
 // S^T for one 16-key block (accumulated into s; two chains over alternate
 // head-dim chunks).  FP8: K codes converted to fp16 (exact); the K scales
 // are applied by the caller.
-template <int D, bool FP8>
+// HP > 1 (FP8 pools): the slice holds the rows of HP adjacent KV heads
+// interleaved (row r of head hd at slice row r * HP + hd, as a TMA box of HP
+// heads lays them out); hd selects the head.
+template <int D, bool FP8, int HP = 1>
 __device__ __forceinline__ void block_scores_t(float (&s)[4], const uint32_t (&qb)[D / 16][2], uint32_t kt, int mi,
-                                               int mr)
+                                               int mr, int hd = 0)
 {
+    static_assert(HP == 1 || FP8, "interleaved heads: FP8 pools only");
     float s1[4] = {0.f, 0.f, 0.f, 0.f};
     if constexpr (!FP8) {
         // matrix mi: keys (mi & 1) * 8 .., dims of half mi >> 1 of the chunk
@@ -285,7 +289,7 @@ __device__ __forceinline__ void block_scores_t(float (&s)[4], const uint32_t (&q
 #pragma unroll
         for (int kk = 0; kk < D / 16; kk += 2) {
             uint32_t r0, r1, r2, r3, a[4], a2[4];
-            ldsm_x4(kt + tile_off<D, true>((mi & 1) * 8 + mr, kk + (mi >> 1)), r0, r1, r2, r3);
+            ldsm_x4(kt + tile_off<D, true>(((mi & 1) * 8 + mr) * HP + hd, kk + (mi >> 1)), r0, r1, r2, r3);
             e4m3x4_to_f16x2x2(r0, a[0], a[2]);
             e4m3x4_to_f16x2x2(r1, a[1], a[3]);
             e4m3x4_to_f16x2x2(r2, a2[0], a2[2]);
@@ -308,11 +312,12 @@ __device__ __forceinline__ int ot_dim(int mt, int r, int hi)
 }
 
 // O^T += V^T P^T for one 16-key block; pb0 / pb1 = P^T for keys 2c, 2c+1 /
-// 2c+8, 2c+9 of row r.
-template <int D, bool FP8>
+// 2c+8, 2c+9 of row r.  HP, hd: interleaved heads, as in block_scores_t.
+template <int D, bool FP8, int HP = 1>
 __device__ __forceinline__ void block_pv_t(float (&o)[D / 16][4], uint32_t pb0, uint32_t pb1, uint32_t vt, int mi,
-                                           int mr)
+                                           int mr, int hd = 0)
 {
+    static_assert(HP == 1 || FP8, "interleaved heads: FP8 pools only");
     if constexpr (!FP8) {
         // matrix mi: keys (mi >> 1) * 8 .., dims of half mi & 1 of tile mt;
         // transposed, a lane gets keys 2c, 2c+1 of one dim
@@ -329,7 +334,7 @@ __device__ __forceinline__ void block_pv_t(float (&o)[D / 16][4], uint32_t pb0, 
 #pragma unroll
         for (int q = 0; q < D / 16; q += 2) {
             uint32_t r0, r1, r2, r3, ev[4], od[4];
-            ldsm_x4_t(vt + tile_off<D, true>((mi >> 1) * 8 + mr, q + (mi & 1)), r0, r1, r2, r3);
+            ldsm_x4_t(vt + tile_off<D, true>(((mi >> 1) * 8 + mr) * HP + hd, q + (mi & 1)), r0, r1, r2, r3);
             e4m3x4_to_f16x2x2(prmt(r0, 0u, 0x3120u), ev[0], od[0]);
             e4m3x4_to_f16x2x2(prmt(r1, 0u, 0x3120u), ev[1], od[1]);
             e4m3x4_to_f16x2x2(prmt(r2, 0u, 0x3120u), ev[2], od[2]);
@@ -359,10 +364,10 @@ __device__ __forceinline__ void mask_scale_t(float (&s)[4], int key, int k_end, 
 // V^T P^T.  m, l: rows 2c, 2c+1 (l summed over this lane's keys only).  The
 // O^T rescale is skipped when no row of the warp raised its maximum.  FP8:
 // each key's V scale (vs: keys r, r+8) is folded into P, which is fp16.
-template <int D, bool FP8, int NB>
+template <int D, bool FP8, int NB, int HP = 1>
 __device__ __forceinline__ void softmax_pv_t(float (&o)[D / 16][4], float (&m)[2], float (&l)[2], float (&s)[NB][4],
                                              const float (&vs)[NB][2], const uint32_t (&vt)[NB], const bool (&has)[NB],
-                                             int mi, int mr)
+                                             int mi, int mr, int hd = 0)
 {
     float alpha[2];
 #pragma unroll
@@ -406,7 +411,7 @@ __device__ __forceinline__ void softmax_pv_t(float (&o)[D / 16][4], float (&m)[2
             lo = pack_bf16x2(s[q][0], s[q][1]);
             hi = pack_bf16x2(s[q][2], s[q][3]);
         }
-        block_pv_t<D, FP8>(o, movmatrix_t(lo), movmatrix_t(hi), vt[q], mi, mr);
+        block_pv_t<D, FP8, HP>(o, movmatrix_t(lo), movmatrix_t(hi), vt[q], mi, mr, hd);
     }
 }
 
@@ -503,13 +508,19 @@ __device__ __forceinline__ void stage_rows(const float (&o)[D / 8][4], const flo
 
 // The same for key-major tiles: lane 4r + c holds rows 2c, 2c+1 (of at
 // most kKeyMajorRows) and their weight sums over keys r, r+8 of each block,
-// which are summed across r here.
-template <int D, bool FP8, int CW>
+// which are summed across r here.  HP > 1: the warp serves KV head hd of a
+// CTA of HP adjacent heads, whose rows the epilogue sees as one group of
+// HP * g query heads: local row x (token x / g, query head x % g of head hd)
+// is staged as row (x / g) * HP * g + hd * g + x % g of warp slot `slot`;
+// only the nr_h real rows are staged.
+template <int D, bool FP8, int CW, int HP = 1>
 __device__ __forceinline__ void stage_rows_t(const float (&o)[D / 16][4], const float (&m)[2], float (&l)[2],
-                                             bool alive, float *mo, float *mml, uint32_t *s_flags)
+                                             bool alive, float *mo, float *mml, uint32_t *s_flags, int slot = -1,
+                                             int hd = 0, int g = 1, int nr_h = kKeyMajorRows)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = lane >> 2, c = lane & 3;
+    if (HP == 1) slot = warp;
 #pragma unroll
     for (int j = 0; j < 2; j++) {
         l[j] += __shfl_xor_sync(0xffffffffu, l[j], 4);
@@ -519,15 +530,18 @@ __device__ __forceinline__ void stage_rows_t(const float (&o)[D / 16][4], const 
     named_bar_sync(1, CW * 32);                                   // every consumer is done with the ring
 #pragma unroll
     for (int j = 0; j < 2; j++) {
-        float *row = mo + (warp * 16 + 2 * c + j) * D;
+        const int x = 2 * c + j;
+        if (HP > 1 && x >= nr_h) continue;
+        const int rc = HP == 1 ? x : (x / g) * (HP * g) + hd * g + x % g;
+        float *row = mo + (slot * 16 + rc) * D;
 #pragma unroll
         for (int mt = 0; mt < D / 16; mt++) {
             row[ot_dim<FP8>(mt, r, 0)] = o[mt][j];
             row[ot_dim<FP8>(mt, r, 1)] = o[mt][2 + j];
         }
         if (r == 0) {
-            mml[(warp * 16 + 2 * c + j) * 2] = m[j];
-            mml[(warp * 16 + 2 * c + j) * 2 + 1] = l[j];
+            mml[(slot * 16 + rc) * 2] = m[j];
+            mml[(slot * 16 + rc) * 2 + 1] = l[j];
         }
     }
     if (!alive && lane == 0) s_flags[0] = 1u;
@@ -952,15 +966,25 @@ __global__ void __launch_bounds__((CW + 1) * 32) attn_mma_kernel(AttnParams p, c
 // 256-request and the 32 x 32768 decode workloads this keeps more copies in
 // flight per SM than the one-block slot ring above, which wins on short,
 // latency-bound ranges instead.
-template <int D, int KG, bool FP8 = false>
+//
+// HP = 2 (FP8 pools, key-major tiles): a CTA serves two adjacent KV heads,
+// and one TMA box of {128 codes, 2 heads, 16 slots} (4 KB) carries a block's
+// K (or V) rows of both, so a block costs half the copy operations per
+// head: with 2 KB code slices the copies, not the bytes, bounded the
+// quantized decode.  Consumer warps 0..KG-1 serve the first head, KG..2KG-1
+// the second (KG = 2).
+template <int D, int KG, bool FP8 = false, int HP = 1>
 struct StreamCfg {
-    static constexpr int kRT = kConsumerWarps / KG;                          // row tiles
+    static_assert(HP == 1 || (FP8 && HP * KG == kConsumerWarps), "two heads per CTA: FP8, 2 key groups per head");
+    static constexpr int kRT = kConsumerWarps / KG;                          // row tiles (HP > 1: heads)
     using T = MmaTile<D, FP8>;
-    static constexpr int kStageBytes = KG * T::kData;
+    static constexpr int kTileH = HP * T::kTile;                             // K (or V) slices of HP heads
+    static constexpr int kBlockBytes = 2 * kTileH + 2 * T::kScaleTile;
+    static constexpr int kStageBytes = KG * kBlockBytes;
     static constexpr int kStages0 = kStageBudget / kStageBytes;
     static constexpr int kStages = kStages0 > 8 ? 8 : (kStages0 < 2 ? 2 : kStages0);
-    static constexpr int kVOff = KG * T::kTile;                              // offsets within a stage
-    static constexpr int kKsOff = 2 * KG * T::kTile;
+    static constexpr int kVOff = KG * kTileH;                                // offsets within a stage
+    static constexpr int kKsOff = 2 * KG * kTileH;
     static constexpr int kVsOff = kKsOff + KG * T::kScaleTile;
     static constexpr int kRingBytes = kStages * kStageBytes;
     static constexpr int kMergeBytes = kConsumerWarps * 16 * (D + 2) * 4;
@@ -968,7 +992,7 @@ struct StreamCfg {
     static constexpr int kSmemBytes = 1024 + kBodyBytes + 2 * kStages * 8;   // + alignment slack, barriers
 };
 
-template <int D, int KG, bool FP8, bool KM>
+template <int D, int KG, bool FP8, bool KM, int HP = 1>
 __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, const __grid_constant__ WorkList wl,
                                                                const __grid_constant__ CUtensorMap kmap,
                                                                const __grid_constant__ CUtensorMap vmap,
@@ -976,7 +1000,8 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
                                                                const __grid_constant__ CUtensorMap vsmap)
 {
     using T = MmaTile<D, FP8>;
-    using C = StreamCfg<D, KG, FP8>;
+    using C = StreamCfg<D, KG, FP8, HP>;
+    static_assert(HP == 1 || KM, "two heads per CTA: key-major tiles only");
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -987,19 +1012,24 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
     auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int kh = blockIdx.x;                                    // the KV heads of an item run side by side
+    // The KV heads of an item run side by side.  HP > 1: this CTA serves
+    // heads HP * kh .. HP * kh + HP - 1, and its rows are those of one group
+    // of HP * g query heads (the epilogue's view: group kh of size gg).
+    const int kh = blockIdx.x;
+    const int kh0 = kh * HP;                                      // first KV head of the CTA
     const int li = find_listed(wl, blockIdx.y);
     const int local = blockIdx.y - wl.item_off[li];
     const int r = wl.req[li];
     const int b = wl.qb[li], t = wl.qt[li], L = wl.len[li];
     const int g = p.group;
+    const int gg = HP * g;
 
     if (L == 0 || t == 0) {                                       // padding request: zero rows
         pdl_wait();                                               // keeps later programmatic waits transitive
         if (threadIdx.x == 0 && local == 0 && kh == 0) check_meta(p, wl, li);
-        for (int idx = threadIdx.x; idx < t * g * D; idx += kMmaThreads) {
+        for (int idx = threadIdx.x; idx < t * gg * D; idx += kMmaThreads) {
             const int rr = idx / D, e = idx - rr * D;
-            p.out[((size_t)(b + rr / g) * p.hq + kh * g + rr % g) * D + e] = __float2bfloat16(0.f);
+            p.out[((size_t)(b + rr / gg) * p.hq + kh * gg + rr % gg) * D + e] = __float2bfloat16(0.f);
         }
         return;
     }
@@ -1019,7 +1049,7 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
         k_begin = window_lo(L - t + i0, p.window) & ~15;
         k_end = L - t + i0 + ntok;                                // one past the tile's last position
     }
-    const int nr = ntok * g;                                      // rows of this CTA
+    const int nr = ntok * g;                                      // rows of this CTA per KV head
     const int blk0 = k_begin >> 4;
     const int nblk = ((k_end + 15) >> 4) - blk0;
     const int iters = (nblk + KG - 1) / KG;
@@ -1057,7 +1087,7 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
             if (!__all_sync(0xffffffffu, ok)) break;
             issued = it + 1;
             const int nv = min(KG, nblk - base);
-            if (lane == 0) mbar_arrive_expect_tx(full_bar(s), nv * T::kData);
+            if (lane == 0) mbar_arrive_expect_tx(full_bar(s), nv * C::kBlockBytes);
             for (int j = 0; j < nv; j++) {
                 int blk = __shfl_sync(0xffffffffu, ids, (base + j) & 31);
                 if (lane == 0) {
@@ -1066,13 +1096,14 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
                         blk = 0;
                     }
                     const uint32_t st = ring + s * C::kStageBytes;
-                    const uint32_t kd = st + j * T::kTile, vd = st + C::kVOff + j * T::kTile;
+                    const uint32_t kd = st + j * C::kTileH, vd = st + C::kVOff + j * C::kTileH;
+                    // HP > 1: the maps' boxes span HP heads (T::kBoxes is 1)
                     for (int x = 0; x < T::kBoxes; x++) {
-                        tma_load_3d(kd + x * T::kBoxBytes, &kmap, full_bar(s), x * T::kBoxCols, kh, blk * 16);
-                        tma_load_3d(vd + x * T::kBoxBytes, &vmap, full_bar(s), x * T::kBoxCols, kh, blk * 16);
+                        tma_load_3d(kd + x * T::kBoxBytes, &kmap, full_bar(s), x * T::kBoxCols, kh0, blk * 16);
+                        tma_load_3d(vd + x * T::kBoxBytes, &vmap, full_bar(s), x * T::kBoxCols, kh0, blk * 16);
                     }
                     if constexpr (FP8) {
-                        const int h4 = kh & ~(kScaleHeads - 1);
+                        const int h4 = kh0 & ~(kScaleHeads - 1);
                         tma_load_2d(st + C::kKsOff + j * T::kScaleTile, &ksmap, full_bar(s), h4, blk * 16);
                         tma_load_2d(st + C::kVsOff + j * T::kScaleTile, &vsmap, full_bar(s), h4, blk * 16);
                     }
@@ -1102,10 +1133,13 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
     float *mml = mo + kConsumerWarps * 16 * D;                    // [warp][16][2]
 
     if constexpr (KM) {
-        // key-major decode tiles (nr <= kKeyMajorRows, one row tile)
+        // key-major decode tiles (nr <= kKeyMajorRows, one row tile per KV
+        // head); HP > 1: warp group rt serves KV head kh0 + rt
+        const int hd = HP > 1 ? rt : 0;
+        const int khw = kh0 + hd;                                 // this warp's KV head
         const int rq = lane >> 2, c2 = 2 * (lane & 3);
         uint32_t qb[D / 16][2];
-        load_qt_frags<D, FP8>(qb, p.q, rq < nr ? (size_t)(b + i0 + rq / g) * p.hq + kh * g + rq % g : 0, rq < nr,
+        load_qt_frags<D, FP8>(qb, p.q, rq < nr ? (size_t)(b + i0 + rq / g) * p.hq + khw * g + rq % g : 0, rq < nr,
                               lane);
         const int qp0 = c2 < nr ? qbase + c2 / g : -1;
         const int qp1 = c2 + 1 < nr ? qbase + (c2 + 1) / g : -1;
@@ -1121,30 +1155,30 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
             }
             const int bl = it * KG + kg;
             if (bl < nblk) {
-                const uint32_t kt = ring + s * C::kStageBytes + kg * T::kTile;
+                const uint32_t kt = ring + s * C::kStageBytes + kg * C::kTileH;
                 float sc[1][4] = {{0.f, 0.f, 0.f, 0.f}}, vs[1][2] = {{1.f, 1.f}};
                 const uint32_t vt[1] = {kt + C::kVOff};
                 const bool has[1] = {true};
-                block_scores_t<D, FP8>(sc[0], qb, kt, mi, mr);
+                block_scores_t<D, FP8, HP>(sc[0], qb, kt, mi, mr, hd);
                 float f0 = sl2, f1 = sl2;
                 if constexpr (FP8) {                              // K and V scales of keys rq, rq + 8
                     const uint8_t *st = ring_ptr + s * C::kStageBytes;
                     const float *sk = reinterpret_cast<const float *>(st + C::kKsOff + kg * T::kScaleTile);
                     const float *sv = reinterpret_cast<const float *>(st + C::kVsOff + kg * T::kScaleTile);
-                    const int hs = kh & (kScaleHeads - 1);
+                    const int hs = khw & (kScaleHeads - 1);
                     f0 *= sk[rq * kScaleHeads + hs];
                     f1 *= sk[(rq + 8) * kScaleHeads + hs];
                     vs[0][0] = sv[rq * kScaleHeads + hs];
                     vs[0][1] = sv[(rq + 8) * kScaleHeads + hs];
                 }
                 mask_scale_t(sc[0], ((blk0 + bl) << 4) + rq, k_end, qp0, qp1, wspan, true, f0, f1);
-                softmax_pv_t<D, FP8, 1>(o, m, l, sc, vs, vt, has, mi, mr);
+                softmax_pv_t<D, FP8, 1, HP>(o, m, l, sc, vs, vt, has, mi, mr, hd);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty_bar(s));
         }
         pdl_launch_dependents();                                  // a combine kernel may start launching
-        stage_rows_t<D, FP8, kConsumerWarps>(o, m, l, alive, mo, mml, s_flags);
+        stage_rows_t<D, FP8, kConsumerWarps, HP>(o, m, l, alive, mo, mml, s_flags, kg, hd, g, nr);
     } else {
         const int row0 = rt * 16;
         const int rA = row0 + (lane >> 2), rB = rA + 8;           // the two rows this lane holds
@@ -1244,7 +1278,7 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
         }
         stage_rows<D, FP8, kConsumerWarps>(o, m, l, alive, mo, mml, s_flags);
     }
-    mma_epilogue<D, KG>(p, wl, li, kh, mo, mml, s_flags, nr, i0, split, partial, b, t, L, g);
+    mma_epilogue<D, KG>(p, wl, li, kh, mo, mml, s_flags, nr * HP, i0, split, partial, b, t, L, gg);
 }
 
 // ---------------------------------------------------------------- host side
@@ -1268,25 +1302,25 @@ static EncodeTiledFn encode_fn()
     return fn;
 }
 
-// Tensor map of one pool viewed as [slots][Hkv][D] with a box of one KV
-// head's 16 rows x box_cols columns; elements of elem_bytes (2: bf16, 1:
-// FP8 codes).
+// Tensor map of one pool viewed as [slots][Hkv][D] with a box of
+// box_heads adjacent KV heads' 16 rows x box_cols columns; elements of
+// elem_bytes (2: bf16, 1: FP8 codes).
 static cudaError_t make_pool_tmap_e(CUtensorMap *map, const void *pool, int64_t num_slots, int hkv, int d,
-                                   int box_cols, bool swizzle128, int elem_bytes)
+                                   int box_cols, bool swizzle128, int elem_bytes, int box_heads = 1)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return cudaErrorNotSupported;
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)hkv, (cuuint64_t)num_slots};
     cuuint64_t strides[2] = {(cuuint64_t)d * elem_bytes, (cuuint64_t)hkv * d * elem_bytes};
-    cuuint32_t box[3] = {(cuuint32_t)box_cols, 1, 16};
+    cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_heads, 16};
     cuuint32_t estr[3] = {1, 1, 1};
-    // a 128-byte code row (FP8, head_dim 128) is promoted to 128 bytes only:
-    // 256 would fetch the next head's row as well
+    // a single 128-byte code row (FP8, head_dim 128) is promoted to 128 bytes
+    // only: 256 would fetch the next head's row as well
+    const int64_t run = (int64_t)d * elem_bytes * box_heads;     // contiguous bytes per slot in a box
     CUresult res = fn(map, elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                       const_cast<void *>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                       swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                      (int64_t)d * elem_bytes >= 256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
-                                                     : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                      run >= 256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return res == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -1351,24 +1385,25 @@ static cudaError_t launch_mma_dk(const AttnParams &p, const WorkList &wl, int nu
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-template <int D, bool FP8, bool KM>
+template <int D, bool FP8, bool KM, int HP = 1>
 static cudaError_t launch_stream_d(const AttnParams &p, const WorkList &wl, int num_items, const CUtensorMap &km,
                                    const CUtensorMap &vm, const CUtensorMap &ksm, const CUtensorMap &vsm,
                                    cudaStream_t stream)
 {
-    constexpr int smem = StreamCfg<D, 4, FP8>::kSmemBytes;
+    constexpr int KG = kConsumerWarps / HP;
+    constexpr int smem = StreamCfg<D, KG, FP8, HP>::kSmemBytes;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(attn_stream_kernel<D, 4, FP8, KM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        smem);
+        attr_err = cudaFuncSetAttribute(attn_stream_kernel<D, KG, FP8, KM, HP>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     });
     if (attr_err != cudaSuccess) return attr_err;
-    if (num_items > 65535) return cudaErrorInvalidConfiguration;
-    dim3 grid(p.hkv, num_items);                                // KV heads adjacent: they share pool pages
+    if (num_items > 65535 || p.hkv % HP != 0) return cudaErrorInvalidConfiguration;
+    dim3 grid(p.hkv / HP, num_items);                           // KV heads adjacent: they share pool pages
     launch_begin(stream, kAttnMmaDecode);
-    cudaError_t e = launch_maybe_pdl(attn_stream_kernel<D, 4, FP8, KM>, grid, dim3(kMmaThreads), smem, stream, p, wl, km,
-                                     vm, ksm, vsm);
+    cudaError_t e = launch_maybe_pdl(attn_stream_kernel<D, KG, FP8, KM, HP>, grid, dim3(kMmaThreads), smem, stream, p,
+                                     wl, km, vm, ksm, vsm);
     launch_end(stream);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -1378,11 +1413,13 @@ static cudaError_t launch_stream_d(const AttnParams &p, const WorkList &wl, int 
 // iteration when ranges are short and latency dominates; key-major tiles
 // when every listed request has at most kKeyMajorRows rows per KV head
 // (PKV_DECODE_ROW_TILES=1 keeps the 16-row tiles, for comparison).
+// Quantized pools stream key-major tiles two KV heads per CTA, with the
+// maps km2 / vm2 whose boxes span two heads.
 // Prefill-class CTAs: 2 row tiles x 2 key groups, two blocks per iteration.
 template <int D, bool FP8>
 static cudaError_t launch_mma_d(const AttnParams &p, const WorkList &wl, int num_items, const CUtensorMap &km,
                                 const CUtensorMap &vm, const CUtensorMap &ksm, const CUtensorMap &vsm,
-                                cudaStream_t stream)
+                                const CUtensorMap &km2, const CUtensorMap &vm2, cudaStream_t stream)
 {
     constexpr int NB = 2;                                       // blocks per warp iteration
     if (wl.mode != kModeDecode) return launch_mma_dk<D, 2, NB, FP8>(p, wl, num_items, km, vm, ksm, vsm, stream);
@@ -1391,6 +1428,9 @@ static cudaError_t launch_mma_d(const AttnParams &p, const WorkList &wl, int num
     const char *env = getenv("PKV_DECODE_ROW_TILES");
     const bool km_tiles = max_t * p.group <= kKeyMajorRows && !(env && *env && atoi(env) != 0);
     if (wl.split_tokens >= kLongSplit) {
+        if constexpr (FP8) {
+            if (km_tiles) return launch_stream_d<D, FP8, true, 2>(p, wl, num_items, km2, vm2, ksm, vsm, stream);
+        }
         return km_tiles ? launch_stream_d<D, FP8, true>(p, wl, num_items, km, vm, ksm, vsm, stream)
                         : launch_stream_d<D, FP8, false>(p, wl, num_items, km, vm, ksm, vsm, stream);
     }
@@ -1407,13 +1447,15 @@ cudaError_t launch_attn_mma(const AttnParams &p, const WorkList &wl, int head_di
     if (k_scale) {                                              // FP8 pool: head_dim 128, 128-byte rows
         if (head_dim != 128 || p.k_scale != k_scale || p.v_scale != v_scale || p.hkv % kScaleHeads != 0)
             return cudaErrorInvalidValue;
-        CUtensorMap ksm, vsm;
+        CUtensorMap ksm, vsm, km2, vm2;
         cudaError_t e = make_pool_tmap_e(&km, k_cache, num_slots, p.hkv, 128, 128, true, 1);
         if (e == cudaSuccess) e = make_pool_tmap_e(&vm, v_cache, num_slots, p.hkv, 128, 128, true, 1);
+        if (e == cudaSuccess) e = make_pool_tmap_e(&km2, k_cache, num_slots, p.hkv, 128, 128, true, 1, 2);
+        if (e == cudaSuccess) e = make_pool_tmap_e(&vm2, v_cache, num_slots, p.hkv, 128, 128, true, 1, 2);
         if (e == cudaSuccess) e = make_scale_tmap(&ksm, k_scale, num_slots, p.hkv);
         if (e == cudaSuccess) e = make_scale_tmap(&vsm, v_scale, num_slots, p.hkv);
         if (e != cudaSuccess) return e;
-        return launch_mma_d<128, true>(p, wl, num_items, km, vm, ksm, vsm, stream);
+        return launch_mma_d<128, true>(p, wl, num_items, km, vm, ksm, vsm, km2, vm2, stream);
     }
     const bool sw = head_dim != 48;
     const int box = sw ? 64 : head_dim;
@@ -1421,9 +1463,9 @@ cudaError_t launch_attn_mma(const AttnParams &p, const WorkList &wl, int head_di
     if (e == cudaSuccess) e = make_pool_tmap(&vm, v_cache, num_slots, p.hkv, head_dim, box, sw);
     if (e != cudaSuccess) return e;
     switch (head_dim) {                                         // (no scale maps: the pool maps stand in)
-    case 48: return launch_mma_d<48, false>(p, wl, num_items, km, vm, km, vm, stream);
-    case 64: return launch_mma_d<64, false>(p, wl, num_items, km, vm, km, vm, stream);
-    case 128: return launch_mma_d<128, false>(p, wl, num_items, km, vm, km, vm, stream);
+    case 48: return launch_mma_d<48, false>(p, wl, num_items, km, vm, km, vm, km, vm, stream);
+    case 64: return launch_mma_d<64, false>(p, wl, num_items, km, vm, km, vm, km, vm, stream);
+    case 128: return launch_mma_d<128, false>(p, wl, num_items, km, vm, km, vm, km, vm, stream);
     default: return cudaErrorInvalidValue;
     }
 }

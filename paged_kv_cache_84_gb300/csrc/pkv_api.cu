@@ -398,7 +398,9 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
     const bool use_fma = env_int("PKV_ATTN_CUDA_CORE", 0) != 0;    // CUDA-core kernels instead of the staged MMA ones
     if (split <= 0) {
         int64_t target_ctas = (int64_t)sms * (use_fma ? 8 : 16);
-        int64_t s = (dec_keys * hkv + target_ctas - 1) / (target_ctas > 0 ? target_ctas : 1);
+        // quantized pools stream two KV heads per CTA: half the CTAs per split
+        const int64_t head_ctas = fp8 ? hkv / 2 : hkv;
+        int64_t s = (dec_keys * head_ctas + target_ctas - 1) / (target_ctas > 0 ? target_ctas : 1);
         if (s < kMinSplit) s = kMinSplit;
         split = (int)((s + 127) / 128 * 128);
     }

@@ -114,6 +114,42 @@ def test_fp8_split_paths_and_window(split, window, row_tiles, monkeypatch):
     assert_close(got, want, f"fp8 split {split} window {window}")
 
 
+HEAD_PAIR_CASES = [
+    # hq, hkv, (computed, new) per request: every request has t * g <= 8 rows
+    # per KV head, so the streaming kernel runs key-major tiles two KV heads
+    # per CTA; ragged tails, a padding request, t > 1 rows per head
+    (8, 8, [(2500, 8), (1033, 3), (4000, 1), (0, 0)]),
+    (32, 16, [(3001, 4), (1700, 1), (2222, 2)]),
+    (16, 4, [(2900, 2), (1111, 1), (0, 0), (3500, 2)]),
+    (64, 8, [(5000, 1), (1800, 1)]),
+]
+
+
+@pytest.mark.parametrize("window", [0, 700])
+@pytest.mark.parametrize("case", HEAD_PAIR_CASES, ids=[f"hq{c[0]}-hkv{c[1]}" for c in HEAD_PAIR_CASES])
+def test_fp8_streaming_head_pairs(case, window, monkeypatch):
+    """Quantized pools on the streaming kernel (splits of 1024 keys): key-major
+    tiles with two KV heads per CTA, every group size the kernel stages."""
+    monkeypatch.setenv("PKV_SPLIT_TOKENS", "1024")
+    hq, hkv, plan = case
+    reqs, nxt = [], 0
+    for computed, new in plan:
+        if new == 0:
+            reqs.append(Req(0, 1, [], pad=True))
+            continue
+        nb = (computed + new + 15) // 16
+        reqs.append(Req(computed, new, list(range(nxt, nxt + nb))))
+        nxt += nb
+    spec = Spec("fp8-head-pairs", reqs, hq, hkv, 128, 16, nxt + 5, 1 / math.sqrt(128), 80 + hq)
+    b = make_batch(spec, device="cpu")
+    pools = _quantized_pools(b, 81)
+    got, _, err, ws = _run(b, pools, window=window)
+    want, _ = _oracle(b, pools, window=window)
+    assert pkv.read_device_error(err) == 0
+    assert pkv.read_device_error(ws) == 0
+    assert_close(got, want, f"fp8 head pairs hq {hq} hkv {hkv} window {window}")
+
+
 def test_fp8_long_decodes_sampled():
     """The 32 x 32768 decode shape (4 requests), the streaming kernel."""
     spec = subset_spec(config_spec(5), 4)
