@@ -41,7 +41,7 @@ constexpr int kMmaThreads = (kConsumerWarps + 1) * 32;
 // head_dim 128 (64 KB): measured faster than three (96 KB) on both decode
 // workloads, 653 vs 679 us and 631 vs 651 us.
 constexpr int kStageBudget = 64 * 1024;
-constexpr int kLongSplit = 512;              // decode splits of at least this many keys use the streaming kernel
+constexpr int kLongSplit = kLongSplitTokens; // decode splits of at least this many keys use the streaming kernel
 
 // Quantized pools: FP8 E4M3 K/V (one byte per element) with an fp32 scale
 // per (slot, KV head).  A block's scales are staged with it as one 2-D TMA
@@ -86,7 +86,8 @@ struct MmaCfg {
     static constexpr int kSlots = kSlotsWanted < kSlotsMax ? kSlotsWanted : kSlotsMax;
     static_assert(kSlots >= KG * NB + KG, "the ring must hold an iteration of every key group plus one block each");
     static constexpr int kRingBytes = kSlots * MmaTile<D, FP8>::kSlot;
-    static constexpr int kMergeBytes = CW * 16 * (D + 2) * 4;
+    // epilogue: per-warp rows, then (cluster combine) the CTA's merged rows
+    static constexpr int kMergeBytes = CW * 16 * (D + 2) * 4 + 16 * (D + 2) * 4;
     static constexpr int kBodyBytes = kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes;
     static constexpr int kSmemBytes = 1024 + kBodyBytes + 2 * kSlots * 8;   // + alignment slack, barriers
 };
@@ -555,10 +556,14 @@ __device__ __forceinline__ void stage_rows_t(const float (&o)[D / 16][4], const 
 // the last one combines them and returns the counter to zero for the next
 // call.  A CTA whose pipeline wait gave up writes nothing but still counts,
 // so counters stay consistent.
+// xo non-null (cluster combine): the merged rows stay in this CTA's shared
+// memory, unnormalised, at xo[row][D] with (m, l) at xml[row], for the
+// cluster's rank 0 to combine.
 template <int D, int KG, int CW = kConsumerWarps>
 __device__ __forceinline__ void mma_epilogue(const AttnParams &p, const WorkList &wl, int li, int kh, float *mo,
                                              float *mml, uint32_t *s_flags, int nr, int i0, int split, bool partial,
-                                             int b, int t, int L, int g)
+                                             int b, int t, int L, int g, float *xo = nullptr,
+                                             float2 *xml = nullptr)
 {
     constexpr int kThreads = CW * 32;
     named_bar_sync(1, kThreads);
@@ -587,7 +592,12 @@ __device__ __forceinline__ void mma_epilogue(const AttnParams &p, const WorkList
             acc[6] = fmaf(w, x1.z, acc[6]); acc[7] = fmaf(w, x1.w, acc[7]);
         }
         const int i = i0 + rowc / g, h = kh * g + rowc % g;
-        if (!partial) {
+        if (xo) {
+            float4 *dst = reinterpret_cast<float4 *>(xo + rowc * D + e0);
+            dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+            if (e0 == 0) xml[rowc] = make_float2(M, ls);
+        } else if (!partial) {
             const float inv = ls > 0.f ? 1.f / ls : 0.f;
             uint4 v;
             v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
@@ -622,7 +632,60 @@ __device__ __forceinline__ void mma_epilogue(const AttnParams &p, const WorkList
     if (threadIdx.x == 0) atomicExch(cnt, 0u);                    // ready for the next call
 }
 
-template <int D, int KG, int NB, bool FP8, int CW, bool KM>
+// Split combine of a cluster of CS CTAs (the CS splits of one request and KV
+// head), after every CTA left its merged rows in xo / xml (mma_epilogue) and
+// its wait status in s_flags[0].  Run by every thread of every CTA of the
+// cluster (`combiner`: the consumer threads of rank 0), so that each passes
+// both cluster barriers: the first publishes every CTA's rows, the second
+// keeps each CTA's shared memory alive until rank 0 has read it.  Rank 0
+// merges o = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c, M = max_c m_c,
+// reading the peers' rows through distributed shared memory, and writes the
+// output rows unless some CTA's pipeline wait gave up.
+template <int D>
+__device__ __forceinline__ void cluster_combine(const AttnParams &p, bool combiner, int CS, const float *xo,
+                                                const float2 *xml, const uint32_t *s_flags, int nr, int i0, int b,
+                                                int kh, int g, int tid, int nthreads)
+{
+    __syncwarp();
+    cluster_sync_all();
+    if (combiner) {
+        bool ok = true;
+        for (int c = 0; c < CS; c++) ok = ok && ld_cluster_u32(cluster_map(smem_u32(s_flags), c)) == 0u;
+        constexpr int kChunks = D / 8;
+        const uint32_t xo_s = smem_u32(xo), xml_s = smem_u32(xml);
+        for (int idx = tid; ok && idx < nr * kChunks; idx += nthreads) {
+            const int rowc = idx / kChunks, e0 = (idx - rowc * kChunks) * 8;
+            float M = -INFINITY, ls = 0.f;
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int c = 0; c < CS; c++) {
+                const float2 ml = ld_cluster_f2(cluster_map(xml_s + rowc * 8, c));
+                const uint32_t xa = cluster_map(xo_s + (rowc * D + e0) * 4, c);
+                const float4 x0 = ld_cluster_f4(xa), x1 = ld_cluster_f4(xa + 16);
+                const float Mn = fmaxf(M, ml.x);
+                const float Ms = Mn == -INFINITY ? 0.f : Mn;
+                const float a = exp2f(M - Ms), w = exp2f(ml.x - Ms);   // 2^-inf = 0
+                ls = fmaf(ls, a, w * ml.y);
+                acc[0] = fmaf(acc[0], a, w * x0.x); acc[1] = fmaf(acc[1], a, w * x0.y);
+                acc[2] = fmaf(acc[2], a, w * x0.z); acc[3] = fmaf(acc[3], a, w * x0.w);
+                acc[4] = fmaf(acc[4], a, w * x1.x); acc[5] = fmaf(acc[5], a, w * x1.y);
+                acc[6] = fmaf(acc[6], a, w * x1.z); acc[7] = fmaf(acc[7], a, w * x1.w);
+                M = Mn;
+            }
+            const float inv = ls > 0.f ? 1.f / ls : 0.f;
+            uint4 v;
+            v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+            v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+            v.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+            v.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+            const int i = i0 + rowc / g, h = kh * g + rowc % g;
+            *reinterpret_cast<uint4 *>(p.out + ((size_t)(b + i) * p.hq + h) * D + e0) = v;
+        }
+    }
+    __syncwarp();
+    cluster_sync_all();
+}
+
+template <int D, int KG, int NB, bool FP8, int CW, bool KM, bool CL = false>
 __global__ void __launch_bounds__((CW + 1) * 32) attn_mma_kernel(AttnParams p, const __grid_constant__ WorkList wl,
                                                                const __grid_constant__ CUtensorMap kmap,
                                                                const __grid_constant__ CUtensorMap vmap,
@@ -631,6 +694,7 @@ __global__ void __launch_bounds__((CW + 1) * 32) attn_mma_kernel(AttnParams p, c
 {
     using T = MmaTile<D, FP8>;
     using C = MmaCfg<D, KG, NB, FP8, CW>;
+    static_assert(!CL || KG * C::kRT == CW, "cluster combine: one CTA-wide merge");
     constexpr int R = C::kSlots;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -663,7 +727,16 @@ __global__ void __launch_bounds__((CW + 1) * 32) attn_mma_kernel(AttnParams p, c
 
     int i0, ntok, k_begin, k_end, split = 0;
     bool partial = false;
-    if (wl.mode == kModeDecode) {
+    if (CL) {
+        // cluster combine (decode-class): the request's wl.cluster splits are
+        // this cluster's CTAs, rank = local, split_len[li] keys each (trailing
+        // splits may be empty); no global partials
+        i0 = 0;
+        ntok = t;
+        split = local;
+        k_begin = decode_key_begin(t, L, p.window) + split * wl.split_len[li];
+        k_end = min(L, k_begin + wl.split_len[li]);
+    } else if (wl.mode == kModeDecode) {
         i0 = 0;
         ntok = t;
         split = local;
@@ -754,6 +827,12 @@ __global__ void __launch_bounds__((CW + 1) * 32) attn_mma_kernel(AttnParams p, c
             for (int i = issued > R ? issued - R : 0; i < issued; i++) mbar_wait(full_bar(i % R), (i / R) & 1, p.err);
         }
         if (lane == 0 && local == 0 && kh == 0) check_meta(p, wl, li);
+        if constexpr (CL) {
+            // the producer passes the cluster barriers too (every thread does)
+            float *xo = reinterpret_cast<float *>(ring_ptr) + CW * 16 * (D + 2);
+            cluster_combine<D>(p, false, wl.cluster, xo, reinterpret_cast<float2 *>(xo + 16 * D), s_flags, 0, 0, b,
+                               kh, g, 0, 1);
+        }
         return;
     }
 
@@ -952,7 +1031,15 @@ __global__ void __launch_bounds__((CW + 1) * 32) attn_mma_kernel(AttnParams p, c
         }
         stage_rows<D, FP8, CW>(o, m, l, alive, mo, mml, s_flags);
     }
-    mma_epilogue<D, KG, CW>(p, wl, li, kh, mo, mml, s_flags, nr, i0, split, partial, b, t, L, g);
+    if constexpr (CL) {
+        float *xo = mml + CW * 16 * 2;                           // after the per-warp rows: [16][D], then (m, l)
+        float2 *xml = reinterpret_cast<float2 *>(xo + 16 * D);
+        mma_epilogue<D, KG, CW>(p, wl, li, kh, mo, mml, s_flags, nr, i0, split, false, b, t, L, g, xo, xml);
+        named_bar_sync(1, CW * 32);                               // every merged row of the CTA is in xo
+        cluster_combine<D>(p, local == 0, wl.cluster, xo, xml, s_flags, nr, i0, b, kh, g, threadIdx.x, CW * 32);
+    } else {
+        mma_epilogue<D, KG, CW>(p, wl, li, kh, mo, mml, s_flags, nr, i0, split, partial, b, t, L, g);
+    }
 }
 
 // ---------------------------------------------------------------- streaming decode
@@ -1363,7 +1450,7 @@ cudaError_t make_q_tmap(CUtensorMap *map, const void *q, int num_tokens, int hq,
     return res == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D, int KG, int NB, bool FP8, int CW = kConsumerWarps, bool KM = false>
+template <int D, int KG, int NB, bool FP8, int CW = kConsumerWarps, bool KM = false, bool CL = false>
 static cudaError_t launch_mma_dk(const AttnParams &p, const WorkList &wl, int num_items, const CUtensorMap &km,
                                  const CUtensorMap &vm, const CUtensorMap &ksm, const CUtensorMap &vsm,
                                  cudaStream_t stream)
@@ -1372,15 +1459,19 @@ static cudaError_t launch_mma_dk(const AttnParams &p, const WorkList &wl, int nu
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(attn_mma_kernel<D, KG, NB, FP8, CW, KM>,
+        attr_err = cudaFuncSetAttribute(attn_mma_kernel<D, KG, NB, FP8, CW, KM, CL>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     });
     if (attr_err != cudaSuccess) return attr_err;
     if (num_items > 65535) return cudaErrorInvalidConfiguration;
+    if (CL && (wl.cluster < 2 || wl.cluster > kMaxClusterSplits || num_items % wl.cluster != 0))
+        return cudaErrorInvalidConfiguration;
     dim3 grid(p.hkv, num_items);                                // KV heads adjacent: they share pool pages
     launch_begin(stream, wl.mode == kModeDecode ? kAttnMmaDecode : kAttnMmaPrefill);
-    cudaError_t e = launch_maybe_pdl(attn_mma_kernel<D, KG, NB, FP8, CW, KM>, grid, dim3((CW + 1) * 32), smem, stream, p,
-                                     wl, km, vm, ksm, vsm);
+    cudaError_t e = CL ? launch_cluster_maybe_pdl(attn_mma_kernel<D, KG, NB, FP8, CW, KM, CL>, grid, dim3((CW + 1) * 32),
+                                                  smem, stream, (unsigned)wl.cluster, p, wl, km, vm, ksm, vsm)
+                       : launch_maybe_pdl(attn_mma_kernel<D, KG, NB, FP8, CW, KM, CL>, grid, dim3((CW + 1) * 32),
+                                          smem, stream, p, wl, km, vm, ksm, vsm);
     launch_end(stream);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -1427,12 +1518,18 @@ static cudaError_t launch_mma_d(const AttnParams &p, const WorkList &wl, int num
     for (int i = 0; i < wl.n; i++) max_t = wl.qt[i] > max_t ? wl.qt[i] : max_t;
     const char *env = getenv("PKV_DECODE_ROW_TILES");
     const bool km_tiles = max_t * p.group <= kKeyMajorRows && !(env && *env && atoi(env) != 0);
-    if (wl.split_tokens >= kLongSplit) {
+    if (wl.split_tokens >= kLongSplit && wl.cluster == 0) {
         if constexpr (FP8) {
             if (km_tiles) return launch_stream_d<D, FP8, true, 2>(p, wl, num_items, km2, vm2, ksm, vsm, stream);
         }
         return km_tiles ? launch_stream_d<D, FP8, true>(p, wl, num_items, km, vm, ksm, vsm, stream)
                         : launch_stream_d<D, FP8, false>(p, wl, num_items, km, vm, ksm, vsm, stream);
+    }
+    if (wl.cluster > 0) {
+        return km_tiles
+                   ? launch_mma_dk<D, 4, NB, FP8, kConsumerWarps, true, true>(p, wl, num_items, km, vm, ksm, vsm, stream)
+                   : launch_mma_dk<D, 4, NB, FP8, kConsumerWarps, false, true>(p, wl, num_items, km, vm, ksm, vsm,
+                                                                               stream);
     }
     return km_tiles ? launch_mma_dk<D, 4, NB, FP8, kConsumerWarps, true>(p, wl, num_items, km, vm, ksm, vsm, stream)
                     : launch_mma_dk<D, 4, NB, FP8>(p, wl, num_items, km, vm, ksm, vsm, stream);

@@ -32,7 +32,16 @@ struct WorkList {
     int32_t qt[kPlanMax];         // query_start_loc[req + 1] - query_start_loc[req]
     int32_t len[kPlanMax];        // seq_lens[req]
     int32_t cnt_off[kPlanMax];    // decode: first split counter of a request combined in-kernel, else -1
+    int32_t cluster;              // decode: 0, or the split count of every request when each request's
+                                  // splits run as one thread-block cluster (combined through its shared memory)
+    int32_t split_len[kPlanMax];  // cluster mode: keys per split of each request (a multiple of the block size)
 };
+
+// Largest cluster of a decode request's splits (the portable cluster size).
+constexpr int kMaxClusterSplits = 8;
+// Decode splits of at least this many keys stream their blocks (streaming
+// kernel); shorter ones use the slot-ring kernel.
+constexpr int kLongSplitTokens = 512;
 
 constexpr int kModeDecode = 0;
 constexpr int kModePrefill = 1;
@@ -216,6 +225,28 @@ cudaError_t launch_maybe_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// The same with clusters of cluster_y CTAs along y.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_cluster_maybe_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                     cudaStream_t stream, unsigned cluster_y, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = cluster_y;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 

@@ -600,6 +600,15 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
         }
         return cudaSuccess;
     };
+    // Short split decodes (the slot-ring kernel) run each request's splits as
+    // one thread-block cluster that combines them through its shared memory:
+    // every request of the launch gets the launch's largest split count, its
+    // keys divided evenly.  Measured on the 48-request engine step, clusters
+    // of more than two CTAs do not run beside the prefill kernel (the step
+    // took the sum of both kernels' times), so next to prefill work the
+    // cluster holds at most two splits.  PKV_CLUSTER=0 turns clusters off,
+    // n >= 2 forces n.
+    const int cluster_env = env_int("PKV_CLUSTER", -1);
     for (size_t c0 = 0; c0 < dec.size(); c0 += kPlanMax) {
         WorkList wl;
         memset(&wl, 0, sizeof wl);
@@ -608,6 +617,30 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
         wl.tile_tokens = 0;
         int items = 0, rows = 1;
         size_t c1 = c0 + kPlanMax < dec.size() ? c0 + kPlanMax : dec.size();
+        int s_max = 1;
+        for (size_t x = c0; x < c1; x++) s_max = std::max(s_max, dec_splits_of(dec[x], split));
+        const int cs = cluster_env >= 2 ? std::min(cluster_env, kMaxClusterSplits) : (fork ? std::min(s_max, 2) : s_max);
+        if (!use_fma && split < kLongSplitTokens && cluster_env != 0 && cs >= 2 && cs <= kMaxClusterSplits) {
+            wl.cluster = cs;
+            for (size_t x = c0; x < c1; x++) {
+                const int32_t r = dec[x], t = qsl_h[r + 1] - qsl_h[r];
+                const int li = list_request(wl, r);
+                const int32_t keys = sl_h[r] - decode_key_begin(t, sl_h[r], window);
+                const int32_t per = (keys + cs - 1) / cs;
+                wl.split_len[li] = std::max(bs, (per + bs - 1) / bs * bs);
+                wl.item_off[li] = items;
+                wl.part_off[li] = -1;
+                items += cs;
+                if (sl_h[r] > 0 && t * g > rows) rows = t * g;
+            }
+            wl.item_off[wl.n] = items;
+            cudaError_t e = launch_attn_mma(p, wl, d, items, k_cache, v_cache, num_slots, dstream, k_scale, v_scale);
+            if (e != cudaSuccess) {
+                join();
+                return cuda_fail(e, "decode attention launch");
+            }
+            continue;
+        }
         for (size_t x = c0; x < c1; x++) {
             int32_t r = dec[x];
             int32_t t = qsl_h[r + 1] - qsl_h[r];

@@ -97,11 +97,16 @@ def test_fp8_write_bit_exact_and_attention_parity(case):
 
 
 @pytest.mark.parametrize("row_tiles", ["0", "1"], ids=["key-major", "row-tiles"])
-@pytest.mark.parametrize("split", ["128", "1024"])
+@pytest.mark.parametrize("split", ["128", "1024", "cluster"])
 @pytest.mark.parametrize("window", [0, 300])
 def test_fp8_split_paths_and_window(split, window, row_tiles, monkeypatch):
-    """Decode splits on the slot-ring (128) and the streaming kernel (1024),
-    in key-major and in 16-row tiles, with and without a sliding window."""
+    """Decode splits on the slot-ring (128, split counters; "cluster": four
+    splits per request combined in a thread-block cluster) and the streaming
+    kernel (1024), in key-major and in 16-row tiles, with and without a
+    sliding window."""
+    if split == "cluster":
+        monkeypatch.setenv("PKV_CLUSTER", "4")
+        split = "256"
     monkeypatch.setenv("PKV_SPLIT_TOKENS", split)
     monkeypatch.setenv("PKV_DECODE_ROW_TILES", row_tiles)
     reqs = [Req(3000, 1, list(range(0, 188))), Req(700, 40, list(range(188, 235))),

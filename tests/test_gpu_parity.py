@@ -490,8 +490,10 @@ def test_in_kernel_split_combine_repeats_and_leaves_counters_zero(split, d, monk
 
 def test_workspace_without_counter_room_uses_the_combine_kernel(monkeypatch):
     """A workspace too small for the counter region still splits (partials
-    after the error word) and combines with the separate kernel."""
+    after the error word) and combines with the separate kernel (clusters
+    off: they would combine without partials)."""
     monkeypatch.setenv("PKV_SPLIT_TOKENS", "256")
+    monkeypatch.setenv("PKV_CLUSTER", "0")
     # one decode at L = 1500: 8 partial rows of 264 bytes per split, so the
     # 12 KiB workspace holds 5 splits (of 512 keys: 3 splits)
     spec = Spec("ws", [Req(1499, 1, list(range(94)))], 8, 2, 64, 16, 100, 0.125, 32)
@@ -506,8 +508,10 @@ def test_workspace_without_counter_room_uses_the_combine_kernel(monkeypatch):
 
 
 def test_nonzero_split_counter_is_flagged(monkeypatch):
-    """A workspace whose counter region was not zero-filled is reported."""
+    """A workspace whose counter region was not zero-filled is reported
+    (split counters: clusters off)."""
     monkeypatch.setenv("PKV_SPLIT_TOKENS", "256")
+    monkeypatch.setenv("PKV_CLUSTER", "0")
     spec = random_spec(33, 4, 2000, 1, 8, 2, 64, decode_frac=1.0)
     b = make_batch(spec, device="cpu")
     dev = DeviceStep(b)
@@ -653,3 +657,67 @@ def test_decode_tile_forms(d, hq, hkv, split, row_tiles, monkeypatch):
         dev.step()
         assert_close(dev.out, oracle_full(ref, window=window), f"decode tiles d{d} split {split} window {window}")
         assert pkv.read_device_error(dev.ws) == 0
+
+
+CLUSTER_LENS = (17, 40, 300, 700, 1000, 1999, 33)
+
+
+@pytest.mark.parametrize("window", [0, 500])
+@pytest.mark.parametrize("cs", [2, 3, 8])
+@pytest.mark.parametrize("d,hq,hkv,row_tiles", [(48, 8, 4, 0), (128, 32, 8, 0), (64, 16, 4, 1), (128, 64, 8, 1)],
+                         ids=["d48g2", "d128g4", "d64g4-rows", "d128g8-rows"])
+def test_cluster_split_combine(d, hq, hkv, row_tiles, cs, window, monkeypatch):
+    """Short split decodes whose splits run as one thread-block cluster and
+    combine through distributed shared memory: cs CTAs per request and KV
+    head, keys divided evenly (short requests leave empty trailing splits),
+    key-major and 16-row tiles, t = 1 and 2, a padding request; two eager calls
+    and two CUDA-graph replays give the same result."""
+    monkeypatch.setenv("PKV_SPLIT_TOKENS", "256")
+    monkeypatch.setenv("PKV_CLUSTER", str(cs))
+    monkeypatch.setenv("PKV_DECODE_ROW_TILES", str(row_tiles))
+    g = hq // hkv
+    reqs, blk = [], 0
+    for i, L in enumerate(CLUSTER_LENS):
+        t = 2 if (i % 2 == 1 and 2 * g <= 16) else 1
+        nb = (L + 15) // 16
+        reqs.append(Req(L - t, t, list(range(blk, blk + nb))))
+        blk += nb
+    reqs.insert(3, Req(0, 1, [], pad=True))
+    spec = Spec("cluster", reqs, hq, hkv, d, 16, blk + 2, 1 / math.sqrt(d), 84)
+    b = make_batch(spec, device="cpu")
+    ref = cpu_copy(b)
+    oracle_write(ref)
+    want = oracle_full(ref, window=window)
+    dev = DeviceStep(b, window=window)
+    dev.write()
+    for i in range(2):
+        dev.out.fill_(float("nan"))
+        dev.attend()
+        assert_close(dev.out, want, f"cluster {cs} d{d} window {window} call {i}")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=s):
+        dev.attend()
+    torch.cuda.synchronize()
+    for i in range(2):
+        dev.out.fill_(float("nan"))
+        gr.replay()
+        torch.cuda.synchronize()
+        assert_close(dev.out, want, f"cluster {cs} d{d} window {window} replay {i}")
+    assert pkv.read_device_error(dev.ws) == 0
+
+
+@pytest.mark.parametrize("cluster", ["0", "-1"], ids=["counters", "cluster"])
+def test_engine_step_split_combine_both_ways(cluster, monkeypatch):
+    """The 48-request engine step with its short decode splits combined by
+    the split counters (PKV_CLUSTER=0) and by clusters (the default)."""
+    monkeypatch.setenv("PKV_CLUSTER", cluster)
+    b = make_batch(config_spec(2), device="cpu")
+    ref = cpu_copy(b)
+    oracle_write(ref)
+    dev = DeviceStep(b)
+    dev.step()
+    _check_write(dev, ref)
+    assert_close(dev.out, oracle_full(ref), f"engine step cluster={cluster}")
+    assert pkv.read_device_error(dev.ws) == 0
