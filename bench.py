@@ -504,10 +504,12 @@ def e2e_workload(pkv, copies, steps, device, dist=None, world=1):
     d2h = outs_h.numel() * outs_h.element_size()
 
     def one(i):
+        # the library's copy kernel moves the packed inputs in and the output
+        # out (pinned host memory addressed by the kernel)
         c, b, d = copies[i % len(copies)], devbufs[i % len(devbufs)], dev[i % len(dev)]
-        b.copy_(host, non_blocking=True)
+        pkv.copy_async(b, host)
         c.run(q=d["q"], k=d["k"], v=d["v"], qsl=d["qsl"], sl=d["sl"], bt=d["bt"], slots=d["slots"])
-        outs_h.copy_(c.out, non_blocking=True)
+        pkv.copy_async(outs_h, c.out)
 
     for i in range(3):
         one(i)
@@ -547,11 +549,11 @@ def e2e_workload(pkv, copies, steps, device, dist=None, world=1):
     ms = graph_ms if graph_ms is not None else eager_ms
     res = {"value": c0.meta.num_tokens * world / (ms / 1e3), "unit": UNIT, "ms_per_step": ms,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "path": ("one CUDA graph of %d steps; each: one h2d copy of the packed pinned inputs, "
-                    "pkv_paged_kv_write + pkv_ragged_paged_attention, d2h copy of the output to pinned memory" % steps
-                    if graph_ms is not None else
-                    "eager Python calls per step: h2d copy of the packed pinned inputs, pkv_paged_kv_write + "
-                    "pkv_ragged_paged_attention, d2h copy of the output to pinned memory"),
+           "path": ("one CUDA graph of %d steps; each: pkv_copy_async of the packed pinned inputs to the device, "
+                    "pkv_paged_kv_write + pkv_ragged_paged_attention, pkv_copy_async of the output to pinned "
+                    "memory" % steps if graph_ms is not None else
+                    "eager Python calls per step: pkv_copy_async of the packed pinned inputs to the device, "
+                    "pkv_paged_kv_write + pkv_ragged_paged_attention, pkv_copy_async of the output to pinned memory"),
            "eager_ms_per_step": eager_ms}
     if why is not None:
         res["graph_unavailable"] = why

@@ -361,6 +361,25 @@ pkv_status pkv_scatter_blocks(void *const *pools, int32_t num_pools, const int32
                               int32_t num_blocks_total, size_t block_bytes, const void *in, uint32_t *device_error,
                               cudaStream_t stream);
 
+/* ---------------------------------------------------------------- staging copies
+ *
+ * "31. Engine v2", "Flattened ragged batches": the batch builder lays out
+ * each step's metadata on the host and the device reads it.  This copies
+ * `bytes` bytes from src to dst with a kernel on `stream`: either side may
+ * be device memory or pinned host memory the device can address (then the
+ * kernel reads or writes host memory directly), so staging a step's packed
+ * inputs and reading back its output add kernels to the stream, not
+ * copy-engine operations between the attention launches.
+ *
+ * Requirements: bytes % 16 == 0 and both pointers 16-byte aligned (else
+ * PKV_ERR_UNSUPPORTED); non-null pointers for bytes > 0 and ranges that do
+ * not overlap (else PKV_ERR_INVALID_ARG).  Zero bytes is a no-op.  A bit
+ * copy; the kernel waits for the kernel before it on `stream` before it
+ * reads src (programmatic launch), and the next kernel waits for it.
+ * Nothing is allocated and nothing synchronises.
+ */
+pkv_status pkv_copy_async(void *dst, const void *src, size_t bytes, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

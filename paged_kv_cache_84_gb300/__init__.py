@@ -17,7 +17,7 @@ __all__ = [
     "PkvError", "load", "paged_kv_write", "ragged_paged_attention", "attention_workspace_bytes",
     "make_workspace", "read_device_error", "clear_device_error", "launch_count", "LIB_PATH",
     "DEVERR_SLOT", "DEVERR_BLOCK", "DEVERR_TIMEOUT", "DEVERR_META", "DEVERR_COUNTER", "WORKSPACE_MIN_BYTES", "profile_start", "profile_stop",
-    "plan_request_kernels", "CLASS_NAMES", "paged_kv_write_fp8", "ragged_paged_attention_fp8", "copy_blocks", "gather_blocks", "scatter_blocks", "MAX_POOLS",
+    "plan_request_kernels", "CLASS_NAMES", "paged_kv_write_fp8", "ragged_paged_attention_fp8", "copy_blocks", "gather_blocks", "scatter_blocks", "MAX_POOLS", "copy_async",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpkv.so")
@@ -92,6 +92,8 @@ def load():
     L.pkv_gather_blocks.argtypes = [_c_p, _c_i32, _c_p, _c_i32, _c_i32, _c_sz, _c_p, _c_p, _c_p]
     L.pkv_scatter_blocks.restype = ctypes.c_int
     L.pkv_scatter_blocks.argtypes = [_c_p, _c_i32, _c_p, _c_i32, _c_i32, _c_sz, _c_p, _c_p, _c_p]
+    L.pkv_copy_async.restype = ctypes.c_int
+    L.pkv_copy_async.argtypes = [_c_p, _c_p, _c_sz, _c_p]
     _lib = L
     return L
 
@@ -286,6 +288,15 @@ def scatter_blocks(pools, blocks, inp, device_error=None, stream=None):
     _check(load().pkv_scatter_blocks(arr, n_pools, _dev(blocks, "blocks", torch.int32), n, nbt, bb,
                                      _buf(inp, "inp"), _err(device_error), _stream(stream)), "scatter_blocks")
 
+
+
+def copy_async(dst, src, stream=None):
+    """dst := src (same byte size) with a copy kernel; either may be a CUDA
+    tensor or pinned host memory the device can address."""
+    n = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != n:
+        raise ValueError("dst and src differ in byte size")
+    _check(load().pkv_copy_async(_buf(dst, "dst"), _buf(src, "src"), n, _stream(stream)), "copy_async")
 
 
 def paged_kv_write_fp8(k, v, k_codes, v_codes, k_scale, v_scale, slot_mapping, device_error=None, stream=None):

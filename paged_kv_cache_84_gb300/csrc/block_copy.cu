@@ -96,4 +96,39 @@ cudaError_t launch_block_copy(int mode, void *const *pools, int32_t num_pools, c
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+// A plain copy of `chunks` 16-byte vectors (pkv_copy_async): staging a
+// step's packed inputs from pinned host memory, or reading its output back.
+// Either side may be pinned host memory the device addresses directly, so
+// the copy is a kernel like the attention launches around it (no copy-engine
+// operation in the stream).  Four independent vectors per thread and
+// iteration keep enough bytes in flight over the host link.
+__global__ void __launch_bounds__(256) byte_copy_kernel(uint4 *dst, const uint4 *src, int64_t chunks)
+{
+    pdl_wait();                                                   // the source may come from the kernel before
+    pdl_launch_dependents();
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t c0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c0 < chunks; c0 += 4 * stride) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; u++)
+            if (c0 + u * stride < chunks) v[u] = src[c0 + u * stride];
+#pragma unroll
+        for (int u = 0; u < 4; u++)
+            if (c0 + u * stride < chunks) dst[c0 + u * stride] = v[u];
+    }
+}
+
+cudaError_t launch_byte_copy(void *dst, const void *src, size_t bytes, cudaStream_t stream)
+{
+    const int64_t chunks = (int64_t)(bytes / 16);
+    if (chunks <= 0) return cudaSuccess;
+    int64_t blocks = (chunks + 4 * 256 - 1) / (4 * 256);
+    if (blocks > 152 * 16) blocks = 152 * 16;                     // grid-stride beyond 16 CTAs per SM
+    launch_begin(stream, kByteCopy);
+    cudaError_t e = launch_maybe_pdl(byte_copy_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
+                                     static_cast<uint4 *>(dst), static_cast<const uint4 *>(src), chunks);
+    launch_end(stream);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 }  // namespace pkv

@@ -183,6 +183,7 @@ constexpr int kMaxPools = 256;
 cudaError_t launch_block_copy(int mode, void *const *pools, int32_t num_pools, const int32_t *src,
                               const int32_t *dst, int32_t n, int32_t nb_total, int64_t block_bytes, void *buf,
                               uint32_t *err, cudaStream_t stream);
+cudaError_t launch_byte_copy(void *dst, const void *src, size_t bytes, cudaStream_t stream);
 
 // Merge split-KV partials of the split requests in `wl` into bf16 output.
 cudaError_t launch_attn_combine(const AttnParams &p, const WorkList &wl, int head_dim,
@@ -198,7 +199,8 @@ enum KernelId : int {
     kAttnMmaDecode = 5,
     kAttnMmaPrefill = 6,
     kBlockCopy = 7,
-    kNumKernelIds = 8
+    kByteCopy = 8,
+    kNumKernelIds = 9
 };
 
 // Call around every kernel launch: counts it and, while profiling is on,

@@ -191,6 +191,7 @@ const char *pkv_kernel_name(int32_t kernel_id)
     case kAttnMmaDecode: return "attn_mma_decode";
     case kAttnMmaPrefill: return "attn_mma_prefill";
     case kBlockCopy: return "block_copy";
+    case kByteCopy: return "byte_copy";
     }
     return "unknown";
 }
@@ -770,6 +771,17 @@ static pkv_status block_copy_common(int mode, void *const *pools, int32_t num_po
     cudaError_t e = launch_block_copy(mode, pools, num_pools, src, dst, n, num_blocks_total, (int64_t)block_bytes,
                                       buf, device_error, stream);
     return e == cudaSuccess ? PKV_OK : cuda_fail(e, "block copy launch");
+}
+
+pkv_status pkv_copy_async(void *dst, const void *src, size_t bytes, cudaStream_t stream)
+{
+    if (bytes == 0) return PKV_OK;
+    if (!dst || !src) return PKV_ERR_INVALID_ARG;
+    if (bytes % 16 != 0 || !aligned(dst, 16) || !aligned(src, 16)) return PKV_ERR_UNSUPPORTED;
+    const uintptr_t d = (uintptr_t)dst, s = (uintptr_t)src;
+    if (d < s + bytes && s < d + bytes) return PKV_ERR_INVALID_ARG;   // overlapping ranges
+    cudaError_t e = launch_byte_copy(dst, src, bytes, stream);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "byte copy launch");
 }
 
 pkv_status pkv_copy_blocks(void *const *pools, int32_t num_pools, const int32_t *src_blocks,

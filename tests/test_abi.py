@@ -127,3 +127,18 @@ def test_block_copy_validation_on_host(lib):
     assert lib.pkv_scatter_blocks(fake, 2, ids, 4, 10, ctypes.c_size_t(512), P((1 << 22) + 8), None, None) == 2
     odd = (P * 2)(1 << 20, (1 << 21) + 4)
     assert lib.pkv_copy_blocks(odd, 2, ids, ids, 4, 10, ctypes.c_size_t(512), None, None) == 2
+
+
+def test_copy_async_validation_on_host(lib):
+    """pkv_copy_async rejects what it cannot copy before touching the device."""
+    lib.pkv_copy_async.restype = ctypes.c_int
+    lib.pkv_copy_async.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    a, b = 1 << 20, 1 << 24                                 # never dereferenced: validation fails first
+    assert lib.pkv_copy_async(a, b, 0, None) == 0          # zero bytes: no-op
+    assert lib.pkv_copy_async(None, b, 64, None) == 1
+    assert lib.pkv_copy_async(a, None, 64, None) == 1
+    assert lib.pkv_copy_async(a, a + 32, 64, None) == 1     # overlapping ranges
+    assert lib.pkv_copy_async(a, b, 24, None) == 2          # not a multiple of 16 bytes
+    assert lib.pkv_copy_async(a + 8, b, 64, None) == 2      # unaligned
+    assert lib.pkv_copy_async(a, b + 8, 64, None) == 2
+

@@ -90,3 +90,41 @@ def test_block_copy_in_a_cuda_graph():
     oracle.copy_blocks(host, src.cpu(), dst.cpu())
     for h, dv in zip(host, dev):
         assert torch.equal(_bits(dv.cpu()), _bits(h))
+
+
+@pytest.mark.parametrize("nbytes", [16, 4096, (1 << 20) + 48, 7 << 20])
+def test_copy_async_host_device_round_trip(nbytes):
+    """pkv_copy_async: pinned host -> device, device -> device, device ->
+    pinned host, bit for bit, inside one stream and in a CUDA graph."""
+    g = torch.Generator().manual_seed(nbytes % 1000)
+    src = torch.randint(0, 256, (nbytes,), generator=g, dtype=torch.uint8).pin_memory()
+    d1 = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    d2 = torch.empty_like(d1)
+    back = torch.zeros(nbytes, dtype=torch.uint8).pin_memory()
+    pkv.copy_async(d1, src)
+    pkv.copy_async(d2, d1)
+    pkv.copy_async(back, d2)
+    torch.cuda.synchronize()
+    assert torch.equal(d1.cpu(), src) and torch.equal(back, src)
+    back.zero_()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=s):
+        pkv.copy_async(d2, src)
+        pkv.copy_async(back, d2)
+    gr.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(back, src)
+
+
+def test_copy_async_rejects_unaligned_and_odd_sizes():
+    d = torch.empty(4096, dtype=torch.uint8, device="cuda")
+    h = torch.empty(4096, dtype=torch.uint8).pin_memory()
+    with pytest.raises(pkv.PkvError):
+        pkv.copy_async(d[8:8 + 64], h[:64])                  # unaligned device side
+    with pytest.raises(pkv.PkvError):
+        pkv.copy_async(d[:24], h[:24])                       # not a multiple of 16 bytes
+    pkv.copy_async(d[:0], h[:0])                             # zero bytes: no-op
+    torch.cuda.synchronize()
+
