@@ -54,6 +54,24 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x: float, dist=None, device=None) -> float:
+    """The largest of every rank's x (the job's time is its slowest rank's).
+    dist: torch.distributed (or None for one process); NCCL reduces a CUDA
+    tensor on `device`, gloo a CPU one."""
+    if dist is None:
+        return float(x)
+    dev = device if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(tokens_per_step: int, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank processes its own copy of the step's
+    tokens (weak scaling, replicas), timed by the slowest rank."""
+    return tokens_per_step * world / (ms_per_step / 1e3)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -396,11 +414,7 @@ def time_workload(pkv, cfg, steps, warmup, device, peaks, dist=None, use_graph=T
     t_wall1 = time.time()
     if dist is not None:
         dist.barrier()
-    elapsed_ms = ev0.elapsed_time(ev1)
-    if dist is not None:
-        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), dist, device)
     ms_per_step = elapsed_ms / steps
 
     per_replay_ms = None
@@ -524,12 +538,7 @@ def e2e_workload(pkv, copies, steps, device, dist=None, world=1):
         fn()
         ev1.record(stream)
         torch.cuda.synchronize()
-        ms = ev0.elapsed_time(ev1) / n
-        if dist is not None:
-            t = torch.tensor([ms], dtype=torch.float64, device=device)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms
+        return max_over_ranks(ev0.elapsed_time(ev1) / n, dist, device)
 
     eager_ms = timed(lambda: [one(i) for i in range(steps)], steps)
     graph_ms, why = None, None
@@ -547,7 +556,7 @@ def e2e_workload(pkv, copies, steps, device, dist=None, world=1):
         why = str(e).splitlines()[0][:160] if str(e) else type(e).__name__
         torch.cuda.synchronize()
     ms = graph_ms if graph_ms is not None else eager_ms
-    res = {"value": c0.meta.num_tokens * world / (ms / 1e3), "unit": UNIT, "ms_per_step": ms,
+    res = {"value": job_value(c0.meta.num_tokens, world, ms), "unit": UNIT, "ms_per_step": ms,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "path": ("one CUDA graph of %d steps; each: pkv_copy_async of the packed pinned inputs to the device, "
                     "pkv_paged_kv_write + pkv_ragged_paged_attention, pkv_copy_async of the output to pinned "
@@ -752,7 +761,10 @@ def run_ours(args):
     device = torch.device("cuda", local)
     import paged_kv_cache_84_gb300 as pkv
     from paged_kv_cache_84_gb300 import build as pkv_build
-    pkv_build.build()
+    if local == 0:
+        pkv_build.build()                                # one build per node, in-tree
+    if dist is not None:
+        dist.barrier()
     pkv.load()
     peaks = load_peaks()
     warmup = max(3, args.warmup)
@@ -789,7 +801,7 @@ def run_ours(args):
     cpu = cpu_baseline(args.workload) if world == 1 and not args.no_cpu_baseline else None
     tokens = head["algorithmic"]["tokens"]
     line = {
-        "metric": METRIC, "value": tokens * world / (head["ms_per_step"] / 1e3), "unit": UNIT,
+        "metric": METRIC, "value": job_value(tokens, world, head["ms_per_step"]), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": warmup, "ms_per_step": head["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 values, shapes of the pages' workloads)",
