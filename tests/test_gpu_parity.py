@@ -721,3 +721,32 @@ def test_engine_step_split_combine_both_ways(cluster, monkeypatch):
     _check_write(dev, ref)
     assert_close(dev.out, oracle_full(ref), f"engine step cluster={cluster}")
     assert pkv.read_device_error(dev.ws) == 0
+
+
+@pytest.mark.parametrize("cluster", ["-1", "0"], ids=["clusters", "counters"])
+def test_more_requests_than_one_launch_lists(cluster, monkeypatch):
+    """600 decode requests and 300 prefill chunks: every kernel class runs
+    several launches of at most 256 listed requests, each launch with its own
+    plan (split counts, cluster size); short and long contexts mixed."""
+    monkeypatch.setenv("PKV_CLUSTER", cluster)
+    gen = torch.Generator().manual_seed(85)
+    reqs, blk = [], 0
+    for i in range(900):
+        if i % 3 == 2:                                   # prefill chunk of 2..40 tokens
+            t = int(torch.randint(2, 41, (1,), generator=gen))
+            c = int(torch.randint(0, 600, (1,), generator=gen))
+        else:                                            # decode over 1..1500 keys
+            t = 1
+            c = int(torch.randint(0, 1500, (1,), generator=gen))
+        nb = (c + t + 15) // 16
+        reqs.append(Req(c, t, list(range(blk, blk + nb))))
+        blk += nb
+    spec = Spec("many", reqs, 8, 2, 64, 16, blk + 4, 0.125, 86)
+    b = make_batch(spec, device="cpu")
+    ref = cpu_copy(b)
+    oracle_write(ref)
+    dev = DeviceStep(b)
+    dev.step()
+    _check_write(dev, ref)
+    assert_close(dev.out, oracle_full(ref), f"900 requests, cluster={cluster}")
+    assert pkv.read_device_error(dev.ws) == 0
