@@ -166,9 +166,10 @@ def accounting(spec, meta, classes):
     for r, cls in enumerate(classes):
         t = meta.query_start_loc[r + 1] - meta.query_start_loc[r]
         L = meta.seq_lens[r]
-        c = per_class.setdefault(cls, {"kv_bytes": 0, "q_out_bytes": 0, "flops": 0.0, "tokens": 0})
+        c = per_class.setdefault(cls, {"kv_bytes": 0, "q_out_bytes": 0, "flops": 0.0, "tokens": 0, "write_bytes": 0})
         c["q_out_bytes"] += 2 * t * hq * d * 2
         c["tokens"] += t
+        c["write_bytes"] += t * hkv * d * 2 * 2 * 2 + t * 8  # its new K/V rows read + written, slots
         if L == 0 or t == 0:
             continue
         c["flops"] += 4.0 * d * hq * (t * (L - t) + t * (t + 1) / 2)
@@ -203,15 +204,22 @@ KERNEL_BOUND = {"paged_kv_write": "hbm", "attn_fma_decode": "hbm", "attn_fma_pre
                 "attn_tc_prefill": "tensor", "attn_split_combine": "hbm"}
 
 
-def kernel_work(name, acc):
-    """(algorithmic bytes, FLOPs) of one step attributable to kernel `name`."""
+DECODE_CLASSES = ("decode", "padding")
+
+
+def kernel_work(name, acc, combined=True):
+    """(algorithmic bytes, FLOPs) of one step attributable to kernel `name`.
+    combined: the step is one pkv_paged_kv_write_attention call, whose decode
+    kernels write the decode-class rows and whose scatter writes the rest."""
     if name == "paged_kv_write":
-        return acc["write_bytes"], 0.0
+        if not combined:
+            return acc["write_bytes"], 0.0
+        return sum(c["write_bytes"] for cls, c in acc["per_class"].items() if cls not in DECODE_CLASSES), 0.0
     b = f = 0.0
     for cls in KERNEL_CLASS.get(name, ()):
         c = acc["per_class"].get(cls)
         if c:
-            b += c["kv_bytes"] + c["q_out_bytes"]
+            b += c["kv_bytes"] + c["q_out_bytes"] + (c["write_bytes"] if combined and cls in DECODE_CLASSES else 0)
             f += c["flops"]
     return b, f
 
@@ -322,12 +330,19 @@ class Step:
         return sum(t.numel() * t.element_size() for t in ts)
 
     def run(self, q=None, k=None, v=None, qsl=None, sl=None, bt=None, slots=None, out=None):
+        """The step: the write and the attention as one pkv_paged_kv_write_attention call."""
+        self.pkv.paged_kv_write_attention(
+            k if k is not None else self.k, v if v is not None else self.v, self.kc, self.vc,
+            slots if slots is not None else self.slots, out if out is not None else self.out,
+            q if q is not None else self.q, qsl if qsl is not None else self.qsl,
+            sl if sl is not None else self.sl, bt if bt is not None else self.bt,
+            self.qsl_h, self.sl_h, self.meta.max_query_len, self.meta.max_seq_len, self.spec.scale, self.ws)
+
+    def run_two_calls(self):
+        """The same step as pkv_paged_kv_write followed by pkv_ragged_paged_attention."""
         pkv = self.pkv
-        pkv.paged_kv_write(k if k is not None else self.k, v if v is not None else self.v, self.kc, self.vc,
-                           slots if slots is not None else self.slots)
-        pkv.ragged_paged_attention(out if out is not None else self.out, q if q is not None else self.q,
-                                   self.kc, self.vc, qsl if qsl is not None else self.qsl,
-                                   sl if sl is not None else self.sl, bt if bt is not None else self.bt,
+        pkv.paged_kv_write(self.k, self.v, self.kc, self.vc, self.slots)
+        pkv.ragged_paged_attention(self.out, self.q, self.kc, self.vc, self.qsl, self.sl, self.bt,
                                    self.qsl_h, self.sl_h, self.meta.max_query_len, self.meta.max_seq_len,
                                    self.spec.scale, self.ws)
 
@@ -417,6 +432,25 @@ def time_workload(pkv, cfg, steps, warmup, device, peaks, dist=None, use_graph=T
     elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), dist, device)
     ms_per_step = elapsed_ms / steps
 
+    # The same steps as two calls (pkv_paged_kv_write, then the attention),
+    # one graph of `steps` steps: the separate-call path, for comparison.
+    two_calls_ms = None
+    if use_graph:
+        side2 = torch.cuda.Stream()
+        side2.wait_stream(stream)
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g2, stream=side2):
+            for i in range(steps):
+                copies[i % len(copies)].run_two_calls()
+        torch.cuda.synchronize()
+        upload_graph(g2, stream)
+        ev0.record(stream)
+        g2.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        two_calls_ms = ev0.elapsed_time(ev1) / steps
+        del g2
+
     per_replay_ms = None
     if per_graphs:
         n = max(len(per_graphs), min(steps, 200))
@@ -473,10 +507,11 @@ def time_workload(pkv, cfg, steps, warmup, device, peaks, dist=None, use_graph=T
         "inputs_bytes_per_copy": copies[0].nbytes(),
         "l2": ("rotating %d copies of the inputs (%.0f MB > 2x L2)" % (len(copies), len(copies) * copies[0].nbytes() / 1e6)
                if len(copies) > 1 else "inputs larger than 2x L2"),
-        "launch": (("one CUDA graph of %d steps over the rotated copies" % steps) +
+        "launch": (("one CUDA graph of %d steps (pkv_paged_kv_write_attention each) over the rotated copies" % steps) +
                    (", uploaded to the device before the timed region" if uploaded else "")
                    if run_graph is not None else "eager"),
         "ms_per_step_one_graph_per_step": per_replay_ms,
+        "ms_per_step_two_calls": two_calls_ms,
         "kernels": kernels, "roofline": roof, "timed_wall": (t_wall0, t_wall1),
     }
     return spec, copies, res
@@ -559,10 +594,10 @@ def e2e_workload(pkv, copies, steps, device, dist=None, world=1):
     res = {"value": job_value(c0.meta.num_tokens, world, ms), "unit": UNIT, "ms_per_step": ms,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "path": ("one CUDA graph of %d steps; each: pkv_copy_async of the packed pinned inputs to the device, "
-                    "pkv_paged_kv_write + pkv_ragged_paged_attention, pkv_copy_async of the output to pinned "
+                    "pkv_paged_kv_write_attention, pkv_copy_async of the output to pinned "
                     "memory" % steps if graph_ms is not None else
                     "eager Python calls per step: pkv_copy_async of the packed pinned inputs to the device, "
-                    "pkv_paged_kv_write + pkv_ragged_paged_attention, pkv_copy_async of the output to pinned memory"),
+                    "pkv_paged_kv_write_attention, pkv_copy_async of the output to pinned memory"),
            "eager_ms_per_step": eager_ms}
     if why is not None:
         res["graph_unavailable"] = why
@@ -810,6 +845,8 @@ def run_ours(args):
                    "block_size": spec.block_size, "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                    "l2": head["l2"], "launch": head["launch"]},
         "step_us": head["step_us"],
+        "step_us_two_calls": (head["ms_per_step_two_calls"] * 1e3 if head["ms_per_step_two_calls"] is not None
+                              else None),
         "step_us_one_graph_per_step": (head["ms_per_step_one_graph_per_step"] * 1e3
                                        if head["ms_per_step_one_graph_per_step"] is not None else None),
         "kv_read_gbs": head["kv_read_gbs"],

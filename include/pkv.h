@@ -216,6 +216,45 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q,
                                       cudaStream_t stream);
 
 /*
+ * One step's write and attention in one call ("31. Engine v2", "Attention
+ * over the pool": every layer writes the step's K/V rows, then attends):
+ * the result is that of pkv_paged_kv_write(k, v, k_cache, v_cache,
+ * slot_mapping, ...) followed by pkv_ragged_paged_attention(...) with the
+ * same arguments, bf16 pools.  The work is arranged differently: the CTAs
+ * that attend for a decode-class request (t * g <= 16 rows per KV head)
+ * write that request's new rows themselves, each the rows in its key range,
+ * just before reading them, and a scatter restricted to the prefill-class
+ * requests' rows runs ahead of the prefill kernels; so decode attention
+ * does not wait for a scatter, and a batch of decodes is one launch.
+ *
+ *   k, v          device bf16 [num_tokens][num_kv_heads][head_dim], 16-byte
+ *                 aligned (the rows pkv_paged_kv_write takes)
+ *   slot_mapping  device int64 [num_tokens]: as for pkv_paged_kv_write; it
+ *                 must agree with the block table (token i of request r at
+ *                 position L - t + i goes to block_table[r][pos / 16] * 16 +
+ *                 pos % 16), as a batch builder makes it.  A decode-class row
+ *                 whose slot differs is still written to its slot_mapping
+ *                 slot but the attention reads the block table's slot, and
+ *                 PKV_DEVERR_META is set.
+ *   other arguments as pkv_ragged_paged_attention (k_cache, v_cache written).
+ * Device errors of the write (PKV_DEVERR_SLOT) go to the workspace's error
+ * word with the attention's.  Return codes as the two calls; nothing is
+ * enqueued when the arguments are rejected.  With PKV_ATTN_CUDA_CORE=1 (or
+ * PKV_SEPARATE_WRITE=1) the call runs the full scatter, then the attention.
+ */
+pkv_status pkv_paged_kv_write_attention(const void *k, const void *v, void *k_cache, void *v_cache,
+                                        const int64_t *slot_mapping, void *out, const void *q,
+                                        const int32_t *query_start_loc, const int32_t *seq_lens,
+                                        const int32_t *block_table, int32_t block_table_stride,
+                                        const int32_t *query_start_loc_host,
+                                        const int32_t *seq_lens_host, int32_t num_reqs,
+                                        int32_t num_tokens, int32_t max_query_len, int32_t max_seq_len,
+                                        int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                        int32_t block_size, int32_t num_blocks_total, float scale,
+                                        int32_t window, void *workspace, size_t workspace_bytes,
+                                        cudaStream_t stream);
+
+/*
  * ragged_paged_attention over a quantized pool (codes and scales as written
  * by pkv_paged_kv_write_fp8).  Arguments as pkv_ragged_paged_attention plus
  * the two scale pools (device fp32, 16-byte aligned).  Keys and values are

@@ -17,7 +17,7 @@ __all__ = [
     "PkvError", "load", "paged_kv_write", "ragged_paged_attention", "attention_workspace_bytes",
     "make_workspace", "read_device_error", "clear_device_error", "launch_count", "LIB_PATH",
     "DEVERR_SLOT", "DEVERR_BLOCK", "DEVERR_TIMEOUT", "DEVERR_META", "DEVERR_COUNTER", "WORKSPACE_MIN_BYTES", "profile_start", "profile_stop",
-    "plan_request_kernels", "CLASS_NAMES", "paged_kv_write_fp8", "ragged_paged_attention_fp8", "copy_blocks", "gather_blocks", "scatter_blocks", "MAX_POOLS", "copy_async",
+    "plan_request_kernels", "CLASS_NAMES", "paged_kv_write_fp8", "ragged_paged_attention_fp8", "copy_blocks", "gather_blocks", "scatter_blocks", "MAX_POOLS", "copy_async", "paged_kv_write_attention",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpkv.so")
@@ -94,6 +94,9 @@ def load():
     L.pkv_scatter_blocks.argtypes = [_c_p, _c_i32, _c_p, _c_i32, _c_i32, _c_sz, _c_p, _c_p, _c_p]
     L.pkv_copy_async.restype = ctypes.c_int
     L.pkv_copy_async.argtypes = [_c_p, _c_p, _c_sz, _c_p]
+    L.pkv_paged_kv_write_attention.restype = ctypes.c_int
+    L.pkv_paged_kv_write_attention.argtypes = [_c_p] * 10 + [_c_i32, _c_p, _c_p] + [_c_i32] * 9 + \
+        [_c_f, _c_i32, _c_p, _c_sz, _c_p]
     _lib = L
     return L
 
@@ -211,6 +214,37 @@ def ragged_paged_attention(out, q, k_cache, v_cache, query_start_loc, seq_lens, 
         hq, hkv, d, bs, nbt, float(scale), int(window), _dev(workspace, "workspace", torch.uint8), workspace.numel(),
         _stream(stream))
     _check(st, "ragged_paged_attention")
+
+
+def paged_kv_write_attention(k, v, k_cache, v_cache, slot_mapping, out, q, query_start_loc, seq_lens, block_table,
+                             query_start_loc_host, seq_lens_host, max_query_len, max_seq_len, scale, workspace,
+                             stream=None, window: int = 0):
+    """paged_kv_write followed by ragged_paged_attention, in one call (decode-class CTAs write their own
+    rows; a batch of decodes is one launch).  Write errors go to the workspace's error word."""
+    L = load()
+    n, hq, d = q.shape
+    nbt, bs, hkv, d2 = k_cache.shape
+    if out.shape != q.shape or d2 != d or v_cache.shape != k_cache.shape:
+        raise ValueError("shape mismatch")
+    if k.shape != (n, hkv, d) or v.shape != k.shape or slot_mapping.numel() != n:
+        raise ValueError("k, v must be [num_tokens, num_kv_heads, head_dim] with one slot per token")
+    qsl_h = _host_i32(query_start_loc_host, "query_start_loc_host")
+    sl_h = _host_i32(seq_lens_host, "seq_lens_host")
+    if qsl_h.numel() != sl_h.numel() + 1:
+        raise ValueError("query_start_loc needs num_reqs + 1 entries")
+    if block_table.dim() != 2:
+        raise ValueError("block_table must be [num_reqs, width]")
+    st = L.pkv_paged_kv_write_attention(
+        _dev(k, "k", torch.bfloat16), _dev(v, "v", torch.bfloat16),
+        _dev(k_cache, "k_cache", torch.bfloat16), _dev(v_cache, "v_cache", torch.bfloat16),
+        _dev(slot_mapping, "slot_mapping", torch.int64),
+        _dev(out, "out", torch.bfloat16), _dev(q, "q", torch.bfloat16),
+        _dev(query_start_loc, "query_start_loc", torch.int32), _dev(seq_lens, "seq_lens", torch.int32),
+        _dev(block_table, "block_table", torch.int32), block_table.shape[1],
+        _c_p(qsl_h.data_ptr()), _c_p(sl_h.data_ptr()), sl_h.numel(), n, int(max_query_len), int(max_seq_len),
+        hq, hkv, d, bs, nbt, float(scale), int(window), _dev(workspace, "workspace", torch.uint8), workspace.numel(),
+        _stream(stream))
+    _check(st, "paged_kv_write_attention")
 
 
 def clear_device_error(word: torch.Tensor, stream=None):

@@ -64,6 +64,23 @@ struct AttnParams {
     int32_t window;             // sliding window: keys above position - window (0: none)
     const float *k_scale;       // FP8 pools: [slots][hkv] scales of the K and V codes (else null)
     const float *v_scale;
+    // Combined write + attention (bf16 pools): decode-class CTAs write their
+    // own requests' new K/V rows (fw_k, fw_v: [N][hkv][D] as 16-byte vectors)
+    // into the pools (fw_kc, fw_vc) at fw_slots[row] before reading them.
+    // Null when the rows were written by a separate scatter.
+    const uint4 *fw_k;
+    const uint4 *fw_v;
+    uint4 *fw_kc;
+    uint4 *fw_vc;
+    const int64_t *fw_slots;
+};
+
+// Token ranges [begin, begin + len) of the rows a ranged scatter writes
+// (the prefill-class requests of a combined write + attention call).
+struct TokenRanges {
+    int32_t n;
+    int32_t begin[kPlanMax];
+    int32_t off[kPlanMax + 1];   // prefix sums of the lengths
 };
 
 // ---------------------------------------------------------------- sliding window
@@ -102,6 +119,55 @@ constexpr int kCounterStride = 8;        // uint32 words between two split count
 
 // Flags a listed request whose device metadata disagrees with the host copies
 // the launch was planned from (the kernels use the planned values).
+// Generic-proxy writes to global memory become visible to the async proxy
+// (TMA loads) issued after this fence.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Combined write + attention, decode-class CTA: copy the request's new rows
+// at positions [pos_lo, pos_hi) of KV head kh (the request's t tokens sit at
+// positions L - t .. L - 1, token row b + pos - (L - t)) into the pools at
+// fw_slots[row] (negative: the scratch slot), with the 32 lanes of the
+// calling warp, then fence them against the async proxy so that the TMA
+// loads this warp issues next see them.  A slot outside the pool is skipped
+// and reported (bit 1, as the scatter does); a slot other than the one the
+// block table gives for the position is reported (kDevErrMeta): the
+// attention reads the block table's slot.  pos_lo = pos_hi - t with L = 0:
+// a padding request, whose rows go to their slots without the table check.
+template <int D>
+__device__ __forceinline__ void fused_kv_write(const AttnParams &p, int r, int b, int t, int L, int kh, int pos_lo,
+                                               int pos_hi, int lane)
+{
+    constexpr int kVec = D * 2 / 16;                      // 16-byte vectors of one row and head
+    const int64_t num_slots = (int64_t)p.nb_total * p.block_size;
+    const int32_t *bt = p.block_table + (size_t)r * p.bt_stride;
+    const int n = (pos_hi - pos_lo) * kVec;
+    for (int idx = lane; idx < n; idx += 32) {
+        const int pos = pos_lo + idx / kVec, c = idx % kVec;
+        const int row = b + pos - (L - t);
+        int64_t slot = __ldg(p.fw_slots + row);
+        if (c == 0 && L > 0 && slot >= 0) {
+            const int64_t want = (int64_t)__ldg(bt + (pos >> 4)) * 16 + (pos & 15);
+            if (slot != want) atomicOr(p.err, kDevErrMeta);
+        }
+        if (slot < 0) slot = num_slots - 1;               // padding row -> scratch slot
+        if (slot >= num_slots) {
+            if (c == 0) atomicOr(p.err, 1u);
+            continue;
+        }
+        const size_t src = ((size_t)row * p.hkv + kh) * kVec + c;
+        const size_t dst = ((size_t)slot * p.hkv + kh) * kVec + c;
+        const uint4 kx = p.fw_k[src], vx = p.fw_v[src];
+        p.fw_kc[dst] = kx;
+        p.fw_vc[dst] = vx;
+    }
+    fence_proxy_async_global();
+    __syncwarp();
+    fence_proxy_async_global();
+}
+
 __device__ __forceinline__ void check_meta(const AttnParams &p, const WorkList &wl, int li)
 {
     const int r = wl.req[li];
@@ -184,6 +250,9 @@ cudaError_t launch_block_copy(int mode, void *const *pools, int32_t num_pools, c
                               const int32_t *dst, int32_t n, int32_t nb_total, int64_t block_bytes, void *buf,
                               uint32_t *err, cudaStream_t stream);
 cudaError_t launch_byte_copy(void *dst, const void *src, size_t bytes, cudaStream_t stream);
+cudaError_t launch_kv_write_ranges(const void *k, const void *v, void *k_cache, void *v_cache,
+                                   const int64_t *slot_mapping, const TokenRanges &ranges, int32_t row_bytes,
+                                   int64_t num_slots, uint32_t *err, cudaStream_t stream);
 
 // Merge split-KV partials of the split requests in `wl` into bf16 output.
 cudaError_t launch_attn_combine(const AttnParams &p, const WorkList &wl, int head_dim,

@@ -88,6 +88,59 @@ __global__ void __launch_bounds__(256) kv_write_fp8_kernel(
     }
 }
 
+// The scatter restricted to token ranges (a combined write + attention
+// call: the decode-class CTAs write their own rows, this kernel the rows of
+// the prefill-class requests).  Chunk c of the ranges' rows maps to token
+// begin[q] + (c / chunks_per_row - off[q]) of the range q that holds it.
+__global__ void __launch_bounds__(256) kv_write_ranges_kernel(
+    const uint4 *__restrict__ k, const uint4 *__restrict__ v, uint4 *__restrict__ k_cache,
+    uint4 *__restrict__ v_cache, const int64_t *__restrict__ slot_mapping, const __grid_constant__ TokenRanges rg,
+    int32_t chunks_per_row, int64_t num_slots, uint32_t *err)
+{
+    pdl_wait();                                           // as the full scatter: nothing is read before this
+    pdl_launch_dependents();
+    const int64_t total = (int64_t)rg.off[rg.n] * chunks_per_row;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < total; c += stride) {
+        const int32_t ri = (int32_t)(c / chunks_per_row);  // row among the ranges' rows
+        const int32_t off = (int32_t)(c - (int64_t)ri * chunks_per_row);
+        int lo = 0, hi = rg.n - 1;
+        while (lo < hi) {                                 // the range holding row ri
+            const int mid = (lo + hi + 1) >> 1;
+            if (rg.off[mid] <= ri) lo = mid; else hi = mid - 1;
+        }
+        const int64_t row = (int64_t)rg.begin[lo] + (ri - rg.off[lo]);
+        int64_t slot = __ldg(slot_mapping + row);
+        const int64_t src = row * chunks_per_row + off;
+        const uint4 kv = ldg_nc_v4(k + src), vv = ldg_nc_v4(v + src);
+        if (slot < 0) slot = num_slots - 1;               // padding row -> scratch slot
+        if (slot >= num_slots) {
+            if (off == 0 && err) atomicOr(err, 1u);
+            continue;
+        }
+        const int64_t dst = slot * chunks_per_row + off;
+        k_cache[dst] = kv;
+        v_cache[dst] = vv;
+    }
+}
+
+cudaError_t launch_kv_write_ranges(const void *k, const void *v, void *k_cache, void *v_cache,
+                                   const int64_t *slot_mapping, const TokenRanges &ranges, int32_t row_bytes,
+                                   int64_t num_slots, uint32_t *err, cudaStream_t stream)
+{
+    const int32_t chunks_per_row = row_bytes / 16;
+    const int64_t total = (int64_t)ranges.off[ranges.n] * chunks_per_row;
+    if (total <= 0) return cudaSuccess;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > 152 * 32) blocks = 152 * 32;
+    launch_begin(stream, kKvWrite);
+    cudaError_t e = launch_maybe_pdl(kv_write_ranges_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
+                                     (const uint4 *)k, (const uint4 *)v, (uint4 *)k_cache, (uint4 *)v_cache,
+                                     slot_mapping, ranges, chunks_per_row, num_slots, err);
+    launch_end(stream);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 cudaError_t launch_kv_write_fp8(const void *k, const void *v, void *k_codes, void *v_codes, float *k_scale,
                                 float *v_scale, const int64_t *slot_mapping, int32_t num_tokens, int32_t hkv,
                                 int64_t num_slots, uint32_t *err, cudaStream_t stream)

@@ -60,6 +60,15 @@ class DeviceStep:
         self.attend()
         return self.out
 
+    def combined(self):
+        """The step as one pkv_paged_kv_write_attention call."""
+        b = self.batch
+        pkv.paged_kv_write_attention(self.k, self.v, self.k_cache, self.v_cache, self.slots, self.out, self.q,
+                                     self.qsl, self.sl, self.bt, b.meta.query_start_loc, b.meta.seq_lens,
+                                     b.meta.max_query_len, b.meta.max_seq_len, b.spec.scale, self.ws,
+                                     window=self.window)
+        return self.out
+
 
 def device_batch(spec, device="cuda") -> Batch:
     """Values drawn on the device (fast for multi-GB pools)."""

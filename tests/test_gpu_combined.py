@@ -1,0 +1,141 @@
+"""pkv_paged_kv_write_attention: the step's write and attention in one call.
+
+The pools must come out bit-exact (whole pool except the scratch slot) and
+the attention within the parity tolerance of the oracle, on every
+arrangement the call makes: decode-class CTAs writing their own rows
+(slot ring with split counters or clusters, streaming kernel, padding
+requests, sliding window), the ranged scatter of prefill-class rows ahead of
+the tcgen05 and warp-MMA prefill kernels, on one stream or two, eager and
+from a CUDA graph.
+"""
+import math
+
+import pytest
+import torch
+
+import paged_kv_cache_84_gb300 as pkv
+from workloads import Req, Spec, config_spec, make_batch, random_spec
+from _helpers import DeviceStep, assert_close, cpu_copy, oracle_full, oracle_write
+
+pytestmark = pytest.mark.gpu
+
+
+def _pool_bits(t):
+    nbt, bs, hkv, d = t.shape
+    return t.contiguous().view(torch.int16).view(nbt * bs, hkv * d)
+
+
+def _check(dev, ref, window=0, what=""):
+    for got, want in ((dev.k_cache, ref.k_cache), (dev.v_cache, ref.v_cache)):
+        assert torch.equal(_pool_bits(got.cpu())[:-1], _pool_bits(want)[:-1]), f"pool {what}"
+    assert_close(dev.out, oracle_full(ref, window=window), what)
+    assert pkv.read_device_error(dev.ws) == 0
+
+
+def _run(spec, window=0, what=""):
+    b = make_batch(spec, device="cpu")
+    ref = cpu_copy(b)
+    oracle_write(ref)
+    dev = DeviceStep(b, window=window)
+    dev.combined()
+    _check(dev, ref, window, what)
+    return b, ref
+
+
+@pytest.mark.parametrize("cfg", [1, 2])
+def test_small_configs(cfg):
+    _run(config_spec(cfg), what=f"config {cfg}")
+
+
+@pytest.mark.parametrize("env", ["default", "no-overlap", "decode-side", "no-cluster", "separate", "no-tcgen05"])
+def test_engine_step_arrangements(env, monkeypatch):
+    """The 48-request engine step under every stream and kernel arrangement."""
+    if env == "no-overlap":
+        monkeypatch.setenv("PKV_NO_OVERLAP", "1")
+    elif env == "decode-side":
+        monkeypatch.setenv("PKV_DECODE_MAIN", "0")
+    elif env == "no-cluster":
+        monkeypatch.setenv("PKV_CLUSTER", "0")
+    elif env == "separate":
+        monkeypatch.setenv("PKV_SEPARATE_WRITE", "1")
+    elif env == "no-tcgen05":
+        monkeypatch.setenv("PKV_DISABLE_TCGEN05", "1")
+    _run(config_spec(2), what=f"engine step {env}")
+
+
+RANDOM = [
+    # seed, reqs, max_ctx, max_new, hq, hkv, d, pad rows, decode fraction
+    (0, 12, 700, 40, 16, 4, 64, 2, 0.5),
+    (1, 20, 3000, 3, 32, 8, 128, 1, 0.9),
+    (2, 8, 1500, 130, 8, 2, 48, 0, 0.5),
+    (3, 30, 400, 8, 8, 8, 128, 3, 1.0),        # decodes and short chunks only: one launch
+    (4, 6, 900, 300, 16, 2, 64, 0, 0.0),       # prefill chunks only: ranged scatter
+]
+
+
+@pytest.mark.parametrize("case", RANDOM, ids=[f"seed{c[0]}" for c in RANDOM])
+@pytest.mark.parametrize("window", [0, 300])
+def test_random_mixes(case, window):
+    seed, reqs, max_ctx, max_new, hq, hkv, d, pad, frac = case
+    spec = random_spec(300 + seed, reqs, max_ctx, max_new, hq, hkv, d, pad_rows=pad, decode_frac=frac)
+    _run(spec, window, f"random {seed} window {window}")
+
+
+@pytest.mark.parametrize("split", ["128", "1024"], ids=["slot-ring", "streaming"])
+def test_split_decodes_write_their_rows(split, monkeypatch):
+    """Splits whose ranges cut through a request's new rows (t up to 8) each
+    write the rows in their own range."""
+    monkeypatch.setenv("PKV_SPLIT_TOKENS", split)
+    reqs, blk = [], 0
+    for L, t in ((1030, 8), (2049, 3), (511, 5), (4000, 1), (129, 8), (0, 0)):
+        if t == 0:
+            reqs.append(Req(0, 1, [], pad=True))
+            continue
+        nb = (L + 15) // 16
+        reqs.append(Req(L - t, t, list(range(blk, blk + nb))))
+        blk += nb
+    spec = Spec("split-writes", reqs, 16, 8, 128, 16, blk + 3, 1 / math.sqrt(128), 87)
+    _run(spec, what=f"split {split}")
+
+
+def test_graph_replays_and_repeated_calls():
+    b = make_batch(config_spec(2), device="cpu")
+    ref = cpu_copy(b)
+    oracle_write(ref)
+    dev = DeviceStep(b)
+    for i in range(2):
+        dev.out.fill_(float("nan"))
+        dev.combined()
+        _check(dev, ref, what=f"eager {i}")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        dev.combined()
+    torch.cuda.synchronize()
+    for i in range(2):
+        dev.out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        _check(dev, ref, what=f"replay {i}")
+
+
+def test_slot_mapping_that_disagrees_with_the_table_is_flagged():
+    """A decode row whose slot differs from the block table's is written to
+    its slot and reported (PKV_DEVERR_META); nothing faults."""
+    spec = random_spec(310, 6, 500, 1, 8, 4, 64, decode_frac=1.0)
+    b = make_batch(spec, device="cpu")
+    dev = DeviceStep(b)
+    dev.slots[0] = (dev.slots[0] + 1) % (spec.num_blocks_total * spec.block_size - 1)
+    dev.combined()
+    assert pkv.read_device_error(dev.ws) & pkv.DEVERR_META
+
+
+def test_out_of_pool_slot_is_skipped_and_flagged():
+    spec = random_spec(311, 6, 500, 20, 8, 4, 64, decode_frac=0.5)
+    b = make_batch(spec, device="cpu")
+    dev = DeviceStep(b)
+    dev.slots[-1] = spec.num_blocks_total * spec.block_size + 5
+    dev.combined()
+    assert pkv.read_device_error(dev.ws) & pkv.DEVERR_SLOT
+    torch.cuda.synchronize()
