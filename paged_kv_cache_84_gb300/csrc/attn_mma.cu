@@ -719,7 +719,7 @@ __global__ void __launch_bounds__((CW + 1) * 32) attn_mma_kernel(AttnParams p, c
         pdl_wait();
         if constexpr (!FP8) {                                     // combined call: its rows (scratch slot)
             if (p.fw_k && wl.mode == kModeDecode && local == 0 && t > 0 && warp == 0)
-                fused_kv_write<D>(p, r, b, t, 0, kh, -t, 0, lane);
+                fused_kv_write<D>(p, r, b, t, 0, kh, -t, 0, lane, 32);
         }
         if (threadIdx.x == 0 && local == 0 && kh == 0) check_meta(p, wl, li);
         for (int idx = threadIdx.x; idx < t * g * D; idx += (CW + 1) * 32) {
@@ -796,8 +796,11 @@ __global__ void __launch_bounds__((CW + 1) * 32) attn_mma_kernel(AttnParams p, c
         if constexpr (!FP8) {
             // combined write + attention: this CTA's share of the request's new
             // rows goes into the pool first (the rows in its key range)
-            if (p.fw_k && wl.mode == kModeDecode)
-                fused_kv_write<D>(p, r, b, t, L, kh, max(k_begin, L - t), min(k_end, L), lane);
+            if (p.fw_k && wl.mode == kModeDecode) {
+                fused_kv_write<D>(p, r, b, t, L, kh, max(k_begin, L - t), min(k_end, L), lane, 32);
+                __syncwarp();
+                fence_proxy_async_global();                       // lane 0 issues the loads
+            }
         }
         for (int i = 0; i < nblk; i++) {
             if ((i & 31) == 0 && i > 0) ids = (i + lane < nblk) ? __ldg(bt + i + lane) : 0;
@@ -1125,7 +1128,7 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
         pdl_wait();                                               // keeps later programmatic waits transitive
         if constexpr (!FP8) {                                     // combined call: its rows (scratch slot)
             if (p.fw_k && wl.mode == kModeDecode && local == 0 && t > 0 && warp == 0)
-                fused_kv_write<D>(p, r, b, t, 0, kh, -t, 0, lane);
+                fused_kv_write<D>(p, r, b, t, 0, kh, -t, 0, lane, 32);
         }
         if (threadIdx.x == 0 && local == 0 && kh == 0) check_meta(p, wl, li);
         for (int idx = threadIdx.x; idx < t * gg * D; idx += kMmaThreads) {
@@ -1182,8 +1185,11 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
         if constexpr (!FP8) {
             // combined write + attention: this CTA's share of the request's new
             // rows goes into the pool first (the rows in its key range)
-            if (p.fw_k && wl.mode == kModeDecode)
-                fused_kv_write<D>(p, r, b, t, L, kh0, max(k_begin, L - t), min(k_end, L), lane);
+            if (p.fw_k && wl.mode == kModeDecode) {
+                fused_kv_write<D>(p, r, b, t, L, kh0, max(k_begin, L - t), min(k_end, L), lane, 32);
+                __syncwarp();
+                fence_proxy_async_global();                       // lane 0 issues the loads
+            }
         }
         for (int it = 0; it < iters; it++) {
             const int base = it * KG;

@@ -126,25 +126,26 @@ __device__ __forceinline__ void fence_proxy_async_global()
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-// Combined write + attention, decode-class CTA: copy the request's new rows
-// at positions [pos_lo, pos_hi) of KV head kh (the request's t tokens sit at
-// positions L - t .. L - 1, token row b + pos - (L - t)) into the pools at
-// fw_slots[row] (negative: the scratch slot), with the 32 lanes of the
-// calling warp, then fence them against the async proxy so that the TMA
-// loads this warp issues next see them.  A slot outside the pool is skipped
+// Combined write + attention: copy a request's new rows at positions
+// [pos_lo, pos_hi) of KV head kh (the request's t tokens sit at positions
+// L - t .. L - 1, token row b + pos - (L - t)) into the pools at
+// fw_slots[row] (negative: the scratch slot), with threads tid of nthreads,
+// each fencing its stores against the async proxy: after a barrier of the
+// writers, TMA loads issued by any of them (or by a thread past the barrier,
+// which fences again) see the rows.  A slot outside the pool is skipped
 // and reported (bit 1, as the scatter does); a slot other than the one the
 // block table gives for the position is reported (kDevErrMeta): the
 // attention reads the block table's slot.  pos_lo = pos_hi - t with L = 0:
 // a padding request, whose rows go to their slots without the table check.
 template <int D>
 __device__ __forceinline__ void fused_kv_write(const AttnParams &p, int r, int b, int t, int L, int kh, int pos_lo,
-                                               int pos_hi, int lane)
+                                               int pos_hi, int tid, int nthreads)
 {
     constexpr int kVec = D * 2 / 16;                      // 16-byte vectors of one row and head
     const int64_t num_slots = (int64_t)p.nb_total * p.block_size;
     const int32_t *bt = p.block_table + (size_t)r * p.bt_stride;
     const int n = (pos_hi - pos_lo) * kVec;
-    for (int idx = lane; idx < n; idx += 32) {
+    for (int idx = tid; idx < n; idx += nthreads) {
         const int pos = pos_lo + idx / kVec, c = idx % kVec;
         const int row = b + pos - (L - t);
         int64_t slot = __ldg(p.fw_slots + row);
@@ -163,8 +164,6 @@ __device__ __forceinline__ void fused_kv_write(const AttnParams &p, int r, int b
         p.fw_kc[dst] = kx;
         p.fw_vc[dst] = vx;
     }
-    fence_proxy_async_global();
-    __syncwarp();
     fence_proxy_async_global();
 }
 

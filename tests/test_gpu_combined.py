@@ -70,6 +70,7 @@ RANDOM = [
     (2, 8, 1500, 130, 8, 2, 48, 0, 0.5),
     (3, 30, 400, 8, 8, 8, 128, 3, 1.0),        # decodes and short chunks only: one launch
     (4, 6, 900, 300, 16, 2, 64, 0, 0.0),       # prefill chunks only: ranged scatter
+    (5, 10, 2000, 60, 32, 8, 128, 1, 0.3),     # chunks of up to 64 tokens (g = 4) on tcgen05
 ]
 
 
