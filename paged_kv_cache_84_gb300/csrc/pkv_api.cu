@@ -405,12 +405,29 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
         return wa > wc;
     });
 
+    // rough times of the two classes (decode ~ its K/V bytes at HBM speed,
+    // prefill ~ its causal pairs at tensor-core speed; only the ratio matters)
+    double dec_us = 0.0, pre_us = 0.0;
+    for (int32_t r : dec) dec_us += (double)sl_h[r] * hkv * d * 4.0 / 6.5e6;
+    for (int32_t r : pre) {
+        const double t = qsl_h[r + 1] - qsl_h[r], L = sl_h[r];
+        pre_us += (t * L - 0.5 * t * t) * hq * d * 4.0 / 1.2e9;
+    }
+    for (int32_t r : tcp) {
+        const double t = qsl_h[r + 1] - qsl_h[r], L = sl_h[r];
+        pre_us += (t * L - 0.5 * t * t) * hq * d * 4.0 / 1.2e9;
+    }
+
     // ---- KV split size, common to every split request
     const int sms = num_sms();
     int split = env_int("PKV_SPLIT_TOKENS", 0);
     const bool use_fma = env_int("PKV_ATTN_CUDA_CORE", 0) != 0;    // CUDA-core kernels instead of the staged MMA ones
     if (split <= 0) {
-        int64_t target_ctas = (int64_t)sms * (use_fma ? 8 : 16);
+        // Decodes beside a longer prefill only fill the SMs its last wave
+        // leaves: fewer, longer splits (measured on the mixed 2048-token-chunk
+        // step: 509 us with splits of ~2048 keys, 514 us with 16 CTAs per SM)
+        const bool filler = !tcp.empty() && pre_us > dec_us;
+        int64_t target_ctas = (int64_t)sms * (use_fma ? 8 : (filler ? 4 : 16));
         // quantized pools stream two KV heads per CTA: half the CTAs per split
         const int64_t head_ctas = fp8 ? hkv / 2 : hkv;
         int64_t s = (dec_keys * head_ctas + target_ctas - 1) / (target_ctas > 0 ? target_ctas : 1);
@@ -520,20 +537,8 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
         // The class on the caller's stream follows the K/V scatter as a
         // programmatic dependent (it starts while the scatter drains); the
         // other one waits for the fork event.
-        // The class expected to take longer goes on the caller's stream:
-        // decode time ~ its K/V bytes at HBM speed, prefill time ~ its
-        // causal pairs at tensor-core speed (rough rates; only the ratio
-        // matters).  PKV_DECODE_MAIN=0/1 forces the choice.
-        double dec_us = 0.0, pre_us = 0.0;
-        for (int32_t r : dec) dec_us += (double)sl_h[r] * hkv * d * 4.0 / 6.5e6;
-        for (int32_t r : pre) {
-            const double t = qsl_h[r + 1] - qsl_h[r], L = sl_h[r];
-            pre_us += (t * L - 0.5 * t * t) * hq * d * 4.0 / 1.2e9;
-        }
-        for (int32_t r : tcp) {
-            const double t = qsl_h[r + 1] - qsl_h[r], L = sl_h[r];
-            pre_us += (t * L - 0.5 * t * t) * hq * d * 4.0 / 1.2e9;
-        }
+        // The class expected to take longer (dec_us, pre_us above) goes on the
+        // caller's stream.  PKV_DECODE_MAIN=0/1 forces the choice.
         const int forced = env_int("PKV_DECODE_MAIN", -1);
         const bool decode_main = forced >= 0 ? forced != 0 : dec_us > pre_us;
         if (decode_main) pstream = side->stream;
