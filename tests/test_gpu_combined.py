@@ -140,3 +140,26 @@ def test_out_of_pool_slot_is_skipped_and_flagged():
     dev.combined()
     assert pkv.read_device_error(dev.ws) & pkv.DEVERR_SLOT
     torch.cuda.synchronize()
+
+
+def test_more_requests_than_one_launch_lists():
+    """600 decodes and 300 prefill chunks in one combined call: the decode
+    class and the ranged scatter each run several launches of at most 256
+    listed requests (or token ranges)."""
+    gen = torch.Generator().manual_seed(88)
+    reqs, blk = [], 0
+    for i in range(900):
+        if i % 3 == 2:
+            t = int(torch.randint(9, 41, (1,), generator=gen))   # t * g > 16: prefill class
+            c = int(torch.randint(0, 600, (1,), generator=gen))
+        else:
+            t, c = 1, int(torch.randint(0, 1500, (1,), generator=gen))
+        nb = (c + t + 15) // 16
+        reqs.append(Req(c, t, list(range(blk, blk + nb))))
+        blk += nb
+    spec = Spec("many", reqs, 8, 2, 64, 16, blk + 4, 0.125, 89)
+    from workloads import build_meta
+    m = build_meta(spec)
+    classes = pkv.plan_request_kernels(m.query_start_loc, m.seq_lens, 8, 2, 64)
+    assert sum(c != "decode" for c in classes) > 256
+    _run(spec, what="900 requests, combined call")
