@@ -605,10 +605,12 @@ def e2e_workload(pkv, copies, steps, device, dist=None, world=1):
 
 
 def fp8_workload(pkv, cfg, device, peaks, steps=20):
-    """The decode workload `cfg` on a quantized pool: the whole bf16 pool is
-    quantized once by the library's quantizing write, then each timed step is
-    the quantizing write of the step's rows + attention over E4M3 codes and
-    per (slot, head) scales, one CUDA graph of `steps` steps."""
+    """Workload `cfg` on a quantized pool: the whole bf16 pool is quantized
+    once by the library's quantizing write, then each timed step is the
+    quantizing write of the step's rows + attention over E4M3 codes and per
+    (slot, head) scales, one CUDA graph of `steps` steps.  The workspace
+    includes pkv_fp8_prefill_scratch_bytes, so prefill chunks run on tcgen05
+    over bf16 copies of their blocks."""
     spec = config_spec(cfg)
     b = make_batch(spec, device=device)
     m = b.meta
@@ -629,8 +631,9 @@ def fp8_workload(pkv, cfg, device, peaks, steps=20):
     sln = torch.tensor(m.seq_lens, dtype=torch.int32, device=device)
     bt = m.block_table.to(device)
     out = torch.empty_like(q)
+    extra = pkv.fp8_prefill_scratch_bytes(m.query_start_loc, m.seq_lens, spec.num_q_heads, spec.num_kv_heads, d)
     ws = pkv.make_workspace(pkv.attention_workspace_bytes(m.num_reqs, m.num_tokens, spec.num_q_heads, d,
-                                                          m.max_seq_len), device)
+                                                          m.max_seq_len) + extra, device)
 
     def step():
         pkv.paged_kv_write_fp8(k, v, kc, vc, ks, vs, slots)
@@ -664,9 +667,14 @@ def fp8_workload(pkv, cfg, device, peaks, steps=20):
     kv_bytes = sum(min(bs, max(0, m.seq_lens[r] - j * bs)) for r in range(m.num_reqs)
                    for j in range((m.seq_lens[r] + bs - 1) // bs)) * hkv * (2 * d + 8)
     other = 2 * q.numel() * 2 + m.num_tokens * hkv * (2 * d * 2 + 2 * d + 8)
+    flops = sum(4.0 * d * spec.num_q_heads * (t * (L - t) + t * (t + 1) / 2)
+                for t, L in ((m.query_start_loc[r + 1] - m.query_start_loc[r], m.seq_lens[r]) for r in range(m.num_reqs))
+                if L > 0 and t > 0)
     res = {"workload": spec.name, "step_us": step_s * 1e6, "query_tokens_per_s": m.num_tokens / step_s,
            "kv_bytes": kv_bytes, "kv_read_gbs": kv_bytes / step_s / 1e9,
            "step_hbm_frac": (kv_bytes + other) / step_s / 1e9 / peaks["hbm_gbs"],
+           "step_tensor_frac": flops / step_s / 1e12 / peaks["bf16_tflops"],
+           "prefill_scratch_bytes": extra,
            "pool": "E4M3 codes + fp32 scale per (slot, head)"}
     del kc, vc, ks, vs, q, k, v, out, ws, g
     torch.cuda.empty_cache()
@@ -817,7 +825,7 @@ def run_ours(args):
     fp8 = None
     if not args.no_breakdown:
         block_copies = block_copy_workload(pkv, device, peaks)
-        fp8 = {str(c): fp8_workload(pkv, c, device, peaks) for c in (3, 5)}
+        fp8 = {str(c): fp8_workload(pkv, c, device, peaks) for c in (3, 4, 5)}
         for cfg in (1, 2, 3, 4, 5):
             if cfg == args.workload:
                 r = dict(head)

@@ -400,6 +400,21 @@ pkv_status pkv_scatter_blocks(void *const *pools, int32_t num_pools, const int32
                               int32_t num_blocks_total, size_t block_bytes, const void *in, uint32_t *device_error,
                               cudaStream_t stream);
 
+/*
+ * Extra workspace bytes that let pkv_ragged_paged_attention_fp8 run this
+ * batch's prefill chunks on the tcgen05 kernel (host only; query_start_loc
+ * and seq_lens as host arrays).  With a workspace at least
+ * pkv_attention_workspace_bytes(...) plus this many bytes, a dequantizing
+ * pass first writes bf16 copies (code * scale, rounded to nearest) of those
+ * requests' blocks and a block table for them into the workspace's end, and
+ * the chunks attend over the copies; with a smaller workspace they run on
+ * the warp-MMA kernel over the codes.  0 when no request of the batch
+ * qualifies (head_dim 128, a group size dividing 128, at least 17 rows).
+ */
+size_t pkv_fp8_prefill_scratch_bytes(const int32_t *query_start_loc_host, const int32_t *seq_lens_host,
+                                     int32_t num_reqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                     int32_t head_dim);
+
 /* ---------------------------------------------------------------- staging copies
  *
  * "31. Engine v2", "Flattened ragged batches": the batch builder lays out

@@ -17,7 +17,7 @@ __all__ = [
     "PkvError", "load", "paged_kv_write", "ragged_paged_attention", "attention_workspace_bytes",
     "make_workspace", "read_device_error", "clear_device_error", "launch_count", "LIB_PATH",
     "DEVERR_SLOT", "DEVERR_BLOCK", "DEVERR_TIMEOUT", "DEVERR_META", "DEVERR_COUNTER", "WORKSPACE_MIN_BYTES", "profile_start", "profile_stop",
-    "plan_request_kernels", "CLASS_NAMES", "paged_kv_write_fp8", "ragged_paged_attention_fp8", "copy_blocks", "gather_blocks", "scatter_blocks", "MAX_POOLS", "copy_async", "paged_kv_write_attention",
+    "plan_request_kernels", "CLASS_NAMES", "paged_kv_write_fp8", "ragged_paged_attention_fp8", "copy_blocks", "gather_blocks", "scatter_blocks", "MAX_POOLS", "copy_async", "paged_kv_write_attention", "fp8_prefill_scratch_bytes",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpkv.so")
@@ -92,6 +92,8 @@ def load():
     L.pkv_gather_blocks.argtypes = [_c_p, _c_i32, _c_p, _c_i32, _c_i32, _c_sz, _c_p, _c_p, _c_p]
     L.pkv_scatter_blocks.restype = ctypes.c_int
     L.pkv_scatter_blocks.argtypes = [_c_p, _c_i32, _c_p, _c_i32, _c_i32, _c_sz, _c_p, _c_p, _c_p]
+    L.pkv_fp8_prefill_scratch_bytes.restype = _c_sz
+    L.pkv_fp8_prefill_scratch_bytes.argtypes = [_c_p, _c_p, _c_i32, _c_i32, _c_i32, _c_i32]
     L.pkv_copy_async.restype = ctypes.c_int
     L.pkv_copy_async.argtypes = [_c_p, _c_p, _c_sz, _c_p]
     L.pkv_paged_kv_write_attention.restype = ctypes.c_int
@@ -322,6 +324,14 @@ def scatter_blocks(pools, blocks, inp, device_error=None, stream=None):
     _check(load().pkv_scatter_blocks(arr, n_pools, _dev(blocks, "blocks", torch.int32), n, nbt, bb,
                                      _buf(inp, "inp"), _err(device_error), _stream(stream)), "scatter_blocks")
 
+
+
+def fp8_prefill_scratch_bytes(query_start_loc_host, seq_lens_host, num_q_heads, num_kv_heads, head_dim) -> int:
+    """Extra workspace bytes that put this batch's quantized-pool prefill on the tcgen05 kernel."""
+    qsl = _host_i32(query_start_loc_host, "query_start_loc_host")
+    sl = _host_i32(seq_lens_host, "seq_lens_host")
+    return int(load().pkv_fp8_prefill_scratch_bytes(_c_p(qsl.data_ptr()), _c_p(sl.data_ptr()), sl.numel(),
+                                                    num_q_heads, num_kv_heads, head_dim))
 
 
 def copy_async(dst, src, stream=None):

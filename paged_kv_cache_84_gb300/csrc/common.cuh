@@ -249,6 +249,8 @@ cudaError_t launch_block_copy(int mode, void *const *pools, int32_t num_pools, c
                               const int32_t *dst, int32_t n, int32_t nb_total, int64_t block_bytes, void *buf,
                               uint32_t *err, cudaStream_t stream);
 cudaError_t launch_byte_copy(void *dst, const void *src, size_t bytes, cudaStream_t stream);
+cudaError_t launch_fp8_dequant(const AttnParams &p, const WorkList &wl, __nv_bfloat16 *k_out, __nv_bfloat16 *v_out,
+                               int32_t *table_out, int32_t table_stride, int32_t sblk0, cudaStream_t stream);
 cudaError_t launch_kv_write_ranges(const void *k, const void *v, void *k_cache, void *v_cache,
                                    const int64_t *slot_mapping, const TokenRanges &ranges, int32_t row_bytes,
                                    int64_t num_slots, uint32_t *err, cudaStream_t stream);

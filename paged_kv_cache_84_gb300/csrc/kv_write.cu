@@ -12,6 +12,22 @@
 
 namespace pkv {
 
+// 8 E4M3 codes (bytes of x, low first) times `scale`, as 8 bf16 rounded to
+// nearest: every E4M3 value converts to half exactly, the product is fp32.
+__device__ __forceinline__ uint4 e4m3x8_to_bf16x8(uint2 x, float scale)
+{
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+        const uint32_t word = q < 2 ? x.x : x.y;
+        const __nv_fp8x2_storage_t pair = (__nv_fp8x2_storage_t)((word >> (16 * (q & 1))) & 0xFFFFu);
+        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
+        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
+        w[q] = pack_bf16x2(f.x * scale, f.y * scale);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 __global__ void __launch_bounds__(256) kv_write_kernel(
     const uint4 *__restrict__ k, const uint4 *__restrict__ v, uint4 *__restrict__ k_cache,
     uint4 *__restrict__ v_cache, const int64_t *__restrict__ slot_mapping, int64_t total_chunks,
@@ -137,6 +153,66 @@ cudaError_t launch_kv_write_ranges(const void *k, const void *v, void *k_cache, 
     cudaError_t e = launch_maybe_pdl(kv_write_ranges_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
                                      (const uint4 *)k, (const uint4 *)v, (uint4 *)k_cache, (uint4 *)v_cache,
                                      slot_mapping, ranges, chunks_per_row, num_slots, err);
+    launch_end(stream);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// Quantized-pool prefill on the tcgen05 kernel: the listed requests' blocks
+// (block i < ceil(L / 16) of request wl.req[li] goes to scratch block
+// sblk0 + item_off[li] + i) as bf16 K and V = code * scale, rounded to nearest, in a
+// scratch pool [blocks][16][hkv][128] with a scratch block table
+// (table_out[r][i] = the scratch block); rows at positions >= L become
+// zeros.  One thread per 8 codes of one (slot row, head).  A block id
+// outside the pool is reported (bit 2) and its rows become zeros.
+__global__ void __launch_bounds__(256) fp8_dequant_kernel(AttnParams p, const __grid_constant__ WorkList wl,
+                                                          uint4 *__restrict__ k_out, uint4 *__restrict__ v_out,
+                                                          int32_t *__restrict__ table_out, int32_t table_stride,
+                                                          int32_t sblk0)
+{
+    pdl_wait();                                           // the step's codes are in the pool
+    pdl_launch_dependents();
+    const int hkv = p.hkv;
+    const int64_t per_block = (int64_t)16 * hkv * 16;     // rows x heads x 8-code chunks
+    const int64_t total = (int64_t)wl.item_off[wl.n] * per_block;
+    const uint2 *kc = reinterpret_cast<const uint2 *>(p.k_cache);
+    const uint2 *vc = reinterpret_cast<const uint2 *>(p.v_cache);
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += stride) {
+        const int32_t lblk = (int32_t)(idx / per_block);  // block among this launch's
+        const int32_t rem = (int32_t)(idx - (int64_t)lblk * per_block);
+        const int rr = rem / (hkv * 16), h = (rem / 16) % hkv, c = rem % 16;
+        const int li = find_listed(wl, lblk);
+        const int r = wl.req[li], i = lblk - wl.item_off[li];
+        const int32_t sblk = sblk0 + lblk;                // scratch block
+        if (rr == 0 && h == 0 && c == 0) table_out[(size_t)r * table_stride + i] = sblk;
+        const int blk = __ldg(p.block_table + (size_t)r * p.bt_stride + i);
+        const bool in_pool = blk >= 0 && blk < p.nb_total;
+        if (!in_pool && rr == 0 && h == 0 && c == 0) atomicOr(p.err, 2u);
+        uint4 ko = make_uint4(0u, 0u, 0u, 0u), vo = ko;
+        if (in_pool && i * 16 + rr < wl.len[li]) {
+            const int64_t row = ((int64_t)blk * 16 + rr) * hkv + h;   // (slot, head)
+            const float ks = __ldg(p.k_scale + row), vs = __ldg(p.v_scale + row);
+            const uint2 kx = kc[row * 16 + c], vx = vc[row * 16 + c];
+            ko = e4m3x8_to_bf16x8(kx, ks);
+            vo = e4m3x8_to_bf16x8(vx, vs);
+        }
+        const int64_t dst = (((int64_t)sblk * 16 + rr) * hkv + h) * 16 + c;
+        k_out[dst] = ko;
+        v_out[dst] = vo;
+    }
+}
+
+cudaError_t launch_fp8_dequant(const AttnParams &p, const WorkList &wl, __nv_bfloat16 *k_out, __nv_bfloat16 *v_out,
+                               int32_t *table_out, int32_t table_stride, int32_t sblk0, cudaStream_t stream)
+{
+    const int64_t total = (int64_t)wl.item_off[wl.n] * 16 * p.hkv * 16;
+    if (total <= 0) return cudaSuccess;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    launch_begin(stream, kKvWrite);
+    cudaError_t e = launch_maybe_pdl(fp8_dequant_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, p, wl,
+                                     reinterpret_cast<uint4 *>(k_out), reinterpret_cast<uint4 *>(v_out), table_out,
+                                     table_stride, sblk0);
     launch_end(stream);
     return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -136,6 +136,14 @@ constexpr int kMaxPrefillRowSplits = 4;   // workspace sizing of split prefill t
 // several 32-row warp-MMA CTAs that each re-read the request's keys.
 constexpr int kTcMinRows = kDecodeRows + 1;
 
+// Quantized pools: prefill requests that the tcgen05 kernel takes when the
+// workspace holds bf16 copies of their blocks (fp8_tc_scratch bytes at the
+// workspace's end: K and V blocks [blocks][16][hkv][d] bf16, then a block
+// table [num_reqs][width] int32).  Returns 0 when no request qualifies.
+static int env_int(const char *name, int dflt);
+static size_t fp8_tc_scratch(const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs, int32_t g, int32_t hkv,
+                             int32_t d, int64_t *blocks_out = nullptr, int32_t *width_out = nullptr);
+
 // Kernel class of request r (host rule shared by the planner and pkv_plan_request_kernels).
 static int env_int(const char *name, int dflt);
 
@@ -150,6 +158,29 @@ static int request_class(int32_t t, int32_t L, int32_t g, int32_t d, bool fp8 = 
         !env_int("PKV_DISABLE_TCGEN05", 0))
         return PKV_CLASS_PREFILL_TENSOR;
     return PKV_CLASS_PREFILL_CUDA_CORE;
+}
+
+static size_t fp8_tc_scratch(const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs, int32_t g, int32_t hkv,
+                             int32_t d, int64_t *blocks_out, int32_t *width_out)
+{
+    if (!tc_prefill_supported(d, g) || env_int("PKV_DISABLE_TCGEN05", 0) || env_int("PKV_FP8_PREFILL_TC", 1) == 0)
+        return 0;
+    const int min_rows = env_int("PKV_TC_MIN_ROWS", kTcMinRows);
+    int64_t blocks = 0;
+    int32_t width = 0;
+    for (int r = 0; r < num_reqs; r++) {
+        const int32_t t = qsl_h[r + 1] - qsl_h[r], L = sl_h[r];
+        if (t == 0 || L == 0 || t * g <= kDecodeRows || t * g < min_rows) continue;
+        const int32_t nb = (L + 15) / 16;
+        blocks += nb;
+        width = nb > width ? nb : width;
+    }
+    if (blocks_out) *blocks_out = blocks;
+    if (width_out) *width_out = width;
+    if (blocks == 0) return 0;
+    const size_t kv = (size_t)blocks * 16 * hkv * d * 2;                 // one of K, V
+    const size_t table = (size_t)num_reqs * width * 4;
+    return 256 + 2 * ((kv + 255) / 256 * 256) + (table + 255) / 256 * 256;
 }
 
 static int env_int(const char *name, int dflt)
@@ -294,6 +325,14 @@ size_t pkv_attention_workspace_bytes(int32_t max_num_reqs, int32_t max_num_token
     return kErrBytes + kCounterBytes + (size_t)rows * ((size_t)head_dim * 4 + 8) + 64;
 }
 
+size_t pkv_fp8_prefill_scratch_bytes(const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs,
+                                     int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim)
+{
+    if (!qsl_h || !sl_h || num_reqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads)
+        return 0;
+    return fp8_tc_scratch(qsl_h, sl_h, num_reqs, num_q_heads / num_kv_heads, num_kv_heads, head_dim);
+}
+
 pkv_status pkv_plan_request_kernels(const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs,
                                     int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                     int32_t *class_out)
@@ -395,6 +434,28 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
         default: break;                                         // no rows at all
         }
     }
+    // Quantized pools: the prefill requests that tcgen05 can take go there
+    // when the workspace has room for bf16 copies of their blocks at its end
+    // (a dequantizing pass fills them); else they stay on the warp-MMA kernel.
+    size_t fp8_scratch = 0;
+    int64_t fp8_blocks = 0;
+    int32_t fp8_width = 0;
+    if (fp8 && !pre.empty()) {
+        fp8_scratch = fp8_tc_scratch(qsl_h, sl_h, num_reqs, g, hkv, d, &fp8_blocks, &fp8_width);
+        if (fp8_scratch > 0 && fp8_blocks * 16 < INT32_MAX &&
+            workspace_bytes >= fp8_scratch + kErrBytes + kCounterBytes + 4096) {
+            const int min_rows = env_int("PKV_TC_MIN_ROWS", kTcMinRows);
+            std::vector<int32_t> keep;
+            for (int32_t r : pre) {
+                const int32_t t = qsl_h[r + 1] - qsl_h[r];
+                if (t * g >= min_rows) tcp.push_back(r);
+                else keep.push_back(r);
+            }
+            pre.swap(keep);
+        } else {
+            fp8_scratch = 0;
+        }
+    }
     if (!tcp.empty() && ((int64_t)num_blocks_total * bs >= INT32_MAX || num_tokens >= INT32_MAX / 2))
         return PKV_ERR_UNSUPPORTED;
     // heaviest tensor-core requests first (work ~ new tokens x context), so
@@ -471,9 +532,11 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
     const size_t row_bytes = (size_t)d * 4 + 8;
     // The layout depends on the workspace size only: [error word][counters,
     // if the workspace holds them][partials].
-    const bool has_counters = workspace_bytes >= kErrBytes + kCounterBytes + 64;
+    // quantized prefill on tcgen05: its scratch takes the workspace's end
+    const size_t ws_front = fp8_scratch ? ((workspace_bytes - fp8_scratch) & ~(size_t)255) : workspace_bytes;
+    const bool has_counters = ws_front >= kErrBytes + kCounterBytes + 64;
     const size_t part_base = kErrBytes + (has_counters ? kCounterBytes : 0);
-    const size_t avail = workspace_bytes - part_base;
+    const size_t avail = ws_front - part_base;
     for (;;) {
         bool too_many = false;
         const size_t rows = partial_rows(split, &too_many);
@@ -611,6 +674,47 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
         }
     }
 
+    // ---- quantized pools: bf16 copies of the tcgen05 requests' blocks
+    AttnParams pt = pp;                                  // the tcgen05 launches' parameters
+    const void *tc_k = k_cache, *tc_v = v_cache;
+    int64_t tc_slots = num_slots;
+    if (fp8_scratch && !tcp.empty()) {
+        char *sc = ws + ws_front;                        // 256-aligned; the scratch fits before the end
+        const size_t kv = ((size_t)fp8_blocks * 16 * hkv * d * 2 + 255) / 256 * 256;
+        __nv_bfloat16 *sk = reinterpret_cast<__nv_bfloat16 *>(sc);
+        __nv_bfloat16 *sv = reinterpret_cast<__nv_bfloat16 *>(sc + kv);
+        int32_t *stab = reinterpret_cast<int32_t *>(sc + 2 * kv);
+        int32_t sblk0 = 0;
+        for (size_t c0 = 0; c0 < tcp.size(); c0 += kPlanMax) {
+            WorkList wl;
+            memset(&wl, 0, sizeof wl);
+            size_t c1 = c0 + kPlanMax < tcp.size() ? c0 + kPlanMax : tcp.size();
+            int32_t blocks = 0;
+            for (size_t x = c0; x < c1; x++) {
+                const int32_t r = tcp[x];
+                const int li = list_request(wl, r);
+                wl.item_off[li] = blocks;
+                blocks += (sl_h[r] + 15) / 16;
+            }
+            wl.item_off[wl.n] = blocks;
+            cudaError_t e = launch_fp8_dequant(p, wl, sk, sv, stab, fp8_width, sblk0, pstream);
+            if (e != cudaSuccess) {
+                join();
+                return cuda_fail(e, "quantized prefill dequant launch");
+            }
+            sblk0 += blocks;
+        }
+        pt.k_cache = sk;
+        pt.v_cache = sv;
+        pt.block_table = stab;
+        pt.bt_stride = fp8_width;
+        pt.nb_total = (int32_t)fp8_blocks;
+        pt.k_scale = pt.v_scale = nullptr;
+        tc_k = sk;
+        tc_v = sv;
+        tc_slots = fp8_blocks * 16;
+    }
+
     // ---- tensor-core prefill launches, submitted first: the longest work
     for (size_t c0 = 0; c0 < tcp.size(); c0 += kPlanMax) {
         WorkList wl;
@@ -628,7 +732,7 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
             items += (t + 2 * wl.tile_tokens - 1) / (2 * wl.tile_tokens);   // pairs of 128-row tiles
         }
         wl.item_off[wl.n] = items;
-        cudaError_t e = launch_attn_tc(pp, wl, items, q, num_tokens, k_cache, v_cache, num_slots, d, pstream);
+        cudaError_t e = launch_attn_tc(pt, wl, items, q, num_tokens, tc_k, tc_v, tc_slots, d, pstream);
         if (e != cudaSuccess) {
             join();
             return cuda_fail(e, "tensor-core prefill launch");

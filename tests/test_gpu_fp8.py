@@ -178,3 +178,47 @@ def test_fp8_unsupported_shapes_are_rejected():
     with pytest.raises(pkv.PkvError) as e:
         _run(b, pools)
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("window", [0, 300])
+@pytest.mark.parametrize("case", [FP8_CASES[0], FP8_CASES[2], FP8_CASES[3]], ids=["seed0", "seed2", "seed3"])
+def test_fp8_prefill_on_tensor_cores(case, window):
+    """With the extra workspace, quantized-pool prefill chunks attend over bf16
+    copies of their blocks on the tcgen05 kernel: parity with the oracle's
+    code * scale attention, and the same pools as with the plain workspace."""
+    seed, reqs, max_ctx, max_new, hq, hkv, pad = case
+    spec = random_spec(200 + seed, reqs, max_ctx, max_new, hq, hkv, 128, pad_rows=pad)
+    b = make_batch(spec, device="cpu")
+    m = b.meta
+    extra = pkv.fp8_prefill_scratch_bytes(m.query_start_loc, m.seq_lens, hq, hkv, 128)
+    assert extra > 0
+    base = pkv.attention_workspace_bytes(max(1, m.num_reqs), max(1, m.num_tokens), hq, 128, max(1, m.max_seq_len))
+    pools = _quantized_pools(b, seed)
+    got, _, err, ws = _run(b, pools, window=window, workspace_bytes=base + extra)
+    want, _ = _oracle(b, pools, window=window)
+    assert pkv.read_device_error(err) == 0
+    assert pkv.read_device_error(ws) == 0
+    assert_close(got, want, f"fp8 tcgen05 prefill seed {seed} window {window}")
+
+
+def test_fp8_mixed_chunk_step_sampled_on_tensor_cores():
+    """The mixed 2048-token-chunk step (a subset: the chunk at 16384 and 10
+    decodes) on a quantized pool with the tcgen05 scratch: sampled rows of
+    the chunk and of the decodes."""
+    spec = subset_spec(config_spec(4), 11)
+    b = make_batch(spec, device="cpu")
+    m = b.meta
+    extra = pkv.fp8_prefill_scratch_bytes(m.query_start_loc, m.seq_lens, spec.num_q_heads, spec.num_kv_heads, 128)
+    base = pkv.attention_workspace_bytes(m.num_reqs, m.num_tokens, spec.num_q_heads, 128, m.max_seq_len)
+    pools = _quantized_pools(b, 74)
+    got, _, _, ws = _run(b, pools, workspace_bytes=base + extra)
+    assert pkv.read_device_error(ws) == 0
+    kc, vc, ks, vs = [t.clone() for t in pools]
+    oracle.paged_kv_write_fp8(kc, vc, ks, vs, b.k, b.v, m.slot_mapping)
+    n = m.num_tokens
+    toks = [0, 1, 777, 1500, 2047, 2048, 2052, n - 3, n - 2, n - 1]
+    heads = [0, 31, 5, 17, 3, 30, 12, 7, 22, 1]
+    want = oracle.attention_rows_fp8(toks, heads, b.q, kc, vc, ks, vs, m.query_start_loc, m.seq_lens,
+                                     m.block_table, spec.scale, threads())
+    assert_close(got[torch.tensor(toks), torch.tensor(heads)], want, "fp8 mixed step on tcgen05")
+
