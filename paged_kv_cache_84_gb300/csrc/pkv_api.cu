@@ -163,7 +163,9 @@ static int request_class(int32_t t, int32_t L, int32_t g, int32_t d, bool fp8 = 
 static size_t fp8_tc_scratch(const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs, int32_t g, int32_t hkv,
                              int32_t d, int64_t *blocks_out, int32_t *width_out)
 {
-    if (!tc_prefill_supported(d, g) || env_int("PKV_DISABLE_TCGEN05", 0) || env_int("PKV_FP8_PREFILL_TC", 1) == 0)
+    // quantized pools have head_dim 128 (128-byte code rows)
+    if (d != 128 || !tc_prefill_supported(d, g) || env_int("PKV_DISABLE_TCGEN05", 0) ||
+        env_int("PKV_FP8_PREFILL_TC", 1) == 0)
         return 0;
     const int min_rows = env_int("PKV_TC_MIN_ROWS", kTcMinRows);
     int64_t blocks = 0;

@@ -142,3 +142,28 @@ def test_copy_async_validation_on_host(lib):
     assert lib.pkv_copy_async(a + 8, b, 64, None) == 2      # unaligned
     assert lib.pkv_copy_async(a, b + 8, 64, None) == 2
 
+
+
+def test_fp8_prefill_scratch_bytes_on_host(lib):
+    """The extra workspace for quantized prefill on tcgen05: bf16 K and V
+    copies of the qualifying chunks' blocks plus a block table, 256-byte
+    aligned parts; nothing for decodes, short chunks or head dims other
+    than 128."""
+    fn = lib.pkv_fp8_prefill_scratch_bytes
+    fn.restype = ctypes.c_size_t
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]
+
+    def call(qsl, sl, hq, hkv, d):
+        q = (ctypes.c_int32 * len(qsl))(*qsl)
+        s = (ctypes.c_int32 * len(sl))(*sl)
+        return fn(q, s, len(sl), hq, hkv, d)
+
+    # a 40-token chunk at 1000 keys (g = 4: 160 rows), a decode, a 3-token chunk (12 rows: decode class)
+    qsl, sl = [0, 40, 41, 44], [1040, 77, 500]
+    blocks, width = 65, 65                                 # ceil(1040 / 16)
+    kv = blocks * 16 * 8 * 128 * 2
+    want = 256 + 2 * ((kv + 255) // 256 * 256) + (3 * width * 4 + 255) // 256 * 256
+    assert call(qsl, sl, 32, 8, 128) == want
+    assert call([0, 1, 2], [77, 500], 32, 8, 128) == 0      # decodes only
+    assert call(qsl, sl, 32, 8, 48) == 0                    # head dim 48: no tcgen05 path for codes
+    assert call(qsl, sl, 24, 8, 128) == 0                   # g = 3 does not divide 128
