@@ -608,7 +608,8 @@ def fp8_workload(pkv, cfg, device, peaks, steps=20):
     """Workload `cfg` on a quantized pool: the whole bf16 pool is quantized
     once by the library's quantizing write, then each timed step is the
     quantizing write of the step's rows + attention over E4M3 codes and per
-    (slot, head) scales, one CUDA graph of `steps` steps.  The workspace
+    (slot, head) scales as one pkv_paged_kv_write_attention_fp8 call, one
+    CUDA graph of `steps` steps.  The workspace
     includes pkv_fp8_prefill_scratch_bytes, so prefill chunks run on tcgen05
     over bf16 copies of their blocks."""
     spec = config_spec(cfg)
@@ -636,9 +637,8 @@ def fp8_workload(pkv, cfg, device, peaks, steps=20):
                                                           m.max_seq_len) + extra, device)
 
     def step():
-        pkv.paged_kv_write_fp8(k, v, kc, vc, ks, vs, slots)
-        pkv.ragged_paged_attention_fp8(out, q, kc, vc, ks, vs, qsl, sln, bt, m.query_start_loc, m.seq_lens,
-                                       m.max_query_len, m.max_seq_len, spec.scale, ws)
+        pkv.paged_kv_write_attention_fp8(k, v, kc, vc, ks, vs, slots, out, q, qsl, sln, bt, m.query_start_loc,
+                                         m.seq_lens, m.max_query_len, m.max_seq_len, spec.scale, ws)
 
     stream = torch.cuda.current_stream()
     side = torch.cuda.Stream()

@@ -263,8 +263,11 @@ pkv_status pkv_paged_kv_write_attention(const void *k, const void *v, void *k_ca
  * range), so |q| and the per-key weight * V scale must stay inside fp16's
  * range (65504).  Requirements (else PKV_ERR_UNSUPPORTED): head_dim 128,
  * num_kv_heads a multiple of 4; the CUDA-core kernels
- * (PKV_ATTN_CUDA_CORE) have no quantized path.  Prefill chunks run on the
- * warp-level MMA kernels, not on tcgen05.
+ * (PKV_ATTN_CUDA_CORE) have no quantized path.  Prefill chunks run on
+ * tcgen05 over bf16 copies of their blocks (code * scale rounded to nearest)
+ * when the workspace holds pkv_fp8_prefill_scratch_bytes(...) more than
+ * pkv_attention_workspace_bytes(...); otherwise on the warp-level MMA kernels
+ * over the codes.
  */
 pkv_status pkv_ragged_paged_attention_fp8(void *out, const void *q,
                                           const void *k_cache, const void *v_cache,
@@ -280,6 +283,31 @@ pkv_status pkv_ragged_paged_attention_fp8(void *out, const void *q,
                                           int32_t num_blocks_total, float scale, int32_t window,
                                           void *workspace, size_t workspace_bytes,
                                           cudaStream_t stream);
+
+/*
+ * pkv_paged_kv_write_fp8 followed by pkv_ragged_paged_attention_fp8 in one
+ * call, arranged as pkv_paged_kv_write_attention: decode-class CTAs quantize
+ * and write their requests' new rows (the same E4M3 codes and scales as the
+ * quantizing scatter, bit for bit) just before reading them, a quantizing
+ * scatter restricted to the prefill-class rows runs ahead of the prefill
+ * kernels.  Arguments: the quantizing scatter's (k, v bf16 [num_tokens][
+ * num_kv_heads][128], 16-byte aligned; codes pools; scale pools written;
+ * slot_mapping agreeing with the block table) and the attention's.  Device
+ * errors of the write go to the workspace's error word; a decode row whose
+ * slot differs from the block table's sets PKV_DEVERR_META.
+ * PKV_SEPARATE_WRITE=1 runs the full quantizing scatter, then the attention.
+ */
+pkv_status pkv_paged_kv_write_attention_fp8(const void *k, const void *v, void *k_cache, void *v_cache,
+                                            float *k_scale, float *v_scale, const int64_t *slot_mapping,
+                                            void *out, const void *q, const int32_t *query_start_loc,
+                                            const int32_t *seq_lens, const int32_t *block_table,
+                                            int32_t block_table_stride, const int32_t *query_start_loc_host,
+                                            const int32_t *seq_lens_host, int32_t num_reqs,
+                                            int32_t num_tokens, int32_t max_query_len, int32_t max_seq_len,
+                                            int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                            int32_t block_size, int32_t num_blocks_total, float scale,
+                                            int32_t window, void *workspace, size_t workspace_bytes,
+                                            cudaStream_t stream);
 
 /*
  * ragged_paged_attention without a caller workspace.  The pages have no

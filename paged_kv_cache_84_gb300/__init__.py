@@ -17,7 +17,7 @@ __all__ = [
     "PkvError", "load", "paged_kv_write", "ragged_paged_attention", "attention_workspace_bytes",
     "make_workspace", "read_device_error", "clear_device_error", "launch_count", "LIB_PATH",
     "DEVERR_SLOT", "DEVERR_BLOCK", "DEVERR_TIMEOUT", "DEVERR_META", "DEVERR_COUNTER", "WORKSPACE_MIN_BYTES", "profile_start", "profile_stop",
-    "plan_request_kernels", "CLASS_NAMES", "paged_kv_write_fp8", "ragged_paged_attention_fp8", "copy_blocks", "gather_blocks", "scatter_blocks", "MAX_POOLS", "copy_async", "paged_kv_write_attention", "fp8_prefill_scratch_bytes",
+    "plan_request_kernels", "CLASS_NAMES", "paged_kv_write_fp8", "ragged_paged_attention_fp8", "copy_blocks", "gather_blocks", "scatter_blocks", "MAX_POOLS", "copy_async", "paged_kv_write_attention", "fp8_prefill_scratch_bytes", "paged_kv_write_attention_fp8",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpkv.so")
@@ -92,6 +92,9 @@ def load():
     L.pkv_gather_blocks.argtypes = [_c_p, _c_i32, _c_p, _c_i32, _c_i32, _c_sz, _c_p, _c_p, _c_p]
     L.pkv_scatter_blocks.restype = ctypes.c_int
     L.pkv_scatter_blocks.argtypes = [_c_p, _c_i32, _c_p, _c_i32, _c_i32, _c_sz, _c_p, _c_p, _c_p]
+    L.pkv_paged_kv_write_attention_fp8.restype = ctypes.c_int
+    L.pkv_paged_kv_write_attention_fp8.argtypes = [_c_p] * 12 + [_c_i32, _c_p, _c_p] + [_c_i32] * 9 + \
+        [_c_f, _c_i32, _c_p, _c_sz, _c_p]
     L.pkv_fp8_prefill_scratch_bytes.restype = _c_sz
     L.pkv_fp8_prefill_scratch_bytes.argtypes = [_c_p, _c_p, _c_i32, _c_i32, _c_i32, _c_i32]
     L.pkv_copy_async.restype = ctypes.c_int
@@ -324,6 +327,38 @@ def scatter_blocks(pools, blocks, inp, device_error=None, stream=None):
     _check(load().pkv_scatter_blocks(arr, n_pools, _dev(blocks, "blocks", torch.int32), n, nbt, bb,
                                      _buf(inp, "inp"), _err(device_error), _stream(stream)), "scatter_blocks")
 
+
+
+def paged_kv_write_attention_fp8(k, v, k_codes, v_codes, k_scale, v_scale, slot_mapping, out, q, query_start_loc,
+                                 seq_lens, block_table, query_start_loc_host, seq_lens_host, max_query_len,
+                                 max_seq_len, scale, workspace, stream=None, window: int = 0):
+    """paged_kv_write_fp8 followed by ragged_paged_attention_fp8 in one call (decode CTAs quantize and
+    write their own rows).  Write errors go to the workspace's error word."""
+    L = load()
+    n, hq, d = q.shape
+    nbt, bs, hkv, d2 = k_codes.shape
+    if out.shape != q.shape or d2 != d or v_codes.shape != k_codes.shape:
+        raise ValueError("shape mismatch")
+    if k.shape != (n, hkv, d) or v.shape != k.shape or slot_mapping.numel() != n:
+        raise ValueError("k, v must be [num_tokens, num_kv_heads, head_dim] with one slot per token")
+    if k_scale.shape != (nbt, bs, hkv) or v_scale.shape != k_scale.shape:
+        raise ValueError("scales must be [num_blocks_total, block_size, num_kv_heads]")
+    qsl_h = _host_i32(query_start_loc_host, "query_start_loc_host")
+    sl_h = _host_i32(seq_lens_host, "seq_lens_host")
+    if qsl_h.numel() != sl_h.numel() + 1:
+        raise ValueError("query_start_loc needs num_reqs + 1 entries")
+    st = L.pkv_paged_kv_write_attention_fp8(
+        _dev(k, "k", torch.bfloat16), _dev(v, "v", torch.bfloat16),
+        _dev(k_codes, "k_codes", torch.uint8), _dev(v_codes, "v_codes", torch.uint8),
+        _dev(k_scale, "k_scale", torch.float32), _dev(v_scale, "v_scale", torch.float32),
+        _dev(slot_mapping, "slot_mapping", torch.int64),
+        _dev(out, "out", torch.bfloat16), _dev(q, "q", torch.bfloat16),
+        _dev(query_start_loc, "query_start_loc", torch.int32), _dev(seq_lens, "seq_lens", torch.int32),
+        _dev(block_table, "block_table", torch.int32), block_table.shape[1],
+        _c_p(qsl_h.data_ptr()), _c_p(sl_h.data_ptr()), sl_h.numel(), n, int(max_query_len), int(max_seq_len),
+        hq, hkv, d, bs, nbt, float(scale), int(window), _dev(workspace, "workspace", torch.uint8), workspace.numel(),
+        _stream(stream))
+    _check(st, "paged_kv_write_attention_fp8")
 
 
 def fp8_prefill_scratch_bytes(query_start_loc_host, seq_lens_host, num_q_heads, num_kv_heads, head_dim) -> int:

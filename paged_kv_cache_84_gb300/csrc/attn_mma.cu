@@ -717,9 +717,9 @@ __global__ void __launch_bounds__((CW + 1) * 32) attn_mma_kernel(AttnParams p, c
         // Wait like every other CTA: this grid then never completes before the
         // grids it follows, which keeps later programmatic waits transitive.
         pdl_wait();
-        if constexpr (!FP8) {                                     // combined call: its rows (scratch slot)
-            if (p.fw_k && wl.mode == kModeDecode && local == 0 && t > 0 && warp == 0)
-                fused_kv_write<D>(p, r, b, t, 0, kh, -t, 0, lane, 32);
+        if (p.fw_k && wl.mode == kModeDecode && local == 0 && t > 0 && warp == 0) {   // combined call: its rows
+            if constexpr (!FP8) fused_kv_write<D>(p, r, b, t, 0, kh, -t, 0, lane, 32);
+            else fused_kv_write_fp8(p, r, b, t, 0, kh, 1, -t, 0, lane);
         }
         if (threadIdx.x == 0 && local == 0 && kh == 0) check_meta(p, wl, li);
         for (int idx = threadIdx.x; idx < t * g * D; idx += (CW + 1) * 32) {
@@ -793,14 +793,13 @@ __global__ void __launch_bounds__((CW + 1) * 32) attn_mma_kernel(AttnParams p, c
         // first 32 block ids while that kernel may still be running.
         int ids = lane < nblk ? __ldg(bt + lane) : 0, issued = 0;
         pdl_wait();                                               // the step's K/V rows are in the pool
-        if constexpr (!FP8) {
-            // combined write + attention: this CTA's share of the request's new
-            // rows goes into the pool first (the rows in its key range)
-            if (p.fw_k && wl.mode == kModeDecode) {
-                fused_kv_write<D>(p, r, b, t, L, kh, max(k_begin, L - t), min(k_end, L), lane, 32);
-                __syncwarp();
-                fence_proxy_async_global();                       // lane 0 issues the loads
-            }
+        // combined write + attention: this CTA's share of the request's new
+        // rows goes into the pool first (the rows in its key range)
+        if (p.fw_k && wl.mode == kModeDecode) {
+            if constexpr (!FP8) fused_kv_write<D>(p, r, b, t, L, kh, max(k_begin, L - t), min(k_end, L), lane, 32);
+            else fused_kv_write_fp8(p, r, b, t, L, kh, 1, max(k_begin, L - t), min(k_end, L), lane);
+            __syncwarp();
+            fence_proxy_async_global();                           // lane 0 issues the loads
         }
         for (int i = 0; i < nblk; i++) {
             if ((i & 31) == 0 && i > 0) ids = (i + lane < nblk) ? __ldg(bt + i + lane) : 0;
@@ -1126,9 +1125,9 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
 
     if (L == 0 || t == 0) {                                       // padding request: zero rows
         pdl_wait();                                               // keeps later programmatic waits transitive
-        if constexpr (!FP8) {                                     // combined call: its rows (scratch slot)
-            if (p.fw_k && wl.mode == kModeDecode && local == 0 && t > 0 && warp == 0)
-                fused_kv_write<D>(p, r, b, t, 0, kh, -t, 0, lane, 32);
+        if (p.fw_k && wl.mode == kModeDecode && local == 0 && t > 0 && warp == 0) {   // combined call: its rows
+            if constexpr (!FP8) fused_kv_write<D>(p, r, b, t, 0, kh0, -t, 0, lane, 32);
+            else fused_kv_write_fp8(p, r, b, t, 0, kh0, HP, -t, 0, lane);
         }
         if (threadIdx.x == 0 && local == 0 && kh == 0) check_meta(p, wl, li);
         for (int idx = threadIdx.x; idx < t * gg * D; idx += kMmaThreads) {
@@ -1182,14 +1181,13 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
         const int32_t *bt = p.block_table + (size_t)r * p.bt_stride + blk0;
         int ids = lane < nblk ? __ldg(bt + lane) : 0, issued = 0;   // not written by the scatter
         pdl_wait();                                               // the step's K/V rows are in the pool
-        if constexpr (!FP8) {
-            // combined write + attention: this CTA's share of the request's new
-            // rows goes into the pool first (the rows in its key range)
-            if (p.fw_k && wl.mode == kModeDecode) {
-                fused_kv_write<D>(p, r, b, t, L, kh0, max(k_begin, L - t), min(k_end, L), lane, 32);
-                __syncwarp();
-                fence_proxy_async_global();                       // lane 0 issues the loads
-            }
+        // combined write + attention: this CTA's share of the request's new
+        // rows (of its HP heads) goes into the pool first (the rows in its key range)
+        if (p.fw_k && wl.mode == kModeDecode) {
+            if constexpr (!FP8) fused_kv_write<D>(p, r, b, t, L, kh0, max(k_begin, L - t), min(k_end, L), lane, 32);
+            else fused_kv_write_fp8(p, r, b, t, L, kh0, HP, max(k_begin, L - t), min(k_end, L), lane);
+            __syncwarp();
+            fence_proxy_async_global();                           // lane 0 issues the loads
         }
         for (int it = 0; it < iters; it++) {
             const int base = it * KG;

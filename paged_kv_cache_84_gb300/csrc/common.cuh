@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -73,6 +74,8 @@ struct AttnParams {
     uint4 *fw_kc;
     uint4 *fw_vc;
     const int64_t *fw_slots;
+    float *fw_ks;               // quantized pools: the scale pools the combined call writes
+    float *fw_vs;
 };
 
 // Token ranges [begin, begin + len) of the rows a ranged scatter writes
@@ -177,6 +180,73 @@ __device__ __forceinline__ void check_meta(const AttnParams &p, const WorkList &
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// One (row, KV head) of 128 dims quantized to E4M3 by a warp ("31. Engine
+// v2", "Attention over the pool": codes with a scale per slot and head; the
+// format is this library's reading): lane l holds dims 4l .. 4l+3 of x (four
+// bf16) and gets their four codes; scale = max |x| / 448 in fp32 (the same in
+// every lane), codes = E4M3(x / scale) rounded to nearest even with
+// saturation; an all-zero row has scale 0 and zero codes.  The quantizing
+// scatter and the combined call's decode CTAs both use it, so their pools
+// agree bit for bit.
+__device__ __forceinline__ uint32_t quantize_e4m3_row(uint2 x, float &scale)
+{
+    const float f[4] = {bf16_lo(x.x), bf16_hi(x.x), bf16_lo(x.y), bf16_hi(x.y)};
+    float amax = fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3])));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    scale = __fdiv_rn(amax, 448.0f);
+    uint32_t codes = 0u;
+    if (scale > 0.f) {
+        const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+            make_float2(__fdiv_rn(f[0], scale), __fdiv_rn(f[1], scale)), __NV_SATFINITE, __NV_E4M3);
+        const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+            make_float2(__fdiv_rn(f[2], scale), __fdiv_rn(f[3], scale)), __NV_SATFINITE, __NV_E4M3);
+        codes = (uint32_t)lo | ((uint32_t)hi << 16);
+    }
+    return codes;
+}
+
+// The combined call on a quantized pool (head_dim 128): as fused_kv_write,
+// rows quantized by the calling warp (quantize_e4m3_row), codes and scales
+// stored at the row's slot; KV heads kh .. kh + nh - 1.
+__device__ __forceinline__ void fused_kv_write_fp8(const AttnParams &p, int r, int b, int t, int L, int kh, int nh,
+                                                   int pos_lo, int pos_hi, int lane)
+{
+    const int64_t num_slots = (int64_t)p.nb_total * p.block_size;
+    const int32_t *bt = p.block_table + (size_t)r * p.bt_stride;
+    const uint2 *k2 = reinterpret_cast<const uint2 *>(p.fw_k);
+    const uint2 *v2 = reinterpret_cast<const uint2 *>(p.fw_v);
+    uint32_t *kcodes = reinterpret_cast<uint32_t *>(p.fw_kc);
+    uint32_t *vcodes = reinterpret_cast<uint32_t *>(p.fw_vc);
+    for (int pos = pos_lo; pos < pos_hi; pos++) {            // warp-uniform
+        const int row = b + pos - (L - t);
+        int64_t slot = __ldg(p.fw_slots + row);
+        if (lane == 0 && L > 0 && slot >= 0) {
+            const int64_t want = (int64_t)__ldg(bt + (pos >> 4)) * 16 + (pos & 15);
+            if (slot != want) atomicOr(p.err, kDevErrMeta);
+        }
+        if (slot < 0) slot = num_slots - 1;                   // padding row -> scratch slot
+        if (slot >= num_slots) {
+            if (lane == 0) atomicOr(p.err, 1u);
+            continue;
+        }
+        for (int h = kh; h < kh + nh; h++) {
+            const size_t src = ((size_t)row * p.hkv + h) * 32 + lane;
+            const size_t dst = (size_t)slot * p.hkv + h;
+            float ks, vs;
+            const uint32_t kq = quantize_e4m3_row(k2[src], ks);
+            const uint32_t vq = quantize_e4m3_row(v2[src], vs);
+            kcodes[dst * 32 + lane] = kq;
+            vcodes[dst * 32 + lane] = vq;
+            if (lane == 0) {
+                p.fw_ks[dst] = ks;
+                p.fw_vs[dst] = vs;
+            }
+        }
+    }
+    fence_proxy_async_global();
+}
+
 __device__ __forceinline__ uint4 ldg_nc_v4(const void *p)
 {
     uint4 r;
@@ -251,6 +321,9 @@ cudaError_t launch_block_copy(int mode, void *const *pools, int32_t num_pools, c
 cudaError_t launch_byte_copy(void *dst, const void *src, size_t bytes, cudaStream_t stream);
 cudaError_t launch_fp8_dequant(const AttnParams &p, const WorkList &wl, __nv_bfloat16 *k_out, __nv_bfloat16 *v_out,
                                int32_t *table_out, int32_t table_stride, int32_t sblk0, cudaStream_t stream);
+cudaError_t launch_kv_write_fp8_ranges(const void *k, const void *v, void *k_codes, void *v_codes, float *k_scale,
+                                       float *v_scale, const int64_t *slot_mapping, const TokenRanges &ranges,
+                                       int32_t hkv, int64_t num_slots, uint32_t *err, cudaStream_t stream);
 cudaError_t launch_kv_write_ranges(const void *k, const void *v, void *k_cache, void *v_cache,
                                    const int64_t *slot_mapping, const TokenRanges &ranges, int32_t row_bytes,
                                    int64_t num_slots, uint32_t *err, cudaStream_t stream);

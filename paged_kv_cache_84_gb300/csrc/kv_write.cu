@@ -84,24 +84,69 @@ __global__ void __launch_bounds__(256) kv_write_fp8_kernel(
         const int64_t dst_row = slot * hkv + (w - i * hkv);
 #pragma unroll
         for (int which = 0; which < 2; which++) {
-            const uint2 x = which ? vx : kx;
-            const float f[4] = {bf16_lo(x.x), bf16_hi(x.x), bf16_lo(x.y), bf16_hi(x.y)};
-            float amax = fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3])));
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            const float scale = __fdiv_rn(amax, 448.0f);
-            uint32_t codes = 0u;
-            if (scale > 0.f) {
-                const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
-                    make_float2(__fdiv_rn(f[0], scale), __fdiv_rn(f[1], scale)), __NV_SATFINITE, __NV_E4M3);
-                const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
-                    make_float2(__fdiv_rn(f[2], scale), __fdiv_rn(f[3], scale)), __NV_SATFINITE, __NV_E4M3);
-                codes = (uint32_t)lo | ((uint32_t)hi << 16);
-            }
+            float scale;
+            const uint32_t codes = quantize_e4m3_row(which ? vx : kx, scale);
             (which ? v_codes : k_codes)[dst_row * 32 + lane] = codes;
             if (lane == 0) (which ? v_scale : k_scale)[dst_row] = scale;
         }
     }
+}
+
+// The quantizing scatter restricted to token ranges (the prefill rows of a
+// combined call on a quantized pool): warp w takes (row, head) w of the
+// ranges' rows.
+__global__ void __launch_bounds__(256) kv_write_fp8_ranges_kernel(
+    const uint2 *__restrict__ k, const uint2 *__restrict__ v, uint32_t *__restrict__ k_codes,
+    uint32_t *__restrict__ v_codes, float *__restrict__ k_scale, float *__restrict__ v_scale,
+    const int64_t *__restrict__ slot_mapping, const __grid_constant__ TokenRanges rg, int32_t hkv, int64_t num_slots,
+    uint32_t *err)
+{
+    pdl_wait();
+    pdl_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int64_t rows = (int64_t)rg.off[rg.n] * hkv;
+    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < rows; w += nwarps) {
+        const int32_t ri = (int32_t)(w / hkv), h = (int32_t)(w - (int64_t)ri * hkv);
+        int lo = 0, hi = rg.n - 1;
+        while (lo < hi) {                                 // the range holding row ri
+            const int mid = (lo + hi + 1) >> 1;
+            if (rg.off[mid] <= ri) lo = mid; else hi = mid - 1;
+        }
+        const int64_t row = (int64_t)rg.begin[lo] + (ri - rg.off[lo]);
+        int64_t slot = __ldg(slot_mapping + row);
+        const uint2 kx = k[(row * hkv + h) * 32 + lane], vx = v[(row * hkv + h) * 32 + lane];
+        if (slot < 0) slot = num_slots - 1;
+        if (slot >= num_slots) {
+            if (lane == 0 && h == 0 && err) atomicOr(err, 1u);
+            continue;
+        }
+        const int64_t dst = slot * hkv + h;
+        float ks, vs;
+        const uint32_t kq = quantize_e4m3_row(kx, ks), vq = quantize_e4m3_row(vx, vs);
+        k_codes[dst * 32 + lane] = kq;
+        v_codes[dst * 32 + lane] = vq;
+        if (lane == 0) {
+            k_scale[dst] = ks;
+            v_scale[dst] = vs;
+        }
+    }
+}
+
+cudaError_t launch_kv_write_fp8_ranges(const void *k, const void *v, void *k_codes, void *v_codes, float *k_scale,
+                                       float *v_scale, const int64_t *slot_mapping, const TokenRanges &ranges,
+                                       int32_t hkv, int64_t num_slots, uint32_t *err, cudaStream_t stream)
+{
+    const int64_t rows = (int64_t)ranges.off[ranges.n] * hkv;
+    if (rows <= 0) return cudaSuccess;
+    int64_t blocks = (rows + 7) / 8;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    launch_begin(stream, kKvWrite);
+    cudaError_t e = launch_maybe_pdl(kv_write_fp8_ranges_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
+                                     (const uint2 *)k, (const uint2 *)v, (uint32_t *)k_codes, (uint32_t *)v_codes,
+                                     k_scale, v_scale, slot_mapping, ranges, hkv, num_slots, err);
+    launch_end(stream);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // The scatter restricted to token ranges (a combined write + attention

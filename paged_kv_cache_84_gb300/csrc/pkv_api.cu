@@ -581,10 +581,13 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
     p.fw_kc = fused ? static_cast<uint4 *>(const_cast<void *>(k_cache)) : nullptr;
     p.fw_vc = fused ? static_cast<uint4 *>(const_cast<void *>(v_cache)) : nullptr;
     p.fw_slots = fused ? fw_slots : nullptr;
+    p.fw_ks = fused && fp8 ? const_cast<float *>(k_scale) : nullptr;
+    p.fw_vs = fused && fp8 ? const_cast<float *>(v_scale) : nullptr;
     AttnParams pp = p;                                   // prefill launches: their rows come from the scatter
     pp.fw_k = pp.fw_v = nullptr;
     pp.fw_kc = pp.fw_vc = nullptr;
     pp.fw_slots = nullptr;
+    pp.fw_ks = pp.fw_vs = nullptr;
 
     // ---- decode-class work runs on a side stream, concurrently with the
     // prefill kernels, when both are present: its CTAs fill the SMs that the
@@ -659,8 +662,11 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
                 rg.off[rg.n + 1] = rg.off[rg.n] + (qsl_h[r + 1] - qsl_h[r]);
                 rg.n++;
             }
-            cudaError_t e = launch_kv_write_ranges(fw_k, fw_v, const_cast<void *>(k_cache), const_cast<void *>(v_cache),
-                                                   fw_slots, rg, hkv * d * 2, num_slots, p.err, pstream);
+            cudaError_t e =
+                fp8 ? launch_kv_write_fp8_ranges(fw_k, fw_v, const_cast<void *>(k_cache), const_cast<void *>(v_cache),
+                                                 p.fw_ks, p.fw_vs, fw_slots, rg, hkv, num_slots, p.err, pstream)
+                    : launch_kv_write_ranges(fw_k, fw_v, const_cast<void *>(k_cache), const_cast<void *>(v_cache),
+                                             fw_slots, rg, hkv * d * 2, num_slots, p.err, pstream);
             if (e != cudaSuccess) {
                 join();
                 return cuda_fail(e, "ranged K/V scatter launch");
@@ -945,6 +951,40 @@ pkv_status pkv_paged_kv_write_attention(const void *k, const void *v, void *k_ca
                               hkv, d, bs, num_blocks_total, scale, window, workspace, workspace_bytes, stream);
     }
     return attention_impl(out, q, k_cache, v_cache, nullptr, nullptr, query_start_loc, seq_lens, block_table,
+                          block_table_stride, qsl_h, sl_h, num_reqs, num_tokens, max_query_len, max_seq_len, hq, hkv,
+                          d, bs, num_blocks_total, scale, window, workspace, workspace_bytes, stream, k, v,
+                          slot_mapping);
+}
+
+pkv_status pkv_paged_kv_write_attention_fp8(const void *k, const void *v, void *k_cache, void *v_cache, float *k_scale,
+                                            float *v_scale, const int64_t *slot_mapping, void *out, const void *q,
+                                            const int32_t *query_start_loc, const int32_t *seq_lens,
+                                            const int32_t *block_table, int32_t block_table_stride,
+                                            const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs,
+                                            int32_t num_tokens, int32_t max_query_len, int32_t max_seq_len, int32_t hq,
+                                            int32_t hkv, int32_t d, int32_t bs, int32_t num_blocks_total, float scale,
+                                            int32_t window, void *workspace, size_t workspace_bytes,
+                                            cudaStream_t stream)
+{
+    if (!k_scale || !v_scale) return PKV_ERR_INVALID_ARG;
+    if (num_tokens > 0 && (!k || !v || !slot_mapping || !k_cache || !v_cache)) return PKV_ERR_INVALID_ARG;
+    if (num_tokens > 0 && (!aligned(k, 16) || !aligned(v, 16) || !aligned(slot_mapping, 8)))
+        return PKV_ERR_UNSUPPORTED;
+    if (env_int("PKV_SEPARATE_WRITE", 0)) {
+        // the full quantizing scatter, then the attention
+        if (!workspace || workspace_bytes < PKV_WORKSPACE_MIN_BYTES || !aligned(workspace, 256))
+            return PKV_ERR_WORKSPACE;
+        if (num_tokens > 0) {
+            pkv_status st = pkv_paged_kv_write_fp8(k, v, k_cache, v_cache, k_scale, v_scale, slot_mapping, num_tokens,
+                                                   hkv, d, bs, num_blocks_total, static_cast<uint32_t *>(workspace),
+                                                   stream);
+            if (st != PKV_OK) return st;
+        }
+        return attention_impl(out, q, k_cache, v_cache, k_scale, v_scale, query_start_loc, seq_lens, block_table,
+                              block_table_stride, qsl_h, sl_h, num_reqs, num_tokens, max_query_len, max_seq_len, hq,
+                              hkv, d, bs, num_blocks_total, scale, window, workspace, workspace_bytes, stream);
+    }
+    return attention_impl(out, q, k_cache, v_cache, k_scale, v_scale, query_start_loc, seq_lens, block_table,
                           block_table_stride, qsl_h, sl_h, num_reqs, num_tokens, max_query_len, max_seq_len, hq, hkv,
                           d, bs, num_blocks_total, scale, window, workspace, workspace_bytes, stream, k, v,
                           slot_mapping);

@@ -222,3 +222,72 @@ def test_fp8_mixed_chunk_step_sampled_on_tensor_cores():
                                      m.block_table, spec.scale, threads())
     assert_close(got[torch.tensor(toks), torch.tensor(heads)], want, "fp8 mixed step on tcgen05")
 
+
+
+def _run_combined(batch, pools, window=0, workspace_bytes=None):
+    spec, m = batch.spec, batch.meta
+    kc, vc, ks, vs = [t.cuda() for t in pools]
+    k, v, q = batch.k.cuda(), batch.v.cuda(), batch.q.cuda()
+    slots = m.slot_mapping.cuda()
+    out = torch.full_like(q, float("nan"))
+    ws = pkv.make_workspace(workspace_bytes or pkv.attention_workspace_bytes(
+        max(1, m.num_reqs), max(1, m.num_tokens), spec.num_q_heads, spec.head_dim, max(1, m.max_seq_len)), "cuda")
+    pkv.paged_kv_write_attention_fp8(k, v, kc, vc, ks, vs, slots, out, q,
+                                     torch.tensor(m.query_start_loc, dtype=torch.int32, device="cuda"),
+                                     torch.tensor(m.seq_lens, dtype=torch.int32, device="cuda"),
+                                     m.block_table.cuda(), m.query_start_loc, m.seq_lens, m.max_query_len,
+                                     m.max_seq_len, spec.scale, ws, window=window)
+    torch.cuda.synchronize()
+    return out, (kc, vc, ks, vs), ws
+
+
+@pytest.mark.parametrize("mode", ["combined", "tcgen05-scratch", "separate"])
+@pytest.mark.parametrize("case", FP8_CASES[:4], ids=[f"seed{c[0]}" for c in FP8_CASES[:4]])
+def test_fp8_combined_write_and_attention(case, mode, monkeypatch):
+    """pkv_paged_kv_write_attention_fp8: decode CTAs quantize and write their
+    own rows, the prefill rows go through the ranged quantizing scatter; codes
+    and scales bit-exact (whole pool except the scratch block), attention
+    within the tolerance; with the tcgen05 prefill scratch; and as the full
+    scatter followed by the attention (PKV_SEPARATE_WRITE=1)."""
+    if mode == "separate":
+        monkeypatch.setenv("PKV_SEPARATE_WRITE", "1")
+    seed, reqs, max_ctx, max_new, hq, hkv, pad = case
+    spec = random_spec(200 + seed, reqs, max_ctx, max_new, hq, hkv, 128, pad_rows=pad)
+    b = make_batch(spec, device="cpu")
+    m = b.meta
+    wsb = None
+    if mode == "tcgen05-scratch":
+        wsb = pkv.attention_workspace_bytes(max(1, m.num_reqs), max(1, m.num_tokens), hq, 128,
+                                            max(1, m.max_seq_len)) + \
+            pkv.fp8_prefill_scratch_bytes(m.query_start_loc, m.seq_lens, hq, hkv, 128)
+    pools = _quantized_pools(b, seed)
+    for window in (0, 300):
+        got, dev_pools, ws = _run_combined(b, pools, window=window, workspace_bytes=wsb)
+        want, ref_pools = _oracle(b, pools, window=window)
+        nbt = spec.num_blocks_total + 1
+        for d, r in zip(dev_pools, ref_pools):
+            assert torch.equal(d.cpu().view(nbt, -1)[:-1].view(torch.uint8), r.view(nbt, -1)[:-1].view(torch.uint8))
+        assert pkv.read_device_error(ws) == 0
+        assert_close(got, want, f"fp8 combined {mode} seed {seed} window {window}")
+
+
+def test_fp8_combined_long_decodes_one_launch():
+    """Decode-only batch on the streaming kernel (two KV heads per CTA): one
+    launch writes and attends."""
+    spec = subset_spec(config_spec(5), 4)
+    b = make_batch(spec, device="cpu")
+    pools = _quantized_pools(b, 75)
+    before = pkv.launch_count()
+    got, dev_pools, ws = _run_combined(b, pools)
+    assert pkv.launch_count() - before == 1
+    m = b.meta
+    kc, vc, ks, vs = [t.clone() for t in pools]
+    oracle.paged_kv_write_fp8(kc, vc, ks, vs, b.k, b.v, m.slot_mapping)
+    for d, r in zip(dev_pools, (kc, vc, ks, vs)):
+        nbt = spec.num_blocks_total + 1
+        assert torch.equal(d.cpu().view(nbt, -1)[:-1].view(torch.uint8), r.view(nbt, -1)[:-1].view(torch.uint8))
+    toks, heads = [0, 1, 2, 3], [0, 21, 42, 63]
+    want = oracle.attention_rows_fp8(toks, heads, b.q, kc, vc, ks, vs, m.query_start_loc, m.seq_lens,
+                                     m.block_table, spec.scale, threads())
+    assert_close(got[torch.tensor(toks), torch.tensor(heads)], want, "fp8 combined long decodes")
+    assert pkv.read_device_error(ws) == 0
