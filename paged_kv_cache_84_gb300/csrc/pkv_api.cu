@@ -373,17 +373,18 @@ pkv_status pkv_read_device_error(const uint32_t *device_error, uint32_t *flags_o
 // attention call.  Decode-class CTAs write their requests' new rows
 // themselves, a ranged scatter writes the prefill-class requests' rows ahead
 // of the prefill kernels, and the decode class does not wait for that scatter.
-static pkv_status attention_impl(void *out, const void *q, const void *k_cache, const void *v_cache,
-                                 const float *k_scale, const float *v_scale, const int32_t *query_start_loc,
-                                 const int32_t *seq_lens, const int32_t *block_table, int32_t block_table_stride,
-                                 const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs, int32_t num_tokens,
-                                 int32_t max_query_len, int32_t max_seq_len, int32_t hq, int32_t hkv, int32_t d,
-                                 int32_t bs, int32_t num_blocks_total, float scale, int32_t window, void *workspace,
-                                 size_t workspace_bytes, cudaStream_t stream, const void *fw_k = nullptr,
-                                 const void *fw_v = nullptr, const int64_t *fw_slots = nullptr)
+// Host validation of an attention call: everything that can be checked
+// before enqueuing.  PKV_OK with *nothing_to_do set for an empty batch.
+static pkv_status validate_attention(const void *out, const void *q, const void *k_cache, const void *v_cache,
+                                     const float *k_scale, const float *v_scale, const int32_t *query_start_loc,
+                                     const int32_t *seq_lens, const int32_t *block_table, int32_t block_table_stride,
+                                     const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs, int32_t num_tokens,
+                                     int32_t max_query_len, int32_t max_seq_len, int32_t hq, int32_t hkv, int32_t d,
+                                     int32_t bs, int32_t num_blocks_total, int32_t window, const void *workspace,
+                                     size_t workspace_bytes, bool *nothing_to_do)
 {
     const bool fp8 = k_scale != nullptr;
-    // ---- host validation
+    *nothing_to_do = false;
     if (num_reqs < 0 || num_tokens < 0 || hq <= 0 || hkv <= 0 || d <= 0 || bs <= 0 || num_blocks_total <= 0)
         return PKV_ERR_INVALID_ARG;
     if (window < 0) return PKV_ERR_INVALID_ARG;
@@ -402,7 +403,10 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
     if (max_query_len < seen_q || max_seq_len < seen_l) return PKV_ERR_INVALID_ARG;
     if (!workspace || workspace_bytes < PKV_WORKSPACE_MIN_BYTES) return PKV_ERR_WORKSPACE;
     if (!aligned(workspace, 256)) return PKV_ERR_WORKSPACE;
-    if (num_tokens == 0) return PKV_OK;
+    if (num_tokens == 0) {
+        *nothing_to_do = true;
+        return PKV_OK;
+    }
     if (!out || !q || !k_cache || !v_cache || !query_start_loc || !seq_lens || !block_table)
         return PKV_ERR_INVALID_ARG;
     const int32_t g = hq / hkv;
@@ -416,84 +420,101 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
     if (fp8 && (d != 128 || hkv % 4 != 0 || !aligned(k_scale, 16) || !aligned(v_scale, 16) ||
                 env_int("PKV_ATTN_CUDA_CORE", 0)))
         return PKV_ERR_UNSUPPORTED;
+    return PKV_OK;
+}
 
-    // ---- classify
-    std::vector<int32_t> dec, pre, tcp;
-    int64_t dec_keys = 0, dec_max_keys = 0;
+// The requests of a batch by kernel class, as the planner launches them.
+struct RequestClasses {
+    std::vector<int32_t> dec;           // decode class and padding requests
+    std::vector<int32_t> pre;           // prefill on the warp-MMA (or CUDA-core) kernel
+    std::vector<int32_t> tcp;           // prefill on tcgen05, heaviest first
+    int64_t dec_keys = 0;               // keys of the decode class
+    int64_t dec_max_keys = 0;           // the longest decode-class key range
+    size_t fp8_scratch = 0;             // quantized pools: scratch for prefill on tcgen05 (0: none)
+    int64_t fp8_blocks = 0;             // ... blocks it copies
+    int32_t fp8_width = 0;              // ... width of its block table
+};
+
+static RequestClasses classify_requests(const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs, int32_t g,
+                                        int32_t hkv, int32_t d, int32_t window, bool fp8, size_t workspace_bytes)
+{
+    RequestClasses c;
     for (int r = 0; r < num_reqs; r++) {
         int32_t t = qsl_h[r + 1] - qsl_h[r], L = sl_h[r];
         switch (request_class(t, L, g, d, fp8)) {
         case PKV_CLASS_PADDING:
         case PKV_CLASS_DECODE: {
-            dec.push_back(r);
+            c.dec.push_back(r);
             const int64_t keys = L - decode_key_begin(t, L, window);
-            dec_keys += keys;
-            dec_max_keys = keys > dec_max_keys ? keys : dec_max_keys;
+            c.dec_keys += keys;
+            c.dec_max_keys = keys > c.dec_max_keys ? keys : c.dec_max_keys;
             break;
         }
-        case PKV_CLASS_PREFILL_CUDA_CORE: pre.push_back(r); break;
-        case PKV_CLASS_PREFILL_TENSOR: tcp.push_back(r); break;
+        case PKV_CLASS_PREFILL_CUDA_CORE: c.pre.push_back(r); break;
+        case PKV_CLASS_PREFILL_TENSOR: c.tcp.push_back(r); break;
         default: break;                                         // no rows at all
         }
     }
     // Quantized pools: the prefill requests that tcgen05 can take go there
     // when the workspace has room for bf16 copies of their blocks at its end
     // (a dequantizing pass fills them); else they stay on the warp-MMA kernel.
-    size_t fp8_scratch = 0;
-    int64_t fp8_blocks = 0;
-    int32_t fp8_width = 0;
-    if (fp8 && !pre.empty()) {
-        fp8_scratch = fp8_tc_scratch(qsl_h, sl_h, num_reqs, g, hkv, d, &fp8_blocks, &fp8_width);
-        if (fp8_scratch > 0 && fp8_blocks * 16 < INT32_MAX &&
-            workspace_bytes >= fp8_scratch + kErrBytes + kCounterBytes + 4096) {
+    if (fp8 && !c.pre.empty()) {
+        c.fp8_scratch = fp8_tc_scratch(qsl_h, sl_h, num_reqs, g, hkv, d, &c.fp8_blocks, &c.fp8_width);
+        if (c.fp8_scratch > 0 && c.fp8_blocks * 16 < INT32_MAX &&
+            workspace_bytes >= c.fp8_scratch + kErrBytes + kCounterBytes + 4096) {
             const int min_rows = env_int("PKV_TC_MIN_ROWS", kTcMinRows);
             std::vector<int32_t> keep;
-            for (int32_t r : pre) {
+            for (int32_t r : c.pre) {
                 const int32_t t = qsl_h[r + 1] - qsl_h[r];
-                if (t * g >= min_rows) tcp.push_back(r);
+                if (t * g >= min_rows) c.tcp.push_back(r);
                 else keep.push_back(r);
             }
-            pre.swap(keep);
+            c.pre.swap(keep);
         } else {
-            fp8_scratch = 0;
+            c.fp8_scratch = 0;
         }
     }
-    if (!tcp.empty() && ((int64_t)num_blocks_total * bs >= INT32_MAX || num_tokens >= INT32_MAX / 2))
-        return PKV_ERR_UNSUPPORTED;
     // heaviest tensor-core requests first (work ~ new tokens x context), so
     // that the long tiles start in the first wave and short ones fill the tail
-    std::stable_sort(tcp.begin(), tcp.end(), [&](int32_t a, int32_t c) {
+    std::stable_sort(c.tcp.begin(), c.tcp.end(), [&](int32_t a, int32_t b) {
         const int64_t wa = (int64_t)(qsl_h[a + 1] - qsl_h[a]) * sl_h[a];
-        const int64_t wc = (int64_t)(qsl_h[c + 1] - qsl_h[c]) * sl_h[c];
-        return wa > wc;
+        const int64_t wb = (int64_t)(qsl_h[b + 1] - qsl_h[b]) * sl_h[b];
+        return wa > wb;
     });
+    return c;
+}
 
-    // rough times of the two classes (decode ~ its K/V bytes at HBM speed,
-    // prefill ~ its causal pairs at tensor-core speed; only the ratio matters)
-    double dec_us = 0.0, pre_us = 0.0;
-    for (int32_t r : dec) dec_us += (double)sl_h[r] * hkv * d * 4.0 / 6.5e6;
-    for (int32_t r : pre) {
-        const double t = qsl_h[r + 1] - qsl_h[r], L = sl_h[r];
-        pre_us += (t * L - 0.5 * t * t) * hq * d * 4.0 / 1.2e9;
+// Rough times of the two classes: decode ~ its K/V bytes at HBM speed,
+// prefill ~ its causal pairs at tensor-core speed (only the ratio is used).
+static void class_times(const RequestClasses &c, const int32_t *qsl_h, const int32_t *sl_h, int32_t hq, int32_t hkv,
+                        int32_t d, double *dec_us, double *pre_us)
+{
+    *dec_us = *pre_us = 0.0;
+    for (int32_t r : c.dec) *dec_us += (double)sl_h[r] * hkv * d * 4.0 / 6.5e6;
+    for (const std::vector<int32_t> *list : {&c.pre, &c.tcp}) {
+        for (int32_t r : *list) {
+            const double t = qsl_h[r + 1] - qsl_h[r], L = sl_h[r];
+            *pre_us += (t * L - 0.5 * t * t) * hq * d * 4.0 / 1.2e9;
+        }
     }
-    for (int32_t r : tcp) {
-        const double t = qsl_h[r + 1] - qsl_h[r], L = sl_h[r];
-        pre_us += (t * L - 0.5 * t * t) * hq * d * 4.0 / 1.2e9;
-    }
+}
 
-    // ---- KV split size, common to every split request
+// Keys per decode split, common to every split request (a multiple of 128
+// before block rounding): about 16 CTAs per SM over the decode class's keys.
+static int decode_split_tokens(const RequestClasses &c, double dec_us, double pre_us, int32_t hkv, bool fp8,
+                               bool use_fma)
+{
     const int sms = num_sms();
     int split = env_int("PKV_SPLIT_TOKENS", 0);
-    const bool use_fma = env_int("PKV_ATTN_CUDA_CORE", 0) != 0;    // CUDA-core kernels instead of the staged MMA ones
     if (split <= 0) {
         // Decodes beside a longer prefill only fill the SMs its last wave
         // leaves: fewer, longer splits (measured on the mixed 2048-token-chunk
         // step: 509 us with splits of ~2048 keys, 514 us with 16 CTAs per SM)
-        const bool filler = !tcp.empty() && pre_us > dec_us;
+        const bool filler = !c.tcp.empty() && pre_us > dec_us;
         int64_t target_ctas = (int64_t)sms * (use_fma ? 8 : (filler ? 4 : 16));
         // quantized pools stream two KV heads per CTA: half the CTAs per split
         const int64_t head_ctas = fp8 ? hkv / 2 : hkv;
-        int64_t s = (dec_keys * head_ctas + target_ctas - 1) / (target_ctas > 0 ? target_ctas : 1);
+        int64_t s = (c.dec_keys * head_ctas + target_ctas - 1) / (target_ctas > 0 ? target_ctas : 1);
         if (s < kMinSplit) s = kMinSplit;
         split = (int)((s + 127) / 128 * 128);
     }
@@ -502,9 +523,46 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
     // measured with 8 requests of 32768 keys (FP8 pool), 64 splits of 512
     // keys took 154 us against 129 us with 37 of 896.
     if (split >= kLongSplitTokens && env_int("PKV_SPLIT_TOKENS", 0) <= 0) {
-        const int64_t floor_split = (dec_max_keys + kMaxStreamSplits - 1) / kMaxStreamSplits;
+        const int64_t floor_split = (c.dec_max_keys + kMaxStreamSplits - 1) / kMaxStreamSplits;
         if (floor_split > split) split = (int)((floor_split + 127) / 128 * 128);
     }
+    return split;
+}
+
+static pkv_status attention_impl(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                 const float *k_scale, const float *v_scale, const int32_t *query_start_loc,
+                                 const int32_t *seq_lens, const int32_t *block_table, int32_t block_table_stride,
+                                 const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs, int32_t num_tokens,
+                                 int32_t max_query_len, int32_t max_seq_len, int32_t hq, int32_t hkv, int32_t d,
+                                 int32_t bs, int32_t num_blocks_total, float scale, int32_t window, void *workspace,
+                                 size_t workspace_bytes, cudaStream_t stream, const void *fw_k = nullptr,
+                                 const void *fw_v = nullptr, const int64_t *fw_slots = nullptr)
+{
+    const bool fp8 = k_scale != nullptr;
+    bool nothing_to_do = false;
+    if (pkv_status st = validate_attention(out, q, k_cache, v_cache, k_scale, v_scale, query_start_loc, seq_lens,
+                                           block_table, block_table_stride, qsl_h, sl_h, num_reqs, num_tokens,
+                                           max_query_len, max_seq_len, hq, hkv, d, bs, num_blocks_total, window,
+                                           workspace, workspace_bytes, &nothing_to_do);
+        st != PKV_OK || nothing_to_do)
+        return st;
+    const int32_t g = hq / hkv;
+    RequestClasses rc = classify_requests(qsl_h, sl_h, num_reqs, g, hkv, d, window, fp8, workspace_bytes);
+    std::vector<int32_t> &dec = rc.dec, &pre = rc.pre, &tcp = rc.tcp;
+    const size_t fp8_scratch = rc.fp8_scratch;
+    const int64_t fp8_blocks = rc.fp8_blocks;
+    const int32_t fp8_width = rc.fp8_width;
+    int32_t seen_l = 0;                                  // the longest context of the batch
+    for (int r = 0; r < num_reqs; r++) seen_l = sl_h[r] > seen_l ? sl_h[r] : seen_l;
+    if (!tcp.empty() && ((int64_t)num_blocks_total * bs >= INT32_MAX || num_tokens >= INT32_MAX / 2))
+        return PKV_ERR_UNSUPPORTED;
+
+    // rough times of the two classes (decode ~ its K/V bytes at HBM speed,
+    // prefill ~ its causal pairs at tensor-core speed; only the ratio matters)
+    double dec_us = 0.0, pre_us = 0.0;
+    class_times(rc, qsl_h, sl_h, hq, hkv, d, &dec_us, &pre_us);
+    const bool use_fma = env_int("PKV_ATTN_CUDA_CORE", 0) != 0;    // CUDA-core kernels instead of the staged MMA ones
+    int split = decode_split_tokens(rc, dec_us, pre_us, hkv, fp8, use_fma);
     if (split % bs) split += bs - split % bs;
     // prefill tiles: every tile of a split request gets ceil(L / split) splits;
     // decode-class requests: splits over their (windowed) key range
@@ -518,7 +576,8 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
     for (int32_t r : pre) pre_ctas += (int64_t)((qsl_h[r + 1] - qsl_h[r] + tile - 1) / tile) * hkv;
     // Measured on the 48-request engine step it costs more (extra CTAs and a
     // combine on the critical path) than it saves, so it is opt-in.
-    const bool pre_split = !use_fma && !pre.empty() && pre_ctas < 2 * (int64_t)sms && env_int("PKV_PREFILL_SPLIT", 0);
+    const bool pre_split =
+        !use_fma && !pre.empty() && pre_ctas < 2 * (int64_t)num_sms() && env_int("PKV_PREFILL_SPLIT", 0);
     // every split request keeps S * t * hq partial rows; grow the split until they fit
     auto partial_rows = [&](int sp, bool *too_many) {
         size_t rows = 0;
