@@ -604,15 +604,17 @@ def e2e_workload(pkv, copies, steps, device, dist=None, world=1):
     return res
 
 
-def fp8_workload(pkv, cfg, device, peaks, steps=20):
+def fp8_workload(pkv, cfg, device, peaks, steps=20, subset=0):
     """Workload `cfg` on a quantized pool: the whole bf16 pool is quantized
     once by the library's quantizing write, then each timed step is the
     quantizing write of the step's rows + attention over E4M3 codes and per
     (slot, head) scales as one pkv_paged_kv_write_attention_fp8 call, one
     CUDA graph of `steps` steps.  The workspace
     includes pkv_fp8_prefill_scratch_bytes, so prefill chunks run on tcgen05
-    over bf16 copies of their blocks."""
+    over bf16 copies of their blocks.  subset: the first N requests only."""
     spec = config_spec(cfg)
+    if subset:
+        spec = subset_spec(spec, subset)
     b = make_batch(spec, device=device)
     m = b.meta
     nbt, bs, hkv, d = b.k_cache.shape
@@ -881,10 +883,28 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--subset", type=int, default=0,
                     help="keep only the first N requests of the workload (smaller profiling runs)")
+    ap.add_argument("--fp8", action="store_true",
+                    help="time only the workload on a quantized pool (a diagnostic line, for profiling runs)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.fp8:
+        return run_fp8(args)
     return run_ours(args)
+
+
+def run_fp8(args):
+    """One workload (or its first --subset requests) on a quantized pool,
+    --steps steps in a CUDA graph; prints the fp8 line (not the headline)."""
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    import paged_kv_cache_84_gb300 as pkv
+    from paged_kv_cache_84_gb300 import build as pkv_build
+    pkv_build.build()
+    pkv.load()
+    res = fp8_workload(pkv, args.workload, device, load_peaks(), steps=max(1, args.steps), subset=args.subset)
+    print(json.dumps({"fp8_pool": res, "steps": args.steps}), flush=True)
+    return 0
 
 
 if __name__ == "__main__":
