@@ -523,8 +523,11 @@ def e2e_workload(pkv, copies, steps, device, dist=None, world=1):
     buffer as a batch builder lays them out) to the device, runs the write and
     the attention, and copies the output back to pinned host memory, all inside
     the timed region.  Timed as one CUDA graph holding exactly `steps` such
-    steps over the rotated device copies (like the kernel-only timing), and
-    also as eager calls from Python (a diagnostic of the per-call host cost)."""
+    steps over the rotated device copies (like the kernel-only timing), with
+    the input and output copies on streams of their own, overlapping other
+    steps' attention (the reported value), with
+    each step's copies in line (serial_ms_per_step), and as eager calls from
+    Python (a diagnostic of the per-call host cost)."""
     c0 = copies[0]
     names = ("q", "k", "v", "qsl", "sl", "bt", "slots")
     offs, total = {}, 0
@@ -545,8 +548,11 @@ def e2e_workload(pkv, copies, steps, device, dist=None, world=1):
     hv = views(host)
     for name in names:
         hv[name].copy_(getattr(c0, name).cpu())
-    devbufs = [torch.empty(total, dtype=torch.uint8, device=device) for _ in copies]
+    # at least two input and output buffers, so that a step's copies can
+    # overlap another step even when one device copy of the workload fills L2
+    devbufs = [torch.empty(total, dtype=torch.uint8, device=device) for _ in range(max(2, len(copies)))]
     dev = [views(b) for b in devbufs]
+    outbufs = [torch.empty_like(c0.out) for _ in devbufs]
     outs_h = torch.empty_like(c0.out, device="cpu").pin_memory()
     stream = torch.cuda.current_stream()
     h2d = sum(hv[name].numel() * hv[name].element_size() for name in names)
@@ -576,7 +582,48 @@ def e2e_workload(pkv, copies, steps, device, dist=None, world=1):
         return max_over_ranks(ev0.elapsed_time(ev1) / n, dist, device)
 
     eager_ms = timed(lambda: [one(i) for i in range(steps)], steps)
-    graph_ms, why = None, None
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def pipelined(n):
+        # Each step's input copy on one stream, its output copy on another,
+        # the steps themselves on the current stream.  Step i waits for its
+        # inputs; its output copy waits for step i.  Step i reads input buffer
+        # i % L and writes output buffer i % L (L >= 2 of each), which step
+        # i - L used: its input copy waits for step i - L's output copy alone,
+        # so the input copies run ahead of the steps and step i's output
+        # buffer is free once its inputs are in.
+        cur = torch.cuda.current_stream()
+        s_in.wait_stream(cur)
+        s_out.wait_stream(cur)
+        L = len(devbufs)
+        ev_in = [torch.cuda.Event() for _ in range(n)]
+        ev_c = [torch.cuda.Event() for _ in range(n)]
+        ev_out = [torch.cuda.Event() for _ in range(n)]
+
+        def copy_in(i):
+            with torch.cuda.stream(s_in):
+                if i >= L:
+                    s_in.wait_event(ev_out[i - L])
+                pkv.copy_async(devbufs[i % L], host)
+                ev_in[i].record(s_in)
+
+        nxt = 0
+        for i in range(n):
+            while nxt < n and nxt - L < i:                  # issue every input copy whose wait is recorded
+                copy_in(nxt)
+                nxt += 1
+            c, d, o = copies[i % len(copies)], dev[i % L], outbufs[i % L]
+            cur.wait_event(ev_in[i])
+            c.run(q=d["q"], k=d["k"], v=d["v"], qsl=d["qsl"], sl=d["sl"], bt=d["bt"], slots=d["slots"], out=o)
+            ev_c[i].record(cur)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_c[i])
+                pkv.copy_async(outs_h, o)
+                ev_out[i].record(s_out)
+        cur.wait_stream(s_in)
+        cur.wait_stream(s_out)
+
+    graph_ms, pipe_ms, why = None, None, None
     try:
         side = torch.cuda.Stream()
         side.wait_stream(stream)
@@ -587,18 +634,31 @@ def e2e_workload(pkv, copies, steps, device, dist=None, world=1):
         torch.cuda.synchronize()
         upload_graph(g, stream)
         graph_ms = timed(g.replay, steps)
+        side.wait_stream(stream)
+        gp = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gp, stream=side):
+            pipelined(steps)
+        torch.cuda.synchronize()
+        upload_graph(gp, stream)
+        pipe_ms = timed(gp.replay, steps)
     except Exception as e:                                  # capture of host copies unsupported
         why = str(e).splitlines()[0][:160] if str(e) else type(e).__name__
         torch.cuda.synchronize()
-    ms = graph_ms if graph_ms is not None else eager_ms
+    ms = pipe_ms if pipe_ms is not None else graph_ms if graph_ms is not None else eager_ms
+    if pipe_ms is not None:
+        path = ("one CUDA graph of %d steps with the copies on two more streams: each step's packed pinned "
+                "inputs move in by pkv_copy_async ahead of the step (up to the rotated buffers), the step runs "
+                "pkv_paged_kv_write_attention once its inputs are in, and its output moves out to pinned "
+                "memory by pkv_copy_async once it is done" % steps)
+    elif graph_ms is not None:
+        path = ("one CUDA graph of %d steps; each: pkv_copy_async of the packed pinned inputs to the device, "
+                "pkv_paged_kv_write_attention, pkv_copy_async of the output to pinned memory" % steps)
+    else:
+        path = ("eager Python calls per step: pkv_copy_async of the packed pinned inputs to the device, "
+                "pkv_paged_kv_write_attention, pkv_copy_async of the output to pinned memory")
     res = {"value": job_value(c0.meta.num_tokens, world, ms), "unit": UNIT, "ms_per_step": ms,
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "path": ("one CUDA graph of %d steps; each: pkv_copy_async of the packed pinned inputs to the device, "
-                    "pkv_paged_kv_write_attention, pkv_copy_async of the output to pinned "
-                    "memory" % steps if graph_ms is not None else
-                    "eager Python calls per step: pkv_copy_async of the packed pinned inputs to the device, "
-                    "pkv_paged_kv_write_attention, pkv_copy_async of the output to pinned memory"),
-           "eager_ms_per_step": eager_ms}
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "path": path,
+           "serial_ms_per_step": graph_ms, "eager_ms_per_step": eager_ms}
     if why is not None:
         res["graph_unavailable"] = why
     return res

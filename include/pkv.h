@@ -458,7 +458,12 @@ size_t pkv_fp8_prefill_scratch_bytes(const int32_t *query_start_loc_host, const 
  * not overlap (else PKV_ERR_INVALID_ARG).  Zero bytes is a no-op.  A bit
  * copy; the kernel waits for the kernel before it on `stream` before it
  * reads src (programmatic launch), and the next kernel waits for it.
- * Nothing is allocated and nothing synchronises.
+ * Nothing is allocated and nothing synchronises.  A copy with a pinned host
+ * side runs on a dozen CTAs (environment PKV_LINK_COPY_CTAS overrides): the
+ * host link is saturated by then, and the rest of the GPU stays free for
+ * attention launched on other streams while the copy runs (staging the next
+ * step's inputs during this step).  A device-to-device copy spreads over
+ * the whole GPU.
  */
 pkv_status pkv_copy_async(void *dst, const void *src, size_t bytes, cudaStream_t stream);
 

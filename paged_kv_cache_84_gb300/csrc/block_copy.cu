@@ -11,6 +11,9 @@
 // layout, so a block is one contiguous byte range).  One launch covers all
 // pools and all listed blocks: each thread moves four independent 16-byte
 // vectors per iteration (four loads in flight before the stores).
+#include <algorithm>
+#include <cstdlib>
+
 #include "common.cuh"
 #include "sm100.cuh"
 
@@ -100,33 +103,71 @@ cudaError_t launch_block_copy(int mode, void *const *pools, int32_t num_pools, c
 // step's packed inputs from pinned host memory, or reading its output back.
 // Either side may be pinned host memory the device addresses directly, so
 // the copy is a kernel like the attention launches around it (no copy-engine
-// operation in the stream).  Four independent vectors per thread and
-// iteration keep enough bytes in flight over the host link.
-__global__ void __launch_bounds__(256) byte_copy_kernel(uint4 *dst, const uint4 *src, int64_t chunks)
+// operation in the stream).  U independent vectors per thread and iteration
+// are in flight at once.
+template <int U, int T>
+__global__ void __launch_bounds__(T) byte_copy_kernel(uint4 *dst, const uint4 *src, int64_t chunks)
 {
     pdl_wait();                                                   // the source may come from the kernel before
     pdl_launch_dependents();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t c0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c0 < chunks; c0 += 4 * stride) {
-        uint4 v[4];
+    for (int64_t c0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c0 < chunks; c0 += U * stride) {
+        uint4 v[U];
 #pragma unroll
-        for (int u = 0; u < 4; u++)
+        for (int u = 0; u < U; u++)
             if (c0 + u * stride < chunks) v[u] = src[c0 + u * stride];
 #pragma unroll
-        for (int u = 0; u < 4; u++)
+        for (int u = 0; u < U; u++)
             if (c0 + u * stride < chunks) dst[c0 + u * stride] = v[u];
     }
+}
+
+static bool is_host_memory(const void *ptr)
+{
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeHost;
+}
+
+// CTAs for a copy that crosses the host link.  A dozen CTAs of 256 threads
+// with 8 vectors each in flight (~390 KB) carry ~360 GB/s from pinned host
+// memory.  More CTAs barely raise that rate but slow the attention kernels
+// that run beside the copy (the next step's inputs staged while this step
+// computes): with the copy spread over 72 CTAs or 152 x 16, the mixed
+// 2048-token-chunk step with its copies overlapped took 875 us against 575 us
+// with 12 CTAs (511 us without copies), and the 48-request engine step 14.3
+// against 11.4 us (10.3 us without copies).
+static int link_copy_ctas()
+{
+    static const int n = [] {
+        const char *s = getenv("PKV_LINK_COPY_CTAS");
+        const int v = (s && *s) ? atoi(s) : 0;
+        return v > 0 ? std::min(v, 152 * 16) : 12;
+    }();
+    return n;
 }
 
 cudaError_t launch_byte_copy(void *dst, const void *src, size_t bytes, cudaStream_t stream)
 {
     const int64_t chunks = (int64_t)(bytes / 16);
     if (chunks <= 0) return cudaSuccess;
-    int64_t blocks = (chunks + 4 * 256 - 1) / (4 * 256);
-    if (blocks > 152 * 16) blocks = 152 * 16;                     // grid-stride beyond 16 CTAs per SM
+    const bool link = is_host_memory(dst) || is_host_memory(src);
+    cudaError_t e;
     launch_begin(stream, kByteCopy);
-    cudaError_t e = launch_maybe_pdl(byte_copy_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
-                                     static_cast<uint4 *>(dst), static_cast<const uint4 *>(src), chunks);
+    if (link) {
+        int64_t blocks = (chunks + 8 * 256 - 1) / (8 * 256);
+        blocks = std::min<int64_t>(blocks, link_copy_ctas());
+        e = launch_maybe_pdl(byte_copy_kernel<8, 256>, dim3((unsigned)blocks), dim3(256), 0, stream,
+                             static_cast<uint4 *>(dst), static_cast<const uint4 *>(src), chunks);
+    } else {
+        int64_t blocks = (chunks + 4 * 256 - 1) / (4 * 256);
+        blocks = std::min<int64_t>(blocks, 152 * 16);             // grid-stride beyond 16 CTAs per SM
+        e = launch_maybe_pdl(byte_copy_kernel<4, 256>, dim3((unsigned)blocks), dim3(256), 0, stream,
+                             static_cast<uint4 *>(dst), static_cast<const uint4 *>(src), chunks);
+    }
     launch_end(stream);
     return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -118,6 +118,27 @@ def test_copy_async_host_device_round_trip(nbytes):
     assert torch.equal(back, src)
 
 
+def test_copy_async_interior_of_pinned_buffers():
+    """Copies between device memory and 16-byte-aligned interiors of larger
+    pinned buffers (how a step's packed inputs are laid out), at a size that
+    takes host-link copies through several grid-stride rounds and a ragged
+    last round, leaving the bytes around the copied range untouched."""
+    n = (12 * 2048 * 2 + 77) * 16
+    g = torch.Generator().manual_seed(7)
+    big = torch.randint(0, 256, (n + 4096,), generator=g, dtype=torch.uint8).pin_memory()
+    d = torch.zeros(n + 512, dtype=torch.uint8, device="cuda")
+    pkv.copy_async(d[256:256 + n], big[1024:1024 + n])
+    torch.cuda.synchronize()
+    got = d.cpu()
+    assert torch.equal(got[256:256 + n], big[1024:1024 + n])
+    assert not got[:256].any() and not got[256 + n:].any()
+    back = torch.full((n + 4096,), 0xA5, dtype=torch.uint8).pin_memory()
+    pkv.copy_async(back[2048:2048 + n], d[256:256 + n])
+    torch.cuda.synchronize()
+    assert torch.equal(back[2048:2048 + n], big[1024:1024 + n])
+    assert bool((back[:2048] == 0xA5).all()) and bool((back[2048 + n:] == 0xA5).all())
+
+
 def test_copy_async_rejects_unaligned_and_odd_sizes():
     d = torch.empty(4096, dtype=torch.uint8, device="cuda")
     h = torch.empty(4096, dtype=torch.uint8).pin_memory()
