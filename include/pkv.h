@@ -353,18 +353,64 @@ pkv_status pkv_ragged_paged_attention_noalloc(void *out, const void *q,
 /*
  * Which kernel path pkv_ragged_paged_attention takes for each request
  * (host only, no CUDA call): class_out[r] receives one of PKV_CLASS_*.
- * Decode-class requests (t * g <= 16) run on the CUDA-core decode kernel,
- * with KV split across CTAs for long contexts; prefill-class requests run
- * in tiles of new tokens.  For accounting and tests.
+ * Decode-class requests (t * g <= 16) run on the warp-level MMA decode
+ * kernels, with KV split across CTAs for long contexts; prefill-class
+ * requests run in tiles of new tokens, on tcgen05 where the head dim and
+ * group fit a 128-row tile.  For accounting and tests.  (With the
+ * environment switch PKV_ATTN_CUDA_CORE=1 the decode and non-tensor
+ * prefill classes run on CUDA-core FMA kernels instead.)
  */
 #define PKV_CLASS_NONE 0                 /* no rows */
 #define PKV_CLASS_PADDING 1              /* seq_len 0: rows zeroed */
-#define PKV_CLASS_DECODE 2               /* CUDA-core decode kernel (+ split combine) */
-#define PKV_CLASS_PREFILL_CUDA_CORE 3    /* CUDA-core prefill tiles */
+#define PKV_CLASS_DECODE 2               /* decode kernels (split KV merged in a cluster or in-kernel) */
+#define PKV_CLASS_PREFILL_CUDA_CORE 3    /* warp-MMA prefill tiles (not on tcgen05) */
 #define PKV_CLASS_PREFILL_TENSOR 4       /* tcgen05 prefill tiles */
 pkv_status pkv_plan_request_kernels(const int32_t *query_start_loc_host, const int32_t *seq_lens_host,
                                     int32_t num_reqs, int32_t num_q_heads, int32_t num_kv_heads,
                                     int32_t head_dim, int32_t *class_out);
+
+/*
+ * The launch plan an attention call would follow (host only; no CUDA call
+ * when num_sms > 0).  For a flattened ragged batch ("31. Engine v2",
+ * "Flattened ragged batches") the planner classifies the requests, picks
+ * one split length for the decode class (about 16 CTAs per SM over its
+ * keys, 4 beside a longer prefill, at least 256 keys, a multiple of 128, at
+ * most 32 streaming splits per request, then doubled until the split
+ * partials fit the workspace), and decides whether the decode and prefill
+ * classes run concurrently on two streams.  This reports those decisions
+ * for the same arguments as pkv_ragged_paged_attention (quantized != 0: its
+ * _fp8 variant; combined != 0: pkv_paged_kv_write_attention), given the
+ * workspace size and the GPU's SM count (num_sms <= 0: the current
+ * device's, which needs a GPU).  Reads the same environment switches as
+ * the attention calls.  query_start_loc_host has num_reqs + 1 entries,
+ * seq_lens_host num_reqs; plan_out is written on success only.
+ *
+ * Errors: PKV_ERR_INVALID_ARG for null pointers, num_reqs < 0, a negative
+ * query length or window, t > seq_len, or heads that do not group;
+ * PKV_ERR_UNSUPPORTED for a head dim, block size, group or quantized shape
+ * the attention calls reject; PKV_ERR_CUDA when num_sms <= 0 and no device
+ * answers.
+ */
+typedef struct pkv_attention_plan {
+    int32_t decode_requests;          /* decode class, padding requests included */
+    int32_t prefill_tensor_requests;  /* prefill on tcgen05 */
+    int32_t prefill_mma_requests;     /* prefill on the warp-MMA (or CUDA-core) kernel */
+    int32_t decode_split_tokens;      /* keys per decode split, a multiple of block_size */
+    int32_t max_decode_splits;        /* the largest split count of a decode request */
+    int32_t decode_cluster;           /* CTAs per thread-block cluster of the first decode launch; 0: none */
+    int32_t decode_streaming;         /* 1: decode splits long enough for the streaming kernel */
+    int32_t split_counters;           /* 1: the workspace holds in-kernel combine counters */
+    int32_t overlap;                  /* 1: decode and prefill classes on two streams */
+    int32_t decode_on_caller_stream;  /* with overlap: 1 if the decodes run on the caller's stream */
+    int32_t prefill_key_splits;       /* 1: warp-MMA prefill tiles split over keys */
+    int32_t reserved;
+    size_t quantized_prefill_scratch; /* workspace bytes of bf16 block copies for quantized prefill */
+    size_t partial_bytes;             /* workspace bytes of split partials */
+} pkv_attention_plan;
+pkv_status pkv_plan_attention(const int32_t *query_start_loc_host, const int32_t *seq_lens_host,
+                              int32_t num_reqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                              int32_t block_size, int32_t window, int32_t quantized, int32_t combined,
+                              size_t workspace_bytes, int32_t num_sms, pkv_attention_plan *plan_out);
 
 /*
  * Set a device error word to zero (enqueued on stream).

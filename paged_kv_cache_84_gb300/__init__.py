@@ -17,7 +17,7 @@ __all__ = [
     "PkvError", "load", "paged_kv_write", "ragged_paged_attention", "attention_workspace_bytes",
     "make_workspace", "read_device_error", "clear_device_error", "launch_count", "LIB_PATH",
     "DEVERR_SLOT", "DEVERR_BLOCK", "DEVERR_TIMEOUT", "DEVERR_META", "DEVERR_COUNTER", "WORKSPACE_MIN_BYTES", "profile_start", "profile_stop",
-    "plan_request_kernels", "CLASS_NAMES", "paged_kv_write_fp8", "ragged_paged_attention_fp8", "copy_blocks", "gather_blocks", "scatter_blocks", "MAX_POOLS", "copy_async", "paged_kv_write_attention", "fp8_prefill_scratch_bytes", "paged_kv_write_attention_fp8",
+    "plan_request_kernels", "CLASS_NAMES", "paged_kv_write_fp8", "ragged_paged_attention_fp8", "copy_blocks", "gather_blocks", "scatter_blocks", "MAX_POOLS", "copy_async", "paged_kv_write_attention", "fp8_prefill_scratch_bytes", "paged_kv_write_attention_fp8", "plan_attention",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpkv.so")
@@ -33,6 +33,16 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape or alignment",
 
 _c_i32, _c_i64, _c_p, _c_f, _c_sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_size_t
 _lib = None
+
+
+class _Plan(ctypes.Structure):
+    """pkv_attention_plan (include/pkv.h)."""
+    _fields_ = [("decode_requests", _c_i32), ("prefill_tensor_requests", _c_i32),
+                ("prefill_mma_requests", _c_i32), ("decode_split_tokens", _c_i32),
+                ("max_decode_splits", _c_i32), ("decode_cluster", _c_i32), ("decode_streaming", _c_i32),
+                ("split_counters", _c_i32), ("overlap", _c_i32), ("decode_on_caller_stream", _c_i32),
+                ("prefill_key_splits", _c_i32), ("reserved", _c_i32),
+                ("quantized_prefill_scratch", _c_sz), ("partial_bytes", _c_sz)]
 
 
 class PkvError(RuntimeError):
@@ -99,6 +109,8 @@ def load():
     L.pkv_fp8_prefill_scratch_bytes.argtypes = [_c_p, _c_p, _c_i32, _c_i32, _c_i32, _c_i32]
     L.pkv_copy_async.restype = ctypes.c_int
     L.pkv_copy_async.argtypes = [_c_p, _c_p, _c_sz, _c_p]
+    L.pkv_plan_attention.restype = ctypes.c_int
+    L.pkv_plan_attention.argtypes = [_c_p, _c_p] + [_c_i32] * 8 + [_c_sz, _c_i32, ctypes.POINTER(_Plan)]
     L.pkv_paged_kv_write_attention.restype = ctypes.c_int
     L.pkv_paged_kv_write_attention.argtypes = [_c_p] * 10 + [_c_i32, _c_p, _c_p] + [_c_i32] * 9 + \
         [_c_f, _c_i32, _c_p, _c_sz, _c_p]
@@ -162,6 +174,26 @@ def plan_request_kernels(query_start_loc_host, seq_lens_host, num_q_heads, num_k
     _check(load().pkv_plan_request_kernels(_c_p(qsl.data_ptr()), _c_p(sl.data_ptr()), sl.numel(), num_q_heads,
                                            num_kv_heads, head_dim, _c_p(out.data_ptr())), "plan_request_kernels")
     return [CLASS_NAMES[int(c)] for c in out]
+
+
+def plan_attention(query_start_loc_host, seq_lens_host, num_q_heads, num_kv_heads, head_dim, block_size=16,
+                   window=0, quantized=False, combined=False, workspace_bytes=None, num_sms=0) -> dict:
+    """The launch plan of an attention call with these host metadata (host
+    only when num_sms > 0): request classes, decode split length and split
+    count, cluster and streaming choice, stream overlap, workspace use.
+    workspace_bytes defaults to attention_workspace_bytes for the batch."""
+    qsl = _host_i32(query_start_loc_host, "query_start_loc_host")
+    sl = _host_i32(seq_lens_host, "seq_lens_host")
+    if workspace_bytes is None:
+        n = sl.numel()
+        workspace_bytes = attention_workspace_bytes(max(1, n), max(1, int(qsl[-1]) if qsl.numel() else 1),
+                                                    num_q_heads, head_dim, max(1, int(sl.max()) if n else 1))
+    out = _Plan()
+    _check(load().pkv_plan_attention(_c_p(qsl.data_ptr()), _c_p(sl.data_ptr()), sl.numel(), num_q_heads,
+                                     num_kv_heads, head_dim, block_size, window, int(bool(quantized)),
+                                     int(bool(combined)), workspace_bytes, num_sms, ctypes.byref(out)),
+           "plan_attention")
+    return {name: int(getattr(out, name)) for name, _ in _Plan._fields_ if name != "reserved"}
 
 
 def launch_count() -> int:

@@ -502,9 +502,8 @@ static void class_times(const RequestClasses &c, const int32_t *qsl_h, const int
 // Keys per decode split, common to every split request (a multiple of 128
 // before block rounding): about 16 CTAs per SM over the decode class's keys.
 static int decode_split_tokens(const RequestClasses &c, double dec_us, double pre_us, int32_t hkv, bool fp8,
-                               bool use_fma)
+                               bool use_fma, int sms)
 {
-    const int sms = num_sms();
     int split = env_int("PKV_SPLIT_TOKENS", 0);
     if (split <= 0) {
         // Decodes beside a longer prefill only fill the SMs its last wave
@@ -529,6 +528,124 @@ static int decode_split_tokens(const RequestClasses &c, double dec_us, double pr
     return split;
 }
 
+// Every host-side decision of one attention call, from the host metadata,
+// the workspace size and the SM count alone (no CUDA call): the request
+// classes, the decode split length, prefill key splits, the workspace
+// layout and the stream arrangement.  attention_impl launches from it and
+// pkv_plan_attention reports it.
+struct AttnPlan {
+    RequestClasses rc;
+    double dec_us = 0.0, pre_us = 0.0;  // rough class times (only the ratio is used)
+    bool use_fma = false;               // CUDA-core kernels instead of the staged MMA ones
+    int split = 0;                      // keys per split, a multiple of the block size
+    int tile = 1;                       // warp-MMA (or CUDA-core) prefill tile, tokens
+    bool pre_split = false;             // warp-MMA prefill tiles split over keys
+    int32_t seen_l = 0;                 // the longest context of the batch
+    size_t ws_front = 0;                // workspace bytes before the quantized-prefill scratch
+    bool has_counters = false;          // the workspace holds in-kernel combine counters
+    size_t part_base = 0;               // byte offset of the split partials
+    size_t total_rows = 0;              // partial rows of all split requests
+    bool fork = false;                  // decode and prefill classes on two streams
+    bool decode_main = false;           // ... the decodes on the caller's stream
+    bool fork_after_scatter = false;    // ... the decodes fork after the ranged scatter
+    int cluster_env = -1;               // PKV_CLUSTER
+};
+
+static int32_t decode_splits_of(const int32_t *qsl_h, const int32_t *sl_h, int32_t r, int32_t window, int sp)
+{
+    return decode_splits(qsl_h[r + 1] - qsl_h[r], sl_h[r], window, sp);
+}
+
+static size_t plan_partial_rows(const AttnPlan &pl, const int32_t *qsl_h, const int32_t *sl_h, int32_t hq,
+                                int32_t window, int sp, bool *too_many)
+{
+    size_t rows = 0;
+    auto add = [&](int32_t r, int32_t S) {
+        if (S > kMaxSplits) *too_many = true;
+        if (S > 1) rows += (size_t)S * (qsl_h[r + 1] - qsl_h[r]) * hq;
+    };
+    for (int32_t r : pl.rc.dec) add(r, decode_splits_of(qsl_h, sl_h, r, window, sp));
+    if (pl.pre_split)
+        for (int32_t r : pl.rc.pre) add(r, sl_h[r] <= 0 ? 1 : (sl_h[r] + sp - 1) / sp);
+    return rows;
+}
+
+static AttnPlan make_plan(const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs, int32_t hq, int32_t hkv,
+                          int32_t d, int32_t bs, int32_t window, bool fp8, bool fused, size_t workspace_bytes, int sms)
+{
+    AttnPlan pl;
+    const int32_t g = hq / hkv;
+    pl.rc = classify_requests(qsl_h, sl_h, num_reqs, g, hkv, d, window, fp8, workspace_bytes);
+    const RequestClasses &rc = pl.rc;
+    for (int r = 0; r < num_reqs; r++) pl.seen_l = sl_h[r] > pl.seen_l ? sl_h[r] : pl.seen_l;
+    class_times(rc, qsl_h, sl_h, hq, hkv, d, &pl.dec_us, &pl.pre_us);
+    pl.use_fma = env_int("PKV_ATTN_CUDA_CORE", 0) != 0;
+    int split = decode_split_tokens(rc, pl.dec_us, pl.pre_us, hkv, fp8, pl.use_fma, sms);
+    if (split % bs) split += bs - split % bs;
+    // Prefill-class tiles are split over keys as well when the batch has too
+    // few of them to fill the GPU (small, latency-bound steps): every tile of
+    // such a request gets the request's number of splits.
+    pl.tile = pl.use_fma ? kDecodeRows / g : (mma_prefill_rows() / g > 0 ? mma_prefill_rows() / g : 1);
+    int64_t pre_ctas = 0;
+    for (int32_t r : rc.pre) pre_ctas += (int64_t)((qsl_h[r + 1] - qsl_h[r] + pl.tile - 1) / pl.tile) * hkv;
+    // Measured on the 48-request engine step it costs more (extra CTAs and a
+    // combine on the critical path) than it saves, so it is opt-in.
+    pl.pre_split = !pl.use_fma && !rc.pre.empty() && pre_ctas < 2 * (int64_t)sms && env_int("PKV_PREFILL_SPLIT", 0);
+    // The layout depends on the workspace size only: [error word][counters,
+    // if the workspace holds them][partials]; quantized prefill on tcgen05:
+    // its scratch takes the workspace's end.
+    pl.ws_front = rc.fp8_scratch ? ((workspace_bytes - rc.fp8_scratch) & ~(size_t)255) : workspace_bytes;
+    pl.has_counters = pl.ws_front >= kErrBytes + kCounterBytes + 64;
+    pl.part_base = kErrBytes + (pl.has_counters ? kCounterBytes : 0);
+    const size_t avail = pl.ws_front - pl.part_base;
+    // every split request keeps S * t * hq partial rows; grow the split until they fit
+    const size_t row_bytes = (size_t)d * 4 + 8;
+    for (;;) {
+        bool too_many = false;
+        const size_t rows = plan_partial_rows(pl, qsl_h, sl_h, hq, window, split, &too_many);
+        if (!too_many && rows * row_bytes + 64 <= avail) break;
+        if (split >= pl.seen_l) break;                          // nothing is split any more
+        split *= 2;
+    }
+    pl.split = split;
+    bool unused = false;
+    pl.total_rows = plan_partial_rows(pl, qsl_h, sl_h, hq, window, split, &unused);
+    // Decode-class work runs on a second stream, concurrently with the
+    // prefill kernels, when both are present; the class expected to take
+    // longer goes on the caller's stream (PKV_DECODE_MAIN=0/1 forces it).
+    pl.fork = !rc.dec.empty() && (!rc.tcp.empty() || !rc.pre.empty()) && !env_int("PKV_NO_OVERLAP", 0);
+    if (pl.fork) {
+        const int forced = env_int("PKV_DECODE_MAIN", -1);
+        pl.decode_main = forced >= 0 ? forced != 0 : pl.dec_us > pl.pre_us;
+        // Combined call with the prefill class on the caller's stream: the
+        // decodes fork after the ranged scatter, as they would after a full
+        // scatter, so that the prefill kernel takes the SMs first (measured
+        // on the mixed 2048-token-chunk step: 514 us this way, 570 us with
+        // the decodes starting at once).
+        pl.fork_after_scatter = fused && !pl.decode_main;
+    }
+    pl.cluster_env = env_int("PKV_CLUSTER", -1);
+    return pl;
+}
+
+// CTAs per thread-block cluster of a decode launch whose requests have at
+// most s_max splits, or 0 for no clusters.  Short split decodes (the
+// slot-ring kernel) run each request's splits as one cluster that combines
+// them through its shared memory: every request of the launch gets the
+// launch's largest split count, its keys divided evenly.  Measured on the
+// 48-request engine step, clusters of more than two CTAs do not run beside
+// the prefill kernel (the step took the sum of both kernels' times), so next
+// to prefill work the cluster holds at most two splits.  PKV_CLUSTER=0
+// turns clusters off, n >= 2 forces n.
+static int decode_cluster_size(const AttnPlan &pl, int s_max)
+{
+    const int cs = pl.cluster_env >= 2 ? std::min(pl.cluster_env, kMaxClusterSplits)
+                                       : (pl.fork ? std::min(s_max, 2) : s_max);
+    return !pl.use_fma && pl.split < kLongSplitTokens && pl.cluster_env != 0 && cs >= 2 && cs <= kMaxClusterSplits
+               ? cs
+               : 0;
+}
+
 static pkv_status attention_impl(void *out, const void *q, const void *k_cache, const void *v_cache,
                                  const float *k_scale, const float *v_scale, const int32_t *query_start_loc,
                                  const int32_t *seq_lens, const int32_t *block_table, int32_t block_table_stride,
@@ -547,64 +664,24 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
         st != PKV_OK || nothing_to_do)
         return st;
     const int32_t g = hq / hkv;
-    RequestClasses rc = classify_requests(qsl_h, sl_h, num_reqs, g, hkv, d, window, fp8, workspace_bytes);
-    std::vector<int32_t> &dec = rc.dec, &pre = rc.pre, &tcp = rc.tcp;
-    const size_t fp8_scratch = rc.fp8_scratch;
-    const int64_t fp8_blocks = rc.fp8_blocks;
-    const int32_t fp8_width = rc.fp8_width;
-    int32_t seen_l = 0;                                  // the longest context of the batch
-    for (int r = 0; r < num_reqs; r++) seen_l = sl_h[r] > seen_l ? sl_h[r] : seen_l;
+    const bool fused = fw_k != nullptr;
+    const AttnPlan pl = make_plan(qsl_h, sl_h, num_reqs, hq, hkv, d, bs, window, fp8, fused, workspace_bytes, num_sms());
+    const std::vector<int32_t> &dec = pl.rc.dec, &pre = pl.rc.pre, &tcp = pl.rc.tcp;
+    const size_t fp8_scratch = pl.rc.fp8_scratch;
+    const int64_t fp8_blocks = pl.rc.fp8_blocks;
+    const int32_t fp8_width = pl.rc.fp8_width;
     if (!tcp.empty() && ((int64_t)num_blocks_total * bs >= INT32_MAX || num_tokens >= INT32_MAX / 2))
         return PKV_ERR_UNSUPPORTED;
-
-    // rough times of the two classes (decode ~ its K/V bytes at HBM speed,
-    // prefill ~ its causal pairs at tensor-core speed; only the ratio matters)
-    double dec_us = 0.0, pre_us = 0.0;
-    class_times(rc, qsl_h, sl_h, hq, hkv, d, &dec_us, &pre_us);
-    const bool use_fma = env_int("PKV_ATTN_CUDA_CORE", 0) != 0;    // CUDA-core kernels instead of the staged MMA ones
-    int split = decode_split_tokens(rc, dec_us, pre_us, hkv, fp8, use_fma);
-    if (split % bs) split += bs - split % bs;
+    const bool use_fma = pl.use_fma;
+    const int split = pl.split;
+    const int tile = pl.tile;
+    const bool pre_split = pl.pre_split;
+    const bool has_counters = pl.has_counters;
+    const size_t ws_front = pl.ws_front, part_base = pl.part_base;
     // prefill tiles: every tile of a split request gets ceil(L / split) splits;
     // decode-class requests: splits over their (windowed) key range
     auto splits_of = [&](int32_t L, int sp) { return L <= 0 ? 1 : (L + sp - 1) / sp; };
-    auto dec_splits_of = [&](int32_t r, int sp) { return decode_splits(qsl_h[r + 1] - qsl_h[r], sl_h[r], window, sp); };
-    // Prefill-class tiles are split over keys as well when the batch has too
-    // few of them to fill the GPU (small, latency-bound steps): every tile of
-    // such a request gets the request's number of splits.
-    const int tile = use_fma ? kDecodeRows / g : (mma_prefill_rows() / g > 0 ? mma_prefill_rows() / g : 1);
-    int64_t pre_ctas = 0;
-    for (int32_t r : pre) pre_ctas += (int64_t)((qsl_h[r + 1] - qsl_h[r] + tile - 1) / tile) * hkv;
-    // Measured on the 48-request engine step it costs more (extra CTAs and a
-    // combine on the critical path) than it saves, so it is opt-in.
-    const bool pre_split =
-        !use_fma && !pre.empty() && pre_ctas < 2 * (int64_t)num_sms() && env_int("PKV_PREFILL_SPLIT", 0);
-    // every split request keeps S * t * hq partial rows; grow the split until they fit
-    auto partial_rows = [&](int sp, bool *too_many) {
-        size_t rows = 0;
-        auto add = [&](int32_t r, int32_t S) {
-            if (S > kMaxSplits) *too_many = true;
-            if (S > 1) rows += (size_t)S * (qsl_h[r + 1] - qsl_h[r]) * hq;
-        };
-        for (int32_t r : dec) add(r, dec_splits_of(r, sp));
-        if (pre_split)
-            for (int32_t r : pre) add(r, splits_of(sl_h[r], sp));
-        return rows;
-    };
-    const size_t row_bytes = (size_t)d * 4 + 8;
-    // The layout depends on the workspace size only: [error word][counters,
-    // if the workspace holds them][partials].
-    // quantized prefill on tcgen05: its scratch takes the workspace's end
-    const size_t ws_front = fp8_scratch ? ((workspace_bytes - fp8_scratch) & ~(size_t)255) : workspace_bytes;
-    const bool has_counters = ws_front >= kErrBytes + kCounterBytes + 64;
-    const size_t part_base = kErrBytes + (has_counters ? kCounterBytes : 0);
-    const size_t avail = ws_front - part_base;
-    for (;;) {
-        bool too_many = false;
-        const size_t rows = partial_rows(split, &too_many);
-        if (!too_many && rows * row_bytes + 64 <= avail) break;
-        if (split >= seen_l) break;                              // nothing is split any more
-        split *= 2;
-    }
+    auto dec_splits_of = [&](int32_t r, int sp) { return decode_splits_of(qsl_h, sl_h, r, window, sp); };
 
     const int64_t num_slots = (int64_t)num_blocks_total * bs;
     char *ws = static_cast<char *>(workspace);
@@ -626,15 +703,13 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
     p.scale_log2 = sc * 1.4426950408889634f;
     p.err = reinterpret_cast<uint32_t *>(ws);
     // partial rows: first all o rows, then the (m, l) pairs
-    bool unused = false;
-    const size_t total_rows = partial_rows(split, &unused);
+    const size_t total_rows = pl.total_rows;
     p.part_o = reinterpret_cast<float *>(ws + part_base);
     p.part_ml = reinterpret_cast<float2 *>(ws + part_base + ((total_rows * d * 4 + 15) / 16) * 16);
     p.counters = has_counters ? reinterpret_cast<uint32_t *>(ws + kErrBytes) : nullptr;
     p.window = window;
     p.k_scale = k_scale;
     p.v_scale = v_scale;
-    const bool fused = fw_k != nullptr;
     p.fw_k = static_cast<const uint4 *>(fw_k);
     p.fw_v = static_cast<const uint4 *>(fw_v);
     p.fw_kc = fused ? static_cast<uint4 *>(const_cast<void *>(k_cache)) : nullptr;
@@ -655,8 +730,8 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
     // capture) is preserved.
     cudaStream_t dstream = stream, pstream = stream;         // decode-class / prefill-class work
     SideStream *side = nullptr;
-    const bool fork = !dec.empty() && (!tcp.empty() || !pre.empty()) && !env_int("PKV_NO_OVERLAP", 0);
-    bool fork_after_scatter = false;
+    const bool fork = pl.fork;
+    const bool fork_after_scatter = pl.fork_after_scatter;
     if (fork) {
         side = side_stream();
         if (!side) return cuda_fail(cudaErrorUnknown, "side stream");
@@ -664,18 +739,8 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
         // The class on the caller's stream follows the K/V scatter as a
         // programmatic dependent (it starts while the scatter drains); the
         // other one waits for the fork event.
-        // The class expected to take longer (dec_us, pre_us above) goes on the
-        // caller's stream.  PKV_DECODE_MAIN=0/1 forces the choice.
-        const int forced = env_int("PKV_DECODE_MAIN", -1);
-        const bool decode_main = forced >= 0 ? forced != 0 : dec_us > pre_us;
-        if (decode_main) pstream = side->stream;
+        if (pl.decode_main) pstream = side->stream;
         else dstream = side->stream;
-        // Combined call with the prefill class on the caller's stream: the
-        // decodes fork after the ranged scatter, as they would after a full
-        // scatter, so that the prefill kernel takes the SMs first (measured
-        // on the mixed 2048-token-chunk step: 514 us this way, 570 us with
-        // the decodes starting at once).
-        fork_after_scatter = fused && !decode_main;
         if (!fork_after_scatter) {
             cudaError_t e = cudaEventRecord(side->fork, stream);
             if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
@@ -848,15 +913,6 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
         }
         return cudaSuccess;
     };
-    // Short split decodes (the slot-ring kernel) run each request's splits as
-    // one thread-block cluster that combines them through its shared memory:
-    // every request of the launch gets the launch's largest split count, its
-    // keys divided evenly.  Measured on the 48-request engine step, clusters
-    // of more than two CTAs do not run beside the prefill kernel (the step
-    // took the sum of both kernels' times), so next to prefill work the
-    // cluster holds at most two splits.  PKV_CLUSTER=0 turns clusters off,
-    // n >= 2 forces n.
-    const int cluster_env = env_int("PKV_CLUSTER", -1);
     for (size_t c0 = 0; c0 < dec.size(); c0 += kPlanMax) {
         WorkList wl;
         memset(&wl, 0, sizeof wl);
@@ -867,8 +923,8 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
         size_t c1 = c0 + kPlanMax < dec.size() ? c0 + kPlanMax : dec.size();
         int s_max = 1;
         for (size_t x = c0; x < c1; x++) s_max = std::max(s_max, dec_splits_of(dec[x], split));
-        const int cs = cluster_env >= 2 ? std::min(cluster_env, kMaxClusterSplits) : (fork ? std::min(s_max, 2) : s_max);
-        if (!use_fma && split < kLongSplitTokens && cluster_env != 0 && cs >= 2 && cs <= kMaxClusterSplits) {
+        const int cs = decode_cluster_size(pl, s_max);
+        if (cs) {
             wl.cluster = cs;
             for (size_t x = c0; x < c1; x++) {
                 const int32_t r = dec[x], t = qsl_h[r + 1] - qsl_h[r];
@@ -977,6 +1033,52 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
     return attention_impl(out, q, k_cache, v_cache, nullptr, nullptr, query_start_loc, seq_lens, block_table,
                           block_table_stride, qsl_h, sl_h, num_reqs, num_tokens, max_query_len, max_seq_len, hq, hkv,
                           d, bs, num_blocks_total, scale, window, workspace, workspace_bytes, stream);
+}
+
+pkv_status pkv_plan_attention(const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs, int32_t hq, int32_t hkv,
+                              int32_t d, int32_t bs, int32_t window, int32_t quantized, int32_t combined,
+                              size_t workspace_bytes, int32_t sms, pkv_attention_plan *out)
+{
+    if (!out || !qsl_h || num_reqs < 0 || (num_reqs > 0 && !sl_h)) return PKV_ERR_INVALID_ARG;
+    if (hq <= 0 || hkv <= 0 || hq % hkv || d <= 0 || bs <= 0 || window < 0) return PKV_ERR_INVALID_ARG;
+    for (int r = 0; r < num_reqs; r++) {
+        const int32_t t = qsl_h[r + 1] - qsl_h[r], L = sl_h[r];
+        if (t < 0 || L < 0 || (L > 0 && t > L)) return PKV_ERR_INVALID_ARG;
+    }
+    const int32_t g = hq / hkv;
+    if ((d != 48 && d != 64 && d != 128) || bs != 16 || g > kDecodeRows) return PKV_ERR_UNSUPPORTED;
+    if (quantized && (d != 128 || hkv % 4 != 0 || env_int("PKV_ATTN_CUDA_CORE", 0))) return PKV_ERR_UNSUPPORTED;
+    if (sms <= 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+            (void)cudaGetLastError();
+            return PKV_ERR_CUDA;
+        }
+    }
+    const AttnPlan pl = make_plan(qsl_h, sl_h, num_reqs, hq, hkv, d, bs, window, quantized != 0, combined != 0,
+                                  workspace_bytes, sms);
+    memset(out, 0, sizeof *out);
+    out->decode_requests = (int32_t)pl.rc.dec.size();
+    out->prefill_tensor_requests = (int32_t)pl.rc.tcp.size();
+    out->prefill_mma_requests = (int32_t)pl.rc.pre.size();
+    out->decode_split_tokens = pl.split;
+    int s_max = 1, s_first = 1;
+    for (size_t x = 0; x < pl.rc.dec.size(); x++) {
+        const int S = decode_splits_of(qsl_h, sl_h, pl.rc.dec[x], window, pl.split);
+        s_max = std::max(s_max, S);
+        if (x < (size_t)kPlanMax) s_first = std::max(s_first, S);
+    }
+    out->max_decode_splits = pl.rc.dec.empty() ? 0 : s_max;
+    out->decode_cluster = pl.rc.dec.empty() ? 0 : decode_cluster_size(pl, s_first);
+    out->decode_streaming = !pl.rc.dec.empty() && !pl.use_fma && out->decode_cluster == 0 && pl.split >= kLongSplitTokens;
+    out->split_counters = pl.has_counters;
+    out->overlap = pl.fork;
+    out->decode_on_caller_stream = pl.fork && pl.decode_main;
+    out->prefill_key_splits = pl.pre_split;
+    out->quantized_prefill_scratch = pl.rc.fp8_scratch;
+    out->partial_bytes = pl.total_rows ? ((pl.total_rows * d * 4 + 15) / 16) * 16 + pl.total_rows * 8 : 0;
+    return PKV_OK;
 }
 
 pkv_status pkv_paged_kv_write_attention(const void *k, const void *v, void *k_cache, void *v_cache,

@@ -1,0 +1,192 @@
+"""The attention planner's decisions on a host without a GPU
+(pkv_plan_attention, include/pkv.h), for the five workload shapes and the
+rules the header states: request classes, one decode split length (about 16
+CTAs per SM over the decode keys, 4 beside a longer prefill, at least 256
+keys, a multiple of 128, at most 32 streaming splits per request, doubled
+until the split partials fit the workspace), short splits merged in
+thread-block clusters (at most two beside prefill work), long ones on the
+streaming kernel, and the two-stream overlap of the decode and prefill
+classes of one flattened ragged batch ("31. Engine v2", "Flattened ragged
+batches").  The expected split lengths restate those rules here."""
+import math
+
+import pytest
+
+import paged_kv_cache_84_gb300 as pkv
+from workloads import config_spec
+
+SMS = 152
+BIG_WS = 1 << 30
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from paged_kv_cache_84_gb300 import build
+    build.build()
+    pkv.load()
+
+
+@pytest.fixture(autouse=True)
+def _no_switches(monkeypatch):
+    for name in ("PKV_ATTN_CUDA_CORE", "PKV_DISABLE_TCGEN05", "PKV_TC_MIN_ROWS", "PKV_FP8_PREFILL_TC",
+                 "PKV_SPLIT_TOKENS", "PKV_CLUSTER", "PKV_DECODE_MAIN", "PKV_NO_OVERLAP", "PKV_PREFILL_SPLIT"):
+        monkeypatch.delenv(name, raising=False)
+
+
+def meta(cfg):
+    spec = config_spec(cfg)
+    qsl = [0]
+    for r in spec.reqs:
+        qsl.append(qsl[-1] + r.new)
+    return spec, qsl, [r.seq_len for r in spec.reqs]
+
+
+def plan(cfg, **kw):
+    spec, qsl, sl = meta(cfg)
+    kw.setdefault("num_sms", SMS)
+    kw.setdefault("workspace_bytes", BIG_WS)
+    return pkv.plan_attention(qsl, sl, spec.num_q_heads, spec.num_kv_heads, spec.head_dim, **kw)
+
+
+def rule_split(keys, head_ctas, ctas_per_sm, sms=SMS, max_keys=0):
+    """The documented split rule, restated: keys x KV-head CTAs spread over
+    ctas_per_sm CTAs per SM, at least 256, rounded up to 128; a streaming
+    split (>= 512 keys) is long enough for at most 32 splits per request."""
+    s = max(256, math.ceil(keys * head_ctas / (sms * ctas_per_sm)))
+    s = -(-s // 128) * 128
+    if s >= 512:
+        s = max(s, -(-math.ceil(max_keys / 32) // 128) * 128)
+    return s
+
+
+def test_layout_example_is_all_decode():
+    p = plan(1)
+    assert (p["decode_requests"], p["prefill_tensor_requests"], p["prefill_mma_requests"]) == (4, 0, 0)
+    assert p["decode_split_tokens"] == 256 and p["max_decode_splits"] == 1
+    assert p["decode_cluster"] == 0 and not p["decode_streaming"] and not p["overlap"]
+    assert p["partial_bytes"] == 0
+
+
+def test_long_decode_streams_ten_splits_per_request():
+    spec, qsl, sl = meta(5)
+    p = plan(5)
+    split = rule_split(sum(sl), spec.num_kv_heads, 16, max_keys=max(sl))
+    assert p["decode_split_tokens"] == split == 3456
+    assert p["max_decode_splits"] == math.ceil(32768 / split) == 10
+    assert p["decode_streaming"] and p["decode_cluster"] == 0 and p["split_counters"]
+    rows = 32 * 10 * spec.num_q_heads                 # S x t x hq partial rows per request
+    assert p["partial_bytes"] == rows * spec.head_dim * 4 + rows * 8
+
+
+def test_split_grows_until_the_partials_fit():
+    spec, qsl, sl = meta(5)
+    base = plan(5)["decode_split_tokens"]
+    p = plan(5, workspace_bytes=4 << 20)
+    assert p["partial_bytes"] <= 4 << 20
+    assert p["decode_split_tokens"] in [base << k for k in range(1, 6)]
+    assert p["max_decode_splits"] == math.ceil(32768 / p["decode_split_tokens"]) == 3
+    # a workspace too small for any partial: nothing is split, no counters
+    q = plan(5, workspace_bytes=pkv.WORKSPACE_MIN_BYTES)
+    assert q["max_decode_splits"] == 1 and q["partial_bytes"] == 0 and not q["split_counters"]
+
+
+def test_decode_batch_uses_sixteen_ctas_per_sm():
+    spec, qsl, sl = meta(3)
+    p = plan(3)
+    split = rule_split(sum(sl), spec.num_kv_heads, 16, max_keys=max(sl))
+    assert p["decode_split_tokens"] == split
+    assert p["max_decode_splits"] == math.ceil(max(sl) / split)
+    assert p["decode_requests"] == 256 and not p["overlap"]
+    assert p["decode_streaming"] == (split >= 512)
+    # half the SMs: about twice the keys per split
+    h = plan(3, num_sms=SMS // 2)
+    assert h["decode_split_tokens"] == rule_split(sum(sl), spec.num_kv_heads, 16, sms=SMS // 2, max_keys=max(sl))
+    assert h["decode_split_tokens"] > split
+
+
+def test_engine_step_overlaps_classes_with_clusters_of_two():
+    spec, qsl, sl = meta(2)
+    p = plan(2, combined=True)
+    assert (p["decode_requests"], p["prefill_tensor_requests"], p["prefill_mma_requests"]) == (32, 16, 0)
+    assert p["overlap"] and p["decode_on_caller_stream"]     # the decodes' K/V bytes outweigh the chunks
+    assert p["decode_split_tokens"] == 256
+    assert p["max_decode_splits"] >= 2 and p["decode_cluster"] == 2 and not p["decode_streaming"]
+    assert p["partial_bytes"] > 0                               # reserved, although clusters merge on chip
+
+
+def test_decodes_beside_a_long_prefill_take_longer_splits():
+    spec, qsl, sl = meta(4)
+    p = plan(4, combined=True)
+    assert (p["decode_requests"], p["prefill_tensor_requests"]) == (64, 3)
+    assert p["overlap"] and not p["decode_on_caller_stream"]   # the 2048-token chunk at 16384 dominates
+    dec = [L for L, a, b in zip(sl, qsl, qsl[1:]) if b - a == 1]
+    assert p["decode_split_tokens"] == rule_split(sum(dec), spec.num_kv_heads, 4, max_keys=max(dec))
+    # the same decodes alone spread over 16 CTAs per SM
+    alone_qsl = list(range(len(dec) + 1))
+    a = pkv.plan_attention(alone_qsl, dec, 32, 8, 128, workspace_bytes=BIG_WS, num_sms=SMS)
+    assert a["decode_split_tokens"] == rule_split(sum(dec), 8, 16, max_keys=max(dec))
+    assert p["decode_split_tokens"] >= 3 * a["decode_split_tokens"]
+
+
+def test_switches(monkeypatch):
+    monkeypatch.setenv("PKV_NO_OVERLAP", "1")
+    assert not plan(2)["overlap"]
+    monkeypatch.delenv("PKV_NO_OVERLAP")
+    monkeypatch.setenv("PKV_DECODE_MAIN", "0")
+    p = plan(2)
+    assert p["overlap"] and not p["decode_on_caller_stream"]
+    monkeypatch.delenv("PKV_DECODE_MAIN")
+    monkeypatch.setenv("PKV_CLUSTER", "0")
+    assert plan(2)["decode_cluster"] == 0
+    monkeypatch.setenv("PKV_CLUSTER", "4")
+    assert plan(2)["decode_cluster"] == 4
+    monkeypatch.delenv("PKV_CLUSTER")
+    monkeypatch.setenv("PKV_SPLIT_TOKENS", "512")
+    p = plan(3)
+    assert p["decode_split_tokens"] == 512 and p["decode_streaming"]
+    monkeypatch.delenv("PKV_SPLIT_TOKENS")
+    monkeypatch.setenv("PKV_DISABLE_TCGEN05", "1")
+    p = plan(2)
+    assert p["prefill_tensor_requests"] == 0 and p["prefill_mma_requests"] == 16
+
+
+def test_quantized_prefill_on_tcgen05_needs_the_scratch():
+    spec, qsl, sl = meta(4)
+    ws = 8 << 20
+    extra = pkv.fp8_prefill_scratch_bytes(qsl, sl, 32, 8, 128)
+    assert extra > ws
+    p = plan(4, quantized=True, workspace_bytes=ws)
+    assert p["prefill_tensor_requests"] == 0 and p["prefill_mma_requests"] == 3
+    assert p["quantized_prefill_scratch"] == 0
+    q = plan(4, quantized=True, workspace_bytes=ws + extra)
+    assert q["prefill_tensor_requests"] == 3 and q["prefill_mma_requests"] == 0
+    assert q["quantized_prefill_scratch"] == extra
+    # two KV heads per streaming CTA: half the CTAs per split than bf16
+    dec = [L for L, a, b in zip(sl, qsl, qsl[1:]) if b - a == 1]
+    assert q["decode_split_tokens"] == rule_split(sum(dec), 8 // 2, 4, max_keys=max(dec))
+
+
+def test_sliding_window_limits_the_decode_keys():
+    p = plan(5, window=4096)
+    keys = 32 * 4096
+    split = rule_split(keys, 8, 16, max_keys=4096)
+    assert p["decode_split_tokens"] == split == 512
+    assert p["max_decode_splits"] == 4096 // split
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(num_q_heads=8, num_kv_heads=3), 1),           # heads do not group
+    (dict(seq_lens=[2]), 1),                            # t > seq_len
+    (dict(window=-1), 1),
+    (dict(block_size=32), 2),
+    (dict(head_dim=96), 2),
+    (dict(quantized=True), 2),                          # quantized pools need head_dim 128
+])
+def test_rejections(args, status):
+    kw = dict(query_start_loc_host=[0, 3], seq_lens=[9], num_q_heads=8, num_kv_heads=4, head_dim=64)
+    kw.update(args)
+    qsl, sl = kw.pop("query_start_loc_host"), kw.pop("seq_lens")
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.plan_attention(qsl, sl, kw.pop("num_q_heads"), kw.pop("num_kv_heads"), kw.pop("head_dim"),
+                           num_sms=SMS, **kw)
+    assert e.value.status == status
