@@ -241,7 +241,7 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q,
  * receives a new row belongs to a block that no other request of the batch
  * reads (a block still being filled has one owner; blocks shared by prefix
  * caching are full).  Another request's CTAs may read such a block before
- * its new rows are written, so a batch that breaks this gets the old rows.
+ * its new rows are written, so a batch that breaks this may see old rows.
  * Device errors of the write (PKV_DEVERR_SLOT) go to the workspace's error
  * word with the attention's.  Return codes as the two calls; nothing is
  * enqueued when the arguments are rejected.  With PKV_ATTN_CUDA_CORE=1 (or
