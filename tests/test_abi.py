@@ -167,3 +167,24 @@ def test_fp8_prefill_scratch_bytes_on_host(lib):
     assert call([0, 1, 2], [77, 500], 32, 8, 128) == 0      # decodes only
     assert call(qsl, sl, 32, 8, 48) == 0                    # head dim 48: no tcgen05 path for codes
     assert call(qsl, sl, 24, 8, 128) == 0                   # g = 3 does not divide 128
+
+
+def test_noalloc_scratch_limit_on_host(lib):
+    """pkv_ragged_paged_attention_noalloc refuses, on the host and before any
+    CUDA call, a batch whose workspace would exceed its static scratch."""
+    fn = lib.pkv_ragged_paged_attention_noalloc
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_void_p] * 7 + [ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p] + \
+        [ctypes.c_int32] * 10 + [ctypes.c_float, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
+    lib.pkv_attention_workspace_bytes.restype = ctypes.c_size_t
+    lib.pkv_attention_workspace_bytes.argtypes = [ctypes.c_int32] * 5
+    scratch = 8 << 20                                      # PKV_NOALLOC_SCRATCH_BYTES
+    assert re.search(r"#define PKV_NOALLOC_SCRATCH_BYTES \(8u << 20\)", open(HEADER).read())
+    big_len = 1 << 20
+    assert lib.pkv_attention_workspace_bytes(2, 4096, 8, 64, big_len) > scratch
+    fake = ctypes.c_void_p(1 << 20)                        # never dereferenced: the size check comes first
+    qsl = (ctypes.c_int32 * 3)(0, 4095, 4096)
+    sl = (ctypes.c_int32 * 2)(8192, big_len)
+    st = fn(fake, fake, fake, fake, fake, fake, fake, big_len // 16, qsl, sl,
+            2, 4096, 4095, big_len, 8, 4, 64, 16, big_len // 16 + 1, ctypes.c_float(0.125), 0, None, None)
+    assert st == 3                                         # PKV_ERR_WORKSPACE
