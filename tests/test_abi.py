@@ -175,7 +175,7 @@ def test_noalloc_scratch_limit_on_host(lib):
     fn = lib.pkv_ragged_paged_attention_noalloc
     fn.restype = ctypes.c_int
     fn.argtypes = [ctypes.c_void_p] * 7 + [ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p] + \
-        [ctypes.c_int32] * 10 + [ctypes.c_float, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
+        [ctypes.c_int32] * 9 + [ctypes.c_float, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
     lib.pkv_attention_workspace_bytes.restype = ctypes.c_size_t
     lib.pkv_attention_workspace_bytes.argtypes = [ctypes.c_int32] * 5
     scratch = 8 << 20                                      # PKV_NOALLOC_SCRATCH_BYTES
