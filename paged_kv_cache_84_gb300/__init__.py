@@ -146,6 +146,15 @@ def _host_i32(x, name):
     return t.contiguous()
 
 
+def _check_meta(query_start_loc, seq_lens, block_table, num_reqs):
+    """Device metadata with room for every request (the kernels index it by
+    request; the library sees only pointers)."""
+    if block_table.dim() != 2 or block_table.shape[0] < num_reqs:
+        raise ValueError("block_table must be [num_reqs, width]")
+    if query_start_loc.numel() < num_reqs + 1 or seq_lens.numel() < num_reqs:
+        raise ValueError("query_start_loc and seq_lens need num_reqs + 1 and num_reqs entries")
+
+
 def profile_start(capacity: int = 4096):
     """Time each library kernel launch with CUDA events on its stream (diagnostics)."""
     _check(load().pkv_profile_start(capacity), "profile_start")
@@ -240,8 +249,7 @@ def ragged_paged_attention(out, q, k_cache, v_cache, query_start_loc, seq_lens, 
     sl_h = _host_i32(seq_lens_host, "seq_lens_host")
     if qsl_h.numel() != sl_h.numel() + 1:
         raise ValueError("query_start_loc needs num_reqs + 1 entries")
-    if block_table.dim() != 2:
-        raise ValueError("block_table must be [num_reqs, width]")
+    _check_meta(query_start_loc, seq_lens, block_table, sl_h.numel())
     st = L.pkv_ragged_paged_attention(
         _dev(out, "out", torch.bfloat16), _dev(q, "q", torch.bfloat16),
         _dev(k_cache, "k_cache", torch.bfloat16), _dev(v_cache, "v_cache", torch.bfloat16),
@@ -269,8 +277,7 @@ def paged_kv_write_attention(k, v, k_cache, v_cache, slot_mapping, out, q, query
     sl_h = _host_i32(seq_lens_host, "seq_lens_host")
     if qsl_h.numel() != sl_h.numel() + 1:
         raise ValueError("query_start_loc needs num_reqs + 1 entries")
-    if block_table.dim() != 2:
-        raise ValueError("block_table must be [num_reqs, width]")
+    _check_meta(query_start_loc, seq_lens, block_table, sl_h.numel())
     st = L.pkv_paged_kv_write_attention(
         _dev(k, "k", torch.bfloat16), _dev(v, "v", torch.bfloat16),
         _dev(k_cache, "k_cache", torch.bfloat16), _dev(v_cache, "v_cache", torch.bfloat16),
@@ -379,6 +386,7 @@ def paged_kv_write_attention_fp8(k, v, k_codes, v_codes, k_scale, v_scale, slot_
     sl_h = _host_i32(seq_lens_host, "seq_lens_host")
     if qsl_h.numel() != sl_h.numel() + 1:
         raise ValueError("query_start_loc needs num_reqs + 1 entries")
+    _check_meta(query_start_loc, seq_lens, block_table, sl_h.numel())
     st = L.pkv_paged_kv_write_attention_fp8(
         _dev(k, "k", torch.bfloat16), _dev(v, "v", torch.bfloat16),
         _dev(k_codes, "k_codes", torch.uint8), _dev(v_codes, "v_codes", torch.uint8),
@@ -441,6 +449,7 @@ def ragged_paged_attention_fp8(out, q, k_codes, v_codes, k_scale, v_scale, query
     sl_h = _host_i32(seq_lens_host, "seq_lens_host")
     if qsl_h.numel() != sl_h.numel() + 1:
         raise ValueError("query_start_loc needs num_reqs + 1 entries")
+    _check_meta(query_start_loc, seq_lens, block_table, sl_h.numel())
     st = L.pkv_ragged_paged_attention_fp8(
         _dev(out, "out", torch.bfloat16), _dev(q, "q", torch.bfloat16),
         _dev(k_codes, "k_codes", torch.uint8), _dev(v_codes, "v_codes", torch.uint8),

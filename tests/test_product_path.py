@@ -40,3 +40,36 @@ def test_binding_and_library_do_not_reach_the_oracle():
             assert not any("oracle" in inc for inc in includes), f"{f} includes the oracle"
             text = re.sub(r"/\*.*?\*/|//[^\n]*|#[^\n]*|\"\"\".*?\"\"\"", "", text, flags=re.S)
             assert not re.search(r"\boracle\b", text), f"{f} refers to the oracle"
+
+
+def test_binding_checks_device_metadata_sizes():
+    """The library sees only pointers, so the binding checks that the device
+    metadata has an entry for every request before anything is passed on
+    (here with host tensors: the size check comes before the device check)."""
+    import torch
+
+    import paged_kv_cache_84_gb300 as pkv
+    from paged_kv_cache_84_gb300 import build
+    build.build()
+    q = torch.zeros(4, 8, 64, dtype=torch.bfloat16)
+    pool = torch.zeros(9, 16, 4, 64, dtype=torch.bfloat16)
+    ws = torch.zeros(1 << 16, dtype=torch.uint8)
+    qsl_h, sl_h = [0, 3, 4], [9, 42]
+    good = dict(qsl=torch.tensor(qsl_h, dtype=torch.int32), sl=torch.tensor(sl_h, dtype=torch.int32),
+                bt=torch.zeros(2, 3, dtype=torch.int32))
+    bad = [dict(good, bt=torch.zeros(1, 3, dtype=torch.int32)),      # one table row for two requests
+           dict(good, bt=torch.zeros(6, dtype=torch.int32)),         # not [num_reqs, width]
+           dict(good, qsl=torch.tensor([0, 3], dtype=torch.int32)),  # query_start_loc too short
+           dict(good, sl=torch.tensor([9], dtype=torch.int32))]      # seq_lens too short
+    for m in bad:
+        with pytest.raises(ValueError):
+            pkv.ragged_paged_attention(torch.empty_like(q), q, pool, pool, m["qsl"], m["sl"], m["bt"],
+                                       qsl_h, sl_h, 3, 42, 0.125, ws)
+        with pytest.raises(ValueError):
+            pkv.paged_kv_write_attention(torch.zeros(4, 4, 64, dtype=torch.bfloat16),
+                                         torch.zeros(4, 4, 64, dtype=torch.bfloat16), pool, pool,
+                                         torch.zeros(4, dtype=torch.int64), torch.empty_like(q), q,
+                                         m["qsl"], m["sl"], m["bt"], qsl_h, sl_h, 3, 42, 0.125, ws)
+    with pytest.raises(TypeError):                                   # sizes fine: host tensors refused
+        pkv.ragged_paged_attention(torch.empty_like(q), q, pool, pool, good["qsl"], good["sl"], good["bt"],
+                                   qsl_h, sl_h, 3, 42, 0.125, ws)
