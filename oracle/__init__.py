@@ -16,6 +16,9 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
+# A prebuilt oracle library to load instead (the mutation test points this
+# at deliberately broken copies to show that the pins catch them).
+_OVERRIDE = os.environ.get("PKV_ORACLE_LIB")
 _lib = None
 
 c_i32, c_i64, c_dbl, c_p = ctypes.c_int32, ctypes.c_int64, ctypes.c_double, ctypes.c_void_p
@@ -23,6 +26,8 @@ c_i32, c_i64, c_dbl, c_p = ctypes.c_int32, ctypes.c_int64, ctypes.c_double, ctyp
 
 def build(force: bool = False) -> str:
     """Compile ``oracle.c`` with gcc (plain -O2, OpenMP, no fast-math)."""
+    if _OVERRIDE:
+        return _OVERRIDE
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
         subprocess.check_call(["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared",
@@ -34,8 +39,7 @@ def build(force: bool = False) -> str:
 def lib():
     global _lib
     if _lib is None:
-        build()
-        L = ctypes.CDLL(_LIB)
+        L = ctypes.CDLL(build())
         L.oracle_slot.restype = c_i64
         L.oracle_slot.argtypes = [c_p, c_i64, c_i32]
         L.oracle_paged_kv_write.restype = ctypes.c_int
