@@ -87,3 +87,28 @@ def test_reference_arm_under_torchrun_two_ranks():
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
     assert line["config"]["workload"] == "layout-example-N9"
+
+
+def test_reference_arm_line_carries_the_contract_keys():
+    """One process: the reference arm's JSON line has every key of the
+    benchmark contract, its e2e moves no bytes, and its value is tokens over
+    the measured step time."""
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--steps", "2", "--warmup", "0", "--workload", "1"]
+    env = dict(os.environ, OMP_NUM_THREADS="2")
+    res = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300, env=env)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [ln for ln in res.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 2 and d["warmup"] >= 3
+    assert d["higher_is_better"] is True and d["unit"] == "query tokens/s"
+    assert d["value"] == pytest.approx(9 / (d["ms_per_step"] * 1e-3))           # 9 query tokens per step
+    assert d["config"]["workload"] == "layout-example-N9"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    e = d["e2e"]
+    assert e["value"] == d["value"] and e["unit"] == d["unit"]
+    assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
