@@ -119,3 +119,23 @@ def test_stored_traffic_only_while_sources_unchanged(tmp_path, monkeypatch):
     assert bench.stored_traffic("attn_mma_decode", "cfg4") is None             # its source file is absent
     (csrc / "common.cuh").write_text("common, edited\n")
     assert bench.stored_traffic("attn_tc_prefill", "cfg4") is None             # stale once a source changes
+
+
+def test_clock_summary_of_the_timed_region():
+    """The clocks line: median SM clock and the throttle reasons seen inside
+    the timed region (samples just outside it are ignored)."""
+    s = bench.ClockSampler(0)
+
+    def row(sm, reason_hw="Not Active", power="150.5"):
+        return ["0", str(sm), "2070", power, "0x0", reason_hw, "Not Active", "Not Active", "Not Active"]
+
+    s.samples = [(9.0, row(1000, "Active")),                       # before the timed region
+                 (10.0, row(2070)), (10.1, row(2055, power="300.0")), (10.2, row(2070)),
+                 (12.0, row(900, "Active"))]                       # after it
+    out = s.summary(10.0, 10.2)
+    assert out["sm_mhz"] == 2070 and out["sm_max_mhz"] == 2070 and out["samples"] == 3
+    assert out["reasons"] == [] and out["power_w_max"] == 300.0 and out["window"] == "timed region"
+    s.samples.append((10.15, row(1500, "Active")))
+    assert s.summary(10.0, 10.2)["reasons"] == ["hw_slowdown"]
+    # a timed region shorter than the sampling interval falls back to every sample
+    assert s.summary(20.0, 20.01)["window"].startswith("whole GPU phase")
