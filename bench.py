@@ -9,10 +9,15 @@ launches).  Inputs are resident in HBM when the timed region starts.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload 1..5] [--no-breakdown]
 
-Prints ONE JSON line on rank 0.  The headline workload is the 48-request
-engine step with a shared system prompt; the other four workloads are
-measured too and reported under "workloads".  `--impl reference` times the
-CPU oracle (the only reference there is) on the host cores.
+Prints ONE JSON line on rank 0.  The headline workload is the largest one
+that fits one GPU and the only full-size step with both kernel classes: the
+mixed step of a 2048-token prefill chunk at position 16384, two fresh
+1024-token prompts and 64 decodes.  The other four workloads are measured
+too and reported under "workloads", each with its own kernel roofline, CPU
+oracle baseline and end-to-end number.  `--impl reference` times the CPU
+oracle (the only reference there is) on the host cores.  `--gpus N` without
+torchrun's environment re-launches itself under torch.distributed.run with
+N ranks (one independent replica per GPU).
 """
 from __future__ import annotations
 
@@ -33,11 +38,11 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from workloads import CONFIG_NAMES, config_spec, fill_normal_bf16, make_batch, subset_spec  # noqa: E402
+from workloads import Batch, CONFIG_NAMES, config_spec, fill_normal_bf16, make_batch, subset_spec  # noqa: E402
 
 METRIC = "ragged paged-attn step µs + KV-read HBM GB/s vs 8 TB/s; query tokens/s"
 UNIT = "query tokens/s"
-HEADLINE = 2
+HEADLINE = 4
 L2_BYTES = 129 * 1024 * 1024
 NOMINAL_HBM_GBS = 8000.0
 SM_COUNT = 152
@@ -461,20 +466,47 @@ def time_workload(pkv, cfg, steps, warmup, device, peaks, dist=None, use_graph=T
         torch.cuda.synchronize()
         per_replay_ms = ev0.elapsed_time(ev1) / n
 
-    # ---- per-kernel durations: eager steps with events around every launch.
-    # Kernels that overlap on a side stream in the timed region run one after
-    # another here, so that each event pair times one kernel alone.
-    prof_steps = max(3, min(steps, 50))
-    saved = os.environ.get("PKV_NO_OVERLAP")
-    os.environ["PKV_NO_OVERLAP"] = "1"
-    pkv.profile_start(prof_steps * launches_per_step + 16)
-    for i in range(prof_steps):
-        copies[i % len(copies)].run()
-    recs = pkv.profile_stop()
-    if saved is None:
-        os.environ.pop("PKV_NO_OVERLAP", None)
+    # ---- per-kernel durations: CUDA events around every library launch,
+    # recorded as event nodes of a second graph of the same `steps` steps
+    # (the step as timed above: overlapped classes, rotated copies), read
+    # after that graph has run once.  Event nodes sit between the kernels,
+    # so each event pair spans its kernel alone; the per-launch eager
+    # events used when capture is unavailable add the launch overhead.
+    recs, kernel_timing = None, None
+    if use_graph:
+        try:
+            pkv.profile_start(steps * launches_per_step + 16)
+            side3 = torch.cuda.Stream()
+            side3.wait_stream(stream)
+            gp = torch.cuda.CUDAGraph()
+            try:
+                with torch.cuda.graph(gp, stream=side3):
+                    for i in range(steps):
+                        copies[i % len(copies)].run()
+            finally:
+                n_rec = pkv.profile_stop(read=False)
+            torch.cuda.synchronize()
+            upload_graph(gp, stream)
+            gp.replay()
+            torch.cuda.synchronize()
+            recs = pkv.profile_records(n_rec)
+            kernel_timing = "event nodes around every launch in a CUDA graph of %d steps" % steps
+            del gp
+        except Exception as e:                          # noqa: BLE001 - fall back to eager events
+            torch.cuda.synchronize()
+            kernel_timing = "eager per-launch events (graph capture of the events failed: %s)" % (
+                str(e).splitlines()[0][:120] if str(e) else type(e).__name__)
+            recs = None
+    if recs is None:
+        prof_steps = max(3, min(steps, 50))
+        pkv.profile_start(prof_steps * launches_per_step + 16)
+        for i in range(prof_steps):
+            copies[i % len(copies)].run()
+        recs = pkv.profile_stop()
+        kernel_timing = kernel_timing or "eager per-launch events over %d steps" % prof_steps
+        prof_steps_seen = prof_steps
     else:
-        os.environ["PKV_NO_OVERLAP"] = saved
+        prof_steps_seen = steps
     kern = {}
     for name, ms in recs:
         k = kern.setdefault(name, {"launches": 0, "total_ms": 0.0})
@@ -483,14 +515,22 @@ def time_workload(pkv, cfg, steps, warmup, device, peaks, dist=None, use_graph=T
     total = sum(k["total_ms"] for k in kern.values()) or 1.0
     kernels = {}
     for name, k in kern.items():
-        kernels[name] = {"launches_per_step": k["launches"] / prof_steps,
+        kernels[name] = {"launches_per_step": k["launches"] / prof_steps_seen,
                          "avg_launch_us": 1e3 * k["total_ms"] / k["launches"],
                          "share": k["total_ms"] / total}
     dominant = max(kern, key=lambda n: kern[n]["total_ms"]) if kern else None
     roof = None
     if dominant:
         avg_s = kern[dominant]["total_ms"] / kern[dominant]["launches"] / 1e3
+        bounded = False
+        # a kernel cannot take longer than the whole step it is part of:
+        # where the event bracket says so (launch overhead on a latency-bound
+        # kernel), the step time bounds the kernel time instead
+        if avg_s * kernels[dominant]["launches_per_step"] > ms_per_step / 1e3:
+            avg_s = ms_per_step / 1e3 / kernels[dominant]["launches_per_step"]
+            bounded = True
         roof = roofline(dominant, avg_s, kernels[dominant]["launches_per_step"], acc, peaks, f"cfg{cfg}")
+        roof["timing"] = kernel_timing + ("; bounded by the step time" if bounded else "")
 
     step_s = ms_per_step / 1e3
     res = {
@@ -793,63 +833,140 @@ def block_copy_workload(pkv, device, peaks, reps=20):
 
 # ---------------------------------------------------------------------------- CPU oracle
 
-def oracle_step_timer(cfg, threads):
-    """Time the CPU oracle (write + attention) on the workload's full step."""
-    import oracle
-    spec = config_spec(cfg)
-    b = make_batch(spec, device="cpu")
-    m = b.meta
+class OracleStep:
+    """The workload's step on the CPU oracle: the write of the step's rows,
+    then attention.  Its inputs are drawn exactly as the GPU arm draws them
+    (on the device when there is one, for the multi-GB pools, then copied to
+    host memory).  A step's attention can be timed whole or on a sample of
+    its query tokens (all heads of every sampled token); a sample's time is
+    scaled to the whole step by the keys the step's rows attend to, which
+    the oracle's work follows (one pass over each visible key per row)."""
 
-    def step():
-        oracle.paged_kv_write(b.k_cache, b.v_cache, b.k, b.v, m.slot_mapping)
-        oracle.ragged_paged_attention(b.q, b.k_cache, b.v_cache, m.query_start_loc, m.seq_lens,
-                                      m.block_table, spec.scale, threads)
-    return spec, m, step
+    def __init__(self, cfg, threads):
+        import oracle
+        self.oracle = oracle
+        self.spec = spec = config_spec(cfg)
+        dev = "cuda" if (cfg not in (1, 2) and torch.cuda.is_available()) else "cpu"
+        b = make_batch(spec, device=dev)
+        if dev != "cpu":
+            b = Batch(spec, b.meta, b.q.cpu(), b.k.cpu(), b.v.cpu(), b.k_cache.cpu(), b.v_cache.cpu())
+            torch.cuda.empty_cache()
+        self.b, self.m, self.threads = b, b.meta, threads
+        m = self.m
+        self.keys = []                                   # keys each query row attends to
+        for r in range(m.num_reqs):
+            t, L = m.query_start_loc[r + 1] - m.query_start_loc[r], m.seq_lens[r]
+            self.keys.extend(0 if L == 0 else L - t + i + 1 for i in range(t))
+        self.total_keys = sum(self.keys)
+        self.tokens = m.num_tokens
+
+    def write(self):
+        b = self.b
+        self.oracle.paged_kv_write(b.k_cache, b.v_cache, b.k, b.v, self.m.slot_mapping)
+
+    def attend_full(self):
+        b, m = self.b, self.m
+        self.oracle.ragged_paged_attention(b.q, b.k_cache, b.v_cache, m.query_start_loc, m.seq_lens,
+                                           m.block_table, self.spec.scale, self.threads)
+
+    def attend_sample(self, stride, offset):
+        """Attention of every stride-th query token (all heads); returns the
+        factor that scales its time to the whole step's attention."""
+        b, m, hq = self.b, self.m, self.spec.num_q_heads
+        toks = list(range(offset % stride, self.tokens, stride))
+        keys = sum(self.keys[t] for t in toks)
+        if not toks or keys == 0:
+            toks, keys = [int(max(range(self.tokens), key=lambda t: self.keys[t]))], 0
+            keys = self.keys[toks[0]]
+        tt = [t for t in toks for _ in range(hq)]
+        hh = [h for _ in toks for h in range(hq)]
+        self.oracle.attention_rows(tt, hh, b.q, b.k_cache, b.v_cache, m.query_start_loc, m.seq_lens,
+                                   m.block_table, self.spec.scale, self.threads)
+        return self.total_keys / keys
+
+    def timed_step(self, stride, offset=0):
+        """Seconds of one step (write + attention), the attention measured on
+        a sample when stride > 1 and scaled to the whole step."""
+        t0 = time.perf_counter()
+        self.write()
+        t1 = time.perf_counter()
+        if stride <= 1:
+            self.attend_full()
+            scale = 1.0
+        else:
+            scale = self.attend_sample(stride, offset)
+        t2 = time.perf_counter()
+        return (t1 - t0) + (t2 - t1) * scale
+
+    def stride_for(self, seconds):
+        """Token stride whose sampled step takes about `seconds` (1: whole steps)."""
+        probe = max(1, self.tokens // 64)
+        t0 = time.perf_counter()
+        scale = self.attend_sample(probe, 0) if probe > 1 else 1.0
+        if probe == 1:
+            self.attend_full()
+        full = (time.perf_counter() - t0) * scale
+        return max(1, math.ceil(full / max(seconds, 1e-3)))
+
+    def describe(self, n, stride, per_step_s):
+        what = ("whole steps" if stride <= 1 else
+                f"steps whose attention ran on every {stride}-th query token (all heads), its time scaled "
+                f"by the keys those rows attend to ({self.total_keys} keys over all rows)")
+        return (f"{n} {what} of the {self.spec.name} workload (write + attention) on {self.threads} threads; "
+                f"{per_step_s * 1e3:.1f} ms per full step")
 
 
-def cpu_baseline(cfg, budget_s=10.0):
+def cpu_baseline(cfg, budget_s=6.0):
+    """The oracle on the host cores, a bounded sample of the workload's step:
+    whole steps where a step fits in a third of the budget, otherwise steps
+    whose attention covers every stride-th query token."""
     threads = os.cpu_count() or 1
-    spec, m, step = oracle_step_timer(cfg, threads)
-    step()                                               # build and warm
+    st = OracleStep(cfg, threads)
+    stride = st.stride_for(budget_s / 3)
+    times = []
     t0 = time.perf_counter()
-    n = 0
-    while True:
-        step()
-        n += 1
-        if time.perf_counter() - t0 >= budget_s:
-            break
-    dt = (time.perf_counter() - t0) / n
-    t1 = time.perf_counter()
-    _, _, step1 = oracle_step_timer(cfg, 1)
-    step1()
-    one_thread = time.perf_counter() - t1
-    return {"value": m.num_tokens / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{n} full steps of the {CONFIG_NAMES[cfg]} workload (write + attention), "
-                      f"{dt * 1e3:.1f} ms each on {threads} threads; one step on 1 thread took {one_thread * 1e3:.0f} ms",
-            "ms_per_step": dt * 1e3, "one_thread_ms_per_step": one_thread * 1e3}
+    while not times or time.perf_counter() - t0 < budget_s:
+        times.append(st.timed_step(stride, offset=len(times)))
+    dt = statistics.median(times)
+    # one step on a single thread: whole if that takes under the budget,
+    # else on a sample `threads` times sparser (about the same wall time)
+    s1 = stride * threads if stride > 1 else (1 if dt * threads < budget_s else threads)
+    st.threads = 1
+    one_s = st.timed_step(s1)
+    st.threads = threads
+    return {"value": st.tokens / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": st.describe(len(times), stride, dt),
+            "ms_per_step": dt * 1e3, "one_thread_ms_per_step": one_s * 1e3,
+            "one_thread_sample_stride": s1, "wall_s": time.perf_counter() - t0}
 
 
 def run_reference(args):
+    """The reference arm: the oracle as it stands on the host cores, K timed
+    steps after W warm-up steps of the same workload; each step's attention
+    runs on a token sample sized so that the whole run ends within about two
+    minutes (whole steps where they are that cheap), scaled to the whole
+    step.  Under torchrun rank 0 alone runs and prints."""
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
     threads = os.cpu_count() or 1
-    spec, m, step = oracle_step_timer(args.workload, threads)
-    for _ in range(max(3, args.warmup)):
-        step()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        step()
-    dt = (time.perf_counter() - t0) / args.steps
-    value = m.num_tokens / dt
-    line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": dt * 1e3,
+    st = OracleStep(args.workload, threads)
+    warm = max(3, args.warmup)
+    per_step = min(5.0, max(0.02, 120.0 / (args.steps + warm)))
+    stride = st.stride_for(per_step)
+    for i in range(warm):
+        st.timed_step(stride, offset=i)
+    times = [st.timed_step(stride, offset=warm + i) for i in range(args.steps)]
+    dt = sum(times) / len(times)
+    value = st.tokens / dt
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": world,
+            "steps": args.steps, "warmup": warm, "ms_per_step": dt * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,1) values, shapes of the pages' workloads)",
-            "config": {"workload": CONFIG_NAMES[args.workload], "query_tokens": m.num_tokens,
-                       "requests": m.num_reqs, "parallelism": "host cores"},
+            "config": {"workload": CONFIG_NAMES[args.workload], "query_tokens": st.tokens,
+                       "requests": st.m.num_reqs, "parallelism": "host cores"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                             "sample": f"full steps of {CONFIG_NAMES[args.workload]} (write + attention)"},
+                             "sample": st.describe(args.steps, stride, dt)},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -891,9 +1008,11 @@ def run_ours(args):
         for cfg in (1, 2, 3, 4, 5):
             if cfg == args.workload:
                 r = dict(head)
+                r["e2e"] = e2e
             else:
                 _, cps, r = time_workload(pkv, cfg, max(10, min(args.steps, 50)), warmup, device, peaks, None)
                 r.pop("timed_wall")
+                r["e2e"] = e2e_workload(pkv, cps, max(10, min(args.steps, 50)), device)
                 del cps
                 torch.cuda.empty_cache()
             breakdown[str(cfg)] = r
@@ -903,7 +1022,11 @@ def run_ours(args):
         if dist is not None:
             dist.destroy_process_group()
         return 0
-    cpu = cpu_baseline(args.workload) if world == 1 and not args.no_cpu_baseline else None
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.workload)
+        for cfg, r in breakdown.items():
+            r["cpu_baseline"] = cpu if int(cfg) == args.workload else cpu_baseline(int(cfg), budget_s=4.0)
     tokens = head["algorithmic"]["tokens"]
     line = {
         "metric": METRIC, "value": job_value(tokens, world, head["ms_per_step"]), "unit": UNIT,
@@ -921,6 +1044,7 @@ def run_ours(args):
                                        if head["ms_per_step_one_graph_per_step"] is not None else None),
         "kv_read_gbs": head["kv_read_gbs"],
         "kv_read_frac_of_8tbs": head["kv_read_frac_of_8tbs"],
+        "step_tensor_frac": head["step_tensor_frac"], "step_hbm_frac": head["step_hbm_frac"],
         "roofline": head["roofline"], "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": head["launches_per_step"] * args.steps,
         "clocks": clocks.summary(t0, t1), "peaks": peaks, "kernels": head["kernels"],
@@ -930,6 +1054,18 @@ def run_ours(args):
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def relaunch_with_ranks(n):
+    """Run this same command as n ranks under torch.distributed.run on
+    127.0.0.1 (one process per GPU); returns its exit status."""
+    import socket
+    with socket.socket() as sock:
+        sock.bind(("127.0.0.1", 0))
+        port = sock.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr=127.0.0.1", f"--master-port={port}", os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.call(cmd)
 
 
 def main():
@@ -946,6 +1082,14 @@ def main():
     ap.add_argument("--fp8", action="store_true",
                     help="time only the workload on a quantized pool (a diagnostic line, for profiling runs)")
     args = ap.parse_args()
+    if args.gpus < 1:
+        ap.error("--gpus must be at least 1")
+    world = os.environ.get("WORLD_SIZE")
+    if world is None and args.gpus > 1:
+        return relaunch_with_ranks(args.gpus)
+    if world is not None and int(world) != args.gpus:
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}: launch one rank per GPU", file=sys.stderr)
+        return 2
     if args.impl == "reference":
         return run_reference(args)
     if args.fp8:

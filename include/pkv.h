@@ -83,7 +83,9 @@ int64_t pkv_launch_count(void);
  * number of records; pkv_profile_read() waits for record `index` and gives
  * its kernel id and duration in ms; pkv_kernel_name() names a kernel id.
  * Events are created once by pkv_profile_start (host-side CUDA objects, no
- * device memory).  Do not profile while capturing a CUDA graph.
+ * device memory).  Launches made while their stream is being captured into
+ * a CUDA graph get their events as event nodes of that graph: read the
+ * records after the graph has run once (each run overwrites them).
  */
 pkv_status pkv_profile_start(int32_t capacity);
 int32_t pkv_profile_stop(void);
@@ -317,29 +319,32 @@ pkv_status pkv_paged_kv_write_attention_fp8(const void *k, const void *v, void *
 /*
  * ragged_paged_attention without a caller workspace.  The pages have no
  * counterpart of this call: it exists for callers that cannot allocate
- * device memory, such as code running under a stream capture that forbids
- * allocation, plain C hosts without a device allocator, and serving loops
- * that must not call cudaMalloc because it may synchronise the device.
+ * device memory, such as plain C hosts without a device allocator of their
+ * own, and serving loops that must not call cudaMalloc because it may
+ * synchronise the device or because their device memory budget is fixed
+ * when they start.
  *
  * Same arguments and results as pkv_ragged_paged_attention, except:
- *  - No workspace: the split-KV partials and the device error word live in
- *    one static device array of PKV_NOALLOC_SCRATCH_BYTES inside the
- *    library.  Every GPU that loads the library holds that array until the
- *    process exits.  The call allocates nothing and calls no allocating
- *    routine.
- *  - A batch whose workspace need, pkv_attention_workspace_bytes(num_reqs,
- *    num_tokens, num_q_heads, head_dim, max_seq_len), exceeds
- *    PKV_NOALLOC_SCRATCH_BYTES is rejected with PKV_ERR_WORKSPACE before
- *    anything is enqueued.
+ *  - No workspace: the split-KV partials, the split counters and the device
+ *    error word live in one static device array of PKV_NOALLOC_SCRATCH_BYTES
+ *    (8 MiB) inside the library.  Every GPU that loads the library holds
+ *    that array until the process exits.  The call allocates nothing and
+ *    calls no allocating routine.
+ *  - The planner fits the split-KV partials into the array, lengthening the
+ *    decode splits where the batch would need more (fewer, longer splits;
+ *    the same results).  The call plans the batch against the array's size
+ *    before it enqueues anything and returns PKV_ERR_WORKSPACE if that plan
+ *    would not fit; the planner's rule makes every batch that the workspace
+ *    entry point accepts fit.
  *  - device_error (device uint32_t, may be NULL) receives this call's
  *    bounds flags (overwritten, not OR-ed).
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress, with that device current) and keeps it; make
  *    that first call before any stream capture.
- *  - All calls share the one array and it keeps the last call's contents:
- *    the call itself resets the error word, and calls whose work overlaps
- *    on the GPU (other streams, other threads) race on the array.
- *    Serialise them, for example on one stream.
+ *  - All calls share the one array and it keeps the last call's contents.
+ *    Each call first zeroes the error word and the split counters on its
+ *    stream.  Calls whose work overlaps on the GPU (other streams, other
+ *    threads) race on the array: serialise them, for example on one stream.
  */
 #define PKV_NOALLOC_SCRATCH_BYTES (8u << 20)
 pkv_status pkv_ragged_paged_attention_noalloc(void *out, const void *q,
@@ -354,6 +359,10 @@ pkv_status pkv_ragged_paged_attention_noalloc(void *out, const void *q,
                                               int32_t head_dim, int32_t block_size,
                                               int32_t num_blocks_total, float scale, int32_t window,
                                               uint32_t *device_error, cudaStream_t stream);
+
+/* Size in bytes of the no-allocation call's static scratch array
+ * (PKV_NOALLOC_SCRATCH_BYTES as this library was built). */
+size_t pkv_noalloc_scratch_bytes(void);
 
 /*
  * Which kernel path pkv_ragged_paged_attention takes for each request

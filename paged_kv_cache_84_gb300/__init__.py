@@ -16,7 +16,7 @@ import torch
 __all__ = [
     "PkvError", "load", "paged_kv_write", "ragged_paged_attention", "attention_workspace_bytes",
     "make_workspace", "read_device_error", "clear_device_error", "launch_count", "LIB_PATH",
-    "DEVERR_SLOT", "DEVERR_BLOCK", "DEVERR_TIMEOUT", "DEVERR_META", "DEVERR_COUNTER", "WORKSPACE_MIN_BYTES", "profile_start", "profile_stop",
+    "DEVERR_SLOT", "DEVERR_BLOCK", "DEVERR_TIMEOUT", "DEVERR_META", "DEVERR_COUNTER", "WORKSPACE_MIN_BYTES", "profile_start", "profile_stop", "profile_records",
     "plan_request_kernels", "CLASS_NAMES", "paged_kv_write_fp8", "ragged_paged_attention_fp8", "copy_blocks", "gather_blocks", "scatter_blocks", "MAX_POOLS", "copy_async", "paged_kv_write_attention", "fp8_prefill_scratch_bytes", "paged_kv_write_attention_fp8", "plan_attention",
 ]
 
@@ -160,10 +160,18 @@ def profile_start(capacity: int = 4096):
     _check(load().pkv_profile_start(capacity), "profile_start")
 
 
-def profile_stop():
-    """Stop recording; return [(kernel name, ms), ...] in launch order (waits for them)."""
+def profile_stop(read: bool = True):
+    """Stop recording; return [(kernel name, ms), ...] in launch order (waits
+    for them).  read=False returns only the number of records, for launches
+    captured into a CUDA graph: read them with profile_records(n) after the
+    graph has run."""
+    n = load().pkv_profile_stop()
+    return profile_records(n) if read else n
+
+
+def profile_records(n: int):
+    """[(kernel name, ms), ...] of the first n records (waits for them)."""
     L = load()
-    n = L.pkv_profile_stop()
     out = []
     kid, ms = _c_i32(0), ctypes.c_float(0)
     for i in range(n):

@@ -120,6 +120,16 @@ constexpr uint32_t kDevErrMeta = 8u;    // device metadata differs from the host
 constexpr uint32_t kDevErrCounter = 16u; // a split counter was not zero at the start of a call
 constexpr int kCounterStride = 8;        // uint32 words between two split counters (32 bytes)
 
+// Workspace layout: the device error word area comes first; then, in every
+// workspace large enough to hold it, the split counters of in-kernel
+// combines (zero-filled by the caller once; each call leaves them zero
+// again), one per (split request, KV head), 32 bytes apart so that
+// concurrent atomics of different requests do not queue on one L2 sector;
+// then split-KV partials.
+constexpr size_t kErrBytes = 256;
+constexpr int kCounterGroups = 2048;
+constexpr size_t kCounterBytes = 4 * (size_t)kCounterStride * kCounterGroups;
+
 // Flags a listed request whose device metadata disagrees with the host copies
 // the launch was planned from (the kernels use the planned values).
 // Generic-proxy writes to global memory become visible to the async proxy

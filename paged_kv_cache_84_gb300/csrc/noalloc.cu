@@ -1,12 +1,12 @@
 // Ragged paged attention for callers that cannot allocate device memory.
 //
 // pkv_ragged_paged_attention needs a caller workspace for its split-KV
-// partials and its device error word.  Some callers have no way to provide
-// one: code that runs while a stream is being captured under a mode that
-// forbids allocation, plain C hosts that have no device allocator of their
-// own, and serving loops that must not call cudaMalloc because it can
-// synchronise the whole device.  This entry point uses a fixed scratch array
-// that lives in the library's own device image instead.  The paged-attention
+// partials, split counters and device error word.  Some callers have no way
+// to provide one: plain C hosts that have no device allocator of their own,
+// and serving loops that must not call cudaMalloc because it can
+// synchronise the whole device or because their device memory budget is
+// fixed when they start.  This entry point uses a fixed scratch array that
+// lives in the library's own device image instead.  The paged-attention
 // pages have no counterpart of it: it is an interface convenience only.
 //
 // The scratch is a file-scope __device__ array.  Host code cannot use its
@@ -16,11 +16,17 @@
 #include <mutex>
 
 #include "pkv.h"
+#include "common.cuh"
 
 namespace {
 
 constexpr size_t kScratchBytes = PKV_NOALLOC_SCRATCH_BYTES;
 constexpr int kMaxDevices = 64;
+// what must be zero when a call starts: the error word area and the split
+// counters (a call that ended early may have left either dirty)
+constexpr size_t kZeroPrefix = pkv::kErrBytes + pkv::kCounterBytes;
+static_assert(kScratchBytes >= PKV_WORKSPACE_MIN_BYTES && kScratchBytes > kZeroPrefix + 4096,
+              "the scratch array must hold the error word, the counters and some partials");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
@@ -45,6 +51,8 @@ pkv_status scratch_for_current_device(void **ptr)
 
 }  // namespace
 
+extern "C" size_t pkv_noalloc_scratch_bytes(void) { return kScratchBytes; }
+
 extern "C" pkv_status pkv_ragged_paged_attention_noalloc(
     void *out, const void *q, const void *k_cache, const void *v_cache, const int32_t *query_start_loc,
     const int32_t *seq_lens, const int32_t *block_table, int32_t block_table_stride,
@@ -53,25 +61,34 @@ extern "C" pkv_status pkv_ragged_paged_attention_noalloc(
     int32_t block_size, int32_t num_blocks_total, float scale, int32_t window, uint32_t *device_error,
     cudaStream_t stream)
 {
-    // Size check on the host, before anything touches the device.
-    size_t need = pkv_attention_workspace_bytes(num_reqs, num_tokens, num_q_heads, head_dim, max_seq_len);
-    if (need > kScratchBytes) return PKV_ERR_WORKSPACE;
-
     void *scratch = nullptr;
     pkv_status st = scratch_for_current_device(&scratch);
     if (st != PKV_OK) return st;
 
-    // The scratch starts as zeros and every successful call leaves its error
-    // word at zero again (below), so each call starts from a clean word.
+    // Size check on the host, before anything is enqueued: the planner fits
+    // the split-KV partials into the array (it lengthens the splits until
+    // they fit), so every batch the workspace entry point accepts fits; a
+    // plan that would not fit is refused rather than run.
+    if (num_tokens > 0) {
+        pkv_attention_plan plan;
+        st = pkv_plan_attention(query_start_loc_host, seq_lens_host, num_reqs, num_q_heads, num_kv_heads, head_dim,
+                                block_size, window, 0, 0, kScratchBytes, 0, &plan);
+        if (st != PKV_OK) return st;
+        const size_t front = plan.split_counters ? kZeroPrefix : pkv::kErrBytes;
+        if (plan.partial_bytes > kScratchBytes - front - 64) return PKV_ERR_WORKSPACE;
+    }
+
+    // Every call starts from a zero error word and zero counters, whatever
+    // an earlier call left there.
+    cudaError_t e = cudaMemsetAsync(scratch, 0, kZeroPrefix, stream);
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
     st = pkv_ragged_paged_attention(out, q, k_cache, v_cache, query_start_loc, seq_lens, block_table,
                                     block_table_stride, query_start_loc_host, seq_lens_host, num_reqs,
                                     num_tokens, max_query_len, max_seq_len, num_q_heads, num_kv_heads,
                                     head_dim, block_size, num_blocks_total, scale, window, scratch,
                                     kScratchBytes, stream);
     if (st != PKV_OK) return st;
-    cudaError_t e = cudaSuccess;
     if (device_error)
         e = cudaMemcpyAsync(device_error, scratch, sizeof(uint32_t), cudaMemcpyDeviceToDevice, stream);
-    if (e == cudaSuccess) e = cudaMemsetAsync(scratch, 0, sizeof(uint32_t), stream);
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

@@ -38,6 +38,18 @@ struct Profile {
 };
 static Profile g_prof;
 
+// A profiling event on `stream`: while the stream is being captured into a
+// CUDA graph the record becomes an event node of the graph (its timestamp
+// is taken each time the graph runs), otherwise an ordinary record.
+static void record_profile_event(cudaEvent_t ev, cudaStream_t stream)
+{
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+        cudaEventRecordWithFlags(ev, stream, cudaEventRecordExternal);
+    else
+        cudaEventRecord(ev, stream);
+}
+
 void launch_begin(cudaStream_t stream, int kernel_id)
 {
     g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -46,7 +58,7 @@ void launch_begin(cudaStream_t stream, int kernel_id)
     if (!g_prof.on || g_prof.n >= (int)g_prof.kernel.size()) return;
     g_prof.open = g_prof.n;
     g_prof.kernel[g_prof.n] = kernel_id;
-    cudaEventRecord(g_prof.events[2 * g_prof.n], stream);
+    record_profile_event(g_prof.events[2 * g_prof.n], stream);
 }
 
 void launch_end(cudaStream_t stream)
@@ -54,7 +66,7 @@ void launch_end(cudaStream_t stream)
     if (!g_prof.on) return;
     std::lock_guard<std::mutex> lock(g_prof.mu);
     if (g_prof.open < 0) return;
-    cudaEventRecord(g_prof.events[2 * g_prof.open + 1], stream);
+    record_profile_event(g_prof.events[2 * g_prof.open + 1], stream);
     g_prof.n = g_prof.open + 1;
     g_prof.open = -1;
 }
@@ -121,14 +133,6 @@ constexpr int kDecodeRows = 16;       // decode-class: t * g <= this
 constexpr int kMinSplit = 256;        // smallest KV split, tokens
 constexpr int kMaxSplits = 64;        // most splits of one request
 constexpr int kMaxStreamSplits = 32;  // most splits of one request on the streaming kernel
-constexpr size_t kErrBytes = 256;     // device error word area at the workspace start
-// Split counters of in-kernel combines: a fixed region after the error word
-// in every workspace large enough to hold it (zero-filled by the caller once;
-// each call leaves it zero again).  One counter per (split request, KV head).
-// Counters sit 32 bytes apart so that concurrent atomics of different
-// requests do not queue on one L2 sector.
-constexpr int kCounterGroups = 2048;
-constexpr size_t kCounterBytes = 4 * (size_t)kCounterStride * kCounterGroups;
 constexpr int kMaxPrefillRowSplits = 4;   // workspace sizing of split prefill tiles
 // Every prefill-class request (more than kDecodeRows query rows) whose head
 // dim and group fit a 128-row tile runs on the tcgen05 kernel: measured on
