@@ -27,8 +27,8 @@
  *    disagrees with its host copy).  The access is skipped, the bit is OR-ed
  *    in, and nothing traps.  The word is sticky until cleared.
  *  - Kernels are launched as programmatic dependents (PDL) of the kernel
- *    before them on `stream` (set PKV_NO_PDL=1 in the environment to turn
- *    this off).  pkv_paged_kv_write reads nothing before its grid-dependency
+ *    before them on `stream` (the attention calls' options can turn this
+ *    off).  The library reads no environment variables.  pkv_paged_kv_write reads nothing before its grid-dependency
  *    wait and releases its dependents only after it.  The attention kernels
  *    read q, query_start_loc, seq_lens and block_table before that wait (only
  *    the pool rows wait for it), so the kernel before them on the stream must
@@ -218,6 +218,62 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q,
                                       cudaStream_t stream);
 
 /*
+ * Options of the attention calls' _ex variants.  Each field overrides one
+ * choice the planner otherwise makes from the batch alone; a zero-filled
+ * struct (or a NULL pointer) leaves every choice to the planner, and the
+ * plain calls are the _ex calls with NULL.  Normal use needs none of them:
+ * they exist so that tests can reach every kernel arrangement and
+ * measurements can compare them.  Results are the same under every option
+ * (within the attention tolerance; the pools bit for bit).
+ *
+ *   disable_tcgen05     1: prefill tiles on the warp-MMA kernel, not tcgen05
+ *   tc_min_rows         > 0: query rows (new tokens x group) from which a
+ *                       prefill request goes to tcgen05 (default 17)
+ *   fp8_prefill_on_mma  1: quantized-pool prefill on the warp-MMA kernel even
+ *                       when the workspace has room for bf16 block copies
+ *   split_tokens        > 0: decode split length in keys (rounded up to the
+ *                       block size), instead of the planner's
+ *   cluster             0: planner; -1: no thread-block clusters (split
+ *                       counters merge the splits); 2..8: clusters of that
+ *                       many splits
+ *   decode_main         0: planner; 1: when the classes overlap the decodes
+ *                       run on the caller's stream; -1: the prefill does
+ *   no_overlap          1: both classes on the caller's stream, in turn
+ *   prefill_key_splits  1: warp-MMA prefill tiles split over keys when they
+ *                       fill less than two waves
+ *   separate_write      1: the combined calls run the full scatter, then the
+ *                       attention
+ *   decode_row_tiles    1: 16-row query tiles for decodes instead of
+ *                       key-major tiles for small groups
+ *   no_pdl              1: no programmatic dependent launches
+ */
+typedef struct pkv_attention_options {
+    int32_t disable_tcgen05;
+    int32_t tc_min_rows;
+    int32_t fp8_prefill_on_mma;
+    int32_t split_tokens;
+    int32_t cluster;
+    int32_t decode_main;
+    int32_t no_overlap;
+    int32_t prefill_key_splits;
+    int32_t separate_write;
+    int32_t decode_row_tiles;
+    int32_t no_pdl;
+    int32_t reserved[5];
+} pkv_attention_options;
+
+/* pkv_ragged_paged_attention with options (NULL: the planner's choices). */
+pkv_status pkv_ragged_paged_attention_ex(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                         const int32_t *query_start_loc, const int32_t *seq_lens,
+                                         const int32_t *block_table, int32_t block_table_stride,
+                                         const int32_t *query_start_loc_host, const int32_t *seq_lens_host,
+                                         int32_t num_reqs, int32_t num_tokens, int32_t max_query_len,
+                                         int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                                         int32_t head_dim, int32_t block_size, int32_t num_blocks_total,
+                                         float scale, int32_t window, void *workspace, size_t workspace_bytes,
+                                         const pkv_attention_options *options, cudaStream_t stream);
+
+/*
  * One step's write and attention in one call ("31. Engine v2", "Attention
  * over the pool": every layer writes the step's K/V rows, then attends):
  * the result is that of pkv_paged_kv_write(k, v, k_cache, v_cache,
@@ -246,8 +302,8 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q,
  * its new rows are written, so a batch that breaks this may see old rows.
  * Device errors of the write (PKV_DEVERR_SLOT) go to the workspace's error
  * word with the attention's.  Return codes as the two calls; nothing is
- * enqueued when the arguments are rejected.  With PKV_ATTN_CUDA_CORE=1 (or
- * PKV_SEPARATE_WRITE=1) the call runs the full scatter, then the attention.
+ * enqueued when the arguments are rejected.  With the separate_write option
+ * the call runs the full scatter, then the attention.
  */
 pkv_status pkv_paged_kv_write_attention(const void *k, const void *v, void *k_cache, void *v_cache,
                                         const int64_t *slot_mapping, void *out, const void *q,
@@ -260,6 +316,16 @@ pkv_status pkv_paged_kv_write_attention(const void *k, const void *v, void *k_ca
                                         int32_t block_size, int32_t num_blocks_total, float scale,
                                         int32_t window, void *workspace, size_t workspace_bytes,
                                         cudaStream_t stream);
+pkv_status pkv_paged_kv_write_attention_ex(const void *k, const void *v, void *k_cache, void *v_cache,
+                                           const int64_t *slot_mapping, void *out, const void *q,
+                                           const int32_t *query_start_loc, const int32_t *seq_lens,
+                                           const int32_t *block_table, int32_t block_table_stride,
+                                           const int32_t *query_start_loc_host, const int32_t *seq_lens_host,
+                                           int32_t num_reqs, int32_t num_tokens, int32_t max_query_len,
+                                           int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                                           int32_t head_dim, int32_t block_size, int32_t num_blocks_total,
+                                           float scale, int32_t window, void *workspace, size_t workspace_bytes,
+                                           const pkv_attention_options *options, cudaStream_t stream);
 
 /*
  * ragged_paged_attention over a quantized pool (codes and scales as written
@@ -269,8 +335,7 @@ pkv_status pkv_paged_kv_write_attention(const void *k, const void *v, void *k_ca
  * (every E4M3 value is an fp16 value; q rounds to fp16 exactly within its
  * range), so |q| and the per-key weight * V scale must stay inside fp16's
  * range (65504).  Requirements (else PKV_ERR_UNSUPPORTED): head_dim 128,
- * num_kv_heads a multiple of 4; the CUDA-core kernels
- * (PKV_ATTN_CUDA_CORE) have no quantized path.  Prefill chunks run on
+ * num_kv_heads a multiple of 4.  Prefill chunks run on
  * tcgen05 over bf16 copies of their blocks (code * scale rounded to nearest)
  * when the workspace holds pkv_fp8_prefill_scratch_bytes(...) more than
  * pkv_attention_workspace_bytes(...); otherwise on the warp-level MMA kernels
@@ -290,6 +355,16 @@ pkv_status pkv_ragged_paged_attention_fp8(void *out, const void *q,
                                           int32_t num_blocks_total, float scale, int32_t window,
                                           void *workspace, size_t workspace_bytes,
                                           cudaStream_t stream);
+pkv_status pkv_ragged_paged_attention_fp8_ex(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                             const float *k_scale, const float *v_scale,
+                                             const int32_t *query_start_loc, const int32_t *seq_lens,
+                                             const int32_t *block_table, int32_t block_table_stride,
+                                             const int32_t *query_start_loc_host, const int32_t *seq_lens_host,
+                                             int32_t num_reqs, int32_t num_tokens, int32_t max_query_len,
+                                             int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                                             int32_t head_dim, int32_t block_size, int32_t num_blocks_total,
+                                             float scale, int32_t window, void *workspace, size_t workspace_bytes,
+                                             const pkv_attention_options *options, cudaStream_t stream);
 
 /*
  * pkv_paged_kv_write_fp8 followed by pkv_ragged_paged_attention_fp8 in one
@@ -301,8 +376,9 @@ pkv_status pkv_ragged_paged_attention_fp8(void *out, const void *q,
  * num_kv_heads][128], 16-byte aligned; codes pools; scale pools written;
  * slot_mapping agreeing with the block table) and the attention's.  Device
  * errors of the write go to the workspace's error word; a decode row whose
- * slot differs from the block table's sets PKV_DEVERR_META.
- * PKV_SEPARATE_WRITE=1 runs the full quantizing scatter, then the attention.
+ * slot differs from the block table's sets PKV_DEVERR_META.  With the
+ * separate_write option the call runs the full quantizing scatter, then the
+ * attention.
  */
 pkv_status pkv_paged_kv_write_attention_fp8(const void *k, const void *v, void *k_cache, void *v_cache,
                                             float *k_scale, float *v_scale, const int64_t *slot_mapping,
@@ -315,6 +391,17 @@ pkv_status pkv_paged_kv_write_attention_fp8(const void *k, const void *v, void *
                                             int32_t block_size, int32_t num_blocks_total, float scale,
                                             int32_t window, void *workspace, size_t workspace_bytes,
                                             cudaStream_t stream);
+pkv_status pkv_paged_kv_write_attention_fp8_ex(const void *k, const void *v, void *k_cache, void *v_cache,
+                                               float *k_scale, float *v_scale, const int64_t *slot_mapping,
+                                               void *out, const void *q, const int32_t *query_start_loc,
+                                               const int32_t *seq_lens, const int32_t *block_table,
+                                               int32_t block_table_stride, const int32_t *query_start_loc_host,
+                                               const int32_t *seq_lens_host, int32_t num_reqs, int32_t num_tokens,
+                                               int32_t max_query_len, int32_t max_seq_len, int32_t num_q_heads,
+                                               int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                               int32_t num_blocks_total, float scale, int32_t window,
+                                               void *workspace, size_t workspace_bytes,
+                                               const pkv_attention_options *options, cudaStream_t stream);
 
 /*
  * ragged_paged_attention without a caller workspace.  The pages have no
@@ -370,14 +457,12 @@ size_t pkv_noalloc_scratch_bytes(void);
  * Decode-class requests (t * g <= 16) run on the warp-level MMA decode
  * kernels, with KV split across CTAs for long contexts; prefill-class
  * requests run in tiles of new tokens, on tcgen05 where the head dim and
- * group fit a 128-row tile.  For accounting and tests.  (With the
- * environment switch PKV_ATTN_CUDA_CORE=1 the decode and non-tensor
- * prefill classes run on CUDA-core FMA kernels instead.)
+ * group fit a 128-row tile.  For accounting and tests.  Default options.
  */
 #define PKV_CLASS_NONE 0                 /* no rows */
 #define PKV_CLASS_PADDING 1              /* seq_len 0: rows zeroed */
 #define PKV_CLASS_DECODE 2               /* decode kernels (split KV merged in a cluster or in-kernel) */
-#define PKV_CLASS_PREFILL_CUDA_CORE 3    /* warp-MMA prefill tiles (not on tcgen05) */
+#define PKV_CLASS_PREFILL_MMA 3    /* warp-MMA prefill tiles (not on tcgen05) */
 #define PKV_CLASS_PREFILL_TENSOR 4       /* tcgen05 prefill tiles */
 pkv_status pkv_plan_request_kernels(const int32_t *query_start_loc_host, const int32_t *seq_lens_host,
                                     int32_t num_reqs, int32_t num_q_heads, int32_t num_kv_heads,
@@ -395,8 +480,7 @@ pkv_status pkv_plan_request_kernels(const int32_t *query_start_loc_host, const i
  * for the same arguments as pkv_ragged_paged_attention (quantized != 0: its
  * _fp8 variant; combined != 0: pkv_paged_kv_write_attention), given the
  * workspace size and the GPU's SM count (num_sms <= 0: the current
- * device's, which needs a GPU).  Reads the same environment switches as
- * the attention calls.  query_start_loc_host has num_reqs + 1 entries,
+ * device's, which needs a GPU) and the call's options (NULL: none).  query_start_loc_host has num_reqs + 1 entries,
  * seq_lens_host num_reqs; plan_out is written on success only.
  *
  * Errors: PKV_ERR_INVALID_ARG for null pointers, num_reqs < 0, a negative
@@ -408,7 +492,7 @@ pkv_status pkv_plan_request_kernels(const int32_t *query_start_loc_host, const i
 typedef struct pkv_attention_plan {
     int32_t decode_requests;          /* decode class, padding requests included */
     int32_t prefill_tensor_requests;  /* prefill on tcgen05 */
-    int32_t prefill_mma_requests;     /* prefill on the warp-MMA (or CUDA-core) kernel */
+    int32_t prefill_mma_requests;     /* prefill on the warp-MMA kernel */
     int32_t decode_split_tokens;      /* keys per decode split, a multiple of block_size */
     int32_t max_decode_splits;        /* the largest split count of a decode request */
     int32_t decode_cluster;           /* CTAs per thread-block cluster of the first decode launch; 0: none */
@@ -424,7 +508,8 @@ typedef struct pkv_attention_plan {
 pkv_status pkv_plan_attention(const int32_t *query_start_loc_host, const int32_t *seq_lens_host,
                               int32_t num_reqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                               int32_t block_size, int32_t window, int32_t quantized, int32_t combined,
-                              size_t workspace_bytes, int32_t num_sms, pkv_attention_plan *plan_out);
+                              size_t workspace_bytes, int32_t num_sms, const pkv_attention_options *options,
+                              pkv_attention_plan *plan_out);
 
 /*
  * Set a device error word to zero (enqueued on stream).
@@ -519,7 +604,7 @@ size_t pkv_fp8_prefill_scratch_bytes(const int32_t *query_start_loc_host, const 
  * copy; the kernel waits for the kernel before it on `stream` before it
  * reads src (programmatic launch), and the next kernel waits for it.
  * Nothing is allocated and nothing synchronises.  A copy with a pinned host
- * side runs on a dozen CTAs (environment PKV_LINK_COPY_CTAS overrides): the
+ * side runs on a dozen CTAs: the
  * host link is saturated by then, and the rest of the GPU stays free for
  * attention launched on other streams while the copy runs (staging the next
  * step's inputs during this step).  A device-to-device copy spreads over

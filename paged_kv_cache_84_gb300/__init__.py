@@ -8,6 +8,7 @@ missing or a call fails, an exception is raised.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -18,6 +19,7 @@ __all__ = [
     "make_workspace", "read_device_error", "clear_device_error", "launch_count", "LIB_PATH",
     "DEVERR_SLOT", "DEVERR_BLOCK", "DEVERR_TIMEOUT", "DEVERR_META", "DEVERR_COUNTER", "WORKSPACE_MIN_BYTES", "profile_start", "profile_stop", "profile_records",
     "plan_request_kernels", "CLASS_NAMES", "paged_kv_write_fp8", "ragged_paged_attention_fp8", "copy_blocks", "gather_blocks", "scatter_blocks", "MAX_POOLS", "copy_async", "paged_kv_write_attention", "fp8_prefill_scratch_bytes", "paged_kv_write_attention_fp8", "plan_attention",
+    "AttentionOptions", "set_options", "reset_options", "options", "current_options",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpkv.so")
@@ -43,6 +45,63 @@ class _Plan(ctypes.Structure):
                 ("split_counters", _c_i32), ("overlap", _c_i32), ("decode_on_caller_stream", _c_i32),
                 ("prefill_key_splits", _c_i32), ("reserved", _c_i32),
                 ("quantized_prefill_scratch", _c_sz), ("partial_bytes", _c_sz)]
+
+
+class AttentionOptions(ctypes.Structure):
+    """pkv_attention_options (include/pkv.h): each field overrides one choice
+    of the planner; all zero leaves every choice to it."""
+    _fields_ = [("disable_tcgen05", _c_i32), ("tc_min_rows", _c_i32), ("fp8_prefill_on_mma", _c_i32),
+                ("split_tokens", _c_i32), ("cluster", _c_i32), ("decode_main", _c_i32), ("no_overlap", _c_i32),
+                ("prefill_key_splits", _c_i32), ("separate_write", _c_i32), ("decode_row_tiles", _c_i32),
+                ("no_pdl", _c_i32), ("reserved", _c_i32 * 5)]
+
+
+# The options the attention wrappers pass to the library's _ex calls (None:
+# a NULL pointer, the planner's choices).  Set by tests and comparisons only.
+_options = None
+
+
+def set_options(**fields):
+    """Override planner choices for the following attention calls (fields of
+    AttentionOptions; merged into the options already set)."""
+    global _options
+    o = AttentionOptions() if _options is None else _options
+    names = {f for f, _ in AttentionOptions._fields_ if f != "reserved"}
+    for k, v in fields.items():
+        if k not in names:
+            raise TypeError(f"unknown attention option {k!r}")
+        setattr(o, k, int(v))
+    _options = o
+
+
+def reset_options():
+    """Back to the planner's choices."""
+    global _options
+    _options = None
+
+
+def current_options():
+    """The options passed to the library now (a dict of the non-zero fields)."""
+    if _options is None:
+        return {}
+    return {f: getattr(_options, f) for f, _ in AttentionOptions._fields_
+            if f != "reserved" and getattr(_options, f)}
+
+
+@contextlib.contextmanager
+def options(**fields):
+    """Attention calls inside the block use these options, then the previous ones again."""
+    global _options
+    saved = None if _options is None else AttentionOptions.from_buffer_copy(_options)
+    try:
+        set_options(**fields)
+        yield
+    finally:
+        _options = saved
+
+
+def _opts():
+    return ctypes.byref(_options) if _options is not None else None
 
 
 class PkvError(RuntimeError):
@@ -110,10 +169,15 @@ def load():
     L.pkv_copy_async.restype = ctypes.c_int
     L.pkv_copy_async.argtypes = [_c_p, _c_p, _c_sz, _c_p]
     L.pkv_plan_attention.restype = ctypes.c_int
-    L.pkv_plan_attention.argtypes = [_c_p, _c_p] + [_c_i32] * 8 + [_c_sz, _c_i32, ctypes.POINTER(_Plan)]
+    L.pkv_plan_attention.argtypes = [_c_p, _c_p] + [_c_i32] * 8 + [_c_sz, _c_i32, _c_p, ctypes.POINTER(_Plan)]
     L.pkv_paged_kv_write_attention.restype = ctypes.c_int
     L.pkv_paged_kv_write_attention.argtypes = [_c_p] * 10 + [_c_i32, _c_p, _c_p] + [_c_i32] * 9 + \
         [_c_f, _c_i32, _c_p, _c_sz, _c_p]
+    for name, n_ptr in (("pkv_ragged_paged_attention_ex", 7), ("pkv_ragged_paged_attention_fp8_ex", 9),
+                        ("pkv_paged_kv_write_attention_ex", 10), ("pkv_paged_kv_write_attention_fp8_ex", 12)):
+        f = getattr(L, name)
+        f.restype = ctypes.c_int
+        f.argtypes = [_c_p] * n_ptr + [_c_i32, _c_p, _c_p] + [_c_i32] * 9 + [_c_f, _c_i32, _c_p, _c_sz, _c_p, _c_p]
     _lib = L
     return L
 
@@ -180,7 +244,7 @@ def profile_records(n: int):
     return out
 
 
-CLASS_NAMES = {0: "none", 1: "padding", 2: "decode", 3: "prefill_cuda_core", 4: "prefill_tensor"}
+CLASS_NAMES = {0: "none", 1: "padding", 2: "decode", 3: "prefill_mma", 4: "prefill_tensor"}
 
 
 def plan_request_kernels(query_start_loc_host, seq_lens_host, num_q_heads, num_kv_heads, head_dim):
@@ -208,7 +272,7 @@ def plan_attention(query_start_loc_host, seq_lens_host, num_q_heads, num_kv_head
     out = _Plan()
     _check(load().pkv_plan_attention(_c_p(qsl.data_ptr()), _c_p(sl.data_ptr()), sl.numel(), num_q_heads,
                                      num_kv_heads, head_dim, block_size, window, int(bool(quantized)),
-                                     int(bool(combined)), workspace_bytes, num_sms, ctypes.byref(out)),
+                                     int(bool(combined)), workspace_bytes, num_sms, _opts(), ctypes.byref(out)),
            "plan_attention")
     return {name: int(getattr(out, name)) for name, _ in _Plan._fields_ if name != "reserved"}
 
@@ -258,14 +322,14 @@ def ragged_paged_attention(out, q, k_cache, v_cache, query_start_loc, seq_lens, 
     if qsl_h.numel() != sl_h.numel() + 1:
         raise ValueError("query_start_loc needs num_reqs + 1 entries")
     _check_meta(query_start_loc, seq_lens, block_table, sl_h.numel())
-    st = L.pkv_ragged_paged_attention(
+    st = L.pkv_ragged_paged_attention_ex(
         _dev(out, "out", torch.bfloat16), _dev(q, "q", torch.bfloat16),
         _dev(k_cache, "k_cache", torch.bfloat16), _dev(v_cache, "v_cache", torch.bfloat16),
         _dev(query_start_loc, "query_start_loc", torch.int32), _dev(seq_lens, "seq_lens", torch.int32),
         _dev(block_table, "block_table", torch.int32), block_table.shape[1],
         _c_p(qsl_h.data_ptr()), _c_p(sl_h.data_ptr()), sl_h.numel(), n, int(max_query_len), int(max_seq_len),
         hq, hkv, d, bs, nbt, float(scale), int(window), _dev(workspace, "workspace", torch.uint8), workspace.numel(),
-        _stream(stream))
+        _opts(), _stream(stream))
     _check(st, "ragged_paged_attention")
 
 
@@ -286,7 +350,7 @@ def paged_kv_write_attention(k, v, k_cache, v_cache, slot_mapping, out, q, query
     if qsl_h.numel() != sl_h.numel() + 1:
         raise ValueError("query_start_loc needs num_reqs + 1 entries")
     _check_meta(query_start_loc, seq_lens, block_table, sl_h.numel())
-    st = L.pkv_paged_kv_write_attention(
+    st = L.pkv_paged_kv_write_attention_ex(
         _dev(k, "k", torch.bfloat16), _dev(v, "v", torch.bfloat16),
         _dev(k_cache, "k_cache", torch.bfloat16), _dev(v_cache, "v_cache", torch.bfloat16),
         _dev(slot_mapping, "slot_mapping", torch.int64),
@@ -295,7 +359,7 @@ def paged_kv_write_attention(k, v, k_cache, v_cache, slot_mapping, out, q, query
         _dev(block_table, "block_table", torch.int32), block_table.shape[1],
         _c_p(qsl_h.data_ptr()), _c_p(sl_h.data_ptr()), sl_h.numel(), n, int(max_query_len), int(max_seq_len),
         hq, hkv, d, bs, nbt, float(scale), int(window), _dev(workspace, "workspace", torch.uint8), workspace.numel(),
-        _stream(stream))
+        _opts(), _stream(stream))
     _check(st, "paged_kv_write_attention")
 
 
@@ -395,7 +459,7 @@ def paged_kv_write_attention_fp8(k, v, k_codes, v_codes, k_scale, v_scale, slot_
     if qsl_h.numel() != sl_h.numel() + 1:
         raise ValueError("query_start_loc needs num_reqs + 1 entries")
     _check_meta(query_start_loc, seq_lens, block_table, sl_h.numel())
-    st = L.pkv_paged_kv_write_attention_fp8(
+    st = L.pkv_paged_kv_write_attention_fp8_ex(
         _dev(k, "k", torch.bfloat16), _dev(v, "v", torch.bfloat16),
         _dev(k_codes, "k_codes", torch.uint8), _dev(v_codes, "v_codes", torch.uint8),
         _dev(k_scale, "k_scale", torch.float32), _dev(v_scale, "v_scale", torch.float32),
@@ -405,7 +469,7 @@ def paged_kv_write_attention_fp8(k, v, k_codes, v_codes, k_scale, v_scale, slot_
         _dev(block_table, "block_table", torch.int32), block_table.shape[1],
         _c_p(qsl_h.data_ptr()), _c_p(sl_h.data_ptr()), sl_h.numel(), n, int(max_query_len), int(max_seq_len),
         hq, hkv, d, bs, nbt, float(scale), int(window), _dev(workspace, "workspace", torch.uint8), workspace.numel(),
-        _stream(stream))
+        _opts(), _stream(stream))
     _check(st, "paged_kv_write_attention_fp8")
 
 
@@ -458,7 +522,7 @@ def ragged_paged_attention_fp8(out, q, k_codes, v_codes, k_scale, v_scale, query
     if qsl_h.numel() != sl_h.numel() + 1:
         raise ValueError("query_start_loc needs num_reqs + 1 entries")
     _check_meta(query_start_loc, seq_lens, block_table, sl_h.numel())
-    st = L.pkv_ragged_paged_attention_fp8(
+    st = L.pkv_ragged_paged_attention_fp8_ex(
         _dev(out, "out", torch.bfloat16), _dev(q, "q", torch.bfloat16),
         _dev(k_codes, "k_codes", torch.uint8), _dev(v_codes, "v_codes", torch.uint8),
         _dev(k_scale, "k_scale", torch.float32), _dev(v_scale, "v_scale", torch.float32),
@@ -466,5 +530,5 @@ def ragged_paged_attention_fp8(out, q, k_codes, v_codes, k_scale, v_scale, query
         _dev(block_table, "block_table", torch.int32), block_table.shape[1],
         _c_p(qsl_h.data_ptr()), _c_p(sl_h.data_ptr()), sl_h.numel(), n, int(max_query_len), int(max_seq_len),
         hq, hkv, d, bs, nbt, float(scale), int(window), _dev(workspace, "workspace", torch.uint8),
-        workspace.numel(), _stream(stream))
+        workspace.numel(), _opts(), _stream(stream))
     _check(st, "ragged_paged_attention_fp8")

@@ -1527,7 +1527,7 @@ static cudaError_t launch_stream_d(const AttnParams &p, const WorkList &wl, int 
 // walks a long key range, the slot-ring kernel with two blocks per
 // iteration when ranges are short and latency dominates; key-major tiles
 // when every listed request has at most kKeyMajorRows rows per KV head
-// (PKV_DECODE_ROW_TILES=1 keeps the 16-row tiles, for comparison).
+// (the decode_row_tiles call option keeps the 16-row tiles, for comparison).
 // Quantized pools stream key-major tiles two KV heads per CTA, with the
 // maps km2 / vm2 whose boxes span two heads.
 // Prefill-class CTAs: 2 row tiles x 2 key groups, two blocks per iteration.
@@ -1540,8 +1540,7 @@ static cudaError_t launch_mma_d(const AttnParams &p, const WorkList &wl, int num
     if (wl.mode != kModeDecode) return launch_mma_dk<D, 2, NB, FP8>(p, wl, num_items, km, vm, ksm, vsm, stream);
     int max_t = 0;
     for (int i = 0; i < wl.n; i++) max_t = wl.qt[i] > max_t ? wl.qt[i] : max_t;
-    const char *env = getenv("PKV_DECODE_ROW_TILES");
-    const bool km_tiles = max_t * p.group <= kKeyMajorRows && !(env && *env && atoi(env) != 0);
+    const bool km_tiles = max_t * p.group <= kKeyMajorRows && !launch_choices().decode_row_tiles;
     if (wl.split_tokens >= kLongSplit && wl.cluster == 0) {
         if constexpr (FP8) {
             if (km_tiles) return launch_stream_d<D, FP8, true, 2>(p, wl, num_items, km2, vm2, ksm, vsm, stream);

@@ -140,15 +140,7 @@ static bool is_host_memory(const void *ptr)
 // 2048-token-chunk step with its copies overlapped took 875 us against 575 us
 // with 12 CTAs (511 us without copies), and the 48-request engine step 14.3
 // against 11.4 us (10.3 us without copies).
-static int link_copy_ctas()
-{
-    static const int n = [] {
-        const char *s = getenv("PKV_LINK_COPY_CTAS");
-        const int v = (s && *s) ? atoi(s) : 0;
-        return v > 0 ? std::min(v, 152 * 16) : 12;
-    }();
-    return n;
-}
+constexpr int kLinkCopyCtas = 12;
 
 cudaError_t launch_byte_copy(void *dst, const void *src, size_t bytes, cudaStream_t stream)
 {
@@ -159,7 +151,7 @@ cudaError_t launch_byte_copy(void *dst, const void *src, size_t bytes, cudaStrea
     launch_begin(stream, kByteCopy);
     if (link) {
         int64_t blocks = (chunks + 8 * 256 - 1) / (8 * 256);
-        blocks = std::min<int64_t>(blocks, link_copy_ctas());
+        blocks = std::min<int64_t>(blocks, kLinkCopyCtas);
         e = launch_maybe_pdl(byte_copy_kernel<8, 256>, dim3((unsigned)blocks), dim3(256), 0, stream,
                              static_cast<uint4 *>(dst), static_cast<const uint4 *>(src), chunks);
     } else {

@@ -303,10 +303,6 @@ cudaError_t launch_kv_write_fp8(const void *k, const void *v, void *k_codes, voi
                                 float *v_scale, const int64_t *slot_mapping, int32_t num_tokens, int32_t hkv,
                                 int64_t num_slots, uint32_t *err, cudaStream_t stream);
 
-// CUDA-core attention over one work list; rows = largest tokens*group of an item.
-cudaError_t launch_attn_fma(const AttnParams &p, const WorkList &wl, int head_dim, int rows,
-                            int num_items, cudaStream_t stream);
-
 // TMA-staged attention with warp-level MMA (decode-class: 4 key groups per
 // CTA; prefill-class: 4 row tiles of 16 per CTA).
 cudaError_t launch_attn_mma(const AttnParams &p, const WorkList &wl, int head_dim, int num_items,
@@ -345,8 +341,6 @@ cudaError_t launch_attn_combine(const AttnParams &p, const WorkList &wl, int hea
 // Kernel ids for launch accounting and the optional per-launch event timing.
 enum KernelId : int {
     kKvWrite = 0,
-    kAttnFmaDecode = 1,
-    kAttnFmaPrefill = 2,
     kAttnCombine = 3,
     kAttnTcPrefill = 4,
     kAttnMmaDecode = 5,
@@ -361,10 +355,42 @@ enum KernelId : int {
 void launch_begin(cudaStream_t stream, int kernel_id);
 void launch_end(cudaStream_t stream);
 
+// Per-call choices that override the planner's (pkv_attention_options in
+// include/pkv.h); a default-constructed value leaves every choice to the
+// planner.
+struct CallOptions {
+    bool disable_tcgen05 = false;     // prefill on the warp-MMA kernel
+    int tc_min_rows = 0;              // > 0: rows from which a prefill request goes to tcgen05
+    bool fp8_prefill_on_mma = false;  // quantized-pool prefill stays on the warp-MMA kernel
+    int split_tokens = 0;             // > 0: fixed decode split length
+    int cluster = 0;                  // 0: planner; -1: no clusters; k >= 2: clusters of k splits
+    int decode_main = 0;              // 0: planner; 1: decodes on the caller's stream; -1: prefill there
+    bool no_overlap = false;          // both classes on the caller's stream
+    bool prefill_key_splits = false;  // key splits for warp-MMA prefill tiles
+    bool separate_write = false;      // combined call as scatter + attention
+    bool decode_row_tiles = false;    // 16-row decode tiles instead of key-major ones
+    bool no_pdl = false;              // no programmatic dependent launches
+};
+
+// Launch-level choices of the attention call in progress on this thread,
+// set for the duration of the call (ScopedLaunchChoices); outside a call,
+// and for the write, copy and block-copy calls, the defaults hold.
+struct LaunchChoices {
+    bool pdl = true;                  // programmatic stream serialization for dependent launches
+    bool decode_row_tiles = false;    // see CallOptions
+};
+LaunchChoices &launch_choices();
+
+struct ScopedLaunchChoices {
+    LaunchChoices saved;
+    explicit ScopedLaunchChoices(const LaunchChoices &c) : saved(launch_choices()) { launch_choices() = c; }
+    ~ScopedLaunchChoices() { launch_choices() = saved; }
+};
+
 // Whether kernels that read what an earlier kernel of the same stream wrote
 // are launched with programmatic stream serialization (they start early and
-// wait in-kernel with griddepcontrol.wait).  Off with PKV_NO_PDL=1.
-bool pdl_enabled();
+// wait in-kernel with griddepcontrol.wait).
+inline bool pdl_enabled() { return launch_choices().pdl; }
 
 template <typename... KArgs, typename... Args>
 cudaError_t launch_maybe_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,

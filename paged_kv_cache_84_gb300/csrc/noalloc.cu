@@ -72,7 +72,7 @@ extern "C" pkv_status pkv_ragged_paged_attention_noalloc(
     if (num_tokens > 0) {
         pkv_attention_plan plan;
         st = pkv_plan_attention(query_start_loc_host, seq_lens_host, num_reqs, num_q_heads, num_kv_heads, head_dim,
-                                block_size, window, 0, 0, kScratchBytes, 0, &plan);
+                                block_size, window, 0, 0, kScratchBytes, 0, nullptr, &plan);
         if (st != PKV_OK) return st;
         const size_t front = plan.split_counters ? kZeroPrefix : pkv::kErrBytes;
         if (plan.partial_bytes > kScratchBytes - front - 64) return PKV_ERR_WORKSPACE;

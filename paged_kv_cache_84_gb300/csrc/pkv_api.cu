@@ -71,10 +71,29 @@ void launch_end(cudaStream_t stream)
     g_prof.open = -1;
 }
 
-bool pdl_enabled()
+LaunchChoices &launch_choices()
 {
-    const char *s = getenv("PKV_NO_PDL");
-    return !(s && *s && atoi(s) != 0);
+    static thread_local LaunchChoices c;
+    return c;
+}
+
+// The internal form of a caller's options (NULL: every choice to the planner).
+static CallOptions call_options(const pkv_attention_options *o)
+{
+    CallOptions c;
+    if (!o) return c;
+    c.disable_tcgen05 = o->disable_tcgen05 != 0;
+    c.tc_min_rows = o->tc_min_rows > 0 ? o->tc_min_rows : 0;
+    c.fp8_prefill_on_mma = o->fp8_prefill_on_mma != 0;
+    c.split_tokens = o->split_tokens > 0 ? o->split_tokens : 0;
+    c.cluster = o->cluster;
+    c.decode_main = o->decode_main > 0 ? 1 : (o->decode_main < 0 ? -1 : 0);
+    c.no_overlap = o->no_overlap != 0;
+    c.prefill_key_splits = o->prefill_key_splits != 0;
+    c.separate_write = o->separate_write != 0;
+    c.decode_row_tiles = o->decode_row_tiles != 0;
+    c.no_pdl = o->no_pdl != 0;
+    return c;
 }
 
 static thread_local char g_cuda_err[256] = "";
@@ -98,32 +117,52 @@ static int num_sms()
     return cached[dev];
 }
 
-// One non-blocking side stream and a fork/join event pair per device,
-// created on first use (host-side CUDA objects, no device memory).
+// Side streams of the decode/prefill overlap: one non-blocking stream and a
+// fork/join event pair for each (device, caller stream), created on first
+// use (host-side CUDA objects, no device memory) and kept until exit.  Each
+// has its own mutex, held for the whole call, so only callers on the same
+// stream share one; callers on different streams never wait for each other
+// through it.  When the table is full the call runs both classes on the
+// caller's stream (no overlap).
 struct SideStream {
     std::mutex mu;
+    int dev = -1;
+    cudaStream_t owner = nullptr;     // the caller stream it serves
     cudaStream_t stream = nullptr;
     cudaEvent_t fork = nullptr, join = nullptr;
 };
+constexpr int kMaxSideStreams = 256;
 
-static SideStream *side_stream()
+static SideStream *side_stream_for(cudaStream_t caller)
 {
-    static SideStream sides[64];
-    static std::mutex init_mu;
+    static SideStream table[kMaxSideStreams];
+    static int used = 0;
+    static std::mutex table_mu;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    SideStream &s = sides[dev];
-    std::lock_guard<std::mutex> lock(init_mu);
-    if (!s.stream) {
-        cudaStream_t st;
-        cudaEvent_t a, b;
-        if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
-        if (cudaEventCreateWithFlags(&a, cudaEventDisableTiming) != cudaSuccess) return nullptr;
-        if (cudaEventCreateWithFlags(&b, cudaEventDisableTiming) != cudaSuccess) return nullptr;
-        s.fork = a;
-        s.join = b;
-        s.stream = st;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    std::lock_guard<std::mutex> lock(table_mu);
+    for (int i = 0; i < used; i++)
+        if (table[i].dev == dev && table[i].owner == caller) return &table[i];
+    if (used == kMaxSideStreams) return nullptr;
+    SideStream &s = table[used];
+    cudaStream_t st;
+    cudaEvent_t a, b;
+    if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+    if (cudaEventCreateWithFlags(&a, cudaEventDisableTiming) != cudaSuccess) {
+        cudaStreamDestroy(st);
+        return nullptr;
     }
+    if (cudaEventCreateWithFlags(&b, cudaEventDisableTiming) != cudaSuccess) {
+        cudaEventDestroy(a);
+        cudaStreamDestroy(st);
+        return nullptr;
+    }
+    s.dev = dev;
+    s.owner = caller;
+    s.fork = a;
+    s.join = b;
+    s.stream = st;
+    used++;
     return &s;
 }
 
@@ -140,38 +179,31 @@ constexpr int kMaxPrefillRowSplits = 4;   // workspace sizing of split prefill t
 // several 32-row warp-MMA CTAs that each re-read the request's keys.
 constexpr int kTcMinRows = kDecodeRows + 1;
 
-// Quantized pools: prefill requests that the tcgen05 kernel takes when the
-// workspace holds bf16 copies of their blocks (fp8_tc_scratch bytes at the
-// workspace's end: K and V blocks [blocks][16][hkv][d] bf16, then a block
-// table [num_reqs][width] int32).  Returns 0 when no request qualifies.
-static int env_int(const char *name, int dflt);
-static size_t fp8_tc_scratch(const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs, int32_t g, int32_t hkv,
-                             int32_t d, int64_t *blocks_out = nullptr, int32_t *width_out = nullptr);
+static int tc_min_rows(const CallOptions &o) { return o.tc_min_rows > 0 ? o.tc_min_rows : kTcMinRows; }
 
 // Kernel class of request r (host rule shared by the planner and pkv_plan_request_kernels).
-static int env_int(const char *name, int dflt);
-
-static int request_class(int32_t t, int32_t L, int32_t g, int32_t d, bool fp8 = false)
+static int request_class(int32_t t, int32_t L, int32_t g, int32_t d, const CallOptions &o, bool fp8 = false)
 {
     if (t == 0) return PKV_CLASS_NONE;
     if (L == 0) return PKV_CLASS_PADDING;
     if (t * g <= kDecodeRows) return PKV_CLASS_DECODE;
     // a request fills at least kTcMinRows of a 128-row tensor-core tile
-    const int min_rows = env_int("PKV_TC_MIN_ROWS", kTcMinRows);
-    if (!fp8 && tc_prefill_supported(d, g) && t * g >= min_rows && !env_int("PKV_ATTN_CUDA_CORE", 0) &&
-        !env_int("PKV_DISABLE_TCGEN05", 0))
+    if (!fp8 && tc_prefill_supported(d, g) && t * g >= tc_min_rows(o) && !o.disable_tcgen05)
         return PKV_CLASS_PREFILL_TENSOR;
-    return PKV_CLASS_PREFILL_CUDA_CORE;
+    return PKV_CLASS_PREFILL_MMA;
 }
 
+// Quantized pools: prefill requests that the tcgen05 kernel takes when the
+// workspace holds bf16 copies of their blocks (fp8_tc_scratch bytes at the
+// workspace's end: K and V blocks [blocks][16][hkv][d] bf16, then a block
+// table [num_reqs][width] int32).  Returns 0 when no request qualifies.
 static size_t fp8_tc_scratch(const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs, int32_t g, int32_t hkv,
-                             int32_t d, int64_t *blocks_out, int32_t *width_out)
+                             int32_t d, const CallOptions &o, int64_t *blocks_out = nullptr,
+                             int32_t *width_out = nullptr)
 {
     // quantized pools have head_dim 128 (128-byte code rows)
-    if (d != 128 || !tc_prefill_supported(d, g) || env_int("PKV_DISABLE_TCGEN05", 0) ||
-        env_int("PKV_FP8_PREFILL_TC", 1) == 0)
-        return 0;
-    const int min_rows = env_int("PKV_TC_MIN_ROWS", kTcMinRows);
+    if (d != 128 || !tc_prefill_supported(d, g) || o.disable_tcgen05 || o.fp8_prefill_on_mma) return 0;
+    const int min_rows = tc_min_rows(o);
     int64_t blocks = 0;
     int32_t width = 0;
     for (int r = 0; r < num_reqs; r++) {
@@ -187,12 +219,6 @@ static size_t fp8_tc_scratch(const int32_t *qsl_h, const int32_t *sl_h, int32_t 
     const size_t kv = (size_t)blocks * 16 * hkv * d * 2;                 // one of K, V
     const size_t table = (size_t)num_reqs * width * 4;
     return 256 + 2 * ((kv + 255) / 256 * 256) + (table + 255) / 256 * 256;
-}
-
-static int env_int(const char *name, int dflt)
-{
-    const char *s = getenv(name);
-    return (s && *s) ? atoi(s) : dflt;
 }
 
 }  // namespace pkv
@@ -222,8 +248,6 @@ const char *pkv_kernel_name(int32_t kernel_id)
 {
     switch (kernel_id) {
     case kKvWrite: return "paged_kv_write";
-    case kAttnFmaDecode: return "attn_fma_decode";
-    case kAttnFmaPrefill: return "attn_fma_prefill";
     case kAttnCombine: return "attn_split_combine";
     case kAttnTcPrefill: return "attn_tc_prefill";
     case kAttnMmaDecode: return "attn_mma_decode";
@@ -336,7 +360,7 @@ size_t pkv_fp8_prefill_scratch_bytes(const int32_t *qsl_h, const int32_t *sl_h, 
 {
     if (!qsl_h || !sl_h || num_reqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads)
         return 0;
-    return fp8_tc_scratch(qsl_h, sl_h, num_reqs, num_q_heads / num_kv_heads, num_kv_heads, head_dim);
+    return fp8_tc_scratch(qsl_h, sl_h, num_reqs, num_q_heads / num_kv_heads, num_kv_heads, head_dim, CallOptions());
 }
 
 pkv_status pkv_plan_request_kernels(const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs,
@@ -347,7 +371,9 @@ pkv_status pkv_plan_request_kernels(const int32_t *qsl_h, const int32_t *sl_h, i
     if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads || head_dim <= 0)
         return PKV_ERR_INVALID_ARG;
     const int32_t g = num_q_heads / num_kv_heads;
-    for (int r = 0; r < num_reqs; r++) class_out[r] = request_class(qsl_h[r + 1] - qsl_h[r], sl_h[r], g, head_dim);
+    const CallOptions defaults;
+    for (int r = 0; r < num_reqs; r++)
+        class_out[r] = request_class(qsl_h[r + 1] - qsl_h[r], sl_h[r], g, head_dim, defaults);
     return PKV_OK;
 }
 
@@ -421,8 +447,7 @@ static pkv_status validate_attention(const void *out, const void *q, const void 
         return PKV_ERR_UNSUPPORTED;
     // quantized pools: head_dim 128 (128-byte code rows), scales staged in
     // boxes of 4 KV heads (KV heads a multiple of 4), warp-MMA kernels
-    if (fp8 && (d != 128 || hkv % 4 != 0 || !aligned(k_scale, 16) || !aligned(v_scale, 16) ||
-                env_int("PKV_ATTN_CUDA_CORE", 0)))
+    if (fp8 && (d != 128 || hkv % 4 != 0 || !aligned(k_scale, 16) || !aligned(v_scale, 16)))
         return PKV_ERR_UNSUPPORTED;
     return PKV_OK;
 }
@@ -440,12 +465,13 @@ struct RequestClasses {
 };
 
 static RequestClasses classify_requests(const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs, int32_t g,
-                                        int32_t hkv, int32_t d, int32_t window, bool fp8, size_t workspace_bytes)
+                                        int32_t hkv, int32_t d, int32_t window, bool fp8, size_t workspace_bytes,
+                                        const CallOptions &o)
 {
     RequestClasses c;
     for (int r = 0; r < num_reqs; r++) {
         int32_t t = qsl_h[r + 1] - qsl_h[r], L = sl_h[r];
-        switch (request_class(t, L, g, d, fp8)) {
+        switch (request_class(t, L, g, d, o, fp8)) {
         case PKV_CLASS_PADDING:
         case PKV_CLASS_DECODE: {
             c.dec.push_back(r);
@@ -454,7 +480,7 @@ static RequestClasses classify_requests(const int32_t *qsl_h, const int32_t *sl_
             c.dec_max_keys = keys > c.dec_max_keys ? keys : c.dec_max_keys;
             break;
         }
-        case PKV_CLASS_PREFILL_CUDA_CORE: c.pre.push_back(r); break;
+        case PKV_CLASS_PREFILL_MMA: c.pre.push_back(r); break;
         case PKV_CLASS_PREFILL_TENSOR: c.tcp.push_back(r); break;
         default: break;                                         // no rows at all
         }
@@ -463,10 +489,10 @@ static RequestClasses classify_requests(const int32_t *qsl_h, const int32_t *sl_
     // when the workspace has room for bf16 copies of their blocks at its end
     // (a dequantizing pass fills them); else they stay on the warp-MMA kernel.
     if (fp8 && !c.pre.empty()) {
-        c.fp8_scratch = fp8_tc_scratch(qsl_h, sl_h, num_reqs, g, hkv, d, &c.fp8_blocks, &c.fp8_width);
+        c.fp8_scratch = fp8_tc_scratch(qsl_h, sl_h, num_reqs, g, hkv, d, o, &c.fp8_blocks, &c.fp8_width);
         if (c.fp8_scratch > 0 && c.fp8_blocks * 16 < INT32_MAX &&
             workspace_bytes >= c.fp8_scratch + kErrBytes + kCounterBytes + 4096) {
-            const int min_rows = env_int("PKV_TC_MIN_ROWS", kTcMinRows);
+            const int min_rows = tc_min_rows(o);
             std::vector<int32_t> keep;
             for (int32_t r : c.pre) {
                 const int32_t t = qsl_h[r + 1] - qsl_h[r];
@@ -506,15 +532,15 @@ static void class_times(const RequestClasses &c, const int32_t *qsl_h, const int
 // Keys per decode split, common to every split request (a multiple of 128
 // before block rounding): about 16 CTAs per SM over the decode class's keys.
 static int decode_split_tokens(const RequestClasses &c, double dec_us, double pre_us, int32_t hkv, bool fp8,
-                               bool use_fma, int sms)
+                               const CallOptions &o, int sms)
 {
-    int split = env_int("PKV_SPLIT_TOKENS", 0);
+    int split = o.split_tokens;
     if (split <= 0) {
         // Decodes beside a longer prefill only fill the SMs its last wave
         // leaves: fewer, longer splits (measured on the mixed 2048-token-chunk
         // step: 509 us with splits of ~2048 keys, 514 us with 16 CTAs per SM)
         const bool filler = !c.tcp.empty() && pre_us > dec_us;
-        int64_t target_ctas = (int64_t)sms * (use_fma ? 8 : (filler ? 4 : 16));
+        int64_t target_ctas = (int64_t)sms * (filler ? 4 : 16);
         // quantized pools stream two KV heads per CTA: half the CTAs per split
         const int64_t head_ctas = fp8 ? hkv / 2 : hkv;
         int64_t s = (c.dec_keys * head_ctas + target_ctas - 1) / (target_ctas > 0 ? target_ctas : 1);
@@ -525,7 +551,7 @@ static int decode_split_tokens(const RequestClasses &c, double dec_us, double pr
     // completes a request's last split reads every split's partial rows;
     // measured with 8 requests of 32768 keys (FP8 pool), 64 splits of 512
     // keys took 154 us against 129 us with 37 of 896.
-    if (split >= kLongSplitTokens && env_int("PKV_SPLIT_TOKENS", 0) <= 0) {
+    if (split >= kLongSplitTokens && o.split_tokens <= 0) {
         const int64_t floor_split = (c.dec_max_keys + kMaxStreamSplits - 1) / kMaxStreamSplits;
         if (floor_split > split) split = (int)((floor_split + 127) / 128 * 128);
     }
@@ -540,7 +566,6 @@ static int decode_split_tokens(const RequestClasses &c, double dec_us, double pr
 struct AttnPlan {
     RequestClasses rc;
     double dec_us = 0.0, pre_us = 0.0;  // rough class times (only the ratio is used)
-    bool use_fma = false;               // CUDA-core kernels instead of the staged MMA ones
     int split = 0;                      // keys per split, a multiple of the block size
     int tile = 1;                       // warp-MMA (or CUDA-core) prefill tile, tokens
     bool pre_split = false;             // warp-MMA prefill tiles split over keys
@@ -552,7 +577,7 @@ struct AttnPlan {
     bool fork = false;                  // decode and prefill classes on two streams
     bool decode_main = false;           // ... the decodes on the caller's stream
     bool fork_after_scatter = false;    // ... the decodes fork after the ranged scatter
-    int cluster_env = -1;               // PKV_CLUSTER
+    int cluster_opt = 0;                // the caller's cluster choice (CallOptions::cluster)
 };
 
 static int32_t decode_splits_of(const int32_t *qsl_h, const int32_t *sl_h, int32_t r, int32_t window, int sp)
@@ -575,26 +600,26 @@ static size_t plan_partial_rows(const AttnPlan &pl, const int32_t *qsl_h, const 
 }
 
 static AttnPlan make_plan(const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs, int32_t hq, int32_t hkv,
-                          int32_t d, int32_t bs, int32_t window, bool fp8, bool fused, size_t workspace_bytes, int sms)
+                          int32_t d, int32_t bs, int32_t window, bool fp8, bool fused, size_t workspace_bytes, int sms,
+                          const CallOptions &o)
 {
     AttnPlan pl;
     const int32_t g = hq / hkv;
-    pl.rc = classify_requests(qsl_h, sl_h, num_reqs, g, hkv, d, window, fp8, workspace_bytes);
+    pl.rc = classify_requests(qsl_h, sl_h, num_reqs, g, hkv, d, window, fp8, workspace_bytes, o);
     const RequestClasses &rc = pl.rc;
     for (int r = 0; r < num_reqs; r++) pl.seen_l = sl_h[r] > pl.seen_l ? sl_h[r] : pl.seen_l;
     class_times(rc, qsl_h, sl_h, hq, hkv, d, &pl.dec_us, &pl.pre_us);
-    pl.use_fma = env_int("PKV_ATTN_CUDA_CORE", 0) != 0;
-    int split = decode_split_tokens(rc, pl.dec_us, pl.pre_us, hkv, fp8, pl.use_fma, sms);
+    int split = decode_split_tokens(rc, pl.dec_us, pl.pre_us, hkv, fp8, o, sms);
     if (split % bs) split += bs - split % bs;
     // Prefill-class tiles are split over keys as well when the batch has too
     // few of them to fill the GPU (small, latency-bound steps): every tile of
     // such a request gets the request's number of splits.
-    pl.tile = pl.use_fma ? kDecodeRows / g : (mma_prefill_rows() / g > 0 ? mma_prefill_rows() / g : 1);
+    pl.tile = mma_prefill_rows() / g > 0 ? mma_prefill_rows() / g : 1;
     int64_t pre_ctas = 0;
     for (int32_t r : rc.pre) pre_ctas += (int64_t)((qsl_h[r + 1] - qsl_h[r] + pl.tile - 1) / pl.tile) * hkv;
     // Measured on the 48-request engine step it costs more (extra CTAs and a
     // combine on the critical path) than it saves, so it is opt-in.
-    pl.pre_split = !pl.use_fma && !rc.pre.empty() && pre_ctas < 2 * (int64_t)sms && env_int("PKV_PREFILL_SPLIT", 0);
+    pl.pre_split = !rc.pre.empty() && pre_ctas < 2 * (int64_t)sms && o.prefill_key_splits;
     // The layout depends on the workspace size only: [error word][counters,
     // if the workspace holds them][partials]; quantized prefill on tcgen05:
     // its scratch takes the workspace's end.
@@ -616,11 +641,10 @@ static AttnPlan make_plan(const int32_t *qsl_h, const int32_t *sl_h, int32_t num
     pl.total_rows = plan_partial_rows(pl, qsl_h, sl_h, hq, window, split, &unused);
     // Decode-class work runs on a second stream, concurrently with the
     // prefill kernels, when both are present; the class expected to take
-    // longer goes on the caller's stream (PKV_DECODE_MAIN=0/1 forces it).
-    pl.fork = !rc.dec.empty() && (!rc.tcp.empty() || !rc.pre.empty()) && !env_int("PKV_NO_OVERLAP", 0);
+    // longer goes on the caller's stream (the decode_main option forces it).
+    pl.fork = !rc.dec.empty() && (!rc.tcp.empty() || !rc.pre.empty()) && !o.no_overlap;
     if (pl.fork) {
-        const int forced = env_int("PKV_DECODE_MAIN", -1);
-        pl.decode_main = forced >= 0 ? forced != 0 : pl.dec_us > pl.pre_us;
+        pl.decode_main = o.decode_main != 0 ? o.decode_main > 0 : pl.dec_us > pl.pre_us;
         // Combined call with the prefill class on the caller's stream: the
         // decodes fork after the ranged scatter, as they would after a full
         // scatter, so that the prefill kernel takes the SMs first (measured
@@ -628,7 +652,7 @@ static AttnPlan make_plan(const int32_t *qsl_h, const int32_t *sl_h, int32_t num
         // the decodes starting at once).
         pl.fork_after_scatter = fused && !pl.decode_main;
     }
-    pl.cluster_env = env_int("PKV_CLUSTER", -1);
+    pl.cluster_opt = o.cluster;
     return pl;
 }
 
@@ -639,15 +663,13 @@ static AttnPlan make_plan(const int32_t *qsl_h, const int32_t *sl_h, int32_t num
 // launch's largest split count, its keys divided evenly.  Measured on the
 // 48-request engine step, clusters of more than two CTAs do not run beside
 // the prefill kernel (the step took the sum of both kernels' times), so next
-// to prefill work the cluster holds at most two splits.  PKV_CLUSTER=0
-// turns clusters off, n >= 2 forces n.
+// to prefill work the cluster holds at most two splits.  The cluster option
+// turns clusters off (-1) or forces n >= 2 CTAs.
 static int decode_cluster_size(const AttnPlan &pl, int s_max)
 {
-    const int cs = pl.cluster_env >= 2 ? std::min(pl.cluster_env, kMaxClusterSplits)
+    const int cs = pl.cluster_opt >= 2 ? std::min(pl.cluster_opt, kMaxClusterSplits)
                                        : (pl.fork ? std::min(s_max, 2) : s_max);
-    return !pl.use_fma && pl.split < kLongSplitTokens && pl.cluster_env != 0 && cs >= 2 && cs <= kMaxClusterSplits
-               ? cs
-               : 0;
+    return pl.split < kLongSplitTokens && pl.cluster_opt >= 0 && cs >= 2 && cs <= kMaxClusterSplits ? cs : 0;
 }
 
 static pkv_status attention_impl(void *out, const void *q, const void *k_cache, const void *v_cache,
@@ -656,8 +678,9 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
                                  const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs, int32_t num_tokens,
                                  int32_t max_query_len, int32_t max_seq_len, int32_t hq, int32_t hkv, int32_t d,
                                  int32_t bs, int32_t num_blocks_total, float scale, int32_t window, void *workspace,
-                                 size_t workspace_bytes, cudaStream_t stream, const void *fw_k = nullptr,
-                                 const void *fw_v = nullptr, const int64_t *fw_slots = nullptr)
+                                 size_t workspace_bytes, cudaStream_t stream, const CallOptions &opts,
+                                 const void *fw_k = nullptr, const void *fw_v = nullptr,
+                                 const int64_t *fw_slots = nullptr)
 {
     const bool fp8 = k_scale != nullptr;
     bool nothing_to_do = false;
@@ -669,14 +692,18 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
         return st;
     const int32_t g = hq / hkv;
     const bool fused = fw_k != nullptr;
-    const AttnPlan pl = make_plan(qsl_h, sl_h, num_reqs, hq, hkv, d, bs, window, fp8, fused, workspace_bytes, num_sms());
+    const AttnPlan pl =
+        make_plan(qsl_h, sl_h, num_reqs, hq, hkv, d, bs, window, fp8, fused, workspace_bytes, num_sms(), opts);
+    LaunchChoices lc;
+    lc.pdl = !opts.no_pdl;
+    lc.decode_row_tiles = opts.decode_row_tiles;
+    const ScopedLaunchChoices scoped(lc);
     const std::vector<int32_t> &dec = pl.rc.dec, &pre = pl.rc.pre, &tcp = pl.rc.tcp;
     const size_t fp8_scratch = pl.rc.fp8_scratch;
     const int64_t fp8_blocks = pl.rc.fp8_blocks;
     const int32_t fp8_width = pl.rc.fp8_width;
     if (!tcp.empty() && ((int64_t)num_blocks_total * bs >= INT32_MAX || num_tokens >= INT32_MAX / 2))
         return PKV_ERR_UNSUPPORTED;
-    const bool use_fma = pl.use_fma;
     const int split = pl.split;
     const int tile = pl.tile;
     const bool pre_split = pl.pre_split;
@@ -733,12 +760,11 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
     // Fork and join with events, so the caller's stream order (and CUDA-graph
     // capture) is preserved.
     cudaStream_t dstream = stream, pstream = stream;         // decode-class / prefill-class work
-    SideStream *side = nullptr;
-    const bool fork = pl.fork;
-    const bool fork_after_scatter = pl.fork_after_scatter;
+    // (without a side stream for the caller's stream, both run on it in turn)
+    SideStream *side = pl.fork ? side_stream_for(stream) : nullptr;
+    const bool fork = side != nullptr;
+    const bool fork_after_scatter = fork && pl.fork_after_scatter;
     if (fork) {
-        side = side_stream();
-        if (!side) return cuda_fail(cudaErrorUnknown, "side stream");
         side->mu.lock();
         // The class on the caller's stream follows the K/V scatter as a
         // programmatic dependent (it starts while the scatter drains); the
@@ -923,7 +949,7 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
         wl.mode = kModeDecode;
         wl.split_tokens = split;
         wl.tile_tokens = 0;
-        int items = 0, rows = 1;
+        int items = 0;
         size_t c1 = c0 + kPlanMax < dec.size() ? c0 + kPlanMax : dec.size();
         int s_max = 1;
         for (size_t x = c0; x < c1; x++) s_max = std::max(s_max, dec_splits_of(dec[x], split));
@@ -939,7 +965,6 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
                 wl.item_off[li] = items;
                 wl.part_off[li] = -1;
                 items += cs;
-                if (sl_h[r] > 0 && t * g > rows) rows = t * g;
             }
             wl.item_off[wl.n] = items;
             cudaError_t e = launch_attn_mma(p, wl, d, items, k_cache, v_cache, num_slots, dstream, k_scale, v_scale);
@@ -957,19 +982,17 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
             wl.item_off[li] = items;
             // split decodes of the MMA kernels combine in the kernel (the CTA
             // finishing a request's last split) when counters are available
-            const bool in_kernel = S > 1 && !use_fma && has_counters && counter_cursor + hkv <= kCounterGroups;
+            const bool in_kernel = S > 1 && has_counters && counter_cursor + hkv <= kCounterGroups;
             wl.part_off[li] = take_partials(dec_combine, r, S, in_kernel);
             if (in_kernel) {
                 wl.cnt_off[li] = counter_cursor;
                 counter_cursor += hkv;
             }
             items += S;
-            if (sl_h[r] > 0 && t * g > rows) rows = t * g;
         }
         wl.item_off[wl.n] = items;
-        cudaError_t e = use_fma ? launch_attn_fma(p, wl, d, rows, items, dstream)
-                                : launch_attn_mma(p, wl, d, items, k_cache, v_cache, num_slots, dstream, k_scale,
-                                                  v_scale);
+        cudaError_t e =
+            launch_attn_mma(p, wl, d, items, k_cache, v_cache, num_slots, dstream, k_scale, v_scale);
         if (e != cudaSuccess) {
             join();
             return cuda_fail(e, "decode attention launch");
@@ -1001,9 +1024,8 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
             items += ((t + tile - 1) / tile) * S;
         }
         wl.item_off[wl.n] = items;
-        cudaError_t e = use_fma ? launch_attn_fma(pp, wl, d, kDecodeRows, items, pstream)
-                                : launch_attn_mma(pp, wl, d, items, k_cache, v_cache, num_slots, pstream, k_scale,
-                                                  v_scale);
+        cudaError_t e =
+            launch_attn_mma(pp, wl, d, items, k_cache, v_cache, num_slots, pstream, k_scale, v_scale);
         if (e != cudaSuccess) {
             join();
             return cuda_fail(e, "prefill attention launch");
@@ -1025,6 +1047,21 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
 
 extern "C" {
 
+pkv_status pkv_ragged_paged_attention_ex(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                         const int32_t *query_start_loc, const int32_t *seq_lens,
+                                         const int32_t *block_table, int32_t block_table_stride,
+                                         const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs,
+                                         int32_t num_tokens, int32_t max_query_len, int32_t max_seq_len, int32_t hq,
+                                         int32_t hkv, int32_t d, int32_t bs, int32_t num_blocks_total, float scale,
+                                         int32_t window, void *workspace, size_t workspace_bytes,
+                                         const pkv_attention_options *options, cudaStream_t stream)
+{
+    return attention_impl(out, q, k_cache, v_cache, nullptr, nullptr, query_start_loc, seq_lens, block_table,
+                          block_table_stride, qsl_h, sl_h, num_reqs, num_tokens, max_query_len, max_seq_len, hq, hkv,
+                          d, bs, num_blocks_total, scale, window, workspace, workspace_bytes, stream,
+                          call_options(options));
+}
+
 pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
                                       const int32_t *query_start_loc, const int32_t *seq_lens,
                                       const int32_t *block_table, int32_t block_table_stride,
@@ -1034,14 +1071,16 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q, const void *k_ca
                                       int32_t num_blocks_total, float scale, int32_t window,
                                       void *workspace, size_t workspace_bytes, cudaStream_t stream)
 {
-    return attention_impl(out, q, k_cache, v_cache, nullptr, nullptr, query_start_loc, seq_lens, block_table,
-                          block_table_stride, qsl_h, sl_h, num_reqs, num_tokens, max_query_len, max_seq_len, hq, hkv,
-                          d, bs, num_blocks_total, scale, window, workspace, workspace_bytes, stream);
+    return pkv_ragged_paged_attention_ex(out, q, k_cache, v_cache, query_start_loc, seq_lens, block_table,
+                                         block_table_stride, qsl_h, sl_h, num_reqs, num_tokens, max_query_len,
+                                         max_seq_len, hq, hkv, d, bs, num_blocks_total, scale, window, workspace,
+                                         workspace_bytes, nullptr, stream);
 }
 
 pkv_status pkv_plan_attention(const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs, int32_t hq, int32_t hkv,
                               int32_t d, int32_t bs, int32_t window, int32_t quantized, int32_t combined,
-                              size_t workspace_bytes, int32_t sms, pkv_attention_plan *out)
+                              size_t workspace_bytes, int32_t sms, const pkv_attention_options *options,
+                              pkv_attention_plan *out)
 {
     if (!out || !qsl_h || num_reqs < 0 || (num_reqs > 0 && !sl_h)) return PKV_ERR_INVALID_ARG;
     if (hq <= 0 || hkv <= 0 || hq % hkv || d <= 0 || bs <= 0 || window < 0) return PKV_ERR_INVALID_ARG;
@@ -1051,7 +1090,7 @@ pkv_status pkv_plan_attention(const int32_t *qsl_h, const int32_t *sl_h, int32_t
     }
     const int32_t g = hq / hkv;
     if ((d != 48 && d != 64 && d != 128) || bs != 16 || g > kDecodeRows) return PKV_ERR_UNSUPPORTED;
-    if (quantized && (d != 128 || hkv % 4 != 0 || env_int("PKV_ATTN_CUDA_CORE", 0))) return PKV_ERR_UNSUPPORTED;
+    if (quantized && (d != 128 || hkv % 4 != 0)) return PKV_ERR_UNSUPPORTED;
     if (sms <= 0) {
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -1061,7 +1100,7 @@ pkv_status pkv_plan_attention(const int32_t *qsl_h, const int32_t *sl_h, int32_t
         }
     }
     const AttnPlan pl = make_plan(qsl_h, sl_h, num_reqs, hq, hkv, d, bs, window, quantized != 0, combined != 0,
-                                  workspace_bytes, sms);
+                                  workspace_bytes, sms, call_options(options));
     memset(out, 0, sizeof *out);
     out->decode_requests = (int32_t)pl.rc.dec.size();
     out->prefill_tensor_requests = (int32_t)pl.rc.tcp.size();
@@ -1075,7 +1114,7 @@ pkv_status pkv_plan_attention(const int32_t *qsl_h, const int32_t *sl_h, int32_t
     }
     out->max_decode_splits = pl.rc.dec.empty() ? 0 : s_max;
     out->decode_cluster = pl.rc.dec.empty() ? 0 : decode_cluster_size(pl, s_first);
-    out->decode_streaming = !pl.rc.dec.empty() && !pl.use_fma && out->decode_cluster == 0 && pl.split >= kLongSplitTokens;
+    out->decode_streaming = !pl.rc.dec.empty() && out->decode_cluster == 0 && pl.split >= kLongSplitTokens;
     out->split_counters = pl.has_counters;
     out->overlap = pl.fork;
     out->decode_on_caller_stream = pl.fork && pl.decode_main;
@@ -1083,6 +1122,44 @@ pkv_status pkv_plan_attention(const int32_t *qsl_h, const int32_t *sl_h, int32_t
     out->quantized_prefill_scratch = pl.rc.fp8_scratch;
     out->partial_bytes = pl.total_rows ? ((pl.total_rows * d * 4 + 15) / 16) * 16 + pl.total_rows * 8 : 0;
     return PKV_OK;
+}
+
+pkv_status pkv_paged_kv_write_attention_ex(const void *k, const void *v, void *k_cache, void *v_cache,
+                                           const int64_t *slot_mapping, void *out, const void *q,
+                                           const int32_t *query_start_loc, const int32_t *seq_lens,
+                                           const int32_t *block_table, int32_t block_table_stride,
+                                           const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs,
+                                           int32_t num_tokens, int32_t max_query_len, int32_t max_seq_len,
+                                           int32_t hq, int32_t hkv, int32_t d, int32_t bs, int32_t num_blocks_total,
+                                           float scale, int32_t window, void *workspace, size_t workspace_bytes,
+                                           const pkv_attention_options *options, cudaStream_t stream)
+{
+    // the scatter's own checks, then the attention's (inside attention_impl)
+    if (num_tokens > 0 && (!k || !v || !slot_mapping || !k_cache || !v_cache)) return PKV_ERR_INVALID_ARG;
+    if (num_tokens > 0 && (!aligned(k, 16) || !aligned(v, 16) || !aligned(slot_mapping, 8)))
+        return PKV_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < PKV_WORKSPACE_MIN_BYTES || !aligned(workspace, 256)) return PKV_ERR_WORKSPACE;
+    const CallOptions opts = call_options(options);
+    if (opts.separate_write) {
+        // the full scatter, then the attention
+        if (num_tokens > 0) {
+            if (hq <= 0 || hkv <= 0 || hq % hkv != 0 || d <= 0 || bs <= 0 || num_blocks_total <= 0)
+                return PKV_ERR_INVALID_ARG;
+            LaunchChoices lc;
+            lc.pdl = !opts.no_pdl;
+            const ScopedLaunchChoices scoped(lc);
+            pkv_status st = pkv_paged_kv_write(k, v, k_cache, v_cache, slot_mapping, num_tokens, hkv, d, bs,
+                                               num_blocks_total, static_cast<uint32_t *>(workspace), stream);
+            if (st != PKV_OK) return st;
+        }
+        return attention_impl(out, q, k_cache, v_cache, nullptr, nullptr, query_start_loc, seq_lens, block_table,
+                              block_table_stride, qsl_h, sl_h, num_reqs, num_tokens, max_query_len, max_seq_len, hq,
+                              hkv, d, bs, num_blocks_total, scale, window, workspace, workspace_bytes, stream, opts);
+    }
+    return attention_impl(out, q, k_cache, v_cache, nullptr, nullptr, query_start_loc, seq_lens, block_table,
+                          block_table_stride, qsl_h, sl_h, num_reqs, num_tokens, max_query_len, max_seq_len, hq, hkv,
+                          d, bs, num_blocks_total, scale, window, workspace, workspace_bytes, stream, opts, k, v,
+                          slot_mapping);
 }
 
 pkv_status pkv_paged_kv_write_attention(const void *k, const void *v, void *k_cache, void *v_cache,
@@ -1095,29 +1172,48 @@ pkv_status pkv_paged_kv_write_attention(const void *k, const void *v, void *k_ca
                                         float scale, int32_t window, void *workspace, size_t workspace_bytes,
                                         cudaStream_t stream)
 {
-    // the scatter's own checks, then the attention's (inside attention_impl)
+    return pkv_paged_kv_write_attention_ex(k, v, k_cache, v_cache, slot_mapping, out, q, query_start_loc, seq_lens,
+                                           block_table, block_table_stride, qsl_h, sl_h, num_reqs, num_tokens,
+                                           max_query_len, max_seq_len, hq, hkv, d, bs, num_blocks_total, scale,
+                                           window, workspace, workspace_bytes, nullptr, stream);
+}
+
+pkv_status pkv_paged_kv_write_attention_fp8_ex(const void *k, const void *v, void *k_cache, void *v_cache,
+                                               float *k_scale, float *v_scale, const int64_t *slot_mapping, void *out,
+                                               const void *q, const int32_t *query_start_loc, const int32_t *seq_lens,
+                                               const int32_t *block_table, int32_t block_table_stride,
+                                               const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs,
+                                               int32_t num_tokens, int32_t max_query_len, int32_t max_seq_len,
+                                               int32_t hq, int32_t hkv, int32_t d, int32_t bs,
+                                               int32_t num_blocks_total, float scale, int32_t window, void *workspace,
+                                               size_t workspace_bytes, const pkv_attention_options *options,
+                                               cudaStream_t stream)
+{
+    if (!k_scale || !v_scale) return PKV_ERR_INVALID_ARG;
     if (num_tokens > 0 && (!k || !v || !slot_mapping || !k_cache || !v_cache)) return PKV_ERR_INVALID_ARG;
     if (num_tokens > 0 && (!aligned(k, 16) || !aligned(v, 16) || !aligned(slot_mapping, 8)))
         return PKV_ERR_UNSUPPORTED;
-    if (!workspace || workspace_bytes < PKV_WORKSPACE_MIN_BYTES || !aligned(workspace, 256)) return PKV_ERR_WORKSPACE;
-    uint32_t *err = static_cast<uint32_t *>(workspace);
-    if (env_int("PKV_ATTN_CUDA_CORE", 0) || env_int("PKV_SEPARATE_WRITE", 0)) {
-        // CUDA-core kernels (or on request): the full scatter, then the attention
-        pkv_status st = PKV_OK;
+    const CallOptions opts = call_options(options);
+    if (opts.separate_write) {
+        // the full quantizing scatter, then the attention
+        if (!workspace || workspace_bytes < PKV_WORKSPACE_MIN_BYTES || !aligned(workspace, 256))
+            return PKV_ERR_WORKSPACE;
         if (num_tokens > 0) {
-            if (hq <= 0 || hkv <= 0 || hq % hkv != 0 || d <= 0 || bs <= 0 || num_blocks_total <= 0)
-                return PKV_ERR_INVALID_ARG;
-            st = pkv_paged_kv_write(k, v, k_cache, v_cache, slot_mapping, num_tokens, hkv, d, bs, num_blocks_total,
-                                    err, stream);
+            LaunchChoices lc;
+            lc.pdl = !opts.no_pdl;
+            const ScopedLaunchChoices scoped(lc);
+            pkv_status st = pkv_paged_kv_write_fp8(k, v, k_cache, v_cache, k_scale, v_scale, slot_mapping, num_tokens,
+                                                   hkv, d, bs, num_blocks_total, static_cast<uint32_t *>(workspace),
+                                                   stream);
+            if (st != PKV_OK) return st;
         }
-        if (st != PKV_OK) return st;
-        return attention_impl(out, q, k_cache, v_cache, nullptr, nullptr, query_start_loc, seq_lens, block_table,
+        return attention_impl(out, q, k_cache, v_cache, k_scale, v_scale, query_start_loc, seq_lens, block_table,
                               block_table_stride, qsl_h, sl_h, num_reqs, num_tokens, max_query_len, max_seq_len, hq,
-                              hkv, d, bs, num_blocks_total, scale, window, workspace, workspace_bytes, stream);
+                              hkv, d, bs, num_blocks_total, scale, window, workspace, workspace_bytes, stream, opts);
     }
-    return attention_impl(out, q, k_cache, v_cache, nullptr, nullptr, query_start_loc, seq_lens, block_table,
+    return attention_impl(out, q, k_cache, v_cache, k_scale, v_scale, query_start_loc, seq_lens, block_table,
                           block_table_stride, qsl_h, sl_h, num_reqs, num_tokens, max_query_len, max_seq_len, hq, hkv,
-                          d, bs, num_blocks_total, scale, window, workspace, workspace_bytes, stream, k, v,
+                          d, bs, num_blocks_total, scale, window, workspace, workspace_bytes, stream, opts, k, v,
                           slot_mapping);
 }
 
@@ -1131,28 +1227,29 @@ pkv_status pkv_paged_kv_write_attention_fp8(const void *k, const void *v, void *
                                             int32_t window, void *workspace, size_t workspace_bytes,
                                             cudaStream_t stream)
 {
+    return pkv_paged_kv_write_attention_fp8_ex(k, v, k_cache, v_cache, k_scale, v_scale, slot_mapping, out, q,
+                                               query_start_loc, seq_lens, block_table, block_table_stride, qsl_h,
+                                               sl_h, num_reqs, num_tokens, max_query_len, max_seq_len, hq, hkv, d, bs,
+                                               num_blocks_total, scale, window, workspace, workspace_bytes, nullptr,
+                                               stream);
+}
+
+pkv_status pkv_ragged_paged_attention_fp8_ex(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                             const float *k_scale, const float *v_scale,
+                                             const int32_t *query_start_loc, const int32_t *seq_lens,
+                                             const int32_t *block_table, int32_t block_table_stride,
+                                             const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs,
+                                             int32_t num_tokens, int32_t max_query_len, int32_t max_seq_len,
+                                             int32_t hq, int32_t hkv, int32_t d, int32_t bs,
+                                             int32_t num_blocks_total, float scale, int32_t window,
+                                             void *workspace, size_t workspace_bytes,
+                                             const pkv_attention_options *options, cudaStream_t stream)
+{
     if (!k_scale || !v_scale) return PKV_ERR_INVALID_ARG;
-    if (num_tokens > 0 && (!k || !v || !slot_mapping || !k_cache || !v_cache)) return PKV_ERR_INVALID_ARG;
-    if (num_tokens > 0 && (!aligned(k, 16) || !aligned(v, 16) || !aligned(slot_mapping, 8)))
-        return PKV_ERR_UNSUPPORTED;
-    if (env_int("PKV_SEPARATE_WRITE", 0)) {
-        // the full quantizing scatter, then the attention
-        if (!workspace || workspace_bytes < PKV_WORKSPACE_MIN_BYTES || !aligned(workspace, 256))
-            return PKV_ERR_WORKSPACE;
-        if (num_tokens > 0) {
-            pkv_status st = pkv_paged_kv_write_fp8(k, v, k_cache, v_cache, k_scale, v_scale, slot_mapping, num_tokens,
-                                                   hkv, d, bs, num_blocks_total, static_cast<uint32_t *>(workspace),
-                                                   stream);
-            if (st != PKV_OK) return st;
-        }
-        return attention_impl(out, q, k_cache, v_cache, k_scale, v_scale, query_start_loc, seq_lens, block_table,
-                              block_table_stride, qsl_h, sl_h, num_reqs, num_tokens, max_query_len, max_seq_len, hq,
-                              hkv, d, bs, num_blocks_total, scale, window, workspace, workspace_bytes, stream);
-    }
     return attention_impl(out, q, k_cache, v_cache, k_scale, v_scale, query_start_loc, seq_lens, block_table,
                           block_table_stride, qsl_h, sl_h, num_reqs, num_tokens, max_query_len, max_seq_len, hq, hkv,
-                          d, bs, num_blocks_total, scale, window, workspace, workspace_bytes, stream, k, v,
-                          slot_mapping);
+                          d, bs, num_blocks_total, scale, window, workspace, workspace_bytes, stream,
+                          call_options(options));
 }
 
 pkv_status pkv_ragged_paged_attention_fp8(void *out, const void *q, const void *k_cache, const void *v_cache,
@@ -1165,10 +1262,10 @@ pkv_status pkv_ragged_paged_attention_fp8(void *out, const void *q, const void *
                                           int32_t num_blocks_total, float scale, int32_t window,
                                           void *workspace, size_t workspace_bytes, cudaStream_t stream)
 {
-    if (!k_scale || !v_scale) return PKV_ERR_INVALID_ARG;
-    return attention_impl(out, q, k_cache, v_cache, k_scale, v_scale, query_start_loc, seq_lens, block_table,
-                          block_table_stride, qsl_h, sl_h, num_reqs, num_tokens, max_query_len, max_seq_len, hq, hkv,
-                          d, bs, num_blocks_total, scale, window, workspace, workspace_bytes, stream);
+    return pkv_ragged_paged_attention_fp8_ex(out, q, k_cache, v_cache, k_scale, v_scale, query_start_loc, seq_lens,
+                                             block_table, block_table_stride, qsl_h, sl_h, num_reqs, num_tokens,
+                                             max_query_len, max_seq_len, hq, hkv, d, bs, num_blocks_total, scale,
+                                             window, workspace, workspace_bytes, nullptr, stream);
 }
 
 }  // extern "C"

@@ -21,3 +21,13 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture
+def attn_options():
+    """Overrides planner choices of the attention calls for one test: call it
+    with fields of pkv.AttentionOptions (merged); reset afterwards."""
+    import paged_kv_cache_84_gb300 as pkv
+    pkv.reset_options()
+    yield pkv.set_options
+    pkv.reset_options()

@@ -62,7 +62,7 @@ def test_host_only_functions(lib):
         ["prefill_tensor", "padding", "none"]
     # 18 rows (t = 6, g = 3) exceed a decode tile; g = 3 does not divide the
     # 128-row tensor-core tile, so the chunk runs on the warp-level MMA kernel
-    assert pkv.plan_request_kernels([0, 6], [40], 9, 3, 64) == ["prefill_cuda_core"]
+    assert pkv.plan_request_kernels([0, 6], [40], 9, 3, 64) == ["prefill_mma"]
 
 
 def _attn_args(qsl, sl, R, N, maxq, maxl, hq=8, hkv=4, d=64, bs=16, stride=4, ws=1 << 20, window=0):

@@ -48,18 +48,18 @@ def test_small_configs(cfg):
 
 
 @pytest.mark.parametrize("env", ["default", "no-overlap", "decode-side", "no-cluster", "separate", "no-tcgen05"])
-def test_engine_step_arrangements(env, monkeypatch):
+def test_engine_step_arrangements(env, attn_options):
     """The 48-request engine step under every stream and kernel arrangement."""
     if env == "no-overlap":
-        monkeypatch.setenv("PKV_NO_OVERLAP", "1")
+        attn_options(no_overlap=1)
     elif env == "decode-side":
-        monkeypatch.setenv("PKV_DECODE_MAIN", "0")
+        attn_options(decode_main=-1)
     elif env == "no-cluster":
-        monkeypatch.setenv("PKV_CLUSTER", "0")
+        attn_options(cluster=-1)
     elif env == "separate":
-        monkeypatch.setenv("PKV_SEPARATE_WRITE", "1")
+        attn_options(separate_write=1)
     elif env == "no-tcgen05":
-        monkeypatch.setenv("PKV_DISABLE_TCGEN05", "1")
+        attn_options(disable_tcgen05=1)
     _run(config_spec(2), what=f"engine step {env}")
 
 
@@ -83,10 +83,10 @@ def test_random_mixes(case, window):
 
 
 @pytest.mark.parametrize("split", ["128", "1024"], ids=["slot-ring", "streaming"])
-def test_split_decodes_write_their_rows(split, monkeypatch):
+def test_split_decodes_write_their_rows(split, attn_options):
     """Splits whose ranges cut through a request's new rows (t up to 8) each
     write the rows in their own range."""
-    monkeypatch.setenv("PKV_SPLIT_TOKENS", split)
+    attn_options(split_tokens=int(split))
     reqs, blk = [], 0
     for L, t in ((1030, 8), (2049, 3), (511, 5), (4000, 1), (129, 8), (0, 0)):
         if t == 0:

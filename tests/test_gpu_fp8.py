@@ -99,16 +99,16 @@ def test_fp8_write_bit_exact_and_attention_parity(case):
 @pytest.mark.parametrize("row_tiles", ["0", "1"], ids=["key-major", "row-tiles"])
 @pytest.mark.parametrize("split", ["128", "1024", "cluster"])
 @pytest.mark.parametrize("window", [0, 300])
-def test_fp8_split_paths_and_window(split, window, row_tiles, monkeypatch):
+def test_fp8_split_paths_and_window(split, window, row_tiles, attn_options):
     """Decode splits on the slot-ring (128, split counters; "cluster": four
     splits per request combined in a thread-block cluster) and the streaming
     kernel (1024), in key-major and in 16-row tiles, with and without a
     sliding window."""
     if split == "cluster":
-        monkeypatch.setenv("PKV_CLUSTER", "4")
+        attn_options(cluster=4)
         split = "256"
-    monkeypatch.setenv("PKV_SPLIT_TOKENS", split)
-    monkeypatch.setenv("PKV_DECODE_ROW_TILES", row_tiles)
+    attn_options(split_tokens=int(split))
+    attn_options(decode_row_tiles=int(row_tiles))
     reqs = [Req(3000, 1, list(range(0, 188))), Req(700, 40, list(range(188, 235))),
             Req(2500, 2, list(range(235, 392))), Req(5000, 1, list(range(392, 705)))]
     spec = Spec("fp8-paths", reqs, 32, 8, 128, 16, 710, 1 / math.sqrt(128), 71)
@@ -132,10 +132,10 @@ HEAD_PAIR_CASES = [
 
 @pytest.mark.parametrize("window", [0, 700])
 @pytest.mark.parametrize("case", HEAD_PAIR_CASES, ids=[f"hq{c[0]}-hkv{c[1]}" for c in HEAD_PAIR_CASES])
-def test_fp8_streaming_head_pairs(case, window, monkeypatch):
+def test_fp8_streaming_head_pairs(case, window, attn_options):
     """Quantized pools on the streaming kernel (splits of 1024 keys): key-major
     tiles with two KV heads per CTA, every group size the kernel stages."""
-    monkeypatch.setenv("PKV_SPLIT_TOKENS", "1024")
+    attn_options(split_tokens=1024)
     hq, hkv, plan = case
     reqs, nxt = [], 0
     for computed, new in plan:
@@ -243,14 +243,14 @@ def _run_combined(batch, pools, window=0, workspace_bytes=None):
 
 @pytest.mark.parametrize("mode", ["combined", "tcgen05-scratch", "separate"])
 @pytest.mark.parametrize("case", FP8_CASES[:4], ids=[f"seed{c[0]}" for c in FP8_CASES[:4]])
-def test_fp8_combined_write_and_attention(case, mode, monkeypatch):
+def test_fp8_combined_write_and_attention(case, mode, attn_options):
     """pkv_paged_kv_write_attention_fp8: decode CTAs quantize and write their
     own rows, the prefill rows go through the ranged quantizing scatter; codes
     and scales bit-exact (whole pool except the scratch block), attention
     within the tolerance; with the tcgen05 prefill scratch; and as the full
-    scatter followed by the attention (PKV_SEPARATE_WRITE=1)."""
+    scatter followed by the attention (the separate_write option)."""
     if mode == "separate":
-        monkeypatch.setenv("PKV_SEPARATE_WRITE", "1")
+        attn_options(separate_write=1)
     seed, reqs, max_ctx, max_new, hq, hkv, pad = case
     spec = random_spec(200 + seed, reqs, max_ctx, max_new, hq, hkv, 128, pad_rows=pad)
     b = make_batch(spec, device="cpu")

@@ -79,31 +79,14 @@ def test_random_mixes_full_parity(case):
     assert_close(dev.out, oracle_full(ref), f"random {seed}")
 
 
-@pytest.mark.parametrize("case", [RANDOM_CASES[1], RANDOM_CASES[2], RANDOM_CASES[5]], ids=["d64", "d128", "g8"])
-def test_cuda_core_kernels_full_parity(case, monkeypatch):
-    """The CUDA-core (FMA) kernels, selected with PKV_ATTN_CUDA_CORE=1."""
-    monkeypatch.setenv("PKV_ATTN_CUDA_CORE", "1")
-    seed, reqs, ctx, new, hq, hkv, d, pad = case
-    spec = random_spec(seed, reqs, ctx, new, hq, hkv, d, pad_rows=pad)
-    b = make_batch(spec, device="cpu")
-    dev = DeviceStep(b)
-    pkv.profile_start(16)
-    dev.step()
-    names = {n for n, _ in pkv.profile_stop()}
-    assert "attn_fma_decode" in names or "attn_fma_prefill" in names
-    ref = cpu_copy(b)
-    oracle_write(ref)
-    assert_close(dev.out, oracle_full(ref), f"cuda-core {seed}")
-
-
 @pytest.mark.parametrize("disable_tc", [False, True])
 @pytest.mark.parametrize("heads", [(32, 8, 128), (16, 4, 64), (8, 4, 48), (16, 2, 48)], ids=["d128g4", "d64g4", "d48g2", "d48g8"])
-def test_long_chunks_tensor_core_path(disable_tc, heads, monkeypatch):
+def test_long_chunks_tensor_core_path(disable_tc, heads, attn_options):
     """Prefill chunks of 128+ rows go to the tcgen05 kernel (head dims below 64
     padded to 64 columns); the same batch with it disabled runs on the
     warp-level MMA kernel.  Both match the oracle."""
     if disable_tc:
-        monkeypatch.setenv("PKV_DISABLE_TCGEN05", "1")
+        attn_options(disable_tcgen05=1)
     hq, hkv, d = heads
     reqs = [Req(1000, 300, list(range(0, 82))), Req(0, 257, list(range(82, 99))), Req(77, 1, list(range(99, 104))),
             Req(5000, 64, list(range(104, 421)))]
@@ -128,14 +111,14 @@ def _mixed_spec():
 
 @pytest.mark.parametrize("shape", ["long-chunks", "engine-step"])
 @pytest.mark.parametrize("overlap", [True, False])
-def test_mixed_step_side_stream_and_cuda_graph(overlap, shape, monkeypatch):
+def test_mixed_step_side_stream_and_cuda_graph(overlap, shape, attn_options):
     """Decodes next to prefill chunks: the decode kernels run on a forked side
-    stream (or, with PKV_NO_OVERLAP=1, on the caller's stream); in the small
+    stream (or, with the no_overlap option, on the caller's stream); in the small
     engine step the short prefill tiles are split over keys and all split
     partials are merged by one combine launch.  The step is also captured in
     a CUDA graph and replayed; every result matches the oracle."""
     if not overlap:
-        monkeypatch.setenv("PKV_NO_OVERLAP", "1")
+        attn_options(no_overlap=1)
     spec = _mixed_spec() if shape == "long-chunks" else config_spec(2)
     b = make_batch(spec, device="cpu")
     dev = DeviceStep(b)
@@ -161,13 +144,13 @@ def test_mixed_step_side_stream_and_cuda_graph(overlap, shape, monkeypatch):
 
 
 @pytest.mark.parametrize("pdl", [True, False])
-def test_programmatic_launch_and_padding_only_decodes(pdl, monkeypatch):
+def test_programmatic_launch_and_padding_only_decodes(pdl, attn_options):
     """Kernels launched with programmatic stream serialization wait in-kernel
     for the pool write.  A batch whose decode-class requests are all padding,
-    next to a prefill chunk, must still see the step's K/V (PKV_NO_PDL=1 gives
+    next to a prefill chunk, must still see the step's K/V (the no_pdl option gives
     plain stream order)."""
     if not pdl:
-        monkeypatch.setenv("PKV_NO_PDL", "1")
+        attn_options(no_pdl=1)
     reqs = [Req(0, 1, [], pad=True), Req(200, 90, list(range(0, 19))), Req(0, 1, [], pad=True)]
     spec = Spec("pad-mix", reqs, 8, 4, 64, 16, 24, 0.125, 31)
     b = make_batch(spec, device="cpu")
@@ -181,13 +164,13 @@ def test_programmatic_launch_and_padding_only_decodes(pdl, monkeypatch):
 
 
 @pytest.mark.parametrize("prefill_split", [False, True])
-def test_engine_step_prefill_split_toggle(prefill_split, monkeypatch):
+def test_engine_step_prefill_split_toggle(prefill_split, attn_options):
     """The small engine step on the warp-level MMA kernels only (tensor cores
     off), with and without key splits of its short prefill tiles
-    (PKV_PREFILL_SPLIT=1)."""
-    monkeypatch.setenv("PKV_DISABLE_TCGEN05", "1")
+    (the prefill_key_splits option)."""
+    attn_options(disable_tcgen05=1)
     if prefill_split:
-        monkeypatch.setenv("PKV_PREFILL_SPLIT", "1")
+        attn_options(prefill_key_splits=1)
     b = make_batch(config_spec(2), device="cpu")
     dev = DeviceStep(b)
     dev.step()
@@ -197,8 +180,8 @@ def test_engine_step_prefill_split_toggle(prefill_split, monkeypatch):
 
 
 @pytest.mark.parametrize("split", [256, 512, 4096])
-def test_forced_split_sizes(split, monkeypatch):
-    monkeypatch.setenv("PKV_SPLIT_TOKENS", str(split))
+def test_forced_split_sizes(split, attn_options):
+    attn_options(split_tokens=split)
     spec = random_spec(11, 10, 3000, 3, 32, 8, 128, decode_frac=0.8)
     b = make_batch(spec, device="cpu")
     dev = DeviceStep(b)
@@ -421,13 +404,14 @@ def test_out_of_pool_slot_sets_flag_and_skips():
     del before
 
 
-@pytest.mark.parametrize("path", ["default", "cuda-core"])
-def test_device_metadata_differing_from_host_copies_is_flagged(path, monkeypatch):
+@pytest.mark.parametrize("path", ["default", "no-tcgen05"])
+def test_device_metadata_differing_from_host_copies_is_flagged(path, attn_options):
     """The kernels take each request's rows and context length from the host
     copies they were planned with; device arrays that disagree set
-    DEVERR_META and change nothing else."""
-    if path == "cuda-core":
-        monkeypatch.setenv("PKV_ATTN_CUDA_CORE", "1")
+    DEVERR_META and change nothing else (prefill on tcgen05, and on the
+    warp-MMA kernel)."""
+    if path == "no-tcgen05":
+        attn_options(disable_tcgen05=1)
     # decodes, short chunks and one tensor-core-sized chunk (t*g >= 128, d 128)
     reqs = [Req(300, 1, list(range(0, 19))), Req(40, 24, list(range(19, 23))),
             Req(100, 64, list(range(23, 34)))]
@@ -456,11 +440,11 @@ COUNTER_BYTES = 65536          # split-counter region after the 256-byte error w
 
 @pytest.mark.parametrize("split", [128, 1024])
 @pytest.mark.parametrize("d", [48, 128])
-def test_in_kernel_split_combine_repeats_and_leaves_counters_zero(split, d, monkeypatch):
+def test_in_kernel_split_combine_repeats_and_leaves_counters_zero(split, d, attn_options):
     """Split decodes combine inside the kernel (the CTA finishing the last
     split of a request and KV head); repeated calls, eager and replayed from a
     CUDA graph, stay exact, and every call leaves the counters at zero."""
-    monkeypatch.setenv("PKV_SPLIT_TOKENS", str(split))
+    attn_options(split_tokens=split)
     spec = random_spec(31, 12, 4000, 3, 16 if d == 128 else 8, 4 if d == 128 else 2, d, decode_frac=0.85)
     b = make_batch(spec, device="cpu")
     dev = DeviceStep(b)
@@ -488,12 +472,12 @@ def test_in_kernel_split_combine_repeats_and_leaves_counters_zero(split, d, monk
     assert pkv.read_device_error(dev.ws) == 0
 
 
-def test_workspace_without_counter_room_uses_the_combine_kernel(monkeypatch):
+def test_workspace_without_counter_room_uses_the_combine_kernel(attn_options):
     """A workspace too small for the counter region still splits (partials
     after the error word) and combines with the separate kernel (clusters
     off: they would combine without partials)."""
-    monkeypatch.setenv("PKV_SPLIT_TOKENS", "256")
-    monkeypatch.setenv("PKV_CLUSTER", "0")
+    attn_options(split_tokens=256)
+    attn_options(cluster=-1)
     # one decode at L = 1500: 8 partial rows of 264 bytes per split, so the
     # 12 KiB workspace holds 5 splits (of 512 keys: 3 splits)
     spec = Spec("ws", [Req(1499, 1, list(range(94)))], 8, 2, 64, 16, 100, 0.125, 32)
@@ -507,11 +491,11 @@ def test_workspace_without_counter_room_uses_the_combine_kernel(monkeypatch):
     assert pkv.launch_count() - before >= 3              # write, attention, combine
 
 
-def test_nonzero_split_counter_is_flagged(monkeypatch):
+def test_nonzero_split_counter_is_flagged(attn_options):
     """A workspace whose counter region was not zero-filled is reported
     (split counters: clusters off)."""
-    monkeypatch.setenv("PKV_SPLIT_TOKENS", "256")
-    monkeypatch.setenv("PKV_CLUSTER", "0")
+    attn_options(split_tokens=256)
+    attn_options(cluster=-1)
     spec = random_spec(33, 4, 2000, 1, 8, 2, 64, decode_frac=1.0)
     b = make_batch(spec, device="cpu")
     dev = DeviceStep(b)
@@ -524,10 +508,10 @@ def test_nonzero_split_counter_is_flagged(monkeypatch):
 
 
 @pytest.mark.parametrize("d", [48, 64, 128])
-def test_short_chunks_on_tensor_cores(d, monkeypatch):
+def test_short_chunks_on_tensor_cores(d, attn_options):
     """With the row threshold lowered, chunks that fill only part of a 128-row
     tile (ragged token counts, unaligned contexts) run on the tcgen05 kernel."""
-    monkeypatch.setenv("PKV_TC_MIN_ROWS", "16")
+    attn_options(tc_min_rows=16)
     reqs = [Req(256 + 64 * k, t, list(range(40 * k, 40 * k + 40))) for k, t in enumerate((64, 17, 33, 5, 1, 40))]
     reqs[4] = Req(300, 1, list(range(160, 200)))                  # a decode stays on the decode kernel
     spec = Spec("short", reqs, 8, 2 if d == 128 else 4, d, 16, 250, 1 / math.sqrt(d), 41)
@@ -566,20 +550,18 @@ def test_sliding_window_random_mixes(case, window):
     assert pkv.read_device_error(dev.ws) == 0
 
 
-@pytest.mark.parametrize("path", ["split64", "split1024", "cuda-core", "prefill-split", "no-tcgen05"])
-def test_sliding_window_on_every_kernel_path(path, monkeypatch):
+@pytest.mark.parametrize("path", ["split64", "split1024", "prefill-split", "no-tcgen05"])
+def test_sliding_window_on_every_kernel_path(path, attn_options):
     if path == "split64":
-        monkeypatch.setenv("PKV_SPLIT_TOKENS", "64")          # many decode splits, in-kernel combine
+        attn_options(split_tokens=64)          # many decode splits, in-kernel combine
     elif path == "split1024":
-        monkeypatch.setenv("PKV_SPLIT_TOKENS", "1024")        # streaming decode kernel
-    elif path == "cuda-core":
-        monkeypatch.setenv("PKV_ATTN_CUDA_CORE", "1")
+        attn_options(split_tokens=1024)        # streaming decode kernel
     elif path == "prefill-split":
-        monkeypatch.setenv("PKV_DISABLE_TCGEN05", "1")
-        monkeypatch.setenv("PKV_PREFILL_SPLIT", "1")
-        monkeypatch.setenv("PKV_SPLIT_TOKENS", "128")
+        attn_options(disable_tcgen05=1)
+        attn_options(prefill_key_splits=1)
+        attn_options(split_tokens=128)
     else:
-        monkeypatch.setenv("PKV_DISABLE_TCGEN05", "1")
+        attn_options(disable_tcgen05=1)
     reqs = [Req(3000, 1, list(range(0, 188))), Req(700, 40, list(range(188, 235))),
             Req(2500, 3, list(range(235, 392))), Req(0, 300, list(range(392, 411))),
             Req(5000, 1, list(range(411, 724)))]
@@ -634,12 +616,12 @@ def test_short_decodes_head_dims_and_windows(d, hq, hkv):
 @pytest.mark.parametrize("row_tiles", [0, 1], ids=["key-major", "row-tiles"])
 @pytest.mark.parametrize("split", [128, 1024], ids=["slot-ring", "streaming"])
 @pytest.mark.parametrize("d,hq,hkv", [(48, 8, 4), (64, 16, 4), (128, 64, 8)])
-def test_decode_tile_forms(d, hq, hkv, split, row_tiles, monkeypatch):
+def test_decode_tile_forms(d, hq, hkv, split, row_tiles, attn_options):
     """Decode CTAs of at most 8 rows per KV head run key-major tiles (keys in
-    the MMA's M dimension); PKV_DECODE_ROW_TILES=1 keeps the 16-row tiles.
+    the MMA's M dimension); the decode_row_tiles option keeps the 16-row tiles.
     Both forms, both decode kernels, t = 1 and 2 where g allows, a window."""
-    monkeypatch.setenv("PKV_SPLIT_TOKENS", str(split))
-    monkeypatch.setenv("PKV_DECODE_ROW_TILES", str(row_tiles))
+    attn_options(split_tokens=split)
+    attn_options(decode_row_tiles=row_tiles)
     g = hq // hkv
     lens = (17, 300, 1000, 2048, 2500, 1, 5000)
     reqs, blk = [], 0
@@ -666,15 +648,15 @@ CLUSTER_LENS = (17, 40, 300, 700, 1000, 1999, 33)
 @pytest.mark.parametrize("cs", [2, 3, 8])
 @pytest.mark.parametrize("d,hq,hkv,row_tiles", [(48, 8, 4, 0), (128, 32, 8, 0), (64, 16, 4, 1), (128, 64, 8, 1)],
                          ids=["d48g2", "d128g4", "d64g4-rows", "d128g8-rows"])
-def test_cluster_split_combine(d, hq, hkv, row_tiles, cs, window, monkeypatch):
+def test_cluster_split_combine(d, hq, hkv, row_tiles, cs, window, attn_options):
     """Short split decodes whose splits run as one thread-block cluster and
     combine through distributed shared memory: cs CTAs per request and KV
     head, keys divided evenly (short requests leave empty trailing splits),
     key-major and 16-row tiles, t = 1 and 2, a padding request; two eager calls
     and two CUDA-graph replays give the same result."""
-    monkeypatch.setenv("PKV_SPLIT_TOKENS", "256")
-    monkeypatch.setenv("PKV_CLUSTER", str(cs))
-    monkeypatch.setenv("PKV_DECODE_ROW_TILES", str(row_tiles))
+    attn_options(split_tokens=256)
+    attn_options(cluster=cs)
+    attn_options(decode_row_tiles=row_tiles)
     g = hq // hkv
     reqs, blk = [], 0
     for i, L in enumerate(CLUSTER_LENS):
@@ -708,11 +690,11 @@ def test_cluster_split_combine(d, hq, hkv, row_tiles, cs, window, monkeypatch):
     assert pkv.read_device_error(dev.ws) == 0
 
 
-@pytest.mark.parametrize("cluster", ["0", "-1"], ids=["counters", "cluster"])
-def test_engine_step_split_combine_both_ways(cluster, monkeypatch):
+@pytest.mark.parametrize("cluster", [-1, 0], ids=["counters", "cluster"])
+def test_engine_step_split_combine_both_ways(cluster, attn_options):
     """The 48-request engine step with its short decode splits combined by
-    the split counters (PKV_CLUSTER=0) and by clusters (the default)."""
-    monkeypatch.setenv("PKV_CLUSTER", cluster)
+    the split counters (cluster option -1) and by clusters (the default)."""
+    attn_options(cluster=cluster)
     b = make_batch(config_spec(2), device="cpu")
     ref = cpu_copy(b)
     oracle_write(ref)
@@ -723,12 +705,12 @@ def test_engine_step_split_combine_both_ways(cluster, monkeypatch):
     assert pkv.read_device_error(dev.ws) == 0
 
 
-@pytest.mark.parametrize("cluster", ["-1", "0"], ids=["clusters", "counters"])
-def test_more_requests_than_one_launch_lists(cluster, monkeypatch):
+@pytest.mark.parametrize("cluster", [0, -1], ids=["clusters", "counters"])
+def test_more_requests_than_one_launch_lists(cluster, attn_options):
     """600 decode requests and 300 prefill chunks: every kernel class runs
     several launches of at most 256 listed requests, each launch with its own
     plan (split counts, cluster size); short and long contexts mixed."""
-    monkeypatch.setenv("PKV_CLUSTER", cluster)
+    attn_options(cluster=cluster)
     gen = torch.Generator().manual_seed(85)
     reqs, blk = [], 0
     for i in range(900):

@@ -27,10 +27,10 @@ def _built():
 
 
 @pytest.fixture(autouse=True)
-def _no_switches(monkeypatch):
-    for name in ("PKV_ATTN_CUDA_CORE", "PKV_DISABLE_TCGEN05", "PKV_TC_MIN_ROWS", "PKV_FP8_PREFILL_TC",
-                 "PKV_SPLIT_TOKENS", "PKV_CLUSTER", "PKV_DECODE_MAIN", "PKV_NO_OVERLAP", "PKV_PREFILL_SPLIT"):
-        monkeypatch.delenv(name, raising=False)
+def _planner_choices():
+    pkv.reset_options()
+    yield
+    pkv.reset_options()
 
 
 def meta(cfg):
@@ -128,26 +128,57 @@ def test_decodes_beside_a_long_prefill_take_longer_splits():
     assert p["decode_split_tokens"] >= 3 * a["decode_split_tokens"]
 
 
-def test_switches(monkeypatch):
-    monkeypatch.setenv("PKV_NO_OVERLAP", "1")
-    assert not plan(2)["overlap"]
-    monkeypatch.delenv("PKV_NO_OVERLAP")
-    monkeypatch.setenv("PKV_DECODE_MAIN", "0")
-    p = plan(2)
-    assert p["overlap"] and not p["decode_on_caller_stream"]
-    monkeypatch.delenv("PKV_DECODE_MAIN")
-    monkeypatch.setenv("PKV_CLUSTER", "0")
-    assert plan(2)["decode_cluster"] == 0
-    monkeypatch.setenv("PKV_CLUSTER", "4")
-    assert plan(2)["decode_cluster"] == 4
-    monkeypatch.delenv("PKV_CLUSTER")
-    monkeypatch.setenv("PKV_SPLIT_TOKENS", "512")
-    p = plan(3)
-    assert p["decode_split_tokens"] == 512 and p["decode_streaming"]
-    monkeypatch.delenv("PKV_SPLIT_TOKENS")
-    monkeypatch.setenv("PKV_DISABLE_TCGEN05", "1")
-    p = plan(2)
-    assert p["prefill_tensor_requests"] == 0 and p["prefill_mma_requests"] == 16
+def test_options():
+    """Each option overrides its planner choice (pkv_attention_options)."""
+    with pkv.options(no_overlap=1):
+        assert not plan(2)["overlap"]
+    with pkv.options(decode_main=-1):
+        p = plan(2)
+        assert p["overlap"] and not p["decode_on_caller_stream"]
+    with pkv.options(cluster=-1):
+        assert plan(2)["decode_cluster"] == 0
+    with pkv.options(cluster=4):
+        assert plan(2)["decode_cluster"] == 4
+    with pkv.options(split_tokens=512):
+        p = plan(3)
+        assert p["decode_split_tokens"] == 512 and p["decode_streaming"]
+    with pkv.options(disable_tcgen05=1):
+        p = plan(2)
+        assert p["prefill_tensor_requests"] == 0 and p["prefill_mma_requests"] == 16
+    with pkv.options(tc_min_rows=1000):
+        p = plan(2)                                      # chunks of <= 64 tokens x g 2 stay below it
+        assert p["prefill_tensor_requests"] == 0 and p["prefill_mma_requests"] == 16
+    with pkv.options(prefill_key_splits=1, disable_tcgen05=1):
+        assert plan(2)["prefill_key_splits"]
+    spec, qsl, sl = meta(4)
+    extra = pkv.fp8_prefill_scratch_bytes(qsl, sl, 32, 8, 128)
+    with pkv.options(fp8_prefill_on_mma=1):
+        p = plan(4, quantized=True, workspace_bytes=BIG_WS + extra)
+        assert p["prefill_tensor_requests"] == 0 and p["quantized_prefill_scratch"] == 0
+    assert pkv.current_options() == {}
+    with pytest.raises(TypeError):
+        pkv.set_options(no_such_option=1)
+
+
+def test_library_reads_no_environment():
+    """The library's planner does not change with environment variables."""
+    import os
+    import subprocess
+    import sys
+    code = ("import json, paged_kv_cache_84_gb300 as pkv; from workloads import config_spec; "
+            "s = config_spec(2); q = [0]; [q.append(q[-1] + r.new) for r in s.reqs]; "
+            "print(json.dumps(pkv.plan_attention(q, [r.seq_len for r in s.reqs], 8, 4, 48, "
+            "workspace_bytes=1 << 30, num_sms=152)))")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ)
+    base = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True)
+    env.update(PKV_NO_OVERLAP="1", PKV_CLUSTER="0", PKV_SPLIT_TOKENS="512", PKV_DISABLE_TCGEN05="1")
+    other = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True)
+    assert base.returncode == 0 and other.returncode == 0, base.stderr + other.stderr
+    assert base.stdout == other.stdout
+    csrc = os.path.join(root, "paged_kv_cache_84_gb300", "csrc")
+    for name in os.listdir(csrc):
+        assert "getenv" not in open(os.path.join(csrc, name)).read(), name
 
 
 def test_quantized_prefill_on_tcgen05_needs_the_scratch():
