@@ -447,6 +447,23 @@ pkv_status pkv_ragged_paged_attention_noalloc(void *out, const void *q,
                                               int32_t num_blocks_total, float scale, int32_t window,
                                               uint32_t *device_error, cudaStream_t stream);
 
+/*
+ * A check of the bounded waits (a diagnostic, for tests).  Every pipeline
+ * wait of the attention kernels gives up after 2 s, sets PKV_DEVERR_TIMEOUT
+ * and lets the kernel leave in order (no thread left at a barrier, tensor
+ * memory freed).  This call launches one small CTA with the same roles —
+ * a tensor-memory owner, a producer lane and consumer warps — whose
+ * mbarriers nothing ever arrives at, waiting with the same routine but a
+ * limit of limit_us microseconds (1 .. 100000).  It returns once every wait
+ * has given up: *device_error gets PKV_DEVERR_TIMEOUT OR-ed in, report[0]
+ * one bit per warp whose wait gave up (warps 0, 2 and 3: 0xD), report[1]
+ * the microseconds the kernel ran.  device_error and report are device
+ * uint32_t (1 and 2 of them).  PKV_ERR_INVALID_ARG for null pointers or a
+ * limit out of range; PKV_ERR_CUDA if the launch fails.
+ */
+pkv_status pkv_check_bounded_wait(uint32_t *device_error, uint32_t *report, uint32_t limit_us,
+                                  cudaStream_t stream);
+
 /* Size in bytes of the no-allocation call's static scratch array
  * (PKV_NOALLOC_SCRATCH_BYTES as this library was built). */
 size_t pkv_noalloc_scratch_bytes(void);

@@ -63,15 +63,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 }
 
 // Wait until the phase with parity `parity` of barrier `bar` has completed.
-// Gives up after kWaitLimitNs (or kWaitLimitIters polls): sets kDevErrTimeout
-// in *err and returns false.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t *err)
+// Gives up after limit_ns (2 s unless given; or kWaitLimitIters polls): sets
+// kDevErrTimeout in *err and returns false.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t *err,
+                                          uint64_t limit_ns = kWaitLimitNs)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1; i < kWaitLimitIters; i++) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) break;
+        if ((i & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) break;
     }
     if (err) atomicOr(err, kDevErrTimeout);
     return false;
