@@ -246,6 +246,9 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q,
  *   decode_row_tiles    1: 16-row query tiles for decodes instead of
  *                       key-major tiles for small groups
  *   no_pdl              1: no programmatic dependent launches
+ *   tc_key_pieces       -1: no tcgen05 pair is cut into key pieces; k >= 2:
+ *                       every tcgen05 pair is cut into k pieces (at most its
+ *                       key tiles), merged by the CTA that finishes last
  */
 typedef struct pkv_attention_options {
     int32_t disable_tcgen05;
@@ -259,7 +262,8 @@ typedef struct pkv_attention_options {
     int32_t separate_write;
     int32_t decode_row_tiles;
     int32_t no_pdl;
-    int32_t reserved[5];
+    int32_t tc_key_pieces;
+    int32_t reserved[4];
 } pkv_attention_options;
 
 /* pkv_ragged_paged_attention with options (NULL: the planner's choices). */
@@ -518,7 +522,7 @@ typedef struct pkv_attention_plan {
     int32_t overlap;                  /* 1: decode and prefill classes on two streams */
     int32_t decode_on_caller_stream;  /* with overlap: 1 if the decodes run on the caller's stream */
     int32_t prefill_key_splits;       /* 1: warp-MMA prefill tiles split over keys */
-    int32_t reserved;
+    int32_t prefill_tensor_pieces;    /* tcgen05 CTAs that run a key piece of a pair (0: no pair is cut) */
     size_t quantized_prefill_scratch; /* workspace bytes of bf16 block copies for quantized prefill */
     size_t partial_bytes;             /* workspace bytes of split partials */
 } pkv_attention_plan;

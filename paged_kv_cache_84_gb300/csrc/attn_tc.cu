@@ -32,6 +32,16 @@
 //               and S alternates between two TMEM buffers (the unused S_b
 //               columns), so the MMA of key tile j+1 overlaps tile j's softmax.
 // TMEM: S_a [0,128), S_b [128,256), O_a [256,384), O_b [384,512).
+//
+// Key pieces: a pair may be cut into consecutive ranges of key tiles, one
+// CTA each (the planner does so for heavy pairs that would start in a later
+// wave, to even out the SMs' loads).  When its loop is done, such a CTA
+// counts itself on the pair's counter.  Every piece but the last to count
+// writes its rows' unscaled O and (running max, weight sum) as fp32
+// partials and signals them on the counter's second word; the last one
+// waits (bounded) for those signals and merges the partials into its own O,
+// still in tensor memory, with the exact split-softmax identity, writes the
+// bf16 output and returns both words to zero.
 // Shared memory (128-byte swizzle): Q_a, Q_b, K and V tiles as [128][64]
 // sub-tiles, K-major for Q and K, MN-major for V.  Head dims below 64 are
 // padded to 64 columns: the TMA box is 64 columns wide and fills the
@@ -217,6 +227,144 @@ __device__ __forceinline__ void tc_store_rows(const AttnParams &p, uint32_t to, 
     }
 }
 
+// Store O columns [32 c0, 32 (c0 + nc)) of this thread's row (clipped to D)
+// unscaled as an fp32 partial row `prow`, and with write_ml its running max
+// (exp2 domain) and weight sum.  valid false: read TMEM only (the load is
+// warp-collective), store nothing.
+template <int D>
+__device__ __forceinline__ void tc_store_partial(const AttnParams &p, uint32_t to, size_t prow, bool valid, float m,
+                                                 float l, int c0, int nc, bool write_ml)
+{
+#pragma unroll 1
+    for (int c = c0; c < c0 + nc; c++) {
+        if (c * 32 >= D) break;                                     // warp-uniform
+        uint32_t v[32];
+        tmem_ld32(to + c * 32, v);
+        tmem_ld_wait();
+        if (valid) {
+            float4 *dst = reinterpret_cast<float4 *>(p.part_o + prow * D + c * 32);
+#pragma unroll
+            for (int q = 0; q < 8; q++) {
+                if (c * 32 + q * 4 >= D) break;
+                dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                     __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+            }
+        }
+    }
+    if (valid && write_ml) p.part_ml[prow] = make_float2(m, l);
+}
+
+// Wait until *word reaches `target` (acquire), for at most the pipeline
+// wait limit; on time-out flag kDevErrTimeout and return false.  Used by the
+// last piece of a pair for the other pieces' partials: those CTAs are past
+// their loops when they count, and only store their rows before they
+// signal, so the wait ends.
+__device__ __forceinline__ bool wait_count(const uint32_t *word, uint32_t target, uint32_t *err)
+{
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 0; i < kWaitLimitIters; i++) {
+        uint32_t v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(word) : "memory");
+        if (v >= target) return true;
+        if ((i & 63u) == 63u && globaltimer_ns() - t0 > kWaitLimitNs) break;
+        __nanosleep(64);
+    }
+    atomicOr(err, kDevErrTimeout);
+    return false;
+}
+
+// The end of a key piece, run by the 256 softmax threads (named barrier 7):
+// this thread's row rr (0..255: tile a, then tile b) holds O columns
+// [32 c0, 32 (c0 + nc)) in TMEM at `to`, with running max m (exp2 domain)
+// and weight sum l over this piece's keys; write_ml: this thread reports
+// (m, l) of its row.  ok: this thread's waits succeeded (CTA-uniform here).
+// Counting, partial store / signal, or wait and merge, as described above.
+template <int D>
+__device__ __forceinline__ void tc_piece_epilogue(const AttnParams &p, uint32_t *cnt, size_t slot0, int piece,
+                                                  int pieces, uint32_t to, int rr, bool valid, float m, float l,
+                                                  int c0, int nc, bool write_ml, bool ok, size_t orow,
+                                                  uint32_t *s_flag)
+{
+    named_bar_sync(7, 256);                                     // every row of the CTA has left its loop
+    if (threadIdx.x == 128) {
+        const uint32_t old = atomicAdd(cnt, 1u);
+        if (old >= (uint32_t)pieces) atomicOr(p.err, kDevErrCounter);   // counters were not zero-filled
+        s_flag[0] = old + 1u == (uint32_t)pieces ? 1u : 0u;
+    }
+    named_bar_sync(7, 256);
+    if (s_flag[0] == 0u) {
+        // not the last: partials out, then signal them (also after a failed
+        // wait, so that the last piece's wait ends)
+        tc_store_partial<D>(p, to, (slot0 + piece) * 256 + rr, valid && ok, m, l, c0, nc, write_ml);
+        named_bar_sync(7, 256);
+        if (threadIdx.x == 128) {
+            __threadfence();                                    // release the partials (cumulative over the barrier)
+            atomicAdd(cnt + 1, 1u);
+        }
+        return;
+    }
+    if (threadIdx.x == 128) s_flag[1] = wait_count(cnt + 1, (uint32_t)pieces - 1u, p.err) ? 1u : 0u;
+    named_bar_sync(7, 256);
+    if (s_flag[1] != 0u) {
+        // row weights: M over every piece, the denominator over every piece
+        float M = m;
+        for (int q = 0; q < pieces; q++)
+            if (q != piece && valid) M = fmaxf(M, __ldcg(&p.part_ml[(slot0 + q) * 256 + rr]).x);
+        const float Ms = M == -INFINITY ? 0.f : M;
+        const float w0 = exp2f(m - Ms);                          // 2^-inf = 0
+        float den = w0 * l;
+        for (int q = 0; q < pieces; q++) {
+            if (q == piece || !valid) continue;
+            const float2 ml = __ldcg(&p.part_ml[(slot0 + q) * 256 + rr]);
+            den = fmaf(exp2f(ml.x - Ms), ml.y, den);
+        }
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+#pragma unroll 1
+        for (int c = c0; c < c0 + nc; c++) {
+            if (c * 32 >= D) break;                             // warp-uniform
+            uint32_t v[32];
+            tmem_ld32(to + c * 32, v);
+            tmem_ld_wait();
+            if (!valid || !ok) continue;
+            float acc[32];
+#pragma unroll
+            for (int k = 0; k < 32; k++) acc[k] = __uint_as_float(v[k]) * w0;
+            for (int q = 0; q < pieces; q++) {
+                if (q == piece) continue;
+                const size_t prow = (slot0 + q) * 256 + rr;
+                const float w = exp2f(__ldcg(&p.part_ml[prow]).x - Ms);
+                const float4 *src = reinterpret_cast<const float4 *>(p.part_o + prow * D + c * 32);
+                float4 x[8];
+#pragma unroll
+                for (int k = 0; k < 8; k++)
+                    if (c * 32 + k * 4 < D) x[k] = __ldcg(src + k);
+#pragma unroll
+                for (int k = 0; k < 8; k++) {
+                    if (c * 32 + k * 4 >= D) break;
+                    acc[4 * k] = fmaf(w, x[k].x, acc[4 * k]);
+                    acc[4 * k + 1] = fmaf(w, x[k].y, acc[4 * k + 1]);
+                    acc[4 * k + 2] = fmaf(w, x[k].z, acc[4 * k + 2]);
+                    acc[4 * k + 3] = fmaf(w, x[k].w, acc[4 * k + 3]);
+                }
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * D + c * 32);
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                if (c * 32 + k * 8 >= D) break;
+                dst[k] = make_uint4(pack_bf16x2(acc[8 * k] * inv, acc[8 * k + 1] * inv),
+                                    pack_bf16x2(acc[8 * k + 2] * inv, acc[8 * k + 3] * inv),
+                                    pack_bf16x2(acc[8 * k + 4] * inv, acc[8 * k + 5] * inv),
+                                    pack_bf16x2(acc[8 * k + 6] * inv, acc[8 * k + 7] * inv));
+            }
+        }
+    }
+    named_bar_sync(7, 256);
+    if (threadIdx.x == 128) {                                   // ready for the next call
+        atomicExch(cnt, 0u);
+        atomicExch(cnt + 1, 0u);
+    }
+}
+
 // DP: head dim padded to the 64-column sub-tile; D: head dim of q and out;
 // WIN: a sliding window is set (p.window > 0).
 template <int DP, int D, bool WIN>
@@ -244,17 +392,34 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, co
     const int g = p.group;
     const int tt = wl.tile_tokens;                                 // tokens per tile: 128 / g
     const int npairs = (t + 2 * tt - 1) / (2 * tt);
-    const int pair = npairs - 1 - (blockIdx.y - wl.item_off[li]);  // longest pairs first
+    // longest pairs first: `whole` pairs as one CTA, then `pieces` CTAs per pair
+    const int local = blockIdx.y - wl.item_off[li];
+    const int whole = tc_split_whole(wl.tc_split[li]), small = tc_split_small(wl.tc_split[li]);
+    int pair = npairs - 1 - local, piece = 0, pieces = 1;
+    if (local >= whole) {                                          // piece-major over the split pairs
+        pieces = tc_split_pieces(wl.tc_split[li]);
+        pair = npairs - 1 - whole - (local - whole) % (npairs - whole);
+        piece = (local - whole) / (npairs - whole);
+    }
     const int i0 = pair * 2 * tt;                                  // first token of tile a
     const int ntok_a = min(tt, t - i0);
     const int ntok_b = max(0, min(tt, t - i0 - tt));
     const bool has_b = ntok_b > 0;
     const int k_end = L - t + i0 + ntok_a + ntok_b;                // one past the last position
-    // key tiles jt0 .. jt0 + nkt - 1: with a sliding window the first is the
-    // one holding the window start of the pair's first row
-    const int jt0 = window_lo(L - t + i0, p.window) / kTcKeys;
-    const int nkt = (k_end + kTcKeys - 1) / kTcKeys - jt0;
-    const int nblk = ((k_end + 15) >> 4) - jt0 * 8;                // blocks from key tile jt0 on
+    // the pair's key tiles start at the one holding the window start of its
+    // first row; this CTA takes key tiles jt0 .. jt0 + nkt - 1 of them
+    const int jt_first = window_lo(L - t + i0, p.window) / kTcKeys;
+    const int nkt_pair = (k_end + kTcKeys - 1) / kTcKeys - jt_first;
+    const int jt0 = jt_first + tc_piece_begin(nkt_pair, piece, pieces, small);
+    const int nkt = jt_first + tc_piece_begin(nkt_pair, piece + 1, pieces, small) - jt0;
+    const int nblk = min((k_end + 15) >> 4, (jt0 + nkt) * 8) - jt0 * 8;   // blocks of those key tiles
+    // split pieces: the pair's partial slots (one per piece) and counter
+    const int split_idx = npairs - 1 - whole - pair;
+    const size_t slot0 =
+        pieces > 1 ? (size_t)wl.part_off[li] + ((size_t)split_idx * p.hkv + kh) * pieces : 0;
+    uint32_t *const piece_cnt =
+        pieces > 1 ? p.counters + (size_t)(wl.cnt_off[li] + split_idx * p.hkv + kh) * kCounterStride : nullptr;
+    uint32_t *const s_piece = tmem_slot + 1;                       // two flag words after the TMEM address
     const int wspan = win_span(p.window);                          // keys <= position - wspan are outside
 
     if (threadIdx.x == 0) {
@@ -491,8 +656,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, co
         }
         pdl_launch_dependents();
         if (ok) ok = mbar_wait(bar(kBarOA + x), (nkt - 1) & 1, p.err);
-        if (__all_sync(0xffffffffu, ok)) {
-            tc_fence_after();
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) tc_fence_after();
+        if (pieces > 1) {
+            const size_t orow = row < nr ? (size_t)(b + tok0 + row / g) * p.hq + kh * g + row % g : 0;
+            tc_piece_epilogue<D>(p, piece_cnt, slot0, piece, pieces, to, x * 128 + row, row < nr, m_used, l, 0,
+                                 DP / 32, true, ok, orow, s_piece);
+        } else if (ok) {
             tc_store_rows<D>(p, to, row, nr, b + tok0, kh, g, l > 0.f ? 1.f / l : 0.f, 0, DP / 32);
         }
     } else if (warp >= 4) {
@@ -555,9 +725,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, co
         if (ok) ok = mbar_wait(bar(kBarOFin), 0, p.err);
         xl[hc * 128 + row] = l;
         ok = named_bar_and(2 + rg, 64, __all_sync(0xffffffffu, ok));
-        if (ok) {
-            tc_fence_after();
-            const float lt = l + xl[(hc ^ 1) * 128 + row];
+        if (ok) tc_fence_after();
+        const float lt = l + xl[(hc ^ 1) * 128 + row];
+        if (pieces > 1) {
+            const size_t orow = row < nr ? (size_t)(b + i0 + row / g) * p.hq + kh * g + row % g : 0;
+            tc_piece_epilogue<D>(p, piece_cnt, slot0, piece, pieces, to, row, row < nr, m_used, lt,
+                                 hc * (DP / 64), DP / 64, hc == 0, ok, orow, s_piece);
+        } else if (ok) {
             tc_store_rows<D>(p, to, row, nr, b + i0, kh, g, lt > 0.f ? 1.f / lt : 0.f, hc * (DP / 64), DP / 64);
         }
     }

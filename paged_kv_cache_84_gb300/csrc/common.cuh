@@ -35,8 +35,37 @@ struct WorkList {
     int32_t cnt_off[kPlanMax];    // decode: first split counter of a request combined in-kernel, else -1
     int32_t cluster;              // decode: 0, or the split count of every request when each request's
                                   // splits run as one thread-block cluster (combined through its shared memory)
-    int32_t split_len[kPlanMax];  // cluster mode: keys per split of each request (a multiple of the block size)
+    union {
+        int32_t split_len[kPlanMax];  // decode, cluster mode: keys per split of each request (a multiple of 16)
+        int32_t tc_split[kPlanMax];   // tcgen05 prefill: (pairs run whole << 5) | key pieces of each other pair
+    };
 };
+
+// tcgen05 prefill work of one listed request: its pairs of 128-row tiles run
+// longest first; the first `whole` of them as one CTA each (per KV head),
+// every later one as `pieces` CTAs over consecutive key-tile ranges, whose
+// fp32 partials the CTA finishing last merges.  The key tiles of such a pair
+// are cut evenly (small = 0), or, with two pieces, into a first piece and a
+// last one of small/64 of the tiles (at least one).  Pieces launch
+// piece-major: every split pair's piece 0, then every piece 1, ...
+__host__ __device__ __forceinline__ int tc_split_pack(int whole, int pieces, int small = 0)
+{
+    return (whole << 11) | (pieces << 6) | small;
+}
+__host__ __device__ __forceinline__ int tc_split_whole(int v) { return v >> 11; }
+__host__ __device__ __forceinline__ int tc_split_pieces(int v) { return (v >> 6) & 31; }
+__host__ __device__ __forceinline__ int tc_split_small(int v) { return v & 63; }
+constexpr int kTcMaxPieces = 16;
+
+// First key tile (relative to the pair's first) of piece q of `pieces` over n
+// key tiles (q = pieces: n).
+__host__ __device__ __forceinline__ int tc_piece_begin(int n, int q, int pieces, int small)
+{
+    if (q >= pieces) return n;
+    if (small == 0 || pieces != 2) return n * q / pieces;
+    const int last = (n * small + 32) / 64 > 0 ? (n * small + 32) / 64 : 1;
+    return q == 0 ? 0 : n - last;
+}
 
 // Largest cluster of a decode request's splits (the portable cluster size).
 constexpr int kMaxClusterSplits = 8;
@@ -370,6 +399,7 @@ struct CallOptions {
     bool separate_write = false;      // combined call as scatter + attention
     bool decode_row_tiles = false;    // 16-row decode tiles instead of key-major ones
     bool no_pdl = false;              // no programmatic dependent launches
+    int tc_key_pieces = 0;            // 0: planner; -1: no key pieces; k >= 2: every tcgen05 pair in k pieces
 };
 
 // Launch-level choices of the attention call in progress on this thread,

@@ -18,6 +18,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <algorithm>
+#include <functional>
 #include <vector>
 
 #include "pkv.h"
@@ -93,6 +94,7 @@ static CallOptions call_options(const pkv_attention_options *o)
     c.separate_write = o->separate_write != 0;
     c.decode_row_tiles = o->decode_row_tiles != 0;
     c.no_pdl = o->no_pdl != 0;
+    c.tc_key_pieces = o->tc_key_pieces < 0 ? -1 : (o->tc_key_pieces >= 2 ? o->tc_key_pieces : 0);
     return c;
 }
 
@@ -352,7 +354,12 @@ size_t pkv_attention_workspace_bytes(int32_t max_num_reqs, int32_t max_num_token
     if (pre_rows > 2 * 152 * 32) pre_rows = 2 * 152 * 32;
     int64_t pre_splits = splits < kMaxPrefillRowSplits ? splits : kMaxPrefillRowSplits;
     rows += pre_rows * pre_splits;
-    return kErrBytes + kCounterBytes + (size_t)rows * ((size_t)head_dim * 4 + 8) + 64;
+    // tcgen05 pairs cut into key pieces: 256-row partial slots, at most 16
+    // per (pair, KV head) group and 6 per SM of a 152-SM GPU
+    int64_t tc_slots = (int64_t)max_num_tokens * num_q_heads / 256 * kTcMaxPieces;
+    if (tc_slots > 6 * 152) tc_slots = 6 * 152;
+    const size_t tc_bytes = (size_t)tc_slots * 256 * ((size_t)head_dim * 4 + 8) + 256;
+    return kErrBytes + kCounterBytes + (size_t)rows * ((size_t)head_dim * 4 + 8) + 64 + tc_bytes;
 }
 
 size_t pkv_fp8_prefill_scratch_bytes(const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs,
@@ -578,7 +585,140 @@ struct AttnPlan {
     bool decode_main = false;           // ... the decodes on the caller's stream
     bool fork_after_scatter = false;    // ... the decodes fork after the ranged scatter
     int cluster_opt = 0;                // the caller's cluster choice (CallOptions::cluster)
+    // tcgen05 prefill key pieces (plan_tc_pieces)
+    std::vector<int32_t> tc_split;      // per tcgen05 request, in launch order: tc_split_pack(whole, pieces)
+    int64_t tc_groups = 0;              // (pair, KV head) groups cut into pieces: one counter each
+    int64_t tc_slots = 0;               // their pieces: one partial slot each
+    int64_t tc_ctas = 0;                // tcgen05 CTAs in all
+    size_t tc_part_off = 0;             // byte offset of the tcgen05 partial slots in the workspace
 };
+
+// ---- tcgen05 prefill: key pieces
+//
+// One tcgen05 CTA runs a pair of 128-row tiles of a prefill request over
+// all of its key tiles; requests and pairs are launched heaviest first, one
+// CTA per SM.  When the heavy pairs outnumber the SMs, those that start in
+// a later wave leave SMs idle at the end; cutting them into consecutive
+// key-tile pieces (merged by the piece that finishes last) evens that out.
+// The planner simulates the greedy schedule (each SM takes the next CTA in
+// launch order when it frees up) for a few piece sizes and keeps the best.
+
+// Key tiles of pair `pair` of a request with t new tokens and context L.
+static int tc_pair_tiles(int t, int L, int tt, int window, int pair)
+{
+    const int i0 = pair * 2 * tt;
+    const int k_end = L - t + i0 + std::min(2 * tt, t - i0);
+    return (k_end + 127) / 128 - window_lo(L - t + i0, window) / 128;
+}
+
+// Costs in key-tile times, measured on the mixed 2048-token-chunk step
+// (per-CTA timestamps): a CTA's start and finish (barriers, tensor memory,
+// the Q tiles, pipeline fill and drain, the output rows) ~3.5; a piece's
+// partial store and its share of the merge ~1 more.
+constexpr double kTcCtaCost = 3.5;
+constexpr double kTcPieceCost = 1.0;
+
+// Greedy list schedule of CTA costs on `sms` SMs: the time the last one ends.
+static double greedy_makespan(const std::vector<double> &costs, int sms)
+{
+    std::vector<double> heap(std::max(1, sms), 0.0);
+    std::make_heap(heap.begin(), heap.end(), std::greater<double>());
+    for (double c : costs) {
+        std::pop_heap(heap.begin(), heap.end(), std::greater<double>());
+        heap.back() += c;
+        std::push_heap(heap.begin(), heap.end(), std::greater<double>());
+    }
+    return *std::max_element(heap.begin(), heap.end());
+}
+
+static void plan_tc_pieces(AttnPlan &pl, const int32_t *qsl_h, const int32_t *sl_h, int32_t g, int32_t hkv,
+                           int32_t d, int32_t window, int sms, size_t room, int64_t counters_free,
+                           const CallOptions &o)
+{
+    const std::vector<int32_t> &tcp = pl.rc.tcp;
+    const int tt = tc_prefill_rows() / g;
+    pl.tc_split.assign(tcp.size(), tc_split_pack(0, 1));
+    pl.tc_groups = pl.tc_slots = 0;
+    // pair costs per request, longest first (the launch order)
+    std::vector<std::vector<int>> tiles(tcp.size());
+    for (size_t x = 0; x < tcp.size(); x++) {
+        const int32_t r = tcp[x], t = qsl_h[r + 1] - qsl_h[r], L = sl_h[r];
+        const int npairs = (t + 2 * tt - 1) / (2 * tt);
+        for (int k = npairs - 1; k >= 0; k--) tiles[x].push_back(tc_pair_tiles(t, L, tt, window, k));
+    }
+    auto count_ctas = [&](const std::vector<int32_t> &split) {
+        int64_t n = 0;
+        for (size_t x = 0; x < tcp.size(); x++) {
+            const int whole = tc_split_whole(split[x]), pieces = tc_split_pieces(split[x]);
+            const int np = (int)tiles[x].size();
+            n += (int64_t)(pieces > 1 ? whole + (np - whole) * pieces : np) * hkv;
+        }
+        return n;
+    };
+    pl.tc_ctas = count_ctas(pl.tc_split);
+    if (tcp.empty() || o.tc_key_pieces < 0) return;
+    const size_t slot_bytes = 256 * ((size_t)d * 4 + 8);
+    // One candidate: pairs that fit in the first wave run whole (forced:
+    // none), every later pair of the request in `want` pieces (at most its
+    // key tiles; uneven: the last piece small/64 of them).  Returns the
+    // simulated makespan in key-tile times, in launch order (piece-major).
+    auto candidate = [&](bool forced, int want, int small, std::vector<int32_t> &split, int64_t *groups,
+                         int64_t *slots) {
+        std::vector<double> costs;
+        int64_t placed = 0;
+        *groups = *slots = 0;
+        for (size_t x = 0; x < tcp.size(); x++) {
+            const std::vector<int> &c = tiles[x];
+            int whole = 0;
+            if (!forced)
+                while (whole < (int)c.size() && placed + (int64_t)(whole + 1) * hkv <= sms) whole++;
+            int pieces = whole < (int)c.size() ? want : 1;
+            for (size_t k = whole; k < c.size(); k++) pieces = std::min(pieces, c[k]);
+            pieces = std::max(1, std::min(pieces, kTcMaxPieces));
+            if (!forced && whole < (int)c.size() && c[whole] < 16) pieces = 1;   // short pairs stay whole
+            const int sm = pieces == 2 ? small : 0;
+            if (pieces == 1) whole = 0;
+            split[x] = tc_split_pack(whole, pieces, sm);
+            for (int k = 0; k < whole; k++)
+                for (int h = 0; h < hkv; h++) costs.push_back(c[k] + kTcCtaCost);
+            if (pieces == 1) {
+                for (size_t k = whole; k < c.size(); k++)
+                    for (int h = 0; h < hkv; h++) costs.push_back(c[k] + kTcCtaCost);
+            } else {
+                for (int q = 0; q < pieces; q++)                    // piece-major
+                    for (size_t k = whole; k < c.size(); k++) {
+                        const int n = tc_piece_begin(c[k], q + 1, pieces, sm) - tc_piece_begin(c[k], q, pieces, sm);
+                        for (int h = 0; h < hkv; h++) costs.push_back(n + kTcCtaCost + kTcPieceCost);
+                    }
+                *groups += (int64_t)(c.size() - whole) * hkv;
+                *slots += (int64_t)(c.size() - whole) * hkv * pieces;
+            }
+            placed += (int64_t)(pieces > 1 ? whole + ((int)c.size() - whole) * pieces : (int)c.size()) * hkv;
+        }
+        return greedy_makespan(costs, sms);
+    };
+    std::vector<int32_t> best(pl.tc_split), cur(tcp.size());
+    int64_t best_groups = 0, best_slots = 0, groups = 0, slots = 0;
+    double best_ms = candidate(false, 1, 0, best, &best_groups, &best_slots);     // every pair whole
+    struct Cand { int pieces, small; };
+    std::vector<Cand> cands;
+    if (o.tc_key_pieces >= 2) cands.push_back({o.tc_key_pieces, 0});
+    else cands = {{2, 0}, {3, 0}, {4, 0}, {2, 8}, {2, 12}, {2, 16}, {2, 20}};
+    for (const Cand &cd : cands) {
+        const double ms = candidate(o.tc_key_pieces >= 2, cd.pieces, cd.small, cur, &groups, &slots);
+        if (groups > counters_free || (size_t)slots * slot_bytes > room || slots == 0) continue;
+        if (ms < best_ms * 0.99 || o.tc_key_pieces >= 2) {
+            best = cur;
+            best_ms = ms;
+            best_groups = groups;
+            best_slots = slots;
+        }
+    }
+    pl.tc_split = best;
+    pl.tc_groups = best_groups;
+    pl.tc_slots = best_slots;
+    pl.tc_ctas = count_ctas(best);
+}
 
 static int32_t decode_splits_of(const int32_t *qsl_h, const int32_t *sl_h, int32_t r, int32_t window, int sp)
 {
@@ -639,6 +779,19 @@ static AttnPlan make_plan(const int32_t *qsl_h, const int32_t *sl_h, int32_t num
     pl.split = split;
     bool unused = false;
     pl.total_rows = plan_partial_rows(pl, qsl_h, sl_h, hq, window, split, &unused);
+    // tcgen05 key pieces: their partial slots follow the decode partials,
+    // their counters come first in the counter region
+    const size_t dec_part = pl.total_rows ? ((pl.total_rows * d * 4 + 15) / 16) * 16 + pl.total_rows * 8 : 0;
+    pl.tc_part_off = (pl.part_base + dec_part + 255) & ~(size_t)255;
+    const size_t tc_room = pl.ws_front > pl.tc_part_off + 64 ? pl.ws_front - pl.tc_part_off - 64 : 0;
+    // Cut tcgen05 pairs only when no decode class runs beside them: measured
+    // on the mixed 2048-token-chunk step, the decodes on the side stream fill
+    // the SMs an uneven prefill leaves idle (step 518 us); with the prefill
+    // evened out they run after it instead (563 us), although the prefill
+    // alone gets faster (461 -> 445 us).
+    const bool tc_alone = rc.dec.empty() || o.tc_key_pieces >= 2;
+    plan_tc_pieces(pl, qsl_h, sl_h, g, hkv, d, window, sms, tc_room,
+                   pl.has_counters && tc_alone ? kCounterGroups / 2 : 0, o);
     // Decode-class work runs on a second stream, concurrently with the
     // prefill kernels, when both are present; the class expected to take
     // longer goes on the caller's stream (the decode_main option forces it).
@@ -877,7 +1030,14 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
         tc_slots = fp8_blocks * 16;
     }
 
-    // ---- tensor-core prefill launches, submitted first: the longest work
+    // ---- tensor-core prefill launches, submitted first: the longest work.
+    // Pairs cut into key pieces keep fp32 partials in slots of 256 rows at
+    // tc_part_off and count on the first tc_groups split counters.
+    if (pl.tc_slots > 0) {
+        pt.part_o = reinterpret_cast<float *>(ws + pl.tc_part_off);
+        pt.part_ml = reinterpret_cast<float2 *>(ws + pl.tc_part_off + (size_t)pl.tc_slots * 256 * d * 4);
+    }
+    int64_t tc_slot_cursor = 0, tc_counter_cursor = 0;
     for (size_t c0 = 0; c0 < tcp.size(); c0 += kPlanMax) {
         WorkList wl;
         memset(&wl, 0, sizeof wl);
@@ -889,9 +1049,19 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
             int32_t r = tcp[x];
             int32_t t = qsl_h[r + 1] - qsl_h[r];
             int li = list_request(wl, r);
+            const int npairs = (t + 2 * wl.tile_tokens - 1) / (2 * wl.tile_tokens);   // pairs of 128-row tiles
+            const int whole = tc_split_whole(pl.tc_split[x]), pieces = tc_split_pieces(pl.tc_split[x]);
+            wl.tc_split[li] = pl.tc_split[x];
             wl.item_off[li] = items;
-            wl.part_off[li] = -1;
-            items += (t + 2 * wl.tile_tokens - 1) / (2 * wl.tile_tokens);   // pairs of 128-row tiles
+            wl.part_off[li] = (int32_t)tc_slot_cursor;
+            wl.cnt_off[li] = (int32_t)tc_counter_cursor;
+            if (pieces > 1) {
+                tc_slot_cursor += (int64_t)(npairs - whole) * hkv * pieces;
+                tc_counter_cursor += (int64_t)(npairs - whole) * hkv;
+                items += whole + (npairs - whole) * pieces;
+            } else {
+                items += npairs;
+            }
         }
         wl.item_off[wl.n] = items;
         cudaError_t e = launch_attn_tc(pt, wl, items, q, num_tokens, tc_k, tc_v, tc_slots, d, pstream);
@@ -908,7 +1078,7 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
     };
     CombineSet dec_combine, pre_combine;
     size_t part_cursor = 0;
-    int counter_cursor = 0;
+    int counter_cursor = (int)pl.tc_groups;                   // after the tcgen05 pieces' counters
     // partial rows of a split request; combined by `set`'s combine launch,
     // or inside the attention kernel when in_kernel
     auto take_partials = [&](CombineSet &set, int32_t r, int32_t S, bool in_kernel = false) -> int32_t {
@@ -1119,6 +1289,7 @@ pkv_status pkv_plan_attention(const int32_t *qsl_h, const int32_t *sl_h, int32_t
     out->overlap = pl.fork;
     out->decode_on_caller_stream = pl.fork && pl.decode_main;
     out->prefill_key_splits = pl.pre_split;
+    out->prefill_tensor_pieces = (int32_t)pl.tc_slots;
     out->quantized_prefill_scratch = pl.rc.fp8_scratch;
     out->partial_bytes = pl.total_rows ? ((pl.total_rows * d * 4 + 15) / 16) * 16 + pl.total_rows * 8 : 0;
     return PKV_OK;

@@ -93,7 +93,7 @@ def test_combined_call_full_size(cfg):
                               spec.head_dim, combined=True, workspace_bytes=dev.ws.numel())
     if cfg == 5:
         assert plan["max_decode_splits"] >= 8 and plan["decode_streaming"]
-    if cfg == 4:
+    if cfg == 4:                                        # decodes on a side stream beside the tcgen05 pairs
         assert plan["overlap"] and plan["prefill_tensor_requests"] == 3
     _replay_in_graph(dev.combined)
     assert torch.isfinite(dev.out.float()).all()
