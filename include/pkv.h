@@ -249,6 +249,10 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q,
  *   tc_key_pieces       -1: no tcgen05 pair is cut into key pieces; k >= 2:
  *                       every tcgen05 pair is cut into k pieces (at most its
  *                       key tiles), merged by the CTA that finishes last
+ *   mixed_launch        1: a batch's decode class runs inside the tcgen05
+ *                       prefill launch whenever it can (one launch for both
+ *                       classes); -1: never; 0: when the planner expects the
+ *                       decode work to fit beside the prefill
  */
 typedef struct pkv_attention_options {
     int32_t disable_tcgen05;
@@ -263,7 +267,8 @@ typedef struct pkv_attention_options {
     int32_t decode_row_tiles;
     int32_t no_pdl;
     int32_t tc_key_pieces;
-    int32_t reserved[4];
+    int32_t mixed_launch;
+    int32_t reserved[3];
 } pkv_attention_options;
 
 /* pkv_ragged_paged_attention with options (NULL: the planner's choices). */
@@ -525,6 +530,8 @@ typedef struct pkv_attention_plan {
     int32_t prefill_tensor_pieces;    /* tcgen05 CTAs that run a key piece of a pair (0: no pair is cut) */
     size_t quantized_prefill_scratch; /* workspace bytes of bf16 block copies for quantized prefill */
     size_t partial_bytes;             /* workspace bytes of split partials */
+    int32_t mixed_launch;             /* 1: decode items run inside the tcgen05 prefill launch (one launch) */
+    int32_t mixed_decode_items;       /* ... how many */
 } pkv_attention_plan;
 pkv_status pkv_plan_attention(const int32_t *query_start_loc_host, const int32_t *seq_lens_host,
                               int32_t num_reqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,

@@ -51,6 +51,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "decode_warp.cuh"
 #include "sm100.cuh"
 
 namespace pkv {
@@ -71,7 +72,14 @@ struct TcCfg {
     static constexpr int kBarOff = kVOff + 2 * kTile;
     static constexpr int kXOff = kBarOff + 256;        // softmax pair exchange: max [2][2][128], sum [2][128]
     static constexpr int kSmem = 1024 + kXOff + 3 * 1024;
+    // mixed batches: warp 3's decode ring (kDecStages stages of a K and a V
+    // slice) after the exchange area; its barriers at kBarOff + 128
+    static constexpr int kDecStages = DP == 128 ? 3 : 6;
+    static constexpr int kDecOff = (kXOff + 3 * 1024 + 1023) / 1024 * 1024;
+    static constexpr int kSmemMix = 1024 + kDecOff + kDecStages * WarpRing<DP>::kStage;
+    static_assert(kSmemMix <= 227 * 1024, "the decode ring must fit beside the prefill tiles");
 };
+
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;  // move the running max only when it grows by more than this
 
@@ -366,13 +374,13 @@ __device__ __forceinline__ void tc_piece_epilogue(const AttnParams &p, uint32_t 
 }
 
 // DP: head dim padded to the 64-column sub-tile; D: head dim of q and out;
-// WIN: a sliding window is set (p.window > 0).
-template <int DP, int D, bool WIN>
-__global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, const __grid_constant__ WorkList wl,
-                                                                const __grid_constant__ CUtensorMap qmap,
-                                                                const __grid_constant__ CUtensorMap kmap,
-                                                                const __grid_constant__ CUtensorMap vmap,
-                                                                int64_t num_slots)
+// WIN: a sliding window is set (p.window > 0).  MIX: a mixed batch, whose
+// decode-class items (list dl, parameters pd, per-row assignment mix) warp 3
+// runs beside the prefill.
+template <int DP, int D, bool WIN, bool MIX>
+__device__ __forceinline__ void attn_tc_body(const AttnParams &p, const WorkList &wl, const CUtensorMap &qmap,
+                                             const CUtensorMap &kmap, const CUtensorMap &vmap, int64_t num_slots,
+                                             const AttnParams *pd, const WorkList *dl, const MixAssign *mix)
 {
     using C = TcCfg<DP>;
     constexpr int kTile = C::kTile, kQOff = C::kQOff, kKOff = C::kKOff, kVOff = C::kVOff, kBarOff = C::kBarOff;
@@ -606,6 +614,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, co
             mbar_wait(bar(kBarMmaDone), 0, p.err);
         }
         __syncwarp();
+    } else if (MIX && warp == 3) {
+        // ------------------------------------------------------------ decode items (mixed batches)
+        const int y = blockIdx.y;
+        const int n = mix->first[y + 1] - mix->first[y];
+        const int a0 = mix->first[y] + n * kh / p.hkv, a1 = mix->first[y] + n * (kh + 1) / p.hkv;
+        if (a0 < a1) {
+            constexpr int NS = C::kDecStages;
+            WarpPipe wp;
+            wp.ring = sb + C::kDecOff;
+            wp.bars = sb + kBarOff + 128;
+            wp.stage_f = reinterpret_cast<float *>(sp + C::kDecOff);
+            wp.seq = 0;
+            if (lane == 0) {
+                for (int s = 0; s < NS; s++) mbar_init(wp.bars + 8u * s, 1);
+                fence_mbar_init();
+            }
+            __syncwarp();
+            pdl_wait();                                            // the step's earlier kernels are done
+            for (int it = a0; it < a1; it++) {
+                warp_decode_item<DP, D, NS>(*pd, *dl, it, wp, &kmap, &vmap, num_slots);
+                __syncwarp();
+                // the epilogue's reads of the ring precede the next item's copies into it
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            }
+        }
     } else if (warp >= 4 && has_b) {
         // ------------------------------------------------------------ softmax, one row per thread
         const int x = warp >= 8 ? 1 : 0;                           // tile a or b
@@ -744,6 +777,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, co
     }
 }
 
+template <int DP, int D, bool WIN>
+__global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, const __grid_constant__ WorkList wl,
+                                                                const __grid_constant__ CUtensorMap qmap,
+                                                                const __grid_constant__ CUtensorMap kmap,
+                                                                const __grid_constant__ CUtensorMap vmap,
+                                                                int64_t num_slots)
+{
+    attn_tc_body<DP, D, WIN, false>(p, wl, qmap, kmap, vmap, num_slots, nullptr, nullptr, nullptr);
+}
+
+template <int DP, int D, bool WIN>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    attn_tc_mix_kernel(AttnParams p, const __grid_constant__ WorkList wl, const __grid_constant__ CUtensorMap qmap,
+                       const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                       int64_t num_slots, AttnParams pd, const __grid_constant__ WorkList dl,
+                       const __grid_constant__ MixAssign mix)
+{
+    attn_tc_body<DP, D, WIN, true>(p, wl, qmap, kmap, vmap, num_slots, &pd, &dl, &mix);
+}
+
 // ---------------------------------------------------------------- host side
 
 cudaError_t make_pool_tmap(CUtensorMap *map, const void *pool, int64_t num_slots, int hkv, int d, int box_cols,
@@ -758,13 +811,17 @@ int tc_prefill_rows() { return kTcRows; }
 
 template <int DP, int D, bool WIN>
 static cudaError_t launch_tc_d(const AttnParams &p, const WorkList &wl, int num_items, const void *q, int num_tokens,
-                               const void *k_cache, const void *v_cache, int64_t num_slots, cudaStream_t stream)
+                               const void *k_cache, const void *v_cache, int64_t num_slots, cudaStream_t stream,
+                               const AttnParams *pd, const WorkList *dl, const MixAssign *mix)
 {
-    constexpr int smem = TcCfg<DP>::kSmem;
+    constexpr int smem = TcCfg<DP>::kSmem, smem_mix = TcCfg<DP>::kSmemMix;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
         attr_err = cudaFuncSetAttribute(attn_tc_kernel<DP, D, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(attn_tc_mix_kernel<DP, D, WIN>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem_mix);
     });
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap qm, km, vm;
@@ -775,30 +832,32 @@ static cudaError_t launch_tc_d(const AttnParams &p, const WorkList &wl, int num_
     if (e != cudaSuccess) return e;
     if (num_items > 65535) return cudaErrorInvalidConfiguration;
     dim3 grid(p.hkv, num_items);                   // items in launch order: the planner puts the longest first
-    launch_begin(stream, kAttnTcPrefill);
-    e = launch_maybe_pdl(attn_tc_kernel<DP, D, WIN>, grid, dim3(kTcThreads), smem, stream, p, wl, qm, km, vm, num_slots);
+    launch_begin(stream, mix ? kAttnTcMixed : kAttnTcPrefill);
+    if (mix)
+        e = launch_maybe_pdl(attn_tc_mix_kernel<DP, D, WIN>, grid, dim3(kTcThreads), smem_mix, stream, p, wl, qm, km,
+                             vm, num_slots, *pd, *dl, *mix);
+    else
+        e = launch_maybe_pdl(attn_tc_kernel<DP, D, WIN>, grid, dim3(kTcThreads), smem, stream, p, wl, qm, km, vm,
+                             num_slots);
     launch_end(stream);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_attn_tc(const AttnParams &p, const WorkList &wl, int num_items, const void *q, int num_tokens,
                            const void *k_cache, const void *v_cache, int64_t num_slots, int head_dim,
-                           cudaStream_t stream)
+                           cudaStream_t stream, const AttnParams *pd, const WorkList *dl, const MixAssign *mix)
 {
     if (num_items <= 0) return cudaSuccess;
+    if (mix && (!pd || !dl || mix->rows != num_items)) return cudaErrorInvalidValue;
     const bool win = p.window > 0;
+#define PKV_TC_ARGS p, wl, num_items, q, num_tokens, k_cache, v_cache, num_slots, stream, pd, dl, mix
     switch (head_dim) {
-    case 48:
-        return win ? launch_tc_d<64, 48, true>(p, wl, num_items, q, num_tokens, k_cache, v_cache, num_slots, stream)
-                   : launch_tc_d<64, 48, false>(p, wl, num_items, q, num_tokens, k_cache, v_cache, num_slots, stream);
-    case 64:
-        return win ? launch_tc_d<64, 64, true>(p, wl, num_items, q, num_tokens, k_cache, v_cache, num_slots, stream)
-                   : launch_tc_d<64, 64, false>(p, wl, num_items, q, num_tokens, k_cache, v_cache, num_slots, stream);
-    case 128:
-        return win ? launch_tc_d<128, 128, true>(p, wl, num_items, q, num_tokens, k_cache, v_cache, num_slots, stream)
-                   : launch_tc_d<128, 128, false>(p, wl, num_items, q, num_tokens, k_cache, v_cache, num_slots, stream);
+    case 48: return win ? launch_tc_d<64, 48, true>(PKV_TC_ARGS) : launch_tc_d<64, 48, false>(PKV_TC_ARGS);
+    case 64: return win ? launch_tc_d<64, 64, true>(PKV_TC_ARGS) : launch_tc_d<64, 64, false>(PKV_TC_ARGS);
+    case 128: return win ? launch_tc_d<128, 128, true>(PKV_TC_ARGS) : launch_tc_d<128, 128, false>(PKV_TC_ARGS);
     default: return cudaErrorInvalidValue;
     }
+#undef PKV_TC_ARGS
 }
 
 }  // namespace pkv

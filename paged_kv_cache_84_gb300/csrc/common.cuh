@@ -339,12 +339,24 @@ cudaError_t launch_attn_mma(const AttnParams &p, const WorkList &wl, int head_di
                             const float *k_scale = nullptr, const float *v_scale = nullptr);
 int mma_prefill_rows();
 
+// Decode items of a mixed launch per grid row: the tcgen05 CTAs of row y
+// (one per KV head) run decode items first[y] .. first[y + 1] - 1 on their
+// warp 3, divided evenly among them.
+constexpr int kMixMaxRows = 1023;
+struct MixAssign {
+    int32_t rows;
+    int32_t first[kMixMaxRows + 1];
+};
+
 // tcgen05 prefill tiles of 128 query rows (head_dim 48, 64 or 128, g dividing 128).
+// With mix (and pd, dl): the mixed-batch kernel, whose warp 3 also runs the
+// decode items of list dl with parameters pd.
 bool tc_prefill_supported(int head_dim, int group);
 int tc_prefill_rows();
 cudaError_t launch_attn_tc(const AttnParams &p, const WorkList &wl, int num_items, const void *q, int num_tokens,
                            const void *k_cache, const void *v_cache, int64_t num_slots, int head_dim,
-                           cudaStream_t stream);
+                           cudaStream_t stream, const AttnParams *pd = nullptr, const WorkList *dl = nullptr,
+                           const MixAssign *mix = nullptr);
 
 // Block copies over up to kMaxPools pools: mode 0 copies block src[i] to
 // dst[i] in every pool, 1 gathers block src[i] of pool q to buf[q][i], 2
@@ -376,7 +388,8 @@ enum KernelId : int {
     kAttnMmaPrefill = 6,
     kBlockCopy = 7,
     kByteCopy = 8,
-    kNumKernelIds = 9
+    kAttnTcMixed = 9,
+    kNumKernelIds = 10
 };
 
 // Call around every kernel launch: counts it and, while profiling is on,
@@ -400,6 +413,7 @@ struct CallOptions {
     bool decode_row_tiles = false;    // 16-row decode tiles instead of key-major ones
     bool no_pdl = false;              // no programmatic dependent launches
     int tc_key_pieces = 0;            // 0: planner; -1: no key pieces; k >= 2: every tcgen05 pair in k pieces
+    int mixed_launch = 0;             // 0: planner; 1: decode class in the tcgen05 launch when it can; -1: never
 };
 
 // Launch-level choices of the attention call in progress on this thread,

@@ -95,6 +95,7 @@ static CallOptions call_options(const pkv_attention_options *o)
     c.decode_row_tiles = o->decode_row_tiles != 0;
     c.no_pdl = o->no_pdl != 0;
     c.tc_key_pieces = o->tc_key_pieces < 0 ? -1 : (o->tc_key_pieces >= 2 ? o->tc_key_pieces : 0);
+    c.mixed_launch = o->mixed_launch > 0 ? 1 : (o->mixed_launch < 0 ? -1 : 0);
     return c;
 }
 
@@ -256,6 +257,7 @@ const char *pkv_kernel_name(int32_t kernel_id)
     case kAttnMmaPrefill: return "attn_mma_prefill";
     case kBlockCopy: return "block_copy";
     case kByteCopy: return "byte_copy";
+    case kAttnTcMixed: return "attn_tc_mixed";
     }
     return "unknown";
 }
@@ -591,6 +593,11 @@ struct AttnPlan {
     int64_t tc_slots = 0;               // their pieces: one partial slot each
     int64_t tc_ctas = 0;                // tcgen05 CTAs in all
     size_t tc_part_off = 0;             // byte offset of the tcgen05 partial slots in the workspace
+    double tc_makespan = 0.0;           // simulated tcgen05 makespan, key-tile times
+    // mixed launch: the decode class inside the tcgen05 launch (warp 3 of its CTAs)
+    bool mix = false;
+    int32_t mix_items = 0;              // decode items (request, split, KV head)
+    std::vector<int32_t> mix_first;     // per tcgen05 grid row: its first decode item (+ the end)
 };
 
 // ---- tcgen05 prefill: key pieces
@@ -718,6 +725,35 @@ static void plan_tc_pieces(AttnPlan &pl, const int32_t *qsl_h, const int32_t *sl
     pl.tc_groups = best_groups;
     pl.tc_slots = best_slots;
     pl.tc_ctas = count_ctas(best);
+    pl.tc_makespan = best_ms;
+}
+
+// Costs of the tcgen05 grid rows in launch order (one row = the CTAs of one
+// pair or piece, one per KV head), in key-tile times: the order in which
+// attn_tc_kernel maps blockIdx.y to pairs and pieces.
+static std::vector<double> tc_row_costs(const AttnPlan &pl, const int32_t *qsl_h, const int32_t *sl_h, int32_t g,
+                                        int32_t window)
+{
+    std::vector<double> rows;
+    const int tt = tc_prefill_rows() / g;
+    for (size_t x = 0; x < pl.rc.tcp.size(); x++) {
+        const int32_t r = pl.rc.tcp[x], t = qsl_h[r + 1] - qsl_h[r], L = sl_h[r];
+        const int npairs = (t + 2 * tt - 1) / (2 * tt);
+        const int whole = tc_split_whole(pl.tc_split[x]), pieces = tc_split_pieces(pl.tc_split[x]);
+        const int sm = tc_split_small(pl.tc_split[x]);
+        std::vector<int> c;
+        for (int k = npairs - 1; k >= 0; k--) c.push_back(tc_pair_tiles(t, L, tt, window, k));
+        if (pieces == 1) {
+            for (int k = 0; k < npairs; k++) rows.push_back(c[k] + kTcCtaCost);
+            continue;
+        }
+        for (int k = 0; k < whole; k++) rows.push_back(c[k] + kTcCtaCost);
+        for (int q = 0; q < pieces; q++)
+            for (int k = whole; k < npairs; k++)
+                rows.push_back(tc_piece_begin(c[k], q + 1, pieces, sm) - tc_piece_begin(c[k], q, pieces, sm) +
+                               kTcCtaCost + kTcPieceCost);
+    }
+    return rows;
 }
 
 static int32_t decode_splits_of(const int32_t *qsl_h, const int32_t *sl_h, int32_t r, int32_t window, int sp)
@@ -739,6 +775,24 @@ static size_t plan_partial_rows(const AttnPlan &pl, const int32_t *qsl_h, const 
     return rows;
 }
 
+// ---- mixed launch: the decode class inside the tcgen05 launch
+//
+// For a batch of prefill chunks on tcgen05 and decodes (one flattened
+// ragged batch, "31. Engine v2", "Flattened ragged batches"), warp 3 of
+// every tcgen05 CTA runs decode items (request, KV head, key split) with
+// its own ring of KV stages, while the other warps run the prefill tiles:
+// one launch for both classes.  The prefill is bound by the tensor pipe, the
+// decodes by HBM, so they share the SMs.  Each grid row gets decode items in
+// proportion to its prefill cost; the planner takes this arrangement when
+// the decode work fits in kMixFill of the prefill's time at kMixWarpGBs per
+// warp, the rate measured on the mixed 2048-token-chunk step (one 1024-key
+// item of head dim 128, 512 KB of K and V, in ~60 us beside the prefill).
+constexpr int kMixDecodeRows = 8;         // decode items: key-major tiles, t * g <= 8 rows per KV head
+constexpr int kMixSplit = 1024;           // keys per decode item
+constexpr double kMixWarpGBs = 8.5;       // one warp's decode rate beside the prefill, GB/s
+constexpr double kMixFill = 0.8;
+constexpr double kTcTileUs = 1.66;        // a key tile of a pair on tcgen05, measured on the mixed step
+
 static AttnPlan make_plan(const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs, int32_t hq, int32_t hkv,
                           int32_t d, int32_t bs, int32_t window, bool fp8, bool fused, size_t workspace_bytes, int sms,
                           const CallOptions &o)
@@ -749,8 +803,6 @@ static AttnPlan make_plan(const int32_t *qsl_h, const int32_t *sl_h, int32_t num
     const RequestClasses &rc = pl.rc;
     for (int r = 0; r < num_reqs; r++) pl.seen_l = sl_h[r] > pl.seen_l ? sl_h[r] : pl.seen_l;
     class_times(rc, qsl_h, sl_h, hq, hkv, d, &pl.dec_us, &pl.pre_us);
-    int split = decode_split_tokens(rc, pl.dec_us, pl.pre_us, hkv, fp8, o, sms);
-    if (split % bs) split += bs - split % bs;
     // Prefill-class tiles are split over keys as well when the batch has too
     // few of them to fill the GPU (small, latency-bound steps): every tile of
     // such a request gets the request's number of splits.
@@ -766,32 +818,93 @@ static AttnPlan make_plan(const int32_t *qsl_h, const int32_t *sl_h, int32_t num
     pl.ws_front = rc.fp8_scratch ? ((workspace_bytes - rc.fp8_scratch) & ~(size_t)255) : workspace_bytes;
     pl.has_counters = pl.ws_front >= kErrBytes + kCounterBytes + 64;
     pl.part_base = kErrBytes + (pl.has_counters ? kCounterBytes : 0);
-    const size_t avail = pl.ws_front - pl.part_base;
-    // every split request keeps S * t * hq partial rows; grow the split until they fit
-    const size_t row_bytes = (size_t)d * 4 + 8;
-    for (;;) {
-        bool too_many = false;
-        const size_t rows = plan_partial_rows(pl, qsl_h, sl_h, hq, window, split, &too_many);
-        if (!too_many && rows * row_bytes + 64 <= avail) break;
-        if (split >= pl.seen_l) break;                          // nothing is split any more
-        split *= 2;
+    pl.cluster_opt = o.cluster;
+
+    // The split length, the workspace layout and the tcgen05 pieces for a
+    // starting split length (grown until the decode partials fit) and
+    // whether decodes run beside the tcgen05 CTAs.
+    auto layout = [&](AttnPlan &q, int split, bool tc_alone) {
+        if (split % bs) split += bs - split % bs;
+        const size_t avail = q.ws_front - q.part_base;
+        // every split request keeps S * t * hq partial rows; grow the split until they fit
+        const size_t row_bytes = (size_t)d * 4 + 8;
+        for (;;) {
+            bool too_many = false;
+            const size_t rows = plan_partial_rows(q, qsl_h, sl_h, hq, window, split, &too_many);
+            if (!too_many && rows * row_bytes + 64 <= avail) break;
+            if (split >= q.seen_l) break;                       // nothing is split any more
+            split *= 2;
+        }
+        q.split = split;
+        bool unused = false;
+        q.total_rows = plan_partial_rows(q, qsl_h, sl_h, hq, window, split, &unused);
+        // tcgen05 key pieces: their partial slots follow the decode partials,
+        // their counters come first in the counter region
+        const size_t dec_part = q.total_rows ? ((q.total_rows * d * 4 + 15) / 16) * 16 + q.total_rows * 8 : 0;
+        q.tc_part_off = (q.part_base + dec_part + 255) & ~(size_t)255;
+        const size_t tc_room = q.ws_front > q.tc_part_off + 64 ? q.ws_front - q.tc_part_off - 64 : 0;
+        plan_tc_pieces(q, qsl_h, sl_h, g, hkv, d, window, sms, tc_room,
+                       q.has_counters && tc_alone ? kCounterGroups / 2 : 0, o);
+    };
+
+    // ---- the decode class inside the tcgen05 launch, when it fits there
+    bool mix_ok = !fp8 && !rc.tcp.empty() && !rc.dec.empty() && rc.pre.empty() && o.mixed_launch >= 0 &&
+                  rc.tcp.size() <= (size_t)kPlanMax && rc.dec.size() <= (size_t)kPlanMax && pl.has_counters &&
+                  (d == 128 || d == 64 || d == 48);
+    for (int32_t r : rc.dec)
+        if ((qsl_h[r + 1] - qsl_h[r]) * g > kMixDecodeRows) mix_ok = false;
+    if (mix_ok) {
+        AttnPlan m = pl;
+        layout(m, o.split_tokens > 0 ? o.split_tokens : kMixSplit, true);
+        int64_t items = 0, counters = m.tc_groups;
+        double dec_bytes = 0.0;
+        std::vector<double> item_cost;
+        for (int32_t r : rc.dec) {
+            const int32_t t = qsl_h[r + 1] - qsl_h[r], L = sl_h[r];
+            const int S = decode_splits(t, L, window, m.split);
+            const int k0 = decode_key_begin(t, L, window);
+            for (int sp = 0; sp < S; sp++) {
+                const int keys = L <= 0 ? 0 : std::min(L, k0 + (sp + 1) * m.split) - (k0 + sp * m.split);
+                for (int h = 0; h < hkv; h++) item_cost.push_back(keys + 16.0);
+                dec_bytes += (double)keys * hkv * d * 4.0;
+            }
+            items += (int64_t)S * hkv;
+            if (S > 1) counters += hkv;
+        }
+        const std::vector<double> rows = tc_row_costs(m, qsl_h, sl_h, g, window);
+        double pre_cost = 0.0;
+        for (double c : rows) pre_cost += c;
+        // SM time of the prefill CTAs vs that of the decode items on warp 3
+        const double pre_sm_us = pre_cost * hkv * kTcTileUs;
+        const double dec_sm_us = dec_bytes / (kMixWarpGBs * 1e3);
+        const bool fits = dec_sm_us <= kMixFill * pre_sm_us;
+        if ((fits || o.mixed_launch > 0) && counters <= kCounterGroups && rows.size() <= (size_t)kMixMaxRows &&
+            items < INT32_MAX) {
+            m.mix = true;
+            m.mix_items = (int32_t)items;
+            // rows get items in proportion to their cost, in launch order
+            double total_dec = 0.0;
+            for (double c : item_cost) total_dec += c;
+            m.mix_first.assign(rows.size() + 1, 0);
+            double cum_pre = 0.0, cum_dec = 0.0;
+            size_t it = 0;
+            for (size_t y = 0; y < rows.size(); y++) {
+                m.mix_first[y] = (int32_t)it;
+                cum_pre += rows[y];
+                const double target = cum_pre / pre_cost * total_dec;
+                while (it < item_cost.size() && cum_dec + 0.5 * item_cost[it] <= target) cum_dec += item_cost[it++];
+            }
+            m.mix_first[rows.size()] = (int32_t)items;
+            return m;
+        }
     }
-    pl.split = split;
-    bool unused = false;
-    pl.total_rows = plan_partial_rows(pl, qsl_h, sl_h, hq, window, split, &unused);
-    // tcgen05 key pieces: their partial slots follow the decode partials,
-    // their counters come first in the counter region
-    const size_t dec_part = pl.total_rows ? ((pl.total_rows * d * 4 + 15) / 16) * 16 + pl.total_rows * 8 : 0;
-    pl.tc_part_off = (pl.part_base + dec_part + 255) & ~(size_t)255;
-    const size_t tc_room = pl.ws_front > pl.tc_part_off + 64 ? pl.ws_front - pl.tc_part_off - 64 : 0;
+
     // Cut tcgen05 pairs only when no decode class runs beside them: measured
     // on the mixed 2048-token-chunk step, the decodes on the side stream fill
     // the SMs an uneven prefill leaves idle (step 518 us); with the prefill
     // evened out they run after it instead (563 us), although the prefill
     // alone gets faster (461 -> 445 us).
-    const bool tc_alone = rc.dec.empty() || o.tc_key_pieces >= 2;
-    plan_tc_pieces(pl, qsl_h, sl_h, g, hkv, d, window, sms, tc_room,
-                   pl.has_counters && tc_alone ? kCounterGroups / 2 : 0, o);
+    layout(pl, decode_split_tokens(rc, pl.dec_us, pl.pre_us, hkv, fp8, o, sms), rc.dec.empty() || o.tc_key_pieces >= 2);
     // Decode-class work runs on a second stream, concurrently with the
     // prefill kernels, when both are present; the class expected to take
     // longer goes on the caller's stream (the decode_main option forces it).
@@ -805,9 +918,9 @@ static AttnPlan make_plan(const int32_t *qsl_h, const int32_t *sl_h, int32_t num
         // the decodes starting at once).
         pl.fork_after_scatter = fused && !pl.decode_main;
     }
-    pl.cluster_opt = o.cluster;
     return pl;
 }
+
 
 // CTAs per thread-block cluster of a decode launch whose requests have at
 // most s_max splits, or 0 for no clusters.  Short split decodes (the
@@ -1030,48 +1143,7 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
         tc_slots = fp8_blocks * 16;
     }
 
-    // ---- tensor-core prefill launches, submitted first: the longest work.
-    // Pairs cut into key pieces keep fp32 partials in slots of 256 rows at
-    // tc_part_off and count on the first tc_groups split counters.
-    if (pl.tc_slots > 0) {
-        pt.part_o = reinterpret_cast<float *>(ws + pl.tc_part_off);
-        pt.part_ml = reinterpret_cast<float2 *>(ws + pl.tc_part_off + (size_t)pl.tc_slots * 256 * d * 4);
-    }
-    int64_t tc_slot_cursor = 0, tc_counter_cursor = 0;
-    for (size_t c0 = 0; c0 < tcp.size(); c0 += kPlanMax) {
-        WorkList wl;
-        memset(&wl, 0, sizeof wl);
-        wl.mode = kModePrefill;
-        wl.tile_tokens = tc_prefill_rows() / g;
-        int items = 0;
-        size_t c1 = c0 + kPlanMax < tcp.size() ? c0 + kPlanMax : tcp.size();
-        for (size_t x = c0; x < c1; x++) {
-            int32_t r = tcp[x];
-            int32_t t = qsl_h[r + 1] - qsl_h[r];
-            int li = list_request(wl, r);
-            const int npairs = (t + 2 * wl.tile_tokens - 1) / (2 * wl.tile_tokens);   // pairs of 128-row tiles
-            const int whole = tc_split_whole(pl.tc_split[x]), pieces = tc_split_pieces(pl.tc_split[x]);
-            wl.tc_split[li] = pl.tc_split[x];
-            wl.item_off[li] = items;
-            wl.part_off[li] = (int32_t)tc_slot_cursor;
-            wl.cnt_off[li] = (int32_t)tc_counter_cursor;
-            if (pieces > 1) {
-                tc_slot_cursor += (int64_t)(npairs - whole) * hkv * pieces;
-                tc_counter_cursor += (int64_t)(npairs - whole) * hkv;
-                items += whole + (npairs - whole) * pieces;
-            } else {
-                items += npairs;
-            }
-        }
-        wl.item_off[wl.n] = items;
-        cudaError_t e = launch_attn_tc(pt, wl, items, q, num_tokens, tc_k, tc_v, tc_slots, d, pstream);
-        if (e != cudaSuccess) {
-            join();
-            return cuda_fail(e, "tensor-core prefill launch");
-        }
-    }
-
-    // ---- decode-class launches (chunks of kPlanMax requests)
+    // ---- split partials and counters of the decode class (and of warp-MMA prefill)
     struct CombineSet {
         std::vector<int32_t> reqs, offs;
         int max_rows = 0;
@@ -1113,7 +1185,76 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
         }
         return cudaSuccess;
     };
-    for (size_t c0 = 0; c0 < dec.size(); c0 += kPlanMax) {
+    // ---- mixed launch: the decode class as warp-3 items of the tcgen05 launch
+    WorkList mix_dl;
+    MixAssign mix_as;
+    if (pl.mix) {
+        memset(&mix_dl, 0, sizeof mix_dl);
+        mix_dl.mode = kModeDecode;
+        mix_dl.split_tokens = split;
+        int items = 0;
+        for (int32_t r : dec) {
+            const int32_t S = dec_splits_of(r, split);
+            const int li = list_request(mix_dl, r);
+            mix_dl.item_off[li] = items;
+            mix_dl.part_off[li] = take_partials(dec_combine, r, S, true);
+            if (S > 1) {
+                mix_dl.cnt_off[li] = counter_cursor;
+                counter_cursor += hkv;
+            }
+            items += S * hkv;
+        }
+        mix_dl.item_off[mix_dl.n] = items;
+        mix_as.rows = (int32_t)pl.mix_first.size() - 1;
+        for (size_t y = 0; y < pl.mix_first.size(); y++) mix_as.first[y] = pl.mix_first[y];
+        if (counter_cursor > kCounterGroups || items != pl.mix_items) return PKV_ERR_UNSUPPORTED;
+    }
+
+    // ---- tensor-core prefill launches, submitted first: the longest work.
+    // Pairs cut into key pieces keep fp32 partials in slots of 256 rows at
+    // tc_part_off and count on the first tc_groups split counters.
+    if (pl.tc_slots > 0) {
+        pt.part_o = reinterpret_cast<float *>(ws + pl.tc_part_off);
+        pt.part_ml = reinterpret_cast<float2 *>(ws + pl.tc_part_off + (size_t)pl.tc_slots * 256 * d * 4);
+    }
+    int64_t tc_slot_cursor = 0, tc_counter_cursor = 0;
+    for (size_t c0 = 0; c0 < tcp.size(); c0 += kPlanMax) {
+        WorkList wl;
+        memset(&wl, 0, sizeof wl);
+        wl.mode = kModePrefill;
+        wl.tile_tokens = tc_prefill_rows() / g;
+        int items = 0;
+        size_t c1 = c0 + kPlanMax < tcp.size() ? c0 + kPlanMax : tcp.size();
+        for (size_t x = c0; x < c1; x++) {
+            int32_t r = tcp[x];
+            int32_t t = qsl_h[r + 1] - qsl_h[r];
+            int li = list_request(wl, r);
+            const int npairs = (t + 2 * wl.tile_tokens - 1) / (2 * wl.tile_tokens);   // pairs of 128-row tiles
+            const int whole = tc_split_whole(pl.tc_split[x]), pieces = tc_split_pieces(pl.tc_split[x]);
+            wl.tc_split[li] = pl.tc_split[x];
+            wl.item_off[li] = items;
+            wl.part_off[li] = (int32_t)tc_slot_cursor;
+            wl.cnt_off[li] = (int32_t)tc_counter_cursor;
+            if (pieces > 1) {
+                tc_slot_cursor += (int64_t)(npairs - whole) * hkv * pieces;
+                tc_counter_cursor += (int64_t)(npairs - whole) * hkv;
+                items += whole + (npairs - whole) * pieces;
+            } else {
+                items += npairs;
+            }
+        }
+        wl.item_off[wl.n] = items;
+        cudaError_t e = pl.mix ? launch_attn_tc(pt, wl, items, q, num_tokens, tc_k, tc_v, tc_slots, d, pstream, &p,
+                                                &mix_dl, &mix_as)
+                               : launch_attn_tc(pt, wl, items, q, num_tokens, tc_k, tc_v, tc_slots, d, pstream);
+        if (e != cudaSuccess) {
+            join();
+            return cuda_fail(e, "tensor-core prefill launch");
+        }
+    }
+
+    // ---- decode-class launches (chunks of kPlanMax requests; none in a mixed launch)
+    for (size_t c0 = 0; !pl.mix && c0 < dec.size(); c0 += kPlanMax) {
         WorkList wl;
         memset(&wl, 0, sizeof wl);
         wl.mode = kModeDecode;
@@ -1290,6 +1431,12 @@ pkv_status pkv_plan_attention(const int32_t *qsl_h, const int32_t *sl_h, int32_t
     out->decode_on_caller_stream = pl.fork && pl.decode_main;
     out->prefill_key_splits = pl.pre_split;
     out->prefill_tensor_pieces = (int32_t)pl.tc_slots;
+    out->mixed_launch = pl.mix;
+    out->mixed_decode_items = pl.mix ? pl.mix_items : 0;
+    if (pl.mix) {
+        out->decode_cluster = 0;
+        out->decode_streaming = 0;
+    }
     out->quantized_prefill_scratch = pl.rc.fp8_scratch;
     out->partial_bytes = pl.total_rows ? ((pl.total_rows * d * 4 + 15) / 16) * 16 + pl.total_rows * 8 : 0;
     return PKV_OK;

@@ -54,7 +54,7 @@ def test_forced_key_pieces(heads, pieces, window, attn_options):
         pkv.profile_start(32)
         dev.attend()
         names = {n for n, _ in pkv.profile_stop()}
-        assert "attn_tc_prefill" in names
+        assert names & {"attn_tc_prefill", "attn_tc_mixed"}
         assert_close(dev.out, want, f"pieces {pieces} d{d} window {window} call {call}")
         assert pkv.read_device_error(dev.ws) == 0
         assert int(dev.ws[COUNTERS].count_nonzero()) == 0
