@@ -202,9 +202,11 @@ def accounting(spec, meta, classes):
 
 
 KERNEL_CLASS = {"attn_mma_decode": ("decode", "padding"), "attn_mma_prefill": ("prefill_mma",),
-                "attn_tc_prefill": ("prefill_tensor",)}
+                "attn_tc_prefill": ("prefill_tensor",),
+                # one launch for a mixed batch: decode CTAs ahead of the tcgen05 prefill CTAs
+                "attn_tc_mixed": ("prefill_tensor", "decode", "padding")}
 KERNEL_BOUND = {"paged_kv_write": "hbm", "attn_mma_decode": "hbm", "attn_mma_prefill": "tensor",
-                "attn_tc_prefill": "tensor", "attn_split_combine": "hbm"}
+                "attn_tc_prefill": "tensor", "attn_tc_mixed": "tensor", "attn_split_combine": "hbm"}
 
 
 DECODE_CLASSES = ("decode", "padding")
@@ -235,14 +237,16 @@ def source_hash(name):
     """Hash of a kernel's source file and the shared device headers, to tell
     whether stored ncu counters are current."""
     fname = {"paged_kv_write": "kv_write.cu", "attn_split_combine": "attn_combine.cu", "attn_tc_prefill": "attn_tc.cu",
-             "attn_mma_decode": "attn_mma.cu", "attn_mma_prefill": "attn_mma.cu"}.get(name)
+             "attn_tc_mixed": "attn_tc.cu", "attn_mma_decode": "attn_mma.cu", "attn_mma_prefill": "attn_mma.cu"}.get(name)
     csrc = os.path.join(ROOT, "paged_kv_cache_84_gb300", "csrc")
     if not fname or not os.path.exists(os.path.join(csrc, fname)):
         return None
     h = hashlib.sha256()
-    for f in (fname, "common.cuh", "sm100.cuh"):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
+    for f in (fname, "common.cuh", "sm100.cuh", "mma_tiles.cuh", "decode_warp.cuh"):
+        path = os.path.join(csrc, f)
+        if os.path.exists(path):
+            with open(path, "rb") as fh:
+                h.update(fh.read())
     return h.hexdigest()[:12]
 
 

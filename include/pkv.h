@@ -251,8 +251,10 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q,
  *                       key tiles), merged by the CTA that finishes last
  *   mixed_launch        1: a batch's decode class runs inside the tcgen05
  *                       prefill launch whenever it can (one launch for both
- *                       classes); -1: never; 0: when the planner expects the
- *                       decode work to fit beside the prefill
+ *                       classes: decode CTAs ahead of the prefill CTAs); -1:
+ *                       never; 0: when the planner expects it to be faster
+ *   mixed_decode_ctas   > 0: that many decode CTAs in a mixed launch (rounded
+ *                       up to a multiple of the KV heads)
  */
 typedef struct pkv_attention_options {
     int32_t disable_tcgen05;
@@ -268,7 +270,8 @@ typedef struct pkv_attention_options {
     int32_t no_pdl;
     int32_t tc_key_pieces;
     int32_t mixed_launch;
-    int32_t reserved[3];
+    int32_t mixed_decode_ctas;
+    int32_t reserved[2];
 } pkv_attention_options;
 
 /* pkv_ragged_paged_attention with options (NULL: the planner's choices). */
@@ -532,6 +535,8 @@ typedef struct pkv_attention_plan {
     size_t partial_bytes;             /* workspace bytes of split partials */
     int32_t mixed_launch;             /* 1: decode items run inside the tcgen05 prefill launch (one launch) */
     int32_t mixed_decode_items;       /* ... how many */
+    int32_t mixed_decode_ctas;        /* ... on how many decode CTAs ahead of the prefill CTAs */
+    int32_t reserved;
 } pkv_attention_plan;
 pkv_status pkv_plan_attention(const int32_t *query_start_loc_host, const int32_t *seq_lens_host,
                               int32_t num_reqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,

@@ -45,7 +45,7 @@ class _Plan(ctypes.Structure):
                 ("split_counters", _c_i32), ("overlap", _c_i32), ("decode_on_caller_stream", _c_i32),
                 ("prefill_key_splits", _c_i32), ("prefill_tensor_pieces", _c_i32),
                 ("quantized_prefill_scratch", _c_sz), ("partial_bytes", _c_sz), ("mixed_launch", _c_i32),
-                ("mixed_decode_items", _c_i32)]
+                ("mixed_decode_items", _c_i32), ("mixed_decode_ctas", _c_i32), ("reserved", _c_i32)]
 
 
 class AttentionOptions(ctypes.Structure):
@@ -54,7 +54,8 @@ class AttentionOptions(ctypes.Structure):
     _fields_ = [("disable_tcgen05", _c_i32), ("tc_min_rows", _c_i32), ("fp8_prefill_on_mma", _c_i32),
                 ("split_tokens", _c_i32), ("cluster", _c_i32), ("decode_main", _c_i32), ("no_overlap", _c_i32),
                 ("prefill_key_splits", _c_i32), ("separate_write", _c_i32), ("decode_row_tiles", _c_i32),
-                ("no_pdl", _c_i32), ("tc_key_pieces", _c_i32), ("mixed_launch", _c_i32), ("reserved", _c_i32 * 3)]
+                ("no_pdl", _c_i32), ("tc_key_pieces", _c_i32), ("mixed_launch", _c_i32), ("mixed_decode_ctas", _c_i32),
+                ("reserved", _c_i32 * 2)]
 
 
 # The options the attention wrappers pass to the library's _ex calls (None:
@@ -275,7 +276,7 @@ def plan_attention(query_start_loc_host, seq_lens_host, num_q_heads, num_kv_head
                                      num_kv_heads, head_dim, block_size, window, int(bool(quantized)),
                                      int(bool(combined)), workspace_bytes, num_sms, _opts(), ctypes.byref(out)),
            "plan_attention")
-    return {name: int(getattr(out, name)) for name, _ in _Plan._fields_}
+    return {name: int(getattr(out, name)) for name, _ in _Plan._fields_ if name != "reserved"}
 
 
 def launch_count() -> int:

@@ -72,12 +72,14 @@ struct TcCfg {
     static constexpr int kBarOff = kVOff + 2 * kTile;
     static constexpr int kXOff = kBarOff + 256;        // softmax pair exchange: max [2][2][128], sum [2][128]
     static constexpr int kSmem = 1024 + kXOff + 3 * 1024;
-    // mixed batches: warp 3's decode ring (kDecStages stages of a K and a V
-    // slice) after the exchange area; its barriers at kBarOff + 128
-    static constexpr int kDecStages = DP == 128 ? 3 : 6;
-    static constexpr int kDecOff = (kXOff + 3 * 1024 + 1023) / 1024 * 1024;
-    static constexpr int kSmemMix = 1024 + kDecOff + kDecStages * WarpRing<DP>::kStage;
-    static_assert(kSmemMix <= 227 * 1024, "the decode ring must fit beside the prefill tiles");
+    // mixed batches, decode CTAs: a ring of kDecStages stages (a K and a V
+    // slice each) per warp, then their barriers
+    static constexpr int kDecStages = DP == 128 ? 2 : 4;
+    static constexpr int kDecRing = kDecStages * WarpRing<DP>::kStage;
+    static constexpr int kDecBarOff = (kTcThreads / 32) * kDecRing;
+    static constexpr int kSmemDec = 1024 + kDecBarOff + (kTcThreads / 32) * kDecStages * 8;
+    static constexpr int kSmemMix = kSmem > kSmemDec ? kSmem : kSmemDec;
+    static_assert(kSmemMix <= 227 * 1024, "the decode rings must fit a CTA's shared memory");
 };
 
 constexpr uint32_t kTmemCols = 512;
@@ -373,15 +375,63 @@ __device__ __forceinline__ void tc_piece_epilogue(const AttnParams &p, uint32_t 
     }
 }
 
+// A decode CTA of a mixed launch: each of its 12 warps runs decode items of
+// list dl (parameters pd) over its own ring, items dealt round-robin over
+// all warps of all decode CTAs (cta: this CTA's index among them).  The
+// warps are independent: nothing is shared but the CTA's shared memory,
+// split into one ring per warp; a warp leaves once its items are done, with
+// no copy in flight.
+template <int DP, int D>
+__device__ __forceinline__ void tc_decode_cta(const AttnParams &pd, const WorkList &dl, int cta, int ctas,
+                                              const CUtensorMap &kmap, const CUtensorMap &vmap, int64_t num_slots)
+{
+    using C = TcCfg<DP>;
+    constexpr int NS = C::kDecStages;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sb = (raw + 1023u) & ~1023u;
+    uint8_t *sp = smem_raw + (sb - raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int kWarps = kTcThreads / 32;
+    WarpPipe wp;
+    wp.ring = sb + warp * C::kDecRing;
+    wp.bars = sb + C::kDecBarOff + warp * NS * 8;
+    wp.stage_f = reinterpret_cast<float *>(sp + warp * C::kDecRing);
+    wp.seq = 0;
+    if (lane == 0) {
+        prefetch_tmap(&kmap);
+        prefetch_tmap(&vmap);
+        for (int s = 0; s < NS; s++) mbar_init(wp.bars + 8u * s, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    pdl_wait();                                                    // the step's earlier kernels are done
+    const int items = dl.item_off[dl.n];
+    for (int it = cta * kWarps + warp; it < items; it += ctas * kWarps) {
+        warp_decode_item<DP, D, NS>(pd, dl, it, wp, &kmap, &vmap, num_slots);
+        __syncwarp();
+        // the epilogue's reads of the ring precede the next item's copies into it
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+}
+
 // DP: head dim padded to the 64-column sub-tile; D: head dim of q and out;
-// WIN: a sliding window is set (p.window > 0).  MIX: a mixed batch, whose
-// decode-class items (list dl, parameters pd, per-row assignment mix) warp 3
-// runs beside the prefill.
+// WIN: a sliding window is set (p.window > 0).  MIX: a mixed batch: the first
+// mix->dec_rows grid rows are decode CTAs (list dl, parameters pd), the
+// tcgen05 prefill CTAs follow.
 template <int DP, int D, bool WIN, bool MIX>
 __device__ __forceinline__ void attn_tc_body(const AttnParams &p, const WorkList &wl, const CUtensorMap &qmap,
                                              const CUtensorMap &kmap, const CUtensorMap &vmap, int64_t num_slots,
                                              const AttnParams *pd, const WorkList *dl, const MixAssign *mix)
 {
+    if constexpr (MIX) {
+        if ((int)blockIdx.y < mix->dec_rows) {
+            tc_decode_cta<DP, D>(*pd, *dl, blockIdx.y * gridDim.x + blockIdx.x, mix->dec_rows * gridDim.x, kmap, vmap,
+                                 num_slots);
+            return;
+        }
+    }
+    const int row = MIX ? (int)blockIdx.y - mix->dec_rows : (int)blockIdx.y;   // this CTA's prefill row
     using C = TcCfg<DP>;
     constexpr int kTile = C::kTile, kQOff = C::kQOff, kKOff = C::kKOff, kVOff = C::kVOff, kBarOff = C::kBarOff;
     constexpr int kHalves = C::kHalves;
@@ -394,14 +444,14 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams &p, const WorkList
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kh = blockIdx.x;                                     // all KV heads of an item are adjacent
-    const int li = find_listed(wl, blockIdx.y);
+    const int li = find_listed(wl, row);
     const int r = wl.req[li];
     const int b = wl.qb[li], t = wl.qt[li], L = wl.len[li];
     const int g = p.group;
     const int tt = wl.tile_tokens;                                 // tokens per tile: 128 / g
     const int npairs = (t + 2 * tt - 1) / (2 * tt);
     // longest pairs first: `whole` pairs as one CTA, then `pieces` CTAs per pair
-    const int local = blockIdx.y - wl.item_off[li];
+    const int local = row - wl.item_off[li];
     const int whole = tc_split_whole(wl.tc_split[li]), small = tc_split_small(wl.tc_split[li]);
     int pair = npairs - 1 - local, piece = 0, pieces = 1;
     if (local >= whole) {                                          // piece-major over the split pairs
@@ -517,7 +567,7 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams &p, const WorkList
             for (int j = issued > 2 ? issued - 2 : 0; j < issued; j++)
                 mbar_wait(bar(full0 + (j & 1)), (j >> 1) & 1, p.err);
         }
-        if (!is_k && lane == 0 && kh == 0 && blockIdx.y == wl.item_off[li]) check_meta(p, wl, li);
+        if (!is_k && lane == 0 && kh == 0 && row == wl.item_off[li]) check_meta(p, wl, li);
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -614,31 +664,6 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams &p, const WorkList
             mbar_wait(bar(kBarMmaDone), 0, p.err);
         }
         __syncwarp();
-    } else if (MIX && warp == 3) {
-        // ------------------------------------------------------------ decode items (mixed batches)
-        const int y = blockIdx.y;
-        const int n = mix->first[y + 1] - mix->first[y];
-        const int a0 = mix->first[y] + n * kh / p.hkv, a1 = mix->first[y] + n * (kh + 1) / p.hkv;
-        if (a0 < a1) {
-            constexpr int NS = C::kDecStages;
-            WarpPipe wp;
-            wp.ring = sb + C::kDecOff;
-            wp.bars = sb + kBarOff + 128;
-            wp.stage_f = reinterpret_cast<float *>(sp + C::kDecOff);
-            wp.seq = 0;
-            if (lane == 0) {
-                for (int s = 0; s < NS; s++) mbar_init(wp.bars + 8u * s, 1);
-                fence_mbar_init();
-            }
-            __syncwarp();
-            pdl_wait();                                            // the step's earlier kernels are done
-            for (int it = a0; it < a1; it++) {
-                warp_decode_item<DP, D, NS>(*pd, *dl, it, wp, &kmap, &vmap, num_slots);
-                __syncwarp();
-                // the epilogue's reads of the ring precede the next item's copies into it
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            }
-        }
     } else if (warp >= 4 && has_b) {
         // ------------------------------------------------------------ softmax, one row per thread
         const int x = warp >= 8 ? 1 : 0;                           // tile a or b
@@ -830,8 +855,9 @@ static cudaError_t launch_tc_d(const AttnParams &p, const WorkList &wl, int num_
     if (e == cudaSuccess) e = make_pool_tmap(&km, k_cache, num_slots, p.hkv, D, 64, true);
     if (e == cudaSuccess) e = make_pool_tmap(&vm, v_cache, num_slots, p.hkv, D, 64, true);
     if (e != cudaSuccess) return e;
-    if (num_items > 65535) return cudaErrorInvalidConfiguration;
-    dim3 grid(p.hkv, num_items);                   // items in launch order: the planner puts the longest first
+    const int rows = num_items + (mix ? mix->dec_rows : 0);
+    if (rows > 65535) return cudaErrorInvalidConfiguration;
+    dim3 grid(p.hkv, rows);                        // items in launch order: the planner puts the longest first
     launch_begin(stream, mix ? kAttnTcMixed : kAttnTcPrefill);
     if (mix)
         e = launch_maybe_pdl(attn_tc_mix_kernel<DP, D, WIN>, grid, dim3(kTcThreads), smem_mix, stream, p, wl, qm, km,
@@ -848,7 +874,7 @@ cudaError_t launch_attn_tc(const AttnParams &p, const WorkList &wl, int num_item
                            cudaStream_t stream, const AttnParams *pd, const WorkList *dl, const MixAssign *mix)
 {
     if (num_items <= 0) return cudaSuccess;
-    if (mix && (!pd || !dl || mix->rows != num_items)) return cudaErrorInvalidValue;
+    if (mix && (!pd || !dl || mix->dec_rows <= 0)) return cudaErrorInvalidValue;
     const bool win = p.window > 0;
 #define PKV_TC_ARGS p, wl, num_items, q, num_tokens, k_cache, v_cache, num_slots, stream, pd, dl, mix
     switch (head_dim) {

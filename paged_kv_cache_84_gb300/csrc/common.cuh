@@ -339,18 +339,16 @@ cudaError_t launch_attn_mma(const AttnParams &p, const WorkList &wl, int head_di
                             const float *k_scale = nullptr, const float *v_scale = nullptr);
 int mma_prefill_rows();
 
-// Decode items of a mixed launch per grid row: the tcgen05 CTAs of row y
-// (one per KV head) run decode items first[y] .. first[y + 1] - 1 on their
-// warp 3, divided evenly among them.
-constexpr int kMixMaxRows = 1023;
+// A mixed launch: its first dec_rows grid rows (dec_rows x hkv CTAs) are
+// decode CTAs, every warp of which runs decode items; the tcgen05 prefill
+// CTAs follow them.
 struct MixAssign {
-    int32_t rows;
-    int32_t first[kMixMaxRows + 1];
+    int32_t dec_rows;
 };
 
 // tcgen05 prefill tiles of 128 query rows (head_dim 48, 64 or 128, g dividing 128).
-// With mix (and pd, dl): the mixed-batch kernel, whose warp 3 also runs the
-// decode items of list dl with parameters pd.
+// With mix (and pd, dl): the mixed-batch kernel, whose leading decode CTAs
+// run the decode items of list dl with parameters pd.
 bool tc_prefill_supported(int head_dim, int group);
 int tc_prefill_rows();
 cudaError_t launch_attn_tc(const AttnParams &p, const WorkList &wl, int num_items, const void *q, int num_tokens,
@@ -414,6 +412,7 @@ struct CallOptions {
     bool no_pdl = false;              // no programmatic dependent launches
     int tc_key_pieces = 0;            // 0: planner; -1: no key pieces; k >= 2: every tcgen05 pair in k pieces
     int mixed_launch = 0;             // 0: planner; 1: decode class in the tcgen05 launch when it can; -1: never
+    int mixed_decode_ctas = 0;        // > 0: decode CTAs of a mixed launch (rounded up to the KV heads)
 };
 
 // Launch-level choices of the attention call in progress on this thread,

@@ -96,6 +96,7 @@ static CallOptions call_options(const pkv_attention_options *o)
     c.no_pdl = o->no_pdl != 0;
     c.tc_key_pieces = o->tc_key_pieces < 0 ? -1 : (o->tc_key_pieces >= 2 ? o->tc_key_pieces : 0);
     c.mixed_launch = o->mixed_launch > 0 ? 1 : (o->mixed_launch < 0 ? -1 : 0);
+    c.mixed_decode_ctas = o->mixed_decode_ctas > 0 ? o->mixed_decode_ctas : 0;
     return c;
 }
 
@@ -597,7 +598,7 @@ struct AttnPlan {
     // mixed launch: the decode class inside the tcgen05 launch (warp 3 of its CTAs)
     bool mix = false;
     int32_t mix_items = 0;              // decode items (request, split, KV head)
-    std::vector<int32_t> mix_first;     // per tcgen05 grid row: its first decode item (+ the end)
+    int32_t mix_dec_rows = 0;           // grid rows of decode CTAs ahead of the prefill (x hkv CTAs)
 };
 
 // ---- tcgen05 prefill: key pieces
@@ -625,10 +626,13 @@ static int tc_pair_tiles(int t, int L, int tt, int window, int pair)
 constexpr double kTcCtaCost = 3.5;
 constexpr double kTcPieceCost = 1.0;
 
-// Greedy list schedule of CTA costs on `sms` SMs: the time the last one ends.
-static double greedy_makespan(const std::vector<double> &costs, int sms)
+// Greedy list schedule of CTA costs on `sms` SMs, `busy` of which are taken
+// until `busy_until` (the decode CTAs of a mixed launch): the time the last
+// CTA ends.
+static double greedy_makespan(const std::vector<double> &costs, int sms, int busy = 0, double busy_until = 0.0)
 {
     std::vector<double> heap(std::max(1, sms), 0.0);
+    for (int i = 0; i < busy && i < (int)heap.size(); i++) heap[i] = busy_until;
     std::make_heap(heap.begin(), heap.end(), std::greater<double>());
     for (double c : costs) {
         std::pop_heap(heap.begin(), heap.end(), std::greater<double>());
@@ -640,7 +644,7 @@ static double greedy_makespan(const std::vector<double> &costs, int sms)
 
 static void plan_tc_pieces(AttnPlan &pl, const int32_t *qsl_h, const int32_t *sl_h, int32_t g, int32_t hkv,
                            int32_t d, int32_t window, int sms, size_t room, int64_t counters_free,
-                           const CallOptions &o)
+                           const CallOptions &o, int busy = 0, double busy_until = 0.0)
 {
     const std::vector<int32_t> &tcp = pl.rc.tcp;
     const int tt = tc_prefill_rows() / g;
@@ -702,7 +706,7 @@ static void plan_tc_pieces(AttnPlan &pl, const int32_t *qsl_h, const int32_t *sl
             }
             placed += (int64_t)(pieces > 1 ? whole + ((int)c.size() - whole) * pieces : (int)c.size()) * hkv;
         }
-        return greedy_makespan(costs, sms);
+        return greedy_makespan(costs, sms, busy, busy_until);
     };
     std::vector<int32_t> best(pl.tc_split), cur(tcp.size());
     int64_t best_groups = 0, best_slots = 0, groups = 0, slots = 0;
@@ -778,19 +782,28 @@ static size_t plan_partial_rows(const AttnPlan &pl, const int32_t *qsl_h, const 
 // ---- mixed launch: the decode class inside the tcgen05 launch
 //
 // For a batch of prefill chunks on tcgen05 and decodes (one flattened
-// ragged batch, "31. Engine v2", "Flattened ragged batches"), warp 3 of
-// every tcgen05 CTA runs decode items (request, KV head, key split) with
-// its own ring of KV stages, while the other warps run the prefill tiles:
-// one launch for both classes.  The prefill is bound by the tensor pipe, the
-// decodes by HBM, so they share the SMs.  Each grid row gets decode items in
-// proportion to its prefill cost; the planner takes this arrangement when
-// the decode work fits in kMixFill of the prefill's time at kMixWarpGBs per
-// warp, the rate measured on the mixed 2048-token-chunk step (one 1024-key
-// item of head dim 128, 512 KB of K and V, in ~60 us beside the prefill).
+// ragged batch, "31. Engine v2", "Flattened ragged batches"), the tcgen05
+// launch opens with a few decode CTAs: every one of their 12 warps runs
+// decode items (request, KV head, key split) over its own ring of KV
+// stages.  They hold their SMs only until the decode work is done, and the
+// prefill CTAs, which follow them in launch order, take every other SM and
+// then those: one launch for both classes, the HBM-bound decodes beside the
+// tensor-bound prefill.  The planner sizes the decode CTAs by simulating the
+// prefill schedule with their SMs busy until the decodes end and takes the
+// arrangement when the predicted time beats the two-stream one's estimate.
+// The decode CTAs' time is the larger of the bytes at kMixCtaGBs per CTA and
+// the items of the busiest warp one after another (kMixItemUs + bytes at
+// kMixWarpGBs each).  Measured on the mixed 2048-token-chunk step (0.67 GB
+// of decode K/V in 1568 items of 1024 keys): 8 decode CTAs took 885 us
+// (~95 GB/s each), 16 and 32 470 us against 520 us on two streams; on the
+// 48-request engine step (128 short items) one item per warp took ~25 us,
+// against 11 us for the whole step on two streams.
 constexpr int kMixDecodeRows = 8;         // decode items: key-major tiles, t * g <= 8 rows per KV head
 constexpr int kMixSplit = 1024;           // keys per decode item
-constexpr double kMixWarpGBs = 8.5;       // one warp's decode rate beside the prefill, GB/s
-constexpr double kMixFill = 0.8;
+constexpr int kMixDecodeWarps = 12;       // warps of a decode CTA (the tcgen05 CTA's 384 threads)
+constexpr double kMixCtaGBs = 95.0;       // a decode CTA's rate, GB/s
+constexpr double kMixWarpGBs = 10.0;      // one warp's rate over an item's blocks, GB/s
+constexpr double kMixItemUs = 8.0;        // an item's start (its q, the first copies) and end
 constexpr double kTcTileUs = 1.66;        // a key tile of a pair on tcgen05, measured on the mixed step
 
 static AttnPlan make_plan(const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs, int32_t hq, int32_t hkv,
@@ -856,46 +869,61 @@ static AttnPlan make_plan(const int32_t *qsl_h, const int32_t *sl_h, int32_t num
     if (mix_ok) {
         AttnPlan m = pl;
         layout(m, o.split_tokens > 0 ? o.split_tokens : kMixSplit, true);
-        int64_t items = 0, counters = m.tc_groups;
+        int64_t items = 0, counters = 0;
         double dec_bytes = 0.0;
-        std::vector<double> item_cost;
         for (int32_t r : rc.dec) {
             const int32_t t = qsl_h[r + 1] - qsl_h[r], L = sl_h[r];
             const int S = decode_splits(t, L, window, m.split);
-            const int k0 = decode_key_begin(t, L, window);
-            for (int sp = 0; sp < S; sp++) {
-                const int keys = L <= 0 ? 0 : std::min(L, k0 + (sp + 1) * m.split) - (k0 + sp * m.split);
-                for (int h = 0; h < hkv; h++) item_cost.push_back(keys + 16.0);
-                dec_bytes += (double)keys * hkv * d * 4.0;
-            }
+            dec_bytes += (double)std::max(0, L - decode_key_begin(t, L, window)) * hkv * d * 4.0;
             items += (int64_t)S * hkv;
             if (S > 1) counters += hkv;
         }
-        const std::vector<double> rows = tc_row_costs(m, qsl_h, sl_h, g, window);
-        double pre_cost = 0.0;
-        for (double c : rows) pre_cost += c;
-        // SM time of the prefill CTAs vs that of the decode items on warp 3
-        const double pre_sm_us = pre_cost * hkv * kTcTileUs;
-        const double dec_sm_us = dec_bytes / (kMixWarpGBs * 1e3);
-        const bool fits = dec_sm_us <= kMixFill * pre_sm_us;
-        if ((fits || o.mixed_launch > 0) && counters <= kCounterGroups && rows.size() <= (size_t)kMixMaxRows &&
-            items < INT32_MAX) {
-            m.mix = true;
-            m.mix_items = (int32_t)items;
-            // rows get items in proportion to their cost, in launch order
-            double total_dec = 0.0;
-            for (double c : item_cost) total_dec += c;
-            m.mix_first.assign(rows.size() + 1, 0);
-            double cum_pre = 0.0, cum_dec = 0.0;
-            size_t it = 0;
-            for (size_t y = 0; y < rows.size(); y++) {
-                m.mix_first[y] = (int32_t)it;
-                cum_pre += rows[y];
-                const double target = cum_pre / pre_cost * total_dec;
-                while (it < item_cost.size() && cum_dec + 0.5 * item_cost[it] <= target) cum_dec += item_cost[it++];
+        // decode CTAs: the count with the shortest simulated step (forced:
+        // the option's count), the prefill pieces planned around them
+        const size_t dec_part = m.total_rows ? ((m.total_rows * d * 4 + 15) / 16) * 16 + m.total_rows * 8 : 0;
+        const size_t tc_room = m.ws_front > m.tc_part_off + 64 ? m.ws_front - m.tc_part_off - 64 : 0;
+        (void)dec_part;
+        double best = 1e30;
+        int best_rows = 0;
+        AttnPlan best_plan = m;
+        for (int rows = 1; rows * hkv <= sms / 2; rows *= 2) {
+            if (o.mixed_decode_ctas > 0 && rows != std::max(1, (o.mixed_decode_ctas + hkv - 1) / hkv)) continue;
+            const int n = rows * hkv;
+            const double per_warp = std::ceil((double)items / (n * kMixDecodeWarps));
+            const double dec_us = std::max(dec_bytes / (n * kMixCtaGBs * 1e3),
+                                           per_warp * (kMixItemUs + dec_bytes / items / (kMixWarpGBs * 1e3))) +
+                                  5.0;
+            AttnPlan q = m;
+            plan_tc_pieces(q, qsl_h, sl_h, g, hkv, d, window, sms, tc_room,
+                           q.has_counters ? kCounterGroups / 2 - counters : 0, o, n, dec_us / kTcTileUs);
+            const double step = std::max(dec_us, q.tc_makespan * kTcTileUs);
+            if (step < best) {
+                best = step;
+                best_rows = rows;
+                best_plan = q;
             }
-            m.mix_first[rows.size()] = (int32_t)items;
-            return m;
+        }
+        if (o.mixed_decode_ctas > 0 && best_rows == 0) {                 // more than half the SMs: as asked
+            const int rows = (o.mixed_decode_ctas + hkv - 1) / hkv;
+            best_plan = m;
+            plan_tc_pieces(best_plan, qsl_h, sl_h, g, hkv, d, window, sms, tc_room,
+                           best_plan.has_counters ? kCounterGroups / 2 - counters : 0, o, rows * hkv,
+                           dec_bytes / (rows * hkv * kMixCtaGBs * 1e3) / kTcTileUs);
+            best_rows = rows;
+            best = 0.0;
+        }
+        // the two-stream arrangement, roughly: the prefill alone (whole
+        // pairs) and the decodes at full HBM speed in what it leaves idle
+        AttnPlan w = pl;
+        layout(w, decode_split_tokens(rc, w.dec_us, w.pre_us, hkv, fp8, o, sms), false);
+        const double two_stream = w.tc_makespan * kTcTileUs + 0.5 * dec_bytes / 6.5e6;
+        counters += best_plan.tc_groups;
+        if (best_rows > 0 && (best < two_stream || o.mixed_launch > 0) && counters <= kCounterGroups &&
+            items < INT32_MAX) {
+            best_plan.mix = true;
+            best_plan.mix_items = (int32_t)items;
+            best_plan.mix_dec_rows = best_rows;
+            return best_plan;
         }
     }
 
@@ -1205,8 +1233,7 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
             items += S * hkv;
         }
         mix_dl.item_off[mix_dl.n] = items;
-        mix_as.rows = (int32_t)pl.mix_first.size() - 1;
-        for (size_t y = 0; y < pl.mix_first.size(); y++) mix_as.first[y] = pl.mix_first[y];
+        mix_as.dec_rows = pl.mix_dec_rows;
         if (counter_cursor > kCounterGroups || items != pl.mix_items) return PKV_ERR_UNSUPPORTED;
     }
 
@@ -1433,6 +1460,7 @@ pkv_status pkv_plan_attention(const int32_t *qsl_h, const int32_t *sl_h, int32_t
     out->prefill_tensor_pieces = (int32_t)pl.tc_slots;
     out->mixed_launch = pl.mix;
     out->mixed_decode_items = pl.mix ? pl.mix_items : 0;
+    out->mixed_decode_ctas = pl.mix ? pl.mix_dec_rows * hkv : 0;
     if (pl.mix) {
         out->decode_cluster = 0;
         out->decode_streaming = 0;

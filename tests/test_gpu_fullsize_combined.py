@@ -17,9 +17,10 @@ way, on the three large workloads at their full sizes:
 
 In these batches the combined call splits the work in ways the small tests
 do not reach: ten streaming splits of 3456 keys per 32768-key decode, merged
-by the CTA that finishes last; 64 decodes that write their own rows beside a
-2048-token chunk on tcgen05 whose rows a ranged scatter writes, the decodes
-forking onto the side stream after that scatter.
+by the CTA that finishes last; 64 decodes that write their own rows, as
+1024-key items on the decode CTAs that open the one launch of the mixed step,
+ahead of the 2048-token chunk's tcgen05 pairs whose rows a ranged scatter
+writes.
 """
 import concurrent.futures as cf
 
@@ -93,8 +94,8 @@ def test_combined_call_full_size(cfg):
                               spec.head_dim, combined=True, workspace_bytes=dev.ws.numel())
     if cfg == 5:
         assert plan["max_decode_splits"] >= 8 and plan["decode_streaming"]
-    if cfg == 4:                                        # decodes on a side stream beside the tcgen05 pairs
-        assert plan["overlap"] and plan["prefill_tensor_requests"] == 3
+    if cfg == 4:                                        # one launch: decode CTAs ahead of the tcgen05 pairs
+        assert plan["mixed_launch"] and plan["mixed_decode_ctas"] > 0 and plan["prefill_tensor_requests"] == 3
     _replay_in_graph(dev.combined)
     assert torch.isfinite(dev.out.float()).all()
     oracle_write(ref)

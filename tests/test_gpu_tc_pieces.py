@@ -93,9 +93,9 @@ def _plan(spec, **kw):
 
 def test_planner_cuts_heavy_pairs_only_without_decodes_beside():
     """The planner's own choice: the 2048-token chunk at 16384 alone (256
-    heavy CTAs on 152 SMs) has its second-wave pairs cut; beside the mixed
-    step's 64 decodes (which fill the idle SMs) and in the engine step's
-    short chunks nothing is cut."""
+    heavy CTAs on 152 SMs) has its second-wave pairs cut; with the mixed
+    step's 64 decodes (on the decode CTAs that open its launch) and in the
+    engine step's short chunks nothing is cut."""
     assert _plan(subset_spec(config_spec(4), 1))["prefill_tensor_pieces"] > 0
     assert _plan(config_spec(4))["prefill_tensor_pieces"] == 0
     assert _plan(config_spec(2))["prefill_tensor_pieces"] == 0

@@ -41,11 +41,14 @@ def meta(cfg):
     return spec, qsl, [r.seq_len for r in spec.reqs]
 
 
-def plan(cfg, **kw):
+def plan(cfg, mixed=-1, **kw):
+    """The plan for workload cfg; by default with the single mixed launch
+    ruled out, so that the two-stream rules below are what is checked."""
     spec, qsl, sl = meta(cfg)
     kw.setdefault("num_sms", SMS)
     kw.setdefault("workspace_bytes", BIG_WS)
-    return pkv.plan_attention(qsl, sl, spec.num_q_heads, spec.num_kv_heads, spec.head_dim, **kw)
+    with pkv.options(mixed_launch=mixed):
+        return pkv.plan_attention(qsl, sl, spec.num_q_heads, spec.num_kv_heads, spec.head_dim, **kw)
 
 
 def rule_split(keys, head_ctas, ctas_per_sm, sms=SMS, max_keys=0):
@@ -221,3 +224,24 @@ def test_rejections(args, status):
         pkv.plan_attention(qsl, sl, kw.pop("num_q_heads"), kw.pop("num_kv_heads"), kw.pop("head_dim"),
                            num_sms=SMS, **kw)
     assert e.value.status == status
+
+
+def test_mixed_launch_choice():
+    """The planner's choice of one launch for both classes (decode CTAs ahead
+    of the tcgen05 prefill CTAs): taken for the mixed 2048-token-chunk step,
+    whose decodes are long (items of 1024 keys dealt to the decode CTAs'
+    warps), not for the engine step's short decodes (one latency-bound item
+    per warp would outlast the whole two-stream step) nor where there is no
+    tcgen05 prefill."""
+    p = plan(4, mixed=0, combined=True)
+    spec, qsl, sl = meta(4)
+    dec = [L for L, a, b in zip(sl, qsl, qsl[1:]) if b - a == 1]
+    assert p["mixed_launch"] == 1 and not p["overlap"]
+    assert p["decode_split_tokens"] == 1024
+    assert p["mixed_decode_items"] == sum(-(-L // 1024) for L in dec) * spec.num_kv_heads
+    assert 8 <= p["mixed_decode_ctas"] <= SMS // 2 and p["mixed_decode_ctas"] % spec.num_kv_heads == 0
+    for cfg in (1, 2, 3, 5):
+        assert plan(cfg, mixed=0, combined=True)["mixed_launch"] == 0, cfg
+    with pkv.options(mixed_decode_ctas=40):
+        q = plan(4, mixed=1, combined=True)
+    assert q["mixed_launch"] == 1 and q["mixed_decode_ctas"] == 40
