@@ -89,6 +89,31 @@ def test_reference_arm_under_torchrun_two_ranks():
     assert line["config"]["workload"] == "layout-example-N9"
 
 
+def test_gpus_two_without_torchrun_relaunches_as_two_ranks():
+    """bench.py --gpus 2 started as one plain process re-runs itself under
+    torch.distributed.run with two ranks: one JSON line, n_gpus 2."""
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--gpus", "2", "--steps", "2", "--warmup", "0",
+           "--workload", "1"]
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    env["OMP_NUM_THREADS"] = "1"
+    res = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300, env=env)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [ln for ln in res.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+
+
+def test_gpus_flag_must_match_the_launched_ranks():
+    """A WORLD_SIZE that disagrees with --gpus is refused before any work."""
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "0",
+           "--workload", "1"]
+    env = dict(os.environ, WORLD_SIZE="3", RANK="0", OMP_NUM_THREADS="1")
+    res = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=120, env=env)
+    assert res.returncode == 2
+    assert "WORLD_SIZE=3" in res.stderr and not res.stdout.strip()
+
+
 def test_reference_arm_line_carries_the_contract_keys():
     """One process: the reference arm's JSON line has every key of the
     benchmark contract, its e2e moves no bytes, and its value is tokens over
