@@ -772,6 +772,34 @@ def fp8_workload(pkv, cfg, device, peaks, steps=20, subset=0):
     e1.record(stream)
     torch.cuda.synchronize()
     step_s = e0.elapsed_time(e1) / steps / 1e3
+    # per-kernel durations: event nodes around every launch of a second graph
+    # of the same steps (as in time_workload)
+    kernels = None
+    try:
+        before = pkv.launch_count()
+        step()
+        torch.cuda.synchronize()
+        per_step = pkv.launch_count() - before
+        pkv.profile_start(steps * per_step + 16)
+        gp = torch.cuda.CUDAGraph()
+        try:
+            with torch.cuda.graph(gp, stream=side):
+                for _ in range(steps):
+                    step()
+        finally:
+            n_rec = pkv.profile_stop(read=False)
+        torch.cuda.synchronize()
+        gp.replay()
+        torch.cuda.synchronize()
+        kern = {}
+        for name, ms in pkv.profile_records(n_rec):
+            k = kern.setdefault(name, [0, 0.0])
+            k[0] += 1
+            k[1] += ms
+        kernels = {name: {"launches_per_step": c / steps, "avg_launch_us": 1e3 * t / c} for name, (c, t) in kern.items()}
+        del gp
+    except Exception:                                   # noqa: BLE001 - a diagnostic only
+        torch.cuda.synchronize()
     # algorithmic bytes: every unique slot read once (codes of K and V + their scales), q, out, the write
     used = set()
     for r in range(m.num_reqs):
@@ -788,7 +816,7 @@ def fp8_workload(pkv, cfg, device, peaks, steps=20, subset=0):
            "step_hbm_frac": (kv_bytes + other) / step_s / 1e9 / peaks["hbm_gbs"],
            "step_tensor_frac": flops / step_s / 1e12 / peaks["bf16_tflops"],
            "prefill_scratch_bytes": extra,
-           "pool": "E4M3 codes + fp32 scale per (slot, head)"}
+           "pool": "E4M3 codes + fp32 scale per (slot, head)", "kernels": kernels}
     del kc, vc, ks, vs, q, k, v, out, ws, g
     torch.cuda.empty_cache()
     return res

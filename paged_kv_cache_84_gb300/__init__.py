@@ -45,7 +45,8 @@ class _Plan(ctypes.Structure):
                 ("split_counters", _c_i32), ("overlap", _c_i32), ("decode_on_caller_stream", _c_i32),
                 ("prefill_key_splits", _c_i32), ("prefill_tensor_pieces", _c_i32),
                 ("quantized_prefill_scratch", _c_sz), ("partial_bytes", _c_sz), ("mixed_launch", _c_i32),
-                ("mixed_decode_items", _c_i32), ("mixed_decode_ctas", _c_i32), ("reserved", _c_i32)]
+                ("mixed_decode_items", _c_i32), ("mixed_decode_ctas", _c_i32),
+                ("mixed_predicted_us", _c_i32)]
 
 
 class AttentionOptions(ctypes.Structure):

@@ -1157,6 +1157,13 @@ cudaError_t make_pool_tmap(CUtensorMap *map, const void *pool, int64_t num_slots
     return make_pool_tmap_e(map, pool, num_slots, hkv, d, box_cols, swizzle128, 2);
 }
 
+// Tensor map of an FP8 pool's codes [slots][Hkv][128] with a box of one
+// head's 128-byte code row x 16 slots, 128-byte swizzle.
+cudaError_t make_code_tmap(CUtensorMap *map, const void *pool, int64_t num_slots, int hkv)
+{
+    return make_pool_tmap_e(map, pool, num_slots, hkv, 128, 128, true, 1);
+}
+
 // Tensor map of an FP8 pool's scales [slots][Hkv] fp32 with a box of 16
 // slots x kScaleHeads heads (16-byte rows; Hkv a multiple of kScaleHeads).
 static cudaError_t make_scale_tmap(CUtensorMap *map, const float *scales, int64_t num_slots, int hkv)

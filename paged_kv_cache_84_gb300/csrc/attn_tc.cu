@@ -80,6 +80,15 @@ struct TcCfg {
     static constexpr int kSmemDec = 1024 + kDecBarOff + (kTcThreads / 32) * kDecStages * 8;
     static constexpr int kSmemMix = kSmem > kSmemDec ? kSmem : kSmemDec;
     static_assert(kSmemMix <= 227 * 1024, "the decode rings must fit a CTA's shared memory");
+    // ... over a quantized pool (head dim 128): rings of E4M3 codes, then
+    // every warp's scale array, then the barriers
+    static constexpr int kDecStagesF8 = 4;
+    static constexpr int kDecRingF8 = kDecStagesF8 * WarpRingF8::kStage;
+    static constexpr int kDecScaleOffF8 = (kTcThreads / 32) * kDecRingF8;
+    static constexpr int kDecBarOffF8 = kDecScaleOffF8 + (kTcThreads / 32) * kDecStagesF8 * WarpRingF8::kScaleStage;
+    static constexpr int kSmemDecF8 = 1024 + kDecBarOffF8 + (kTcThreads / 32) * kDecStagesF8 * 8;
+    static constexpr int kSmemMixF8 = kSmem > kSmemDecF8 ? kSmem : kSmemDecF8;
+    static_assert(kSmemMixF8 <= 227 * 1024, "the decode rings must fit a CTA's shared memory");
 };
 
 constexpr uint32_t kTmemCols = 512;
@@ -380,13 +389,15 @@ __device__ __forceinline__ void tc_piece_epilogue(const AttnParams &p, uint32_t 
 // all warps of all decode CTAs (cta: this CTA's index among them).  The
 // warps are independent: nothing is shared but the CTA's shared memory,
 // split into one ring per warp; a warp leaves once its items are done, with
-// no copy in flight.
-template <int DP, int D>
+// no copy in flight.  FP8: the pool holds E4M3 codes and scales.
+template <int DP, int D, bool FP8>
 __device__ __forceinline__ void tc_decode_cta(const AttnParams &pd, const WorkList &dl, int cta, int ctas,
-                                              const CUtensorMap &kmap, const CUtensorMap &vmap, int64_t num_slots)
+                                              const DecodeMaps &maps)
 {
     using C = TcCfg<DP>;
-    constexpr int NS = C::kDecStages;
+    constexpr int NS = FP8 ? C::kDecStagesF8 : C::kDecStages;
+    constexpr int kRing = FP8 ? C::kDecRingF8 : C::kDecRing;
+    constexpr int kBarOff = FP8 ? C::kDecBarOffF8 : C::kDecBarOff;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sb = (raw + 1023u) & ~1023u;
@@ -394,13 +405,20 @@ __device__ __forceinline__ void tc_decode_cta(const AttnParams &pd, const WorkLi
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int kWarps = kTcThreads / 32;
     WarpPipe wp;
-    wp.ring = sb + warp * C::kDecRing;
-    wp.bars = sb + C::kDecBarOff + warp * NS * 8;
-    wp.stage_f = reinterpret_cast<float *>(sp + warp * C::kDecRing);
+    wp.ring = sb + warp * kRing;
+    wp.bars = sb + kBarOff + warp * NS * 8;
+    wp.stage_ptr = sp + warp * kRing;
+    wp.scales = 0u;
+    wp.scale_f = nullptr;
+    if constexpr (FP8) {
+        constexpr int kScales = NS * WarpRingF8::kScaleStage;
+        wp.scales = sb + C::kDecScaleOffF8 + warp * kScales;
+        wp.scale_f = reinterpret_cast<const float *>(sp + C::kDecScaleOffF8 + warp * kScales);
+    }
     wp.seq = 0;
     if (lane == 0) {
-        prefetch_tmap(&kmap);
-        prefetch_tmap(&vmap);
+        prefetch_tmap(&maps.k);
+        prefetch_tmap(&maps.v);
         for (int s = 0; s < NS; s++) mbar_init(wp.bars + 8u * s, 1);
         fence_mbar_init();
     }
@@ -408,7 +426,7 @@ __device__ __forceinline__ void tc_decode_cta(const AttnParams &pd, const WorkLi
     pdl_wait();                                                    // the step's earlier kernels are done
     const int items = dl.item_off[dl.n];
     for (int it = cta * kWarps + warp; it < items; it += ctas * kWarps) {
-        warp_decode_item<DP, D, NS>(pd, dl, it, wp, &kmap, &vmap, num_slots);
+        warp_decode_item<DP, D, NS, FP8>(pd, dl, it, wp, maps);
         __syncwarp();
         // the epilogue's reads of the ring precede the next item's copies into it
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -416,22 +434,25 @@ __device__ __forceinline__ void tc_decode_cta(const AttnParams &pd, const WorkLi
 }
 
 // DP: head dim padded to the 64-column sub-tile; D: head dim of q and out;
-// WIN: a sliding window is set (p.window > 0).  MIX: a mixed batch: the first
-// mix->dec_rows grid rows are decode CTAs (list dl, parameters pd), the
-// tcgen05 prefill CTAs follow.
-template <int DP, int D, bool WIN, bool MIX>
+// WIN: a sliding window is set (p.window > 0).  MIX: a mixed batch (0:
+// none, kMixBf16 or kMixFp8: decodes over a bf16 or a quantized pool): the
+// first mix->dec_rows grid rows are decode CTAs (list dl, parameters pd,
+// the pool's maps dm), the tcgen05 prefill CTAs follow.
+constexpr int kMixBf16 = 1, kMixFp8 = 2;
+template <int DP, int D, bool WIN, int MIX>
 __device__ __forceinline__ void attn_tc_body(const AttnParams &p, const WorkList &wl, const CUtensorMap &qmap,
                                              const CUtensorMap &kmap, const CUtensorMap &vmap, int64_t num_slots,
-                                             const AttnParams *pd, const WorkList *dl, const MixAssign *mix)
+                                             const AttnParams *pd, const WorkList *dl, const MixAssign *mix,
+                                             const DecodeMaps *dm)
 {
-    if constexpr (MIX) {
+    if constexpr (MIX != 0) {
         if ((int)blockIdx.y < mix->dec_rows) {
-            tc_decode_cta<DP, D>(*pd, *dl, blockIdx.y * gridDim.x + blockIdx.x, mix->dec_rows * gridDim.x, kmap, vmap,
-                                 num_slots);
+            tc_decode_cta<DP, D, MIX == kMixFp8>(*pd, *dl, blockIdx.y * gridDim.x + blockIdx.x,
+                                                 mix->dec_rows * gridDim.x, *dm);
             return;
         }
     }
-    const int row = MIX ? (int)blockIdx.y - mix->dec_rows : (int)blockIdx.y;   // this CTA's prefill row
+    const int row = MIX != 0 ? (int)blockIdx.y - mix->dec_rows : (int)blockIdx.y;   // this CTA's prefill row
     using C = TcCfg<DP>;
     constexpr int kTile = C::kTile, kQOff = C::kQOff, kKOff = C::kKOff, kVOff = C::kVOff, kBarOff = C::kBarOff;
     constexpr int kHalves = C::kHalves;
@@ -809,17 +830,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, co
                                                                 const __grid_constant__ CUtensorMap vmap,
                                                                 int64_t num_slots)
 {
-    attn_tc_body<DP, D, WIN, false>(p, wl, qmap, kmap, vmap, num_slots, nullptr, nullptr, nullptr);
+    attn_tc_body<DP, D, WIN, 0>(p, wl, qmap, kmap, vmap, num_slots, nullptr, nullptr, nullptr, nullptr);
 }
 
-template <int DP, int D, bool WIN>
+template <int DP, int D, bool WIN, int MIX>
 __global__ void __launch_bounds__(kTcThreads, 1)
     attn_tc_mix_kernel(AttnParams p, const __grid_constant__ WorkList wl, const __grid_constant__ CUtensorMap qmap,
                        const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                        int64_t num_slots, AttnParams pd, const __grid_constant__ WorkList dl,
-                       const __grid_constant__ MixAssign mix)
+                       const __grid_constant__ MixAssign mix, const __grid_constant__ DecodeMaps dm)
 {
-    attn_tc_body<DP, D, WIN, true>(p, wl, qmap, kmap, vmap, num_slots, &pd, &dl, &mix);
+    attn_tc_body<DP, D, WIN, MIX>(p, wl, qmap, kmap, vmap, num_slots, &pd, &dl, &mix, &dm);
 }
 
 // ---------------------------------------------------------------- host side
@@ -827,6 +848,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 cudaError_t make_pool_tmap(CUtensorMap *map, const void *pool, int64_t num_slots, int hkv, int d, int box_cols,
                            bool swizzle128);
 cudaError_t make_q_tmap(CUtensorMap *map, const void *q, int num_tokens, int hq, int d, int g);
+cudaError_t make_code_tmap(CUtensorMap *map, const void *pool, int64_t num_slots, int hkv);
 
 bool tc_prefill_supported(int head_dim, int group)
 {
@@ -839,29 +861,52 @@ static cudaError_t launch_tc_d(const AttnParams &p, const WorkList &wl, int num_
                                const void *k_cache, const void *v_cache, int64_t num_slots, cudaStream_t stream,
                                const AttnParams *pd, const WorkList *dl, const MixAssign *mix)
 {
-    constexpr int smem = TcCfg<DP>::kSmem, smem_mix = TcCfg<DP>::kSmemMix;
+    constexpr int smem = TcCfg<DP>::kSmem, smem_mix = TcCfg<DP>::kSmemMix, smem_f8 = TcCfg<DP>::kSmemMixF8;
+    constexpr bool kHasF8 = DP == 128 && D == 128;                 // quantized pools: head dim 128
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
         attr_err = cudaFuncSetAttribute(attn_tc_kernel<DP, D, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(attn_tc_mix_kernel<DP, D, WIN>,
+            attr_err = cudaFuncSetAttribute(attn_tc_mix_kernel<DP, D, WIN, kMixBf16>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem_mix);
+        if (attr_err == cudaSuccess && kHasF8)
+            attr_err = cudaFuncSetAttribute(attn_tc_mix_kernel<DP, D, WIN, kHasF8 ? kMixFp8 : kMixBf16>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem_f8);
     });
     if (attr_err != cudaSuccess) return attr_err;
+    const bool fp8_dec = mix && pd->k_scale != nullptr;
+    if (fp8_dec && !kHasF8) return cudaErrorInvalidValue;
     CUtensorMap qm, km, vm;
     // 64-column boxes; for D < 64 they reach past the row and TMA fills zeros
     cudaError_t e = make_q_tmap(&qm, q, num_tokens, p.hq, D, p.group);
     if (e == cudaSuccess) e = make_pool_tmap(&km, k_cache, num_slots, p.hkv, D, 64, true);
     if (e == cudaSuccess) e = make_pool_tmap(&vm, v_cache, num_slots, p.hkv, D, 64, true);
     if (e != cudaSuccess) return e;
+    // the decode items' pool: the prefill's own (bf16), or the quantized
+    // pool whose bf16 copies the prefill reads
+    DecodeMaps dm;
+    if (mix) {
+        if (fp8_dec) {
+            const int64_t dslots = (int64_t)pd->nb_total * 16;
+            e = make_code_tmap(&dm.k, pd->k_cache, dslots, pd->hkv);
+            if (e == cudaSuccess) e = make_code_tmap(&dm.v, pd->v_cache, dslots, pd->hkv);
+            if (e != cudaSuccess) return e;
+        } else {
+            dm.k = km;
+            dm.v = vm;
+        }
+    }
     const int rows = num_items + (mix ? mix->dec_rows : 0);
     if (rows > 65535) return cudaErrorInvalidConfiguration;
     dim3 grid(p.hkv, rows);                        // items in launch order: the planner puts the longest first
     launch_begin(stream, mix ? kAttnTcMixed : kAttnTcPrefill);
-    if (mix)
-        e = launch_maybe_pdl(attn_tc_mix_kernel<DP, D, WIN>, grid, dim3(kTcThreads), smem_mix, stream, p, wl, qm, km,
-                             vm, num_slots, *pd, *dl, *mix);
+    if (fp8_dec)
+        e = launch_maybe_pdl(attn_tc_mix_kernel<DP, D, WIN, kHasF8 ? kMixFp8 : kMixBf16>, grid, dim3(kTcThreads),
+                             smem_f8, stream, p, wl, qm, km, vm, num_slots, *pd, *dl, *mix, dm);
+    else if (mix)
+        e = launch_maybe_pdl(attn_tc_mix_kernel<DP, D, WIN, kMixBf16>, grid, dim3(kTcThreads), smem_mix, stream, p,
+                             wl, qm, km, vm, num_slots, *pd, *dl, *mix, dm);
     else
         e = launch_maybe_pdl(attn_tc_kernel<DP, D, WIN>, grid, dim3(kTcThreads), smem, stream, p, wl, qm, km, vm,
                              num_slots);

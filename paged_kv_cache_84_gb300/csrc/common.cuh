@@ -387,7 +387,8 @@ enum KernelId : int {
     kBlockCopy = 7,
     kByteCopy = 8,
     kAttnTcMixed = 9,
-    kNumKernelIds = 10
+    kFp8Dequant = 10,
+    kNumKernelIds = 11
 };
 
 // Call around every kernel launch: counts it and, while profiling is on,

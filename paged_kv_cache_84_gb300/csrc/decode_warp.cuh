@@ -1,13 +1,13 @@
 // Decode attention run by a single warp over its own ring of KV stages.
 //
-// The tcgen05 prefill kernel for mixed batches gives the decode-class work
-// of the step to its one otherwise idle warp (warp 3): its CTAs are bound
-// by the tensor pipe, while decode attention is bound by HBM, so the two
-// share the SMs without slowing each other much.  A decode item is one
+// The decode CTAs of a mixed tcgen05 launch run the decode-class work of
+// the step: its CTAs are bound by the tensor pipe, decode attention by
+// HBM, so the two share the GPU in one launch.  A decode item is one
 // (request, KV head, key split) of a decode-class request (t * g <= 8 rows
 // per KV head).  The warp walks the item's key blocks ("31. Engine v2",
 // "Attention over the pool": key j in block table[j / 16], row j % 16),
-// lane 0 issuing one TMA copy per 16-row K and V slice into the next of NS
+// lane 0 issuing the TMA copies of a block's K and V slices (quantized
+// pools: E4M3 codes and their per (slot, head) scales) into the next of NS
 // stages, every lane computing key-major MMA tiles (S^T = K Q^T, then
 // O^T += V^T P^T, online softmax in the exp2 domain: mma_tiles.cuh) as the
 // stages land.  The stage count carries over from item to item (`seq`), so
@@ -27,6 +27,25 @@ template <int DP>
 struct WarpRing {
     static constexpr int kSlice = 16 * DP * 2;
     static constexpr int kStage = 2 * kSlice;
+    static constexpr int kBytes = kStage;                       // what a stage's copies deliver
+};
+
+// Stage layout of a warp ring over a quantized pool (head dim 128): the K
+// codes [16][128] as one 128-byte-swizzled box, then the V codes.  The
+// block's K and V scales of the item's KV head (16 fp32 each) go to a
+// separate array of kScaleStage bytes per stage: the warp's lanes copy them
+// with cp.async, one scale each, so that a block takes two TMA copies.
+struct WarpRingF8 {
+    static constexpr int kSlice = 16 * 128;
+    static constexpr int kStage = 2 * kSlice;
+    static constexpr int kBytes = kStage;                       // what a stage's TMA copies deliver
+    static constexpr int kScaleStage = 2 * 16 * 4;
+};
+
+// Tensor maps of the pool the decode items read: K and V (boxes of 64
+// bf16 columns, or 128 E4M3 codes, x 1 head x 16 slots, 128-byte swizzle).
+struct DecodeMaps {
+    CUtensorMap k, v;
 };
 
 // Q^T of this lane's row as B fragments for head dims padded to DP: lane
@@ -46,12 +65,15 @@ __device__ __forceinline__ void load_qt_frags_pad(uint32_t (&qb)[DP / 16][2], co
 }
 
 // Per-warp pipeline state: its ring (shared address, 1024-aligned), the NS
-// full barriers, scratch for the epilogue (a generic pointer to the ring:
-// the stages are free by then), and the blocks consumed so far.
+// full barriers, a generic pointer to the ring (the epilogue's scratch sits
+// in it: the stages are free by then), the quantized pools' scale array
+// (shared address and generic pointer), and the blocks consumed so far.
 struct WarpPipe {
     uint32_t ring;
     uint32_t bars;
-    float *stage_f;
+    uint8_t *stage_ptr;
+    uint32_t scales;
+    const float *scale_f;
     uint32_t seq;
 };
 
@@ -63,12 +85,14 @@ struct WarpPipe {
 // kh): the warp that counts last merges the splits.  Combined calls (fw_k):
 // the item whose key range holds the request's new rows writes them into the
 // pool first.
-template <int DP, int D, int NS>
+template <int DP, int D, int NS, bool FP8 = false>
 __device__ __forceinline__ void warp_decode_item(const AttnParams &p, const WorkList &dl, int item, WarpPipe &wp,
-                                                 const CUtensorMap *kmap, const CUtensorMap *vmap,
-                                                 int64_t num_slots)
+                                                 const DecodeMaps &maps)
 {
-    using R = WarpRing<DP>;
+    static_assert(!FP8 || (DP == 128 && D == 128), "quantized pools have head dim 128");
+    constexpr int kSlice = FP8 ? WarpRingF8::kSlice : WarpRing<DP>::kSlice;
+    constexpr int kStage = FP8 ? WarpRingF8::kStage : WarpRing<DP>::kStage;
+    constexpr int kTx = FP8 ? WarpRingF8::kBytes : WarpRing<DP>::kBytes;
     const int lane = threadIdx.x & 31;
     const int li = find_listed(dl, item);
     const int local = item - dl.item_off[li];
@@ -79,7 +103,10 @@ __device__ __forceinline__ void warp_decode_item(const AttnParams &p, const Work
     const int nr = t * g;
     if (L == 0 || t == 0) {                                        // padding request: zero rows
         if (split == 0) {
-            if (p.fw_k && t > 0) fused_kv_write<D>(p, r, b, t, 0, kh, -t, 0, lane, 32);
+            if (p.fw_k && t > 0) {
+                if constexpr (!FP8) fused_kv_write<D>(p, r, b, t, 0, kh, -t, 0, lane, 32);
+                else fused_kv_write_fp8(p, r, b, t, 0, kh, 1, -t, 0, lane);
+            }
             for (int idx = lane; idx < nr * D; idx += 32) {
                 const int rr = idx / D, e = idx - rr * D;
                 p.out[((size_t)(b + rr / g) * p.hq + kh * g + rr % g) * D + e] = __float2bfloat16(0.f);
@@ -96,24 +123,39 @@ __device__ __forceinline__ void warp_decode_item(const AttnParams &p, const Work
     const int32_t *bt = p.block_table + (size_t)r * p.bt_stride + blk0;
     int ids = lane < nblk ? __ldg(bt + lane) : 0;
     if (p.fw_k) {                                                  // combined call: this item's new rows first
-        fused_kv_write<D>(p, r, b, t, L, kh, max(k_begin, L - t), min(k_end, L), lane, 32);
+        if constexpr (!FP8) fused_kv_write<D>(p, r, b, t, L, kh, max(k_begin, L - t), min(k_end, L), lane, 32);
+        else fused_kv_write_fp8(p, r, b, t, L, kh, 1, max(k_begin, L - t), min(k_end, L), lane);
         __syncwarp();
         fence_proxy_async_global();
     }
-    auto issue = [&](int j) {                                      // block j of the item (lane 0; ids current)
+    auto issue = [&](int j) {                                      // block j of the item (every lane; ids current)
         int blk = __shfl_sync(0xffffffffu, ids, j & 31);
+        if (blk < 0 || blk >= p.nb_total) {                        // outside the pool: report, read block 0
+            if (lane == 0) atomicOr(p.err, 2u);
+            blk = 0;
+        }
+        const int s = (wp.seq + j) % NS;
+        const uint32_t st = wp.ring + s * kStage, bar = wp.bars + 8u * s;
+        if constexpr (FP8) {
+            // lane i < 16: the K scale of the block's slot i, lane 16 + i its
+            // V scale; every lane's arrival is counted before lane 0's
+            const int key = lane & 15;
+            const float *src = (lane < 16 ? p.k_scale : p.v_scale) + ((int64_t)blk * 16 + key) * p.hkv + kh;
+            cp_async_4(wp.scales + s * WarpRingF8::kScaleStage + lane * 4, src);
+            cp_async_mbar_arrive(bar);
+            __syncwarp();
+        }
         if (lane == 0) {
-            if (blk < 0 || blk >= p.nb_total) {                    // outside the pool: report, read block 0
-                atomicOr(p.err, 2u);
-                blk = 0;
-            }
-            const int s = (wp.seq + j) % NS;
-            const uint32_t st = wp.ring + s * R::kStage, bar = wp.bars + 8u * s;
-            mbar_arrive_expect_tx(bar, R::kStage);
+            mbar_arrive_expect_tx(bar, kTx);
+            if constexpr (FP8) {
+                tma_load_3d(st, &maps.k, bar, 0, kh, blk * 16);
+                tma_load_3d(st + kSlice, &maps.v, bar, 0, kh, blk * 16);
+            } else {
 #pragma unroll
-            for (int x = 0; x < DP / 64; x++) {
-                tma_load_3d(st + x * 2048, kmap, bar, x * 64, kh, blk * 16);
-                tma_load_3d(st + R::kSlice + x * 2048, vmap, bar, x * 64, kh, blk * 16);
+                for (int x = 0; x < DP / 64; x++) {
+                    tma_load_3d(st + x * 2048, &maps.k, bar, x * 64, kh, blk * 16);
+                    tma_load_3d(st + kSlice + x * 2048, &maps.v, bar, x * 64, kh, blk * 16);
+                }
             }
         }
     };
@@ -123,7 +165,9 @@ __device__ __forceinline__ void warp_decode_item(const AttnParams &p, const Work
     const int rq = lane >> 2, c2 = 2 * (lane & 3);
     const int mi = lane >> 3, mr = lane & 7;
     uint32_t qb[DP / 16][2];
-    load_qt_frags_pad<DP, D>(qb, p.q, rq < nr ? (size_t)(b + rq / g) * p.hq + kh * g + rq % g : 0, rq < nr, lane);
+    const size_t qrow = rq < nr ? (size_t)(b + rq / g) * p.hq + kh * g + rq % g : 0;
+    if constexpr (FP8) load_qt_frags<D, true>(qb, p.q, qrow, rq < nr, lane);
+    else load_qt_frags_pad<DP, D>(qb, p.q, qrow, rq < nr, lane);
     const int qbase = L - t;
     const int qp0 = c2 < nr ? qbase + c2 / g : -1;
     const int qp1 = c2 + 1 < nr ? qbase + (c2 + 1) / g : -1;
@@ -141,13 +185,21 @@ __device__ __forceinline__ void warp_decode_item(const AttnParams &p, const Work
             break;
         }
         consumed = j + 1;
-        const uint32_t kt = wp.ring + s * R::kStage;
+        const uint32_t kt = wp.ring + s * kStage;
         float sc[1][4] = {{0.f, 0.f, 0.f, 0.f}}, vs[1][2] = {{1.f, 1.f}};
-        const uint32_t vt[1] = {kt + R::kSlice};
+        const uint32_t vt[1] = {kt + kSlice};
         const bool has[1] = {true};
-        block_scores_t<DP, false>(sc[0], qb, kt, mi, mr);
-        mask_scale_t(sc[0], ((blk0 + j) << 4) + rq, k_end, qp0, qp1, wspan, true, p.scale_log2, p.scale_log2);
-        softmax_pv_t<DP, false, 1>(o, m, l, sc, vs, vt, has, mi, mr);
+        block_scores_t<DP, FP8>(sc[0], qb, kt, mi, mr);
+        float f0 = p.scale_log2, f1 = p.scale_log2;
+        if constexpr (FP8) {                                       // K and V scales of keys rq, rq + 8
+            const float *sk = wp.scale_f + s * (WarpRingF8::kScaleStage / 4);
+            f0 *= sk[rq];
+            f1 *= sk[rq + 8];
+            vs[0][0] = sk[16 + rq];
+            vs[0][1] = sk[16 + rq + 8];
+        }
+        mask_scale_t(sc[0], ((blk0 + j) << 4) + rq, k_end, qp0, qp1, wspan, true, f0, f1);
+        softmax_pv_t<DP, FP8, 1>(o, m, l, sc, vs, vt, has, mi, mr);
         __syncwarp();
         if (j + NS < nblk) {
             // the slot's reads are done; make them precede the copy that refills it
@@ -170,15 +222,15 @@ __device__ __forceinline__ void warp_decode_item(const AttnParams &p, const Work
         l[j] += __shfl_xor_sync(0xffffffffu, l[j], 8);
         l[j] += __shfl_xor_sync(0xffffffffu, l[j], 16);
     }
-    float *mo = wp.stage_f;                                        // [8][DP] then (m, l) [8][2]
+    float *mo = reinterpret_cast<float *>(wp.stage_ptr);          // [8][DP] then (m, l) [8][2]
     float *mml = mo + 8 * DP;
 #pragma unroll
     for (int j = 0; j < 2; j++) {
         const int x = c2 + j;
 #pragma unroll
         for (int mt = 0; mt < DP / 16; mt++) {
-            mo[x * DP + ot_dim<false>(mt, rq, 0)] = o[mt][j];
-            mo[x * DP + ot_dim<false>(mt, rq, 1)] = o[mt][2 + j];
+            mo[x * DP + ot_dim<FP8>(mt, rq, 0)] = o[mt][j];
+            mo[x * DP + ot_dim<FP8>(mt, rq, 1)] = o[mt][2 + j];
         }
         if (rq == 0) {
             mml[x * 2] = m[j];

@@ -207,56 +207,81 @@ cudaError_t launch_kv_write_ranges(const void *k, const void *v, void *k_cache, 
 // sblk0 + item_off[li] + i) as bf16 K and V = code * scale, rounded to nearest, in a
 // scratch pool [blocks][16][hkv][128] with a scratch block table
 // (table_out[r][i] = the scratch block); rows at positions >= L become
-// zeros.  One thread per 8 codes of one (slot row, head).  A block id
-// outside the pool is reported (bit 2) and its rows become zeros.
-__global__ void __launch_bounds__(256) fp8_dequant_kernel(AttnParams p, const __grid_constant__ WorkList wl,
-                                                          uint4 *__restrict__ k_out, uint4 *__restrict__ v_out,
-                                                          int32_t *__restrict__ table_out, int32_t table_stride,
-                                                          int32_t sblk0)
+// zeros.  A block id outside the pool is reported (bit 2) and its rows
+// become zeros.  One CTA per scratch block (grid-stride): the request and
+// the block index come from one search of the list per block; each thread
+// then converts 16-code chunks (a chunk lies in one (slot, head) row, so one
+// scale load serves 16 codes), kDequantBatch chunks of K and of V loaded
+// before any is converted, so that their loads are in flight together.
+constexpr int kDequantThreads = 128;
+constexpr int kDequantBatch = 4;
+
+__global__ void __launch_bounds__(kDequantThreads) fp8_dequant_kernel(AttnParams p, const __grid_constant__ WorkList wl,
+                                                                      uint4 *__restrict__ k_out,
+                                                                      uint4 *__restrict__ v_out,
+                                                                      int32_t *__restrict__ table_out,
+                                                                      int32_t table_stride, int32_t sblk0)
 {
     pdl_wait();                                           // the step's codes are in the pool
     pdl_launch_dependents();
     const int hkv = p.hkv;
-    const int64_t per_block = (int64_t)16 * hkv * 16;     // rows x heads x 8-code chunks
-    const int64_t total = (int64_t)wl.item_off[wl.n] * per_block;
-    const uint2 *kc = reinterpret_cast<const uint2 *>(p.k_cache);
-    const uint2 *vc = reinterpret_cast<const uint2 *>(p.v_cache);
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += stride) {
-        const int32_t lblk = (int32_t)(idx / per_block);  // block among this launch's
-        const int32_t rem = (int32_t)(idx - (int64_t)lblk * per_block);
-        const int rr = rem / (hkv * 16), h = (rem / 16) % hkv, c = rem % 16;
+    const int chunks = 16 * hkv * 8;                      // 16-code chunks of a block's K (or V) codes
+    const int nblocks = wl.item_off[wl.n];
+    const uint4 *kc = reinterpret_cast<const uint4 *>(p.k_cache);
+    const uint4 *vc = reinterpret_cast<const uint4 *>(p.v_cache);
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    for (int lblk = blockIdx.x; lblk < nblocks; lblk += gridDim.x) {
         const int li = find_listed(wl, lblk);
         const int r = wl.req[li], i = lblk - wl.item_off[li];
-        const int32_t sblk = sblk0 + lblk;                // scratch block
-        if (rr == 0 && h == 0 && c == 0) table_out[(size_t)r * table_stride + i] = sblk;
+        const int64_t sbase = (int64_t)(sblk0 + lblk) * 16 * hkv;    // first (slot, head) row of the scratch block
+        if (threadIdx.x == 0) table_out[(size_t)r * table_stride + i] = sblk0 + lblk;
         const int blk = __ldg(p.block_table + (size_t)r * p.bt_stride + i);
         const bool in_pool = blk >= 0 && blk < p.nb_total;
-        if (!in_pool && rr == 0 && h == 0 && c == 0) atomicOr(p.err, 2u);
-        uint4 ko = make_uint4(0u, 0u, 0u, 0u), vo = ko;
-        if (in_pool && i * 16 + rr < wl.len[li]) {
-            const int64_t row = ((int64_t)blk * 16 + rr) * hkv + h;   // (slot, head)
-            const float ks = __ldg(p.k_scale + row), vs = __ldg(p.v_scale + row);
-            const uint2 kx = kc[row * 16 + c], vx = vc[row * 16 + c];
-            ko = e4m3x8_to_bf16x8(kx, ks);
-            vo = e4m3x8_to_bf16x8(vx, vs);
+        if (!in_pool && threadIdx.x == 0) atomicOr(p.err, 2u);
+        const int valid_rows = in_pool ? min(16, wl.len[li] - i * 16) * hkv : 0;   // (slot, head) rows to convert
+        const int64_t pbase = (int64_t)(in_pool ? blk : 0) * 16 * hkv;              // ... in the pool
+        for (int c0 = threadIdx.x; c0 < chunks; c0 += kDequantBatch * kDequantThreads) {
+            uint4 kx[kDequantBatch], vx[kDequantBatch];
+            float ks[kDequantBatch], vs[kDequantBatch];
+#pragma unroll
+            for (int u = 0; u < kDequantBatch; u++) {
+                const int c = c0 + u * kDequantThreads;
+                const int rowh = c >> 3;
+                kx[u] = vx[u] = zero;
+                ks[u] = vs[u] = 0.f;
+                if (c < chunks && rowh < valid_rows) {
+                    const int64_t row = pbase + rowh;
+                    kx[u] = __ldg(kc + row * 8 + (c & 7));
+                    vx[u] = __ldg(vc + row * 8 + (c & 7));
+                    ks[u] = __ldg(p.k_scale + row);
+                    vs[u] = __ldg(p.v_scale + row);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kDequantBatch; u++) {
+                const int c = c0 + u * kDequantThreads;
+                if (c >= chunks) break;
+                const int rowh = c >> 3;
+                const int64_t dst = (sbase + rowh) * 16 + (c & 7) * 2;   // 16-byte vectors of bf16 rows
+                const bool ok = rowh < valid_rows;
+                k_out[dst] = ok ? e4m3x8_to_bf16x8(make_uint2(kx[u].x, kx[u].y), ks[u]) : zero;
+                k_out[dst + 1] = ok ? e4m3x8_to_bf16x8(make_uint2(kx[u].z, kx[u].w), ks[u]) : zero;
+                v_out[dst] = ok ? e4m3x8_to_bf16x8(make_uint2(vx[u].x, vx[u].y), vs[u]) : zero;
+                v_out[dst + 1] = ok ? e4m3x8_to_bf16x8(make_uint2(vx[u].z, vx[u].w), vs[u]) : zero;
+            }
         }
-        const int64_t dst = (((int64_t)sblk * 16 + rr) * hkv + h) * 16 + c;
-        k_out[dst] = ko;
-        v_out[dst] = vo;
     }
 }
 
 cudaError_t launch_fp8_dequant(const AttnParams &p, const WorkList &wl, __nv_bfloat16 *k_out, __nv_bfloat16 *v_out,
                                int32_t *table_out, int32_t table_stride, int32_t sblk0, cudaStream_t stream)
 {
-    const int64_t total = (int64_t)wl.item_off[wl.n] * 16 * p.hkv * 16;
-    if (total <= 0) return cudaSuccess;
-    int64_t blocks = (total + 255) / 256;
-    if (blocks > 152 * 16) blocks = 152 * 16;
-    launch_begin(stream, kKvWrite);
-    cudaError_t e = launch_maybe_pdl(fp8_dequant_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, p, wl,
-                                     reinterpret_cast<uint4 *>(k_out), reinterpret_cast<uint4 *>(v_out), table_out,
+    const int64_t nblocks = wl.item_off[wl.n];
+    if (nblocks <= 0) return cudaSuccess;
+    const int64_t grid = nblocks < 152 * 64 ? nblocks : 152 * 64;
+    launch_begin(stream, kFp8Dequant);
+    cudaError_t e = launch_maybe_pdl(fp8_dequant_kernel, dim3((unsigned)grid), dim3(kDequantThreads), 0, stream, p,
+                                     wl, reinterpret_cast<uint4 *>(k_out), reinterpret_cast<uint4 *>(v_out), table_out,
                                      table_stride, sblk0);
     launch_end(stream);
     return e != cudaSuccess ? e : cudaGetLastError();

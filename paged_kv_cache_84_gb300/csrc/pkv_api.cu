@@ -259,6 +259,7 @@ const char *pkv_kernel_name(int32_t kernel_id)
     case kBlockCopy: return "block_copy";
     case kByteCopy: return "byte_copy";
     case kAttnTcMixed: return "attn_tc_mixed";
+    case kFp8Dequant: return "fp8_dequant";
     }
     return "unknown";
 }
@@ -599,6 +600,7 @@ struct AttnPlan {
     bool mix = false;
     int32_t mix_items = 0;              // decode items (request, split, KV head)
     int32_t mix_dec_rows = 0;           // grid rows of decode CTAs ahead of the prefill (x hkv CTAs)
+    double mix_pred_us = 0.0;           // the planner's time of the mixed launch
 };
 
 // ---- tcgen05 prefill: key pieces
@@ -793,7 +795,9 @@ static size_t plan_partial_rows(const AttnPlan &pl, const int32_t *qsl_h, const 
 // arrangement when the predicted time beats the two-stream one's estimate.
 // The decode CTAs' time is the larger of the bytes at kMixCtaGBs per CTA and
 // the items of the busiest warp one after another (kMixItemUs + bytes at
-// kMixWarpGBs each).  Measured on the mixed 2048-token-chunk step (0.67 GB
+// kMixWarpGBs each).  (Items taken from a queue counter instead of dealt
+// round-robin evened the warps out but made the launch slower: 481 against
+// 471 us on the same GPU.)  Measured on the mixed 2048-token-chunk step (0.67 GB
 // of decode K/V in 1568 items of 1024 keys): 8 decode CTAs took 885 us
 // (~95 GB/s each), 16 and 32 470 us against 520 us on two streams; on the
 // 48-request engine step (128 short items) one item per warp took ~25 us,
@@ -804,6 +808,7 @@ constexpr int kMixDecodeWarps = 12;       // warps of a decode CTA (the tcgen05 
 constexpr double kMixCtaGBs = 95.0;       // a decode CTA's rate, GB/s
 constexpr double kMixWarpGBs = 10.0;      // one warp's rate over an item's blocks, GB/s
 constexpr double kMixItemUs = 8.0;        // an item's start (its q, the first copies) and end
+constexpr double kMixFp8Rate = 0.45;      // bytes per second of quantized-pool decode items, relative
 constexpr double kTcTileUs = 1.66;        // a key tile of a pair on tcgen05, measured on the mixed step
 
 static AttnPlan make_plan(const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs, int32_t hq, int32_t hkv,
@@ -861,7 +866,10 @@ static AttnPlan make_plan(const int32_t *qsl_h, const int32_t *sl_h, int32_t num
     };
 
     // ---- the decode class inside the tcgen05 launch, when it fits there
-    bool mix_ok = !fp8 && !rc.tcp.empty() && !rc.dec.empty() && rc.pre.empty() && o.mixed_launch >= 0 &&
+    // (quantized pools: the decode CTAs read the codes, the prefill CTAs the
+    // bf16 copies of their requests' blocks)
+    bool mix_ok = (!fp8 || (rc.fp8_scratch > 0 && d == 128)) && !rc.tcp.empty() && !rc.dec.empty() &&
+                  rc.pre.empty() && o.mixed_launch >= 0 &&
                   rc.tcp.size() <= (size_t)kPlanMax && rc.dec.size() <= (size_t)kPlanMax && pl.has_counters &&
                   (d == 128 || d == 64 || d == 48);
     for (int32_t r : rc.dec)
@@ -871,10 +879,15 @@ static AttnPlan make_plan(const int32_t *qsl_h, const int32_t *sl_h, int32_t num
         layout(m, o.split_tokens > 0 ? o.split_tokens : kMixSplit, true);
         int64_t items = 0, counters = 0;
         double dec_bytes = 0.0;
+        const double key_bytes = fp8 ? 2.0 * d + 8.0 : 4.0 * d;    // K and V of one key and head
+        // quantized pools: a block carries half the bytes for the same MMA
+        // work and the code conversions, so fewer bytes per second
+        const double cta_gbs = fp8 ? kMixCtaGBs * kMixFp8Rate : kMixCtaGBs;
+        const double warp_gbs = fp8 ? kMixWarpGBs * kMixFp8Rate : kMixWarpGBs;
         for (int32_t r : rc.dec) {
             const int32_t t = qsl_h[r + 1] - qsl_h[r], L = sl_h[r];
             const int S = decode_splits(t, L, window, m.split);
-            dec_bytes += (double)std::max(0, L - decode_key_begin(t, L, window)) * hkv * d * 4.0;
+            dec_bytes += (double)std::max(0, L - decode_key_begin(t, L, window)) * hkv * key_bytes;
             items += (int64_t)S * hkv;
             if (S > 1) counters += hkv;
         }
@@ -883,19 +896,27 @@ static AttnPlan make_plan(const int32_t *qsl_h, const int32_t *sl_h, int32_t num
         const size_t dec_part = m.total_rows ? ((m.total_rows * d * 4 + 15) / 16) * 16 + m.total_rows * 8 : 0;
         const size_t tc_room = m.ws_front > m.tc_part_off + 64 ? m.ws_front - m.tc_part_off - 64 : 0;
         (void)dec_part;
+        const bool q_pieces_ok = m.has_counters && o.tc_key_pieces >= 2;
         double best = 1e30;
         int best_rows = 0;
         AttnPlan best_plan = m;
+        // Pairs are cut into key pieces beside the decode CTAs only when the
+        // option asks for pieces: measured on the mixed 2048-token-chunk step
+        // on a quantized pool (32 decode CTAs), the pieces' merges cost more
+        // than the evener prefill saved (497 against 472 us for the launch).
+        const int piece_groups = q_pieces_ok ? kCounterGroups / 2 - (int)counters : 0;
         for (int rows = 1; rows * hkv <= sms / 2; rows *= 2) {
             if (o.mixed_decode_ctas > 0 && rows != std::max(1, (o.mixed_decode_ctas + hkv - 1) / hkv)) continue;
             const int n = rows * hkv;
+            const double item_us = kMixItemUs + dec_bytes / items / (warp_gbs * 1e3);
             const double per_warp = std::ceil((double)items / (n * kMixDecodeWarps));
-            const double dec_us = std::max(dec_bytes / (n * kMixCtaGBs * 1e3),
-                                           per_warp * (kMixItemUs + dec_bytes / items / (kMixWarpGBs * 1e3))) +
-                                  5.0;
+            const double dec_us = std::max(dec_bytes / (n * cta_gbs * 1e3), per_warp * item_us) + 5.0;
+            // the decode CTAs' SMs go to the prefill as their warps finish:
+            // the simulation holds them until the warps' mean finish
+            const double free_us = std::max(dec_bytes / (n * cta_gbs * 1e3),
+                                            items * item_us / (n * kMixDecodeWarps)) + 5.0;
             AttnPlan q = m;
-            plan_tc_pieces(q, qsl_h, sl_h, g, hkv, d, window, sms, tc_room,
-                           q.has_counters ? kCounterGroups / 2 - counters : 0, o, n, dec_us / kTcTileUs);
+            plan_tc_pieces(q, qsl_h, sl_h, g, hkv, d, window, sms, tc_room, piece_groups, o, n, free_us / kTcTileUs);
             const double step = std::max(dec_us, q.tc_makespan * kTcTileUs);
             if (step < best) {
                 best = step;
@@ -906,9 +927,8 @@ static AttnPlan make_plan(const int32_t *qsl_h, const int32_t *sl_h, int32_t num
         if (o.mixed_decode_ctas > 0 && best_rows == 0) {                 // more than half the SMs: as asked
             const int rows = (o.mixed_decode_ctas + hkv - 1) / hkv;
             best_plan = m;
-            plan_tc_pieces(best_plan, qsl_h, sl_h, g, hkv, d, window, sms, tc_room,
-                           best_plan.has_counters ? kCounterGroups / 2 - counters : 0, o, rows * hkv,
-                           dec_bytes / (rows * hkv * kMixCtaGBs * 1e3) / kTcTileUs);
+            plan_tc_pieces(best_plan, qsl_h, sl_h, g, hkv, d, window, sms, tc_room, piece_groups, o, rows * hkv,
+                           dec_bytes / (rows * hkv * cta_gbs * 1e3) / kTcTileUs);
             best_rows = rows;
             best = 0.0;
         }
@@ -916,13 +936,17 @@ static AttnPlan make_plan(const int32_t *qsl_h, const int32_t *sl_h, int32_t num
         // pairs) and the decodes at full HBM speed in what it leaves idle
         AttnPlan w = pl;
         layout(w, decode_split_tokens(rc, w.dec_us, w.pre_us, hkv, fp8, o, sms), false);
-        const double two_stream = w.tc_makespan * kTcTileUs + 0.5 * dec_bytes / 6.5e6;
+        // (quantized pools: the decode kernel over codes is not twice as fast
+        // for half the bytes; measured on the mixed 2048-token-chunk step,
+        // 120-127 us against 133 us on the bf16 pool)
+        const double two_stream = w.tc_makespan * kTcTileUs + 0.5 * dec_bytes / (6.5e6 * (fp8 ? 0.5 : 1.0));
         counters += best_plan.tc_groups;
         if (best_rows > 0 && (best < two_stream || o.mixed_launch > 0) && counters <= kCounterGroups &&
             items < INT32_MAX) {
             best_plan.mix = true;
             best_plan.mix_items = (int32_t)items;
             best_plan.mix_dec_rows = best_rows;
+            best_plan.mix_pred_us = best;
             return best_plan;
         }
     }
@@ -1461,6 +1485,7 @@ pkv_status pkv_plan_attention(const int32_t *qsl_h, const int32_t *sl_h, int32_t
     out->mixed_launch = pl.mix;
     out->mixed_decode_items = pl.mix ? pl.mix_items : 0;
     out->mixed_decode_ctas = pl.mix ? pl.mix_dec_rows * hkv : 0;
+    out->mixed_predicted_us = pl.mix ? (int32_t)std::lround(pl.mix_pred_us) : 0;
     if (pl.mix) {
         out->decode_cluster = 0;
         out->decode_streaming = 0;

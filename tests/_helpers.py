@@ -8,7 +8,7 @@ import torch
 
 import oracle
 import paged_kv_cache_84_gb300 as pkv
-from workloads import Batch, make_batch
+from workloads import Batch, Req, Spec, build_meta, make_batch
 
 MAX_ERR = 2e-2       # max |float(out_bf16) - oracle|
 MEAN_ERR = 2e-3      # mean |float(out_bf16) - oracle|
@@ -110,3 +110,28 @@ def assert_close(got_bf16, want, what=""):
     mx, mean = errors(got_bf16, want)
     assert mx <= MAX_ERR and mean <= MEAN_ERR, f"{what}: max {mx:.3e} mean {mean:.3e}"
     return mx, mean
+
+
+def quantized_pools(batch, seed):
+    """Junk codes and scales everywhere (never NaN codes), then the history of
+    every request written by the oracle's quantizing write from bf16 values."""
+    spec, m = batch.spec, batch.meta
+    nbt = spec.num_blocks_total + 1
+    g = torch.Generator().manual_seed(seed)
+    shape = (nbt, spec.block_size, spec.num_kv_heads, spec.head_dim)
+    kc = torch.randint(0, 255, shape, generator=g, dtype=torch.uint8)
+    vc = torch.randint(0, 255, shape, generator=g, dtype=torch.uint8)
+    kc[(kc & 0x7F) == 0x7F] = 0
+    vc[(vc & 0x7F) == 0x7F] = 0
+    ks = torch.rand(shape[:3], generator=g)
+    vs = torch.rand(shape[:3], generator=g)
+    # history rows (positions 0 .. c-1) from the batch's bf16 pools
+    hist = build_meta(Spec("hist", [Req(0, r.computed, r.table) for r in spec.reqs if not r.pad],
+                           spec.num_q_heads, spec.num_kv_heads, spec.head_dim, spec.block_size,
+                           spec.num_blocks_total, 1.0, 0))
+    if hist.num_tokens:
+        sm = hist.slot_mapping
+        kh = batch.k_cache.view(-1, spec.num_kv_heads, spec.head_dim)[sm]
+        vh = batch.v_cache.view(-1, spec.num_kv_heads, spec.head_dim)[sm]
+        oracle.paged_kv_write_fp8(kc, vc, ks, vs, kh, vh, sm)
+    return kc, vc, ks, vs

@@ -245,3 +245,22 @@ def test_mixed_launch_choice():
     with pkv.options(mixed_decode_ctas=40):
         q = plan(4, mixed=1, combined=True)
     assert q["mixed_launch"] == 1 and q["mixed_decode_ctas"] == 40
+    assert q["mixed_predicted_us"] == 0 and p["mixed_predicted_us"] > 0
+    # beside decode CTAs no pair is cut into key pieces unless asked
+    assert p["prefill_tensor_pieces"] == 0
+    with pkv.options(tc_key_pieces=3):
+        assert plan(4, mixed=1, combined=True)["prefill_tensor_pieces"] > 0
+
+
+def test_mixed_launch_choice_quantized():
+    """Quantized pools: with room for the bf16 copies of the prefill blocks,
+    the mixed step runs as one tcgen05 launch whose decode CTAs read the
+    codes; without that room the prefill stays on the warp-MMA kernel and
+    there is no mixed launch."""
+    spec, qsl, sl = meta(4)
+    extra = pkv.fp8_prefill_scratch_bytes(qsl, sl, spec.num_q_heads, spec.num_kv_heads, 128)
+    p = plan(4, mixed=0, combined=True, quantized=True, workspace_bytes=BIG_WS + extra)
+    assert p["mixed_launch"] == 1 and p["quantized_prefill_scratch"] == extra
+    assert p["mixed_decode_ctas"] % spec.num_kv_heads == 0 and p["prefill_tensor_pieces"] == 0
+    q = plan(4, mixed=0, combined=True, quantized=True, workspace_bytes=32 << 20)   # no room for the copies
+    assert q["mixed_launch"] == 0 and q["quantized_prefill_scratch"] == 0 and q["prefill_mma_requests"] > 0
