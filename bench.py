@@ -599,9 +599,10 @@ def e2e_workload(pkv, copies, steps, device, dist=None, world=1):
     hv = views(host)
     for name in names:
         hv[name].copy_(getattr(c0, name).cpu())
-    # at least two input and output buffers, so that a step's copies can
-    # overlap another step even when one device copy of the workload fills L2
-    devbufs = [torch.empty(total, dtype=torch.uint8, device=device) for _ in range(max(2, len(copies)))]
+    # at least four input and output buffers, so that a step's copies can
+    # overlap other steps even when one device copy of the workload fills
+    # L2: step i's input copy waits only for the output copy of step i - 4
+    devbufs = [torch.empty(total, dtype=torch.uint8, device=device) for _ in range(max(4, len(copies)))]
     dev = [views(b) for b in devbufs]
     outbufs = [torch.empty_like(c0.out) for _ in devbufs]
     outs_h = torch.empty_like(c0.out, device="cpu").pin_memory()

@@ -641,7 +641,10 @@ size_t pkv_fp8_prefill_scratch_bytes(const int32_t *query_start_loc_host, const 
  * host link is saturated by then, and the rest of the GPU stays free for
  * attention launched on other streams while the copy runs (staging the next
  * step's inputs during this step).  A device-to-device copy spreads over
- * the whole GPU.
+ * the whole GPU.  A copy with a pinned host side of 8 MiB or more is a
+ * copy-engine operation (cudaMemcpyAsync on `stream`) instead, which takes
+ * no SM from attention running beside it; it is ordered on `stream` like
+ * the kernel.
  */
 pkv_status pkv_copy_async(void *dst, const void *src, size_t bytes, cudaStream_t stream);
 

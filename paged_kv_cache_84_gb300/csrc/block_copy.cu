@@ -142,11 +142,20 @@ static bool is_host_memory(const void *ptr)
 // against 11.4 us (10.3 us without copies).
 constexpr int kLinkCopyCtas = 12;
 
+// A copy across the link of kDmaCopyBytes or more goes to the copy engine
+// instead: it then takes no SM from attention launched beside it, whose CTAs
+// may hold whole SMs (a tcgen05 launch: 384 threads x 168 registers), and
+// its hand-off cost (a few us between a copy-engine operation and a kernel)
+// is small against its duration.  Measured with the mixed 2048-token-chunk
+// step's 51 MB of inputs and 34 MB of output overlapped with other steps.
+constexpr size_t kDmaCopyBytes = 8u << 20;
+
 cudaError_t launch_byte_copy(void *dst, const void *src, size_t bytes, cudaStream_t stream)
 {
     const int64_t chunks = (int64_t)(bytes / 16);
     if (chunks <= 0) return cudaSuccess;
     const bool link = is_host_memory(dst) || is_host_memory(src);
+    if (link && bytes >= kDmaCopyBytes) return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDefault, stream);
     cudaError_t e;
     launch_begin(stream, kByteCopy);
     if (link) {

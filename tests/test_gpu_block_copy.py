@@ -92,10 +92,11 @@ def test_block_copy_in_a_cuda_graph():
         assert torch.equal(_bits(dv.cpu()), _bits(h))
 
 
-@pytest.mark.parametrize("nbytes", [16, 4096, (1 << 20) + 48, 7 << 20])
+@pytest.mark.parametrize("nbytes", [16, 4096, (1 << 20) + 48, 7 << 20, (8 << 20) + 48, 51 << 20])
 def test_copy_async_host_device_round_trip(nbytes):
     """pkv_copy_async: pinned host -> device, device -> device, device ->
-    pinned host, bit for bit, inside one stream and in a CUDA graph."""
+    pinned host, bit for bit, inside one stream and in a CUDA graph (copies
+    across the link of 8 MiB or more go to the copy engine)."""
     g = torch.Generator().manual_seed(nbytes % 1000)
     src = torch.randint(0, 256, (nbytes,), generator=g, dtype=torch.uint8).pin_memory()
     d1 = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
