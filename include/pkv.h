@@ -255,6 +255,24 @@ pkv_status pkv_ragged_paged_attention(void *out, const void *q,
  *                       never; 0: when the planner expects it to be faster
  *   mixed_decode_ctas   > 0: that many decode CTAs in a mixed launch (rounded
  *                       up to a multiple of the KV heads)
+ *   device_lengths      1: a batch of decode-class requests whose context
+ *                       lengths the kernels read from the device seq_lens when
+ *                       they run.  The host seq_lens then give each request's
+ *                       capacity (the plan: splits, partials, grids), and the
+ *                       device value may be anything from 0 (a padding row)
+ *                       to it.  So a call captured in a CUDA graph can be
+ *                       replayed after the caller has rewritten seq_lens,
+ *                       block_table, slot_mapping, q, k and v in place for
+ *                       another batch of the same shape ("31. Engine v2",
+ *                       "Flattened ragged batches": the batch builder pads
+ *                       decode batches, pad_to, so that one captured step
+ *                       serves them all).  query_start_loc must stay as
+ *                       planned.  A device length above the capacity is
+ *                       clamped to it and reported (PKV_DEVERR_META).  Every
+ *                       request must be decode class (t * g <= 16 rows per
+ *                       KV head): PKV_ERR_UNSUPPORTED otherwise.  With this
+ *                       option results follow the device lengths; with every
+ *                       other option they are the same as without it.
  */
 typedef struct pkv_attention_options {
     int32_t disable_tcgen05;
@@ -271,7 +289,8 @@ typedef struct pkv_attention_options {
     int32_t tc_key_pieces;
     int32_t mixed_launch;
     int32_t mixed_decode_ctas;
-    int32_t reserved[2];
+    int32_t device_lengths;
+    int32_t reserved;
 } pkv_attention_options;
 
 /* pkv_ragged_paged_attention with options (NULL: the planner's choices). */

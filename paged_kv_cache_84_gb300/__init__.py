@@ -56,7 +56,7 @@ class AttentionOptions(ctypes.Structure):
                 ("split_tokens", _c_i32), ("cluster", _c_i32), ("decode_main", _c_i32), ("no_overlap", _c_i32),
                 ("prefill_key_splits", _c_i32), ("separate_write", _c_i32), ("decode_row_tiles", _c_i32),
                 ("no_pdl", _c_i32), ("tc_key_pieces", _c_i32), ("mixed_launch", _c_i32), ("mixed_decode_ctas", _c_i32),
-                ("reserved", _c_i32 * 2)]
+                ("device_lengths", _c_i32), ("reserved", _c_i32)]
 
 
 # The options the attention wrappers pass to the library's _ex calls (None:

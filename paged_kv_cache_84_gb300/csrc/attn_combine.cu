@@ -20,7 +20,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnParams p,
 {
     constexpr int EPL = D >= 128 ? 4 : 2;                 // output elements per lane
     const int li = blockIdx.x;
-    const int b = wl.qb[li], t = wl.qt[li], L = wl.len[li];
+    const int b = wl.qb[li], t = wl.qt[li], L = wl.len[li];      // the planned length fixes the split count
     // decode-class requests split their (windowed) key range; every tile of a
     // split prefill request has ceil(L / split) splits
     const int S = wl.mode == kModeDecode ? decode_splits(t, L, p.window, wl.split_tokens)
@@ -30,6 +30,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnParams p,
     const int row = blockIdx.y * (blockDim.x / 32) + (threadIdx.x >> 5);
     pdl_wait();                                                   // the split partials are written
     if (row >= rows) return;
+    if (run_len(p, wl, li) == 0) return;                          // a padding row at run time: zeros written
     const size_t base = (size_t)wl.part_off[li];
 
     float M = -INFINITY;

@@ -330,7 +330,9 @@ __device__ __forceinline__ void mma_epilogue(const AttnParams &p, const WorkList
     }
     if (!partial || wl.cnt_off[li] < 0) return;
     // ---- in-kernel split combine: count this split, the last one combines
-    const int S = decode_splits(t, L, p.window, wl.split_tokens);
+    // every planned split counts (with device lengths, those past the run's
+    // keys counted with empty partials)
+    const int S = decode_splits(t, wl.len[li], p.window, wl.split_tokens);
     uint32_t *cnt = p.counters + (size_t)(wl.cnt_off[li] + kh) * kCounterStride;
     named_bar_sync(1, kThreads);                                  // every partial store of the CTA is issued
     if (threadIdx.x == 0) {
@@ -425,7 +427,7 @@ __global__ void __launch_bounds__((CW + 1) * 32) attn_mma_kernel(AttnParams p, c
     const int li = find_listed(wl, blockIdx.y);
     const int local = blockIdx.y - wl.item_off[li];
     const int r = wl.req[li];
-    const int b = wl.qb[li], t = wl.qt[li], L = wl.len[li];
+    const int b = wl.qb[li], t = wl.qt[li], L = run_len(p, wl, li);
     const int g = p.group;
 
     if (L == 0 || t == 0) {                                       // padding request: zero rows
@@ -834,7 +836,7 @@ __global__ void __launch_bounds__(kMmaThreads) attn_stream_kernel(AttnParams p, 
     const int li = find_listed(wl, blockIdx.y);
     const int local = blockIdx.y - wl.item_off[li];
     const int r = wl.req[li];
-    const int b = wl.qb[li], t = wl.qt[li], L = wl.len[li];
+    const int b = wl.qb[li], t = wl.qt[li], L = run_len(p, wl, li);
     const int g = p.group;
     const int gg = HP * g;
 

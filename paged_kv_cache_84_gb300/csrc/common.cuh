@@ -105,6 +105,9 @@ struct AttnParams {
     const int64_t *fw_slots;
     float *fw_ks;               // quantized pools: the scale pools the combined call writes
     float *fw_vs;
+    // Decode batches planned for capacities: each request's context length is
+    // the device seq_lens entry (at most the planned one) instead of the plan's.
+    int32_t dev_len;
 };
 
 // Token ranges [begin, begin + len) of the rows a ranged scatter writes
@@ -213,7 +216,19 @@ __device__ __forceinline__ void check_meta(const AttnParams &p, const WorkList &
 {
     const int r = wl.req[li];
     const int b = p.qsl[r], e = p.qsl[r + 1], L = p.seq_lens[r];
-    if (b != wl.qb[li] || e - b != wl.qt[li] || L != wl.len[li]) atomicOr(p.err, kDevErrMeta);
+    const bool len_ok = p.dev_len ? L <= wl.len[li] : L == wl.len[li];
+    if (b != wl.qb[li] || e - b != wl.qt[li] || !len_ok) atomicOr(p.err, kDevErrMeta);
+}
+
+// Context length of listed request li as this call runs it: the planned one,
+// or (p.dev_len) the device seq_lens entry, clamped to [0, planned] (a longer
+// one is reported by check_meta).  The planned length fixes the split count.
+__device__ __forceinline__ int run_len(const AttnParams &p, const WorkList &wl, int li)
+{
+    const int planned = wl.len[li];
+    if (!p.dev_len) return planned;
+    const int L = __ldg(p.seq_lens + wl.req[li]);
+    return L < 0 ? 0 : (L > planned ? planned : L);
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -414,6 +429,7 @@ struct CallOptions {
     int tc_key_pieces = 0;            // 0: planner; -1: no key pieces; k >= 2: every tcgen05 pair in k pieces
     int mixed_launch = 0;             // 0: planner; 1: decode class in the tcgen05 launch when it can; -1: never
     int mixed_decode_ctas = 0;        // > 0: decode CTAs of a mixed launch (rounded up to the KV heads)
+    bool device_lengths = false;      // decode batch: context lengths read from the device at run time
 };
 
 // Launch-level choices of the attention call in progress on this thread,

@@ -97,6 +97,7 @@ static CallOptions call_options(const pkv_attention_options *o)
     c.tc_key_pieces = o->tc_key_pieces < 0 ? -1 : (o->tc_key_pieces >= 2 ? o->tc_key_pieces : 0);
     c.mixed_launch = o->mixed_launch > 0 ? 1 : (o->mixed_launch < 0 ? -1 : 0);
     c.mixed_decode_ctas = o->mixed_decode_ctas > 0 ? o->mixed_decode_ctas : 0;
+    c.device_lengths = o->device_lengths != 0;
     return c;
 }
 
@@ -836,7 +837,9 @@ static AttnPlan make_plan(const int32_t *qsl_h, const int32_t *sl_h, int32_t num
     pl.ws_front = rc.fp8_scratch ? ((workspace_bytes - rc.fp8_scratch) & ~(size_t)255) : workspace_bytes;
     pl.has_counters = pl.ws_front >= kErrBytes + kCounterBytes + 64;
     pl.part_base = kErrBytes + (pl.has_counters ? kCounterBytes : 0);
-    pl.cluster_opt = o.cluster;
+    // with device lengths a request's keys are known only on the device:
+    // splits merge through the counters, not clusters of evenly cut splits
+    pl.cluster_opt = o.device_lengths ? -1 : o.cluster;
 
     // The split length, the workspace layout and the tcgen05 pieces for a
     // starting split length (grown until the decode partials fit) and
@@ -1012,6 +1015,8 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
     const bool fused = fw_k != nullptr;
     const AttnPlan pl =
         make_plan(qsl_h, sl_h, num_reqs, hq, hkv, d, bs, window, fp8, fused, workspace_bytes, num_sms(), opts);
+    // device lengths: decode batches only (prefill tiles are planned from their lengths)
+    if (opts.device_lengths && (!pl.rc.tcp.empty() || !pl.rc.pre.empty())) return PKV_ERR_UNSUPPORTED;
     LaunchChoices lc;
     lc.pdl = !opts.no_pdl;
     lc.decode_row_tiles = opts.decode_row_tiles;
@@ -1034,7 +1039,7 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
 
     const int64_t num_slots = (int64_t)num_blocks_total * bs;
     char *ws = static_cast<char *>(workspace);
-    AttnParams p;
+    AttnParams p = {};
     p.out = static_cast<__nv_bfloat16 *>(out);
     p.q = static_cast<const __nv_bfloat16 *>(q);
     p.k_cache = static_cast<const __nv_bfloat16 *>(k_cache);
@@ -1066,6 +1071,7 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
     p.fw_slots = fused ? fw_slots : nullptr;
     p.fw_ks = fused && fp8 ? const_cast<float *>(k_scale) : nullptr;
     p.fw_vs = fused && fp8 ? const_cast<float *>(v_scale) : nullptr;
+    p.dev_len = opts.device_lengths ? 1 : 0;
     AttnParams pp = p;                                   // prefill launches: their rows come from the scatter
     pp.fw_k = pp.fw_v = nullptr;
     pp.fw_kc = pp.fw_vc = nullptr;
@@ -1461,8 +1467,10 @@ pkv_status pkv_plan_attention(const int32_t *qsl_h, const int32_t *sl_h, int32_t
             return PKV_ERR_CUDA;
         }
     }
+    const CallOptions copts = call_options(options);
     const AttnPlan pl = make_plan(qsl_h, sl_h, num_reqs, hq, hkv, d, bs, window, quantized != 0, combined != 0,
-                                  workspace_bytes, sms, call_options(options));
+                                  workspace_bytes, sms, copts);
+    if (copts.device_lengths && (!pl.rc.tcp.empty() || !pl.rc.pre.empty())) return PKV_ERR_UNSUPPORTED;
     memset(out, 0, sizeof *out);
     out->decode_requests = (int32_t)pl.rc.dec.size();
     out->prefill_tensor_requests = (int32_t)pl.rc.tcp.size();

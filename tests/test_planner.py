@@ -264,3 +264,17 @@ def test_mixed_launch_choice_quantized():
     assert p["mixed_decode_ctas"] % spec.num_kv_heads == 0 and p["prefill_tensor_pieces"] == 0
     q = plan(4, mixed=0, combined=True, quantized=True, workspace_bytes=32 << 20)   # no room for the copies
     assert q["mixed_launch"] == 0 and q["quantized_prefill_scratch"] == 0 and q["prefill_mma_requests"] > 0
+
+
+def test_device_lengths_plan_decode_batches_only():
+    """With device lengths (a padded decode step planned at capacity) only
+    decode-class batches are accepted: a prefill chunk, whose tiles are
+    planned from its own length, is refused before anything is enqueued;
+    split decodes merge through the counters, never clusters."""
+    with pkv.options(device_lengths=1):
+        with pytest.raises(pkv.PkvError):
+            pkv.plan_attention([0, 1, 65], [500, 300], 32, 8, 128, num_sms=SMS)
+        p = pkv.plan_attention(list(range(49)), [4096] * 48, 8, 4, 48, num_sms=SMS)
+    assert p["decode_requests"] == 48 and p["decode_cluster"] == 0
+    q = pkv.plan_attention(list(range(49)), [4096] * 48, 8, 4, 48, num_sms=SMS)
+    assert q["decode_requests"] == 48
