@@ -149,9 +149,12 @@ pkv_status pkv_paged_kv_write_fp8(const void *k, const void *v, void *k_cache, v
  * then splits less.  The workspace holds the device error word (first 256
  * bytes), then — when it has room for them (64 KiB) — the split counters of
  * the combines that run inside the attention kernels, then fp32 split-KV
- * partials.  Zero-fill a workspace once before its first use: every call
- * leaves the counters zero again.  Use one workspace at one size, on one
- * stream at a time.
+ * partials; for pools of blocks of more than 16 slots its last
+ * ceil(num_reqs * ceil(L_max / 16) * 4 / 256) * 256 bytes take the block
+ * table in 16-slot entries (written by the call; PKV_ERR_WORKSPACE when
+ * they do not fit beside PKV_WORKSPACE_MIN_BYTES).  Zero-fill a workspace
+ * once before its first use: every call leaves the counters zero again.
+ * Use one workspace at one size, on one stream at a time.
  */
 #define PKV_WORKSPACE_MIN_BYTES 256
 size_t pkv_attention_workspace_bytes(int32_t max_num_reqs, int32_t max_num_tokens,
@@ -200,8 +203,9 @@ size_t pkv_attention_workspace_bytes(int32_t max_num_reqs, int32_t max_num_token
  *   query_start_loc_host not non-decreasing from 0 to num_tokens; a request
  *   with L > 0 and t > L; ceil(L / block_size) > block_table_stride;
  *   num_q_heads % num_kv_heads != 0; the max_* arguments below the data.
- * PKV_ERR_UNSUPPORTED: head_dim not in {48, 64, 128}, block_size not 16,
- *   or misaligned pointers.
+ * PKV_ERR_UNSUPPORTED: head_dim not in {48, 64, 128}, block_size not one
+ *   of 16, 32, 64, 128, 256 (the kernels walk a block as sub-blocks of 16
+ *   slots), or misaligned pointers.
  */
 pkv_status pkv_ragged_paged_attention(void *out, const void *q,
                                       const void *k_cache, const void *v_cache,

@@ -379,6 +379,10 @@ cudaError_t launch_block_copy(int mode, void *const *pools, int32_t num_pools, c
                               const int32_t *dst, int32_t n, int32_t nb_total, int64_t block_bytes, void *buf,
                               uint32_t *err, cudaStream_t stream);
 cudaError_t launch_byte_copy(void *dst, const void *src, size_t bytes, cudaStream_t stream);
+// Block table in blocks of 16 slots (bt16 [num_reqs][w16]) for a pool of
+// blocks of 16 << shift slots; the next launch on `stream` waits for it to end.
+cudaError_t launch_expand_table(const int32_t *bt, int32_t stride, int32_t *bt16, int32_t w16, int32_t num_reqs,
+                                int32_t shift, int32_t nb_total, cudaStream_t stream);
 cudaError_t launch_fp8_dequant(const AttnParams &p, const WorkList &wl, __nv_bfloat16 *k_out, __nv_bfloat16 *v_out,
                                int32_t *table_out, int32_t table_stride, int32_t sblk0, cudaStream_t stream);
 cudaError_t launch_kv_write_fp8_ranges(const void *k, const void *v, void *k_codes, void *v_codes, float *k_scale,
@@ -403,7 +407,8 @@ enum KernelId : int {
     kByteCopy = 8,
     kAttnTcMixed = 9,
     kFp8Dequant = 10,
-    kNumKernelIds = 11
+    kTableExpand = 11,
+    kNumKernelIds = 12
 };
 
 // Call around every kernel launch: counts it and, while profiling is on,
@@ -438,6 +443,10 @@ struct CallOptions {
 struct LaunchChoices {
     bool pdl = true;                  // programmatic stream serialization for dependent launches
     bool decode_row_tiles = false;    // see CallOptions
+    // the next launch on this stream waits for the kernel before it to end:
+    // that kernel wrote data the next one reads before its programmatic wait
+    cudaStream_t full_wait_stream = nullptr;
+    bool full_wait_pending = false;
 };
 LaunchChoices &launch_choices();
 
@@ -452,6 +461,17 @@ struct ScopedLaunchChoices {
 // wait in-kernel with griddepcontrol.wait).
 inline bool pdl_enabled() { return launch_choices().pdl; }
 
+// The same for a launch on `stream` (consumes a pending full wait on it).
+inline bool pdl_for(cudaStream_t stream)
+{
+    LaunchChoices &c = launch_choices();
+    if (c.full_wait_pending && c.full_wait_stream == stream) {
+        c.full_wait_pending = false;
+        return false;
+    }
+    return c.pdl;
+}
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_maybe_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                              Args... args)
@@ -465,7 +485,7 @@ cudaError_t launch_maybe_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    cfg.numAttrs = pdl_for(stream) ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
@@ -487,7 +507,7 @@ cudaError_t launch_cluster_maybe_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 b
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = pdl_enabled() ? 2 : 1;
+    cfg.numAttrs = pdl_for(stream) ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 

@@ -287,6 +287,44 @@ cudaError_t launch_fp8_dequant(const AttnParams &p, const WorkList &wl, __nv_bfl
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+// Pools of blocks of 16 << shift slots are pools of blocks of 16 slots, as
+// many times more of them ("31. Engine v2", "Attention over the pool": key j
+// in slot table[j / block_size] * block_size + j % block_size): entry j of
+// request r's row in 16-slot blocks is (table[r][j >> shift] << shift) +
+// (j & (2^shift - 1)).  An id outside the pool becomes -1, which the
+// attention kernels report (PKV_DEVERR_BLOCK) and do not read.
+__global__ void __launch_bounds__(256) expand_table_kernel(const int32_t *__restrict__ bt, int32_t stride,
+                                                           int32_t *__restrict__ bt16, int32_t w16, int64_t total,
+                                                           int32_t shift, int32_t nb_total)
+{
+    pdl_wait();                                           // the table may come from the kernel before
+    const int64_t step = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += step) {
+        const int64_t r = idx / w16;
+        const int j = (int)(idx - r * w16);
+        const int b = __ldg(bt + r * stride + (j >> shift));
+        bt16[idx] = (b < 0 || b >= nb_total) ? -1 : (b << shift) + (j & ((1 << shift) - 1));
+    }
+}
+
+cudaError_t launch_expand_table(const int32_t *bt, int32_t stride, int32_t *bt16, int32_t w16, int32_t num_reqs,
+                                int32_t shift, int32_t nb_total, cudaStream_t stream)
+{
+    const int64_t total = (int64_t)num_reqs * w16;
+    if (total <= 0) return cudaSuccess;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > 152 * 8) blocks = 152 * 8;
+    launch_begin(stream, kTableExpand);
+    cudaError_t e = launch_maybe_pdl(expand_table_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, bt, stride,
+                                     bt16, w16, total, shift, nb_total);
+    launch_end(stream);
+    // the attention kernels read block ids before their programmatic wait
+    LaunchChoices &c = launch_choices();
+    c.full_wait_stream = stream;
+    c.full_wait_pending = true;
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 cudaError_t launch_kv_write_fp8(const void *k, const void *v, void *k_codes, void *v_codes, float *k_scale,
                                 float *v_scale, const int64_t *slot_mapping, int32_t num_tokens, int32_t hkv,
                                 int64_t num_slots, uint32_t *err, cudaStream_t stream)

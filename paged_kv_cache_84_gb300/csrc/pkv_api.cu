@@ -109,6 +109,29 @@ static pkv_status cuda_fail(cudaError_t e, const char *where)
     return PKV_ERR_CUDA;
 }
 
+// log2(bs / 16) for the block sizes the kernels walk in sub-blocks of 16
+// slots (16, 32, 64, 128, 256), else -1.
+static int block_shift(int32_t bs)
+{
+    for (int s = 0; s <= 4; s++)
+        if (bs == (16 << s)) return s;
+    return -1;
+}
+
+// Blocks of more than 16 slots: the attention kernels walk a block table in
+// blocks of 16 slots, which an expansion kernel writes at the workspace's
+// end (w16 = ceil(longest host length / 16) entries per request).  Returns
+// its bytes (0 for 16-slot blocks) and sets *w16.
+static size_t table16_bytes(const int32_t *sl_h, int32_t num_reqs, int32_t bs, int32_t *w16)
+{
+    *w16 = 0;
+    if (block_shift(bs) <= 0) return 0;
+    int32_t max_l = 1;
+    for (int r = 0; r < num_reqs; r++) max_l = sl_h[r] > max_l ? sl_h[r] : max_l;
+    *w16 = (max_l + 15) / 16;
+    return ((size_t)num_reqs * *w16 * 4 + 255) / 256 * 256;
+}
+
 static int num_sms()
 {
     static int cached[64] = {0};
@@ -261,6 +284,7 @@ const char *pkv_kernel_name(int32_t kernel_id)
     case kByteCopy: return "byte_copy";
     case kAttnTcMixed: return "attn_tc_mixed";
     case kFp8Dequant: return "fp8_dequant";
+    case kTableExpand: return "block_table_expand";
     }
     return "unknown";
 }
@@ -364,7 +388,9 @@ size_t pkv_attention_workspace_bytes(int32_t max_num_reqs, int32_t max_num_token
     int64_t tc_slots = (int64_t)max_num_tokens * num_q_heads / 256 * kTcMaxPieces;
     if (tc_slots > 6 * 152) tc_slots = 6 * 152;
     const size_t tc_bytes = (size_t)tc_slots * 256 * ((size_t)head_dim * 4 + 8) + 256;
-    return kErrBytes + kCounterBytes + (size_t)rows * ((size_t)head_dim * 4 + 8) + 64 + tc_bytes;
+    // pools of blocks of more than 16 slots: the block table in 16-slot entries
+    const size_t t16_bytes = ((size_t)max_num_reqs * ((max_seq_len + 15) / 16) * 4 + 255) / 256 * 256 + 256;
+    return kErrBytes + kCounterBytes + (size_t)rows * ((size_t)head_dim * 4 + 8) + 64 + tc_bytes + t16_bytes;
 }
 
 size_t pkv_fp8_prefill_scratch_bytes(const int32_t *qsl_h, const int32_t *sl_h, int32_t num_reqs,
@@ -453,7 +479,8 @@ static pkv_status validate_attention(const void *out, const void *q, const void 
         return PKV_ERR_INVALID_ARG;
     const int32_t g = hq / hkv;
     if (d != 48 && d != 64 && d != 128) return PKV_ERR_UNSUPPORTED;
-    if (bs != 16) return PKV_ERR_UNSUPPORTED;
+    if (block_shift(bs) < 0) return PKV_ERR_UNSUPPORTED;
+    if ((int64_t)num_blocks_total * (bs / 16) > INT32_MAX) return PKV_ERR_UNSUPPORTED;
     if (g > kDecodeRows) return PKV_ERR_UNSUPPORTED;
     if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
         return PKV_ERR_UNSUPPORTED;
@@ -1013,8 +1040,13 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
         return st;
     const int32_t g = hq / hkv;
     const bool fused = fw_k != nullptr;
+    // blocks of more than 16 slots: the 16-slot block table takes the workspace's end
+    int32_t w16 = 0;
+    const size_t t16 = table16_bytes(sl_h, num_reqs, bs, &w16);
+    if (t16 && workspace_bytes < t16 + PKV_WORKSPACE_MIN_BYTES + 256) return PKV_ERR_WORKSPACE;
+    const size_t plan_ws = t16 ? (workspace_bytes - t16) & ~(size_t)255 : workspace_bytes;
     const AttnPlan pl =
-        make_plan(qsl_h, sl_h, num_reqs, hq, hkv, d, bs, window, fp8, fused, workspace_bytes, num_sms(), opts);
+        make_plan(qsl_h, sl_h, num_reqs, hq, hkv, d, bs, window, fp8, fused, plan_ws, num_sms(), opts);
     // device lengths: decode batches only (prefill tiles are planned from their lengths)
     if (opts.device_lengths && (!pl.rc.tcp.empty() || !pl.rc.pre.empty())) return PKV_ERR_UNSUPPORTED;
     LaunchChoices lc;
@@ -1072,6 +1104,20 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
     p.fw_ks = fused && fp8 ? const_cast<float *>(k_scale) : nullptr;
     p.fw_vs = fused && fp8 ? const_cast<float *>(v_scale) : nullptr;
     p.dev_len = opts.device_lengths ? 1 : 0;
+    // blocks of more than 16 slots: the same pool as blocks of 16 slots (the
+    // layout [blocks][16 << s][Hkv][d] is [blocks << s][16][Hkv][d]), read
+    // through a table of 16-slot entries expanded at the workspace's end
+    if (t16) {
+        const int shift = block_shift(bs);
+        int32_t *bt16 = reinterpret_cast<int32_t *>(ws + plan_ws);
+        cudaError_t e = launch_expand_table(block_table, block_table_stride, bt16, w16, num_reqs, shift,
+                                            num_blocks_total, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "block table expansion launch");
+        p.block_table = bt16;
+        p.bt_stride = w16;
+        p.nb_total = num_blocks_total << shift;
+        p.block_size = 16;
+    }
     AttnParams pp = p;                                   // prefill launches: their rows come from the scatter
     pp.fw_k = pp.fw_v = nullptr;
     pp.fw_kc = pp.fw_vc = nullptr;
@@ -1194,7 +1240,8 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
         pt.v_cache = sv;
         pt.block_table = stab;
         pt.bt_stride = fp8_width;
-        pt.nb_total = (int32_t)fp8_blocks;
+        pt.nb_total = (int32_t)fp8_blocks;              // blocks of 16 slots
+        pt.block_size = 16;
         pt.k_scale = pt.v_scale = nullptr;
         tc_k = sk;
         tc_v = sv;
@@ -1457,7 +1504,7 @@ pkv_status pkv_plan_attention(const int32_t *qsl_h, const int32_t *sl_h, int32_t
         if (t < 0 || L < 0 || (L > 0 && t > L)) return PKV_ERR_INVALID_ARG;
     }
     const int32_t g = hq / hkv;
-    if ((d != 48 && d != 64 && d != 128) || bs != 16 || g > kDecodeRows) return PKV_ERR_UNSUPPORTED;
+    if ((d != 48 && d != 64 && d != 128) || block_shift(bs) < 0 || g > kDecodeRows) return PKV_ERR_UNSUPPORTED;
     if (quantized && (d != 128 || hkv % 4 != 0)) return PKV_ERR_UNSUPPORTED;
     if (sms <= 0) {
         int dev = 0;
@@ -1468,8 +1515,12 @@ pkv_status pkv_plan_attention(const int32_t *qsl_h, const int32_t *sl_h, int32_t
         }
     }
     const CallOptions copts = call_options(options);
+    int32_t w16 = 0;
+    const size_t t16 = table16_bytes(sl_h, num_reqs, bs, &w16);
+    if (t16 && workspace_bytes < t16 + PKV_WORKSPACE_MIN_BYTES + 256) return PKV_ERR_WORKSPACE;
+    const size_t plan_ws = t16 ? (workspace_bytes - t16) & ~(size_t)255 : workspace_bytes;
     const AttnPlan pl = make_plan(qsl_h, sl_h, num_reqs, hq, hkv, d, bs, window, quantized != 0, combined != 0,
-                                  workspace_bytes, sms, copts);
+                                  plan_ws, sms, copts);
     if (copts.device_lengths && (!pl.rc.tcp.empty() || !pl.rc.pre.empty())) return PKV_ERR_UNSUPPORTED;
     memset(out, 0, sizeof *out);
     out->decode_requests = (int32_t)pl.rc.dec.size();

@@ -92,7 +92,7 @@ def test_attention_host_validation(lib, qsl, sl, maxq, maxl, kw):
 def test_attention_unsupported_and_workspace(lib):
     lib.pkv_ragged_paged_attention.restype = ctypes.c_int
     assert lib.pkv_ragged_paged_attention(*_attn_args([0, 1], [5], 1, 1, 1, 5, d=96)) == 2
-    assert lib.pkv_ragged_paged_attention(*_attn_args([0, 1], [5], 1, 1, 1, 5, bs=32)) == 2
+    assert lib.pkv_ragged_paged_attention(*_attn_args([0, 1], [5], 1, 1, 1, 5, bs=48)) == 2   # not 16 << k
     assert lib.pkv_ragged_paged_attention(*_attn_args([0, 1], [5], 1, 1, 1, 5, ws=64)) == 3
 
 

@@ -30,9 +30,9 @@ COUNTERS = slice(256, 256 + 65536)
 BS = 16
 
 
-def _batch_spec(seed, nreq, cap, hq, hkv, d, nblocks, pad_frac=0.15):
+def _batch_spec(seed, nreq, cap, hq, hkv, d, nblocks, pad_frac=0.15, bs=BS):
     """nreq decode requests of 1 new token each, context 1 .. cap (some
-    padding rows), each on its own random blocks; tables cap/16 wide."""
+    padding rows), each on its own random blocks; tables cap/bs wide."""
     rnd = random.Random(seed)
     perm = list(range(nblocks))
     rnd.shuffle(perm)
@@ -42,17 +42,17 @@ def _batch_spec(seed, nreq, cap, hq, hkv, d, nblocks, pad_frac=0.15):
             reqs.append(Req(0, 1, [], pad=True))
             continue
         L = rnd.choice([1, 15, 16, 17, cap, rnd.randint(1, cap), rnd.randint(1, cap)])
-        nb = -(-L // BS)
+        nb = -(-L // bs)
         reqs.append(Req(L - 1, 1, perm[cur:cur + nb]))
         cur += nb
-    return Spec("graph-replay", reqs, hq, hkv, d, BS, nblocks, 1 / math.sqrt(d), seed, table_width=-(-cap // BS))
+    return Spec("graph-replay", reqs, hq, hkv, d, bs, nblocks, 1 / math.sqrt(d), seed, table_width=-(-cap // bs))
 
 
 class Captured:
     """Device buffers of a padded decode step and the combined call captured
     over them once, planned at capacity `cap` for every row."""
 
-    def __init__(self, nreq, cap, hq, hkv, d, pools, window=0, fp8=None):
+    def __init__(self, nreq, cap, hq, hkv, d, pools, window=0, fp8=None, bs=BS):
         self.nreq, self.cap, self.window, self.fp8 = nreq, cap, window, fp8
         dev = torch.device("cuda")
         self.k_cache, self.v_cache = pools[0], pools[1]
@@ -61,7 +61,7 @@ class Captured:
         self.v = torch.zeros_like(self.k)
         self.qsl = torch.arange(nreq + 1, dtype=torch.int32, device=dev)
         self.sl = torch.zeros(nreq, dtype=torch.int32, device=dev)
-        self.bt = torch.zeros((nreq, -(-cap // BS)), dtype=torch.int32, device=dev)
+        self.bt = torch.zeros((nreq, -(-cap // bs)), dtype=torch.int32, device=dev)
         self.slots = torch.full((nreq,), -1, dtype=torch.int64, device=dev)
         self.out = torch.zeros_like(self.q)
         self.qsl_h = list(range(nreq + 1))
@@ -219,3 +219,27 @@ def test_longer_device_length_is_clamped_and_reported(attn_options):
     torch.cuda.synchronize()
     assert pkv.read_device_error(cs.ws) & pkv.DEVERR_META
     assert torch.isfinite(cs.out.float()).all()
+
+
+@pytest.mark.parametrize("bs", [32, 64])
+def test_replay_at_other_block_sizes(bs, attn_options):
+    """The replayed padded step with blocks of 32 and 64 slots."""
+    attn_options(device_lengths=1)
+    hq, hkv, d, nreq, cap = 32, 8, 128, 24, 2100
+    nblocks = nreq * -(-cap // bs)
+    first = make_batch(_batch_spec(120 + bs, nreq, cap, hq, hkv, d, nblocks, bs=bs), device="cpu")
+    ref_k, ref_v = first.k_cache.clone(), first.v_cache.clone()
+    cs = Captured(nreq, cap, hq, hkv, d, (first.k_cache.cuda(), first.v_cache.cuda()), bs=bs)
+    cs.load(first)
+    cs.capture()
+    for i in range(3):
+        b = first if i == 0 else make_batch(_batch_spec(130 + bs + i, nreq, cap, hq, hkv, d, nblocks, bs=bs),
+                                            device="cpu")
+        cs.load(b)
+        cs.graph.replay()
+        torch.cuda.synchronize()
+        ref = Batch(b.spec, b.meta, b.q, b.k, b.v, ref_k, ref_v)
+        oracle_write(ref)
+        assert_close(cs.out, oracle_full(ref), f"block size {bs}, replay {i}")
+        assert pkv.read_device_error(cs.ws) == 0
+        assert int(cs.ws[COUNTERS].count_nonzero()) == 0

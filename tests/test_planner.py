@@ -212,7 +212,9 @@ def test_sliding_window_limits_the_decode_keys():
     (dict(num_q_heads=8, num_kv_heads=3), 1),           # heads do not group
     (dict(seq_lens=[2]), 1),                            # t > seq_len
     (dict(window=-1), 1),
-    (dict(block_size=32), 2),
+    (dict(block_size=48), 2),                           # not 16 times a power of two
+    (dict(block_size=8), 2),
+    (dict(block_size=512), 2),
     (dict(head_dim=96), 2),
     (dict(quantized=True), 2),                          # quantized pools need head_dim 128
 ])
@@ -278,3 +280,12 @@ def test_device_lengths_plan_decode_batches_only():
     assert p["decode_requests"] == 48 and p["decode_cluster"] == 0
     q = pkv.plan_attention(list(range(49)), [4096] * 48, 8, 4, 48, num_sms=SMS)
     assert q["decode_requests"] == 48
+
+
+@pytest.mark.parametrize("bs", [16, 32, 64, 128, 256])
+def test_block_sizes_the_kernels_walk(bs):
+    """Blocks of 16 times a power of two slots (up to 256) are planned: the
+    kernels walk a block as sub-blocks of 16 slots."""
+    p = pkv.plan_attention([0, 1, 300], [100, 2000], 32, 8, 128, block_size=bs, num_sms=SMS)
+    assert p["decode_requests"] == 1 and p["prefill_tensor_requests"] == 1
+    assert p["decode_split_tokens"] % bs == 0
