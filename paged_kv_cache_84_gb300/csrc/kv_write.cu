@@ -5,6 +5,9 @@
 // negative slot marks a padding row and goes to the pool's last slot, the
 // scratch block.  A bit copy: 16-byte vectors, one per thread, the K and the
 // V chunk of the same offset handled together.
+#include <algorithm>
+#include <mutex>
+
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -273,16 +276,116 @@ __global__ void __launch_bounds__(kDequantThreads) fp8_dequant_kernel(AttnParams
     }
 }
 
+// The same with the block's bf16 rows assembled in shared memory (K, then
+// V: 16 x hkv rows of 256 bytes each) and written out as two bulk copies of
+// the whole scratch block, which is contiguous: the threads' 32-byte row
+// pieces become two copies of 4 KB x hkv instead of 16-byte stores at a
+// 32-byte stride.  A CTA takes blocks in turn; before it overwrites its
+// shared rows, the copies of the block before have read them.
+constexpr int kDequantSmemMax = 192 * 1024;
+
+__global__ void __launch_bounds__(kDequantThreads) fp8_dequant_staged_kernel(AttnParams p,
+                                                                             const __grid_constant__ WorkList wl,
+                                                                             uint4 *__restrict__ k_out,
+                                                                             uint4 *__restrict__ v_out,
+                                                                             int32_t *__restrict__ table_out,
+                                                                             int32_t table_stride, int32_t sblk0)
+{
+    extern __shared__ __align__(128) uint4 rows_s[];      // [2][16 * hkv * 16] 16-byte vectors
+    pdl_wait();                                           // the step's codes are in the pool
+    pdl_launch_dependents();
+    const int hkv = p.hkv;
+    const int chunks = 16 * hkv * 8;                      // 16-code chunks of a block's K (or V) codes
+    const int vecs = 16 * hkv * 16;                       // 16-byte vectors of a block's bf16 K (or V)
+    const int nblocks = wl.item_off[wl.n];
+    const uint4 *kc = reinterpret_cast<const uint4 *>(p.k_cache);
+    const uint4 *vc = reinterpret_cast<const uint4 *>(p.v_cache);
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    uint4 *ks_rows = rows_s, *vs_rows = rows_s + vecs;
+    for (int lblk = blockIdx.x; lblk < nblocks; lblk += gridDim.x) {
+        const int li = find_listed(wl, lblk);
+        const int r = wl.req[li], i = lblk - wl.item_off[li];
+        const int64_t sbase = (int64_t)(sblk0 + lblk) * 16 * hkv;    // first (slot, head) row of the scratch block
+        if (threadIdx.x == 0) table_out[(size_t)r * table_stride + i] = sblk0 + lblk;
+        const int blk = __ldg(p.block_table + (size_t)r * p.bt_stride + i);
+        const bool in_pool = blk >= 0 && blk < p.nb_total;
+        if (!in_pool && threadIdx.x == 0) atomicOr(p.err, 2u);
+        const int valid_rows = in_pool ? min(16, wl.len[li] - i * 16) * hkv : 0;   // (slot, head) rows to convert
+        const int64_t pbase = (int64_t)(in_pool ? blk : 0) * 16 * hkv;              // ... in the pool
+        for (int c0 = threadIdx.x, pass = 0; c0 < chunks; c0 += kDequantBatch * kDequantThreads, pass++) {
+            uint4 kx[kDequantBatch], vx[kDequantBatch];
+            float ks[kDequantBatch], vs[kDequantBatch];
+#pragma unroll
+            for (int u = 0; u < kDequantBatch; u++) {
+                const int c = c0 + u * kDequantThreads;
+                const int rowh = c >> 3;
+                kx[u] = vx[u] = zero;
+                ks[u] = vs[u] = 0.f;
+                if (c < chunks && rowh < valid_rows) {
+                    const int64_t row = pbase + rowh;
+                    kx[u] = __ldg(kc + row * 8 + (c & 7));
+                    vx[u] = __ldg(vc + row * 8 + (c & 7));
+                    ks[u] = __ldg(p.k_scale + row);
+                    vs[u] = __ldg(p.v_scale + row);
+                }
+            }
+            if (pass == 0) {                                  // the previous block's copies have read the rows
+                if (threadIdx.x == 0) bulk_wait_read();
+                __syncthreads();
+            }
+#pragma unroll
+            for (int u = 0; u < kDequantBatch; u++) {
+                const int c = c0 + u * kDequantThreads;
+                if (c >= chunks) break;
+                const int v = (c >> 3) * 16 + (c & 7) * 2;        // 16-byte vector of the block's rows
+                const bool ok = (c >> 3) < valid_rows;
+                ks_rows[v] = ok ? e4m3x8_to_bf16x8(make_uint2(kx[u].x, kx[u].y), ks[u]) : zero;
+                ks_rows[v + 1] = ok ? e4m3x8_to_bf16x8(make_uint2(kx[u].z, kx[u].w), ks[u]) : zero;
+                vs_rows[v] = ok ? e4m3x8_to_bf16x8(make_uint2(vx[u].x, vx[u].y), vs[u]) : zero;
+                vs_rows[v + 1] = ok ? e4m3x8_to_bf16x8(make_uint2(vx[u].z, vx[u].w), vs[u]) : zero;
+            }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the rows, visible to the bulk copies
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            bulk_store(k_out + sbase * 16, smem_u32(ks_rows), (uint32_t)vecs * 16);
+            bulk_store(v_out + sbase * 16, smem_u32(vs_rows), (uint32_t)vecs * 16);
+            bulk_commit();
+        }
+    }
+    if (threadIdx.x == 0) bulk_wait_all();                   // the copies are done before the grid is
+}
+
 cudaError_t launch_fp8_dequant(const AttnParams &p, const WorkList &wl, __nv_bfloat16 *k_out, __nv_bfloat16 *v_out,
                                int32_t *table_out, int32_t table_stride, int32_t sblk0, cudaStream_t stream)
 {
     const int64_t nblocks = wl.item_off[wl.n];
     if (nblocks <= 0) return cudaSuccess;
-    const int64_t grid = nblocks < 152 * 64 ? nblocks : 152 * 64;
+    const int smem = 2 * 16 * p.hkv * 256;                // bf16 K and V rows of one block
+    cudaError_t e;
     launch_begin(stream, kFp8Dequant);
-    cudaError_t e = launch_maybe_pdl(fp8_dequant_kernel, dim3((unsigned)grid), dim3(kDequantThreads), 0, stream, p,
-                                     wl, reinterpret_cast<uint4 *>(k_out), reinterpret_cast<uint4 *>(v_out), table_out,
-                                     table_stride, sblk0);
+    if (smem <= kDequantSmemMax) {
+        static std::once_flag once;
+        static cudaError_t attr_err = cudaSuccess;
+        std::call_once(once, [] {
+            attr_err = cudaFuncSetAttribute(fp8_dequant_staged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            kDequantSmemMax);
+        });
+        if (attr_err != cudaSuccess) {
+            launch_end(stream);
+            return attr_err;
+        }
+        const int per_sm = std::max(1, std::min(16, 220 * 1024 / (smem + 1024)));
+        const int64_t grid = std::min<int64_t>(nblocks, (int64_t)152 * per_sm);
+        e = launch_maybe_pdl(fp8_dequant_staged_kernel, dim3((unsigned)grid), dim3(kDequantThreads), (size_t)smem,
+                             stream, p, wl, reinterpret_cast<uint4 *>(k_out), reinterpret_cast<uint4 *>(v_out),
+                             table_out, table_stride, sblk0);
+    } else {
+        const int64_t grid = nblocks < 152 * 64 ? nblocks : 152 * 64;
+        e = launch_maybe_pdl(fp8_dequant_kernel, dim3((unsigned)grid), dim3(kDequantThreads), 0, stream, p, wl,
+                             reinterpret_cast<uint4 *>(k_out), reinterpret_cast<uint4 *>(v_out), table_out,
+                             table_stride, sblk0);
+    }
     launch_end(stream);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
