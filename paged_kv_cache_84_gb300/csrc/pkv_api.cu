@@ -624,7 +624,7 @@ struct AttnPlan {
     int64_t tc_ctas = 0;                // tcgen05 CTAs in all
     size_t tc_part_off = 0;             // byte offset of the tcgen05 partial slots in the workspace
     double tc_makespan = 0.0;           // simulated tcgen05 makespan, key-tile times
-    // mixed launch: the decode class inside the tcgen05 launch (warp 3 of its CTAs)
+    // mixed launch: the decode class inside the tcgen05 launch (its leading decode CTAs)
     bool mix = false;
     int32_t mix_items = 0;              // decode items (request, split, KV head)
     int32_t mix_dec_rows = 0;           // grid rows of decode CTAs ahead of the prefill (x hkv CTAs)
@@ -1290,7 +1290,7 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
         }
         return cudaSuccess;
     };
-    // ---- mixed launch: the decode class as warp-3 items of the tcgen05 launch
+    // ---- mixed launch: the decode class as items of the tcgen05 launch's decode CTAs
     WorkList mix_dl;
     MixAssign mix_as;
     if (pl.mix) {
