@@ -285,11 +285,15 @@ def roofline(name, avg_s, launches_per_step, acc, peaks, workload):
     else:
         achieved, peak, unit = f / avg_s / 1e12, alu_peak_tflops(peaks), "TFLOP/s"
         note = "of fp32 FMA peak derived as 152 SMs x 128 lanes x 2 flop x max SM clock"
-    return {"kernel": name, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-            "frac": achieved / peak, "traffic": stored_traffic(name, workload), "peak_note": note,
-            "hbm_frac": hbm_frac, "tensor_frac": tensor_frac,
-            "algorithmic_bytes_per_launch": b, "algorithmic_flops_per_launch": f,
-            "avg_launch_us": avg_s * 1e6}
+    res = {"kernel": name, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+           "frac": achieved / peak, "traffic": stored_traffic(name, workload), "peak_note": note,
+           "hbm_frac": hbm_frac, "tensor_frac": tensor_frac,
+           "algorithmic_bytes_per_launch": b, "algorithmic_flops_per_launch": f,
+           "avg_launch_us": avg_s * 1e6}
+    if bound == "tensor" and peaks.get("bf16_tflops_sustained"):
+        # beside the burst peak: the measured rate of a seconds-long GEMM loop under the power cap
+        res["frac_of_sustained"] = achieved / peaks["bf16_tflops_sustained"]
+    return res
 
 
 # ---------------------------------------------------------------------------- GPU arm
