@@ -149,3 +149,21 @@ def test_noalloc_reports_bounds_flags_per_call():
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     assert_close(out, oracle_full(ref), "no-allocation call after a flagged call")
+
+
+def test_noalloc_blocks_of_64_slots():
+    """Blocks of 64 slots: the array also holds the block table in 16-slot
+    entries, and the results match the oracle and the workspace entry point."""
+    b = make_batch(random_spec(83, 12, 3000, 1, 32, 8, 128, block_size=64, decode_frac=1.0, pad_rows=1),
+                   device="cpu")
+    ref = cpu_copy(b)
+    oracle_write(ref)
+    dev = DeviceStep(b)
+    dev.write()
+    dev.attend()
+    for _ in range(2):
+        st, out = _call(dev)
+        assert st == 0
+        torch.cuda.synchronize()
+        assert_close(out, oracle_full(ref), "no-allocation call, blocks of 64 slots")
+        assert _close(out, dev.out)
