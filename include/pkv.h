@@ -51,7 +51,7 @@ extern "C" {
 typedef enum pkv_status {
     PKV_OK = 0,
     PKV_ERR_INVALID_ARG = 1,    /* inconsistent or out-of-range host arguments */
-    PKV_ERR_UNSUPPORTED = 2,    /* valid, but a shape or alignment this build has no kernel for */
+    PKV_ERR_UNSUPPORTED = 2,    /* valid, but a shape or alignment the library has no kernel for */
     PKV_ERR_WORKSPACE = 3,      /* workspace missing or smaller than the minimum */
     PKV_ERR_CUDA = 4,           /* a CUDA runtime call failed (see pkv_last_cuda_error) */
     PKV_ERR_DEVICE_BOUNDS = 5   /* pkv_read_device_error found bounds violations */
