@@ -266,3 +266,62 @@ def test_fp8_combined_long_decodes_one_launch():
                                      m.block_table, spec.scale, threads())
     assert_close(got[torch.tensor(toks), torch.tensor(heads)], want, "fp8 combined long decodes")
     assert pkv.read_device_error(ws) == 0
+
+
+def _midpoint_rows(shape, seed):
+    """bf16 rows [N, Hkv, 128] whose quotients by their scale are exactly E4M3
+    rounding midpoints, where the code is decided by the tie rule alone.  A
+    row's largest magnitude is 7 * o * 2^(a+6), in [0.5, 2) (the size of the
+    other tests' values, so that the attention check's absolute tolerance
+    means the same), so its scale max/448 = o * 2^a is exact (o = 3, 5 or 7);
+    every other value is +-o * m * 2^p with m odd in 17..31, whose quotient
+    m * 2^(p-a) lies halfway between two neighbouring E4M3 values."""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    n, hkv, d = shape
+    rows = np.empty((n * hkv, d), dtype=np.float32)
+    for i in range(n * hkv):
+        o = int(rng.choice([3, 5, 7]))
+        a = int(rng.integers(0, 2)) - math.ceil(math.log2(7 * o)) - 6     # max in [0.5, 2)
+        ms = np.array([m for m in range(17, 32, 2) if o * m <= 255])
+        x = o * rng.choice(ms, d) * np.exp2(rng.integers(a - 4, a + 4, d))
+        x[rng.integers(0, d)] = 7 * o * 2.0 ** (a + 6)
+        rows[i] = x * np.where(rng.random(d) < 0.5, -1.0, 1.0)
+    return torch.from_numpy(rows).to(torch.bfloat16).view(n, hkv, d)
+
+
+def _share_on_midpoints(x):
+    """Share of the values of bf16 rows x [R, 128] whose quotient by the row's
+    scale (fp32, as the write computes it) is an E4M3 rounding midpoint: a
+    5-bit significand ending in a one, in E4M3's normal range."""
+    import numpy as np
+    f = x.to(torch.float32).numpy()
+    s = np.abs(f).max(axis=1, keepdims=True) / np.float32(448.0)
+    q = np.abs(f / s).astype(np.float32)
+    man, ex = np.frexp(q.astype(np.float64))                 # q = man * 2^ex, man in [0.5, 1)
+    sig = man * 32.0                                         # 5 significant bits
+    return float(np.mean((sig == np.round(sig)) & (np.round(sig) % 2 == 1) & (q >= 2.0 ** -6)))
+
+
+@pytest.mark.parametrize("mode", ["write", "combined"])
+def test_fp8_write_ties_on_rounding_midpoints(mode):
+    """Values whose quotient by the scale sits exactly halfway between two
+    E4M3 values: the quantizing write (and the combined call: decode CTAs and
+    the ranged scatter) takes the even code, bit for bit as the oracle."""
+    spec = random_spec(410, 6, 1500, 90, 32, 8, 128, pad_rows=1)
+    b = make_batch(spec, device="cpu")
+    b.k = _midpoint_rows(tuple(b.k.shape), 411)
+    b.v = _midpoint_rows(tuple(b.v.shape), 412)
+    assert _share_on_midpoints(b.k.view(-1, 128)) > 0.9
+    pools = _quantized_pools(b, 413)
+    if mode == "write":
+        got, dev_pools, err, ws = _run(b, pools)
+        assert pkv.read_device_error(err) == 0
+    else:
+        got, dev_pools, ws = _run_combined(b, pools)
+    want, ref_pools = _oracle(b, pools)
+    nbt = spec.num_blocks_total + 1
+    for d, r in zip(dev_pools, ref_pools):
+        assert torch.equal(d.cpu().view(nbt, -1)[:-1].view(torch.uint8), r.view(nbt, -1)[:-1].view(torch.uint8))
+    assert pkv.read_device_error(ws) == 0
+    assert_close(got, want, f"fp8 midpoint rows, {mode}")
