@@ -483,6 +483,34 @@ def time_workload(pkv, cfg, steps, warmup, device, peaks, dist=None, use_graph=T
         warm_ms = ev0.elapsed_time(ev1) / steps
         del g4
 
+    # Latency-bound workloads (inputs that fit in L2): the floor of one
+    # library launch, a graph of `steps` back-to-back 16-byte device copies
+    # (pkv_copy_async, each a programmatic dependent of the one before, as
+    # the step's launches are), reported beside the step.
+    floor_ms = None
+    if use_graph and len(copies) > 1:
+        a = torch.zeros(4, dtype=torch.int32, device=device)
+        b_ = torch.ones(4, dtype=torch.int32, device=device)
+        side5 = torch.cuda.Stream()
+        side5.wait_stream(stream)
+        with torch.cuda.stream(side5):
+            pkv.copy_async(a, b_, stream=side5)
+        torch.cuda.synchronize()
+        g5 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g5, stream=side5):
+            for i in range(steps):
+                pkv.copy_async(a if i % 2 else b_, b_ if i % 2 else a, stream=side5)
+        torch.cuda.synchronize()
+        upload_graph(g5, stream)
+        g5.replay()
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        g5.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        floor_ms = ev0.elapsed_time(ev1) / steps
+        del g5
+
     per_replay_ms = None
     if per_graphs:
         n = max(len(per_graphs), min(steps, 200))
@@ -590,6 +618,7 @@ def time_workload(pkv, cfg, steps, warmup, device, peaks, dist=None, use_graph=T
         "ms_per_step_one_graph_per_step": per_replay_ms,
         "ms_per_step_two_calls": two_calls_ms,
         "step_us_warm_l2": warm_ms * 1e3 if warm_ms is not None else None,
+        "launch_floor_us": floor_ms * 1e3 if floor_ms is not None else None,
         "kernels": kernels, "roofline": roof, "timed_wall": (t_wall0, t_wall1),
     }
     return spec, copies, res
@@ -1110,6 +1139,7 @@ def run_ours(args):
         "step_us_one_graph_per_step": (head["ms_per_step_one_graph_per_step"] * 1e3
                                        if head["ms_per_step_one_graph_per_step"] is not None else None),
         "step_us_warm_l2": head["step_us_warm_l2"],
+        "launch_floor_us": head["launch_floor_us"],
         "kv_read_gbs": head["kv_read_gbs"],
         "kv_read_frac_of_8tbs": head["kv_read_frac_of_8tbs"],
         "step_tensor_frac": head["step_tensor_frac"], "step_hbm_frac": head["step_hbm_frac"],

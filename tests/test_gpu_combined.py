@@ -47,6 +47,25 @@ def test_small_configs(cfg):
     _run(config_spec(cfg), what=f"config {cfg}")
 
 
+def test_layout_example_is_one_launch():
+    """The pages' layout example ("Flattened ragged batches": a 3-token chunk,
+    two decodes and a 4-token prompt, g = 2) as one combined call is one
+    library launch: its chunks are short enough for the decode kernel (at
+    most 16/g tokens), whose CTAs write their own rows.  A second call writes
+    the same rows again, so pools and output are checked after it."""
+    b = make_batch(config_spec(1), device="cpu")
+    ref = cpu_copy(b)
+    oracle_write(ref)
+    dev = DeviceStep(b)
+    dev.combined()                       # the first call also sets kernel attributes
+    torch.cuda.synchronize()
+    before = pkv.launch_count()
+    dev.combined()
+    torch.cuda.synchronize()
+    assert pkv.launch_count() - before == 1
+    _check(dev, ref, 0, "layout example, one launch")
+
+
 @pytest.mark.parametrize("env", ["default", "no-overlap", "decode-side", "no-cluster", "separate", "no-tcgen05"])
 def test_engine_step_arrangements(env, attn_options):
     """The 48-request engine step under every stream and kernel arrangement."""
