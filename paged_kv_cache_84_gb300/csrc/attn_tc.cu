@@ -16,6 +16,12 @@
 //               V tiles, each into a 2-stage ring (a K stage is refilled once
 //               both S MMAs that read it are done, a V stage once both PV
 //               MMAs are done); a tile's 16 boxes go out from 16 lanes at once;
+//   warps 3..11 combined write + attention calls: when this CTA is the only
+//               one of its request and KV head (one pair of tiles, uncut),
+//               they first write the request's new K/V rows of that head
+//               into the pool and signal the producers, which wait for it
+//               before the first key tile that holds a new row (the other
+//               requests' rows come from a scatter ahead of the launch);
 //   warp 1      MMA issuer (one thread) and TMEM owner; per key tile it
 //               issues PV_a(j-1), S_a(j), PV_b(j-1), S_b(j), so the tensor
 //               core always has the other tile's work while a softmax runs;
@@ -103,7 +109,8 @@ enum TcBar {
     kBarOA = 9, kBarOB = 10,          // PV of tile a / b done (also frees a V stage)
     kBarMmaDone = 11,
     kBarOFin = 12,                    // single tile: every PV done (one phase)
-    kNumTcBars = 13
+    kBarW = 13,                       // the CTA's own new K/V rows are in the pool (one phase)
+    kNumTcBars = 14
 };
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
@@ -439,6 +446,44 @@ __device__ __forceinline__ void tc_decode_cta(const AttnParams &pd, const WorkLi
 // first mix->dec_rows grid rows are decode CTAs (list dl, parameters pd,
 // the pool's maps dm), the tcgen05 prefill CTAs follow.
 constexpr int kMixBf16 = 1, kMixFp8 = 2;
+// Warps 3 .. 11 write a single-CTA request's new rows (combined call).
+constexpr uint32_t kOwnRowWarps = 9;
+
+// The new rows of request r (t tokens at positions L - t .. L - 1, token
+// rows b ..) of KV head kh into the pools at fw_slots[row], as
+// fused_kv_write does (a negative slot: the scratch slot; one outside the
+// pool: skipped, bit 1; one other than the block table's: kDevErrMeta), by
+// threads tid of nthreads.  A thread loads its rows' K and V before their
+// slot, so its loads overlap; it fences its stores against the async proxy.
+template <int D>
+__device__ __forceinline__ void tc_own_rows(const AttnParams &p, int r, int b, int t, int L, int kh, int tid,
+                                            int nthreads)
+{
+    constexpr int kVec = D * 2 / 16;                      // 16-byte vectors of one row and head
+    const int64_t num_slots = (int64_t)p.nb_total * p.block_size;
+    const int32_t *bt = p.block_table + (size_t)r * p.bt_stride;
+    for (int idx = tid; idx < t * kVec; idx += nthreads) {
+        const int i = idx / kVec, c = idx - i * kVec;
+        const int row = b + i, pos = L - t + i;
+        const size_t src = ((size_t)row * p.hkv + kh) * kVec + c;
+        const uint4 kx = p.fw_k[src], vx = p.fw_v[src];
+        int64_t slot = __ldg(p.fw_slots + row);
+        if (c == 0 && slot >= 0) {
+            const int64_t want = (int64_t)__ldg(bt + (pos >> 4)) * 16 + (pos & 15);
+            if (slot != want) atomicOr(p.err, kDevErrMeta);
+        }
+        if (slot < 0) slot = num_slots - 1;               // padding row -> scratch slot
+        if (slot >= num_slots) {
+            if (c == 0) atomicOr(p.err, 1u);
+            continue;
+        }
+        const size_t dst = ((size_t)slot * p.hkv + kh) * kVec + c;
+        p.fw_kc[dst] = kx;
+        p.fw_vc[dst] = vx;
+    }
+    fence_proxy_async_global();
+}
+
 template <int DP, int D, bool WIN, int MIX>
 __device__ __forceinline__ void attn_tc_body(const AttnParams &p, const WorkList &wl, const CUtensorMap &qmap,
                                              const CUtensorMap &kmap, const CUtensorMap &vmap, int64_t num_slots,
@@ -500,6 +545,12 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams &p, const WorkList
         pieces > 1 ? p.counters + (size_t)(wl.cnt_off[li] + split_idx * p.hkv + kh) * kCounterStride : nullptr;
     uint32_t *const s_piece = tmem_slot + 1;                       // two flag words after the TMEM address
     const int wspan = win_span(p.window);                          // keys <= position - wspan are outside
+    // Combined call (p.fw_k set): a request whose rows of this KV head are
+    // all one CTA's (a single pair, uncut) has its new rows written by that
+    // CTA's warps 3 .. 11, not by a scatter ahead of the launch; the
+    // producers wait for them before the first key tile that holds one.
+    const bool self_write = p.fw_k != nullptr && npairs == 1 && pieces == 1;
+    const int first_new_tile = (L - t) / kTcKeys;                  // key tile of position L - t
 
     if (threadIdx.x == 0) {
         // P of tile a comes from 8 warps when a single tile splits its rows;
@@ -507,7 +558,7 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams &p, const WorkList
         // (odd j): a warp may start tile j+1 (its S is double-buffered)
         // before every warp has arrived for tile j
         for (int i = 0; i < kNumTcBars; i++)
-            mbar_init(bar(i), (i == kBarPA || i == kBarPB) ? (has_b ? 4u : 8u) : 1u);
+            mbar_init(bar(i), (i == kBarPA || i == kBarPB) ? (has_b ? 4u : 8u) : i == kBarW ? kOwnRowWarps : 1u);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -518,6 +569,16 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams &p, const WorkList
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+
+    if (self_write && warp >= 3) {
+        // ------------------------------------------------------------ own rows (combined call)
+        // warp 3 and the softmax warps, which have nothing to do before the
+        // first S: the request's new rows of this KV head into the pool
+        pdl_wait();                                                // k, v and slot_mapping come from before
+        tc_own_rows<D>(p, r, b, t, L, kh, threadIdx.x - 96, kOwnRowWarps * 32);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarW));
+    }
 
     if (warp == 0 || warp == 2) {
         // ------------------------------------------------------------ TMA producers
@@ -553,6 +614,7 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams &p, const WorkList
         // 32 block ids are read while that kernel may still be running
         int ids = lane < nblk ? __ldg(bt + lane) : INT_MIN, issued = 0;
         pdl_wait();                                                // the step's K/V rows are in the pool
+        bool rows_in = !self_write;
         for (int j = 0; j < nkt; j++) {
             const int st = j & 1;
             if ((j & 3) == 0 && j > 0) {                           // 32 block ids = 4 key tiles
@@ -575,6 +637,11 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams &p, const WorkList
             if (j >= 2)
                 ok = (is_k && !has_b) ? mbar_wait(bar(kBarSA + (j & 1)), ((j - 2) >> 1) & 1, p.err)
                                       : mbar_wait(bar(done_bar), (j - 2) & 1, p.err);
+            if (!rows_in && jt0 + j >= first_new_tile) {           // this tile holds new rows: wait for them
+                ok = mbar_wait(bar(kBarW), 0, p.err) && ok;
+                fence_proxy_async_global();
+                rows_in = true;
+            }
             if (!__all_sync(0xffffffffu, ok)) break;
             issued = j + 1;
             if (lane == 0) mbar_arrive_expect_tx(bar(full0 + st), kTile);

@@ -1172,9 +1172,26 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
     };
 
     // ---- combined call: the prefill-class rows are scattered ahead of the
-    // prefill kernels, on their stream (the decode class writes its own)
+    // prefill kernels, on their stream (the decode class writes its own, and
+    // so does the tcgen05 CTA of a bf16 request whose rows of a KV head are
+    // all that one CTA's: a single pair of tiles, not cut into key pieces)
+    std::vector<char> tc_self(tcp.size(), 0);
+    bool any_self = false;
+    if (fused && !fp8) {
+        const int tt = tc_prefill_rows() / g;
+        for (size_t x = 0; x < tcp.size(); x++) {
+            const int32_t t = qsl_h[tcp[x] + 1] - qsl_h[tcp[x]];
+            const int npairs = (t + 2 * tt - 1) / (2 * tt);
+            const int whole = tc_split_whole(pl.tc_split[x]), pieces = tc_split_pieces(pl.tc_split[x]);
+            const int ctas = pieces > 1 ? whole + (npairs - whole) * pieces : npairs;
+            tc_self[x] = ctas == 1;
+            any_self = any_self || ctas == 1;
+        }
+    }
     if (fused) {
-        std::vector<int32_t> prows(tcp);
+        std::vector<int32_t> prows;
+        for (size_t x = 0; x < tcp.size(); x++)
+            if (!tc_self[x]) prows.push_back(tcp[x]);
         prows.insert(prows.end(), pre.begin(), pre.end());
         for (size_t c0 = 0; c0 < prows.size(); c0 += kPlanMax) {
             TokenRanges rg;
@@ -1208,6 +1225,13 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
 
     // ---- quantized pools: bf16 copies of the tcgen05 requests' blocks
     AttnParams pt = pp;                                  // the tcgen05 launches' parameters
+    if (any_self) {                                      // their single-CTA requests write their own rows
+        pt.fw_k = p.fw_k;
+        pt.fw_v = p.fw_v;
+        pt.fw_kc = p.fw_kc;
+        pt.fw_vc = p.fw_vc;
+        pt.fw_slots = p.fw_slots;
+    }
     const void *tc_k = k_cache, *tc_v = v_cache;
     int64_t tc_slots = num_slots;
     if (fp8_scratch && !tcp.empty()) {

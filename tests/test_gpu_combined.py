@@ -66,6 +66,36 @@ def test_layout_example_is_one_launch():
     _check(dev, ref, 0, "layout example, one launch")
 
 
+def test_engine_step_chunks_write_their_own_rows():
+    """The 48-request engine step: every prefill chunk (at most 64 tokens,
+    g = 2: one pair of 128-row tiles per KV head) is one tcgen05 CTA per KV
+    head, which writes the chunk's new rows itself, so the call is two
+    launches (the tcgen05 prefill and the decode kernel), no scatter."""
+    b = make_batch(config_spec(2), device="cpu")
+    ref = cpu_copy(b)
+    oracle_write(ref)
+    dev = DeviceStep(b)
+    dev.combined()
+    torch.cuda.synchronize()
+    before = pkv.launch_count()
+    dev.combined()
+    torch.cuda.synchronize()
+    assert pkv.launch_count() - before == 2
+    _check(dev, ref, 0, "engine step, chunks writing their own rows")
+
+
+@pytest.mark.parametrize("t", [1, 40, 64, 65, 130])
+def test_chunk_rows_written_by_its_own_cta_or_the_scatter(t):
+    """Chunks of t tokens (g = 4: 32 tokens per tile, 64 per pair) beside a
+    decode: up to 64 tokens one tcgen05 CTA per KV head writes the chunk's
+    rows (its first new key tile after older ones, or the first tile), above
+    it the scatter does; pools bit-exact, attention within tolerance."""
+    hq, hkv, d = 32, 8, 128
+    reqs = [Req(300, t, list(range(0, 30))), Req(900, 1, list(range(30, 88))), Req(0, t, list(range(88, 98)))]
+    spec = Spec(f"self-write-{t}", reqs, hq, hkv, d, 16, 120, 1 / math.sqrt(d), 61 + t)
+    _run(spec, what=f"chunks of {t}")
+
+
 @pytest.mark.parametrize("env", ["default", "no-overlap", "decode-side", "no-cluster", "separate", "no-tcgen05"])
 def test_engine_step_arrangements(env, attn_options):
     """The 48-request engine step under every stream and kernel arrangement."""
