@@ -316,8 +316,10 @@ pkv_status pkv_ragged_paged_attention_ex(void *out, const void *q, const void *k
  * same arguments, bf16 pools.  The work is arranged differently: the CTAs
  * that attend for a decode-class request (t * g <= 16 rows per KV head)
  * write that request's new rows themselves, each the rows in its key range,
- * just before reading them, and a scatter restricted to the prefill-class
- * requests' rows runs ahead of the prefill kernels; so decode attention
+ * just before reading them; so does the tensor-core CTA of a prefill
+ * request whose rows of a KV head are all that one CTA's (t * g <= 256,
+ * not cut into key pieces); a scatter restricted to the other prefill-class
+ * requests' rows runs ahead of the prefill kernels.  So decode attention
  * does not wait for a scatter, and a batch of decodes is one launch.
  *
  *   k, v          device bf16 [num_tokens][num_kv_heads][head_dim], 16-byte
