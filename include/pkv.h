@@ -318,7 +318,8 @@ pkv_status pkv_ragged_paged_attention_ex(void *out, const void *q, const void *k
  * write that request's new rows themselves, each the rows in its key range,
  * just before reading them; so does the tensor-core CTA of a prefill
  * request whose rows of a KV head are all that one CTA's (t * g <= 256,
- * not cut into key pieces); a scatter restricted to the other prefill-class
+ * not cut into key pieces, the prefill not in one launch with the
+ * decodes); a scatter restricted to the other prefill-class
  * requests' rows runs ahead of the prefill kernels.  So decode attention
  * does not wait for a scatter, and a batch of decodes is one launch.
  *

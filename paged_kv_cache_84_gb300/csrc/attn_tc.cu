@@ -20,8 +20,9 @@
 //               one of its request and KV head (one pair of tiles, uncut),
 //               they first write the request's new K/V rows of that head
 //               into the pool and signal the producers, which wait for it
-//               before the first key tile that holds a new row (the other
-//               requests' rows come from a scatter ahead of the launch);
+//               before the first key tile that holds a new row (plain
+//               launches only; the other requests' rows, and a mixed
+//               launch's, come from a scatter ahead of the launch);
 //   warp 1      MMA issuer (one thread) and TMEM owner; per key tile it
 //               issues PV_a(j-1), S_a(j), PV_b(j-1), S_b(j), so the tensor
 //               core always has the other tile's work while a softmax runs;
@@ -109,8 +110,8 @@ enum TcBar {
     kBarOA = 9, kBarOB = 10,          // PV of tile a / b done (also frees a V stage)
     kBarMmaDone = 11,
     kBarOFin = 12,                    // single tile: every PV done (one phase)
-    kBarW = 13,                       // the CTA's own new K/V rows are in the pool (one phase)
-    kNumTcBars = 14
+    kNumTcBars = 13,
+    kBarW = 13                        // OWN launches only: the CTA's own new K/V rows are in the pool
 };
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
@@ -484,7 +485,7 @@ __device__ __forceinline__ void tc_own_rows(const AttnParams &p, int r, int b, i
     fence_proxy_async_global();
 }
 
-template <int DP, int D, bool WIN, int MIX>
+template <int DP, int D, bool WIN, int MIX, bool OWN>
 __device__ __forceinline__ void attn_tc_body(const AttnParams &p, const WorkList &wl, const CUtensorMap &qmap,
                                              const CUtensorMap &kmap, const CUtensorMap &vmap, int64_t num_slots,
                                              const AttnParams *pd, const WorkList *dl, const MixAssign *mix,
@@ -506,7 +507,8 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams &p, const WorkList
     const uint32_t sb = (raw + 1023u) & ~1023u;
     uint8_t *sp = smem_raw + (sb - raw);
     auto bar = [&](int i) { return sb + kBarOff + 8u * i; };
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sp + kBarOff + 8 * kNumTcBars);
+    constexpr int kBars = OWN ? kNumTcBars + 1 : kNumTcBars;      // kBarW after the others
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sp + kBarOff + 8 * kBars);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kh = blockIdx.x;                                     // all KV heads of an item are adjacent
@@ -549,8 +551,8 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams &p, const WorkList
     // all one CTA's (a single pair, uncut) has its new rows written by that
     // CTA's warps 3 .. 11, not by a scatter ahead of the launch; the
     // producers wait for them before the first key tile that holds one.
-    const bool self_write = p.fw_k != nullptr && npairs == 1 && pieces == 1;
-    const int first_new_tile = (L - t) / kTcKeys;                  // key tile of position L - t
+    const bool self_write = OWN && p.fw_k != nullptr && npairs == 1 && pieces == 1;
+    [[maybe_unused]] const int first_new_tile = (L - t) / kTcKeys; // key tile of position L - t
 
     if (threadIdx.x == 0) {
         // P of tile a comes from 8 warps when a single tile splits its rows;
@@ -558,7 +560,8 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams &p, const WorkList
         // (odd j): a warp may start tile j+1 (its S is double-buffered)
         // before every warp has arrived for tile j
         for (int i = 0; i < kNumTcBars; i++)
-            mbar_init(bar(i), (i == kBarPA || i == kBarPB) ? (has_b ? 4u : 8u) : i == kBarW ? kOwnRowWarps : 1u);
+            mbar_init(bar(i), (i == kBarPA || i == kBarPB) ? (has_b ? 4u : 8u) : 1u);
+        if constexpr (OWN) mbar_init(bar(kBarW), kOwnRowWarps);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -570,14 +573,16 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams &p, const WorkList
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (self_write && warp >= 3) {
-        // ------------------------------------------------------------ own rows (combined call)
-        // warp 3 and the softmax warps, which have nothing to do before the
-        // first S: the request's new rows of this KV head into the pool
-        pdl_wait();                                                // k, v and slot_mapping come from before
-        tc_own_rows<D>(p, r, b, t, L, kh, threadIdx.x - 96, kOwnRowWarps * 32);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarW));
+    if constexpr (OWN) {
+        if (self_write && warp >= 3) {
+            // -------------------------------------------------------- own rows (combined call)
+            // warp 3 and the softmax warps, which have nothing to do before
+            // the first S: the request's new rows of this KV head into the pool
+            pdl_wait();                                            // k, v and slot_mapping come from before
+            tc_own_rows<D>(p, r, b, t, L, kh, threadIdx.x - 96, kOwnRowWarps * 32);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarW));
+        }
     }
 
     if (warp == 0 || warp == 2) {
@@ -614,7 +619,7 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams &p, const WorkList
         // 32 block ids are read while that kernel may still be running
         int ids = lane < nblk ? __ldg(bt + lane) : INT_MIN, issued = 0;
         pdl_wait();                                                // the step's K/V rows are in the pool
-        bool rows_in = !self_write;
+        [[maybe_unused]] bool rows_in = !self_write;
         for (int j = 0; j < nkt; j++) {
             const int st = j & 1;
             if ((j & 3) == 0 && j > 0) {                           // 32 block ids = 4 key tiles
@@ -637,10 +642,12 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams &p, const WorkList
             if (j >= 2)
                 ok = (is_k && !has_b) ? mbar_wait(bar(kBarSA + (j & 1)), ((j - 2) >> 1) & 1, p.err)
                                       : mbar_wait(bar(done_bar), (j - 2) & 1, p.err);
-            if (!rows_in && jt0 + j >= first_new_tile) {           // this tile holds new rows: wait for them
-                ok = mbar_wait(bar(kBarW), 0, p.err) && ok;
-                fence_proxy_async_global();
-                rows_in = true;
+            if constexpr (OWN) {
+                if (!rows_in && jt0 + j >= first_new_tile) {       // this tile holds new rows: wait for them
+                    ok = mbar_wait(bar(kBarW), 0, p.err) && ok;
+                    fence_proxy_async_global();
+                    rows_in = true;
+                }
             }
             if (!__all_sync(0xffffffffu, ok)) break;
             issued = j + 1;
@@ -890,14 +897,17 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams &p, const WorkList
     }
 }
 
-template <int DP, int D, bool WIN>
+// OWN: combined calls whose single-CTA requests write their own rows (a
+// separate instantiation, so that the other launches' code is not touched
+// by the writers' prologue).
+template <int DP, int D, bool WIN, bool OWN>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnParams p, const __grid_constant__ WorkList wl,
                                                                 const __grid_constant__ CUtensorMap qmap,
                                                                 const __grid_constant__ CUtensorMap kmap,
                                                                 const __grid_constant__ CUtensorMap vmap,
                                                                 int64_t num_slots)
 {
-    attn_tc_body<DP, D, WIN, 0>(p, wl, qmap, kmap, vmap, num_slots, nullptr, nullptr, nullptr, nullptr);
+    attn_tc_body<DP, D, WIN, 0, OWN>(p, wl, qmap, kmap, vmap, num_slots, nullptr, nullptr, nullptr, nullptr);
 }
 
 template <int DP, int D, bool WIN, int MIX>
@@ -907,7 +917,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                        int64_t num_slots, AttnParams pd, const __grid_constant__ WorkList dl,
                        const __grid_constant__ MixAssign mix, const __grid_constant__ DecodeMaps dm)
 {
-    attn_tc_body<DP, D, WIN, MIX>(p, wl, qmap, kmap, vmap, num_slots, &pd, &dl, &mix, &dm);
+    attn_tc_body<DP, D, WIN, MIX, false>(p, wl, qmap, kmap, vmap, num_slots, &pd, &dl, &mix, &dm);
 }
 
 // ---------------------------------------------------------------- host side
@@ -933,7 +943,11 @@ static cudaError_t launch_tc_d(const AttnParams &p, const WorkList &wl, int num_
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(attn_tc_kernel<DP, D, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        attr_err = cudaFuncSetAttribute(attn_tc_kernel<DP, D, WIN, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        smem);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(attn_tc_kernel<DP, D, WIN, true>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (attr_err == cudaSuccess)
             attr_err = cudaFuncSetAttribute(attn_tc_mix_kernel<DP, D, WIN, kMixBf16>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem_mix);
@@ -944,6 +958,7 @@ static cudaError_t launch_tc_d(const AttnParams &p, const WorkList &wl, int num_
     if (attr_err != cudaSuccess) return attr_err;
     const bool fp8_dec = mix && pd->k_scale != nullptr;
     if (fp8_dec && !kHasF8) return cudaErrorInvalidValue;
+    if (mix && p.fw_k) return cudaErrorInvalidValue;                // a mixed launch's chunks come from the scatter
     CUtensorMap qm, km, vm;
     // 64-column boxes; for D < 64 they reach past the row and TMA fills zeros
     cudaError_t e = make_q_tmap(&qm, q, num_tokens, p.hq, D, p.group);
@@ -974,9 +989,12 @@ static cudaError_t launch_tc_d(const AttnParams &p, const WorkList &wl, int num_
     else if (mix)
         e = launch_maybe_pdl(attn_tc_mix_kernel<DP, D, WIN, kMixBf16>, grid, dim3(kTcThreads), smem_mix, stream, p,
                              wl, qm, km, vm, num_slots, *pd, *dl, *mix, dm);
+    else if (p.fw_k)
+        e = launch_maybe_pdl(attn_tc_kernel<DP, D, WIN, true>, grid, dim3(kTcThreads), smem, stream, p, wl, qm, km,
+                             vm, num_slots);
     else
-        e = launch_maybe_pdl(attn_tc_kernel<DP, D, WIN>, grid, dim3(kTcThreads), smem, stream, p, wl, qm, km, vm,
-                             num_slots);
+        e = launch_maybe_pdl(attn_tc_kernel<DP, D, WIN, false>, grid, dim3(kTcThreads), smem, stream, p, wl, qm, km,
+                             vm, num_slots);
     launch_end(stream);
     return e != cudaSuccess ? e : cudaGetLastError();
 }

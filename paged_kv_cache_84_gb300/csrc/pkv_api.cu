@@ -1174,10 +1174,11 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
     // ---- combined call: the prefill-class rows are scattered ahead of the
     // prefill kernels, on their stream (the decode class writes its own, and
     // so does the tcgen05 CTA of a bf16 request whose rows of a KV head are
-    // all that one CTA's: a single pair of tiles, not cut into key pieces)
+    // all that one CTA's: a single pair of tiles, not cut into key pieces,
+    // outside a mixed launch)
     std::vector<char> tc_self(tcp.size(), 0);
     bool any_self = false;
-    if (fused && !fp8) {
+    if (fused && !fp8 && !pl.mix) {
         const int tt = tc_prefill_rows() / g;
         for (size_t x = 0; x < tcp.size(); x++) {
             const int32_t t = qsl_h[tcp[x] + 1] - qsl_h[tcp[x]];
