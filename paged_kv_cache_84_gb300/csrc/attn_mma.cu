@@ -518,35 +518,41 @@ __global__ void __launch_bounds__((CW + 1) * 32) attn_mma_kernel(AttnParams p, c
             __syncwarp();
             fence_proxy_async_global();                           // lane 0 issues the loads
         }
-        for (int i = 0; i < nblk; i++) {
-            if ((i & 31) == 0 && i > 0) ids = (i + lane < nblk) ? __ldg(bt + i + lane) : 0;
+        // a block's K and V slices of this head into slot s, and for FP8
+        // pools the block's K and V scales of this head's group of four
+        auto issue = [&](int s, int blk) {
+            if (blk < 0 || blk >= p.nb_total) {                   // outside the pool: report, read block 0
+                atomicOr(p.err, 2u);
+                blk = 0;
+            }
+            mbar_arrive_expect_tx(full_bar(s), T::kData);
+            const uint32_t dst = slot_addr(s);
+#pragma unroll
+            for (int x = 0; x < T::kBoxes; x++) {
+                tma_load_3d(dst + x * T::kBoxBytes, &kmap, full_bar(s), x * T::kBoxCols, kh, blk * 16);
+                tma_load_3d(dst + T::kTile + x * T::kBoxBytes, &vmap, full_bar(s), x * T::kBoxCols, kh, blk * 16);
+            }
+            if constexpr (FP8) {
+                tma_load_2d(dst + 2 * T::kTile, &ksmap, full_bar(s), kh & ~(kScaleHeads - 1), blk * 16);
+                tma_load_2d(dst + 2 * T::kTile + T::kScaleTile, &vsmap, full_bar(s), kh & ~(kScaleHeads - 1),
+                            blk * 16);
+            }
+        };
+        // the ring's first round goes out from one lane per block at once;
+        // later blocks, one at a time, as slots come free
+        const int first = min(nblk, R < 32 ? R : 32);
+        if (lane < first) issue(lane, ids);
+        __syncwarp();
+        issued = first;
+        for (int i = first; i < nblk; i++) {
+            if ((i & 31) == 0) ids = (i + lane < nblk) ? __ldg(bt + i + lane) : 0;
             const int s = i % R;
             bool ok = true;
             if (i >= R) ok = mbar_wait(empty_bar(s), ((i / R) - 1) & 1, p.err);
             if (!__all_sync(0xffffffffu, ok)) break;
             issued = i + 1;
-            int blk = __shfl_sync(0xffffffffu, ids, i & 31);
-            if (lane == 0) {
-                if (blk < 0 || blk >= p.nb_total) {               // outside the pool: report, read block 0
-                    atomicOr(p.err, 2u);
-                    blk = 0;
-                }
-                // a block's K and V slices of this head, and for FP8 pools the
-                // block's K and V scales of this head's group of four
-                mbar_arrive_expect_tx(full_bar(s), T::kData);
-                const uint32_t dst = slot_addr(s);
-#pragma unroll
-                for (int x = 0; x < T::kBoxes; x++) {
-                    tma_load_3d(dst + x * T::kBoxBytes, &kmap, full_bar(s), x * T::kBoxCols, kh, blk * 16);
-                    tma_load_3d(dst + T::kTile + x * T::kBoxBytes, &vmap, full_bar(s), x * T::kBoxCols, kh,
-                                blk * 16);
-                }
-                if constexpr (FP8) {
-                    tma_load_2d(dst + 2 * T::kTile, &ksmap, full_bar(s), kh & ~(kScaleHeads - 1), blk * 16);
-                    tma_load_2d(dst + 2 * T::kTile + T::kScaleTile, &vsmap, full_bar(s), kh & ~(kScaleHeads - 1),
-                                blk * 16);
-                }
-            }
+            const int blk = __shfl_sync(0xffffffffu, ids, i & 31);
+            if (lane == 0) issue(s, blk);
             __syncwarp();
         }
         // Normally every issued block has been consumed by now.  If a wait
