@@ -563,6 +563,7 @@ typedef struct pkv_attention_plan {
     int32_t mixed_decode_items;       /* ... how many */
     int32_t mixed_decode_ctas;        /* ... on how many decode CTAs ahead of the prefill CTAs */
     int32_t mixed_predicted_us;       /* ... the planner's estimate of its time, us (0 when forced) */
+    int32_t prefill_tensor_own_rows;  /* combined call: tcgen05 requests whose CTAs write their new rows */
 } pkv_attention_plan;
 pkv_status pkv_plan_attention(const int32_t *query_start_loc_host, const int32_t *seq_lens_host,
                               int32_t num_reqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,

@@ -46,7 +46,7 @@ class _Plan(ctypes.Structure):
                 ("prefill_key_splits", _c_i32), ("prefill_tensor_pieces", _c_i32),
                 ("quantized_prefill_scratch", _c_sz), ("partial_bytes", _c_sz), ("mixed_launch", _c_i32),
                 ("mixed_decode_items", _c_i32), ("mixed_decode_ctas", _c_i32),
-                ("mixed_predicted_us", _c_i32)]
+                ("mixed_predicted_us", _c_i32), ("prefill_tensor_own_rows", _c_i32)]
 
 
 class AttentionOptions(ctypes.Structure):

@@ -629,6 +629,9 @@ struct AttnPlan {
     int32_t mix_items = 0;              // decode items (request, split, KV head)
     int32_t mix_dec_rows = 0;           // grid rows of decode CTAs ahead of the prefill (x hkv CTAs)
     double mix_pred_us = 0.0;           // the planner's time of the mixed launch
+    // combined call: per tcgen05 request, whether its CTAs write its new rows
+    // (each KV head's rows are one CTA's), so that no scatter does
+    std::vector<char> tc_self;
 };
 
 // ---- tcgen05 prefill: key pieces
@@ -977,6 +980,7 @@ static AttnPlan make_plan(const int32_t *qsl_h, const int32_t *sl_h, int32_t num
             best_plan.mix_items = (int32_t)items;
             best_plan.mix_dec_rows = best_rows;
             best_plan.mix_pred_us = best;
+            best_plan.tc_self.assign(best_plan.rc.tcp.size(), 0);   // a mixed launch's chunks come from the scatter
             return best_plan;
         }
     }
@@ -999,6 +1003,19 @@ static AttnPlan make_plan(const int32_t *qsl_h, const int32_t *sl_h, int32_t num
         // on the mixed 2048-token-chunk step: 514 us this way, 570 us with
         // the decodes starting at once).
         pl.fork_after_scatter = fused && !pl.decode_main;
+    }
+    // Combined call on a bf16 pool, outside a mixed launch: a tcgen05 request
+    // whose rows of each KV head are all one CTA's (a single pair of tiles,
+    // not cut into key pieces) has its new rows written by that CTA.
+    pl.tc_self.assign(rc.tcp.size(), 0);
+    if (fused && !fp8 && !pl.mix) {
+        const int tt = tc_prefill_rows() / g;
+        for (size_t x = 0; x < rc.tcp.size(); x++) {
+            const int32_t t = qsl_h[rc.tcp[x] + 1] - qsl_h[rc.tcp[x]];
+            const int npairs = (t + 2 * tt - 1) / (2 * tt);
+            const int whole = tc_split_whole(pl.tc_split[x]), pieces = tc_split_pieces(pl.tc_split[x]);
+            pl.tc_self[x] = (pieces > 1 ? whole + (npairs - whole) * pieces : npairs) == 1;
+        }
     }
     return pl;
 }
@@ -1176,23 +1193,12 @@ static pkv_status attention_impl(void *out, const void *q, const void *k_cache, 
     // so does the tcgen05 CTA of a bf16 request whose rows of a KV head are
     // all that one CTA's: a single pair of tiles, not cut into key pieces,
     // outside a mixed launch)
-    std::vector<char> tc_self(tcp.size(), 0);
-    bool any_self = false;
-    if (fused && !fp8 && !pl.mix) {
-        const int tt = tc_prefill_rows() / g;
-        for (size_t x = 0; x < tcp.size(); x++) {
-            const int32_t t = qsl_h[tcp[x] + 1] - qsl_h[tcp[x]];
-            const int npairs = (t + 2 * tt - 1) / (2 * tt);
-            const int whole = tc_split_whole(pl.tc_split[x]), pieces = tc_split_pieces(pl.tc_split[x]);
-            const int ctas = pieces > 1 ? whole + (npairs - whole) * pieces : npairs;
-            tc_self[x] = ctas == 1;
-            any_self = any_self || ctas == 1;
-        }
-    }
+    const std::vector<char> &tc_self = pl.tc_self;
+    const bool any_self = std::find(tc_self.begin(), tc_self.end(), 1) != tc_self.end();
     if (fused) {
         std::vector<int32_t> prows;
         for (size_t x = 0; x < tcp.size(); x++)
-            if (!tc_self[x]) prows.push_back(tcp[x]);
+            if (x >= tc_self.size() || !tc_self[x]) prows.push_back(tcp[x]);
         prows.insert(prows.end(), pre.begin(), pre.end());
         for (size_t c0 = 0; c0 < prows.size(); c0 += kPlanMax) {
             TokenRanges rg;
@@ -1570,6 +1576,7 @@ pkv_status pkv_plan_attention(const int32_t *qsl_h, const int32_t *sl_h, int32_t
     out->mixed_decode_items = pl.mix ? pl.mix_items : 0;
     out->mixed_decode_ctas = pl.mix ? pl.mix_dec_rows * hkv : 0;
     out->mixed_predicted_us = pl.mix ? (int32_t)std::lround(pl.mix_pred_us) : 0;
+    out->prefill_tensor_own_rows = (int32_t)std::count(pl.tc_self.begin(), pl.tc_self.end(), 1);
     if (pl.mix) {
         out->decode_cluster = 0;
         out->decode_streaming = 0;

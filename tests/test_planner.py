@@ -117,6 +117,30 @@ def test_engine_step_overlaps_classes_with_clusters_of_two():
     assert p["partial_bytes"] > 0                               # reserved, although clusters merge on chip
 
 
+def test_chunks_that_are_one_cta_per_kv_head_write_their_own_rows():
+    """Combined call, bf16 pool: a tcgen05 request whose rows of each KV
+    head fit one pair of 128-row tiles (t * g <= 256) and are not cut into
+    key pieces is written by its own CTAs, not by the scatter; never on a
+    quantized pool, in a mixed launch, or outside the combined call."""
+    p = plan(2, combined=True)
+    assert p["prefill_tensor_own_rows"] == p["prefill_tensor_requests"] == 16   # chunks of <= 64 tokens, g = 2
+    assert plan(2, combined=False)["prefill_tensor_own_rows"] == 0
+    assert plan(4, mixed=0, combined=True)["prefill_tensor_own_rows"] == 0       # one mixed launch
+    assert plan(4, combined=True)["prefill_tensor_own_rows"] == 0                # 2048- and 1024-token chunks
+    # g = 4: 64 tokens per pair; a 64-token and a 65-token chunk beside a decode
+    for t, own in ((64, 1), (65, 0)):
+        qsl, sl = [0, t, t + 1], [300 + t, 900]
+        q = pkv.plan_attention(qsl, sl, 32, 8, 128, combined=True, num_sms=SMS, workspace_bytes=BIG_WS)
+        assert (q["prefill_tensor_requests"], q["prefill_tensor_own_rows"]) == (1, own), t
+        q = pkv.plan_attention(qsl, sl, 32, 8, 128, quantized=True, combined=True, num_sms=SMS,
+                               workspace_bytes=BIG_WS)                     # quantized pool (head dim 128)
+        assert (q["prefill_tensor_requests"], q["prefill_tensor_own_rows"]) == (1, 0), t
+    with pkv.options(tc_key_pieces=2):                                         # a pair cut into pieces
+        q = pkv.plan_attention([0, 64, 65], [8192, 900], 32, 8, 128, combined=True, num_sms=SMS,
+                               workspace_bytes=BIG_WS)
+        assert q["prefill_tensor_pieces"] > 0 and q["prefill_tensor_own_rows"] == 0
+
+
 def test_decodes_beside_a_long_prefill_take_longer_splits():
     spec, qsl, sl = meta(4)
     p = plan(4, combined=True)
