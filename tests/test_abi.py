@@ -189,3 +189,34 @@ def test_noalloc_scratch_fits_every_workload_plan(lib):
                                   workspace_bytes=scratch, num_sms=152)
         front = 256 + (65536 if plan["split_counters"] else 0)
         assert plan["partial_bytes"] + front <= scratch, cfg
+
+
+def _c_layout(struct, fields, tmp_path):
+    """sizeof and every field's offsetof of `struct` as the C compiler lays it
+    out from include/pkv.h."""
+    lines = [f'printf("%zu\\n", sizeof({struct}));']
+    lines += [f'printf("%zu\\n", offsetof({struct}, {f}));' for f in fields]
+    src = ('#include <stddef.h>\n#include <stdio.h>\n#include "pkv.h"\nint main(void){\n' + "\n".join(lines) +
+           '\nreturn 0;}\n')
+    exe = str(tmp_path / "layout")
+    r = subprocess.run(["gcc", "-x", "c", "-std=c99", "-I", os.path.join(ROOT, "include"), "-I",
+                        "/usr/local/cuda/include", "-o", exe, "-"], input=src, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    vals = [int(v) for v in subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split()]
+    return vals[0], dict(zip(fields, vals[1:]))
+
+
+@pytest.mark.parametrize("struct, name", [("pkv_attention_plan", "_Plan"),
+                                          ("pkv_attention_options", "AttentionOptions")])
+def test_binding_structs_match_the_header(struct, name, tmp_path):
+    """The ctypes mirrors of the header's structs have the C layout: the same
+    fields in the same order at the same offsets, and the same size."""
+    import paged_kv_cache_84_gb300 as pkv
+    cls = getattr(pkv, name)
+    fields = [f for f, _ in cls._fields_]
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    body = re.search(r"typedef struct %s \{(.*?)\}" % struct, text, flags=re.S).group(1)
+    assert re.findall(r"\b(\w+);", body) == fields
+    size, offsets = _c_layout(struct, fields, tmp_path)
+    assert ctypes.sizeof(cls) == size
+    assert {f: getattr(cls, f).offset for f in fields} == offsets
